@@ -1,0 +1,342 @@
+/*
+ * moe_oracle.c -- plain CPU oracle of the group-limited MoE layer forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * CPU-baseline / reference legs of bench.py may load or call this code.  The
+ * CUDA library never links it and shares no code, header, table or helper
+ * with it.  It is deliberately slow: plain loops, double accumulation, and a
+ * single rounding to fp32 wherever the method fixes fp32.
+ *
+ * What it follows.  "The routing page" is the article
+ *   "InternLumina-U2中256个专家的路由秘密：分组受限Top-K、Expert Bias与Fused MoE详解".
+ * "The pitfalls page" is the InternLumina-U2 training-pitfalls article
+ *   (m.lqnn.cn/news/279712), section "MoE 负载均衡 Loss 别忘加".
+ *
+ * Readings taken where the pages are silent or garbled (each one is listed
+ * with its reason in the design notes of the repository):
+ *   - group scores and the final top-k both use the biased score s + bias;
+ *     the weights use the unbiased s (routing page, section 三);
+ *   - ties go to the lower index, for groups and for experts; the k chosen
+ *     experts are returned in order of (biased score desc, index asc);
+ *   - the normaliser is (sum of the k chosen s, in that order, in fp32) + eps,
+ *     then w = fp32(fp32(s / den) * rsf)  (routing page, section 二 step 3);
+ *   - the SwiGLU intermediate silu(G) * U is rounded to bf16 once, because it
+ *     is the bf16 operand of the down projection;
+ *   - the shared expert is added unscaled (routing page, section 五).
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (no fused
+ * multiply-add contraction, so x86 and Arm give identical results).
+ */
+#include <math.h>
+#include <omp.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+typedef struct {
+    int T, H, E, n_group, topk_group, k, I, Is;
+    float rsf, eps;
+} orc_cfg;
+
+/* Thread count of the OpenMP loops below (the CPU baseline reports it). */
+void orc_set_threads(int n)
+{
+    if (n > 0)
+        omp_set_num_threads(n);
+}
+
+int orc_max_threads(void)
+{
+    return omp_get_max_threads();
+}
+
+/* ---------------------------------------------------------------- bf16 */
+
+/* bf16 is the top half of an IEEE binary32. */
+double orc_bf16_value(uint16_t v)
+{
+    uint32_t u = (uint32_t)v << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* binary32 -> bf16, round to nearest, ties to even; NaN stays a quiet NaN. */
+uint16_t orc_bf16_round(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+void orc_bf16_round_array(const float *in, uint16_t *out, long n)
+{
+    for (long i = 0; i < n; ++i)
+        out[i] = orc_bf16_round(in[i]);
+}
+
+/* ------------------------------------------------------ routing page 二.1 */
+
+/* Router linear layer in fp32 (routing page, section 二, step 1):
+ * logits[t, e] = sum_h x[t, h] * W[e, h].  Here every product and the sum are
+ * exact to double precision and the result is rounded once to fp32. */
+void orc_router_logits(int T, int H, int E, const uint16_t *x, const float *W, float *logits)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        const uint16_t *xt = x + (size_t)t * H;
+        for (int e = 0; e < E; ++e) {
+            const float *we = W + (size_t)e * H;
+            double acc = 0.0;
+            for (int h = 0; h < H; ++h)
+                acc += orc_bf16_value(xt[h]) * (double)we[h];
+            logits[(size_t)t * E + e] = (float)acc;
+        }
+    }
+}
+
+/* Sigmoid scoring (routing page, section 二, step 1): each expert is scored
+ * on its own, s = 1 / (1 + exp(-logit)), computed in double, rounded to fp32. */
+static float sigmoid_f32(float logit)
+{
+    return (float)(1.0 / (1.0 + exp(-(double)logit)));
+}
+
+/* (value desc, index asc) */
+static int before(float va, int ia, float vb, int ib)
+{
+    return va > vb || (va == vb && ia < ib);
+}
+
+/* Group-limited top-k for every token, from fp32 logits.
+ *
+ * Routing page, section 二 step 2: the E experts are cut in order into n_group
+ * groups of E/n_group; a group's score is the sum of its two highest scores;
+ * the topk_group best groups survive and the others are masked to -inf; the
+ * top k of the surviving experts are chosen.  Section 三: the score used for
+ * choosing is s + expert_bias.  Section 二 step 3: the weights are the
+ * unbiased s of the chosen experts, divided by (their sum + eps), times rsf.
+ *
+ * Outputs: idx [T,k], w [T,k]; optional scores [T,E] (the unbiased s);
+ * optional margins [T] in double: the gap between the topk_group-th and the
+ * next group score, and between the k-th and the next surviving biased score
+ * (+inf where there is no next one).
+ *
+ * Returns 0, or -1 for an unsupported shape, -2 for a non-finite input.
+ */
+int orc_route(const orc_cfg *c, const float *logits, const float *bias,
+              int32_t *idx, float *w, float *scores,
+              double *margin_group, double *margin_expert)
+{
+    const int E = c->E, G = c->n_group, TG = c->topk_group, K = c->k;
+    if (G <= 0 || E % G != 0 || E / G < 2 || TG < 1 || TG > G || K < 1 || K > TG * (E / G))
+        return -1;
+    const int GS = E / G;
+    int bad = 0;
+
+#pragma omp parallel
+    {
+        float *s = malloc(sizeof(float) * E);
+        float *b = malloc(sizeof(float) * E);
+        float *g = malloc(sizeof(float) * G);
+        int *gorder = malloc(sizeof(int) * G);
+        int *cand = malloc(sizeof(int) * E);
+#pragma omp for schedule(static)
+        for (int t = 0; t < c->T; ++t) {
+            const float *L = logits + (size_t)t * E;
+            for (int e = 0; e < E; ++e) {
+                if (!isfinite(L[e]) || (bias && !isfinite(bias[e]))) {
+#pragma omp atomic write
+                    bad = 1;
+                }
+                s[e] = sigmoid_f32(L[e]);
+                b[e] = s[e] + (bias ? bias[e] : 0.0f); /* one fp32 add */
+                if (scores)
+                    scores[(size_t)t * E + e] = s[e];
+            }
+            /* group score = top-1 + top-2 of the biased scores in the group */
+            for (int j = 0; j < G; ++j) {
+                float m1 = -INFINITY, m2 = -INFINITY;
+                for (int q = 0; q < GS; ++q) {
+                    float v = b[j * GS + q];
+                    if (v > m1) {
+                        m2 = m1;
+                        m1 = v;
+                    } else if (v > m2) {
+                        m2 = v;
+                    }
+                }
+                g[j] = m1 + m2;
+            }
+            /* order the groups by (score desc, index asc): selection sort */
+            for (int j = 0; j < G; ++j)
+                gorder[j] = j;
+            for (int a = 0; a < G; ++a)
+                for (int z = a + 1; z < G; ++z)
+                    if (before(g[gorder[z]], gorder[z], g[gorder[a]], gorder[a])) {
+                        int tmp = gorder[a];
+                        gorder[a] = gorder[z];
+                        gorder[z] = tmp;
+                    }
+            if (margin_group)
+                margin_group[t] = (TG < G) ? (double)g[gorder[TG - 1]] - (double)g[gorder[TG]] : INFINITY;
+            /* survivors: the experts of the kept groups (the rest are -inf) */
+            int nc = 0;
+            for (int a = 0; a < TG; ++a)
+                for (int q = 0; q < GS; ++q)
+                    cand[nc++] = gorder[a] * GS + q;
+            /* partial selection sort of the survivors by (b desc, index asc) */
+            for (int a = 0; a < K && a < nc; ++a)
+                for (int z = a + 1; z < nc; ++z)
+                    if (before(b[cand[z]], cand[z], b[cand[a]], cand[a])) {
+                        int tmp = cand[a];
+                        cand[a] = cand[z];
+                        cand[z] = tmp;
+                    }
+            if (margin_expert) {
+                if (K < nc) {
+                    /* best remaining survivor after the first K */
+                    int best = cand[K];
+                    for (int z = K + 1; z < nc; ++z)
+                        if (before(b[cand[z]], cand[z], b[best], best))
+                            best = cand[z];
+                    margin_expert[t] = (double)b[cand[K - 1]] - (double)b[best];
+                } else {
+                    margin_expert[t] = INFINITY;
+                }
+            }
+            /* weights from the unbiased scores, normalised, scaled */
+            float den = 0.0f;
+            for (int a = 0; a < K; ++a)
+                den += s[cand[a]];
+            den += c->eps;
+            for (int a = 0; a < K; ++a) {
+                float q = s[cand[a]] / den;
+                idx[(size_t)t * K + a] = cand[a];
+                w[(size_t)t * K + a] = q * c->rsf;
+            }
+        }
+        free(s);
+        free(b);
+        free(g);
+        free(gorder);
+        free(cand);
+    }
+    return bad ? -2 : 0;
+}
+
+/* ---------------------------------------------- pitfalls page, aux loss */
+
+/* Expert hit counts (routing page, section 六: a bincount of the chosen
+ * indices) and the load-balancing loss E * sum_i f_i * P_i (pitfalls page):
+ *   f_i = counts_i / (k T)                      (share of the k T selections)
+ *   P_i = (1/T) sum_t s[t,i] / sum_e s[t,e]     (mean normalised router score)
+ * P and the loss in double.  Returns the loss. */
+double orc_counts_aux(int T, int E, int K, const int32_t *idx, const float *scores,
+                      int32_t *counts, double *P)
+{
+    for (int e = 0; e < E; ++e)
+        counts[e] = 0;
+    for (long q = 0; q < (long)T * K; ++q)
+        if (idx[q] >= 0 && idx[q] < E)
+            counts[idx[q]] += 1;
+    if (!scores || !P)
+        return 0.0;
+    for (int e = 0; e < E; ++e)
+        P[e] = 0.0;
+    for (int t = 0; t < T; ++t) {
+        double tot = 0.0;
+        for (int e = 0; e < E; ++e)
+            tot += (double)scores[(size_t)t * E + e];
+        for (int e = 0; e < E; ++e)
+            P[e] += (double)scores[(size_t)t * E + e] / tot;
+    }
+    double aux = 0.0;
+    for (int e = 0; e < E; ++e) {
+        P[e] /= (double)T;
+        aux += ((double)counts[e] / ((double)K * T)) * P[e];
+    }
+    return (double)E * aux;
+}
+
+/* --------------------------------------------- routing page 四 and 五 */
+
+/* One SwiGLU expert on one token (routing page, section 四: gate, up and down
+ * stacked as [experts, 512, 2048]):
+ *   G_i = x . Wgu[i, :],  U_i = x . Wgu[I + i, :]     (i < I)
+ *   a_i = bf16(fp32(silu(G_i) * U_i)),  silu(z) = z / (1 + exp(-z))
+ *   y_h = sum_i a_i * Wd[i, h]
+ * and y * weight is added to acc.  Wgu is [2I, H] (gate rows, then up rows),
+ * Wd is [I, H]; all products and sums in double. */
+static void swiglu_expert_add(int H, int I, const double *x, const uint16_t *Wgu,
+                              const uint16_t *Wd, double weight, double *a, double *acc)
+{
+    for (int i = 0; i < I; ++i) {
+        const uint16_t *wg = Wgu + (size_t)i * H;
+        const uint16_t *wu = Wgu + (size_t)(I + i) * H;
+        double G = 0.0, U = 0.0;
+        for (int h = 0; h < H; ++h) {
+            G += x[h] * orc_bf16_value(wg[h]);
+            U += x[h] * orc_bf16_value(wu[h]);
+        }
+        double act = G / (1.0 + exp(-G)) * U;
+        a[i] = orc_bf16_value(orc_bf16_round((float)act));
+    }
+    for (int i = 0; i < I; ++i) {
+        const uint16_t *wd = Wd + (size_t)i * H;
+        double ai = a[i] * weight;
+        if (a[i] == 0.0)
+            continue;
+        for (int h = 0; h < H; ++h)
+            acc[h] += ai * orc_bf16_value(wd[h]);
+    }
+}
+
+/* Layer output for a list of tokens (routing page, sections 四 and 五):
+ *   out[t] = sum_j w[t,j] * expert_{idx[t,j]}(x[t]) + shared(x[t]) (+ residual[t])
+ * in double.  tokens (nullable) lists which rows of x to compute; out has one
+ * row of H per listed token.  Indices outside [0, E) contribute nothing and
+ * are reported by returning -1. */
+int orc_experts(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const uint16_t *Wd,
+                const uint16_t *sgu, const uint16_t *sd, const int32_t *idx, const float *w,
+                const uint16_t *residual, int n_tok, const int32_t *tokens, double *out)
+{
+    const int H = c->H, I = c->I, Is = c->Is, K = c->k, E = c->E;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *xd = malloc(sizeof(double) * H);
+        double *a = malloc(sizeof(double) * (I > Is ? I : Is));
+#pragma omp for schedule(dynamic, 1)
+        for (int q = 0; q < n_tok; ++q) {
+            int t = tokens ? tokens[q] : q;
+            double *acc = out + (size_t)q * H;
+            for (int h = 0; h < H; ++h) {
+                xd[h] = orc_bf16_value(x[(size_t)t * H + h]);
+                acc[h] = 0.0;
+            }
+            for (int j = 0; j < K; ++j) {
+                int e = idx[(size_t)t * K + j];
+                if (e < 0 || e >= E) {
+#pragma omp atomic write
+                    bad = 1;
+                    continue;
+                }
+                swiglu_expert_add(H, I, xd, Wgu + (size_t)e * 2 * I * H, Wd + (size_t)e * I * H,
+                                  (double)w[(size_t)t * K + j], a, acc);
+            }
+            if (sgu && sd)
+                swiglu_expert_add(H, Is, xd, sgu, sd, 1.0, a, acc);
+            if (residual)
+                for (int h = 0; h < H; ++h)
+                    acc[h] += orc_bf16_value(residual[(size_t)t * H + h]);
+        }
+        free(xd);
+        free(a);
+    }
+    return bad ? -1 : 0;
+}
