@@ -1,0 +1,406 @@
+"""Benchmark of the GB300 MoE layer forward (route + expert stage).
+
+One step = moe_route + moe_forward over one batch of T tokens of the full-size
+skewed workload (T=32768, hidden 2048, 256 experts in 8 groups, top-4 groups,
+top-8, SwiGLU experts [256, 512, 2048], one shared expert, 16 hot experts with
+router rows x3 and expert_bias ~ N(0, 0.05)).  Inputs are seeded synthetic
+tensors already resident in HBM; they are larger than L2 (1.61 GB of expert
+weights and 134 MB of hidden states per step), so no L2 flush is needed.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the
+plain C reference of the same method) on a bounded sample of the same
+workload.  Multi-GPU (torchrun): every rank runs its own replica on its own
+batch (weak scaling, no collective on the data path); the step time is the
+maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s on 1 GB300; % of tensor/HBM roofline per stage"
+WORKLOAD_ID = 4
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(device_index)
+        self.sel = sel
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------- work
+def algorithmic_work(T, H, E, I, k):
+    """Per-launch algorithmic bytes / flops of each kernel (the method's own
+    work: bytes every stage must move at least once, flops of the products)."""
+    kT = k * T
+    return {
+        "router_gemm": dict(bound="tensor", flops=2.0 * T * E * H,
+                            bytes=T * H * 2 + E * H * 4 + T * E * 4),
+        "route_select": dict(bound="hbm", bytes=T * E * 4 + T * k * 8),
+        "bucket_scatter": dict(bound="hbm", bytes=T * k * 4 * 2 + T * H * 2 + kT * H * 2),
+        "gemm_gate_up_swiglu": dict(bound="tensor", flops=2.0 * (kT + T) * H * 2 * I,
+                                    bytes=(kT + T) * H * 2 + E * 2 * I * H * 2 + (kT + T) * I * 2),
+        "gemm_down": dict(bound="tensor", flops=2.0 * (kT + T) * I * H,
+                          bytes=(kT + T) * I * 2 + E * I * H * 2 + (kT + T) * H * 2),
+        "combine": dict(bound="hbm", bytes=(kT + T) * H * 2 + T * H * 2 + T * k * 8),
+    }
+
+
+def init_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value, device):
+    if world == 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------- CPU oracle
+class CpuSample:
+    """The workload's inputs on the host (drawn once) and a timer of the CPU
+    oracle -- router logits, routing and expert stage -- on its first n tokens."""
+
+    def __init__(self, threads: int = 0):
+        import oracle
+        from group_limited_routing_gb300 import workloads as wl
+
+        self.oracle = oracle
+        if threads:
+            oracle.set_threads(threads)
+        w0 = wl.WORKLOADS[WORKLOAD_ID]
+
+        def u16(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+        self.x = u16(wl.hidden(w0))
+        self.W = wl.router_weight(w0).numpy()
+        self.b = wl.expert_bias(w0).numpy()
+        Wgu, Wd = wl.expert_weights(w0)
+        sgu, sd = wl.shared_weights(w0)
+        self.gu, self.dn, self.sgu, self.sd = u16(Wgu), u16(Wd), u16(sgu), u16(sd)
+
+    def run(self, n_tokens: int):
+        """Returns (tokens/s, threads used, seconds)."""
+        o = self.oracle
+        xs = np.ascontiguousarray(self.x[:n_tokens])
+        t0 = time.perf_counter()
+        L = o.router_logits(xs, self.W)
+        r = o.route(L, bias=self.b)
+        o.experts(xs, self.gu, self.dn, self.sgu, self.sd, r["idx"], r["w"])
+        dt = time.perf_counter() - t0
+        return n_tokens / dt, o.max_threads(), dt
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args, world, rank, local):
+    from group_limited_routing_gb300 import moe, workloads as wl
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w0 = wl.WORKLOADS[WORKLOAD_ID]
+    T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
+    cfg = moe.MoeConfig(T=T, H=H, E=E, n_group=w0.n_group, topk_group=w0.topk_group, k=k, I=I, Is=w0.Is)
+    d = wl.layer_inputs(w0, dev)
+    x = wl.hidden(w0, dev, layer=rank) if rank else d["hidden"]   # each replica its own batch
+    layer = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
+                         d["shared_gate_up"], d["shared_down"])
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        layer(x, out=out)
+    torch.cuda.synchronize(dev)
+    if layer.status() != 0:
+        raise RuntimeError("device status after warm-up: %d" % layer.status())
+
+    # ---- timed region: K steps, inputs resident
+    launches = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        e0.record(stream)
+        for _ in range(args.steps):
+            layer(x, out=out)
+            launches += layer.last_launches
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_max = max_over_ranks(world, ms, dev)
+    status = layer.status()
+    if status != 0:
+        raise RuntimeError("device status after the timed region: %d" % status)
+
+    # ---- per-kernel durations (CUDA events around each launch, same stream)
+    moe.profile_read(reset=True)
+    moe.profile_enable(True)
+    nprof = max(3, min(args.steps, 10))
+    for _ in range(nprof):
+        layer(x, out=out)
+    torch.cuda.synchronize(dev)
+    moe.profile_enable(False)
+    prof = moe.profile_read(reset=True)
+
+    # ---- end to end through the public API: pinned host in, pinned host out
+    x_h = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    x_h.copy_(x)
+    out_h = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    x_d = torch.empty_like(x)
+    for _ in range(2):
+        x_d.copy_(x_h, non_blocking=True)
+        layer(x_d, out=out)
+        out_h.copy_(out, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        x_d.copy_(x_h, non_blocking=True)
+        layer(x_d, out=out)
+        out_h.copy_(out, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(world, f0.elapsed_time(f1) / args.steps, dev)
+    barrier(world)
+
+    if rank != 0:
+        return None
+
+    pk = peaks()
+    work = algorithmic_work(T, H, E, I, k)
+    stages = {}
+    for name, (tot, n) in prof.items():
+        if n == 0:
+            continue
+        avg = tot / n
+        st = {"ms": round(avg, 4), "launches_per_step": round(n / nprof, 2)}
+        if name in work:
+            wk = work[name]
+            if wk["bound"] == "tensor":
+                tf = wk["flops"] / (avg * 1e-3) / 1e12
+                st.update(bound="tensor", tflops=round(tf, 1), frac=round(tf / pk["bf16_sustained"], 4),
+                          gbs=round(wk["bytes"] / (avg * 1e-3) / 1e9, 1))
+            else:
+                gb = wk["bytes"] / (avg * 1e-3) / 1e9
+                st.update(bound="hbm", gbs=round(gb, 1), frac=round(gb / pk["hbm"], 4))
+        stages[name] = st
+    # router + permute as one HBM stage
+    rp_names = ("split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist", "bucket_scan",
+                "bucket_scatter")
+    rp_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in rp_names if n in stages)
+    rp_bytes = T * H * 2 + E * H * 4 + T * k * 8 + T * k * 4 * 2 + T * H * 2 + k * T * H * 2
+    stages["router_plus_permute"] = {"ms": round(rp_ms, 4), "bound": "hbm",
+                                     "gbs": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
+                                     "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / pk["hbm"], 4)}
+    g1 = work["gemm_gate_up_swiglu"]
+    g1_ms = prof["gemm_gate_up_swiglu"][0] / max(1, prof["gemm_gate_up_swiglu"][1])
+    g1_tf = g1["flops"] / (g1_ms * 1e-3) / 1e12
+    gemms_ms = g1_ms + stages.get("gemm_down", {"ms": 0})["ms"]
+    gemm_flops = work["gemm_gate_up_swiglu"]["flops"] + work["gemm_down"]["flops"]
+    stages["expert_gemms"] = {"ms": round(gemms_ms, 4), "bound": "tensor",
+                              "tflops": round(gemm_flops / (gemms_ms * 1e-3) / 1e12, 1),
+                              "frac": round(gemm_flops / (gemms_ms * 1e-3) / 1e12 / pk["bf16_sustained"], 4)}
+
+    value = world * T / (ms_max * 1e-3)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": "T=32768 full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)",
+                   "T_per_gpu": T, "hidden": H, "experts": E, "groups": w0.n_group, "topk_group": w0.topk_group,
+                   "k": k, "inter": I, "shared_inter": w0.Is, "parallelism": "replicas (dp%d)" % world,
+                   "l2": "inputs larger than L2 (1.61 GB expert weights + 134 MB hidden per step), no flush"},
+        "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": "tensor", "achieved": round(g1_tf, 1),
+                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                     "frac": round(g1_tf / pk["bf16_sustained"], 4), "traffic": None,
+                     "peak_kind": "%s bf16 dense, sustained" % pk["source"],
+                     "algorithmic_flops_per_launch": g1["flops"]},
+        "stages": stages,
+        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        tps, thr, secs = CpuSample().run(args.cpu_tokens)
+        line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                "sample": "first %d tokens of the workload: router logits, routing and expert "
+                                          "stage (%.1f s)" % (args.cpu_tokens, secs)}
+    return line
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle as it stands, on the host cores, one bounded sample per step."""
+    if rank != 0:
+        return None
+    sample = CpuSample()
+    for _ in range(args.warmup):
+        sample.run(args.ref_tokens)
+    secs = 0.0
+    thr = 0
+    for _ in range(args.steps):
+        _, thr, dt = sample.run(args.ref_tokens)
+        secs += dt
+    value = args.ref_tokens * args.steps / secs
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * secs / args.steps, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded; shapes and distributions of the workload)",
+        "config": {"workload": "T=32768 full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)",
+                   "sample_tokens_per_step": args.ref_tokens},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                         "sample": "first %d tokens per step: router logits, routing and expert stage"
+                                   % args.ref_tokens},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-tokens", type=int, default=1024, help="oracle sample for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        line = run_reference(args, world, rank)
+    else:
+        world, rank, local = init_dist()
+        line = run_ours(args, world, rank, local)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,554 @@
+// C-ABI entry points (include/moe.h): argument checks, workspace layout,
+// TMA tensor maps and the launch sequence of the MoE layer forward.
+//
+// Every check runs on the host before any CUDA call, so a wrong argument
+// returns an error code without touching the device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "kernels.h"
+#include "moe.h"
+
+using namespace glr;
+
+namespace {
+
+thread_local int g_last_launches = 0;
+
+// ------------------------------------------------------------- profiling
+enum KernelId {
+    KID_SPLIT = 0, KID_ROUTER_GEMM, KID_SELECT, KID_FINALIZE, KID_HIST, KID_SCAN, KID_SCATTER,
+    KID_GEMM_GATE_UP, KID_GEMM_DOWN, KID_COMBINE
+};
+const char *const kKernelNames[MOE_KERNEL_COUNT] = {
+    "split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist",
+    "bucket_scan", "bucket_scatter", "gemm_gate_up_swiglu", "gemm_down", "combine"};
+
+struct ProfRecord {
+    cudaEvent_t start, stop;
+    int kid;
+};
+
+std::atomic<int> g_prof_on{0};
+std::mutex g_prof_mu;
+std::vector<ProfRecord> g_prof_pending;
+std::vector<cudaEvent_t> g_event_pool;
+double g_prof_ms[MOE_KERNEL_COUNT];
+long long g_prof_n[MOE_KERNEL_COUNT];
+
+cudaEvent_t pool_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+struct ProfScope {
+    bool on;
+    ProfRecord r;
+    cudaStream_t s;
+    ProfScope(int kid, cudaStream_t st) : on(g_prof_on.load(std::memory_order_relaxed) != 0), s(st)
+    {
+        if (!on)
+            return;
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        r.start = pool_event();
+        r.stop = pool_event();
+        r.kid = kid;
+        cudaEventRecord(r.start, s);
+    }
+    void done()
+    {
+        if (!on)
+            return;
+        cudaEventRecord(r.stop, s);
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        g_prof_pending.push_back(r);
+        on = false;
+    }
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ------------------------------------------------------------- validation
+int check_route_cfg(const moe_cfg *c)
+{
+    if (!c)
+        return MOE_ERR_INVALID_ARG;
+    if (c->T < 1 || c->H < 1 || c->E < 1 || c->n_group < 1 || c->topk_group < 1 || c->k < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (c->E % c->n_group != 0 || c->E / c->n_group < 2 || c->topk_group > c->n_group ||
+        c->k > c->topk_group * (c->E / c->n_group))
+        return MOE_ERR_INVALID_ARG;
+    if (!isfinite(c->rsf) || !isfinite(c->eps) || c->eps < 0.0f)
+        return MOE_ERR_INVALID_ARG;
+    if (c->E != 32 * c->n_group || c->n_group > MAX_GROUPS || c->E % 128 != 0 || c->k > 32)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->H % GEMM_BK != 0 || c->T > (1 << 24))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+int check_forward_cfg(const moe_cfg *c)
+{
+    if (!c)
+        return MOE_ERR_INVALID_ARG;
+    if (c->T < 1 || c->H < 1 || c->E < 1 || c->k < 1 || c->I < 1 || c->Is < 1 || c->k > c->E)
+        return MOE_ERR_INVALID_ARG;
+    if (c->E > 256 || c->k > 32 || c->T > (1 << 24))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->H % 256 != 0 || c->I % 128 != 0 || c->Is != c->I)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+// ---------------------------------------------------------------- layouts
+struct RouteLayout {
+    size_t w3, logits, hist, ppart, total;
+    int nchunk;
+};
+
+RouteLayout route_layout(const moe_cfg &c)
+{
+    RouteLayout L;
+    L.nchunk = (c.T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    size_t off = sizeof(WsHeader);
+    L.w3 = off;
+    off = align_up(off + 3ull * c.E * c.H * 2, 256);
+    L.logits = off;
+    off = align_up(off + (size_t)c.T * c.E * 4, 256);
+    L.hist = off;
+    off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
+    L.ppart = off;
+    off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
+    L.total = off;
+    return L;
+}
+
+struct FwdLayout {
+    size_t hist, mtiles, slot_of, xperm, aint, y, total;
+    int nchunk, max_mtiles;
+};
+
+FwdLayout fwd_layout(const moe_cfg &c)
+{
+    FwdLayout L;
+    const size_t T = c.T, K = c.k, H = c.H, I = c.I;
+    L.nchunk = (c.T + PERM_CHUNK - 1) / PERM_CHUNK;
+    // sum over buckets of ceil(n_e / 128) <= K T / 128 + E, plus the shared group
+    L.max_mtiles = (int)((K * T) / GEMM_BM + c.E + (T + GEMM_BM - 1) / GEMM_BM + 1);
+    size_t off = sizeof(WsHeader);
+    L.hist = off;
+    off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
+    L.mtiles = off;
+    off = align_up(off + (size_t)L.max_mtiles * 16, 256);
+    L.slot_of = off;
+    off = align_up(off + T * K * 4, 256);
+    L.xperm = off;
+    off = align_up(off + K * T * H * 2, 256);
+    L.aint = off;
+    off = align_up(off + (K + 1) * T * I * 2, 256);
+    L.y = off;
+    off = align_up(off + (K + 1) * T * H * 2, 256);
+    L.total = off;
+    return L;
+}
+
+// --------------------------------------------------------------- device
+int device_check(int *sms)
+{
+    static int cached_sms[64];
+    static int cached_ok[64];   // 0 unknown, 1 ok, -1 unsupported
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64)
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    if (cached_ok[dev] == 0) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        cached_sms[dev] = n;
+        cached_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (cached_ok[dev] < 0)
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    *sms = cached_sms[dev];
+    return MOE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 2D bf16 tensor [rows, cols] (row-major), box [box_rows, box_cols], 128-byte
+// swizzle (box_cols * 2 == 128), zero fill outside the tensor.
+bool make_map_bf16(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                   uint32_t box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+WsHeader *header(void *ws) { return static_cast<WsHeader *>(ws); }
+
+template <typename T>
+T *at(void *ws, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<char *>(ws) + off);
+}
+
+#define GLR_LAUNCH(kid, expr)                  \
+    do {                                       \
+        ProfScope prof_scope_((kid), s);       \
+        if ((expr) != cudaSuccess)             \
+            return MOE_ERR_CUDA;               \
+        prof_scope_.done();                    \
+        ++launches;                            \
+    } while (0)
+
+int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, float *logits, void *ws,
+                const RouteLayout &L, int sms, cudaStream_t s, int &launches)
+{
+    uint16_t *W3 = at<uint16_t>(ws, L.w3);
+    GLR_LAUNCH(KID_SPLIT, launch_split_router(W, W3, c.E, c.H, s));
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p.tmB0, W3, 3ull * c.E, c.H, GEMM_BK, 128))
+        return MOE_ERR_CUDA;
+    p.out = logits;
+    p.n_tiles = c.E / 128;
+    p.num_tiles_static = ((c.T + GEMM_BM - 1) / GEMM_BM) * p.n_tiles;
+    p.kblocks = c.H / GEMM_BK;
+    p.T = c.T;
+    p.E = c.E;
+    p.H = c.H;
+    p.ld_out = c.E;
+    p.status = &header(ws)->status;
+    GLR_LAUNCH(KID_ROUTER_GEMM, launch_gemm(GK_ROUTER, p, std::min(sms, p.num_tiles_static), s));
+    return MOE_OK;
+}
+
+int route_select(const moe_cfg &c, const float *logits, const float *bias, int32_t *idx, float *w,
+                 int32_t *counts, float *aux_P, float *aux_loss, void *ws, const RouteLayout &L, cudaStream_t s,
+                 int &launches)
+{
+    int32_t *hist = at<int32_t>(ws, L.hist);
+    float *ppart = (aux_P || aux_loss) ? at<float>(ws, L.ppart) : nullptr;
+    GLR_LAUNCH(KID_SELECT, launch_route_select(logits, bias, c.T, c.E, c.n_group, c.topk_group, c.k, c.rsf, c.eps, idx, w,
+                                   hist, ppart, &header(ws)->status, s));
+    GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(hist, ppart, L.nchunk, c.T, c.E, c.k, counts, aux_P, aux_loss, s));
+    return MOE_OK;
+}
+
+int check_ws(void *ws, size_t ws_bytes, size_t need)
+{
+    if (!ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256))
+        return MOE_ERR_MISALIGNED;
+    if (ws_bytes < need)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return MOE_OK;
+}
+
+}  // namespace
+
+// ===================================================================== ABI
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_cfg *cfg, int which)
+{
+    if (which == MOE_WS_ROUTE)
+        return check_route_cfg(cfg) == MOE_OK ? route_layout(*cfg).total : 0;
+    if (which == MOE_WS_FORWARD)
+        return check_forward_cfg(cfg) == MOE_OK ? fwd_layout(*cfg).total : 0;
+    return 0;
+}
+
+int moe_workspace_init(void *ws, size_t ws_bytes, void *stream)
+{
+    int rc = check_ws(ws, ws_bytes, sizeof(WsHeader));
+    if (rc != MOE_OK)
+        return rc;
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_router_logits(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, float *logits, void *ws,
+                      size_t ws_bytes, void *stream)
+{
+    int rc = check_route_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !W_router || !logits)
+        return MOE_ERR_INVALID_ARG;
+    const RouteLayout L = route_layout(*cfg);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(W_router, 4) || !aligned(logits, 16))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    int launches = 0;
+    rc = router_gemm(*cfg, hidden, W_router, logits, ws, L, sms, static_cast<cudaStream_t>(stream), launches);
+    g_last_launches = launches;
+    return rc;
+}
+
+int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *expert_bias, int32_t *topk_idx,
+                          float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss, void *ws,
+                          size_t ws_bytes, void *stream)
+{
+    int rc = check_route_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!logits || !topk_idx || !topk_w || !expert_counts)
+        return MOE_ERR_INVALID_ARG;
+    const RouteLayout L = route_layout(*cfg);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(logits, 4) || !aligned(expert_bias, 4) || !aligned(topk_idx, 4) || !aligned(topk_w, 4) ||
+        !aligned(expert_counts, 4) || !aligned(aux_P, 4) || !aligned(aux_loss, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    int launches = 0;
+    rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L,
+                      static_cast<cudaStream_t>(stream), launches);
+    g_last_launches = launches;
+    return rc;
+}
+
+int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const float *expert_bias,
+              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss, void *ws,
+              size_t ws_bytes, void *stream)
+{
+    int rc = check_route_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !W_router || !topk_idx || !topk_w || !expert_counts)
+        return MOE_ERR_INVALID_ARG;
+    const RouteLayout L = route_layout(*cfg);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(W_router, 4) || !aligned(expert_bias, 4) || !aligned(topk_idx, 4) ||
+        !aligned(topk_w, 4) || !aligned(expert_counts, 4) || !aligned(aux_P, 4) || !aligned(aux_loss, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    float *logits = at<float>(ws, L.logits);
+    rc = router_gemm(*cfg, hidden, W_router, logits, ws, L, sms, s, launches);
+    if (rc == MOE_OK)
+        rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
+                          launches);
+    g_last_launches = launches;
+    return rc;
+}
+
+int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
+                const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const int32_t *topk_idx,
+                const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *ws, size_t ws_bytes,
+                void *stream)
+{
+    int rc = check_forward_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !W_gate_up || !W_down || !shared_gate_up || !shared_down || !topk_idx || !topk_w || !out)
+        return MOE_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(*cfg);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(shared_gate_up, 16) ||
+        !aligned(shared_down, 16) || !aligned(residual, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) ||
+        !aligned(topk_w, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const moe_cfg &c = *cfg;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    WsHeader *hdr = header(ws);
+    int32_t *hist = at<int32_t>(ws, L.hist);
+    int4 *mtiles = at<int4>(ws, L.mtiles);
+    int32_t *slot_of = at<int32_t>(ws, L.slot_of);
+    uint16_t *xperm = at<uint16_t>(ws, L.xperm);
+    uint16_t *aint = at<uint16_t>(ws, L.aint);
+    uint16_t *y = at<uint16_t>(ws, L.y);
+    const uint64_t kT = (uint64_t)c.k * c.T;
+
+    // bucket the (token, expert) pairs by expert (stable), gather rows
+    GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
+    GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.T, c.E, c.k, mtiles, hdr, s));
+    GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, c.T, c.H, c.E, c.k, slot_of, xperm, s));
+
+    // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E)
+    GemmParams p1;
+    memset(&p1, 0, sizeof(p1));
+    if (!make_map_bf16(&p1.tmA0, xperm, kT, c.H, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p1.tmA1, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p1.tmB0, W_gate_up, 2ull * c.I * c.E, c.H, GEMM_BK, 128) ||
+        !make_map_bf16(&p1.tmB1, shared_gate_up, 2ull * c.I, c.H, GEMM_BK, 128))
+        return MOE_ERR_CUDA;
+    p1.out = aint;
+    p1.mtiles = mtiles;
+    p1.num_mtiles = &hdr->num_mtiles;
+    p1.n_tiles = c.I / 128;
+    p1.kblocks = c.H / GEMM_BK;
+    p1.T = c.T;
+    p1.E = c.E;
+    p1.I = c.I;
+    p1.H = c.H;
+    p1.kT = (int)kT;
+    p1.ld_out = c.I;
+    p1.status = &hdr->status;
+    GLR_LAUNCH(KID_GEMM_GATE_UP, launch_gemm(GK_GATE_UP, p1, std::min(sms, L.max_mtiles * p1.n_tiles), s));
+
+    // grouped down GEMM (W_down stacked [E, I, H]: an MN-major B operand)
+    GemmParams p2;
+    memset(&p2, 0, sizeof(p2));
+    if (!make_map_bf16(&p2.tmA0, aint, kT + c.T, c.I, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p2.tmB0, W_down, (uint64_t)c.I * c.E, c.H, 64, GEMM_BK) ||
+        !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, 64, GEMM_BK))
+        return MOE_ERR_CUDA;
+    p2.out = y;
+    p2.mtiles = mtiles;
+    p2.num_mtiles = &hdr->num_mtiles;
+    p2.n_tiles = c.H / 256;
+    p2.kblocks = c.I / GEMM_BK;
+    p2.T = c.T;
+    p2.E = c.E;
+    p2.I = c.I;
+    p2.H = c.H;
+    p2.kT = (int)kT;
+    p2.ld_out = c.H;
+    p2.status = &hdr->status;
+    GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(GK_DOWN, p2, std::min(sms, L.max_mtiles * p2.n_tiles), s));
+
+    // weighted combine + shared expert (+ residual), one rounding to bf16
+    GLR_LAUNCH(KID_COMBINE, launch_combine(y, slot_of, topk_w, residual, c.T, c.H, c.k, out, s));
+    g_last_launches = launches;
+    return MOE_OK;
+}
+
+int moe_get_status(void *ws, size_t ws_bytes, void *stream, int32_t *status, int reset)
+{
+    int rc = check_ws(ws, ws_bytes, sizeof(WsHeader));
+    if (rc != MOE_OK)
+        return rc;
+    if (!status)
+        return MOE_ERR_INVALID_ARG;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, &header(ws)->status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (reset && cudaMemsetAsync(&header(ws)->status, 0, sizeof(int32_t), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    *status = v;
+    return MOE_OK;
+}
+
+int moe_last_launch_count(void) { return g_last_launches; }
+
+int moe_profile_enable(int on)
+{
+    g_prof_on.store(on ? 1 : 0);
+    return MOE_OK;
+}
+
+int moe_profile_read(int kernel_id, double *total_ms, int32_t *launches, int reset)
+{
+    if (kernel_id < 0 || kernel_id >= MOE_KERNEL_COUNT || !total_ms || !launches)
+        return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    int rc = MOE_OK;
+    for (const ProfRecord &r : g_prof_pending) {
+        float ms = 0.0f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
+        g_prof_ms[r.kid] += ms;
+        g_prof_n[r.kid] += 1;
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_prof_pending.clear();
+    *total_ms = g_prof_ms[kernel_id];
+    *launches = (int32_t)g_prof_n[kernel_id];
+    if (reset) {
+        g_prof_ms[kernel_id] = 0.0;
+        g_prof_n[kernel_id] = 0;
+    }
+    return rc;
+}
+
+const char *moe_kernel_name(int kernel_id)
+{
+    if (kernel_id < 0 || kernel_id >= MOE_KERNEL_COUNT)
+        return "";
+    return kKernelNames[kernel_id];
+}
+
+const char *moe_strerror(int code)
+{
+    switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, non-positive size or inconsistent config)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "shape not supported by this implementation";
+    case MOE_ERR_MISALIGNED: return "pointer not aligned (16 bytes for tensor-core operands, 256 for workspaces)";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than moe_workspace_bytes()";
+    case MOE_ERR_CUDA: return "a CUDA call or kernel launch failed";
+    case MOE_ERR_DEVICE_STATUS: return "the device reported a fault in the status word";
+    case MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300)";
+    default: return "unknown error code";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernels.
+// Not installed; the public contract is include/moe.h.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace glr {
+
+// ---- sizes shared by the host layer and the kernels -------------------------
+constexpr int ROUTE_CHUNK = 128;   // tokens per block of the routing kernel
+constexpr int PERM_CHUNK = 128;    // tokens per block of the bucketing kernels
+constexpr int GEMM_BM = 128;       // tensor-core tile rows (tokens)
+constexpr int GEMM_BK = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16)
+constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int MAX_GROUPS = 8;      // routing warp: one expert per lane per group
+
+// status bits (mirror include/moe.h)
+constexpr int ST_NONFINITE = 1;
+constexpr int ST_BAD_INDEX = 2;
+constexpr int ST_TIMEOUT = 4;
+constexpr int ST_COUNT_MISMATCH = 8;
+
+// Workspace header (first 256 bytes of every workspace).
+struct WsHeader {
+    int status;      // OR of ST_* bits
+    int num_mtiles;  // m-tiles of the grouped GEMMs (written on the device)
+    int pad[62];
+};
+
+enum GemmKind { GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2 };
+
+// Parameters of the tensor-core GEMM kernels.  Tensor maps live in the
+// kernel's parameter space (__grid_constant__), so TMA reads them in place.
+struct GemmParams {
+    CUtensorMap tmA0;   // router: hidden; gate_up: X_perm; down: intermediate
+    CUtensorMap tmA1;   // gate_up: hidden (shared-expert rows)
+    CUtensorMap tmB0;   // router: W split [3E, H]; gate_up: W_gate_up [E*2I, H]; down: W_down [E*I, H]
+    CUtensorMap tmB1;   // gate_up: shared_gate_up [2I, H]; down: shared_down [I, H]
+    void *out;          // router: logits fp32 [T, E]; gate_up: intermediate bf16; down: Y bf16
+    const int4 *mtiles; // grouped: {group, first row, rows, 0}
+    const int *num_mtiles;
+    int num_tiles_static; // router: tiles known on the host
+    int n_tiles;          // n-tiles per m-tile
+    int kblocks;          // K / GEMM_BK
+    int T, E, I, H, kT;
+    int ld_out;           // output row stride in elements
+    int *status;
+};
+
+// Smem bytes a GEMM kind needs (stages + alignment slack + barriers).
+int gemm_smem_bytes(int kind);
+int gemm_tmem_cols(int kind);
+
+cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s);
+
+cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, cudaStream_t s);
+
+cudaError_t launch_route_select(const float *logits, const float *bias, int T, int E, int n_group,
+                                int topk_group, int k, float rsf, float eps, int32_t *idx, float *w,
+                                int32_t *hist, float *ppart, int *status, cudaStream_t s);
+
+cudaError_t launch_route_finalize(const int32_t *hist, const float *ppart, int nchunk, int T, int E, int k,
+                                  int32_t *counts, float *aux_P, float *aux_loss, cudaStream_t s);
+
+cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status,
+                               cudaStream_t s);
+
+cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int T, int E, int k, int4 *mtiles,
+                               WsHeader *hdr, cudaStream_t s);
+
+cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base, int T,
+                                  int H, int E, int k, int32_t *slot_of, uint16_t *x_perm, cudaStream_t s);
+
+cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
+                           int T, int H, int k, uint16_t *out, cudaStream_t s);
+
+}  // namespace glr

@@ -1,0 +1,295 @@
+// Bucketing (permute) and combine kernels of the MoE layer forward (SIMT, sm_103a).
+//
+// The routing page ("InternLumina-U2中256个专家的路由秘密：分组受限Top-K、Expert
+// Bias与Fused MoE详解", section 四, the eager inference path) sorts tokens into
+// one bucket per expert, runs each bucket through its expert and sums the
+// weighted results.  Here:
+//   bucket_hist    per 128-token chunk, hits per expert        (reads topk_idx)
+//   bucket_scan    bucket offsets (exclusive scan of the counts), each chunk's
+//                  start inside every bucket, and the m-tile list of the
+//                  grouped GEMMs (the shared expert is group E, all T tokens)
+//   bucket_scatter stable slot of every (token, j) pair -- slots in a bucket in
+//                  ascending (token, j) order -- and the gather of hidden rows
+//                  into the bucketed activation matrix X_perm
+//   combine        out[t] = bf16( sum_j w[t,j] * Y[slot(t,j)] + Y_shared[t]
+//                  (+ residual[t]) ) in fp32 (section 五: the shared expert is
+//                  added directly)
+// Everything is deterministic: no float atomics, fixed summation order.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+
+namespace glr {
+
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) bucket_hist_kernel(const int32_t *__restrict__ idx, int T, int E, int K,
+                                                          int32_t *__restrict__ hist, int *__restrict__ status)
+{
+    extern __shared__ int sh[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        sh[e] = 0;
+    __syncthreads();
+    const long long n0 = (long long)blockIdx.x * PERM_CHUNK * K;
+    const long long n1 = min((long long)T * K, n0 + (long long)PERM_CHUNK * K);
+    bool bad = false;
+    for (long long i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
+        const int e = idx[i];
+        if (e >= 0 && e < E)
+            atomicAdd(&sh[e], 1);
+        else
+            bad = true;
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0)
+        atomicOr(status, ST_BAD_INDEX);
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        hist[(size_t)blockIdx.x * E + e] = sh[e];
+}
+
+cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status, cudaStream_t s)
+{
+    const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
+    bucket_hist_kernel<<<blocks, 256, E * sizeof(int), s>>>(idx, T, E, k, hist, status);
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
+// One block of 1024 threads, E <= 256: thread (q, e) owns expert e's column
+// for the chunks of quarter q.  In place, hist[c][e] becomes the first slot of
+// chunk c inside bucket e.
+__global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t *__restrict__ hist, int nchunk, int T, int E,
+                                                           int K, int4 *__restrict__ mtiles,
+                                                           WsHeader *__restrict__ hdr)
+{
+    __shared__ int part[4][257];
+    __shared__ int total[257];
+    __shared__ int offset[258];
+    __shared__ int tstart[258];
+    const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
+    const int per = (nchunk + 3) / 4;
+    const int c0 = min(nchunk, q * per), c1 = min(nchunk, c0 + per);
+
+    int sum = 0;
+    if (e < E)
+        for (int c = c0; c < c1; ++c)
+            sum += hist[(size_t)c * E + e];
+    part[q][e] = sum;
+    __syncthreads();
+    if (q == 0) {
+        total[e] = (e < E) ? part[0][e] + part[1][e] + part[2][e] + part[3][e] : 0;
+        if (e == 0)
+            total[256] = 0;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // bucket offsets and first m-tile of every group (E routed + shared)
+        int off = 0, tiles = 0;
+        for (int g = 0; g < E; ++g) {
+            offset[g] = off;
+            tstart[g] = tiles;
+            off += total[g];
+            tiles += (total[g] + GEMM_BM - 1) / GEMM_BM;
+        }
+        offset[E] = off;             // == K*T unless indices were out of range
+        tstart[E] = tiles;
+        tiles += (T + GEMM_BM - 1) / GEMM_BM;
+        tstart[E + 1] = tiles;
+        hdr->num_mtiles = tiles;
+        if (off != K * T)
+            atomicOr(&hdr->status, ST_COUNT_MISMATCH);
+    }
+    __syncthreads();
+    if (e < E) {
+        int run = offset[e];
+        for (int qq = 0; qq < q; ++qq)
+            run += part[qq][e];
+        for (int c = c0; c < c1; ++c) {
+            const int h = hist[(size_t)c * E + e];
+            hist[(size_t)c * E + e] = run;
+            run += h;
+        }
+    }
+    // m-tile lists: routed buckets by q == 0 threads, the shared group by the rest
+    if (q == 0 && e < E) {
+        const int n = total[e];
+        for (int i = 0, r = 0; r < n; ++i, r += GEMM_BM)
+            mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n - r), 0);
+    }
+    {
+        const int ntile_sh = (T + GEMM_BM - 1) / GEMM_BM;
+        for (int i = threadIdx.x - 256; i >= 0 && i < ntile_sh; i += 768)
+            mtiles[tstart[E] + i] = make_int4(E, i * GEMM_BM, min(GEMM_BM, T - i * GEMM_BM), 0);
+    }
+}
+
+cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int T, int E, int k, int4 *mtiles, WsHeader *hdr,
+                               cudaStream_t s)
+{
+    bucket_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunk, T, E, k, mtiles, hdr);
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Stable slots for one chunk, then the row gather.  Warp 0 assigns slots in
+// (token, j) order, 32 pairs at a time: lanes holding the same expert find
+// each other with __match_any_sync and take consecutive slots by lane rank.
+__global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__restrict__ idx,
+                                                             const uint16_t *__restrict__ x,
+                                                             const int32_t *__restrict__ chunk_base, int T, int H,
+                                                             int E, int K, int32_t *__restrict__ slot_of,
+                                                             uint16_t *__restrict__ x_perm)
+{
+    extern __shared__ int sm[];
+    int *next = sm;            // [E]   next free slot of each bucket for this chunk
+    int *slots = sm + E;       // [PERM_CHUNK * K]
+    const int t0 = blockIdx.x * PERM_CHUNK;
+    const int nt = min(PERM_CHUNK, T - t0);
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        next[e] = chunk_base[(size_t)blockIdx.x * E + e];
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const int n = nt * K;
+        const int32_t *src = idx + (size_t)t0 * K;
+        for (int base = 0; base < n; base += 32) {
+            const int i = base + lane;
+            const bool in = i < n;
+            const int e = in ? src[i] : -1;
+            const bool ok = in && e >= 0 && e < E;
+            const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+            int slot = -1;
+            if (ok)
+                slot = next[e] + __popc(peers & ((1u << lane) - 1u));
+            __syncwarp();
+            if (ok && (__ffs(peers) - 1) == lane)   // lowest lane of the peer group
+                next[e] += __popc(peers);
+            __syncwarp();
+            if (in) {
+                slots[i] = slot;
+                slot_of[(size_t)t0 * K + i] = slot;
+            }
+        }
+    }
+    __syncthreads();
+    // gather: each token row is read once and written to its K slots
+    const int vec_per_row = H / 8;                    // 16-byte vectors
+    const int rows_per_pass = blockDim.x / vec_per_row > 0 ? blockDim.x / vec_per_row : 1;
+    const int sub = threadIdx.x / vec_per_row;
+    const int v = threadIdx.x % vec_per_row;
+    if (sub < rows_per_pass) {
+        for (int vv = v; vv < vec_per_row; vv += blockDim.x) {
+            // four tokens per step so that four loads are in flight per thread
+            for (int tl = sub; tl < nt; tl += 4 * rows_per_pass) {
+                uint4 val[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int tt = tl + u * rows_per_pass;
+                    if (tt < nt)
+                        val[u] = reinterpret_cast<const uint4 *>(x + (size_t)(t0 + tt) * H)[vv];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int tt = tl + u * rows_per_pass;
+                    if (tt < nt)
+                        for (int j = 0; j < K; ++j) {
+                            const int slot = slots[tt * K + j];
+                            if (slot >= 0)
+                                reinterpret_cast<uint4 *>(x_perm + (size_t)slot * H)[vv] = val[u];
+                        }
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base, int T, int H,
+                                  int E, int k, int32_t *slot_of, uint16_t *x_perm, cudaStream_t s)
+{
+    const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
+    const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
+    bucket_scatter_kernel<<<blocks, 256, smem, s>>>(idx, x, chunk_base, T, H, E, k, slot_of, x_perm);
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
+// out[t] = bf16( sum_j w[t,j] * Y[slot_of[t,j]] + Y[K*T + t] (+ residual[t]) ),
+// fp32 accumulation in j order.  A thread owns 8 consecutive columns (one
+// 16-byte vector) of a token; a 256-thread block covers 2048 columns.
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ Y,
+                                                      const int32_t *__restrict__ slot_of,
+                                                      const float *__restrict__ w,
+                                                      const uint16_t *__restrict__ residual, int T, int H, int K,
+                                                      uint16_t *__restrict__ out)
+{
+    const int vec_per_row = H / 8;
+    const long long total = (long long)T * vec_per_row;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int t = (int)(i / vec_per_row);
+        const int v = (int)(i % vec_per_row);
+        float acc[8];
+        {
+            const uint4 sv = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + t) * H)[v];
+            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&sv);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __bfloat1622float2(p2[q]);
+                acc[2 * q] = f.x;
+                acc[2 * q + 1] = f.y;
+            }
+        }
+        float racc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            racc[q] = 0.0f;
+        for (int j = 0; j < K; ++j) {
+            const int slot = slot_of[(size_t)t * K + j];
+            if (slot < 0)
+                continue;
+            const float wj = w[(size_t)t * K + j];
+            const uint4 yv = reinterpret_cast<const uint4 *>(Y + (size_t)slot * H)[v];
+            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&yv);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __bfloat1622float2(p2[q]);
+                racc[2 * q] += wj * f.x;
+                racc[2 * q + 1] += wj * f.y;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            acc[q] += racc[q];
+        if (residual) {
+            const uint4 rv = reinterpret_cast<const uint4 *>(residual + (size_t)t * H)[v];
+            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&rv);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float2 f = __bfloat1622float2(p2[q]);
+                acc[2 * q] += f.x;
+                acc[2 * q + 1] += f.y;
+            }
+        }
+        uint4 o;
+        uint32_t *op = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            op[q] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        reinterpret_cast<uint4 *>(out + (size_t)t * H)[v] = o;
+    }
+}
+
+cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
+                           int T, int H, int k, uint16_t *out, cudaStream_t s)
+{
+    const long long total = (long long)T * (H / 8);
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long want = (total + 255) / 256;
+    const int blocks = (int)min(want, (long long)sms * 8);
+    combine_kernel<<<blocks, 256, 0, s>>>(Y, slot_of, w, residual, T, H, k, out);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace glr

@@ -1,0 +1,241 @@
+"""PyTorch-facing calls of the GB300 MoE layer forward.
+
+Each function checks tensor shapes, dtypes and devices, passes raw pointers
+and the current CUDA stream to the C ABI (include/moe.h) and returns torch
+tensors.  No arithmetic of the layer happens here: routing, bucketing, the
+expert GEMMs and the combine all run in libglr_moe.so's kernels.
+
+The layer is the one of the article "InternLumina-U2中256个专家的路由秘密：
+分组受限Top-K、Expert Bias与Fused MoE详解": fp32 sigmoid router over E experts,
+group-limited top-k (section 二), selection-only expert bias (section 三),
+SwiGLU experts with stacked [E, I, H] weights (section 四) and one shared
+expert (section 五).
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import Optional
+
+import torch
+
+from . import _lib
+
+
+@dataclasses.dataclass(frozen=True)
+class MoeConfig:
+    """moe_cfg of include/moe.h (defaults: the article's hyper-parameter table)."""
+    T: int
+    H: int = 2048
+    E: int = 256
+    n_group: int = 8
+    topk_group: int = 4
+    k: int = 8
+    I: int = 512
+    Is: int = 512
+    rsf: float = 2.5
+    eps: float = 1e-20
+
+    def c(self) -> _lib.MoeCfg:
+        return _lib.MoeCfg(self.T, self.H, self.E, self.n_group, self.topk_group, self.k, self.I, self.Is,
+                           self.rsf, self.eps)
+
+    def with_T(self, T: int) -> "MoeConfig":
+        return dataclasses.replace(self, T=T)
+
+
+def workspace_bytes(cfg: MoeConfig, which: int) -> int:
+    n = _lib.load().moe_workspace_bytes(ctypes.byref(cfg.c()), which)
+    if n == 0:
+        raise ValueError("configuration not supported: %r" % (cfg,))
+    return int(n)
+
+
+class Workspace:
+    """A device workspace for moe_route (ROUTE) or moe_forward (FORWARD)."""
+
+    def __init__(self, cfg: MoeConfig, which: int, device=None):
+        self.which = which
+        self.nbytes = workspace_bytes(cfg, which)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        assert self.buf.data_ptr() % 256 == 0
+        _lib.check(_lib.load().moe_workspace_init(self.ptr, self.nbytes, _stream(self.buf.device)),
+                   "moe_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def fits(self, cfg: MoeConfig) -> bool:
+        return workspace_bytes(cfg, self.which) <= self.nbytes
+
+    def status(self, reset: bool = True) -> int:
+        v = ctypes.c_int32(0)
+        _lib.check(_lib.load().moe_get_status(self.ptr, self.nbytes, _stream(self.buf.device), ctypes.byref(v),
+                                              1 if reset else 0), "moe_get_status")
+        return int(v.value)
+
+
+def _stream(device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape, device) -> int:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if t.device != device:
+        raise ValueError("%s must be on %s, got %s" % (name, device, t.device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _opt(t, name, dtype, shape, device) -> Optional[int]:
+    return None if t is None else _need(t, name, dtype, shape, device)
+
+
+def _ws(ws: Optional[Workspace], cfg: MoeConfig, which: int, device) -> Workspace:
+    if ws is None:
+        ws = Workspace(cfg, which, device)
+    elif ws.which != which or not ws.fits(cfg):
+        raise ValueError("workspace of the wrong kind or too small")
+    return ws
+
+
+def route(cfg: MoeConfig, hidden, W_router, expert_bias=None, *, aux: bool = False,
+          ws: Optional[Workspace] = None, out=None):
+    """moe_route: (topk_idx [T,k] int32, topk_w [T,k] fp32, expert_counts [E]
+    int32, aux_P [E] fp32 or None, aux_loss [1] fp32 or None)."""
+    dev = hidden.device
+    ph = _need(hidden, "hidden", torch.bfloat16, (cfg.T, cfg.H), dev)
+    pw = _need(W_router, "W_router", torch.float32, (cfg.E, cfg.H), dev)
+    pb = _opt(expert_bias, "expert_bias", torch.float32, (cfg.E,), dev)
+    if out is None:
+        idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+        w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+        counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+        aux_P = torch.empty(cfg.E, dtype=torch.float32, device=dev) if aux else None
+        aux_loss = torch.empty(1, dtype=torch.float32, device=dev) if aux else None
+    else:
+        idx, w, counts, aux_P, aux_loss = out
+    ws = _ws(ws, cfg, _lib.MOE_WS_ROUTE, dev)
+    rc = _lib.load().moe_route(ctypes.byref(cfg.c()), ph, pw, pb, idx.data_ptr(), w.data_ptr(), counts.data_ptr(),
+                               None if aux_P is None else aux_P.data_ptr(),
+                               None if aux_loss is None else aux_loss.data_ptr(),
+                               ws.ptr, ws.nbytes, _stream(dev))
+    _lib.check(rc, "moe_route")
+    return idx, w, counts, aux_P, aux_loss
+
+
+def router_logits(cfg: MoeConfig, hidden, W_router, *, ws: Optional[Workspace] = None):
+    """moe_router_logits: fp32 logits [T, E]."""
+    dev = hidden.device
+    ph = _need(hidden, "hidden", torch.bfloat16, (cfg.T, cfg.H), dev)
+    pw = _need(W_router, "W_router", torch.float32, (cfg.E, cfg.H), dev)
+    logits = torch.empty(cfg.T, cfg.E, dtype=torch.float32, device=dev)
+    ws = _ws(ws, cfg, _lib.MOE_WS_ROUTE, dev)
+    _lib.check(_lib.load().moe_router_logits(ctypes.byref(cfg.c()), ph, pw, logits.data_ptr(), ws.ptr, ws.nbytes,
+                                             _stream(dev)), "moe_router_logits")
+    return logits
+
+
+def route_from_logits(cfg: MoeConfig, logits, expert_bias=None, *, aux: bool = False,
+                      ws: Optional[Workspace] = None):
+    """moe_route_from_logits: same outputs as route(), from fp32 logits."""
+    dev = logits.device
+    pl = _need(logits, "logits", torch.float32, (cfg.T, cfg.E), dev)
+    pb = _opt(expert_bias, "expert_bias", torch.float32, (cfg.E,), dev)
+    idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+    w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=dev)
+    aux_P = torch.empty(cfg.E, dtype=torch.float32, device=dev) if aux else None
+    aux_loss = torch.empty(1, dtype=torch.float32, device=dev) if aux else None
+    ws = _ws(ws, cfg, _lib.MOE_WS_ROUTE, dev)
+    rc = _lib.load().moe_route_from_logits(ctypes.byref(cfg.c()), pl, pb, idx.data_ptr(), w.data_ptr(),
+                                           counts.data_ptr(), None if aux_P is None else aux_P.data_ptr(),
+                                           None if aux_loss is None else aux_loss.data_ptr(), ws.ptr, ws.nbytes,
+                                           _stream(dev))
+    _lib.check(rc, "moe_route_from_logits")
+    return idx, w, counts, aux_P, aux_loss
+
+
+def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w,
+            residual=None, *, ws: Optional[Workspace] = None, out=None):
+    """moe_forward: out [T, H] bf16 = sum_j w * SwiGLU_e(x) + shared(x) (+ residual)."""
+    dev = hidden.device
+    bf = torch.bfloat16
+    ph = _need(hidden, "hidden", bf, (cfg.T, cfg.H), dev)
+    pgu = _need(W_gate_up, "W_gate_up", bf, (cfg.E, 2 * cfg.I, cfg.H), dev)
+    pd = _need(W_down, "W_down", bf, (cfg.E, cfg.I, cfg.H), dev)
+    psgu = _need(shared_gate_up, "shared_gate_up", bf, (2 * cfg.Is, cfg.H), dev)
+    psd = _need(shared_down, "shared_down", bf, (cfg.Is, cfg.H), dev)
+    pi = _need(topk_idx, "topk_idx", torch.int32, (cfg.T, cfg.k), dev)
+    pw = _need(topk_w, "topk_w", torch.float32, (cfg.T, cfg.k), dev)
+    pr = _opt(residual, "residual", bf, (cfg.T, cfg.H), dev)
+    if out is None:
+        out = torch.empty(cfg.T, cfg.H, dtype=bf, device=dev)
+    po = _need(out, "out", bf, (cfg.T, cfg.H), dev)
+    ws = _ws(ws, cfg, _lib.MOE_WS_FORWARD, dev)
+    rc = _lib.load().moe_forward(ctypes.byref(cfg.c()), ph, pgu, pd, psgu, psd, pi, pw, pr, po, ws.ptr, ws.nbytes,
+                                 _stream(dev))
+    _lib.check(rc, "moe_forward")
+    return out
+
+
+def last_launch_count() -> int:
+    """Kernels the last call on this thread enqueued."""
+    return int(_lib.load().moe_last_launch_count())
+
+
+def profile_enable(on: bool = True) -> None:
+    """Bracket every kernel the library launches with CUDA events."""
+    _lib.load().moe_profile_enable(1 if on else 0)
+
+
+def profile_read(reset: bool = True) -> dict:
+    """{kernel name: (total ms, launches)} recorded since the last reset."""
+    lib = _lib.load()
+    out = {}
+    for kid in range(_lib.MOE_KERNEL_COUNT):
+        ms = ctypes.c_double(0.0)
+        n = ctypes.c_int32(0)
+        _lib.check(lib.moe_profile_read(kid, ctypes.byref(ms), ctypes.byref(n), 1 if reset else 0),
+                   "moe_profile_read")
+        out[lib.moe_kernel_name(kid).decode()] = (float(ms.value), int(n.value))
+    return out
+
+
+class MoELayer:
+    """One MoE layer: weights on the device plus its two workspaces.
+
+    __call__(hidden) runs moe_route then moe_forward on the current stream."""
+
+    def __init__(self, cfg: MoeConfig, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
+                 aux: bool = False):
+        self.cfg = cfg
+        self.W_router, self.expert_bias = W_router, expert_bias
+        self.W_gate_up, self.W_down = W_gate_up, W_down
+        self.shared_gate_up, self.shared_down = shared_gate_up, shared_down
+        self.aux = aux
+        dev = W_router.device
+        self.ws_route = Workspace(cfg, _lib.MOE_WS_ROUTE, dev)
+        self.ws_fwd = Workspace(cfg, _lib.MOE_WS_FORWARD, dev)
+        self.routing = None
+        self.last_launches = 0
+
+    def __call__(self, hidden, residual=None, out=None):
+        self.routing = route(self.cfg, hidden, self.W_router, self.expert_bias, aux=self.aux, ws=self.ws_route,
+                             out=self.routing)
+        n = last_launch_count()
+        idx, w = self.routing[0], self.routing[1]
+        y = forward(self.cfg, hidden, self.W_gate_up, self.W_down, self.shared_gate_up, self.shared_down, idx,
+                    w, residual, ws=self.ws_fwd, out=out)
+        self.last_launches = n + last_launch_count()
+        return y
+
+    def status(self) -> int:
+        return self.ws_route.status() | self.ws_fwd.status()

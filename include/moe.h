@@ -1,0 +1,190 @@
+/*
+ * moe.h -- C ABI of the group-limited MoE layer forward on GB300 (sm_103a).
+ *
+ * The layer is the one described in the article
+ *   "InternLumina-U2中256个专家的路由秘密：分组受限Top-K、Expert Bias与Fused MoE详解"
+ * (called "the routing page" below):
+ *   - an fp32 linear router followed by an element-wise sigmoid (section 二, step 1);
+ *   - group-limited top-k: the experts are cut in order into n_group groups, a
+ *     group scores the sum of its two best scores, the topk_group best groups
+ *     survive and the top k of their experts are chosen (section 二, step 2);
+ *   - expert_bias is added to the scores for choosing only (section 三);
+ *   - the weights are the chosen unbiased scores over (their sum + eps), times
+ *     routed_scaling_factor (section 二, step 3);
+ *   - every chosen expert is a SwiGLU FFN whose gate, up and down weights are
+ *     stacked per expert (section 四); one shared expert is always added
+ *     (section 五); expert hit counts are kept (section 六).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise; all
+ *     tensors are dense, row-major, with no padding between rows.
+ *   - bf16 tensors are passed as their 16-bit patterns (moe_bf16).
+ *   - The caller owns every buffer, including the workspace.  The library
+ *     never allocates or frees device memory and never synchronises the stream
+ *     (moe_get_status excepted).  Work is enqueued on `stream`, a cudaStream_t
+ *     passed as void* (NULL = the legacy default stream); outputs are ready
+ *     when that stream reaches the point of the call.
+ *   - Every entry point validates its arguments first and returns a negative
+ *     MOE_ERR_* code without launching anything when they are wrong.  It never
+ *     truncates or clamps silently.  MOE_ERR_CUDA means a launch failed; the
+ *     CUDA error is left for the caller to read with cudaGetLastError().
+ *   - Faults found on the device (non-finite logits, an expert index out of
+ *     range, a wait that ran out) never trap: the kernel records a bit in the
+ *     workspace's status word, skips the offending item, and returns.  Read
+ *     and clear the word with moe_get_status().
+ *   - Workspaces are 256-byte aligned blocks of moe_workspace_bytes() bytes.
+ *     Call moe_workspace_init() once after allocating one.  Two calls that use
+ *     the same workspace must not run concurrently.
+ *   - Pointers handed to the tensor-core kernels must be 16-byte aligned
+ *     (MOE_ERR_MISALIGNED otherwise).
+ *
+ * Supported shapes (MOE_ERR_UNSUPPORTED_SHAPE otherwise): E == 32 * n_group
+ * with 1 <= n_group <= 8 (one expert per lane per group in the routing warp),
+ * 1 <= topk_group <= n_group, 1 <= k <= min(32, 32 * topk_group), E % 128 == 0
+ * for the router GEMM, H % 256 == 0, I % 128 == 0, Is == I, 1 <= T <= 2^24.
+ */
+#ifndef GLR_MOE_H
+#define GLR_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16; /* bf16 bit pattern */
+
+/* Layer configuration (routing page, section 一, hyper-parameter table):
+ * T tokens, hidden size H, E routed experts in n_group groups of which
+ * topk_group survive, k experts per token, expert FFN inner size I, shared
+ * expert inner size Is, routed_scaling_factor rsf (2.5) and the normaliser's
+ * eps (1e-20, section 二 step 3). */
+typedef struct moe_cfg {
+    int32_t T, H, E, n_group, topk_group, k, I, Is;
+    float rsf, eps;
+} moe_cfg;
+
+/* return codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)
+#define MOE_ERR_UNSUPPORTED_SHAPE (-2)
+#define MOE_ERR_MISALIGNED (-3)
+#define MOE_ERR_WORKSPACE_TOO_SMALL (-4)
+#define MOE_ERR_CUDA (-5)
+#define MOE_ERR_DEVICE_STATUS (-6)
+#define MOE_ERR_TIMEOUT (-7)
+#define MOE_ERR_UNSUPPORTED_DEVICE (-8)
+
+/* bits of the device status word */
+#define MOE_STATUS_NONFINITE_LOGIT 1   /* a logit, score or bias was NaN/inf     */
+#define MOE_STATUS_BAD_EXPERT_INDEX 2  /* topk_idx held an id outside [0, E)     */
+#define MOE_STATUS_TIMEOUT 4           /* a bounded device wait ran out          */
+#define MOE_STATUS_COUNT_MISMATCH 8    /* bucketed rows != k*T (follows from 2)  */
+
+/* workspace kinds */
+#define MOE_WS_ROUTE 0
+#define MOE_WS_FORWARD 1
+
+/* Bytes of workspace that moe_route (which = MOE_WS_ROUTE) or moe_forward
+ * (which = MOE_WS_FORWARD) needs for this configuration; 0 if the
+ * configuration is invalid or unsupported.  Host only, no CUDA call. */
+size_t moe_workspace_bytes(const moe_cfg *cfg, int which);
+
+/* Clears the status word and the bookkeeping header of a freshly allocated
+ * workspace (an asynchronous memset on `stream`). */
+int moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/* Router of the routing page, section 二 steps 1-3 and section 三, for T tokens.
+ *   hidden       [T, H] bf16
+ *   W_router     [E, H] fp32 (the router is computed to fp32 accuracy: the
+ *                weight is split into three bf16 parts whose products with
+ *                the bf16 hidden state are exact, accumulated in fp32)
+ *   expert_bias  [E] fp32, or NULL for zero; used for choosing only
+ *   topk_idx     [T, k] int32 out: chosen experts in order of (biased score
+ *                desc, index asc); ties go to the lower index
+ *   topk_w       [T, k] fp32 out: s / (sum of the k chosen s + eps) * rsf,
+ *                s the unbiased sigmoid scores
+ *   expert_counts[E] int32 out: hits per expert over the T tokens (section 六)
+ *   aux_P        [E] fp32 out or NULL: mean over tokens of each expert's
+ *                score divided by the token's score sum
+ *   aux_loss     [1] fp32 out or NULL: E * sum_i (counts_i / (k T)) * P_i,
+ *                the load-balancing loss of the pitfalls page ("MoE 负载均衡
+ *                Loss 别忘加" of the InternLumina-U2 training-pitfalls article)
+ *   ws           workspace of moe_workspace_bytes(cfg, MOE_WS_ROUTE) bytes
+ * Deterministic: the same inputs give bit-identical outputs. */
+int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
+              const float *expert_bias, int32_t *topk_idx, float *topk_w,
+              int32_t *expert_counts, float *aux_P, float *aux_loss,
+              void *ws, size_t ws_bytes, void *stream);
+
+/* The first half of moe_route alone: logits [T, E] fp32 = hidden . W_router^T
+ * (routing page, section 二 step 1).  Same arguments and workspace. */
+int moe_router_logits(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
+                      float *logits, void *ws, size_t ws_bytes, void *stream);
+
+/* The second half of moe_route alone: selection, weights, counts and the
+ * balance loss from given fp32 logits [T, E] (routing page, section 二 steps
+ * 1-3, section 三).  Same outputs and workspace as moe_route; non-finite
+ * logits set MOE_STATUS_NONFINITE_LOGIT. */
+int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *expert_bias,
+                          int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                          float *aux_P, float *aux_loss, void *ws, size_t ws_bytes, void *stream);
+
+/* Expert stage of the routing page, sections 四 and 五:
+ *   out[t] = bf16( sum_j topk_w[t,j] * FFN_{topk_idx[t,j]}(hidden[t])
+ *                  + FFN_shared(hidden[t]) (+ residual[t]) )
+ * with FFN(x) = down( silu(gate x) * up x ), silu(z) = z / (1 + exp(-z)); the
+ * products run on tensor cores with bf16 operands and fp32 accumulation; the
+ * SwiGLU intermediate and each expert's output row are stored as bf16; the
+ * weighted sum is fp32 and rounded once.
+ *   hidden          [T, H] bf16
+ *   W_gate_up       [E, 2I, H] bf16: per expert, rows [0, I) are gate_proj and
+ *                   rows [I, 2I) are up_proj (each [I, H], the page's
+ *                   [256, 512, 2048] stacks)
+ *   W_down          [E, I, H] bf16: down_proj as the page stacks it,
+ *                   expert output = intermediate[1, I] @ W_down[e]
+ *   shared_gate_up  [2Is, H] bf16, same layout as one expert of W_gate_up
+ *   shared_down     [Is, H] bf16
+ *   topk_idx        [T, k] int32 (any order; an id outside [0, E) is skipped
+ *                   and sets MOE_STATUS_BAD_EXPERT_INDEX)
+ *   topk_w          [T, k] fp32
+ *   residual        [T, H] bf16 or NULL: added before the final rounding
+ *                   (a decoder layer's residual connection)
+ *   out             [T, H] bf16 out (may alias residual, not hidden)
+ *   ws              workspace of moe_workspace_bytes(cfg, MOE_WS_FORWARD) bytes
+ * Tokens are bucketed by expert in a stable order (the "sort tokens into
+ * buckets" inference path of section 四), so outputs are deterministic. */
+int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_gate_up,
+                const moe_bf16 *W_down, const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down,
+                const int32_t *topk_idx, const float *topk_w, const moe_bf16 *residual,
+                moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Waits for `stream`, then copies the workspace's status word (MOE_STATUS_*
+ * bits, OR-ed over every call since the last reset) to *status (a HOST
+ * pointer); clears it when reset != 0.  Returns MOE_OK, or MOE_ERR_CUDA. */
+int moe_get_status(void *ws, size_t ws_bytes, void *stream, int32_t *status, int reset);
+
+/* Number of kernels the last successful moe_route / moe_forward /
+ * moe_route_from_logits / moe_router_logits call on this thread enqueued. */
+int moe_last_launch_count(void);
+
+/* Per-kernel timing.  While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on its stream (a few microseconds of
+ * overhead per launch, no synchronisation).  moe_profile_read() waits for
+ * the recorded events, folds them into per-kernel totals and returns the
+ * total milliseconds and launch count of kernel `kernel_id` (0 <=
+ * kernel_id < MOE_KERNEL_COUNT), clearing them when reset != 0. */
+#define MOE_KERNEL_COUNT 10
+int moe_profile_enable(int on);
+int moe_profile_read(int kernel_id, double *total_ms, int32_t *launches, int reset);
+const char *moe_kernel_name(int kernel_id);
+
+/* Static description of a return code. */
+const char *moe_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GLR_MOE_H */

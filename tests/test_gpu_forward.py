@@ -1,0 +1,183 @@
+"""Expert-stage parity on the GPU: moe_forward against the CPU oracle.
+
+The oracle takes the routing the GPU uses as its input (teacher forcing), so
+near-tie routing decisions cannot pollute the output check.  Cases cover the
+five workloads' shapes (sampled tokens at full size), ragged T, empty and
+overfull buckets (0, 1, 127, 128, 129 rows and one expert holding every
+row), zero weights (shared expert only), the residual, bad indices and
+determinism."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from group_limited_routing_gb300 import moe, workloads as wl
+from parity import assert_output_close, bf16_to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def u16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+class Host:
+    """Host copies of a layer's bf16 weights for the oracle (bit patterns)."""
+
+    def __init__(self, d):
+        self.x = u16(d["hidden"])
+        self.gu = u16(d["W_gate_up"])
+        self.dn = u16(d["W_down"])
+        self.sgu = u16(d["shared_gate_up"])
+        self.sd = u16(d["shared_down"])
+
+
+def check(cfg, d, idx, w, tokens=None, residual=None, what="", host=None):
+    out = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"],
+                      idx, w, residual)
+    torch.cuda.synchronize()
+    h = host or Host(d)
+    tok = None if tokens is None else np.asarray(tokens, dtype=np.int32)
+    ref = oracle.experts(h.x, h.gu, h.dn, h.sgu, h.sd, idx.cpu().numpy(), w.cpu().numpy(),
+                         residual=None if residual is None else u16(residual), tokens=tok)
+    got = bf16_to_f64(out)
+    if tok is not None:
+        got = got[tok]
+    e = assert_output_close(got, ref, what)
+    print("%s: max err %.3e (max ref %.3e), mean rel %.3e, rel-L2 %.3e" % (what, e["max_err"], e["max_ref"],
+                                                                             e["mean_rel"], e["rel_l2"]))
+    return out
+
+
+def small_layer(T, H=512, I=128, E=256, seed=0):
+    w0 = wl.Workload(90 + seed, "test", T=T, H=H, E=E, n_group=E // 32, I=I, Is=I)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T, H=H, E=E, n_group=E // 32, I=I, Is=I)
+    return cfg, d
+
+
+@pytest.mark.parametrize("wid,T,nsample", [(1, 128, None), (2, 16, None), (3, 4096, 256), (4, 32768, 256),
+                                           (5, 8192, 192)])
+def test_forward_matches_oracle_on_workloads(wid, T, nsample):
+    w0 = wl.WORKLOADS[wid].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
+    idx, w, _, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    tokens = None
+    if nsample is not None:
+        tokens = np.union1d(wl.token_sample(T, nsample, seed=wid).numpy(), [0, T - 1]).astype(np.int32)
+    check(cfg, d, idx, w, tokens, what="workload %d T=%d" % (wid, T))
+
+
+@pytest.mark.parametrize("T", [1, 7, 128, 300, 1000])
+def test_forward_ragged_T_random_routing(T):
+    cfg, d = small_layer(T, seed=T % 7)
+    idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=T, device=DEV)
+    check(cfg, d, idx, w, what="ragged T=%d" % T)
+
+
+def test_forward_bucket_sizes_and_empty_experts():
+    # bucket sizes 0, 1, 127, 128, 129 and one large bucket, by construction
+    T, k, E = 1200, 8, 256
+    cfg, d = small_layer(T, E=E, seed=3)
+    rng = np.random.default_rng(5)
+    sizes = {10: 1, 11: 127, 12: 128, 13: 129, 14: 255}
+    pairs = []
+    for e, n in sizes.items():
+        pairs += [e] * n
+    rest = [e for e in range(20, 200)] * 100
+    need = T * k - len(pairs)
+    pairs += rest[:need]
+    pairs = np.array(pairs, dtype=np.int32)
+    # token t gets pairs[t::T]; a token may hold an expert twice, which the
+    # expert stage treats as two separate (token, expert) pairs
+    idx = pairs.reshape(k, T).T.copy()
+    counts = np.bincount(idx.ravel(), minlength=E)
+    assert [counts[e] for e in sizes] == list(sizes.values()) and counts[0] == 0
+    w = rng.random((T, k)).astype(np.float32)
+    check(cfg, d, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), what="bucket sizes")
+
+
+def test_forward_one_expert_holds_every_row():
+    T = 500
+    cfg, d = small_layer(T, seed=4)
+    idx = torch.full((T, cfg.k), 77, dtype=torch.int32, device=DEV)   # every slot to expert 77
+    w = torch.rand(T, cfg.k, device=DEV) * 0.3
+    check(cfg, d, idx, w, what="one expert, %d rows" % (T * cfg.k))
+
+
+def test_forward_zero_weights_is_shared_expert_only():
+    T = 256
+    cfg, d = small_layer(T, seed=5)
+    idx, _ = wl.random_routing(T, cfg.E, cfg.k, seed=9, device=DEV)
+    w = torch.zeros(T, cfg.k, device=DEV)
+    out = check(cfg, d, idx, w, what="zero weights")
+    # the same as routing every token nowhere useful: equals shared(x) computed with other indices
+    idx2, _ = wl.random_routing(T, cfg.E, cfg.k, seed=10, device=DEV)
+    out2 = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"],
+                       idx2, w)
+    assert torch.equal(out, out2)
+
+
+def test_forward_with_residual_full_size():
+    w0 = wl.WORKLOADS[5].with_T(1024)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=1024)
+    idx, w, _, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    res = torch.randn(1024, 2048, device=DEV).to(torch.bfloat16)
+    tokens = wl.token_sample(1024, 128, seed=2).numpy()
+    check(cfg, d, idx, w, tokens, residual=res, what="residual")
+
+
+def test_forward_out_may_alias_residual():
+    T = 200
+    cfg, d = small_layer(T, seed=6)
+    idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=11, device=DEV)
+    res = torch.randn(T, cfg.H, device=DEV).to(torch.bfloat16)
+    expect = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"],
+                         idx, w, res.clone())
+    buf = res.clone()
+    moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w,
+                buf, out=buf)
+    assert torch.equal(buf, expect)
+
+
+def test_forward_bad_index_is_skipped_and_reported():
+    T = 64
+    cfg, d = small_layer(T, seed=7)
+    idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=12, device=DEV)
+    bad = idx.clone()
+    bad[3, 2] = cfg.E          # out of range: the kernels skip it and flag it
+    bad[9, 0] = -1
+    ws = moe.Workspace(cfg, 1, DEV)
+    out = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"],
+                      bad, w, ws=ws)
+    st = ws.status()
+    assert st & 2 and st & 8
+    # the skipped pairs contribute nothing: same as weight 0 for them
+    w2 = w.clone()
+    w2[3, 2] = 0.0
+    w2[9, 0] = 0.0
+    ok = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"],
+                     idx, w2)
+    assert torch.equal(out, ok)
+    assert ws.status() == 0
+
+
+def test_forward_is_deterministic():
+    w0 = wl.WORKLOADS[3].with_T(4096)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=4096)
+    idx, w, _, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    a = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
+    b = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
+    assert torch.equal(a, b)
+
+
+def test_forward_launch_count():
+    T = 128
+    cfg, d = small_layer(T, seed=8)
+    idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=13, device=DEV)
+    moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
+    assert moe.last_launch_count() == 6   # hist, scan, scatter, gate/up GEMM, down GEMM, combine

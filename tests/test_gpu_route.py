@@ -1,0 +1,127 @@
+"""Router parity on the GPU: moe_router_logits, moe_route_from_logits and
+moe_route against the CPU oracle, on the five workloads' shapes and on edge
+cases (ties, ragged T, other group settings)."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from group_limited_routing_gb300 import moe, workloads as wl
+from parity import compare_counts, compare_routing
+from test_oracle_pins import _parse_logits
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def u16(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def run_route(cfg, x, W, bias, aux=True):
+    idx, w, counts, P, loss = moe.route(cfg, x, W, bias, aux=aux)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), w.cpu().numpy(), counts.cpu().numpy(), \
+        (P.cpu().numpy() if P is not None else None), (float(loss.item()) if loss is not None else None)
+
+
+@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (3, 4096), (4, 32768), (5, 8192)])
+def test_route_matches_oracle(wid, T):
+    w0 = wl.WORKLOADS[wid].with_T(T)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
+    gi, gw, gc, gP, gloss = run_route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    x = u16(d["hidden"])
+    L = oracle.router_logits(x, d["W_router"].cpu().numpy())
+    ref = oracle.route(L, bias=d["expert_bias"].cpu().numpy())
+    rep = {}
+    n_near, near = compare_routing(gi, gw, ref, cfg.E, rep, bias=d["expert_bias"].cpu().numpy())
+    rc, rP, rloss = oracle.counts_aux(ref["idx"], ref["scores"])
+    compare_counts(gc, gi, rc, ref["idx"], near, cfg.E)
+    np.testing.assert_allclose(gP, rP, rtol=1e-4, atol=1e-7)
+    assert abs(gloss - rloss) <= 1e-4 * abs(rloss)
+    print("workload %d T=%d near-tie tokens %d (%.3f%%), order-only ties %d, max w err %.2e" % (
+        wid, T, n_near, 100.0 * n_near / T, rep["order_tie_tokens"], rep["max_w_err"]))
+    assert n_near <= max(2, T // 100)
+
+
+@pytest.mark.parametrize("wid,T", [(1, 128), (3, 4096), (4, 2048)])
+def test_router_logits_accuracy(wid, T):
+    w0 = wl.WORKLOADS[wid].with_T(T)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
+    g = moe.router_logits(cfg, d["hidden"], d["W_router"]).cpu().numpy()
+    L = oracle.router_logits(u16(d["hidden"]), d["W_router"].cpu().numpy())
+    err = np.abs(g.astype(np.float64) - L)
+    # bf16 x (hi + mid + lo) products are exact; only fp32 accumulation differs
+    assert err.max() <= 2e-6 + 2e-6 * np.abs(L).max(), err.max()
+    print("workload %d: router logits max abs err %.3e (max |logit| %.2f)" % (wid, err.max(), np.abs(L).max()))
+
+
+@pytest.mark.parametrize("T,n_group,topk_group,k,scale", [
+    (1, 8, 4, 8, 1.0), (130, 8, 4, 8, 1.0), (1000, 8, 1, 8, 2.0), (777, 8, 8, 8, 1.0),
+    (513, 8, 4, 1, 1.0), (300, 8, 4, 32, 1.0), (257, 4, 2, 6, 1.0), (129, 4, 4, 32, 3.0),
+])
+def test_route_from_logits_edge_shapes(T, n_group, topk_group, k, scale):
+    rng = np.random.default_rng(T * 7 + k)
+    E = 32 * n_group
+    L = (rng.standard_normal((T, E)) * scale).astype(np.float32)
+    bias = (rng.standard_normal(E) * 0.05).astype(np.float32)
+    cfg = moe.MoeConfig(T=T, H=2048, E=E, n_group=n_group, topk_group=topk_group, k=k)
+    gi, gw, gc, gP, gl = [a.cpu().numpy() if a is not None else None for a in
+                          moe.route_from_logits(cfg, torch.from_numpy(L).to(DEV), torch.from_numpy(bias).to(DEV),
+                                                aux=True)]
+    ref = oracle.route(L, bias=bias, n_group=n_group, topk_group=topk_group, k=k)
+    n_near, near = compare_routing(gi, gw, ref, E, bias=bias)
+    rc, rP, rl = oracle.counts_aux(ref["idx"], ref["scores"], E=E)
+    compare_counts(gc, gi, rc, ref["idx"], near, E)
+    np.testing.assert_allclose(gP, rP, rtol=1e-4, atol=1e-7)
+    assert abs(gl[0] - rl) <= 1e-4 * abs(rl)
+
+
+def test_route_handworked_golden_tokens():
+    with open(os.path.join(GOLDEN, "route_handworked.json")) as f:
+        fx = json.load(f)
+    for tok in fx["tokens"]:
+        L, bias = _parse_logits(tok)
+        cfg = moe.MoeConfig(T=1)
+        gi, gw, gc, _, _ = moe.route_from_logits(cfg, torch.from_numpy(L[None, :]).to(DEV),
+                                                 torch.from_numpy(bias).to(DEV))
+        assert gi.cpu().numpy()[0].tolist() == tok["idx"], tok["name"]
+        np.testing.assert_allclose(gw.cpu().numpy()[0], tok["w"], atol=1e-6, err_msg=tok["name"])
+        assert gc.sum().item() == 8
+
+
+def test_route_is_deterministic():
+    w0 = wl.WORKLOADS[4].with_T(8192)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=8192)
+    a = run_route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    b = run_route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    for x, y in zip(a[:4], b[:4]):
+        assert np.array_equal(x, y)
+    assert a[4] == b[4]
+
+
+def test_nonfinite_logits_set_status():
+    T = 64
+    L = torch.zeros(T, 256, device=DEV)
+    L[5, 17] = float("nan")
+    cfg = moe.MoeConfig(T=T)
+    ws = moe.Workspace(cfg, 0, DEV)
+    moe.route_from_logits(cfg, L, None, ws=ws)
+    assert ws.status() & 1
+    assert ws.status() == 0          # reset by the previous read
+    moe.route_from_logits(cfg, torch.zeros(T, 256, device=DEV), None, ws=ws)
+    assert ws.status() == 0
+
+
+def test_route_launch_count():
+    cfg = moe.MoeConfig(T=256)
+    d = wl.layer_inputs(wl.WORKLOADS[3].with_T(256), DEV, with_experts=False)
+    moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    assert moe.last_launch_count() == 4   # W split, router GEMM, select, finalize
