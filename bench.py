@@ -197,6 +197,8 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w0 = wl.WORKLOADS[WORKLOAD_ID]
+    if args.tokens:
+        w0 = w0.with_T(args.tokens)
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
     cfg = moe.MoeConfig(T=T, H=H, E=E, n_group=w0.n_group, topk_group=w0.topk_group, k=k, I=I, Is=w0.Is)
     d = wl.layer_inputs(w0, dev)
@@ -243,6 +245,17 @@ def run_ours(args, world, rank, local):
     prof = moe.profile_read(reset=True)
 
     # ---- end to end through the public API: pinned host in, pinned host out
+    e2e_ms = None
+    if not args.no_e2e:
+        e2e_ms = time_e2e(args, world, layer, x, out, stream, dev)
+
+    if rank != 0:
+        return None
+    return report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk)
+
+
+def time_e2e(args, world, layer, x, out, stream, dev):
+    T, H = x.shape
     x_h = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
     x_h.copy_(x)
     out_h = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
@@ -263,10 +276,11 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(world, f0.elapsed_time(f1) / args.steps, dev)
     barrier(world)
+    return e2e_ms
 
-    if rank != 0:
-        return None
 
+def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
+    T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
     pk = peaks()
     work = algorithmic_work(T, H, E, I, k)
     stages = {}
@@ -316,7 +330,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": "T=32768 full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)",
+        "config": {"workload": "T=%d full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)" % T,
                    "T_per_gpu": T, "hidden": H, "experts": E, "groups": w0.n_group, "topk_group": w0.topk_group,
                    "k": k, "inter": I, "shared_inter": w0.Is, "parallelism": "replicas (dp%d)" % world,
                    "l2": "inputs larger than L2 (1.61 GB expert weights + 134 MB hidden per step), no flush"},
@@ -326,8 +340,9 @@ def run_ours(args, world, rank, local):
                      "peak_kind": "%s bf16 dense, sustained" % pk["source"],
                      "algorithmic_flops_per_launch": g1["flops"]},
         "stages": stages,
-        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
+        "e2e": None if e2e_ms is None else
+        {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+         "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
@@ -383,7 +398,10 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-tokens", type=int, default=1024, help="oracle sample for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per reference step")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per step (default: the workload's 32768); smaller sizes for profiling captures")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

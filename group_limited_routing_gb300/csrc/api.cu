@@ -120,7 +120,7 @@ int check_forward_cfg(const moe_cfg *c)
 
 // ---------------------------------------------------------------- layouts
 struct RouteLayout {
-    size_t w3, logits, hist, ppart, total;
+    size_t w3, logits, ppart, total;
     int nchunk;
 };
 
@@ -133,8 +133,6 @@ RouteLayout route_layout(const moe_cfg &c)
     off = align_up(off + 3ull * c.E * c.H * 2, 256);
     L.logits = off;
     off = align_up(off + (size_t)c.T * c.E * 4, 256);
-    L.hist = off;
-    off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
     L.ppart = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
     L.total = off;
@@ -244,11 +242,12 @@ T *at(void *ws, size_t off)
         ++launches;                            \
     } while (0)
 
-int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, float *logits, void *ws,
-                const RouteLayout &L, int sms, cudaStream_t s, int &launches)
+// counts (nullable) is cleared by the split kernel, for the routing kernel after it.
+int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, float *logits, int32_t *counts,
+                void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches)
 {
     uint16_t *W3 = at<uint16_t>(ws, L.w3);
-    GLR_LAUNCH(KID_SPLIT, launch_split_router(W, W3, c.E, c.H, s));
+    GLR_LAUNCH(KID_SPLIT, launch_split_router(W, W3, c.E, c.H, counts, s));
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
@@ -267,15 +266,16 @@ int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, float 
     return MOE_OK;
 }
 
+// counts must be zero on the stream when this runs.
 int route_select(const moe_cfg &c, const float *logits, const float *bias, int32_t *idx, float *w,
                  int32_t *counts, float *aux_P, float *aux_loss, void *ws, const RouteLayout &L, cudaStream_t s,
                  int &launches)
 {
-    int32_t *hist = at<int32_t>(ws, L.hist);
     float *ppart = (aux_P || aux_loss) ? at<float>(ws, L.ppart) : nullptr;
-    GLR_LAUNCH(KID_SELECT, launch_route_select(logits, bias, c.T, c.E, c.n_group, c.topk_group, c.k, c.rsf, c.eps, idx, w,
-                                   hist, ppart, &header(ws)->status, s));
-    GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(hist, ppart, L.nchunk, c.T, c.E, c.k, counts, aux_P, aux_loss, s));
+    GLR_LAUNCH(KID_SELECT, launch_route_select(logits, bias, c.T, c.E, c.n_group, c.topk_group, c.k, c.rsf, c.eps, idx,
+                                               w, counts, ppart, &header(ws)->status, s));
+    if (ppart)
+        GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(counts, ppart, L.nchunk, c.T, c.E, c.k, aux_P, aux_loss, s));
     return MOE_OK;
 }
 
@@ -331,7 +331,8 @@ int moe_router_logits(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W
     if ((rc = device_check(&sms)) != MOE_OK)
         return rc;
     int launches = 0;
-    rc = router_gemm(*cfg, hidden, W_router, logits, ws, L, sms, static_cast<cudaStream_t>(stream), launches);
+    rc = router_gemm(*cfg, hidden, W_router, logits, nullptr, ws, L, sms, static_cast<cudaStream_t>(stream),
+                     launches);
     g_last_launches = launches;
     return rc;
 }
@@ -355,8 +356,11 @@ int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *
     if ((rc = device_check(&sms)) != MOE_OK)
         return rc;
     int launches = 0;
-    rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L,
-                      static_cast<cudaStream_t>(stream), launches);
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * cfg->E, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
+                      launches);
     g_last_launches = launches;
     return rc;
 }
@@ -382,7 +386,7 @@ int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     float *logits = at<float>(ws, L.logits);
-    rc = router_gemm(*cfg, hidden, W_router, logits, ws, L, sms, s, launches);
+    rc = router_gemm(*cfg, hidden, W_router, logits, expert_counts, ws, L, sms, s, launches);
     if (rc == MOE_OK)
         rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
                           launches);

@@ -1,12 +1,15 @@
 // Tensor-core GEMMs of the MoE layer forward on sm_103a (tcgen05 + TMEM + TMA).
 //
 // One persistent, warp-specialised kernel template serves three products:
-//   GK_ROUTER   logits[T, E] = hidden[T, H] . W^T in fp32 accuracy: W (fp32)
-//               is pre-split into hi + mid + lo bf16 parts, every product of a
-//               bf16 hidden value with a bf16 part is exact, and the three
-//               MMAs accumulate into one fp32 TMEM accumulator.  (Routing
+//   GK_ROUTER   logits[T, E] = hidden[T, H] . W^T to fp32 accuracy.  (Routing
 //               article "InternLumina-U2中256个专家的路由秘密…", section 二 step 1:
-//               the router linear layer runs in fp32.)
+//               the router linear layer runs in fp32.)  W (fp32) is pre-split
+//               into hi + mid + lo bf16 parts, so every product of a bf16
+//               hidden value with a part is exact.  Each 64-wide K block is
+//               summed on the tensor core into a fresh TMEM slot (12 MMAs) and
+//               the epilogue warps add the K-block partial sums in fp32 with
+//               round-to-nearest: the tensor core's own accumulation never
+//               runs over more than one K block.
 //   GK_GATE_UP  per expert bucket: G = X_e . Wgate^T, U = X_e . Wup^T, written
 //               as bf16( silu(G) * U )  (section 四: SwiGLU experts stacked as
 //               3D weights; the shared expert of section 五 is the last group).
@@ -18,8 +21,10 @@
 //   warp 1           : allocates TMEM; one lane issues tcgen05.mma and commits
 //   warps 2..5       : epilogue, TMEM -> registers -> global; warp w reads TMEM
 //                      lanes 32*(w%4) .. +31 (the lane quadrant it may access)
-// Two TMEM accumulators let the epilogue of one tile overlap the MMAs of the
-// next.  Tiles are 128 rows x BN columns; CTAs walk the tile list round-robin.
+// TMEM holds SLOTS accumulators: two whole-tile accumulators for the grouped
+// GEMMs (the epilogue of one tile overlaps the MMAs of the next), four K-block
+// slots for the router.  Tiles are 128 rows x BN columns; CTAs walk the tile
+// list round-robin.
 //
 // Every wait is bounded (see ptx.cuh).  When one runs out the CTA sets an
 // abort flag, every role leaves its loop, the producer waits (bounded) for its
@@ -38,12 +43,12 @@ struct GemmCfg;
 template <>
 struct GemmCfg<GK_ROUTER> {
     static constexpr int BN = 128;                     // experts per tile
-    static constexpr int NB = 3;                       // W parts: hi, mid, lo
     static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
-    static constexpr int B_PART = BN * GEMM_BK * 2;    // 16 KB per part
-    static constexpr int B_BYTES = NB * B_PART;
+    static constexpr int B_PART = BN * GEMM_BK * 2;    // 16 KB per W part
+    static constexpr int B_BYTES = 3 * B_PART;         // hi, mid, lo
     static constexpr int STAGES = 3;
-    static constexpr int TMEM_COLS = 256;              // 2 accumulators x 128
+    static constexpr int SLOTS = 4;                    // one slot per K block in flight
+    static constexpr int TMEM_COLS = SLOTS * BN;       // 512
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
 };
 
@@ -54,6 +59,7 @@ struct GemmCfg<GK_GATE_UP> {
     static constexpr int B_HALF = 128 * GEMM_BK * 2;   // 16 KB
     static constexpr int B_BYTES = BN * GEMM_BK * 2;
     static constexpr int STAGES = 4;
+    static constexpr int SLOTS = 2;
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
 };
@@ -65,6 +71,7 @@ struct GemmCfg<GK_DOWN> {
     static constexpr int B_ATOM = 64 * GEMM_BK * 2;    // 64 N x 64 K box, 8 KB
     static constexpr int B_BYTES = BN * GEMM_BK * 2;
     static constexpr int STAGES = 4;
+    static constexpr int SLOTS = 2;
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, true);
 };
@@ -73,8 +80,10 @@ template <int KIND>
 struct GemmLayout {
     using C = GemmCfg<KIND>;
     static constexpr int STAGE_BYTES = C::A_BYTES + C::B_BYTES;
-    static constexpr int NBARS = 2 * C::STAGES + 5;    // full, empty, tfull x2, tempty x2, fin
-    static constexpr int SMEM = C::STAGES * STAGE_BYTES + 1024 /*align*/ + NBARS * 8 + 16;
+    static constexpr int STAGING = 4 * 4096;           // 32 rows x 128 B per epilogue warp
+    // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin
+    static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1;
+    static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16;
 };
 
 struct TileInfo {
@@ -119,28 +128,29 @@ __device__ __forceinline__ void issue_loads(const GemmParams &p, const TileInfo 
 {
     using C = GemmCfg<KIND>;
     const int k0 = kb * GEMM_BK;
-    if (KIND == GK_ROUTER) {
+    if constexpr (KIND == GK_ROUTER) {
         tma_load_2d(sA, &p.tmA0, bar, k0, ti.a_row);
 #pragma unroll
         for (int s = 0; s < 3; ++s)
-            tma_load_2d(sB + s * GemmCfg<GK_ROUTER>::B_PART, &p.tmB0, bar, k0, s * p.E + ti.nt * C::BN);
-    } else if (KIND == GK_GATE_UP) {
+            tma_load_2d(sB + s * C::B_PART, &p.tmB0, bar, k0, s * p.E + ti.nt * C::BN);
+    } else if constexpr (KIND == GK_GATE_UP) {
         const CUtensorMap *ma = ti.shared ? &p.tmA1 : &p.tmA0;
         const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
         const int wrow = (ti.shared ? 0 : ti.group * 2 * p.I) + ti.nt * 128;
         tma_load_2d(sA, ma, bar, k0, ti.a_row);
-        tma_load_2d(sB, mb, bar, k0, wrow);                                      // gate rows
-        tma_load_2d(sB + GemmCfg<GK_GATE_UP>::B_HALF, mb, bar, k0, wrow + p.I);  // up rows
+        tma_load_2d(sB, mb, bar, k0, wrow);                    // gate rows
+        tma_load_2d(sB + C::B_HALF, mb, bar, k0, wrow + p.I);  // up rows
     } else {
         const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
         const int krow = (ti.shared ? 0 : ti.group * p.I) + k0;
         tma_load_2d(sA, &p.tmA0, bar, k0, ti.a_row);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            tma_load_2d(sB + q * GemmCfg<GK_DOWN>::B_ATOM, mb, bar, ti.nt * C::BN + q * 64, krow);
+            tma_load_2d(sB + q * C::B_ATOM, mb, bar, ti.nt * C::BN + q * 64, krow);
     }
 }
 
+// MMAs of one K block (64) into TMEM column base d; `acc_in` = add to what is there.
 template <int KIND>
 __device__ __forceinline__ void issue_mmas(uint32_t sA, uint32_t sB, uint32_t d, bool acc_in)
 {
@@ -148,16 +158,16 @@ __device__ __forceinline__ void issue_mmas(uint32_t sA, uint32_t sB, uint32_t d,
 #pragma unroll
     for (int kk = 0; kk < GEMM_BK / 16; ++kk) {
         const uint64_t ad = sdesc_kmajor_sw128(sA + kk * 32);
-        if (KIND == GK_ROUTER) {
+        if constexpr (KIND == GK_ROUTER) {
 #pragma unroll
             for (int s = 0; s < 3; ++s)
-                umma_bf16(d, ad, sdesc_kmajor_sw128(sB + s * GemmCfg<GK_ROUTER>::B_PART + kk * 32), C::IDESC,
+                umma_bf16(d, ad, sdesc_kmajor_sw128(sB + s * C::B_PART + kk * 32), C::IDESC,
                           (acc_in || kk > 0 || s > 0) ? 1u : 0u);
-        } else if (KIND == GK_GATE_UP) {
+        } else if constexpr (KIND == GK_GATE_UP) {
             umma_bf16(d, ad, sdesc_kmajor_sw128(sB + kk * 32), C::IDESC, (acc_in || kk > 0) ? 1u : 0u);
         } else {
             // 16 K rows = two 8-row atoms = 2048 B further into each 64-wide N atom
-            umma_bf16(d, ad, sdesc_mnmajor_sw128(sB + kk * 2048, GemmCfg<GK_DOWN>::B_ATOM), C::IDESC,
+            umma_bf16(d, ad, sdesc_mnmajor_sw128(sB + kk * 2048, C::B_ATOM), C::IDESC,
                       (acc_in || kk > 0) ? 1u : 0u);
         }
     }
@@ -174,61 +184,125 @@ __device__ __forceinline__ float silu_times(float g, float u)
     return g / (1.0f + __expf(-g)) * u;
 }
 
-// Epilogue of one tile for the thread that owns accumulator row `row`.
-template <int KIND>
-__device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int row)
+// Writes one 128-byte piece of each of the warp's 32 rows (lane = row, eight
+// 16-byte chunks in v) to global memory.  The pieces go through the warp's
+// 4 KB staging buffer (16-byte chunks XOR-swizzled by row, so both the
+// writes and the reads are free of bank conflicts) and come out so that each
+// store instruction writes four whole 128-byte lines instead of 32 scattered
+// 16-byte pieces.  gbase is the address of the piece of the warp's row 0;
+// rows >= valid_rows are not written.
+__device__ __forceinline__ void warp_store_rows128(uint8_t *stage, const uint4 (&v)[8], int lane, char *gbase,
+                                                   size_t ld_bytes, int valid_rows)
 {
-    const bool valid = row < ti.rows;
-    if (KIND == GK_ROUTER) {
-        float *dst = static_cast<float *>(p.out) + (size_t)(ti.out_row + row) * p.ld_out + ti.nt * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4 *>(stage + lane * 128 + ((q ^ (lane & 7)) << 4)) = v[q];
+    __syncwarp();
+    const int q = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = i * 4 + (lane >> 3);
+        const uint4 val = *reinterpret_cast<const uint4 *>(stage + r * 128 + ((q ^ (r & 7)) << 4));
+        if (r < valid_rows)
+            *reinterpret_cast<uint4 *>(gbase + (size_t)r * ld_bytes + q * 16) = val;
+    }
+    __syncwarp();
+}
+
+// Epilogue of one grouped-GEMM tile for one epilogue warp (32 rows).
+template <int KIND>
+__device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
+                                              int lane, uint8_t *stage)
+{
+    const int valid_rows = ti.rows - quad * 32;
+    const size_t ld_bytes = (size_t)p.ld_out * 2;
+    if constexpr (KIND == GK_GATE_UP) {
+        // TMEM columns [0,128) = gate, [128,256) = up; 64 outputs per pass
+        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes + ti.nt * 256;
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-            uint32_t r[32];
-            tmem_load32(tacc + c, r);
-            if (valid) {
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
+        for (int c = 0; c < 128; c += 64) {
+            uint32_t g[64], u[64];
+            tmem_load64(tacc + c, g);
+            tmem_load64(tacc + 128 + c, u);
+            uint4 v[8];
+            uint32_t *pk = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    d4[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-            }
-        }
-    } else if (KIND == GK_GATE_UP) {
-        uint16_t *dst = static_cast<uint16_t *>(p.out) + (size_t)(ti.out_row + row) * p.ld_out + ti.nt * 128;
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-            uint32_t g[32], u[32];
-            tmem_load32(tacc + c, g);
-            tmem_load32(tacc + 128 + c, u);
-            if (valid) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(silu_times(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
-                                        silu_times(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
+            for (int i = 0; i < 32; ++i)
+                pk[i] = pack_bf16x2(silu_times(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
+                                    silu_times(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
+            if (valid_rows > 0)
+                warp_store_rows128(stage, v, lane, gbase + c * 2, ld_bytes, valid_rows);
         }
     } else {
-        uint16_t *dst = static_cast<uint16_t *>(p.out) + (size_t)(ti.out_row + row) * p.ld_out + ti.nt * 256;
+        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes + ti.nt * 512;
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-            uint32_t r[32];
-            tmem_load32(tacc + c, r);
-            if (valid) {
-                uint32_t pk[16];
+        for (int c = 0; c < 256; c += 64) {
+            uint32_t r[64];
+            tmem_load64(tacc + c, r);
+            uint4 v[8];
+            uint32_t *pk = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst + c);
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            }
+            for (int i = 0; i < 32; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+            if (valid_rows > 0)
+                warp_store_rows128(stage, v, lane, gbase + c * 2, ld_bytes, valid_rows);
         }
     }
+}
+
+// Router epilogue warp: adds the K-block partial sums of its 32 rows in fp32
+// (K-block order, round-to-nearest), then writes the 128 logits of each row.
+__device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem,
+                                                     int quad, int lane, uint32_t tfull0, uint32_t tempty0,
+                                                     uint32_t &kctr, volatile int *abort_flag, uint8_t *stage)
+{
+    using C = GemmCfg<GK_ROUTER>;
+    float acc[C::BN];
+#pragma unroll
+    for (int c = 0; c < C::BN; ++c)
+        acc[c] = 0.0f;
+    for (int kb = 0; kb < p.kblocks; ++kb, ++kctr) {
+        const uint32_t slot = kctr % C::SLOTS;
+        const uint32_t par = (kctr / C::SLOTS) & 1u;
+        int ok = 1;
+        if (lane == 0)
+            ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok)
+            return false;
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + slot * C::BN;
+#pragma unroll
+        for (int c = 0; c < C::BN; c += 64) {
+            uint32_t r[64];
+            tmem_load64(taddr + c, r);
+            if (c + 64 == C::BN) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty0 + 8u * slot);   // slot free again: the values are in registers
+            }
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                acc[c + i] += __uint_as_float(r[i]);
+        }
+    }
+    const int valid_rows = ti.rows - quad * 32;
+    if (valid_rows > 0) {
+        const size_t ld_bytes = (size_t)p.ld_out * 4;
+        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes + ti.nt * C::BN * 4;
+#pragma unroll
+        for (int c = 0; c < C::BN; c += 32) {
+            uint4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                v[q] = make_uint4(__float_as_uint(acc[c + 4 * q]), __float_as_uint(acc[c + 4 * q + 1]),
+                                  __float_as_uint(acc[c + 4 * q + 2]), __float_as_uint(acc[c + 4 * q + 3]));
+            warp_store_rows128(stage, v, lane, gbase + c * 4, ld_bytes, valid_rows);
+        }
+    }
+    return true;
 }
 
 template <int KIND>
@@ -236,21 +310,23 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
 {
     using C = GemmCfg<KIND>;
     using L = GemmLayout<KIND>;
+    constexpr bool ROUTER = (KIND == GK_ROUTER);
     extern __shared__ uint8_t dsmem[];
 
     const uint32_t raw = smem_u32(dsmem);
     const uint32_t base = (raw + 1023u) & ~1023u;                 // swizzle atoms need 1024-B alignment
     uint8_t *base_ptr = dsmem + (base - raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(base_ptr + C::STAGES * L::STAGE_BYTES);
+    uint8_t *staging = base_ptr + C::STAGES * L::STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + L::STAGING);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + L::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
-    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
-    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
-    const uint32_t fin_bar = bar0 + 8u * (2 * C::STAGES + 4);
+    const uint32_t tfull0 = bar0 + 8u * (2 * C::STAGES);
+    const uint32_t tempty0 = tfull0 + 8u * C::SLOTS;
+    const uint32_t fin_bar = tempty0 + 8u * C::SLOTS;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -260,9 +336,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 4);
+        for (int a = 0; a < C::SLOTS; ++a) {
+            mbar_init(tfull0 + 8u * a, 1);
+            mbar_init(tempty0 + 8u * a, 4);
         }
         mbar_init(fin_bar, 1);
         *abort_flag = 0;
@@ -279,7 +355,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    const int num_tiles = (KIND == GK_ROUTER) ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
+    const int num_tiles = ROUTER ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -318,30 +394,45 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            int local = 0;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
-                const int acc = local & 1;
-                const uint32_t acc_phase = (local >> 1) & 1;
-                if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag))
-                    break;
-                tc_fence_after();
-                const uint32_t d = tmem + acc * C::BN;
+            uint32_t ctr = 0;   // accumulators used so far (tiles, or K blocks for the router)
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                if (!ROUTER) {
+                    const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                    if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag))
+                        break;
+                    tc_fence_after();
+                }
                 for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (ROUTER) {
+                        const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                        if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
                     if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t sA = base + stage * L::STAGE_BYTES;
-                    issue_mmas<KIND>(sA, sA + C::A_BYTES, d, kb > 0);
-                    umma_commit(empty_bar(stage));   // frees the stage once these MMAs have read it
+                    const uint32_t d = tmem + (ctr % C::SLOTS) * C::BN;
+                    issue_mmas<KIND>(sA, sA + C::A_BYTES, d, ROUTER ? false : kb > 0);
+                    umma_commit(empty_bar(stage));               // frees the stage once read
+                    if (ROUTER) {
+                        umma_commit(tfull0 + 8u * (ctr % C::SLOTS));  // K-block partial ready
+                        ++ctr;
+                    }
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (ok)
-                    umma_commit(tfull_bar(acc));     // accumulator ready for the epilogue
+                if (!ROUTER && ok) {
+                    umma_commit(tfull0 + 8u * (ctr % C::SLOTS));      // tile accumulator ready
+                    ++ctr;
+                }
             }
             // no MMA may still be writing TMEM when it is freed
             umma_commit(fin_bar);
@@ -350,26 +441,31 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        int local = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-            const int acc = local & 1;
-            const uint32_t acc_phase = (local >> 1) & 1;
-            int ok = 1;
-            if (lane == 0)
-                ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok)
-                break;
-            __syncwarp();
-            tc_fence_after();
+        uint8_t *stage = staging + (warp - 2) * 4096;
+        uint32_t ctr = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<KIND>(p, tile);
-            const uint32_t tacc = tmem + ((uint32_t)(quad * 32) << 16) + acc * C::BN;
-            epilogue_tile<KIND>(p, ti, tacc, row);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(tempty_bar(acc));
+            if constexpr (ROUTER) {
+                if (!router_epilogue_tile(p, ti, tmem, quad, lane, tfull0, tempty0, ctr, abort_flag, stage))
+                    break;
+            } else {
+                const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                int ok = 1;
+                if (lane == 0)
+                    ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok)
+                    break;
+                __syncwarp();
+                tc_fence_after();
+                const uint32_t tacc = tmem + ((uint32_t)(quad * 32) << 16) + slot * C::BN;
+                epilogue_tile<KIND>(p, ti, tacc, quad, lane, stage);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(tempty0 + 8u * slot);
+                ++ctr;
+            }
         }
     }
 

@@ -9,8 +9,8 @@
 namespace glr {
 
 // ---- sizes shared by the host layer and the kernels -------------------------
-constexpr int ROUTE_CHUNK = 128;   // tokens per block of the routing kernel
-constexpr int PERM_CHUNK = 128;    // tokens per block of the bucketing kernels
+constexpr int ROUTE_CHUNK = 32;    // tokens per block of the routing kernel (4 per warp)
+constexpr int PERM_CHUNK = 64;     // tokens per block of the bucketing kernels
 constexpr int GEMM_BM = 128;       // tensor-core tile rows (tokens)
 constexpr int GEMM_BK = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
@@ -55,14 +55,16 @@ int gemm_tmem_cols(int kind);
 
 cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s);
 
-cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, cudaStream_t s);
+// W (fp32) -> hi/mid/lo bf16 parts [3][E][H]; also zeroes counts[E] when given.
+cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, int32_t *counts, cudaStream_t s);
 
+// counts[E] must be zero (or hold counts to add to) before the launch.
 cudaError_t launch_route_select(const float *logits, const float *bias, int T, int E, int n_group,
                                 int topk_group, int k, float rsf, float eps, int32_t *idx, float *w,
-                                int32_t *hist, float *ppart, int *status, cudaStream_t s);
+                                int32_t *counts, float *ppart, int *status, cudaStream_t s);
 
-cudaError_t launch_route_finalize(const int32_t *hist, const float *ppart, int nchunk, int T, int E, int k,
-                                  int32_t *counts, float *aux_P, float *aux_loss, cudaStream_t s);
+cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int nchunk, int T, int E, int k,
+                                  float *aux_P, float *aux_loss, cudaStream_t s);
 
 cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status,
                                cudaStream_t s);

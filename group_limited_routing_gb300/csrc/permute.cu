@@ -64,14 +64,18 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t *__restrict__
     __shared__ int total[257];
     __shared__ int offset[258];
     __shared__ int tstart[258];
+    __shared__ int wsum_rows[8];
+    __shared__ int wsum_tiles[8];
     const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
     const int per = (nchunk + 3) / 4;
     const int c0 = min(nchunk, q * per), c1 = min(nchunk, c0 + per);
 
     int sum = 0;
-    if (e < E)
+    if (e < E) {
+#pragma unroll 8
         for (int c = c0; c < c1; ++c)
             sum += hist[(size_t)c * E + e];
+    }
     part[q][e] = sum;
     __syncthreads();
     if (q == 0) {
@@ -80,14 +84,46 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t *__restrict__
             total[256] = 0;
     }
     __syncthreads();
+    // bucket offsets and first m-tile of every group: exclusive scans over the
+    // E routed groups by the first 8 warps (the shared group E comes last)
+    if (threadIdx.x < 256) {
+        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+        const int n = (e < E) ? total[e] : 0;
+        const int nt = (n + GEMM_BM - 1) / GEMM_BM;
+        int a = n, b = nt;                      // inclusive warp scans
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, a, off);
+            const int yb = __shfl_up_sync(0xffffffffu, b, off);
+            if (lane >= off) {
+                a += ya;
+                b += yb;
+            }
+        }
+        if (lane == 31) {
+            wsum_rows[w] = a;
+            wsum_tiles[w] = b;
+        }
+        __syncwarp();
+        offset[e] = a - n;                      // warp-local exclusive, fixed below
+        tstart[e] = b - nt;
+    }
+    __syncthreads();
+    if (threadIdx.x < 256) {
+        int ra = 0, rb = 0;
+        for (int w = 0; w < (threadIdx.x >> 5); ++w) {
+            ra += wsum_rows[w];
+            rb += wsum_tiles[w];
+        }
+        offset[e] += ra;
+        tstart[e] += rb;
+    }
+    __syncthreads();
     if (threadIdx.x == 0) {
-        // bucket offsets and first m-tile of every group (E routed + shared)
         int off = 0, tiles = 0;
-        for (int g = 0; g < E; ++g) {
-            offset[g] = off;
-            tstart[g] = tiles;
-            off += total[g];
-            tiles += (total[g] + GEMM_BM - 1) / GEMM_BM;
+        for (int w = 0; w < 8; ++w) {
+            off += wsum_rows[w];
+            tiles += wsum_tiles[w];
         }
         offset[E] = off;             // == K*T unless indices were out of range
         tstart[E] = tiles;
@@ -102,6 +138,7 @@ __global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t *__restrict__
         int run = offset[e];
         for (int qq = 0; qq < q; ++qq)
             run += part[qq][e];
+#pragma unroll 8
         for (int c = c0; c < c1; ++c) {
             const int h = hist[(size_t)c * E + e];
             hist[(size_t)c * E + e] = run;
@@ -211,83 +248,106 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
 }
 
 // ---------------------------------------------------------------------------
-// out[t] = bf16( sum_j w[t,j] * Y[slot_of[t,j]] + Y[K*T + t] (+ residual[t]) ),
-// fp32 accumulation in j order.  A thread owns 8 consecutive columns (one
-// 16-byte vector) of a token; a 256-thread block covers 2048 columns.
+// out[t] = bf16( Y[K*T + t] + sum_j w[t,j] * Y[slot_of[t,j]] (+ residual[t]) ),
+// fp32 accumulation in j order.  A block takes COMBINE_TOK tokens at a time:
+// their slots and weights are loaded once into shared memory, then a thread
+// owns one 16-byte column vector (8 values) of a token and issues all of its
+// row loads before the first use.
+constexpr int COMBINE_TOK = 32;
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v, float wgt)
+{
+    const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(p2[q]);
+        acc[2 * q] += wgt * f.x;
+        acc[2 * q + 1] += wgt * f.y;
+    }
+}
+
+// One token's 16-byte column vector: the K expert rows (in batches of eight,
+// every load of a batch issued before any use) and the shared row.
+__device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, const int *s_slot, const float *s_w,
+                                            const uint16_t *__restrict__ residual, int T, int H, int K, int t,
+                                            int tl, int vv, uint16_t *__restrict__ out)
+{
+    float acc[8], racc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        acc[q] = 0.0f;
+        racc[q] = 0.0f;
+    }
+    const uint4 sv = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + t) * H)[vv];
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int j0 = 0; j0 < K; j0 += 8) {
+        uint4 yv[8];
+        float wv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int j = j0 + u;
+            const int slot = (j < K) ? s_slot[tl * K + j] : -1;
+            wv[u] = (slot >= 0) ? s_w[tl * K + j] : 0.0f;
+            yv[u] = (slot >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)slot * H)[vv] : zero;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            add_bf16x8(racc, yv[u], wv[u]);      // skipped pairs hold weight 0 and a zero row
+    }
+    add_bf16x8(acc, sv, 1.0f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        acc[q] += racc[q];
+    if (residual)
+        add_bf16x8(acc, reinterpret_cast<const uint4 *>(residual + (size_t)t * H)[vv], 1.0f);
+    uint4 o;
+    uint32_t *op = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+        op[q] = *reinterpret_cast<uint32_t *>(&b);
+    }
+    reinterpret_cast<uint4 *>(out + (size_t)t * H)[vv] = o;
+}
+
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ Y,
                                                       const int32_t *__restrict__ slot_of,
                                                       const float *__restrict__ w,
                                                       const uint16_t *__restrict__ residual, int T, int H, int K,
                                                       uint16_t *__restrict__ out)
 {
-    const int vec_per_row = H / 8;
-    const long long total = (long long)T * vec_per_row;
-    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int t = (int)(i / vec_per_row);
-        const int v = (int)(i % vec_per_row);
-        float acc[8];
-        {
-            const uint4 sv = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + t) * H)[v];
-            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&sv);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 f = __bfloat1622float2(p2[q]);
-                acc[2 * q] = f.x;
-                acc[2 * q + 1] = f.y;
-            }
+    __shared__ int s_slot[COMBINE_TOK * 32];
+    __shared__ float s_w[COMBINE_TOK * 32];
+    const int vpr = H / 8;                                   // 16-byte vectors per row
+    const int rpp = max(1, (int)blockDim.x / vpr);           // tokens per pass
+    const int sub = threadIdx.x / vpr, v = threadIdx.x % vpr;
+    const int nchunks = (T + COMBINE_TOK - 1) / COMBINE_TOK;
+    for (int chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+        const int t0 = chunk * COMBINE_TOK;
+        const int nt = min(COMBINE_TOK, T - t0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * K; i += blockDim.x) {
+            s_slot[i] = slot_of[(size_t)t0 * K + i];
+            s_w[i] = w[(size_t)t0 * K + i];
         }
-        float racc[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            racc[q] = 0.0f;
-        for (int j = 0; j < K; ++j) {
-            const int slot = slot_of[(size_t)t * K + j];
-            if (slot < 0)
-                continue;
-            const float wj = w[(size_t)t * K + j];
-            const uint4 yv = reinterpret_cast<const uint4 *>(Y + (size_t)slot * H)[v];
-            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&yv);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 f = __bfloat1622float2(p2[q]);
-                racc[2 * q] += wj * f.x;
-                racc[2 * q + 1] += wj * f.y;
-            }
+        __syncthreads();
+        if (sub >= rpp)
+            continue;
+        for (int vv = v; vv < vpr; vv += blockDim.x) {
+            for (int tl = sub; tl < nt; tl += rpp)
+                combine_one(Y, s_slot, s_w, residual, T, H, K, t0 + tl, tl, vv, out);
         }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            acc[q] += racc[q];
-        if (residual) {
-            const uint4 rv = reinterpret_cast<const uint4 *>(residual + (size_t)t * H)[v];
-            const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&rv);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float2 f = __bfloat1622float2(p2[q]);
-                acc[2 * q] += f.x;
-                acc[2 * q + 1] += f.y;
-            }
-        }
-        uint4 o;
-        uint32_t *op = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-            op[q] = *reinterpret_cast<uint32_t *>(&b);
-        }
-        reinterpret_cast<uint4 *>(out + (size_t)t * H)[v] = o;
     }
 }
 
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s)
 {
-    const long long total = (long long)T * (H / 8);
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long want = (total + 255) / 256;
-    const int blocks = (int)min(want, (long long)sms * 8);
+    const int nchunks = (T + COMBINE_TOK - 1) / COMBINE_TOK;
+    const int blocks = min(nchunks, sms * 8);
     combine_kernel<<<blocks, 256, 0, s>>>(Y, slot_of, w, residual, T, H, k, out);
     return cudaPeekAtLastError();
 }

@@ -26,8 +26,14 @@ namespace glr {
 // W (fp32) -> hi, mid, lo (bf16) with hi + mid + lo == W exactly for normal
 // values: each part is the bf16 rounding of what the previous parts left.
 // Layout of W3: [3][E][H].
-__global__ void split_router_kernel(const float *__restrict__ W, uint16_t *__restrict__ W3, int n)
+// The same launch also clears `counts` (E entries) for the routing kernel
+// that follows it on the stream.
+__global__ void split_router_kernel(const float *__restrict__ W, uint16_t *__restrict__ W3, int n,
+                                    int32_t *__restrict__ counts, int E)
 {
+    if (blockIdx.x == 0)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            counts[e] = 0;
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const float w = W[i];
         const __nv_bfloat16 hi = __float2bfloat16_rn(w);
@@ -41,34 +47,47 @@ __global__ void split_router_kernel(const float *__restrict__ W, uint16_t *__res
     }
 }
 
-cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, cudaStream_t s)
+cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, int32_t *counts, cudaStream_t s)
 {
     const int n = E * H;
     const int blocks = min((n + 255) / 256, 4096);
-    split_router_kernel<<<blocks, 256, 0, s>>>(W, W3, n);
+    split_router_kernel<<<blocks, 256, 0, s>>>(W, W3, n, counts, counts ? E : 0);
     return cudaPeekAtLastError();
 }
 
 // ---------------------------------------------------------------------------
-// (value desc, index asc) ordering with an explicit "no candidate" state
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib)
+// Order-preserving map of fp32 onto uint32 (for non-NaN values): a > b as
+// floats exactly when key(a) > key(b), so warp-wide float max is one
+// __reduce_max_sync.  +0 and -0 get neighbouring keys; the scores compared
+// here (sigmoid + bias, and sums of two of them) are never -0.
+__device__ __forceinline__ uint32_t fkey(float f)
 {
-    return ib < 0 || (ia >= 0 && (va > vb || (va == vb && ia < ib)));
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float fkey_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // One warp per token.  Lane l holds experts 32*j + l for j < n_group, so each
 // group lives in one register index across the 32 lanes, and every load of a
-// logits row is a run of 128-byte coalesced accesses.
+// logits row is a run of 128-byte coalesced accesses.  Group maxima and the
+// top-k arg-max rounds are warp reductions (redux) on the keys above.
 //
-// Block: 8 warps, ROUTE_CHUNK tokens; writes its per-expert hit histogram and
-// (optionally) per-expert sums of the token-normalised scores for the chunk.
+// Block: 8 warps, ROUTE_CHUNK tokens.  Hits per expert go to a shared-memory
+// histogram and then to `counts` with integer atomics (exact, order-free).
+// With `ppart`, the block also writes per-expert sums of the token-normalised
+// scores of its chunk for the balance loss.
 template <int G>
 __global__ void __launch_bounds__(256) route_select_kernel(
     const float *__restrict__ logits, const float *__restrict__ bias, int T, int TG, int K, float rsf, float eps,
-    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ hist, float *__restrict__ ppart,
-    int *__restrict__ status)
+    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
+    float *__restrict__ ppart, int *__restrict__ status)
 {
     constexpr int E = 32 * G;
+    constexpr unsigned FULL = 0xffffffffu;
     __shared__ int sh_hist[E];
     __shared__ float sh_p[8][E];
 
@@ -104,16 +123,11 @@ __global__ void __launch_bounds__(256) route_select_kernel(
         float g[G];
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            float m1 = b[j], m2 = -INFINITY;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float o1 = __shfl_xor_sync(0xffffffffu, m1, off);
-                const float o2 = __shfl_xor_sync(0xffffffffu, m2, off);
-                const float hi = fmaxf(m1, o1), lo = fminf(m1, o1);
-                m2 = fmaxf(lo, fmaxf(m2, o2));
-                m1 = hi;
-            }
-            g[j] = m1 + m2;
+            const uint32_t u = fkey(b[j]);
+            const uint32_t m1 = __reduce_max_sync(FULL, u);
+            const int first = __ffs(__ballot_sync(FULL, u == m1)) - 1;
+            const uint32_t m2 = __reduce_max_sync(FULL, lane == first ? 0u : u);   // best of the others
+            g[j] = fkey_value(m1) + fkey_value(m2);
         }
 
         // keep the TG best groups (ties to the lower group index)
@@ -127,42 +141,36 @@ __global__ void __launch_bounds__(256) route_select_kernel(
             keep |= (rank < TG ? 1u : 0u) << j;
         }
 
-        // top-K of the surviving experts, K rounds of warp arg-max
-        uint32_t taken = 0;
+        // top-K of the surviving experts: K rounds of (max key, then lowest index)
+        uint32_t avail = keep;   // this lane's candidates not yet taken, by group
         float den = 0.0f;
         int my_e = -1;
         float my_s = 0.0f;
         for (int r = 0; r < K; ++r) {
-            float bv = -INFINITY;
-            int be = -1;
+            uint32_t bk = 0;
+            int bj = -1;
 #pragma unroll
-            for (int j = 0; j < G; ++j)
-                if (((keep >> j) & 1u) && !((taken >> j) & 1u) && better(b[j], 32 * j + lane, bv, be)) {
-                    bv = b[j];
-                    be = 32 * j + lane;
-                }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (better(ov, oe, bv, be)) {
-                    bv = ov;
-                    be = oe;
+            for (int j = 0; j < G; ++j) {
+                const uint32_t kj = fkey(b[j]);
+                if (((avail >> j) & 1u) && (bj < 0 || kj > bk)) {   // ascending j: ties keep the lower index
+                    bk = kj;
+                    bj = j;
                 }
             }
-            // every lane now holds the same winner be (>= 0: 32*TG >= K survivors)
-            const int wj = be >> 5, wl = be & 31;
-            float sw = 0.0f;
+            const uint32_t wk = __reduce_max_sync(FULL, bj >= 0 ? bk : 0u);
+            const uint32_t we = __reduce_min_sync(FULL, (bj >= 0 && bk == wk) ? (uint32_t)(32 * bj + lane) : 0xffffffffu);
+            const int wl = (int)(we & 31u), wj = (int)(we >> 5);
+            float sl = 0.0f;
 #pragma unroll
             for (int j = 0; j < G; ++j)
-                if (j == wj)
-                    sw = s[j];
-            sw = __shfl_sync(0xffffffffu, sw, wl);
+                if (j == bj)
+                    sl = s[j];
+            const float sw = __shfl_sync(FULL, sl, wl);   // the winner's unbiased score
             if (lane == wl)
-                taken |= 1u << wj;
-            den += sw;                                // sequential, in output order
+                avail &= ~(1u << wj);
+            den += sw;                                    // sequential, in output order
             if (lane == r) {
-                my_e = be;
+                my_e = (int)we;
                 my_s = sw;
             }
         }
@@ -170,7 +178,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(
         if (lane < K) {
             idx_out[(size_t)t * K + lane] = my_e;
             w_out[(size_t)t * K + lane] = (my_s / den) * rsf;   // section 二 step 3
-            atomicAdd(&sh_hist[my_e], 1);                       // integer: order-free
+            atomicAdd(&sh_hist[my_e], 1);
         }
 
         if (ppart) {
@@ -180,14 +188,14 @@ __global__ void __launch_bounds__(256) route_select_kernel(
                 tot += s[j];
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
-                tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                tot += __shfl_xor_sync(FULL, tot, off);
             const float inv = 1.0f / tot;
 #pragma unroll
             for (int j = 0; j < G; ++j)
                 pacc[j] += s[j] * inv;
         }
     }
-    if (__any_sync(0xffffffffu, nonfinite) && lane == 0)
+    if (__any_sync(FULL, nonfinite) && lane == 0)
         atomicOr(status, ST_NONFINITE);
 
     if (ppart) {
@@ -197,7 +205,8 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        hist[(size_t)blockIdx.x * E + e] = sh_hist[e];
+        if (sh_hist[e])
+            atomicAdd(&counts[e], sh_hist[e]);      // integer sums: the result is order-free
         if (ppart) {
             float v = 0.0f;
             for (int q = 0; q < 8; ++q)
@@ -208,14 +217,14 @@ __global__ void __launch_bounds__(256) route_select_kernel(
 }
 
 cudaError_t launch_route_select(const float *logits, const float *bias, int T, int E, int n_group, int topk_group,
-                                int k, float rsf, float eps, int32_t *idx, float *w, int32_t *hist, float *ppart,
+                                int k, float rsf, float eps, int32_t *idx, float *w, int32_t *counts, float *ppart,
                                 int *status, cudaStream_t s)
 {
     const int blocks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
 #define GLR_ROUTE_CASE(GG)                                                                                  \
     case GG:                                                                                                \
         route_select_kernel<GG><<<blocks, 256, 0, s>>>(logits, bias, T, topk_group, k, rsf, eps, idx, w,   \
-                                                       hist, ppart, status);                                \
+                                                       counts, ppart, status);                              \
         break;
     switch (n_group) {
         GLR_ROUTE_CASE(1)
@@ -234,55 +243,68 @@ cudaError_t launch_route_select(const float *logits, const float *bias, int T, i
 }
 
 // ---------------------------------------------------------------------------
-// counts[e] = sum over chunks of hist[c][e]; P[e] = sum of ppart[c][e] / T;
-// aux = E * sum_e counts[e] / (k T) * P[e].  One block of 1024 threads: four
-// threads per expert each take a fixed quarter of the chunks; all sums run
-// in a fixed order, so the result is reproducible bit for bit.
-__global__ void __launch_bounds__(1024) route_finalize_kernel(const int32_t *__restrict__ hist,
-                                                              const float *__restrict__ ppart, int nchunk, int T,
-                                                              int E, int K, int32_t *__restrict__ counts,
-                                                              float *__restrict__ aux_P, float *__restrict__ aux_loss)
+// Balance loss (only when asked for): P[e] = sum over chunks of ppart[c][e] / T
+// and aux = E * sum_e counts[e] / (k T) * P[e].  One block of 512 threads:
+// warp w reads chunk rows w, w + 16, ... (lane l takes experts l, l + 32, ...,
+// so every load is a coalesced 128-byte run); the 16 warp partials are then
+// added in warp order.  Every sum runs in a fixed order, so the result is
+// reproducible bit for bit.
+constexpr int FIN_WARPS = 16;
+
+__global__ void __launch_bounds__(FIN_WARPS * 32) route_finalize_kernel(const int32_t *__restrict__ counts,
+                                                                         const float *__restrict__ ppart, int nchunk,
+                                                                         int T, int E, int K, float *__restrict__ aux_P,
+                                                                         float *__restrict__ aux_loss)
 {
-    __shared__ long long sc[4][256];
-    __shared__ double sp[4][256];
-    __shared__ double red[1024];
-    const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
-    long long c = 0;
-    double pv = 0.0;
-    if (e < E) {
-        for (int ch = q; ch < nchunk; ch += 4) {
-            c += hist[(size_t)ch * E + e];
-            if (ppart)
-                pv += (double)ppart[(size_t)ch * E + e];
-        }
+    __shared__ float sp[FIN_WARPS][MAX_GROUPS * 32];
+    __shared__ double red[FIN_WARPS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = E / 32;
+    float pv[MAX_GROUPS];
+#pragma unroll
+    for (int j = 0; j < MAX_GROUPS; ++j)
+        pv[j] = 0.0f;
+#pragma unroll 4
+    for (int ch = warp; ch < nchunk; ch += FIN_WARPS) {
+#pragma unroll
+        for (int j = 0; j < MAX_GROUPS; ++j)
+            if (j < G)
+                pv[j] += ppart[(size_t)ch * E + 32 * j + lane];
     }
-    sc[q][e] = c;
-    sp[q][e] = pv;
+#pragma unroll
+    for (int j = 0; j < MAX_GROUPS; ++j)
+        if (j < G)
+            sp[warp][32 * j + lane] = pv[j];
     __syncthreads();
     double contrib = 0.0;
-    if (q == 0 && e < E) {
-        const long long tot = sc[0][e] + sc[1][e] + sc[2][e] + sc[3][e];
-        counts[e] = (int32_t)tot;
-        const double P = (sp[0][e] + sp[1][e] + sp[2][e] + sp[3][e]) / (double)T;
+    const int e = threadIdx.x;
+    if (e < E) {
+        double psum = 0.0;
+        for (int w = 0; w < FIN_WARPS; ++w)
+            psum += (double)sp[w][e];
+        const double P = psum / (double)T;
         if (aux_P)
             aux_P[e] = (float)P;
-        contrib = (double)tot / ((double)K * (double)T) * P;
+        contrib = (double)counts[e] / ((double)K * (double)T) * P;
     }
-    red[threadIdx.x] = contrib;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        contrib += __shfl_xor_sync(0xffffffffu, contrib, off);
+    if (lane == 0)
+        red[warp] = contrib;
     __syncthreads();
-    for (int off = 512; off > 0; off >>= 1) {
-        if (threadIdx.x < off)
-            red[threadIdx.x] += red[threadIdx.x + off];
-        __syncthreads();
+    if (threadIdx.x == 0 && aux_loss) {
+        double a = 0.0;
+        for (int w = 0; w < FIN_WARPS; ++w)
+            a += red[w];
+        *aux_loss = (float)((double)E * a);
     }
-    if (threadIdx.x == 0 && aux_loss)
-        *aux_loss = (float)((double)E * red[0]);
 }
 
-cudaError_t launch_route_finalize(const int32_t *hist, const float *ppart, int nchunk, int T, int E, int k,
-                                  int32_t *counts, float *aux_P, float *aux_loss, cudaStream_t s)
+cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int nchunk, int T, int E, int k,
+                                  float *aux_P, float *aux_loss, cudaStream_t s)
 {
-    route_finalize_kernel<<<1, 1024, 0, s>>>(hist, ppart, nchunk, T, E, k, counts, aux_P, aux_loss);
+    route_finalize_kernel<<<1, FIN_WARPS * 32, 0, s>>>(counts, ppart, nchunk, T, E, k, aux_P, aux_loss);
     return cudaPeekAtLastError();
 }
 

@@ -124,4 +124,6 @@ def test_route_launch_count():
     cfg = moe.MoeConfig(T=256)
     d = wl.layer_inputs(wl.WORKLOADS[3].with_T(256), DEV, with_experts=False)
     moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
-    assert moe.last_launch_count() == 4   # W split, router GEMM, select, finalize
+    assert moe.last_launch_count() == 3   # W split, router GEMM, select
+    moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=True)
+    assert moe.last_launch_count() == 4   # + the balance-loss reduction
