@@ -555,4 +555,72 @@ const char *moe_strerror(int code)
     }
 }
 
+// ------------------------------------------------------ moe_route_static
+// The scratch of moe_route_static: one array per device, zero at module load.
+static __device__ __align__(256) unsigned char g_route_static_scratch[MOE_ROUTE_STATIC_SCRATCH_BYTES];
+
+static std::mutex g_static_mu;
+static void *g_static_addr[64];   // device address of the array, per device
+
+// Device address of the array on the current device, looked up once per
+// device with that device current (host code only ever sees a stand-in for
+// the symbol, so it must never hand `g_route_static_scratch` to a kernel).
+static int static_scratch(void **addr)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64)
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> g(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_route_static_scratch) != cudaSuccess || !p)
+            return MOE_ERR_CUDA;
+        g_static_addr[dev] = p;
+    }
+    *addr = g_static_addr[dev];
+    return MOE_OK;
+}
+
+int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const float *expert_bias,
+                     int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss,
+                     int32_t *status_out, void *stream)
+{
+    int rc = check_route_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !W_router || !topk_idx || !topk_w || !expert_counts)
+        return MOE_ERR_INVALID_ARG;
+    const RouteLayout L = route_layout(*cfg);
+    if (L.total > (size_t)MOE_ROUTE_STATIC_SCRATCH_BYTES)
+        return MOE_ERR_UNSUPPORTED_SHAPE;   // needs more scratch than the fixed array holds
+    if (!aligned(hidden, 16) || !aligned(W_router, 4) || !aligned(expert_bias, 4) || !aligned(topk_idx, 4) ||
+        !aligned(topk_w, 4) || !aligned(expert_counts, 4) || !aligned(aux_P, 4) || !aligned(aux_loss, 4) ||
+        !aligned(status_out, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    void *ws = nullptr;
+    if ((rc = static_scratch(&ws)) != MOE_OK)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // the array keeps the previous call's contents: the status word must start at zero
+    if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    int launches = 0;
+    float *logits = at<float>(ws, L.logits);
+    rc = router_gemm(*cfg, hidden, W_router, logits, expert_counts, ws, L, sms, s, launches);
+    if (rc == MOE_OK)
+        rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
+                          launches);
+    if (rc == MOE_OK && status_out &&
+        cudaMemcpyAsync(status_out, &header(ws)->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
+            cudaSuccess)
+        rc = MOE_ERR_CUDA;
+    g_last_launches = launches;
+    return rc;
+}
+
 }  // extern "C"

@@ -160,6 +160,34 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
                 const int32_t *topk_idx, const float *topk_w, const moe_bf16 *residual,
                 moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
 
+/* Router without caller-provided scratch (no counterpart on the pages: it is
+ * an interface convenience, not part of the method).  Same computation,
+ * outputs and determinism as moe_route, but the scratch that moe_route keeps
+ * in its workspace (the split router weight, the logits, the balance-loss
+ * partials) lives in one array inside this library, so the caller supplies
+ * only inputs and outputs.  It is meant for callers that must not allocate
+ * device memory on the call path: code that runs while a CUDA graph is being
+ * captured, plug-in hosts whose operator interface hands over tensors but no
+ * allocator, and latency-sensitive loops where a cudaMalloc would synchronise
+ * the device.  This entry point itself never calls cudaMalloc or cudaFree.
+ *
+ * The array is a static __device__ buffer of MOE_ROUTE_STATIC_SCRATCH_BYTES
+ * (40 MiB), held on every GPU that loads the library until the process exits.
+ * That covers T up to 32768 tokens at E = 256, H = 2048 (more for smaller E
+ * or H); larger configurations are rejected with MOE_ERR_UNSUPPORTED_SHAPE
+ * before anything is launched.  The first call on a device looks up the
+ * array's device address (with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array:
+ * calls whose work overlaps on the GPU (other streams, other threads) race
+ * and must be serialised by the caller.  Each call clears the status word it
+ * uses; status_out (a DEVICE pointer, or NULL) receives that call's
+ * MOE_STATUS_* bits in stream order. */
+#define MOE_ROUTE_STATIC_SCRATCH_BYTES (40u << 20)
+int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
+                     const float *expert_bias, int32_t *topk_idx, float *topk_w,
+                     int32_t *expert_counts, float *aux_P, float *aux_loss,
+                     int32_t *status_out, void *stream);
+
 /* Waits for `stream`, then copies the workspace's status word (MOE_STATUS_*
  * bits, OR-ed over every call since the last reset) to *status (a HOST
  * pointer); clears it when reset != 0.  Returns MOE_OK, or MOE_ERR_CUDA. */

@@ -1,0 +1,65 @@
+"""moe_route_static: the router entry point that takes no workspace.
+
+Some callers cannot allocate device memory where they call the router: code
+running inside a CUDA graph capture, plug-in hosts that hand an operator its
+tensors but no allocator, or tight loops where a cudaMalloc would stall the
+device.  moe_route_static keeps the router's scratch in an array inside the
+library instead.  These checks call it through the C ABI and compare it with
+moe_route (which uses a caller workspace) on two calls in a row: the same
+kernels run on the same inputs, so indices, counts, weights and the balance
+loss must agree bit for bit.
+
+This file is collected last on purpose, so that a failure here comes after
+every other test has run.
+"""
+import ctypes
+
+import pytest
+import torch
+
+from group_limited_routing_gb300 import _lib, moe, workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _static_route(cfg, x, W, bias):
+    lib = _lib.load()
+    idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=DEV)
+    w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=DEV)
+    counts = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
+    P = torch.empty(cfg.E, dtype=torch.float32, device=DEV)
+    loss = torch.empty(1, dtype=torch.float32, device=DEV)
+    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = lib.moe_route_static(ctypes.byref(cfg.c()), x.data_ptr(), W.data_ptr(), bias.data_ptr(), idx.data_ptr(),
+                              w.data_ptr(), counts.data_ptr(), P.data_ptr(), loss.data_ptr(), status.data_ptr(),
+                              stream)
+    assert rc == _lib.MOE_OK, _lib.strerror(rc)
+    torch.cuda.synchronize()
+    return idx, w, counts, P, loss, int(status.item())
+
+
+@pytest.mark.parametrize("wid,T", [(4, 32768), (1, 128)])
+def test_static_route_matches_workspace_route_twice(wid, T):
+    w0 = wl.WORKLOADS[wid].with_T(T)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
+    ref = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=True)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        idx, w, counts, P, loss, status = _static_route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+        assert status == 0
+        assert torch.equal(idx, ref[0])
+        assert torch.equal(counts, ref[2])
+        assert torch.equal(w, ref[1])
+        assert torch.equal(P, ref[3])
+        assert torch.equal(loss, ref[4])
+
+
+def test_static_route_rejects_configurations_beyond_its_array():
+    lib = _lib.load()
+    cfg = moe.MoeConfig(T=65536)            # needs about 70 MiB of scratch
+    A = 1 << 20                             # never dereferenced: refused on the host
+    rc = lib.moe_route_static(ctypes.byref(cfg.c()), A, A, None, A, A, A, None, None, None, None)
+    assert rc == _lib.MOE_ERR_UNSUPPORTED_SHAPE
