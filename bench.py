@@ -46,6 +46,27 @@ def peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+def gemm_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the GEMM sources have changed since that capture."""
+    import hashlib
+    csrc = os.path.join(ROOT, "group_limited_routing_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "kernels.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    try:
+        with open(os.path.join(ROOT, "profiles", "gemm_dram_traffic_T32768.md")) as fh:
+            text = fh.read()
+    except OSError:
+        return None
+    tags = dict(line.split(": ", 1) for line in text.splitlines() if line.startswith(("gemm-source", "traffic-")))
+    if tags.get("gemm-source-sha256-16") != h.hexdigest()[:16]:
+        return None
+    v = tags.get("traffic-" + kernel)
+    return int(v) if v else None
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """nvidia-smi samples every 200 ms while the timed region runs."""
@@ -336,7 +357,9 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
                    "l2": "inputs larger than L2 (1.61 GB expert weights + 134 MB hidden per step), no flush"},
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": "tensor", "achieved": round(g1_tf, 1),
                      "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": round(g1_tf / pk["bf16_sustained"], 4), "traffic": None,
+                     "frac": round(g1_tf / pk["bf16_sustained"], 4),
+                     "traffic": gemm_traffic("gemm_gate_up_swiglu") if T == 32768 else None,
+                     "traffic_unit": "bytes per launch (ncu dram read + write, profiles/gemm_dram_traffic_T32768.md)",
                      "peak_kind": "%s bf16 dense, sustained" % pk["source"],
                      "algorithmic_flops_per_launch": g1["flops"]},
         "stages": stages,

@@ -39,6 +39,7 @@ struct ProfRecord {
 };
 
 std::atomic<int> g_prof_on{0};
+std::atomic<int> g_inject_timeouts{0};   // test-only: gate/up GEMM launches left to sabotage
 std::mutex g_prof_mu;
 std::vector<ProfRecord> g_prof_pending;
 std::vector<cudaEvent_t> g_event_pool;
@@ -451,6 +452,10 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     p1.kT = (int)kT;
     p1.ld_out = c.I;
     p1.status = &hdr->status;
+    if (g_inject_timeouts.load() > 0 && g_inject_timeouts.fetch_sub(1) > 0) {
+        p1.inject_withhold = 1;
+        p1.wait_limit_ns = 50000000ull;
+    }
     GLR_LAUNCH(KID_GEMM_GATE_UP, launch_gemm(GK_GATE_UP, p1, std::min(sms, L.max_mtiles * p1.n_tiles), s));
 
     // grouped down GEMM (W_down stacked [E, I, H]: an MN-major B operand)
@@ -480,6 +485,21 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     return MOE_OK;
 }
 
+int moe_rmsnorm(int32_t T, int32_t H, const moe_bf16 *x, moe_bf16 *out, float eps, void *stream)
+{
+    if (T < 1 || H < 8 || H % 8 != 0 || !x || !out || !isfinite(eps) || eps < 0.0f)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(out, 16))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0, rc = device_check(&sms);
+    if (rc != MOE_OK)
+        return rc;
+    if (launch_rmsnorm(x, out, T, H, eps, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    g_last_launches = 1;
+    return MOE_OK;
+}
+
 int moe_get_status(void *ws, size_t ws_bytes, void *stream, int32_t *status, int reset)
 {
     int rc = check_ws(ws, ws_bytes, sizeof(WsHeader));
@@ -500,6 +520,14 @@ int moe_get_status(void *ws, size_t ws_bytes, void *stream, int32_t *status, int
 }
 
 int moe_last_launch_count(void) { return g_last_launches; }
+
+int moe_debug_inject_timeout(int launches)
+{
+    if (launches < 0)
+        return MOE_ERR_INVALID_ARG;
+    g_inject_timeouts.store(launches);
+    return MOE_OK;
+}
 
 int moe_profile_enable(int on)
 {

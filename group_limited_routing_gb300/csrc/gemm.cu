@@ -254,7 +254,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
 // (K-block order, round-to-nearest), then writes the 128 logits of each row.
 __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem,
                                                      int quad, int lane, uint32_t tfull0, uint32_t tempty0,
-                                                     uint32_t &kctr, volatile int *abort_flag, uint8_t *stage)
+                                                     uint32_t &kctr, volatile int *abort_flag, uint8_t *stage,
+                                                     unsigned long long limit)
 {
     using C = GemmCfg<GK_ROUTER>;
     float acc[C::BN];
@@ -266,7 +267,7 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
         const uint32_t par = (kctr / C::SLOTS) & 1u;
         int ok = 1;
         if (lane == 0)
-            ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag) ? 1 : 0;
+            ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag, limit) ? 1 : 0;
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok)
             return false;
@@ -356,6 +357,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     const uint32_t tmem = *tmem_holder;
 
     const int num_tiles = ROUTER ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
+    const unsigned long long limit = p.wait_limit_ns ? p.wait_limit_ns : WAIT_LIMIT_NS;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -363,10 +365,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int tile = blockIdx.x; ok && !p.inject_withhold && tile < num_tiles; tile += gridDim.x) {
                 const TileInfo ti = tile_info<KIND>(p, tile);
                 for (int kb = 0; kb < p.kblocks; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag)) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, limit)) {
                         ok = false;
                         break;
                     }
@@ -398,20 +400,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 if (!ROUTER) {
                     const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
-                    if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag))
+                    if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit))
                         break;
                     tc_fence_after();
                 }
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     if (ROUTER) {
                         const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
-                        if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag)) {
+                        if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                     }
-                    if (!mbar_wait(full_bar(stage), phase, abort_flag)) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, limit)) {
                         ok = false;
                         break;
                     }
@@ -446,13 +448,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<KIND>(p, tile);
             if constexpr (ROUTER) {
-                if (!router_epilogue_tile(p, ti, tmem, quad, lane, tfull0, tempty0, ctr, abort_flag, stage))
+                if (!router_epilogue_tile(p, ti, tmem, quad, lane, tfull0, tempty0, ctr, abort_flag, stage, limit))
                     break;
             } else {
                 const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
                 int ok = 1;
                 if (lane == 0)
-                    ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag) ? 1 : 0;
+                    ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag, limit) ? 1 : 0;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok)
                     break;

@@ -47,6 +47,10 @@ struct GemmParams {
     int T, E, I, H, kT;
     int ld_out;           // output row stride in elements
     int *status;
+    // fault injection for tests: when set, the producer issues no loads, so
+    // the first wait of the MMA lane runs out after wait_limit_ns
+    int inject_withhold;
+    unsigned long long wait_limit_ns;
 };
 
 // Smem bytes a GEMM kind needs (stages + alignment slack + barriers).
@@ -77,5 +81,7 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
 
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s);
+
+cudaError_t launch_rmsnorm(const uint16_t *x, uint16_t *out, int T, int H, float eps, cudaStream_t s);
 
 }  // namespace glr

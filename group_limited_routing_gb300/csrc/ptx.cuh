@@ -59,9 +59,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Waits for the phase of `parity` to complete.  Gives up (returns false) when
-// *abort is set by another role, or after WAIT_LIMIT_NS, in which case it sets
+// *abort is set by another role, or after limit_ns, in which case it sets
 // *abort itself so that every role of the CTA winds down.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          unsigned long long limit_ns = WAIT_LIMIT_NS)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -72,7 +73,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
         if ((it & 63u) == 0) {
             if (*abort)
                 return false;
-            if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+            if (globaltimer_ns() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }

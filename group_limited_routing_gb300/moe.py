@@ -186,6 +186,17 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
     return out
 
 
+def rmsnorm(x, eps: float = 1e-6, out=None):
+    """moe_rmsnorm: bf16(x / sqrt(mean(x^2) + eps)) per row (decoder pre-norm)."""
+    T, H = x.shape
+    _need(x, "x", torch.bfloat16, (T, H), x.device)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, (T, H), x.device)
+    _lib.check(_lib.load().moe_rmsnorm(T, H, x.data_ptr(), out.data_ptr(), eps, _stream(x.device)), "moe_rmsnorm")
+    return out
+
+
 def last_launch_count() -> int:
     """Kernels the last call on this thread enqueued."""
     return int(_lib.load().moe_last_launch_count())

@@ -188,6 +188,12 @@ int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_
                      int32_t *expert_counts, float *aux_P, float *aux_loss,
                      int32_t *status_out, void *stream);
 
+/* Decoder-layer pre-norm for stacking MoE layers (the routing page, §五,
+ * builds its MoE blocks into decoder layers but does not describe their norm):
+ *   out[t] = bf16( x[t] / sqrt(mean_h x[t,h]^2 + eps) )  (unit weight, fp32)
+ * x, out [T, H] bf16 (may alias), H % 8 == 0, 16-byte aligned. */
+int moe_rmsnorm(int32_t T, int32_t H, const moe_bf16 *x, moe_bf16 *out, float eps, void *stream);
+
 /* Waits for `stream`, then copies the workspace's status word (MOE_STATUS_*
  * bits, OR-ed over every call since the last reset) to *status (a HOST
  * pointer); clears it when reset != 0.  Returns MOE_OK, or MOE_ERR_CUDA. */
@@ -207,6 +213,14 @@ int moe_last_launch_count(void);
 int moe_profile_enable(int on);
 int moe_profile_read(int kernel_id, double *total_ms, int32_t *launches, int reset);
 const char *moe_kernel_name(int kernel_id);
+
+/* Fault injection for tests of the failure path (no counterpart on the pages).
+ * The next `launches` grouped gate/up GEMM launches made by moe_forward, in
+ * this process, run with their TMA producer withholding every load and a
+ * 50 ms wait limit: the MMA lane's first wait runs out, the kernel winds down
+ * (copies drained, TMEM freed) and sets MOE_STATUS_TIMEOUT; the call's output
+ * is then meaningless, but the CUDA context stays usable.  0 cancels. */
+int moe_debug_inject_timeout(int launches);
 
 /* Static description of a return code. */
 const char *moe_strerror(int code);

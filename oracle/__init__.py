@@ -59,6 +59,7 @@ def _load():
             lib.orc_experts.argtypes = [ctypes.POINTER(_Cfg)] + [P] * 8 + [ctypes.c_int, P, P]
             lib.orc_experts.restype = ctypes.c_int
             lib.orc_bf16_round_array.argtypes = [P, P, ctypes.c_long]
+            lib.orc_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
             lib.orc_set_threads.argtypes = [ctypes.c_int]
             lib.orc_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -158,6 +159,15 @@ def experts(x_bf16, W_gate_up, W_down, shared_gate_up, shared_down, idx, w,
                              _p(res), n, _p(tok), _p(out))
     if rc != 0:
         raise IndexError("expert index out of range")
+    return out
+
+
+def rmsnorm(x_bf16: np.ndarray, eps: float = 1e-6) -> np.ndarray:
+    """Decoder pre-norm: bf16 bits of x / sqrt(mean(x^2) + eps), row by row."""
+    x = _c(x_bf16, np.uint16)
+    T, H = x.shape
+    out = np.empty_like(x)
+    _load().orc_rmsnorm(T, H, _p(x), eps, _p(out))
     return out
 
 

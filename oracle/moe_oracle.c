@@ -340,3 +340,24 @@ int orc_experts(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const 
     }
     return bad ? -1 : 0;
 }
+
+/* ------------------------------------------------ stacking (routing page 五) */
+
+/* Pre-norm in front of each MoE block when layers are stacked into decoder
+ * layers (routing page, section 五 names the decoder layer, not its norm; the
+ * reading taken is an RMS norm with unit weight):
+ *   out[t, h] = bf16( x[t, h] / sqrt(mean_h x[t, h]^2 + eps) ), in double. */
+void orc_rmsnorm(int T, int H, const uint16_t *x, float eps, uint16_t *out)
+{
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t) {
+        double ss = 0.0;
+        for (int h = 0; h < H; ++h) {
+            double v = orc_bf16_value(x[(size_t)t * H + h]);
+            ss += v * v;
+        }
+        double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
+        for (int h = 0; h < H; ++h)
+            out[(size_t)t * H + h] = orc_bf16_round((float)(orc_bf16_value(x[(size_t)t * H + h]) * inv));
+    }
+}

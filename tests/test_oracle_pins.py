@@ -397,3 +397,16 @@ def test_out_of_range_expert_index_is_reported():
     idx[3, 1] = Wgu.shape[0]
     with pytest.raises(IndexError):
         oracle.experts(x, Wgu, Wd, sgu, sd, idx, np.ones(idx.shape, np.float32))
+
+
+# ------------------------------------------------------------- stacking norm
+
+def test_rmsnorm_matches_numpy():
+    rng = np.random.default_rng(18)
+    x = bf16(rng.standard_normal((50, 512)) * rng.uniform(0.01, 30, (50, 1)))
+    ours = f32_of(oracle.rmsnorm(x, 1e-6)).astype(np.float64)
+    X = f32_of(x).astype(np.float64)
+    ref = X / np.sqrt((X * X).mean(axis=1, keepdims=True) + 1e-6)
+    # the oracle rounds once to bf16: within half a bf16 ulp (2^-9 relative)
+    assert np.all(np.abs(ours - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
+    np.testing.assert_allclose(np.sqrt((ours ** 2).mean(axis=1)), 1.0, atol=1e-2)
