@@ -250,3 +250,53 @@ class MoELayer:
 
     def status(self) -> int:
         return self.ws_route.status() | self.ws_fwd.status()
+
+
+class HostPipeline:
+    """Runs a MoELayer over batches that live in (pinned) host memory.
+
+    Every batch is copied host -> device, run through the layer, and its
+    output copied device -> host.  The copies run on their own streams with two
+    device buffers per direction, so the upload of batch i+1 and the download
+    of batch i-1 overlap the layer's kernels on batch i; the layer itself runs
+    on the caller's current stream, one batch after the other."""
+
+    def __init__(self, layer: "MoELayer", depth: int = 2):
+        cfg = layer.cfg
+        dev = layer.W_router.device
+        self.layer = layer
+        self.depth = depth
+        self.x_dev = [torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.y_dev = [torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev) for _ in range(depth)]
+        self.s_in = torch.cuda.Stream(dev)
+        self.s_out = torch.cuda.Stream(dev)
+        self.ev_loaded = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_done = [torch.cuda.Event() for _ in range(depth)]
+        self.ev_saved = [torch.cuda.Event() for _ in range(depth)]
+        self.launches = 0
+
+    def run(self, host_in, host_out) -> None:
+        """host_in[i] -> layer -> host_out[i] for every i (pinned bf16 [T, H])."""
+        comp = torch.cuda.current_stream(self.x_dev[0].device)
+        used = [False] * self.depth
+        for i, (hi, ho) in enumerate(zip(host_in, host_out)):
+            b = i % self.depth
+            with torch.cuda.stream(self.s_in):
+                if used[b]:
+                    self.s_in.wait_event(self.ev_done[b])       # the layer has read this buffer
+                self.x_dev[b].copy_(hi, non_blocking=True)
+                self.ev_loaded[b].record(self.s_in)
+            comp.wait_event(self.ev_loaded[b])
+            if used[b]:
+                comp.wait_event(self.ev_saved[b])               # the previous output has left
+            self.layer(self.x_dev[b], out=self.y_dev[b])
+            self.launches += self.layer.last_launches
+            self.ev_done[b].record(comp)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(self.ev_done[b])
+                ho.copy_(self.y_dev[b], non_blocking=True)
+                self.ev_saved[b].record(self.s_out)
+            used[b] = True
+        for b in range(self.depth):
+            if used[b]:
+                comp.wait_event(self.ev_saved[b])               # the caller's stream sees every output

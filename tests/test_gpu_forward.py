@@ -181,3 +181,22 @@ def test_forward_launch_count():
     idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=13, device=DEV)
     moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
     assert moe.last_launch_count() == 6   # hist, scan, scatter, gate/up GEMM, down GEMM, combine
+
+
+def test_host_pipeline_matches_the_layer():
+    """Batches streamed from pinned host memory give the layer's own outputs."""
+    T = 1024
+    w0 = wl.WORKLOADS[3].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T)
+    layer = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"], d["shared_gate_up"],
+                         d["shared_down"])
+    xs = [torch.randn(T, cfg.H).to(torch.bfloat16).pin_memory() for _ in range(5)]
+    outs = [torch.empty(T, cfg.H, dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    pipe = moe.HostPipeline(layer)
+    pipe.run(xs, outs)
+    torch.cuda.synchronize()
+    for xh, oh in zip(xs, outs):
+        ref = layer(xh.to(DEV)).cpu()
+        assert torch.equal(oh, ref)
+    assert pipe.launches == 5 * 9
