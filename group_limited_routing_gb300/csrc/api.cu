@@ -440,6 +440,8 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
         !make_map_bf16(&p1.tmB0, W_gate_up, 2ull * c.I * c.E, c.H, GEMM_BK, 128) ||
         !make_map_bf16(&p1.tmB1, shared_gate_up, 2ull * c.I, c.H, GEMM_BK, 128))
         return MOE_ERR_CUDA;
+    if (!make_map_bf16(&p1.tmOut, aint, kT + c.T, c.I, 64, 32))
+        return MOE_ERR_CUDA;
     p1.out = aint;
     p1.mtiles = mtiles;
     p1.num_mtiles = &hdr->num_mtiles;
@@ -464,6 +466,8 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     if (!make_map_bf16(&p2.tmA0, aint, kT + c.T, c.I, GEMM_BK, GEMM_BM) ||
         !make_map_bf16(&p2.tmB0, W_down, (uint64_t)c.I * c.E, c.H, 64, GEMM_BK) ||
         !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, 64, GEMM_BK))
+        return MOE_ERR_CUDA;
+    if (!make_map_bf16(&p2.tmOut, y, kT + c.T, c.H, 64, 32))
         return MOE_ERR_CUDA;
     p2.out = y;
     p2.mtiles = mtiles;

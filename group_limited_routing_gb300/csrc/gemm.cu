@@ -80,7 +80,9 @@ template <int KIND>
 struct GemmLayout {
     using C = GemmCfg<KIND>;
     static constexpr int STAGE_BYTES = C::A_BYTES + C::B_BYTES;
-    static constexpr int STAGING = 4 * 4096;           // 32 rows x 128 B per epilogue warp
+    // per epilogue warp, 32 rows x 128 B: one buffer for the router, two for
+    // the grouped GEMMs (a TMA store can drain one while the other is filled)
+    static constexpr int STAGING = (KIND == GK_ROUTER ? 1 : 2) * 4 * 4096;
     // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin
     static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1;
     static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16;
@@ -209,16 +211,52 @@ __device__ __forceinline__ void warp_store_rows128(uint8_t *stage, const uint4 (
     __syncwarp();
 }
 
+// One 32-row x 64-column bf16 piece of a grouped-GEMM output (lane = row,
+// eight 16-byte chunks in v).  When all 32 rows belong to the tile, the piece
+// goes out with a TMA store from a double-buffered, 128B-swizzled staging
+// buffer (lane 0 issues it; the buffer is reused only after the store before
+// the previous one has read it).  Otherwise -- the last tile of a bucket,
+// whose other rows belong to the next expert -- the masked line-wise path.
+__device__ __forceinline__ void store_piece(const GemmParams &p, uint8_t *stage2, int &buf, const uint4 (&v)[8],
+                                            int lane, int valid_rows, char *gbase, size_t ld_bytes, int col,
+                                            int row0)
+{
+    if (valid_rows >= 32) {
+        uint8_t *stage = stage2 + buf * 4096;
+        if (lane == 0)
+            bulk_wait_group_read<1>();          // this buffer's previous store has left smem
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4 *>(stage + lane * 128 + ((q ^ (lane & 7)) << 4)) = v[q];
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(&p.tmOut, smem_u32(stage), col, row0);
+            bulk_commit_group();
+        }
+        buf ^= 1;
+    } else if (valid_rows > 0) {
+        uint8_t *stage = stage2 + buf * 4096;
+        if (lane == 0)
+            bulk_wait_group_read<1>();
+        __syncwarp();
+        warp_store_rows128(stage, v, lane, gbase, ld_bytes, valid_rows);
+        buf ^= 1;
+    }
+}
+
 // Epilogue of one grouped-GEMM tile for one epilogue warp (32 rows).
 template <int KIND>
 __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
-                                              int lane, uint8_t *stage)
+                                              int lane, uint8_t *stage2, int &buf)
 {
     const int valid_rows = ti.rows - quad * 32;
     const size_t ld_bytes = (size_t)p.ld_out * 2;
+    const int row0 = ti.out_row + quad * 32;
     if constexpr (KIND == GK_GATE_UP) {
         // TMEM columns [0,128) = gate, [128,256) = up; 64 outputs per pass
-        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes + ti.nt * 256;
+        char *gbase = static_cast<char *>(p.out) + (size_t)row0 * ld_bytes + ti.nt * 256;
 #pragma unroll 1
         for (int c = 0; c < 128; c += 64) {
             uint32_t g[64], u[64];
@@ -230,11 +268,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
             for (int i = 0; i < 32; ++i)
                 pk[i] = pack_bf16x2(silu_times(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
                                     silu_times(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-            if (valid_rows > 0)
-                warp_store_rows128(stage, v, lane, gbase + c * 2, ld_bytes, valid_rows);
+            store_piece(p, stage2, buf, v, lane, valid_rows, gbase + c * 2, ld_bytes, ti.nt * 128 + c, row0);
         }
     } else {
-        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes + ti.nt * 512;
+        char *gbase = static_cast<char *>(p.out) + (size_t)row0 * ld_bytes + ti.nt * 512;
 #pragma unroll 1
         for (int c = 0; c < 256; c += 64) {
             uint32_t r[64];
@@ -244,8 +281,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            if (valid_rows > 0)
-                warp_store_rows128(stage, v, lane, gbase + c * 2, ld_bytes, valid_rows);
+            store_piece(p, stage2, buf, v, lane, valid_rows, gbase + c * 2, ld_bytes, ti.nt * 256 + c, row0);
         }
     }
 }
@@ -443,7 +479,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
-        uint8_t *stage = staging + (warp - 2) * 4096;
+        uint8_t *stage = staging + (warp - 2) * (ROUTER ? 4096 : 8192);
+        int buf = 0;
         uint32_t ctr = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const TileInfo ti = tile_info<KIND>(p, tile);
@@ -461,7 +498,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
                 __syncwarp();
                 tc_fence_after();
                 const uint32_t tacc = tmem + ((uint32_t)(quad * 32) << 16) + slot * C::BN;
-                epilogue_tile<KIND>(p, ti, tacc, quad, lane, stage);
+                epilogue_tile<KIND>(p, ti, tacc, quad, lane, stage, buf);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
@@ -469,6 +506,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
                 ++ctr;
             }
         }
+        if (!ROUTER && lane == 0)
+            bulk_wait_group_all();              // this warp's output stores have completed
     }
 
     __syncwarp();

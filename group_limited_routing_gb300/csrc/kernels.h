@@ -38,6 +38,7 @@ struct GemmParams {
     CUtensorMap tmA1;   // gate_up: hidden (shared-expert rows)
     CUtensorMap tmB0;   // router: W split [3E, H]; gate_up: W_gate_up [E*2I, H]; down: W_down [E*I, H]
     CUtensorMap tmB1;   // gate_up: shared_gate_up [2I, H]; down: shared_down [I, H]
+    CUtensorMap tmOut;  // grouped: the output, boxes of 64 columns x 32 rows (TMA stores)
     void *out;          // router: logits fp32 [T, E]; gate_up: intermediate bf16; down: Y bf16
     const int4 *mtiles; // grouped: {group, first row, rows, 0}
     const int *num_mtiles;
