@@ -141,7 +141,7 @@ RouteLayout route_layout(const moe_cfg &c)
 }
 
 struct FwdLayout {
-    size_t hist, mtiles, slot_of, xperm, aint, y, total;
+    size_t hist, sizes, mtiles, slot_of, xperm, aint, y, total;
     int nchunk, max_mtiles;
 };
 
@@ -155,6 +155,8 @@ FwdLayout fwd_layout(const moe_cfg &c)
     size_t off = sizeof(WsHeader);
     L.hist = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
+    L.sizes = off;
+    off = align_up(off + (size_t)c.E * 4, 256);
     L.mtiles = off;
     off = align_up(off + (size_t)L.max_mtiles * 16, 256);
     L.slot_of = off;
@@ -429,8 +431,10 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
 
     // bucket the (token, expert) pairs by expert (stable), gather rows
     GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
-    GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.T, c.E, c.k, mtiles, hdr, s));
-    GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, c.T, c.H, c.E, c.k, slot_of, xperm, s));
+    int32_t *sizes = at<int32_t>(ws, L.sizes);
+    GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
+    GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of, xperm,
+                                                  mtiles, hdr, s));
 
     // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E)
     GemmParams p1;

@@ -74,11 +74,12 @@ cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int
 cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status,
                                cudaStream_t s);
 
-cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int T, int E, int k, int4 *mtiles,
-                               WsHeader *hdr, cudaStream_t s);
+// hist [E][nchunk] -> per-chunk starts inside each bucket (relative); sizes[E]
+cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s);
 
-cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base, int T,
-                                  int H, int E, int k, int32_t *slot_of, uint16_t *x_perm, cudaStream_t s);
+cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
+                                  const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
+                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s);
 
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s);

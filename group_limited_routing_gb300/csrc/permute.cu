@@ -5,10 +5,12 @@
 // one bucket per expert, runs each bucket through its expert and sums the
 // weighted results.  Here:
 //   bucket_hist    per 128-token chunk, hits per expert        (reads topk_idx)
-//   bucket_scan    bucket offsets (exclusive scan of the counts), each chunk's
-//                  start inside every bucket, and the m-tile list of the
-//                  grouped GEMMs (the shared expert is group E, all T tokens)
-//   bucket_scatter stable slot of every (token, j) pair -- slots in a bucket in
+//   bucket_scan    each chunk's start inside every bucket (relative) and the
+//                  bucket sizes
+//   bucket_scatter bucket offsets (exclusive scan of the sizes) and, block 0,
+//                  the m-tile list of the grouped GEMMs (the shared expert is
+//                  group E, all T tokens); then, per chunk:
+//                  stable slot of every (token, j) pair -- slots in a bucket in
 //                  ascending (token, j) order -- and the gather of hidden rows
 //                  into the bucketed activation matrix X_perm
 //   combine        out[t] = bf16( sum_j w[t,j] * Y[slot(t,j)] + Y_shared[t]
@@ -42,7 +44,7 @@ __global__ void __launch_bounds__(256) bucket_hist_kernel(const int32_t *__restr
     if (__syncthreads_or(bad) && threadIdx.x == 0)
         atomicOr(status, ST_BAD_INDEX);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
-        hist[(size_t)blockIdx.x * E + e] = sh[e];
+        hist[(size_t)e * gridDim.x + blockIdx.x] = sh[e];   // [expert][chunk]
 }
 
 cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status, cudaStream_t s)
@@ -53,116 +55,101 @@ cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t 
 }
 
 // ---------------------------------------------------------------------------
-// One block of 1024 threads, E <= 256: thread (q, e) owns expert e's column
-// for the chunks of quarter q.  In place, hist[c][e] becomes the first slot of
-// chunk c inside bucket e.
-__global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t *__restrict__ hist, int nchunk, int T, int E,
-                                                           int K, int4 *__restrict__ mtiles,
-                                                           WsHeader *__restrict__ hdr)
+// Per-bucket scan: one warp per expert (8 per block).  hist is
+// [expert][chunk]; in place, hist[e][c] becomes the number of bucket-e rows of
+// the chunks before c (contiguous loads, warp prefix sums), and sizes[e] the
+// bucket's size.  The bucket offsets follow in bucket_scatter.
+__global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ hist, int nchunk, int E,
+                                                          int32_t *__restrict__ sizes)
 {
-    __shared__ int part[4][257];
-    __shared__ int total[257];
-    __shared__ int offset[258];
-    __shared__ int tstart[258];
-    __shared__ int wsum_rows[8];
-    __shared__ int wsum_tiles[8];
-    const int e = threadIdx.x & 255, q = threadIdx.x >> 8;
-    const int per = (nchunk + 3) / 4;
-    const int c0 = min(nchunk, q * per), c1 = min(nchunk, c0 + per);
-
-    int sum = 0;
-    if (e < E) {
-#pragma unroll 8
-        for (int c = c0; c < c1; ++c)
-            sum += hist[(size_t)c * E + e];
-    }
-    part[q][e] = sum;
-    __syncthreads();
-    if (q == 0) {
-        total[e] = (e < E) ? part[0][e] + part[1][e] + part[2][e] + part[3][e] : 0;
-        if (e == 0)
-            total[256] = 0;
-    }
-    __syncthreads();
-    // bucket offsets and first m-tile of every group: exclusive scans over the
-    // E routed groups by the first 8 warps (the shared group E comes last)
-    if (threadIdx.x < 256) {
-        const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-        const int n = (e < E) ? total[e] : 0;
-        const int nt = (n + GEMM_BM - 1) / GEMM_BM;
-        int a = n, b = nt;                      // inclusive warp scans
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (e >= E)
+        return;
+    int32_t *row = hist + (size_t)e * nchunk;
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunk; c0 += 32) {
+        const int c = c0 + lane;
+        const int h = (c < nchunk) ? row[c] : 0;
+        int incl = h;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int ya = __shfl_up_sync(0xffffffffu, a, off);
-            const int yb = __shfl_up_sync(0xffffffffu, b, off);
-            if (lane >= off) {
-                a += ya;
-                b += yb;
-            }
+            const int y = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off)
+                incl += y;
         }
-        if (lane == 31) {
-            wsum_rows[w] = a;
-            wsum_tiles[w] = b;
+        if (c < nchunk)
+            row[c] = carry + incl - h;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0)
+        sizes[e] = carry;
+}
+
+cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s)
+{
+    bucket_scan_kernel<<<(E + 7) / 8, 256, 0, s>>>(hist, nchunk, E, sizes);
+    return cudaPeekAtLastError();
+}
+
+// Bucket offsets (exclusive scan of the E sizes) and first m-tile of every
+// group, by a 256-thread block into shared memory; thread 0 also checks that
+// every pair was bucketed.  With `write_tiles`, the block writes the m-tile
+// list of the grouped GEMMs (the shared expert is group E, all T tokens).
+__device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, int K, int *offset, int *tstart,
+                               int *wsum_rows, int *wsum_tiles, bool write_tiles, int4 *__restrict__ mtiles,
+                               WsHeader *__restrict__ hdr)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int e = threadIdx.x;   // blockDim.x == 256 >= E
+    const int n = (e < E) ? sizes[e] : 0;
+    const int nt = (n + GEMM_BM - 1) / GEMM_BM;
+    int a = n, b = nt;           // inclusive warp scans
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, a, off);
+        const int yb = __shfl_up_sync(0xffffffffu, b, off);
+        if (lane >= off) {
+            a += ya;
+            b += yb;
         }
-        __syncwarp();
-        offset[e] = a - n;                      // warp-local exclusive, fixed below
-        tstart[e] = b - nt;
+    }
+    if (lane == 31) {
+        wsum_rows[w] = a;
+        wsum_tiles[w] = b;
     }
     __syncthreads();
-    if (threadIdx.x < 256) {
-        int ra = 0, rb = 0;
-        for (int w = 0; w < (threadIdx.x >> 5); ++w) {
-            ra += wsum_rows[w];
-            rb += wsum_tiles[w];
-        }
-        offset[e] += ra;
-        tstart[e] += rb;
+    int ra = 0, rb = 0;
+    for (int q = 0; q < w; ++q) {
+        ra += wsum_rows[q];
+        rb += wsum_tiles[q];
     }
+    offset[e] = ra + a - n;
+    tstart[e] = rb + b - nt;
     __syncthreads();
     if (threadIdx.x == 0) {
         int off = 0, tiles = 0;
-        for (int w = 0; w < 8; ++w) {
-            off += wsum_rows[w];
-            tiles += wsum_tiles[w];
+        for (int q = 0; q < 8; ++q) {
+            off += wsum_rows[q];
+            tiles += wsum_tiles[q];
         }
         offset[E] = off;             // == K*T unless indices were out of range
         tstart[E] = tiles;
-        tiles += (T + GEMM_BM - 1) / GEMM_BM;
-        tstart[E + 1] = tiles;
-        hdr->num_mtiles = tiles;
-        if (off != K * T)
-            atomicOr(&hdr->status, ST_COUNT_MISMATCH);
-    }
-    __syncthreads();
-    if (e < E) {
-        int run = offset[e];
-        for (int qq = 0; qq < q; ++qq)
-            run += part[qq][e];
-#pragma unroll 8
-        for (int c = c0; c < c1; ++c) {
-            const int h = hist[(size_t)c * E + e];
-            hist[(size_t)c * E + e] = run;
-            run += h;
+        if (write_tiles) {
+            hdr->num_mtiles = tiles + (T + GEMM_BM - 1) / GEMM_BM;
+            if (off != K * T)
+                atomicOr(&hdr->status, ST_COUNT_MISMATCH);
         }
     }
-    // m-tile lists: routed buckets by q == 0 threads, the shared group by the rest
-    if (q == 0 && e < E) {
-        const int n = total[e];
-        for (int i = 0, r = 0; r < n; ++i, r += GEMM_BM)
-            mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n - r), 0);
-    }
-    {
+    __syncthreads();
+    if (write_tiles) {
+        if (e < E)
+            for (int i = 0, r = 0; r < n; ++i, r += GEMM_BM)
+                mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n - r), 0);
         const int ntile_sh = (T + GEMM_BM - 1) / GEMM_BM;
-        for (int i = threadIdx.x - 256; i >= 0 && i < ntile_sh; i += 768)
+        for (int i = threadIdx.x; i < ntile_sh; i += blockDim.x)
             mtiles[tstart[E] + i] = make_int4(E, i * GEMM_BM, min(GEMM_BM, T - i * GEMM_BM), 0);
     }
-}
-
-cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int T, int E, int k, int4 *mtiles, WsHeader *hdr,
-                               cudaStream_t s)
-{
-    bucket_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunk, T, E, k, mtiles, hdr);
-    return cudaPeekAtLastError();
 }
 
 // ---------------------------------------------------------------------------
@@ -171,17 +158,24 @@ cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int T, int E, int k, i
 // each other with __match_any_sync and take consecutive slots by lane rank.
 __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__restrict__ idx,
                                                              const uint16_t *__restrict__ x,
-                                                             const int32_t *__restrict__ chunk_base, int T, int H,
+                                                             const int32_t *__restrict__ chunk_base,
+                                                             const int32_t *__restrict__ sizes, int T, int H,
                                                              int E, int K, int32_t *__restrict__ slot_of,
-                                                             uint16_t *__restrict__ x_perm)
+                                                             uint16_t *__restrict__ x_perm, int4 *__restrict__ mtiles,
+                                                             WsHeader *__restrict__ hdr)
 {
+    __shared__ int offset[258];
+    __shared__ int tstart[258];
+    __shared__ int wsum_rows[8];
+    __shared__ int wsum_tiles[8];
     extern __shared__ int sm[];
     int *next = sm;            // [E]   next free slot of each bucket for this chunk
     int *slots = sm + E;       // [PERM_CHUNK * K]
     const int t0 = blockIdx.x * PERM_CHUNK;
     const int nt = min(PERM_CHUNK, T - t0);
+    bucket_offsets(sizes, T, E, K, offset, tstart, wsum_rows, wsum_tiles, blockIdx.x == 0, mtiles, hdr);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
-        next[e] = chunk_base[(size_t)blockIdx.x * E + e];
+        next[e] = offset[e] + chunk_base[(size_t)e * gridDim.x + blockIdx.x];   // [expert][chunk]
     __syncthreads();
     if (threadIdx.x < 32) {
         const int lane = threadIdx.x;
@@ -238,12 +232,14 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
     }
 }
 
-cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base, int T, int H,
-                                  int E, int k, int32_t *slot_of, uint16_t *x_perm, cudaStream_t s)
+cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
+                                  const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
+                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s)
 {
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
-    bucket_scatter_kernel<<<blocks, 256, smem, s>>>(idx, x, chunk_base, T, H, E, k, slot_of, x_perm);
+    bucket_scatter_kernel<<<blocks, 256, smem, s>>>(idx, x, chunk_base, sizes, T, H, E, k, slot_of, x_perm, mtiles,
+                                                    hdr);
     return cudaPeekAtLastError();
 }
 
@@ -310,6 +306,64 @@ __device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, cons
     reinterpret_cast<uint4 *>(out + (size_t)t * H)[vv] = o;
 }
 
+// Two tokens at once: both tokens' row loads are issued before any is used
+// (same arithmetic, in the same order, as combine_one for each token).
+__device__ __forceinline__ void combine_two(const uint16_t *__restrict__ Y, const int *s_slot, const float *s_w,
+                                            const uint16_t *__restrict__ residual, int T, int H, int K, int ta,
+                                            int tla, int tb, int tlb, int vv, uint16_t *__restrict__ out)
+{
+    if (K > 8) {
+        combine_one(Y, s_slot, s_w, residual, T, H, K, ta, tla, vv, out);
+        combine_one(Y, s_slot, s_w, residual, T, H, K, tb, tlb, vv, out);
+        return;
+    }
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    uint4 ya[8], yb[8];
+    float wa[8], wb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const int sa = (u < K) ? s_slot[tla * K + u] : -1;
+        const int sb = (u < K) ? s_slot[tlb * K + u] : -1;
+        wa[u] = (sa >= 0) ? s_w[tla * K + u] : 0.0f;
+        wb[u] = (sb >= 0) ? s_w[tlb * K + u] : 0.0f;
+        ya[u] = (sa >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)sa * H)[vv] : zero;
+        yb[u] = (sb >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)sb * H)[vv] : zero;
+    }
+    const uint4 sva = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + ta) * H)[vv];
+    const uint4 svb = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + tb) * H)[vv];
+    uint4 rva = zero, rvb = zero;
+    if (residual) {
+        rva = reinterpret_cast<const uint4 *>(residual + (size_t)ta * H)[vv];
+        rvb = reinterpret_cast<const uint4 *>(residual + (size_t)tb * H)[vv];
+    }
+    float acc[8], racc[8];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            acc[q] = 0.0f;
+            racc[q] = 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            add_bf16x8(racc, half ? yb[u] : ya[u], half ? wb[u] : wa[u]);
+        add_bf16x8(acc, half ? svb : sva, 1.0f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            acc[q] += racc[q];
+        if (residual)
+            add_bf16x8(acc, half ? rvb : rva, 1.0f);
+        uint4 o;
+        uint32_t *op = reinterpret_cast<uint32_t *>(&o);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            op[q] = *reinterpret_cast<uint32_t *>(&b);
+        }
+        reinterpret_cast<uint4 *>(out + (size_t)(half ? tb : ta) * H)[vv] = o;
+    }
+}
+
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict__ Y,
                                                       const int32_t *__restrict__ slot_of,
                                                       const float *__restrict__ w,
@@ -334,8 +388,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
         if (sub >= rpp)
             continue;
         for (int vv = v; vv < vpr; vv += blockDim.x) {
-            for (int tl = sub; tl < nt; tl += rpp)
-                combine_one(Y, s_slot, s_w, residual, T, H, K, t0 + tl, tl, vv, out);
+            for (int tl = sub; tl < nt; tl += 2 * rpp) {
+                if (tl + rpp < nt)
+                    combine_two(Y, s_slot, s_w, residual, T, H, K, t0 + tl, tl, t0 + tl + rpp, tl + rpp, vv, out);
+                else
+                    combine_one(Y, s_slot, s_w, residual, T, H, K, t0 + tl, tl, vv, out);
+            }
         }
     }
 }

@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(
         for (int j = 0; j < G; ++j) {
             const float L = __ldg(row + 32 * j + lane);
             nonfinite |= !isfinite(L) || !isfinite(bias_r[j]);
-            s[j] = 1.0f / (1.0f + expf(-L));          // section 二 step 1
+            s[j] = __frcp_rn(1.0f + expf(-L));        // section 二 step 1 (IEEE-rounded 1/x)
             b[j] = s[j] + bias_r[j];                  // section 三: choose on s + bias
         }
 
@@ -130,18 +130,24 @@ __global__ void __launch_bounds__(256) route_select_kernel(
             g[j] = fkey_value(m1) + fkey_value(m2);
         }
 
-        // keep the TG best groups (ties to the lower group index)
-        uint32_t keep = 0;
+        // keep the TG best groups (ties to the lower group index): lane j < G
+        // ranks group j, one ballot collects the verdicts
+        float gl = g[0];
 #pragma unroll
-        for (int j = 0; j < G; ++j) {
-            int rank = 0;
+        for (int j = 1; j < G; ++j)
+            if (lane == j)
+                gl = g[j];
+        int rank = 0;
 #pragma unroll
-            for (int i = 0; i < G; ++i)
-                rank += (g[i] > g[j] || (g[i] == g[j] && i < j)) ? 1 : 0;
-            keep |= (rank < TG ? 1u : 0u) << j;
-        }
+        for (int i = 0; i < G; ++i)
+            rank += (g[i] > gl || (g[i] == gl && i < lane)) ? 1 : 0;
+        const uint32_t keep = __ballot_sync(FULL, lane < G && rank < TG) & ((1u << G) - 1u);
 
         // top-K of the surviving experts: K rounds of (max key, then lowest index)
+        uint32_t kb_[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            kb_[j] = fkey(b[j]);
         uint32_t avail = keep;   // this lane's candidates not yet taken, by group
         float den = 0.0f;
         int my_e = -1;
@@ -151,9 +157,8 @@ __global__ void __launch_bounds__(256) route_select_kernel(
             int bj = -1;
 #pragma unroll
             for (int j = 0; j < G; ++j) {
-                const uint32_t kj = fkey(b[j]);
-                if (((avail >> j) & 1u) && (bj < 0 || kj > bk)) {   // ascending j: ties keep the lower index
-                    bk = kj;
+                if (((avail >> j) & 1u) && (bj < 0 || kb_[j] > bk)) {   // ascending j: ties keep the lower index
+                    bk = kb_[j];
                     bj = j;
                 }
             }
