@@ -249,6 +249,11 @@ T *at(void *ws, size_t off)
 int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, float *logits, int32_t *counts,
                 void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches)
 {
+    if (c.T <= ROUTER_SIMT_MAX_T && c.H % 4 == 0) {
+        // a few token tiles cannot fill the tensor-core kernel: CUDA cores, fp32 W as is
+        GLR_LAUNCH(KID_ROUTER_GEMM, launch_router_simt(hidden, W, c.T, c.E, c.H, logits, counts, s));
+        return MOE_OK;
+    }
     uint16_t *W3 = at<uint16_t>(ws, L.w3);
     GLR_LAUNCH(KID_SPLIT, launch_split_router(W, W3, c.E, c.H, counts, s));
     GemmParams p;

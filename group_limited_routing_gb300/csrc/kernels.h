@@ -63,6 +63,11 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
 // W (fp32) -> hi/mid/lo bf16 parts [3][E][H]; also zeroes counts[E] when given.
 cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, int32_t *counts, cudaStream_t s);
 
+// Small-T router logits on the CUDA cores (fp32 W read as is); clears counts.
+constexpr int ROUTER_SIMT_MAX_T = 32;   // decode sizes; the tensor-core path wins above
+cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, int H, float *logits,
+                               int32_t *counts, cudaStream_t s);
+
 // counts[E] must be zero (or hold counts to add to) before the launch.
 cudaError_t launch_route_select(const float *logits, const float *bias, int T, int E, int n_group,
                                 int topk_group, int k, float rsf, float eps, int32_t *idx, float *w,

@@ -56,6 +56,78 @@ cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, int3
 }
 
 // ---------------------------------------------------------------------------
+// Router logits for small T on the CUDA cores.  A block covers 8 experts x
+// SIMT_TOK tokens: warp w keeps 2048 columns of expert (8 bx + w)'s fp32 weight
+// row in registers (as it is, no split) and computes its dot products with
+// the block's tokens, each lane summing a strided 1/32 of the products with
+// fused multiply-adds, then one butterfly reduction per token.  Faster than
+// the tensor-core path when a handful of token tiles cannot fill the GPU.
+// Block (0, 0) also clears `counts` for the routing kernel that follows.
+constexpr int SIMT_TOK = 8;
+
+__global__ void __launch_bounds__(256) router_simt_kernel(const uint16_t *__restrict__ x,
+                                                          const float *__restrict__ W, int T, int E, int H,
+                                                          float *__restrict__ logits, int32_t *__restrict__ counts)
+{
+    if (blockIdx.x == 0 && blockIdx.y == 0 && counts)
+        for (int e = threadIdx.x; e < E; e += blockDim.x)
+            counts[e] = 0;
+    const int lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int t0 = blockIdx.y * SIMT_TOK;
+    const int nt = min(SIMT_TOK, T - t0);
+    if (e >= E || nt <= 0)
+        return;
+    float acc[SIMT_TOK];
+#pragma unroll
+    for (int tt = 0; tt < SIMT_TOK; ++tt)
+        acc[tt] = 0.0f;
+    const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)e * H);
+    for (int h0 = 0; h0 < H / 4; h0 += 16 * 32) {             // 2048 columns per pass
+        float4 wr[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int v = h0 + lane + 32 * i;
+            wr[i] = (v < H / 4) ? __ldg(w4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int tt = 0; tt < SIMT_TOK; ++tt) {
+            if (tt < nt) {
+                const uint2 *x4 = reinterpret_cast<const uint2 *>(x + (size_t)(t0 + tt) * H);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int v = h0 + lane + 32 * i;
+                    if (v < H / 4) {
+                        const uint2 xv = __ldg(x4 + v);
+                        acc[tt] = fmaf(__uint_as_float(xv.x << 16), wr[i].x, acc[tt]);
+                        acc[tt] = fmaf(__uint_as_float(xv.x & 0xffff0000u), wr[i].y, acc[tt]);
+                        acc[tt] = fmaf(__uint_as_float(xv.y << 16), wr[i].z, acc[tt]);
+                        acc[tt] = fmaf(__uint_as_float(xv.y & 0xffff0000u), wr[i].w, acc[tt]);
+                    }
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int tt = 0; tt < SIMT_TOK; ++tt) {
+        float a = acc[tt];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            a += __shfl_xor_sync(0xffffffffu, a, off);
+        if (lane == 0 && tt < nt)
+            logits[(size_t)(t0 + tt) * E + e] = a;
+    }
+}
+
+cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, int H, float *logits,
+                               int32_t *counts, cudaStream_t s)
+{
+    const dim3 grid((E + 7) / 8, (T + SIMT_TOK - 1) / SIMT_TOK);
+    router_simt_kernel<<<grid, 256, 0, s>>>(x, W, T, E, H, logits, counts);
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
 // Order-preserving map of fp32 onto uint32 (for non-NaN values): a > b as
 // floats exactly when key(a) > key(b), so warp-wide float max is one
 // __reduce_max_sync.  +0 and -0 get neighbouring keys; the scores compared

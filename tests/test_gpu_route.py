@@ -49,7 +49,7 @@ def test_route_matches_oracle(wid, T):
     assert n_near <= max(2, T // 100)
 
 
-@pytest.mark.parametrize("wid,T", [(1, 128), (3, 4096), (4, 2048)])
+@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (4, 32), (3, 4096), (4, 2048)])
 def test_router_logits_accuracy(wid, T):
     w0 = wl.WORKLOADS[wid].with_T(T)
     d = wl.layer_inputs(w0, DEV, with_experts=False)
@@ -120,10 +120,12 @@ def test_nonfinite_logits_set_status():
     assert ws.status() == 0
 
 
-def test_route_launch_count():
-    cfg = moe.MoeConfig(T=256)
-    d = wl.layer_inputs(wl.WORKLOADS[3].with_T(256), DEV, with_experts=False)
+@pytest.mark.parametrize("T,kernels", [(16, 2), (256, 3)])
+def test_route_launch_count(T, kernels):
+    # small T: CUDA-core router + select; otherwise W split + tensor-core router + select
+    cfg = moe.MoeConfig(T=T)
+    d = wl.layer_inputs(wl.WORKLOADS[3].with_T(T), DEV, with_experts=False)
     moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
-    assert moe.last_launch_count() == 3   # W split, router GEMM, select
+    assert moe.last_launch_count() == kernels
     moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=True)
-    assert moe.last_launch_count() == 4   # + the balance-loss reduction
+    assert moe.last_launch_count() == kernels + 1   # + the balance-loss reduction
