@@ -34,7 +34,7 @@ MOE_WS_FORWARD = 1
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router_logits",
            "moe_route_from_logits", "moe_forward", "moe_get_status", "moe_last_launch_count",
            "moe_profile_enable", "moe_profile_read", "moe_kernel_name", "moe_strerror", "moe_route_static",
-           "moe_debug_inject_timeout", "moe_rmsnorm")
+           "moe_debug_inject_timeout", "moe_rmsnorm", "moe_expert_feedback")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
 MOE_KERNEL_COUNT = 10
 
@@ -90,6 +90,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.moe_profile_read.restype = ctypes.c_int
         lib.moe_kernel_name.argtypes = [ctypes.c_int]
         lib.moe_kernel_name.restype = ctypes.c_char_p
+        lib.moe_expert_feedback.argtypes = [C, P, ctypes.c_float, P, P, P]
+        lib.moe_expert_feedback.restype = ctypes.c_int
         lib.moe_rmsnorm.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, ctypes.c_float, P]
         lib.moe_rmsnorm.restype = ctypes.c_int
         lib.moe_debug_inject_timeout.argtypes = [ctypes.c_int]

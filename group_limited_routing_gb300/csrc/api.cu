@@ -498,6 +498,24 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     return MOE_OK;
 }
 
+int moe_expert_feedback(const moe_cfg *cfg, const int32_t *expert_counts, float gamma, float *expert_bias,
+                        int64_t *totals, void *stream)
+{
+    if (!cfg || cfg->E < 1 || cfg->T < 1 || cfg->k < 1 || !expert_counts || !isfinite(gamma))
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(expert_counts, 4) || !aligned(expert_bias, 4) || !aligned(totals, 8))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0, rc = device_check(&sms);
+    if (rc != MOE_OK)
+        return rc;
+    if (launch_expert_feedback(expert_counts, cfg->E, cfg->T, cfg->k, gamma, expert_bias,
+                               reinterpret_cast<long long *>(totals), static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    g_last_launches = 1;
+    return MOE_OK;
+}
+
 int moe_rmsnorm(int32_t T, int32_t H, const moe_bf16 *x, moe_bf16 *out, float eps, void *stream)
 {
     if (T < 1 || H < 8 || H % 8 != 0 || !x || !out || !isfinite(eps) || eps < 0.0f)

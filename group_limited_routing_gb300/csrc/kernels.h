@@ -89,6 +89,9 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s);
 
+cudaError_t launch_expert_feedback(const int32_t *counts, int E, int T, int k, float gamma, float *bias,
+                                   long long *totals, cudaStream_t s);
+
 cudaError_t launch_rmsnorm(const uint16_t *x, uint16_t *out, int T, int H, float eps, cudaStream_t s);
 
 }  // namespace glr

@@ -385,4 +385,31 @@ cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int
     return cudaPeekAtLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Expert-bias feedback and hit tracking (training side of the routing page:
+// section 三, cold experts up and hot experts down; section 六, running hit
+// totals).  bias[e] += +gamma / -gamma / 0 as counts[e] is below / above /
+// at the balanced load k T / E; totals[e] += counts[e].
+__global__ void expert_feedback_kernel(const int32_t *__restrict__ counts, int E, double mean, float gamma,
+                                       float *__restrict__ bias, long long *__restrict__ totals)
+{
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= E)
+        return;
+    const int c = counts[e];
+    if (totals)
+        totals[e] += c;
+    if (bias) {
+        const float step = ((double)c < mean) ? gamma : (((double)c > mean) ? -gamma : 0.0f);
+        bias[e] = bias[e] + step;
+    }
+}
+
+cudaError_t launch_expert_feedback(const int32_t *counts, int E, int T, int k, float gamma, float *bias,
+                                   long long *totals, cudaStream_t s)
+{
+    expert_feedback_kernel<<<(E + 255) / 256, 256, 0, s>>>(counts, E, (double)k * T / E, gamma, bias, totals);
+    return cudaPeekAtLastError();
+}
+
 }  // namespace glr

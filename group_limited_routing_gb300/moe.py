@@ -186,6 +186,17 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
     return out
 
 
+def expert_feedback(cfg: MoeConfig, counts, gamma: float, expert_bias=None, totals=None) -> None:
+    """moe_expert_feedback: in place, bias += +-gamma toward the balanced load
+    (routing article §三) and totals += counts (§六)."""
+    dev = counts.device
+    pc = _need(counts, "expert_counts", torch.int32, (cfg.E,), dev)
+    pb = _opt(expert_bias, "expert_bias", torch.float32, (cfg.E,), dev)
+    pt = _opt(totals, "totals", torch.int64, (cfg.E,), dev)
+    _lib.check(_lib.load().moe_expert_feedback(ctypes.byref(cfg.c()), pc, gamma, pb, pt, _stream(dev)),
+               "moe_expert_feedback")
+
+
 def rmsnorm(x, eps: float = 1e-6, out=None):
     """moe_rmsnorm: bf16(x / sqrt(mean(x^2) + eps)) per row (decoder pre-norm)."""
     T, H = x.shape
@@ -250,6 +261,15 @@ class MoELayer:
 
     def status(self) -> int:
         return self.ws_route.status() | self.ws_fwd.status()
+
+    def feedback(self, gamma: float, totals=None) -> None:
+        """After a call: nudge expert_bias toward balanced load from this
+        step's expert counts and add them to `totals` (see expert_feedback)."""
+        if self.routing is None:
+            raise RuntimeError("feedback() needs a routed step first")
+        if self.expert_bias is None:
+            self.expert_bias = torch.zeros(self.cfg.E, dtype=torch.float32, device=self.W_router.device)
+        expert_feedback(self.cfg, self.routing[2], gamma, self.expert_bias, totals)
 
 
 class HostPipeline:

@@ -188,6 +188,19 @@ int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_
                      int32_t *expert_counts, float *aux_P, float *aux_loss,
                      int32_t *status_out, void *stream);
 
+/* Training-side feedback after a routing step (routing page, section 三: the
+ * bias of cold experts is raised and that of overloaded experts lowered so
+ * that tokens drift to idle experts; section 六: per-expert hit totals are
+ * kept).  The page gives no formula; this is a sign step around the balanced
+ * load k T / E:
+ *   expert_bias[e] += gamma  if expert_counts[e] < k T / E,
+ *                     -gamma if expert_counts[e] > k T / E, unchanged if equal;
+ *   totals[e]      += expert_counts[e].
+ * expert_counts [E] int32 (moe_route's output), expert_bias [E] fp32 or NULL,
+ * totals [E] int64 or NULL (device pointers, updated in place on `stream`). */
+int moe_expert_feedback(const moe_cfg *cfg, const int32_t *expert_counts, float gamma, float *expert_bias,
+                        int64_t *totals, void *stream);
+
 /* Decoder-layer pre-norm for stacking MoE layers (the routing page, §五,
  * builds its MoE blocks into decoder layers but does not describe their norm):
  *   out[t] = bf16( x[t] / sqrt(mean_h x[t,h]^2 + eps) )  (unit weight, fp32)

@@ -60,6 +60,7 @@ def _load():
             lib.orc_experts.restype = ctypes.c_int
             lib.orc_bf16_round_array.argtypes = [P, P, ctypes.c_long]
             lib.orc_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
+            lib.orc_expert_feedback.argtypes = [ctypes.c_int] * 3 + [P, ctypes.c_float, P, P]
             lib.orc_set_threads.argtypes = [ctypes.c_int]
             lib.orc_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -169,6 +170,16 @@ def rmsnorm(x_bf16: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     out = np.empty_like(x)
     _load().orc_rmsnorm(T, H, _p(x), eps, _p(out))
     return out
+
+
+def expert_feedback(counts, T, k, gamma, bias=None, totals=None):
+    """(new bias or None, new totals or None) after one routing step."""
+    c = _c(counts, np.int32)
+    E = c.size
+    b = None if bias is None else np.array(bias, dtype=np.float32, copy=True)
+    tot = None if totals is None else np.array(totals, dtype=np.int64, copy=True)
+    _load().orc_expert_feedback(E, T, k, _p(c), gamma, _p(b), _p(tot))
+    return b, tot
 
 
 def set_threads(n: int) -> None:

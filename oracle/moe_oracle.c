@@ -361,3 +361,30 @@ void orc_rmsnorm(int T, int H, const uint16_t *x, float eps, uint16_t *out)
             out[(size_t)t * H + h] = orc_bf16_round((float)(orc_bf16_value(x[(size_t)t * H + h]) * inv));
     }
 }
+
+/* ------------------------------------------ routing page 三 and 六 (training) */
+
+/* Expert-bias feedback and hit tracking after a routing step.
+ * Routing page, section 三: during training the bias of cold experts is
+ * raised and that of overloaded experts lowered; read here as a sign step
+ * around the balanced load k T / E:
+ *   bias[e] = fp32( bias[e] + step ),  step = +gamma if counts[e] < k T / E,
+ *                                              -gamma if counts[e] > k T / E, 0 otherwise.
+ * Section 六: the running per-expert totals accumulate every step's counts.
+ * Either output may be NULL. */
+void orc_expert_feedback(int E, int T, int K, const int32_t *counts, float gamma, float *bias, int64_t *totals)
+{
+    const double mean = (double)K * (double)T / (double)E;
+    for (int e = 0; e < E; ++e) {
+        if (totals)
+            totals[e] += counts[e];
+        if (bias) {
+            float step = 0.0f;
+            if ((double)counts[e] < mean)
+                step = gamma;
+            else if ((double)counts[e] > mean)
+                step = -gamma;
+            bias[e] = bias[e] + step;
+        }
+    }
+}

@@ -129,3 +129,21 @@ def test_route_launch_count(T, kernels):
     assert moe.last_launch_count() == kernels
     moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=True)
     assert moe.last_launch_count() == kernels + 1   # + the balance-loss reduction
+
+
+def test_expert_feedback_matches_oracle():
+    w0 = wl.WORKLOADS[4].with_T(4096)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=4096)
+    idx, w, counts, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    bias = d["expert_bias"].clone()
+    totals = torch.arange(256, dtype=torch.int64, device=DEV)
+    moe.expert_feedback(cfg, counts, 1e-3, bias, totals)
+    torch.cuda.synchronize()
+    ref_b, ref_t = oracle.expert_feedback(counts.cpu().numpy(), 4096, 8, 1e-3,
+                                          bias=d["expert_bias"].cpu().numpy(), totals=np.arange(256))
+    assert np.array_equal(bias.cpu().numpy(), ref_b)
+    assert np.array_equal(totals.cpu().numpy(), ref_t)
+    # the hot experts of this workload get their bias lowered
+    hot = wl.hot_experts(w0).numpy()
+    assert (bias.cpu().numpy()[hot] < d["expert_bias"].cpu().numpy()[hot]).all()

@@ -410,3 +410,29 @@ def test_rmsnorm_matches_numpy():
     # the oracle rounds once to bf16: within half a bf16 ulp (2^-9 relative)
     assert np.all(np.abs(ours - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-30)
     np.testing.assert_allclose(np.sqrt((ours ** 2).mean(axis=1)), 1.0, atol=1e-2)
+
+
+# ------------------------------------------------------ bias feedback (NEXT)
+
+def test_expert_feedback_moves_bias_toward_balance():
+    """Routing article §三: cold experts are raised, hot ones lowered; an
+    expert at exactly the balanced load k T / E is left alone; totals add up."""
+    E, T, k, g = 8, 4, 2, 0.001
+    counts = np.array([0, 1, 2, 3, 1, 1, 0, 0], dtype=np.int32)   # sum = 8 = k T, mean = 1
+    bias = np.linspace(-0.1, 0.1, E).astype(np.float32)
+    nb, tot = oracle.expert_feedback(counts, T, k, g, bias=bias, totals=np.arange(E))
+    step = nb.astype(np.float64) - bias.astype(np.float64)
+    assert np.all(step[counts < 1] > 0) and np.all(step[counts > 1] < 0) and np.all(step[counts == 1] == 0)
+    np.testing.assert_allclose(np.abs(step[counts != 1]), g, rtol=1e-5)
+    assert np.array_equal(tot, np.arange(E) + counts)
+    # perfectly balanced counts leave the bias unchanged
+    nb2, _ = oracle.expert_feedback(np.full(E, 1, np.int32), T, k, g, bias=bias)
+    assert np.array_equal(nb2, bias)
+    # repeated feedback on a routed batch lowers the most-hit expert's bias
+    rng = np.random.default_rng(19)
+    L = rng.standard_normal((256, 256)).astype(np.float32)
+    L[:, 7] += 3.0
+    r = oracle.route(L)
+    c, _, _ = oracle.counts_aux(r["idx"])
+    nb3, _ = oracle.expert_feedback(c, 256, 8, 0.01, bias=np.zeros(256, np.float32))
+    assert nb3[7] == np.float32(-0.01) and c[7] == c.max()
