@@ -147,6 +147,14 @@ def algorithmic_work(T, H, E, I, k):
     }
 
 
+def workload_name(w0):
+    if w0.wid == 4:
+        return "T=%d full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)" % w0.T
+    if w0.wid == 5:
+        return "%d-layer stack (x + moe(rmsnorm(x))), T=%d, full size" % (w0.layers, w0.T)
+    return "%s (T=%d)" % (w0.name, w0.T)
+
+
 def init_dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -180,14 +188,15 @@ class CpuSample:
     """The workload's inputs on the host (drawn once) and a timer of the CPU
     oracle -- router logits, routing and expert stage -- on its first n tokens."""
 
-    def __init__(self, threads: int = 0):
+    def __init__(self, workload: int = WORKLOAD_ID, threads: int = 0):
         import oracle
         from group_limited_routing_gb300 import workloads as wl
 
         self.oracle = oracle
         if threads:
             oracle.set_threads(threads)
-        w0 = wl.WORKLOADS[WORKLOAD_ID]
+        w0 = wl.WORKLOADS[workload]
+        self.layers = w0.layers     # a stack is timed on its first layer: rate / layers
 
         def u16(t):
             return t.contiguous().view(torch.int16).numpy().view(np.uint16)
@@ -208,24 +217,37 @@ class CpuSample:
         r = o.route(L, bias=self.b)
         o.experts(xs, self.gu, self.dn, self.sgu, self.sd, r["idx"], r["w"])
         dt = time.perf_counter() - t0
-        return n_tokens / dt, o.max_threads(), dt
+        return n_tokens / dt / self.layers, o.max_threads(), dt
 
 
 # ------------------------------------------------------------------- ours
+def build_model(w0, dev):
+    """The step's model: one MoE layer, or the 19-layer stack of workload 5."""
+    from group_limited_routing_gb300 import moe, workloads as wl
+
+    cfg = moe.MoeConfig(T=w0.T, H=w0.H, E=w0.E, n_group=w0.n_group, topk_group=w0.topk_group, k=w0.k, I=w0.I,
+                        Is=w0.Is)
+    ws_r = moe.Workspace(cfg, 0, dev)
+    ws_f = moe.Workspace(cfg, 1, dev)
+    layers = []
+    for layer in range(w0.layers):
+        d = wl.layer_inputs(w0, dev, layer=layer)
+        layers.append(moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
+                                   d["shared_gate_up"], d["shared_down"], ws_route=ws_r, ws_fwd=ws_f))
+    return cfg, (moe.MoEStack(layers) if w0.layers > 1 else layers[0])
+
+
 def run_ours(args, world, rank, local):
     from group_limited_routing_gb300 import moe, workloads as wl
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w0 = wl.WORKLOADS[WORKLOAD_ID]
+    w0 = wl.WORKLOADS[args.workload]
     if args.tokens:
         w0 = w0.with_T(args.tokens)
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
-    cfg = moe.MoeConfig(T=T, H=H, E=E, n_group=w0.n_group, topk_group=w0.topk_group, k=k, I=I, Is=w0.Is)
-    d = wl.layer_inputs(w0, dev)
-    x = wl.hidden(w0, dev, layer=rank) if rank else d["hidden"]   # each replica its own batch
-    layer = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
-                         d["shared_gate_up"], d["shared_down"])
+    cfg, layer = build_model(w0, dev)
+    x = wl.hidden(w0, dev, layer=rank)      # each replica its own batch
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -272,7 +294,7 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return None
-    return report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk)
+    return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk)
 
 
 def time_e2e(args, world, layer, x, out, stream, dev):
@@ -301,6 +323,7 @@ def time_e2e(args, world, layer, x, out, stream, dev):
 
 
 def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
+    """nprof = layer-steps profiled (steps x layers): per-stage numbers are per layer."""
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
     pk = peaks()
     work = algorithmic_work(T, H, E, I, k)
@@ -351,10 +374,12 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": "T=%d full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)" % T,
+        "config": {"workload": workload_name(w0),
                    "T_per_gpu": T, "hidden": H, "experts": E, "groups": w0.n_group, "topk_group": w0.topk_group,
-                   "k": k, "inter": I, "shared_inter": w0.Is, "parallelism": "replicas (dp%d)" % world,
-                   "l2": "inputs larger than L2 (1.61 GB expert weights + 134 MB hidden per step), no flush"},
+                   "k": k, "inter": I, "shared_inter": w0.Is, "layers": w0.layers,
+                   "parallelism": "replicas (dp%d)" % world,
+                   "l2": "expert weights (%.2f GB per layer) larger than L2, no flush" % (
+                       3 * E * I * H * 2 / 1e9)},
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": "tensor", "achieved": round(g1_tf, 1),
                      "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": round(g1_tf / pk["bf16_sustained"], 4),
@@ -370,10 +395,13 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        tps, thr, secs = CpuSample().run(args.cpu_tokens)
+        tps, thr, secs = CpuSample(args.workload).run(args.cpu_tokens)
         line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": "first %d tokens of the workload: router logits, routing and expert "
-                                          "stage (%.1f s)" % (args.cpu_tokens, secs)}
+                                          "stage (%.1f s)%s" % (
+                                              args.cpu_tokens, secs,
+                                              "" if w0.layers == 1 else
+                                              ", layer 0 only, rate divided by %d layers" % w0.layers)}
     return line
 
 
@@ -381,7 +409,10 @@ def run_reference(args, world, rank):
     """The CPU oracle as it stands, on the host cores, one bounded sample per step."""
     if rank != 0:
         return None
-    sample = CpuSample()
+    from group_limited_routing_gb300 import workloads as wl
+
+    w0 = wl.WORKLOADS[args.workload]
+    sample = CpuSample(args.workload)
     for _ in range(args.warmup):
         sample.run(args.ref_tokens)
     secs = 0.0
@@ -389,7 +420,7 @@ def run_reference(args, world, rank):
     for _ in range(args.steps):
         _, thr, dt = sample.run(args.ref_tokens)
         secs += dt
-    value = args.ref_tokens * args.steps / secs
+    value = args.ref_tokens * args.steps / secs / sample.layers
     return {
         "impl": "reference",
         "metric": METRIC,
@@ -404,11 +435,11 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": "T=32768 full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)",
-                   "sample_tokens_per_step": args.ref_tokens},
+        "config": {"workload": workload_name(w0), "sample_tokens_per_step": args.ref_tokens},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
-                         "sample": "first %d tokens per step: router logits, routing and expert stage"
-                                   % args.ref_tokens},
+                         "sample": "first %d tokens per step: router logits, routing and expert stage%s"
+                                   % (args.ref_tokens, "" if w0.layers == 1 else
+                                      " (layer 0 only, rate divided by %d layers)" % w0.layers)},
         "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -419,10 +450,12 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-tokens", type=int, default=1024, help="oracle sample for cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=8192, help="oracle sample for cpu_baseline")
     ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=(1, 2, 3, 4, 5),
+                    help="1 tiny, 2 decode T=16, 3 T=4096, 4 T=32768 skewed (the bench line), 5 19-layer stack")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step (default: the workload's 32768); smaller sizes for profiling captures")
     args = ap.parse_args()

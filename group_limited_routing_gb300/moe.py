@@ -237,15 +237,15 @@ class MoELayer:
     __call__(hidden) runs moe_route then moe_forward on the current stream."""
 
     def __init__(self, cfg: MoeConfig, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
-                 aux: bool = False):
+                 aux: bool = False, ws_route: Optional[Workspace] = None, ws_fwd: Optional[Workspace] = None):
         self.cfg = cfg
         self.W_router, self.expert_bias = W_router, expert_bias
         self.W_gate_up, self.W_down = W_gate_up, W_down
         self.shared_gate_up, self.shared_down = shared_gate_up, shared_down
         self.aux = aux
-        dev = W_router.device
-        self.ws_route = Workspace(cfg, _lib.MOE_WS_ROUTE, dev)
-        self.ws_fwd = Workspace(cfg, _lib.MOE_WS_FORWARD, dev)
+        self.device = W_router.device
+        self.ws_route = ws_route or Workspace(cfg, _lib.MOE_WS_ROUTE, self.device)
+        self.ws_fwd = ws_fwd or Workspace(cfg, _lib.MOE_WS_FORWARD, self.device)
         self.routing = None
         self.last_launches = 0
 
@@ -272,8 +272,40 @@ class MoELayer:
         expert_feedback(self.cfg, self.routing[2], gamma, self.expert_bias, totals)
 
 
+class MoEStack:
+    """Decoder-style stack of MoE layers (the routing article's layout after
+    its dense first layer): x <- x + layer(rmsnorm(x)) for every layer, all
+    layers sharing one pair of workspaces.  __call__(hidden, out=None) runs the
+    whole stack on the current stream."""
+
+    def __init__(self, layers, eps: float = 1e-6):
+        self.layers = list(layers)
+        self.cfg = self.layers[0].cfg
+        self.device = self.layers[0].device
+        self.eps = eps
+        T, H = self.cfg.T, self.cfg.H
+        self._x = [torch.empty(T, H, dtype=torch.bfloat16, device=self.device) for _ in range(2)]
+        self._norm = torch.empty(T, H, dtype=torch.bfloat16, device=self.device)
+        self.last_launches = 0
+
+    def __call__(self, hidden, out=None):
+        n = 0
+        x = hidden
+        for i, layer in enumerate(self.layers):
+            rmsnorm(x, self.eps, out=self._norm)
+            dst = out if (out is not None and i == len(self.layers) - 1) else self._x[i % 2]
+            layer(self._norm, residual=x, out=dst)
+            n += 1 + layer.last_launches
+            x = dst
+        self.last_launches = n
+        return x
+
+    def status(self) -> int:
+        return self.layers[0].ws_route.status() | self.layers[0].ws_fwd.status()
+
+
 class HostPipeline:
-    """Runs a MoELayer over batches that live in (pinned) host memory.
+    """Runs a MoELayer (or MoEStack) over batches that live in (pinned) host memory.
 
     Every batch is copied host -> device, run through the layer, and its
     output copied device -> host.  The copies run on their own streams with two
@@ -281,9 +313,9 @@ class HostPipeline:
     of batch i-1 overlap the layer's kernels on batch i; the layer itself runs
     on the caller's current stream, one batch after the other."""
 
-    def __init__(self, layer: "MoELayer", depth: int = 2):
+    def __init__(self, layer, depth: int = 2):
         cfg = layer.cfg
-        dev = layer.W_router.device
+        dev = layer.device
         self.layer = layer
         self.depth = depth
         self.x_dev = [torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev) for _ in range(depth)]

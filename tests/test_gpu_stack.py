@@ -80,3 +80,38 @@ def test_rmsnorm_matches_oracle():
     # both round once to bf16 (fp32 vs double before it): at most one bf16 step apart
     assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -7 + 1e-30)
     assert (got != ref).mean() < 0.01
+
+
+def test_moe_stack_object_matches_layer_loop():
+    """MoEStack (shared workspaces, ping-pong buffers) computes exactly what the
+    layer-by-layer loop above computes: same kernels, deterministic, so bit-equal;
+    HostPipeline over the stack gives the same bytes again."""
+    w0 = wl.WORKLOADS[5].with_T(1000)
+    cfg = moe.MoeConfig(T=w0.T, H=w0.H, I=w0.I, Is=w0.Is)
+    ws_r = moe.Workspace(cfg, 0, DEV)
+    ws_f = moe.Workspace(cfg, 1, DEV)
+    layers = []
+    for layer in range(3):
+        d = wl.layer_inputs(w0, DEV, layer=layer)
+        layers.append(moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
+                                   d["shared_gate_up"], d["shared_down"], ws_route=ws_r, ws_fwd=ws_f))
+    stack = moe.MoEStack(layers)
+    x = wl.hidden(w0, DEV)
+    y = torch.empty_like(x)
+    got = stack(x, out=y)
+    assert got.data_ptr() == y.data_ptr()
+    assert stack.last_launches == sum(1 + L.last_launches for L in layers)
+    ref = x
+    for L in layers:
+        ref = L(moe.rmsnorm(ref), residual=ref)
+    torch.cuda.synchronize()
+    assert stack.status() == 0
+    assert torch.equal(y, ref)
+
+    xh = x.cpu().pin_memory()
+    outs = [torch.empty_like(xh).pin_memory() for _ in range(3)]
+    pipe = moe.HostPipeline(stack)
+    pipe.run([xh] * 3, outs)
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o, ref.cpu())
