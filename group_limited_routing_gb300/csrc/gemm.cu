@@ -391,6 +391,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    // the prologue above overlaps the previous kernel's teardown; its outputs
+    // (the tile list, A rows) are read only after this
+    pdl_wait();
 
     const int num_tiles = ROUTER ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
     const unsigned long long limit = p.wait_limit_ns ? p.wait_limit_ns : WAIT_LIMIT_NS;
@@ -552,7 +555,10 @@ static cudaError_t launch_kind(const GemmParams &p, int grid, cudaStream_t s)
             return e;
         configured_device = dev;
     }
-    umma_gemm_kernel<KIND><<<grid, GEMM_THREADS, GemmLayout<KIND>::SMEM, s>>>(p);
+    const cudaError_t le = launch_pdl(umma_gemm_kernel<KIND>, dim3(grid), dim3(GEMM_THREADS),
+                                      (size_t)GemmLayout<KIND>::SMEM, s, p);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 

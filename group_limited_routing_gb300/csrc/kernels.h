@@ -6,7 +6,41 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace glr {
+
+// ---- programmatic dependent launch ------------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialisation and starts with pdl_wait(), which returns once the kernel
+// before it in the stream has completed and its writes are visible -- before
+// any global memory is touched.  No kernel triggers its dependents early, so
+// the next kernel is launched when this one finishes, but its launch
+// processing and (for the GEMMs) its prologue overlap this one's teardown.
+// (Triggering at the start of each CTA was measured slower: the dependents'
+// waiting CTAs then sit beside the running ones.)  Since every kernel waits,
+// completion stays ordered along the whole stream.
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---- sizes shared by the host layer and the kernels -------------------------
 constexpr int ROUTE_CHUNK = 32;    // tokens per block of the routing kernel (4 per warp)

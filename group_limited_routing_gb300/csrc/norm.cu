@@ -14,6 +14,7 @@ namespace glr {
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ out,
                                                       int T, int H, float eps)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= T)
@@ -53,7 +54,9 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *__restrict
 cudaError_t launch_rmsnorm(const uint16_t *x, uint16_t *out, int T, int H, float eps, cudaStream_t s)
 {
     const int blocks = (T + 7) / 8;
-    rmsnorm_kernel<<<blocks, 256, 0, s>>>(x, out, T, H, eps);
+    const cudaError_t le = launch_pdl(rmsnorm_kernel, dim3(blocks), dim3(256), 0, s, x, out, T, H, eps);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 

@@ -27,6 +27,7 @@ namespace glr {
 __global__ void __launch_bounds__(256) bucket_hist_kernel(const int32_t *__restrict__ idx, int T, int E, int K,
                                                           int32_t *__restrict__ hist, int *__restrict__ status)
 {
+    pdl_wait();
     extern __shared__ int sh[];
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         sh[e] = 0;
@@ -50,7 +51,10 @@ __global__ void __launch_bounds__(256) bucket_hist_kernel(const int32_t *__restr
 cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status, cudaStream_t s)
 {
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
-    bucket_hist_kernel<<<blocks, 256, E * sizeof(int), s>>>(idx, T, E, k, hist, status);
+    const cudaError_t le = launch_pdl(bucket_hist_kernel, dim3(blocks), dim3(256), E * sizeof(int), s, idx, T, E, k,
+                                      hist, status);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 
@@ -62,6 +66,7 @@ cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t 
 __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ hist, int nchunk, int E,
                                                           int32_t *__restrict__ sizes)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (e >= E)
@@ -88,7 +93,9 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ 
 
 cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s)
 {
-    bucket_scan_kernel<<<(E + 7) / 8, 256, 0, s>>>(hist, nchunk, E, sizes);
+    const cudaError_t le = launch_pdl(bucket_scan_kernel, dim3((E + 7) / 8), dim3(256), 0, s, hist, nchunk, E, sizes);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 
@@ -164,6 +171,7 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
                                                              uint16_t *__restrict__ x_perm, int4 *__restrict__ mtiles,
                                                              WsHeader *__restrict__ hdr)
 {
+    pdl_wait();
     __shared__ int offset[258];
     __shared__ int tstart[258];
     __shared__ int wsum_rows[8];
@@ -238,8 +246,10 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
 {
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
-    bucket_scatter_kernel<<<blocks, 256, smem, s>>>(idx, x, chunk_base, sizes, T, H, E, k, slot_of, x_perm, mtiles,
-                                                    hdr);
+    const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
+                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 
@@ -370,6 +380,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                                                       const uint16_t *__restrict__ residual, int T, int H, int K,
                                                       uint16_t *__restrict__ out)
 {
+    pdl_wait();
     __shared__ int s_slot[COMBINE_TOK * 32];
     __shared__ float s_w[COMBINE_TOK * 32];
     const int vpr = H / 8;                                   // 16-byte vectors per row
@@ -406,7 +417,10 @@ cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const floa
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int nchunks = (T + COMBINE_TOK - 1) / COMBINE_TOK;
     const int blocks = min(nchunks, sms * 8);
-    combine_kernel<<<blocks, 256, 0, s>>>(Y, slot_of, w, residual, T, H, k, out);
+    const cudaError_t le = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, Y, slot_of, w, residual, T, H, k,
+                                      out);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 

@@ -31,6 +31,7 @@ namespace glr {
 __global__ void split_router_kernel(const float *__restrict__ W, uint16_t *__restrict__ W3, int n,
                                     int32_t *__restrict__ counts, int E)
 {
+    pdl_wait();
     if (blockIdx.x == 0)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             counts[e] = 0;
@@ -51,7 +52,10 @@ cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, int3
 {
     const int n = E * H;
     const int blocks = min((n + 255) / 256, 4096);
-    split_router_kernel<<<blocks, 256, 0, s>>>(W, W3, n, counts, counts ? E : 0);
+    const cudaError_t le = launch_pdl(split_router_kernel, dim3(blocks), dim3(256), 0, s, W, W3, n, counts,
+                                      counts ? E : 0);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 
@@ -69,6 +73,7 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const uint16_t *__rest
                                                           const float *__restrict__ W, int T, int E, int H,
                                                           float *__restrict__ logits, int32_t *__restrict__ counts)
 {
+    pdl_wait();
     if (blockIdx.x == 0 && blockIdx.y == 0 && counts)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             counts[e] = 0;
@@ -123,7 +128,9 @@ cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, 
                                int32_t *counts, cudaStream_t s)
 {
     const dim3 grid((E + 7) / 8, (T + SIMT_TOK - 1) / SIMT_TOK);
-    router_simt_kernel<<<grid, 256, 0, s>>>(x, W, T, E, H, logits, counts);
+    const cudaError_t le = launch_pdl(router_simt_kernel, dim3(grid), dim3(256), 0, s, x, W, T, E, H, logits, counts);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 
@@ -158,6 +165,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     float *__restrict__ ppart, int *__restrict__ status)
 {
+    pdl_wait();
     constexpr int E = 32 * G;
     constexpr unsigned FULL = 0xffffffffu;
     __shared__ int sh_hist[E];
@@ -298,11 +306,14 @@ cudaError_t launch_route_select(const float *logits, const float *bias, int T, i
                                 int *status, cudaStream_t s)
 {
     const int blocks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
-#define GLR_ROUTE_CASE(GG)                                                                                  \
-    case GG:                                                                                                \
-        route_select_kernel<GG><<<blocks, 256, 0, s>>>(logits, bias, T, topk_group, k, rsf, eps, idx, w,   \
-                                                       counts, ppart, status);                              \
-        break;
+#define GLR_ROUTE_CASE(GG)                                                                                   \
+    case GG: {                                                                                               \
+        const cudaError_t le = launch_pdl(route_select_kernel<GG>, dim3(blocks), dim3(256), 0, s, logits, bias, \
+                                          T, topk_group, k, rsf, eps, idx, w, counts, ppart, status);          \
+        if (le != cudaSuccess)                                                                               \
+            return le;                                                                                       \
+        break;                                                                                               \
+    }
     switch (n_group) {
         GLR_ROUTE_CASE(1)
         GLR_ROUTE_CASE(2)
@@ -333,6 +344,7 @@ __global__ void __launch_bounds__(FIN_WARPS * 32) route_finalize_kernel(const in
                                                                          int T, int E, int K, float *__restrict__ aux_P,
                                                                          float *__restrict__ aux_loss)
 {
+    pdl_wait();
     __shared__ float sp[FIN_WARPS][MAX_GROUPS * 32];
     __shared__ double red[FIN_WARPS];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -381,7 +393,10 @@ __global__ void __launch_bounds__(FIN_WARPS * 32) route_finalize_kernel(const in
 cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int nchunk, int T, int E, int k,
                                   float *aux_P, float *aux_loss, cudaStream_t s)
 {
-    route_finalize_kernel<<<1, FIN_WARPS * 32, 0, s>>>(counts, ppart, nchunk, T, E, k, aux_P, aux_loss);
+    const cudaError_t le = launch_pdl(route_finalize_kernel, dim3(1), dim3(FIN_WARPS * 32), 0, s, counts, ppart,
+                                      nchunk, T, E, k, aux_P, aux_loss);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 
@@ -393,6 +408,7 @@ cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int
 __global__ void expert_feedback_kernel(const int32_t *__restrict__ counts, int E, double mean, float gamma,
                                        float *__restrict__ bias, long long *__restrict__ totals)
 {
+    pdl_wait();
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= E)
         return;
@@ -408,7 +424,10 @@ __global__ void expert_feedback_kernel(const int32_t *__restrict__ counts, int E
 cudaError_t launch_expert_feedback(const int32_t *counts, int E, int T, int k, float gamma, float *bias,
                                    long long *totals, cudaStream_t s)
 {
-    expert_feedback_kernel<<<(E + 255) / 256, 256, 0, s>>>(counts, E, (double)k * T / E, gamma, bias, totals);
+    const cudaError_t le = launch_pdl(expert_feedback_kernel, dim3((E + 255) / 256), dim3(256), 0, s, counts, E,
+                                      (double)k * T / E, gamma, bias, totals);
+    if (le != cudaSuccess)
+        return le;
     return cudaPeekAtLastError();
 }
 
