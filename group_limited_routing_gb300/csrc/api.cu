@@ -441,11 +441,15 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of, xperm,
                                                   mtiles, hdr, s));
 
-    // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E)
+    // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E);
+    // for T <= GEMM_SMALL_T no bucket has more than T rows: the small kinds
+    // load only that many A rows per stage and keep more weights in flight
+    const bool small = c.T <= GEMM_SMALL_T;
+    const int a_rows = small ? GEMM_SMALL_T : GEMM_BM;
     GemmParams p1;
     memset(&p1, 0, sizeof(p1));
-    if (!make_map_bf16(&p1.tmA0, xperm, kT, c.H, GEMM_BK, GEMM_BM) ||
-        !make_map_bf16(&p1.tmA1, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
+    if (!make_map_bf16(&p1.tmA0, xperm, kT, c.H, GEMM_BK, a_rows) ||
+        !make_map_bf16(&p1.tmA1, hidden, c.T, c.H, GEMM_BK, a_rows) ||
         !make_map_bf16(&p1.tmB0, W_gate_up, 2ull * c.I * c.E, c.H, GEMM_BK, 128) ||
         !make_map_bf16(&p1.tmB1, shared_gate_up, 2ull * c.I, c.H, GEMM_BK, 128))
         return MOE_ERR_CUDA;
@@ -467,12 +471,13 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
         p1.inject_withhold = 1;
         p1.wait_limit_ns = 50000000ull;
     }
-    GLR_LAUNCH(KID_GEMM_GATE_UP, launch_gemm(GK_GATE_UP, p1, std::min(sms, L.max_mtiles * p1.n_tiles), s));
+    GLR_LAUNCH(KID_GEMM_GATE_UP, launch_gemm(small ? GK_GATE_UP_SMALL : GK_GATE_UP, p1,
+                                             std::min(sms, L.max_mtiles * p1.n_tiles), s));
 
     // grouped down GEMM (W_down stacked [E, I, H]: an MN-major B operand)
     GemmParams p2;
     memset(&p2, 0, sizeof(p2));
-    if (!make_map_bf16(&p2.tmA0, aint, kT + c.T, c.I, GEMM_BK, GEMM_BM) ||
+    if (!make_map_bf16(&p2.tmA0, aint, kT + c.T, c.I, GEMM_BK, a_rows) ||
         !make_map_bf16(&p2.tmB0, W_down, (uint64_t)c.I * c.E, c.H, 64, GEMM_BK) ||
         !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, 64, GEMM_BK))
         return MOE_ERR_CUDA;
@@ -490,7 +495,8 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     p2.kT = (int)kT;
     p2.ld_out = c.H;
     p2.status = &hdr->status;
-    GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(GK_DOWN, p2, std::min(sms, L.max_mtiles * p2.n_tiles), s));
+    GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(small ? GK_DOWN_SMALL : GK_DOWN, p2,
+                                          std::min(sms, L.max_mtiles * p2.n_tiles), s));
 
     // weighted combine + shared expert (+ residual), one rounding to bf16
     GLR_LAUNCH(KID_COMBINE, launch_combine(y, slot_of, topk_w, residual, c.T, c.H, c.k, out, s));

@@ -40,6 +40,12 @@ namespace glr {
 template <int KIND>
 struct GemmCfg;
 
+// the product a kind computes (the _SMALL kinds differ only in staging)
+__host__ __device__ constexpr int base_kind(int kind)
+{
+    return kind == GK_GATE_UP_SMALL ? GK_GATE_UP : kind == GK_DOWN_SMALL ? GK_DOWN : kind;
+}
+
 template <>
 struct GemmCfg<GK_ROUTER> {
     static constexpr int BN = 128;                     // experts per tile
@@ -50,6 +56,8 @@ struct GemmCfg<GK_ROUTER> {
     static constexpr int SLOTS = 4;                    // one slot per K block in flight
     static constexpr int TMEM_COLS = SLOTS * BN;       // 512
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
+    static constexpr int A_ROWS = GEMM_BM;
+    static constexpr int NBUF = 1;
 };
 
 template <>
@@ -62,6 +70,8 @@ struct GemmCfg<GK_GATE_UP> {
     static constexpr int SLOTS = 2;
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
+    static constexpr int A_ROWS = GEMM_BM;             // A rows loaded per stage
+    static constexpr int NBUF = 2;                     // staging buffers per epilogue warp
 };
 
 template <>
@@ -74,7 +84,29 @@ struct GemmCfg<GK_DOWN> {
     static constexpr int SLOTS = 2;
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, true);
+    static constexpr int A_ROWS = GEMM_BM;
+    static constexpr int NBUF = 2;
 };
+
+// Small-T kinds: only GEMM_SMALL_T A rows per stage (2 KB); the MMA still
+// reads 128 rows, the rest alias the stage's B bytes and only feed
+// accumulator rows that are never stored.  Six stages of 34 KB keep 192 KB of
+// weights in flight per SM instead of 128 KB (decode streams the hit experts'
+// weights and nothing else); one staging buffer per epilogue warp, since at
+// most one warp has rows to store.
+template <int BASE>
+struct GemmCfgSmall : GemmCfg<BASE> {
+    static constexpr int A_ROWS = GEMM_SMALL_T;
+    static constexpr int A_BYTES = A_ROWS * GEMM_BK * 2;
+    static constexpr int STAGES = 6;
+    static constexpr int NBUF = 1;
+};
+
+template <>
+struct GemmCfg<GK_GATE_UP_SMALL> : GemmCfgSmall<GK_GATE_UP> {};
+
+template <>
+struct GemmCfg<GK_DOWN_SMALL> : GemmCfgSmall<GK_DOWN> {};
 
 template <int KIND>
 struct GemmLayout {
@@ -82,10 +114,12 @@ struct GemmLayout {
     static constexpr int STAGE_BYTES = C::A_BYTES + C::B_BYTES;
     // per epilogue warp, 32 rows x 128 B: one buffer for the router, two for
     // the grouped GEMMs (a TMA store can drain one while the other is filled)
-    static constexpr int STAGING = (KIND == GK_ROUTER ? 1 : 2) * 4 * 4096;
+    static constexpr int STAGING = C::NBUF * 4 * 4096;
     // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin
     static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1;
     static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16;
+    static_assert(SMEM <= 232448, "more than 227 KB of shared memory");
+    static_assert(C::A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms need 1024-B alignment");
 };
 
 struct TileInfo {
@@ -102,7 +136,8 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
 {
     TileInfo ti;
     ti.nt = tile % p.n_tiles;
-    if (KIND == GK_ROUTER) {
+    constexpr int BASE = base_kind(KIND);
+    if (BASE == GK_ROUTER) {
         ti.a_row = (tile / p.n_tiles) * GEMM_BM;
         ti.out_row = ti.a_row;
         ti.rows = min(GEMM_BM, p.T - ti.a_row);
@@ -113,7 +148,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
         ti.group = m.x;
         ti.shared = (m.x == p.E);
         ti.rows = m.z;
-        if (KIND == GK_GATE_UP) {
+        if (BASE == GK_GATE_UP) {
             ti.a_row = m.y;                               // X_perm slot, or token for the shared expert
             ti.out_row = ti.shared ? p.kT + m.y : m.y;
         } else {
@@ -129,13 +164,14 @@ __device__ __forceinline__ void issue_loads(const GemmParams &p, const TileInfo 
                                             uint32_t sB, uint32_t bar)
 {
     using C = GemmCfg<KIND>;
+    constexpr int BASE = base_kind(KIND);
     const int k0 = kb * GEMM_BK;
-    if constexpr (KIND == GK_ROUTER) {
+    if constexpr (BASE == GK_ROUTER) {
         tma_load_2d(sA, &p.tmA0, bar, k0, ti.a_row);
 #pragma unroll
         for (int s = 0; s < 3; ++s)
             tma_load_2d(sB + s * C::B_PART, &p.tmB0, bar, k0, s * p.E + ti.nt * C::BN);
-    } else if constexpr (KIND == GK_GATE_UP) {
+    } else if constexpr (BASE == GK_GATE_UP) {
         const CUtensorMap *ma = ti.shared ? &p.tmA1 : &p.tmA0;
         const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
         const int wrow = (ti.shared ? 0 : ti.group * 2 * p.I) + ti.nt * 128;
@@ -160,12 +196,13 @@ __device__ __forceinline__ void issue_mmas(uint32_t sA, uint32_t sB, uint32_t d,
 #pragma unroll
     for (int kk = 0; kk < GEMM_BK / 16; ++kk) {
         const uint64_t ad = sdesc_kmajor_sw128(sA + kk * 32);
-        if constexpr (KIND == GK_ROUTER) {
+        constexpr int BASE = base_kind(KIND);
+        if constexpr (BASE == GK_ROUTER) {
 #pragma unroll
             for (int s = 0; s < 3; ++s)
                 umma_bf16(d, ad, sdesc_kmajor_sw128(sB + s * C::B_PART + kk * 32), C::IDESC,
                           (acc_in || kk > 0 || s > 0) ? 1u : 0u);
-        } else if constexpr (KIND == GK_GATE_UP) {
+        } else if constexpr (BASE == GK_GATE_UP) {
             umma_bf16(d, ad, sdesc_kmajor_sw128(sB + kk * 32), C::IDESC, (acc_in || kk > 0) ? 1u : 0u);
         } else {
             // 16 K rows = two 8-row atoms = 2048 B further into each 64-wide N atom
@@ -217,6 +254,7 @@ __device__ __forceinline__ void warp_store_rows128(uint8_t *stage, const uint4 (
 // buffer (lane 0 issues it; the buffer is reused only after the store before
 // the previous one has read it).  Otherwise -- the last tile of a bucket,
 // whose other rows belong to the next expert -- the masked line-wise path.
+template <int NBUF>
 __device__ __forceinline__ void store_piece(const GemmParams &p, uint8_t *stage2, int &buf, const uint4 (&v)[8],
                                             int lane, int valid_rows, char *gbase, size_t ld_bytes, int col,
                                             int row0)
@@ -224,7 +262,7 @@ __device__ __forceinline__ void store_piece(const GemmParams &p, uint8_t *stage2
     if (valid_rows >= 32) {
         uint8_t *stage = stage2 + buf * 4096;
         if (lane == 0)
-            bulk_wait_group_read<1>();          // this buffer's previous store has left smem
+            bulk_wait_group_read<NBUF - 1>();   // this buffer's previous store has left smem
         __syncwarp();
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -235,14 +273,14 @@ __device__ __forceinline__ void store_piece(const GemmParams &p, uint8_t *stage2
             tma_store_2d(&p.tmOut, smem_u32(stage), col, row0);
             bulk_commit_group();
         }
-        buf ^= 1;
+        buf = (buf + 1) % NBUF;
     } else if (valid_rows > 0) {
         uint8_t *stage = stage2 + buf * 4096;
         if (lane == 0)
-            bulk_wait_group_read<1>();
+            bulk_wait_group_read<NBUF - 1>();
         __syncwarp();
         warp_store_rows128(stage, v, lane, gbase, ld_bytes, valid_rows);
-        buf ^= 1;
+        buf = (buf + 1) % NBUF;
     }
 }
 
@@ -254,7 +292,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
     const int valid_rows = ti.rows - quad * 32;
     const size_t ld_bytes = (size_t)p.ld_out * 2;
     const int row0 = ti.out_row + quad * 32;
-    if constexpr (KIND == GK_GATE_UP) {
+    if constexpr (base_kind(KIND) == GK_GATE_UP) {
         // TMEM columns [0,128) = gate, [128,256) = up; 64 outputs per pass
         char *gbase = static_cast<char *>(p.out) + (size_t)row0 * ld_bytes + ti.nt * 256;
 #pragma unroll 1
@@ -268,7 +306,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
             for (int i = 0; i < 32; ++i)
                 pk[i] = pack_bf16x2(silu_times(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])),
                                     silu_times(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
-            store_piece(p, stage2, buf, v, lane, valid_rows, gbase + c * 2, ld_bytes, ti.nt * 128 + c, row0);
+            store_piece<GemmCfg<KIND>::NBUF>(p, stage2, buf, v, lane, valid_rows, gbase + c * 2, ld_bytes, ti.nt * 128 + c, row0);
         }
     } else {
         char *gbase = static_cast<char *>(p.out) + (size_t)row0 * ld_bytes + ti.nt * 512;
@@ -281,7 +319,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-            store_piece(p, stage2, buf, v, lane, valid_rows, gbase + c * 2, ld_bytes, ti.nt * 256 + c, row0);
+            store_piece<GemmCfg<KIND>::NBUF>(p, stage2, buf, v, lane, valid_rows, gbase + c * 2, ld_bytes, ti.nt * 256 + c, row0);
         }
     }
 }
@@ -482,7 +520,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     } else {
         // ------------------------------------------------------------ epilogue
         const int quad = warp & 3;
-        uint8_t *stage = staging + (warp - 2) * (ROUTER ? 4096 : 8192);
+        uint8_t *stage = staging + (warp - 2) * (C::NBUF * 4096);
         int buf = 0;
         uint32_t ctr = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
@@ -529,6 +567,8 @@ int gemm_smem_bytes(int kind)
     switch (kind) {
     case GK_ROUTER: return GemmLayout<GK_ROUTER>::SMEM;
     case GK_GATE_UP: return GemmLayout<GK_GATE_UP>::SMEM;
+    case GK_GATE_UP_SMALL: return GemmLayout<GK_GATE_UP_SMALL>::SMEM;
+    case GK_DOWN_SMALL: return GemmLayout<GK_DOWN_SMALL>::SMEM;
     default: return GemmLayout<GK_DOWN>::SMEM;
     }
 }
@@ -537,7 +577,7 @@ int gemm_tmem_cols(int kind)
 {
     switch (kind) {
     case GK_ROUTER: return GemmCfg<GK_ROUTER>::TMEM_COLS;
-    case GK_GATE_UP: return GemmCfg<GK_GATE_UP>::TMEM_COLS;
+    case GK_GATE_UP: case GK_GATE_UP_SMALL: return GemmCfg<GK_GATE_UP>::TMEM_COLS;
     default: return GemmCfg<GK_DOWN>::TMEM_COLS;
     }
 }
@@ -567,6 +607,8 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
     switch (kind) {
     case GK_ROUTER: return launch_kind<GK_ROUTER>(p, grid, s);
     case GK_GATE_UP: return launch_kind<GK_GATE_UP>(p, grid, s);
+    case GK_GATE_UP_SMALL: return launch_kind<GK_GATE_UP_SMALL>(p, grid, s);
+    case GK_DOWN_SMALL: return launch_kind<GK_DOWN_SMALL>(p, grid, s);
     default: return launch_kind<GK_DOWN>(p, grid, s);
     }
 }

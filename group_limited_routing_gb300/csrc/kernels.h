@@ -63,7 +63,11 @@ struct WsHeader {
     int pad[62];
 };
 
-enum GemmKind { GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2 };
+// The _SMALL kinds are the grouped GEMMs for T <= GEMM_SMALL_T (decode): every
+// bucket then has at most T rows, so only GEMM_SMALL_T A rows are loaded per
+// stage and the smem this frees goes to a deeper weight ring.
+enum GemmKind { GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4 };
+constexpr int GEMM_SMALL_T = 16;
 
 // Parameters of the tensor-core GEMM kernels.  Tensor maps live in the
 // kernel's parameter space (__grid_constant__), so TMA reads them in place.

@@ -255,7 +255,7 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
 
 // ---------------------------------------------------------------------------
 // out[t] = bf16( Y[K*T + t] + sum_j w[t,j] * Y[slot_of[t,j]] (+ residual[t]) ),
-// fp32 accumulation in j order.  A block takes COMBINE_TOK tokens at a time:
+// fp32 accumulation in j order.  A block takes ctok <= COMBINE_TOK tokens at a time:
 // their slots and weights are loaded once into shared memory, then a thread
 // owns one 16-byte column vector (8 values) of a token and issues all of its
 // row loads before the first use.
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                                                       const int32_t *__restrict__ slot_of,
                                                       const float *__restrict__ w,
                                                       const uint16_t *__restrict__ residual, int T, int H, int K,
-                                                      uint16_t *__restrict__ out)
+                                                      int ctok, uint16_t *__restrict__ out)
 {
     pdl_wait();
     __shared__ int s_slot[COMBINE_TOK * 32];
@@ -386,10 +386,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     const int vpr = H / 8;                                   // 16-byte vectors per row
     const int rpp = max(1, (int)blockDim.x / vpr);           // tokens per pass
     const int sub = threadIdx.x / vpr, v = threadIdx.x % vpr;
-    const int nchunks = (T + COMBINE_TOK - 1) / COMBINE_TOK;
+    const int nchunks = (T + ctok - 1) / ctok;
     for (int chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
-        const int t0 = chunk * COMBINE_TOK;
-        const int nt = min(COMBINE_TOK, T - t0);
+        const int t0 = chunk * ctok;
+        const int nt = min(ctok, T - t0);
         __syncthreads();
         for (int i = threadIdx.x; i < nt * K; i += blockDim.x) {
             s_slot[i] = slot_of[(size_t)t0 * K + i];
@@ -415,10 +415,15 @@ cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const floa
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int nchunks = (T + COMBINE_TOK - 1) / COMBINE_TOK;
+    // tokens per chunk: COMBINE_TOK, halved (down to 2) until there are at
+    // least four chunks per SM, so that small batches still spread over the GPU
+    int ctok = COMBINE_TOK;
+    while (ctok > 2 && (T + ctok - 1) / ctok < 4 * sms)
+        ctok >>= 1;
+    const int nchunks = (T + ctok - 1) / ctok;
     const int blocks = min(nchunks, sms * 8);
     const cudaError_t le = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, Y, slot_of, w, residual, T, H, k,
-                                      out);
+                                      ctok, out);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

@@ -70,8 +70,9 @@ def test_forward_matches_oracle_on_workloads(wid, T, nsample):
     check(cfg, d, idx, w, tokens, what="workload %d T=%d" % (wid, T))
 
 
-@pytest.mark.parametrize("T", [1, 7, 128, 300, 1000])
+@pytest.mark.parametrize("T", [1, 7, 16, 17, 128, 300, 1000])
 def test_forward_ragged_T_random_routing(T):
+    # T <= 16 runs the small-T GEMM kinds (16 A rows per stage), 17 the others
     cfg, d = small_layer(T, seed=T % 7)
     idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=T, device=DEV)
     check(cfg, d, idx, w, what="ragged T=%d" % T)
