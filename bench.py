@@ -69,7 +69,9 @@ def gemm_traffic(kernel: str):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 100 ms; summary() keeps those taken between
+    mark('load') (start of the untimed loaded lead-in) and mark('end') (end of
+    the timed region)."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -87,7 +89,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", self.sel, "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -97,7 +99,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def mark(self, name: str) -> None:
+        """Record when the loaded window ('load') and the timed region ('end') start/finish."""
+        setattr(self, "t_" + name, time.monotonic())
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -111,7 +117,11 @@ class ClockSampler:
     def summary(self):
         sm, smax, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        t0 = getattr(self, "t_load", None)
+        t1 = getattr(self, "t_end", None)
+        for t, ln in self.lines:
+            if t0 is not None and t1 is not None and not (t0 <= t <= t1 + 0.15):
+                continue                  # only samples taken while the GPU ran the step
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -257,21 +267,46 @@ def run_ours(args, world, rank, local):
     if layer.status() != 0:
         raise RuntimeError("device status after warm-up: %d" % layer.status())
 
-    # ---- timed region: K steps, inputs resident
-    launches = 0
+    # ---- timed region: K steps, inputs resident.  It follows ~0.5 s of untimed
+    # steps so that clocks and power are in their loaded state and sampled.
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    layer(x, out=out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    lead = max(1, min(2000, int(500.0 / max(e0.elapsed_time(e1), 1e-3))))
+    flush = args.flush_l2 or w0.wid == 1
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
+    launches = 0
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        time.sleep(0.3)
-        e0.record(stream)
-        for _ in range(args.steps):
+        time.sleep(0.25)
+        clk.mark("load")
+        for _ in range(lead):
             layer(x, out=out)
-            launches += layer.last_launches
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        if flush:
+            # per-step events with a 256 MB scrub of L2 between steps (not timed)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            for a, b in evs:
+                scrub.zero_()
+                a.record(stream)
+                layer(x, out=out)
+                b.record(stream)
+                launches += layer.last_launches
+            torch.cuda.synchronize(dev)
+            ms = sum(a.elapsed_time(b) for a, b in evs) / args.steps
+        else:
+            e0.record(stream)
+            for _ in range(args.steps):
+                layer(x, out=out)
+                launches += layer.last_launches
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1) / args.steps
+        clk.mark("end")
     barrier(world)
-    ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(world, ms, dev)
     status = layer.status()
     if status != 0:
@@ -294,7 +329,13 @@ def run_ours(args, world, rank, local):
 
     if rank != 0:
         return None
-    return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk)
+    hot = wl.hot_experts(w0)
+    hot_share = None
+    if hot.numel() and getattr(layer, "routing", None) is not None:
+        counts = layer.routing[2].double().cpu()
+        hot_share = float(counts[hot].sum() / counts.sum())
+    return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk,
+                  dict(flush=flush, lead=lead, hot_share=hot_share))
 
 
 def time_e2e(args, world, layer, x, out, stream, dev):
@@ -322,7 +363,7 @@ def time_e2e(args, world, layer, x, out, stream, dev):
     return e2e_ms
 
 
-def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
+def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
     """nprof = layer-steps profiled (steps x layers): per-stage numbers are per layer."""
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
     pk = peaks()
@@ -378,8 +419,11 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
                    "T_per_gpu": T, "hidden": H, "experts": E, "groups": w0.n_group, "topk_group": w0.topk_group,
                    "k": k, "inter": I, "shared_inter": w0.Is, "layers": w0.layers,
                    "parallelism": "replicas (dp%d)" % world,
-                   "l2": "expert weights (%.2f GB per layer) larger than L2, no flush" % (
-                       3 * E * I * H * 2 / 1e9)},
+                   "l2": ("L2 scrubbed (256 MB write) between timed steps, per-step CUDA events"
+                          if extra["flush"] else
+                          "expert weights (%.2f GB per layer) larger than L2, no flush" % (3 * E * I * H * 2 / 1e9)),
+                   "untimed_lead_in_steps": extra["lead"],
+                   "hot_expert_share": None if extra["hot_share"] is None else round(extra["hot_share"], 4)},
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": "tensor", "achieved": round(g1_tf, 1),
                      "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": round(g1_tf / pk["bf16_sustained"], 4),
@@ -395,13 +439,22 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk):
         "clocks": clk.summary(),
     }
     if world == 1 and not args.no_cpu_baseline:
-        tps, thr, secs = CpuSample(args.workload).run(args.cpu_tokens)
+        sample = CpuSample(args.workload)
+        tps, thr, secs = sample.run(args.cpu_tokens)
         line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                 "sample": "first %d tokens of the workload: router logits, routing and expert "
                                           "stage (%.1f s)%s" % (
                                               args.cpu_tokens, secs,
                                               "" if w0.layers == 1 else
                                               ", layer 0 only, rate divided by %d layers" % w0.layers)}
+        if args.cpu_tokens_1t:
+            import oracle
+            oracle.set_threads(1)
+            tps1, _, secs1 = sample.run(args.cpu_tokens_1t)
+            oracle.set_threads(thr)
+            line["cpu_baseline"]["value_1thread"] = round(tps1, 2)
+            line["cpu_baseline"]["sample_1thread"] = "first %d tokens, one thread (%.1f s)" % (
+                args.cpu_tokens_1t, secs1)
     return line
 
 
@@ -454,6 +507,10 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--flush-l2", action="store_true",
+                    help="scrub L2 between timed steps (always on for workload 1, whose weights fit in L2)")
+    ap.add_argument("--cpu-tokens-1t", type=int, default=256,
+                    help="oracle sample for the single-thread CPU figure (0 = skip)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=(1, 2, 3, 4, 5),
                     help="1 tiny, 2 decode T=16, 3 T=4096, 4 T=32768 skewed (the bench line), 5 19-layer stack")
     ap.add_argument("--tokens", type=int, default=0,

@@ -34,7 +34,8 @@ MOE_WS_FORWARD = 1
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router_logits",
            "moe_route_from_logits", "moe_forward", "moe_get_status", "moe_last_launch_count",
            "moe_profile_enable", "moe_profile_read", "moe_kernel_name", "moe_strerror", "moe_route_static",
-           "moe_debug_inject_timeout", "moe_rmsnorm", "moe_expert_feedback")
+           "moe_debug_inject_timeout", "moe_rmsnorm", "moe_expert_feedback", "moe_prepare_router",
+           "moe_route_prepared")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
 MOE_KERNEL_COUNT = 10
 
@@ -79,6 +80,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.moe_workspace_init.argtypes = [P, S, P]
         lib.moe_route.argtypes = [C, P, P, P, P, P, P, P, P, P, S, P]
         lib.moe_router_logits.argtypes = [C, P, P, P, P, S, P]
+        lib.moe_prepare_router.argtypes = [C, P, P, P]
+        lib.moe_prepare_router.restype = ctypes.c_int
+        lib.moe_route_prepared.argtypes = [C, P, P, P, P, P, P, P, P, P, P, S, P]
+        lib.moe_route_prepared.restype = ctypes.c_int
         lib.moe_route_from_logits.argtypes = [C, P, P, P, P, P, P, P, P, S, P]
         lib.moe_forward.argtypes = [C, P, P, P, P, P, P, P, P, P, P, S, P]
         lib.moe_get_status.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int]

@@ -246,16 +246,24 @@ T *at(void *ws, size_t off)
     } while (0)
 
 // counts (nullable) is cleared by the split kernel, for the routing kernel after it.
-int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, float *logits, int32_t *counts,
-                void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches)
+// W_split: the bf16 x 3 split of W made by moe_prepare_router, or NULL to
+// split W into the workspace here (that launch also clears counts).
+int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split, float *logits,
+                int32_t *counts, void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches)
 {
     if (c.T <= ROUTER_SIMT_MAX_T && c.H % 4 == 0) {
         // a few token tiles cannot fill the tensor-core kernel: CUDA cores, fp32 W as is
         GLR_LAUNCH(KID_ROUTER_GEMM, launch_router_simt(hidden, W, c.T, c.E, c.H, logits, counts, s));
         return MOE_OK;
     }
-    uint16_t *W3 = at<uint16_t>(ws, L.w3);
-    GLR_LAUNCH(KID_SPLIT, launch_split_router(W, W3, c.E, c.H, counts, s));
+    const uint16_t *W3 = reinterpret_cast<const uint16_t *>(W_split);
+    if (!W3) {
+        uint16_t *W3ws = at<uint16_t>(ws, L.w3);
+        GLR_LAUNCH(KID_SPLIT, launch_split_router(W, W3ws, c.E, c.H, counts, s));
+        W3 = W3ws;
+    } else if (counts && cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s) != cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
@@ -339,8 +347,8 @@ int moe_router_logits(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W
     if ((rc = device_check(&sms)) != MOE_OK)
         return rc;
     int launches = 0;
-    rc = router_gemm(*cfg, hidden, W_router, logits, nullptr, ws, L, sms, static_cast<cudaStream_t>(stream),
-                     launches);
+    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, nullptr, ws, L, sms,
+                     static_cast<cudaStream_t>(stream), launches);
     g_last_launches = launches;
     return rc;
 }
@@ -394,7 +402,57 @@ int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     float *logits = at<float>(ws, L.logits);
-    rc = router_gemm(*cfg, hidden, W_router, logits, expert_counts, ws, L, sms, s, launches);
+    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches);
+    if (rc == MOE_OK)
+        rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
+                          launches);
+    g_last_launches = launches;
+    return rc;
+}
+
+int moe_prepare_router(const moe_cfg *cfg, const float *W_router, moe_bf16 *W_split, void *stream)
+{
+    int rc = check_route_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!W_router || !W_split)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(W_router, 4) || !aligned(W_split, 16))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    GLR_LAUNCH(KID_SPLIT, launch_split_router(W_router, reinterpret_cast<uint16_t *>(W_split), cfg->E, cfg->H,
+                                              nullptr, s));
+    g_last_launches = launches;
+    return MOE_OK;
+}
+
+int moe_route_prepared(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const moe_bf16 *W_split,
+                       const float *expert_bias, int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                       float *aux_P, float *aux_loss, void *ws, size_t ws_bytes, void *stream)
+{
+    int rc = check_route_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !W_router || !W_split || !topk_idx || !topk_w || !expert_counts)
+        return MOE_ERR_INVALID_ARG;
+    const RouteLayout L = route_layout(*cfg);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(W_router, 4) || !aligned(W_split, 16) || !aligned(expert_bias, 4) ||
+        !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(expert_counts, 4) || !aligned(aux_P, 4) ||
+        !aligned(aux_loss, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    float *logits = at<float>(ws, L.logits);
+    rc = router_gemm(*cfg, hidden, W_router, W_split, logits, expert_counts, ws, L, sms, s, launches);
     if (rc == MOE_OK)
         rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
                           launches);
@@ -676,7 +734,7 @@ int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_
         return MOE_ERR_CUDA;
     int launches = 0;
     float *logits = at<float>(ws, L.logits);
-    rc = router_gemm(*cfg, hidden, W_router, logits, expert_counts, ws, L, sms, s, launches);
+    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches);
     if (rc == MOE_OK)
         rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
                           launches);

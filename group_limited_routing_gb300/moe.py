@@ -106,14 +106,27 @@ def _ws(ws: Optional[Workspace], cfg: MoeConfig, which: int, device) -> Workspac
     return ws
 
 
+def prepare_router(cfg: MoeConfig, W_router, out=None):
+    """moe_prepare_router: the exact bf16 x 3 split of the fp32 router weight,
+    [3, E, H] bf16, for route(..., W_split=...)."""
+    dev = W_router.device
+    pw = _need(W_router, "W_router", torch.float32, (cfg.E, cfg.H), dev)
+    W_split = out if out is not None else torch.empty(3, cfg.E, cfg.H, dtype=torch.bfloat16, device=dev)
+    ps = _need(W_split, "W_split", torch.bfloat16, (3, cfg.E, cfg.H), dev)
+    _lib.check(_lib.load().moe_prepare_router(ctypes.byref(cfg.c()), pw, ps, _stream(dev)), "moe_prepare_router")
+    return W_split
+
+
 def route(cfg: MoeConfig, hidden, W_router, expert_bias=None, *, aux: bool = False,
-          ws: Optional[Workspace] = None, out=None):
-    """moe_route: (topk_idx [T,k] int32, topk_w [T,k] fp32, expert_counts [E]
+          ws: Optional[Workspace] = None, out=None, W_split=None):
+    """moe_route (or moe_route_prepared when W_split = prepare_router(W_router)
+    is given): (topk_idx [T,k] int32, topk_w [T,k] fp32, expert_counts [E]
     int32, aux_P [E] fp32 or None, aux_loss [1] fp32 or None)."""
     dev = hidden.device
     ph = _need(hidden, "hidden", torch.bfloat16, (cfg.T, cfg.H), dev)
     pw = _need(W_router, "W_router", torch.float32, (cfg.E, cfg.H), dev)
     pb = _opt(expert_bias, "expert_bias", torch.float32, (cfg.E,), dev)
+    ps = None if W_split is None else _need(W_split, "W_split", torch.bfloat16, (3, cfg.E, cfg.H), dev)
     if out is None:
         idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
         w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev)
@@ -123,11 +136,17 @@ def route(cfg: MoeConfig, hidden, W_router, expert_bias=None, *, aux: bool = Fal
     else:
         idx, w, counts, aux_P, aux_loss = out
     ws = _ws(ws, cfg, _lib.MOE_WS_ROUTE, dev)
-    rc = _lib.load().moe_route(ctypes.byref(cfg.c()), ph, pw, pb, idx.data_ptr(), w.data_ptr(), counts.data_ptr(),
-                               None if aux_P is None else aux_P.data_ptr(),
-                               None if aux_loss is None else aux_loss.data_ptr(),
-                               ws.ptr, ws.nbytes, _stream(dev))
-    _lib.check(rc, "moe_route")
+    pP = None if aux_P is None else aux_P.data_ptr()
+    pL = None if aux_loss is None else aux_loss.data_ptr()
+    lib = _lib.load()
+    if ps is None:
+        rc = lib.moe_route(ctypes.byref(cfg.c()), ph, pw, pb, idx.data_ptr(), w.data_ptr(), counts.data_ptr(),
+                           pP, pL, ws.ptr, ws.nbytes, _stream(dev))
+        _lib.check(rc, "moe_route")
+    else:
+        rc = lib.moe_route_prepared(ctypes.byref(cfg.c()), ph, pw, ps, pb, idx.data_ptr(), w.data_ptr(),
+                                    counts.data_ptr(), pP, pL, ws.ptr, ws.nbytes, _stream(dev))
+        _lib.check(rc, "moe_route_prepared")
     return idx, w, counts, aux_P, aux_loss
 
 
@@ -234,7 +253,9 @@ def profile_read(reset: bool = True) -> dict:
 class MoELayer:
     """One MoE layer: weights on the device plus its two workspaces.
 
-    __call__(hidden) runs moe_route then moe_forward on the current stream."""
+    __call__(hidden) runs moe_route then moe_forward on the current stream.
+    The router weight is split once at construction (prepare_router); call
+    prepare() again after changing W_router in place."""
 
     def __init__(self, cfg: MoeConfig, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
                  aux: bool = False, ws_route: Optional[Workspace] = None, ws_fwd: Optional[Workspace] = None):
@@ -248,10 +269,16 @@ class MoELayer:
         self.ws_fwd = ws_fwd or Workspace(cfg, _lib.MOE_WS_FORWARD, self.device)
         self.routing = None
         self.last_launches = 0
+        self.W_split = None
+        self.prepare()
+
+    def prepare(self) -> None:
+        """(Re)make the bf16 x 3 split of W_router that routing reads."""
+        self.W_split = prepare_router(self.cfg, self.W_router, out=self.W_split)
 
     def __call__(self, hidden, residual=None, out=None):
         self.routing = route(self.cfg, hidden, self.W_router, self.expert_bias, aux=self.aux, ws=self.ws_route,
-                             out=self.routing)
+                             out=self.routing, W_split=self.W_split)
         n = last_launch_count()
         idx, w = self.routing[0], self.routing[1]
         y = forward(self.cfg, hidden, self.W_gate_up, self.W_down, self.shared_gate_up, self.shared_down, idx,

@@ -118,6 +118,27 @@ int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
               int32_t *expert_counts, float *aux_P, float *aux_loss,
               void *ws, size_t ws_bytes, void *stream);
 
+/* One-time preparation of the router weight for moe_route_prepared: writes
+ * its exact bf16 x 3 split, W_split [3, E, H] bf16 (hi, mid, lo with
+ * hi + mid + lo == W_router for every normal fp32 value), on `stream`.
+ * W_router [E, H] fp32 (4-byte aligned), W_split 16-byte aligned, owned by
+ * the caller.  The routing page computes the router in fp32 (section 二 step
+ * 1); this is how the tensor-core path stays fp32-exact.  The split has no
+ * counterpart on the page: it moves the per-call split of moe_route out of the
+ * step. */
+int moe_prepare_router(const moe_cfg *cfg, const float *W_router, moe_bf16 *W_split, void *stream);
+
+/* moe_route with the weight prepared by moe_prepare_router: same outputs,
+ * bit for bit, as moe_route(cfg, hidden, W_router, ...).  W_router is still
+ * read for small T (<= 32 tokens run on the CUDA cores with the fp32 weight);
+ * W_split must hold moe_prepare_router(W_router) (a stale split gives the
+ * logits of the weight it was made from).  expert_counts is cleared with an
+ * asynchronous memset on `stream`. */
+int moe_route_prepared(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
+                       const moe_bf16 *W_split, const float *expert_bias, int32_t *topk_idx,
+                       float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss,
+                       void *ws, size_t ws_bytes, void *stream);
+
 /* The first half of moe_route alone: logits [T, E] fp32 = hidden . W_router^T
  * (routing page, section 二 step 1).  Same arguments and workspace. */
 int moe_router_logits(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,

@@ -147,3 +147,25 @@ def test_expert_feedback_matches_oracle():
     # the hot experts of this workload get their bias lowered
     hot = wl.hot_experts(w0).numpy()
     assert (bias.cpu().numpy()[hot] < d["expert_bias"].cpu().numpy()[hot]).all()
+
+
+@pytest.mark.parametrize("T", [16, 33, 1000])
+def test_prepared_router_matches_route_bit_for_bit(T):
+    """moe_prepare_router writes an exact split (hi + mid + lo == W) and
+    moe_route_prepared gives moe_route's outputs bit for bit; the prepared
+    tensor-core path launches the router GEMM and the selection only."""
+    w0 = wl.WORKLOADS[4].with_T(T)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=T)
+    W = d["W_router"]
+    W3 = moe.prepare_router(cfg, W)
+    torch.cuda.synchronize()
+    parts = W3.float().double()
+    assert torch.equal(parts[0] + parts[1] + parts[2], W.double())
+    assert torch.equal(W3[0], W.to(torch.bfloat16))                    # hi = RN(W)
+    a = moe.route(cfg, d["hidden"], W, d["expert_bias"], aux=True)
+    b = moe.route(cfg, d["hidden"], W, d["expert_bias"], aux=True, W_split=W3)
+    assert moe.last_launch_count() == 3      # router (CUDA-core or tensor-core) + select + loss
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
