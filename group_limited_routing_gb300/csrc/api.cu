@@ -150,8 +150,10 @@ FwdLayout fwd_layout(const moe_cfg &c)
     FwdLayout L;
     const size_t T = c.T, K = c.k, H = c.H, I = c.I;
     L.nchunk = (c.T + PERM_CHUNK - 1) / PERM_CHUNK;
-    // sum over buckets of ceil(n_e / 128) <= K T / 128 + E, plus the shared group
-    L.max_mtiles = (int)((K * T) / GEMM_BM + c.E + (T + GEMM_BM - 1) / GEMM_BM + 1);
+    // sum over buckets of ceil(n_e / mt) <= K T / mt + E, plus the shared group;
+    // mt = rows per m-tile (GEMM_SMALL_T for the small-T GEMM kinds)
+    const size_t mt = (c.T <= GEMM_SMALL_T) ? GEMM_SMALL_T : GEMM_BM;
+    L.max_mtiles = (int)((K * T) / mt + c.E + (T + mt - 1) / mt + 1);
     size_t off = sizeof(WsHeader);
     L.hist = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
@@ -493,11 +495,18 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     const uint64_t kT = (uint64_t)c.k * c.T;
 
     // bucket the (token, expert) pairs by expert (stable), gather rows
-    GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
     int32_t *sizes = at<int32_t>(ws, L.sizes);
-    GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
-    GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of, xperm,
-                                                  mtiles, hdr, s));
+    if (c.T <= BUCKET_SMALL_MAX_T) {
+        // a handful of tokens: the three bucketing steps in one launch
+        const int mt = c.T <= GEMM_SMALL_T ? GEMM_SMALL_T : GEMM_BM;
+        GLR_LAUNCH(KID_SCATTER, launch_bucket_small(topk_idx, hidden, c.T, c.H, c.E, c.k, mt, sizes, slot_of,
+                                                    xperm, mtiles, hdr, s));
+    } else {
+        GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
+        GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
+        GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
+                                                      xperm, mtiles, hdr, s));
+    }
 
     // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E);
     // for T <= GEMM_SMALL_T no bucket has more than T rows: the small kinds

@@ -124,6 +124,13 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
                                   const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
                                   uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s);
 
+// T <= BUCKET_SMALL_MAX_T: hist, scan and scatter in one launch (same outputs)
+constexpr int BUCKET_SMALL_MAX_T = 32;
+// (m-tiles of at most mt rows)
+cudaError_t launch_bucket_small(const int32_t *idx, const uint16_t *x, int T, int H, int E, int k, int mt,
+                                int32_t *sizes, int32_t *slot_of, uint16_t *x_perm, int4 *mtiles, WsHeader *hdr,
+                                cudaStream_t s);
+
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s);
 

@@ -254,6 +254,120 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
 }
 
 // ---------------------------------------------------------------------------
+// Small batches (T <= BUCKET_SMALL_MAX_T): the three bucketing steps in one
+// launch.  Every block recomputes the (tiny) bucketing from topk_idx in shared
+// memory -- thread e counts expert e's pairs, a block scan gives the bucket
+// offsets, then thread e walks the pairs in (token, j) order and hands out its
+// bucket's slots, so slots are stable exactly as in the general path -- and
+// copies its share of the hidden rows into X_perm; block 0 also writes the
+// bucket sizes, slot_of and the m-tile list, in tiles of at most `mt` rows
+// (16 for the small-T GEMM kinds, else 128; a bucket can exceed T rows when a
+// token lists an expert twice), then the shared group (all T tokens).
+__global__ void __launch_bounds__(256) bucket_small_kernel(const int32_t *__restrict__ idx,
+                                                           const uint16_t *__restrict__ x, int T, int H, int E,
+                                                           int K, int mt, int32_t *__restrict__ sizes,
+                                                           int32_t *__restrict__ slot_of,
+                                                           uint16_t *__restrict__ x_perm, int4 *__restrict__ mtiles,
+                                                           WsHeader *__restrict__ hdr)
+{
+    pdl_wait();
+    __shared__ int s_idx[BUCKET_SMALL_MAX_T * 32];
+    __shared__ int s_slot[BUCKET_SMALL_MAX_T * 32];
+    __shared__ int s_wsum[8][2];
+    const int n = T * K;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    bool bad = false;
+    for (int i = tid; i < n; i += blockDim.x) {
+        const int e = idx[i];
+        const bool ok = e >= 0 && e < E;
+        bad |= !ok;
+        s_idx[i] = ok ? e : -1;
+        s_slot[i] = -1;
+    }
+    __syncthreads();
+    const int e = tid;                       // blockDim.x == 256 >= E
+    int cnt = 0;
+    if (e < E)
+        for (int i = 0; i < n; ++i)
+            cnt += (s_idx[i] == e) ? 1 : 0;
+    const int ntile = (cnt + mt - 1) / mt;   // m-tiles of bucket e
+    int a = cnt, b = ntile;                  // inclusive warp scans: rows, m-tiles
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, a, off);
+        const int yb = __shfl_up_sync(0xffffffffu, b, off);
+        if (lane >= off) {
+            a += ya;
+            b += yb;
+        }
+    }
+    if (lane == 31) {
+        s_wsum[w][0] = a;
+        s_wsum[w][1] = b;
+    }
+    __syncthreads();
+    int ra = 0, rb = 0, ta = 0, tb = 0;
+    for (int q = 0; q < 8; ++q) {
+        if (q < w) {
+            ra += s_wsum[q][0];
+            rb += s_wsum[q][1];
+        }
+        ta += s_wsum[q][0];
+        tb += s_wsum[q][1];
+    }
+    const int offset = ra + a - cnt;         // first slot of bucket e
+    const int tile = rb + b - ntile;         // its first m-tile
+    if (e < E && cnt)
+        for (int i = 0, s = offset; i < n; ++i)
+            if (s_idx[i] == e)
+                s_slot[i] = s++;
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        if (e < E) {
+            sizes[e] = cnt;
+            for (int q = 0; q < ntile; ++q)
+                mtiles[tile + q] = make_int4(e, offset + q * mt, min(mt, cnt - q * mt), 0);
+        }
+        for (int i = tid; i < n; i += blockDim.x)
+            slot_of[i] = s_slot[i];
+        const int nsh = (T + mt - 1) / mt;
+        for (int q = tid; q < nsh; q += blockDim.x)
+            mtiles[tb + q] = make_int4(E, q * mt, min(mt, T - q * mt), 0);
+        if (tid == 0) {
+            hdr->num_mtiles = tb + nsh;
+            if (ta != n)
+                atomicOr(&hdr->status, ST_COUNT_MISMATCH);
+        }
+        if (__syncthreads_or(bad) && tid == 0)
+            atomicOr(&hdr->status, ST_BAD_INDEX);
+    }
+    const int vpr = H / 8;                   // 16-byte vectors per row
+    for (int i = blockIdx.x; i < n; i += gridDim.x) {
+        const int slot = s_slot[i];
+        if (slot < 0)
+            continue;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)(i / K) * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(x_perm + (size_t)slot * H);
+        for (int v = tid; v < vpr; v += blockDim.x)
+            dst[v] = src[v];
+    }
+}
+
+cudaError_t launch_bucket_small(const int32_t *idx, const uint16_t *x, int T, int H, int E, int k, int mt,
+                                int32_t *sizes, int32_t *slot_of, uint16_t *x_perm, int4 *mtiles, WsHeader *hdr,
+                                cudaStream_t s)
+{
+    if (T > BUCKET_SMALL_MAX_T || k > 32 || E > 256 || mt <= 0)
+        return cudaErrorInvalidValue;
+    const int blocks = T * k;                // one row copy per block
+    const cudaError_t le = launch_pdl(bucket_small_kernel, dim3(blocks), dim3(256), 0, s, idx, x, T, H, E, k, mt,
+                                      sizes, slot_of, x_perm, mtiles, hdr);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
 // out[t] = bf16( Y[K*T + t] + sum_j w[t,j] * Y[slot_of[t,j]] (+ residual[t]) ),
 // fp32 accumulation in j order.  A block takes ctok <= COMBINE_TOK tokens at a time:
 // their slots and weights are loaded once into shared memory, then a thread

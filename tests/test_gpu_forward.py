@@ -70,7 +70,7 @@ def test_forward_matches_oracle_on_workloads(wid, T, nsample):
     check(cfg, d, idx, w, tokens, what="workload %d T=%d" % (wid, T))
 
 
-@pytest.mark.parametrize("T", [1, 7, 16, 17, 128, 300, 1000])
+@pytest.mark.parametrize("T", [1, 7, 16, 17, 32, 33, 128, 300, 1000])
 def test_forward_ragged_T_random_routing(T):
     # T <= 16 runs the small-T GEMM kinds (16 A rows per stage), 17 the others
     cfg, d = small_layer(T, seed=T % 7)
@@ -100,8 +100,10 @@ def test_forward_bucket_sizes_and_empty_experts():
     check(cfg, d, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), what="bucket sizes")
 
 
-def test_forward_one_expert_holds_every_row():
-    T = 500
+@pytest.mark.parametrize("T", [500, 32, 16, 5])
+def test_forward_one_expert_holds_every_row(T):
+    # T <= 32: one-launch bucketing; T <= 16: 16-row m-tiles of the small GEMM
+    # kinds (a bucket of k T rows is then split into k T / 16 tiles)
     cfg, d = small_layer(T, seed=4)
     idx = torch.full((T, cfg.k), 77, dtype=torch.int32, device=DEV)   # every slot to expert 77
     w = torch.rand(T, cfg.k, device=DEV) * 0.3
@@ -144,8 +146,8 @@ def test_forward_out_may_alias_residual():
     assert torch.equal(buf, expect)
 
 
-def test_forward_bad_index_is_skipped_and_reported():
-    T = 64
+@pytest.mark.parametrize("T", [64, 16])
+def test_forward_bad_index_is_skipped_and_reported(T):
     cfg, d = small_layer(T, seed=7)
     idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=12, device=DEV)
     bad = idx.clone()
@@ -176,12 +178,13 @@ def test_forward_is_deterministic():
     assert torch.equal(a, b)
 
 
-def test_forward_launch_count():
-    T = 128
+@pytest.mark.parametrize("T,kernels", [(128, 6), (32, 4), (16, 4)])
+def test_forward_launch_count(T, kernels):
+    # hist, scan, scatter (one launch for T <= 32), gate/up GEMM, down GEMM, combine
     cfg, d = small_layer(T, seed=8)
     idx, w = wl.random_routing(T, cfg.E, cfg.k, seed=13, device=DEV)
     moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
-    assert moe.last_launch_count() == 6   # hist, scan, scatter, gate/up GEMM, down GEMM, combine
+    assert moe.last_launch_count() == kernels
 
 
 def test_host_pipeline_matches_the_layer():
