@@ -128,7 +128,7 @@ struct RouteLayout {
 RouteLayout route_layout(const moe_cfg &c)
 {
     RouteLayout L;
-    L.nchunk = (c.T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    L.nchunk = (c.T + route_chunk(c.T) - 1) / route_chunk(c.T);
     size_t off = sizeof(WsHeader);
     L.w3 = off;
     off = align_up(off + 3ull * c.E * c.H * 2, 256);

@@ -61,19 +61,23 @@ cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, int3
 
 // ---------------------------------------------------------------------------
 // Router logits for small T on the CUDA cores.  A block covers 8 experts x
-// SIMT_TOK tokens: warp w keeps 2048 columns of expert (8 bx + w)'s fp32 weight
-// row in registers (as it is, no split) and computes its dot products with
-// the block's tokens, each lane summing a strided 1/32 of the products with
-// fused multiply-adds, then one butterfly reduction per token.  Faster than
-// the tensor-core path when a handful of token tiles cannot fill the GPU.
-// Block (0, 0) also clears `counts` for the routing kernel that follows.
+// SIMT_TOK tokens: the block first stages its tokens' hidden rows in shared
+// memory while warp w loads 2048 columns of expert (8 bx + w)'s fp32 weight
+// row into registers (as it is, no split), so both loads are in flight at
+// once; then each lane sums a strided 1/32 of every token's products with
+// fused multiply-adds, and one butterfly reduction per token finishes the dot
+// product.  Faster than the tensor-core path when a handful of token tiles
+// cannot fill the GPU.  Block (0, 0) also clears `counts` for the routing
+// kernel that follows.
 constexpr int SIMT_TOK = 8;
+constexpr int SIMT_MAX_H = 2048;   // hidden rows staged in shared memory (H <= this; else H-chunks)
 
 __global__ void __launch_bounds__(256) router_simt_kernel(const uint16_t *__restrict__ x,
                                                           const float *__restrict__ W, int T, int E, int H,
                                                           float *__restrict__ logits, int32_t *__restrict__ counts)
 {
     pdl_wait();
+    __shared__ __align__(16) uint16_t xs[SIMT_TOK * SIMT_MAX_H];
     if (blockIdx.x == 0 && blockIdx.y == 0 && counts)
         for (int e = threadIdx.x; e < E; e += blockDim.x)
             counts[e] = 0;
@@ -81,29 +85,36 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const uint16_t *__rest
     const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int t0 = blockIdx.y * SIMT_TOK;
     const int nt = min(SIMT_TOK, T - t0);
-    if (e >= E || nt <= 0)
-        return;
     float acc[SIMT_TOK];
 #pragma unroll
     for (int tt = 0; tt < SIMT_TOK; ++tt)
         acc[tt] = 0.0f;
-    const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)e * H);
-    for (int h0 = 0; h0 < H / 4; h0 += 16 * 32) {             // 2048 columns per pass
-        float4 wr[16];
+    const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)min(e, E - 1) * H);
+    for (int hc = 0; hc < H; hc += SIMT_MAX_H) {              // H-chunks of at most SIMT_MAX_H columns
+        const int hw = min(SIMT_MAX_H, H - hc);
+        __syncthreads();                                     // the previous chunk's readers are done
+        const int vrow = hw / 8;                             // 16-byte vectors per staged row
+        for (int i = threadIdx.x; i < nt * vrow; i += blockDim.x) {
+            const int tt = i / vrow, v = i % vrow;
+            reinterpret_cast<uint4 *>(xs + tt * SIMT_MAX_H)[v] =
+                __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + tt) * H + hc) + v);
+        }
+        float4 wr[16];                                       // this lane's weights of the chunk
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            const int v = h0 + lane + 32 * i;
-            wr[i] = (v < H / 4) ? __ldg(w4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int v = lane + 32 * i;
+            wr[i] = (v < hw / 4) ? __ldg(w4 + hc / 4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        __syncthreads();
 #pragma unroll
         for (int tt = 0; tt < SIMT_TOK; ++tt) {
             if (tt < nt) {
-                const uint2 *x4 = reinterpret_cast<const uint2 *>(x + (size_t)(t0 + tt) * H);
+                const uint2 *x4 = reinterpret_cast<const uint2 *>(xs + tt * SIMT_MAX_H);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int v = h0 + lane + 32 * i;
-                    if (v < H / 4) {
-                        const uint2 xv = __ldg(x4 + v);
+                    const int v = lane + 32 * i;
+                    if (v < hw / 4) {
+                        const uint2 xv = x4[v];
                         acc[tt] = fmaf(__uint_as_float(xv.x << 16), wr[i].x, acc[tt]);
                         acc[tt] = fmaf(__uint_as_float(xv.x & 0xffff0000u), wr[i].y, acc[tt]);
                         acc[tt] = fmaf(__uint_as_float(xv.y << 16), wr[i].z, acc[tt]);
@@ -113,6 +124,8 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const uint16_t *__rest
             }
         }
     }
+    if (e >= E)
+        return;
 #pragma unroll
     for (int tt = 0; tt < SIMT_TOK; ++tt) {
         float a = acc[tt];
@@ -155,13 +168,14 @@ __device__ __forceinline__ float fkey_value(uint32_t k)
 // logits row is a run of 128-byte coalesced accesses.  Group maxima and the
 // top-k arg-max rounds are warp reductions (redux) on the keys above.
 //
-// Block: 8 warps, ROUTE_CHUNK tokens.  Hits per expert go to a shared-memory
+// Block: 8 warps, `chunk` tokens (route_chunk(T)).  Hits per expert go to a shared-memory
 // histogram and then to `counts` with integer atomics (exact, order-free).
 // With `ppart`, the block also writes per-expert sums of the token-normalised
 // scores of its chunk for the balance loss.
 template <int G>
 __global__ void __launch_bounds__(256) route_select_kernel(
-    const float *__restrict__ logits, const float *__restrict__ bias, int T, int TG, int K, float rsf, float eps,
+    const float *__restrict__ logits, const float *__restrict__ bias, int T, int chunk, int TG, int K, float rsf,
+    float eps,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     float *__restrict__ ppart, int *__restrict__ status)
 {
@@ -186,8 +200,8 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     __syncthreads();
 
     bool nonfinite = false;
-    const int t0 = blockIdx.x * ROUTE_CHUNK;
-    const int t1 = min(T, t0 + ROUTE_CHUNK);
+    const int t0 = blockIdx.x * chunk;
+    const int t1 = min(T, t0 + chunk);
     for (int t = t0 + warp; t < t1; t += 8) {
         const float *row = logits + (size_t)t * E;
         float s[G], b[G];
@@ -305,11 +319,12 @@ cudaError_t launch_route_select(const float *logits, const float *bias, int T, i
                                 int k, float rsf, float eps, int32_t *idx, float *w, int32_t *counts, float *ppart,
                                 int *status, cudaStream_t s)
 {
-    const int blocks = (T + ROUTE_CHUNK - 1) / ROUTE_CHUNK;
+    const int chunk = route_chunk(T);
+    const int blocks = (T + chunk - 1) / chunk;
 #define GLR_ROUTE_CASE(GG)                                                                                   \
     case GG: {                                                                                               \
         const cudaError_t le = launch_pdl(route_select_kernel<GG>, dim3(blocks), dim3(256), 0, s, logits, bias, \
-                                          T, topk_group, k, rsf, eps, idx, w, counts, ppart, status);          \
+                                          T, chunk, topk_group, k, rsf, eps, idx, w, counts, ppart, status);   \
         if (le != cudaSuccess)                                                                               \
             return le;                                                                                       \
         break;                                                                                               \
