@@ -322,6 +322,23 @@ def run_ours(args, world, rank, local):
     moe.profile_enable(False)
     prof = moe.profile_read(reset=True)
 
+    # ---- the same step replayed from a CUDA graph (no host work per step)
+    graph_ms = None
+    if not args.no_graph and not flush:
+        g = moe.GraphedStep(layer, x)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        graph_ms = max_over_ranks(world, e0.elapsed_time(e1) / args.steps, dev)
+        if g.status() != 0:
+            raise RuntimeError("device status after the graph replays: %d" % g.status())
+        del g
+
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e_ms = None
     if not args.no_e2e:
@@ -335,7 +352,7 @@ def run_ours(args, world, rank, local):
         counts = layer.routing[2].double().cpu()
         hot_share = float(counts[hot].sum() / counts.sum())
     return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk,
-                  dict(flush=flush, lead=lead, hot_share=hot_share))
+                  dict(flush=flush, lead=lead, hot_share=hot_share, graph_ms=graph_ms))
 
 
 def time_e2e(args, world, layer, x, out, stream, dev):
@@ -435,6 +452,9 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         "e2e": None if e2e_ms is None else
         {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
          "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 2},
+        "graph": None if extra["graph_ms"] is None else
+        {"ms_per_step": round(extra["graph_ms"], 4), "value": round(world * T / (extra["graph_ms"] * 1e-3), 1),
+         "unit": "tokens/s", "what": "the same step captured once in a CUDA graph and replayed (inputs resident)"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
@@ -507,6 +527,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=128, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--flush-l2", action="store_true",
                     help="scrub L2 between timed steps (always on for workload 1, whose weights fit in L2)")
     ap.add_argument("--cpu-tokens-1t", type=int, default=256,

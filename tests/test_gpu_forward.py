@@ -204,3 +204,22 @@ def test_host_pipeline_matches_the_layer():
         ref = layer(xh.to(DEV)).cpu()
         assert torch.equal(oh, ref)
     assert pipe.launches == 5 * 8      # prepared router: GEMM + select, then 6 forward kernels
+
+
+@pytest.mark.parametrize("T", [16, 1000])
+def test_graphed_step_matches_eager(T):
+    """A MoELayer step captured in a CUDA graph gives the eager step's output
+    bit for bit, replay after replay, on new inputs copied into it."""
+    w0 = wl.WORKLOADS[3].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T)
+    layer = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"], d["shared_gate_up"],
+                         d["shared_down"])
+    g = moe.GraphedStep(layer, d["hidden"])
+    for seed in range(3):
+        x = (torch.randn(T, cfg.H, device=DEV, generator=torch.Generator(DEV).manual_seed(seed))).to(torch.bfloat16)
+        ref = layer(x).clone()
+        got = g(x).clone()
+        torch.cuda.synchronize()
+        assert torch.equal(got, ref)
+    assert g.status() == 0
