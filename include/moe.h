@@ -233,8 +233,9 @@ int moe_rmsnorm(int32_t T, int32_t H, const moe_bf16 *x, moe_bf16 *out, float ep
  * pointer); clears it when reset != 0.  Returns MOE_OK, or MOE_ERR_CUDA. */
 int moe_get_status(void *ws, size_t ws_bytes, void *stream, int32_t *status, int reset);
 
-/* Number of kernels the last successful moe_route / moe_forward /
- * moe_route_from_logits / moe_router_logits call on this thread enqueued. */
+/* Number of kernels the last successful moe_route / moe_route_prepared /
+ * moe_prepare_router / moe_forward / moe_route_from_logits /
+ * moe_router_logits call on this thread enqueued (memsets not counted). */
 int moe_last_launch_count(void);
 
 /* Per-kernel timing.  While enabled, every kernel the library launches is
