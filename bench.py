@@ -140,6 +140,16 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------- work
+def dense_work(T, H, I):
+    """Algorithmic work of the dense MLP: its two GEMMs and the final copy."""
+    return {
+        "gemm_gate_up_swiglu": dict(bound="tensor", flops=2.0 * T * H * 2 * I,
+                                    bytes=T * H * 2 + 2 * I * H * 2 + T * I * 2),
+        "gemm_down": dict(bound="tensor", flops=2.0 * T * I * H, bytes=T * I * 2 + I * H * 2 + T * H * 2),
+        "combine": dict(bound="hbm", bytes=T * H * 2 * 2),
+    }
+
+
 def algorithmic_work(T, H, E, I, k):
     """Per-launch algorithmic bytes / flops of each kernel (the method's own
     work: bytes every stage must move at least once, flops of the products)."""
@@ -157,7 +167,13 @@ def algorithmic_work(T, H, E, I, k):
     }
 
 
-def workload_name(w0):
+def workload_name(w0, dense=0):
+    if dense:
+        return "dense first-layer SwiGLU MLP, T=%d, H=%d, I=%d (size assumed)" % (w0.T, w0.H, dense)
+    return workload_name_moe(w0)
+
+
+def workload_name_moe(w0):
     if w0.wid == 4:
         return "T=%d full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)" % w0.T
     if w0.wid == 5:
@@ -231,9 +247,17 @@ class CpuSample:
 
 
 # ------------------------------------------------------------------- ours
-def build_model(w0, dev):
-    """The step's model: one MoE layer, or the 19-layer stack of workload 5."""
+def build_model(w0, dev, dense_inter=0):
+    """The step's model: one MoE layer, the 19-layer stack of workload 5, or
+    (dense_inter > 0) the dense first-layer MLP of that intermediate size."""
     from group_limited_routing_gb300 import moe, workloads as wl
+
+    if dense_inter:
+        g = torch.Generator(device=dev)
+        g.manual_seed(7000 + dense_inter)
+        gu = (torch.randn(2 * dense_inter, w0.H, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        dn = (torch.randn(dense_inter, w0.H, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        return None, moe.DenseLayer(gu, dn, w0.T)
 
     cfg = moe.MoeConfig(T=w0.T, H=w0.H, E=w0.E, n_group=w0.n_group, topk_group=w0.topk_group, k=w0.k, I=w0.I,
                         Is=w0.Is)
@@ -256,7 +280,7 @@ def run_ours(args, world, rank, local):
     if args.tokens:
         w0 = w0.with_T(args.tokens)
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
-    cfg, layer = build_model(w0, dev)
+    cfg, layer = build_model(w0, dev, args.dense)
     x = wl.hidden(w0, dev, layer=rank)      # each replica its own batch
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -352,7 +376,7 @@ def run_ours(args, world, rank, local):
         counts = layer.routing[2].double().cpu()
         hot_share = float(counts[hot].sum() / counts.sum())
     return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk,
-                  dict(flush=flush, lead=lead, hot_share=hot_share, graph_ms=graph_ms))
+                  dict(flush=flush, lead=lead, hot_share=hot_share, graph_ms=graph_ms, dense=args.dense))
 
 
 def time_e2e(args, world, layer, x, out, stream, dev):
@@ -396,7 +420,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
     """nprof = layer-steps profiled (steps x layers): per-stage numbers are per layer."""
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
     pk = peaks()
-    work = algorithmic_work(T, H, E, I, k)
+    work = dense_work(T, H, extra["dense"]) if extra["dense"] else algorithmic_work(T, H, E, I, k)
     stages = {}
     for name, (tot, n) in prof.items():
         if n == 0:
@@ -418,9 +442,10 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
                 "bucket_scatter")
     rp_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in rp_names if n in stages)
     rp_bytes = T * H * 2 + E * H * 4 + T * k * 8 + T * k * 4 * 2 + T * H * 2 + k * T * H * 2
-    stages["router_plus_permute"] = {"ms": round(rp_ms, 4), "bound": "hbm",
-                                     "gbs": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
-                                     "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / pk["hbm"], 4)}
+    if rp_ms > 0:
+        stages["router_plus_permute"] = {"ms": round(rp_ms, 4), "bound": "hbm",
+                                         "gbs": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
+                                         "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / pk["hbm"], 4)}
     g1 = work["gemm_gate_up_swiglu"]
     g1_ms = prof["gemm_gate_up_swiglu"][0] / max(1, prof["gemm_gate_up_swiglu"][1])
     g1_tf = g1["flops"] / (g1_ms * 1e-3) / 1e12
@@ -444,7 +469,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": workload_name(w0),
+        "config": {"workload": workload_name(w0, extra["dense"]),
                    "T_per_gpu": T, "hidden": H, "experts": E, "groups": w0.n_group, "topk_group": w0.topk_group,
                    "k": k, "inter": I, "shared_inter": w0.Is, "layers": w0.layers,
                    "parallelism": "replicas (dp%d)" % world,
@@ -456,7 +481,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": "tensor", "achieved": round(g1_tf, 1),
                      "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": round(g1_tf / pk["bf16_sustained"], 4),
-                     "traffic": gemm_traffic("gemm_gate_up_swiglu") if T == 32768 else None,
+                     "traffic": gemm_traffic("gemm_gate_up_swiglu") if T == 32768 and not extra["dense"] else None,
                      "traffic_unit": "bytes per launch (ncu dram read + write, profiles/gemm_dram_traffic_T32768.md)",
                      "peak_kind": "%s bf16 dense, sustained" % pk["source"],
                      "algorithmic_flops_per_launch": g1["flops"]},
@@ -471,7 +496,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not extra["dense"]:
         sample = CpuSample(args.workload)
         tps, thr, secs = sample.run(args.cpu_tokens)
         line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
@@ -521,7 +546,7 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": workload_name(w0), "sample_tokens_per_step": args.ref_tokens},
+        "config": {"workload": workload_name(w0, extra["dense"]), "sample_tokens_per_step": args.ref_tokens},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                          "sample": "first %d tokens per step: router logits, routing and expert stage%s"
                                    % (args.ref_tokens, "" if w0.layers == 1 else
@@ -541,6 +566,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--dense", type=int, default=0, metavar="I",
+                    help="time the dense first-layer MLP of intermediate size I instead of the MoE layer")
     ap.add_argument("--flush-l2", action="store_true",
                     help="scrub L2 between timed steps (always on for workload 1, whose weights fit in L2)")
     ap.add_argument("--cpu-tokens-1t", type=int, default=256,

@@ -35,9 +35,9 @@ EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router
            "moe_route_from_logits", "moe_forward", "moe_get_status", "moe_last_launch_count",
            "moe_profile_enable", "moe_profile_read", "moe_kernel_name", "moe_strerror", "moe_route_static",
            "moe_debug_inject_timeout", "moe_rmsnorm", "moe_expert_feedback", "moe_prepare_router",
-           "moe_route_prepared")
+           "moe_route_prepared", "moe_dense_workspace_bytes", "moe_dense_ffn")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
-MOE_KERNEL_COUNT = 10
+MOE_KERNEL_COUNT = 11
 
 
 class MoeCfg(ctypes.Structure):
@@ -80,6 +80,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.moe_workspace_init.argtypes = [P, S, P]
         lib.moe_route.argtypes = [C, P, P, P, P, P, P, P, P, P, S, P]
         lib.moe_router_logits.argtypes = [C, P, P, P, P, S, P]
+        I32 = ctypes.c_int32
+        lib.moe_dense_workspace_bytes.argtypes = [I32, I32, I32]
+        lib.moe_dense_workspace_bytes.restype = S
+        lib.moe_dense_ffn.argtypes = [I32, I32, I32, P, P, P, P, P, P, S, P]
+        lib.moe_dense_ffn.restype = ctypes.c_int
         lib.moe_prepare_router.argtypes = [C, P, P, P]
         lib.moe_prepare_router.restype = ctypes.c_int
         lib.moe_route_prepared.argtypes = [C, P, P, P, P, P, P, P, P, P, P, S, P]

@@ -27,11 +27,11 @@ thread_local int g_last_launches = 0;
 // ------------------------------------------------------------- profiling
 enum KernelId {
     KID_SPLIT = 0, KID_ROUTER_GEMM, KID_SELECT, KID_FINALIZE, KID_HIST, KID_SCAN, KID_SCATTER,
-    KID_GEMM_GATE_UP, KID_GEMM_DOWN, KID_COMBINE
+    KID_GEMM_GATE_UP, KID_GEMM_DOWN, KID_COMBINE, KID_DENSE_TILES
 };
 const char *const kKernelNames[MOE_KERNEL_COUNT] = {
     "split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist",
-    "bucket_scan", "bucket_scatter", "gemm_gate_up_swiglu", "gemm_down", "combine"};
+    "bucket_scan", "bucket_scatter", "gemm_gate_up_swiglu", "gemm_down", "combine", "dense_tiles"};
 
 struct ProfRecord {
     cudaEvent_t start, stop;
@@ -460,6 +460,120 @@ int moe_route_prepared(const moe_cfg *cfg, const moe_bf16 *hidden, const float *
                           launches);
     g_last_launches = launches;
     return rc;
+}
+
+int check_dense(int32_t T, int32_t H, int32_t I)
+{
+    if (T < 1 || H < 1 || I < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (T > (1 << 24) || H % 256 != 0 || I % 128 != 0)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+struct DenseLayout {
+    size_t mtiles, aint, y, total;
+    int mt;
+};
+
+DenseLayout dense_layout(int32_t T, int32_t H, int32_t I)
+{
+    DenseLayout L;
+    L.mt = (T <= GEMM_SMALL_T) ? GEMM_SMALL_T : GEMM_BM;
+    size_t off = sizeof(WsHeader);
+    L.mtiles = off;
+    off = align_up(off + (size_t)((T + L.mt - 1) / L.mt + 1) * 16, 256);
+    L.aint = off;
+    off = align_up(off + (size_t)T * I * 2, 256);
+    L.y = off;
+    off = align_up(off + (size_t)T * H * 2, 256);
+    L.total = off;
+    return L;
+}
+
+size_t moe_dense_workspace_bytes(int32_t T, int32_t H, int32_t I)
+{
+    return check_dense(T, H, I) == MOE_OK ? dense_layout(T, H, I).total : 0;
+}
+
+int moe_dense_ffn(int32_t T, int32_t H, int32_t I, const moe_bf16 *hidden, const moe_bf16 *W_gate_up,
+                  const moe_bf16 *W_down, const moe_bf16 *residual, moe_bf16 *out, void *ws, size_t ws_bytes,
+                  void *stream)
+{
+    int rc = check_dense(T, H, I);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !W_gate_up || !W_down || !out)
+        return MOE_ERR_INVALID_ARG;
+    const DenseLayout L = dense_layout(T, H, I);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(residual, 16) ||
+        !aligned(out, 16))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    WsHeader *hdr = header(ws);
+    int4 *mtiles = at<int4>(ws, L.mtiles);
+    uint16_t *aint = at<uint16_t>(ws, L.aint);
+    uint16_t *y = at<uint16_t>(ws, L.y);
+    const bool small = T <= GEMM_SMALL_T;
+    const int a_rows = small ? GEMM_SMALL_T : GEMM_BM;
+    const int ntile = (T + L.mt - 1) / L.mt;
+    GLR_LAUNCH(KID_DENSE_TILES, launch_dense_tiles(T, L.mt, mtiles, hdr, s));
+
+    // the grouped GEMMs with one group: group 0 == E = 0 takes the "shared"
+    // operands (tmA1 / tmB1), rows 0 .. T-1 of the intermediate and of Y
+    GemmParams p1;
+    memset(&p1, 0, sizeof(p1));
+    if (!make_map_bf16(&p1.tmA1, hidden, T, H, GEMM_BK, a_rows) ||
+        !make_map_bf16(&p1.tmB1, W_gate_up, 2ull * I, H, GEMM_BK, 128) ||
+        !make_map_bf16(&p1.tmOut, aint, T, I, 64, 32))
+        return MOE_ERR_CUDA;
+    p1.tmA0 = p1.tmA1;
+    p1.tmB0 = p1.tmB1;
+    p1.out = aint;
+    p1.mtiles = mtiles;
+    p1.num_mtiles = &hdr->num_mtiles;
+    p1.n_tiles = I / 128;
+    p1.kblocks = H / GEMM_BK;
+    p1.T = T;
+    p1.E = 0;
+    p1.I = I;
+    p1.H = H;
+    p1.kT = 0;
+    p1.ld_out = I;
+    p1.status = &hdr->status;
+    GLR_LAUNCH(KID_GEMM_GATE_UP, launch_gemm(small ? GK_GATE_UP_SMALL : GK_GATE_UP, p1,
+                                             std::min(sms, ntile * p1.n_tiles), s));
+    GemmParams p2;
+    memset(&p2, 0, sizeof(p2));
+    if (!make_map_bf16(&p2.tmA0, aint, T, I, GEMM_BK, a_rows) ||
+        !make_map_bf16(&p2.tmB1, W_down, (uint64_t)I, H, 64, GEMM_BK) ||
+        !make_map_bf16(&p2.tmOut, y, T, H, 64, 32))
+        return MOE_ERR_CUDA;
+    p2.tmB0 = p2.tmB1;
+    p2.out = y;
+    p2.mtiles = mtiles;
+    p2.num_mtiles = &hdr->num_mtiles;
+    p2.n_tiles = H / 256;
+    p2.kblocks = I / GEMM_BK;
+    p2.T = T;
+    p2.E = 0;
+    p2.I = I;
+    p2.H = H;
+    p2.kT = 0;
+    p2.ld_out = H;
+    p2.status = &hdr->status;
+    GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(small ? GK_DOWN_SMALL : GK_DOWN, p2, std::min(sms, ntile * p2.n_tiles),
+                                          s));
+    // k = 0 combine: out = bf16(Y (+ residual))
+    GLR_LAUNCH(KID_COMBINE, launch_combine(y, nullptr, nullptr, residual, T, H, 0, out, s));
+    g_last_launches = launches;
+    return MOE_OK;
 }
 
 int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,

@@ -134,6 +134,9 @@ cudaError_t launch_bucket_small(const int32_t *idx, const uint16_t *x, int T, in
                                 int32_t *sizes, int32_t *slot_of, uint16_t *x_perm, int4 *mtiles, WsHeader *hdr,
                                 cudaStream_t s);
 
+// m-tile list of a dense MLP: T tokens in tiles of mt rows, group 0
+cudaError_t launch_dense_tiles(int T, int mt, int4 *mtiles, WsHeader *hdr, cudaStream_t s);
+
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s);
 

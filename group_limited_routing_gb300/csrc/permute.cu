@@ -368,6 +368,28 @@ cudaError_t launch_bucket_small(const int32_t *idx, const uint16_t *x, int T, in
 }
 
 // ---------------------------------------------------------------------------
+// Dense MLP: every token runs through the one weight set, so the m-tile list
+// is just the T tokens in tiles of `mt` rows (the GEMMs' "shared" group).
+__global__ void dense_tiles_kernel(int T, int mt, int4 *__restrict__ mtiles, WsHeader *__restrict__ hdr)
+{
+    pdl_wait();
+    const int n = (T + mt - 1) / mt;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+        mtiles[i] = make_int4(0, i * mt, min(mt, T - i * mt), 0);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        hdr->num_mtiles = n;
+}
+
+cudaError_t launch_dense_tiles(int T, int mt, int4 *mtiles, WsHeader *hdr, cudaStream_t s)
+{
+    const int n = (T + mt - 1) / mt;
+    const cudaError_t le = launch_pdl(dense_tiles_kernel, dim3((n + 255) / 256), dim3(256), 0, s, T, mt, mtiles, hdr);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
 // out[t] = bf16( Y[K*T + t] + sum_j w[t,j] * Y[slot_of[t,j]] (+ residual[t]) ),
 // fp32 accumulation in j order.  A block takes ctok <= COMBINE_TOK tokens at a time:
 // their slots and weights are loaded once into shared memory, then a thread

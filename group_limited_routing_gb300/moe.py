@@ -14,6 +14,7 @@ expert (section 五).
 from __future__ import annotations
 
 import ctypes
+import types
 import dataclasses
 from typing import Optional
 
@@ -205,6 +206,51 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
     return out
 
 
+class DenseWorkspace:
+    """A device workspace for moe_dense_ffn (T tokens, hidden H, inner size I)."""
+
+    def __init__(self, T: int, H: int, I: int, device=None):
+        self.shape = (T, H, I)
+        self.nbytes = int(_lib.load().moe_dense_workspace_bytes(T, H, I))
+        if self.nbytes == 0:
+            raise ValueError("unsupported dense shape T=%d H=%d I=%d" % (T, H, I))
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        assert self.buf.data_ptr() % 256 == 0
+        _lib.check(_lib.load().moe_workspace_init(self.ptr, self.nbytes, _stream(self.buf.device)),
+                   "moe_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def status(self, reset: bool = True) -> int:
+        v = ctypes.c_int32(0)
+        _lib.check(_lib.load().moe_get_status(self.ptr, self.nbytes, _stream(self.buf.device), ctypes.byref(v),
+                                              1 if reset else 0), "moe_get_status")
+        return int(v.value)
+
+
+def dense_ffn(hidden, W_gate_up, W_down, residual=None, *, ws: Optional[DenseWorkspace] = None, out=None):
+    """moe_dense_ffn: out [T, H] bf16 = down(silu(gate x) * up x) (+ residual),
+    W_gate_up [2I, H] (gate rows, then up rows), W_down [I, H]."""
+    dev = hidden.device
+    bf = torch.bfloat16
+    T, H = hidden.shape
+    I = W_down.shape[0]
+    ph = _need(hidden, "hidden", bf, (T, H), dev)
+    pgu = _need(W_gate_up, "W_gate_up", bf, (2 * I, H), dev)
+    pd = _need(W_down, "W_down", bf, (I, H), dev)
+    pr = _opt(residual, "residual", bf, (T, H), dev)
+    if out is None:
+        out = torch.empty(T, H, dtype=bf, device=dev)
+    po = _need(out, "out", bf, (T, H), dev)
+    if ws is None or ws.shape != (T, H, I):
+        ws = DenseWorkspace(T, H, I, dev)
+    rc = _lib.load().moe_dense_ffn(T, H, I, ph, pgu, pd, pr, po, ws.ptr, ws.nbytes, _stream(dev))
+    _lib.check(rc, "moe_dense_ffn")
+    return out
+
+
 def expert_feedback(cfg: MoeConfig, counts, gamma: float, expert_bias=None, totals=None) -> None:
     """moe_expert_feedback: in place, bias += +-gamma toward the balanced load
     (routing article §三) and totals += counts (§六)."""
@@ -297,6 +343,28 @@ class MoELayer:
         if self.expert_bias is None:
             self.expert_bias = torch.zeros(self.cfg.E, dtype=torch.float32, device=self.W_router.device)
         expert_feedback(self.cfg, self.routing[2], gamma, self.expert_bias, totals)
+
+
+class DenseLayer:
+    """The dense first decoder layer (an ordinary SwiGLU MLP, routing article
+    §五 "first_k_dense_replace = 1"): weights [2I, H] / [I, H] and a
+    workspace; __call__(hidden, residual=None, out=None) runs moe_dense_ffn."""
+
+    def __init__(self, W_gate_up, W_down, T: int):
+        self.W_gate_up, self.W_down = W_gate_up, W_down
+        self.device = W_down.device
+        I, H = W_down.shape
+        self.cfg = types.SimpleNamespace(T=T, H=H, I=I)
+        self.ws = DenseWorkspace(T, H, I, self.device)
+        self.last_launches = 0
+
+    def __call__(self, hidden, residual=None, out=None):
+        y = dense_ffn(hidden, self.W_gate_up, self.W_down, residual, ws=self.ws, out=out)
+        self.last_launches = last_launch_count()
+        return y
+
+    def status(self) -> int:
+        return self.ws.status()
 
 
 class MoEStack:

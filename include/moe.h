@@ -181,6 +181,23 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
                 const int32_t *topk_idx, const float *topk_w, const moe_bf16 *residual,
                 moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
 
+/* Dense SwiGLU MLP: the first decoder layer of the model on the routing page
+ * ("first_k_dense_replace = 1", section 五: layer 0 is an ordinary MLP, the
+ * 19 layers after it are MoE).  The page gives the layer neither a formula
+ * nor a size; this takes the experts' form with its own intermediate size I:
+ *   out[t] = bf16( down( silu(gate x[t]) * up x[t] ) (+ residual[t]) )
+ * run on the grouped tensor-core GEMMs with a single weight group.
+ *   hidden     [T, H] bf16, H % 256 == 0
+ *   W_gate_up  [2I, H] bf16: rows [0, I) gate, [I, 2I) up; I % 128 == 0
+ *   W_down     [I, H] bf16: out = a[1, I] @ W_down
+ *   residual   [T, H] bf16 or NULL; out [T, H] bf16 (may alias residual)
+ *   ws         workspace of moe_dense_workspace_bytes(T, H, I) bytes
+ *              (moe_workspace_init() once after allocating it) */
+size_t moe_dense_workspace_bytes(int32_t T, int32_t H, int32_t I);
+int moe_dense_ffn(int32_t T, int32_t H, int32_t I, const moe_bf16 *hidden, const moe_bf16 *W_gate_up,
+                  const moe_bf16 *W_down, const moe_bf16 *residual, moe_bf16 *out, void *ws,
+                  size_t ws_bytes, void *stream);
+
 /* Router without caller-provided scratch (no counterpart on the pages: it is
  * an interface convenience, not part of the method).  Same computation,
  * outputs and determinism as moe_route, but the scratch that moe_route keeps
@@ -244,7 +261,7 @@ int moe_last_launch_count(void);
  * the recorded events, folds them into per-kernel totals and returns the
  * total milliseconds and launch count of kernel `kernel_id` (0 <=
  * kernel_id < MOE_KERNEL_COUNT), clearing them when reset != 0. */
-#define MOE_KERNEL_COUNT 10
+#define MOE_KERNEL_COUNT 11
 int moe_profile_enable(int on);
 int moe_profile_read(int kernel_id, double *total_ms, int32_t *launches, int reset);
 const char *moe_kernel_name(int kernel_id);

@@ -163,6 +163,22 @@ def experts(x_bf16, W_gate_up, W_down, shared_gate_up, shared_down, idx, w,
     return out
 
 
+def dense_ffn(x_bf16, W_gate_up, W_down, residual=None, tokens=None):
+    """Dense SwiGLU MLP in float64: down(silu(gate x) * up x) (+ residual),
+    with the intermediate rounded to bf16 as in the expert path; it is the
+    expert stage with no routed pairs and the dense weights as its one
+    always-on MLP."""
+    x = _c(x_bf16, np.uint16)
+    T, H = x.shape
+    gu = _c(W_gate_up, np.uint16)
+    dn = _c(W_down, np.uint16)
+    I = dn.shape[0]
+    dummy_gu = np.zeros((1, 2 * I, H), dtype=np.uint16)
+    dummy_dn = np.zeros((1, I, H), dtype=np.uint16)
+    return experts(x, dummy_gu, dummy_dn, gu, dn, np.zeros((T, 0), dtype=np.int32),
+                   np.zeros((T, 0), dtype=np.float32), residual=residual, tokens=tokens)
+
+
 def rmsnorm(x_bf16: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     """Decoder pre-norm: bf16 bits of x / sqrt(mean(x^2) + eps), row by row."""
     x = _c(x_bf16, np.uint16)

@@ -143,3 +143,13 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_handle", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load()
+
+
+def test_dense_workspace_bytes(lib):
+    f = lib.moe_dense_workspace_bytes(1000, 2048, 4608)
+    # intermediate + output dominate
+    assert f >= 1000 * 4608 * 2 + 1000 * 2048 * 2 and f % 256 == 0
+    assert lib.moe_dense_workspace_bytes(1000, 2048, 100) == 0      # I % 128
+    assert lib.moe_dense_workspace_bytes(1000, 2000, 4608) == 0     # H % 256
+    assert lib.moe_dense_workspace_bytes(0, 2048, 4608) == 0
+    assert lib.moe_dense_workspace_bytes(2000, 2048, 4608) > f

@@ -223,3 +223,34 @@ def test_graphed_step_matches_eager(T):
         torch.cuda.synchronize()
         assert torch.equal(got, ref)
     assert g.status() == 0
+
+
+@pytest.mark.parametrize("T,I,nsample", [(1, 4608, None), (16, 4608, None), (17, 1024, None), (300, 4608, None),
+                                         (4096, 4608, 128)])
+def test_dense_ffn_matches_oracle(T, I, nsample):
+    """The dense first-layer MLP (one weight group through the grouped GEMMs,
+    T <= 16 on the small-T kinds) against the oracle, with a residual."""
+    H = 2048
+    g = torch.Generator(DEV).manual_seed(T + I)
+    x = torch.randn(T, H, device=DEV, generator=g).to(torch.bfloat16)
+    gu = (torch.randn(2 * I, H, device=DEV, generator=g) * 0.02).to(torch.bfloat16)
+    dn = (torch.randn(I, H, device=DEV, generator=g) * 0.02).to(torch.bfloat16)
+    res = torch.randn(T, H, device=DEV, generator=g).to(torch.bfloat16)
+    ws = moe.DenseWorkspace(T, H, I, DEV)
+    out = moe.dense_ffn(x, gu, dn, res, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    assert moe.last_launch_count() == 4          # tile list, gate/up GEMM, down GEMM, combine
+    tokens = None
+    if nsample is not None:
+        tokens = np.union1d(wl.token_sample(T, nsample, seed=3).numpy(), [0, T - 1]).astype(np.int32)
+    ref = oracle.dense_ffn(u16(x), u16(gu), u16(dn), residual=u16(res), tokens=tokens)
+    got = bf16_to_f64(out)
+    if tokens is not None:
+        got = got[tokens]
+    assert_output_close(got, ref, "dense T=%d I=%d" % (T, I))
+    # no residual: the MLP alone
+    out2 = moe.dense_ffn(x, gu, dn, ws=ws)
+    ref2 = oracle.dense_ffn(u16(x), u16(gu), u16(dn), tokens=tokens)
+    got2 = bf16_to_f64(out2)
+    assert_output_close(got2 if tokens is None else got2[tokens], ref2, "dense T=%d I=%d, no residual" % (T, I))

@@ -359,6 +359,23 @@ def test_zero_weights_leave_the_shared_expert():
     np.testing.assert_allclose(out, _textbook_swiglu(x, sgu, sd), rtol=1e-9, atol=1e-12)
 
 
+def test_dense_mlp_is_textbook_swiglu_with_its_own_size():
+    # the dense first layer: one SwiGLU MLP of intermediate size I != the experts'
+    rng = np.random.default_rng(21)
+    T, H, I = 9, 128, 96
+    x = bf16(rng.standard_normal((T, H)))
+    gu = bf16(rng.standard_normal((2 * I, H)) * 0.05)
+    dn = bf16(rng.standard_normal((I, H)) * 0.05)
+    res = bf16(rng.standard_normal((T, H)))
+    np.testing.assert_allclose(oracle.dense_ffn(x, gu, dn), _textbook_swiglu(x, gu, dn), rtol=1e-9, atol=1e-12)
+    np.testing.assert_allclose(oracle.dense_ffn(x, gu, dn, residual=res),
+                               _textbook_swiglu(x, gu, dn) + f32_of(res).astype(np.float64), rtol=1e-9,
+                               atol=1e-12)
+    # gate and up are not interchangeable (silu(gate) * up)
+    swapped = np.concatenate([gu[I:], gu[:I]])
+    assert np.abs(oracle.dense_ffn(x, swapped, dn) - oracle.dense_ffn(x, gu, dn)).max() > 1e-3
+
+
 def test_weighted_sum_of_experts_plus_shared_and_residual():
     rng, x, Wgu, Wd, sgu, sd = _expert_setup(seed=15)
     T = x.shape[0]
