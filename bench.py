@@ -546,7 +546,7 @@ def run_reference(args, world, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": workload_name(w0, extra["dense"]), "sample_tokens_per_step": args.ref_tokens},
+        "config": {"workload": workload_name(w0), "sample_tokens_per_step": args.ref_tokens},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                          "sample": "first %d tokens per step: router logits, routing and expert stage%s"
                                    % (args.ref_tokens, "" if w0.layers == 1 else
