@@ -15,6 +15,13 @@
 //               3D weights; the shared expert of section 五 is the last group).
 //   GK_DOWN     per expert bucket: Y = intermediate_e . W_down[e], W_down
 //               stacked [E, I, H] as on the page (an MN-major B operand).
+//   GK_*_SMALL  the two grouped products for T <= GEMM_SMALL_T (decode): 16 A
+//               rows per stage and a 6-deep ring of weight tiles.
+// The grouped kinds also serve the dense first-layer MLP (one weight group).
+//
+// Every kernel starts with griddepcontrol.wait (programmatic dependent
+// launch): its prologue (barriers, TMEM, descriptor prefetch) overlaps the
+// previous kernel's teardown, and nothing global is read before the wait.
 //
 // Roles (192 threads, one CTA per SM):
 //   warp 0, one lane : TMA producer, fills a STAGES-deep ring of smem stages
