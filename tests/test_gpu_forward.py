@@ -254,3 +254,19 @@ def test_dense_ffn_matches_oracle(T, I, nsample):
     ref2 = oracle.dense_ffn(u16(x), u16(gu), u16(dn), tokens=tokens)
     got2 = bf16_to_f64(out2)
     assert_output_close(got2 if tokens is None else got2[tokens], ref2, "dense T=%d I=%d, no residual" % (T, I))
+
+
+def test_large_batch_sampled_parity():
+    """T = 131072 (4x the bench batch; ~1M bucket rows, 32-bit row indices and
+    byte offsets well past 2^31 bytes in X_perm and Y): routing counts are
+    exact, and sampled outputs match the oracle."""
+    T = 131072
+    w0 = wl.WORKLOADS[4].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
+    idx, w, counts, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    torch.cuda.synchronize()
+    assert int(counts.sum()) == 8 * T
+    assert torch.equal(counts.cpu(), torch.bincount(idx.cpu().view(-1).long(), minlength=256).to(torch.int32))
+    tokens = np.union1d(wl.token_sample(T, 96, seed=77).numpy(), [0, T - 1]).astype(np.int32)
+    check(cfg, d, idx, w, tokens, what="T=%d sampled" % T)
