@@ -57,6 +57,10 @@ def _load():
             lib.orc_counts_aux.argtypes = [ctypes.c_int] * 3 + [P, P, P, P]
             lib.orc_counts_aux.restype = ctypes.c_double
             lib.orc_experts.argtypes = [ctypes.POINTER(_Cfg)] + [P] * 8 + [ctypes.c_int, P, P]
+            lib.orc_experts_opt.argtypes = [ctypes.POINTER(_Cfg)] + [P] * 8 + [ctypes.c_int, P, P, ctypes.c_int]
+            lib.orc_experts_opt.restype = ctypes.c_int
+            lib.orc_experts_backward.argtypes = [ctypes.POINTER(_Cfg)] + [P] * 8 + [ctypes.c_int] + [P] * 6
+            lib.orc_experts_backward.restype = ctypes.c_int
             lib.orc_experts.restype = ctypes.c_int
             lib.orc_bf16_round_array.argtypes = [P, P, ctypes.c_long]
             lib.orc_rmsnorm.argtypes = [ctypes.c_int, ctypes.c_int, P, ctypes.c_float, P]
@@ -136,9 +140,11 @@ def counts_aux(idx: np.ndarray, scores=None, E=256):
 
 
 def experts(x_bf16, W_gate_up, W_down, shared_gate_up, shared_down, idx, w,
-            residual=None, tokens=None, E=None):
+            residual=None, tokens=None, E=None, round_act=True):
     """Layer output in float64 for the listed tokens (all by default):
-    sum_j w[t,j] * SwiGLU_{idx[t,j]}(x[t]) + shared(x[t]) (+ residual[t])."""
+    sum_j w[t,j] * SwiGLU_{idx[t,j]}(x[t]) + shared(x[t]) (+ residual[t]).
+    round_act=False keeps the SwiGLU intermediate unrounded (a smooth function
+    of every input, for finite-difference checks of the backward)."""
     x = _c(x_bf16, np.uint16)
     T, H = x.shape
     Wgu = _c(W_gate_up, np.uint16)
@@ -156,11 +162,41 @@ def experts(x_bf16, W_gate_up, W_down, shared_gate_up, shared_down, idx, w,
     n = T if tok is None else tok.size
     c = _cfg(T=T, H=H, E=E, k=k, I=I, Is=Is)
     out = np.empty((n, H), dtype=np.float64)
-    rc = _load().orc_experts(ctypes.byref(c), _p(x), _p(Wgu), _p(Wd), _p(sgu), _p(sd), _p(idx), _p(w),
-                             _p(res), n, _p(tok), _p(out))
+    rc = _load().orc_experts_opt(ctypes.byref(c), _p(x), _p(Wgu), _p(Wd), _p(sgu), _p(sd), _p(idx), _p(w),
+                                 _p(res), n, _p(tok), _p(out), 1 if round_act else 0)
     if rc != 0:
         raise IndexError("expert index out of range")
     return out
+
+
+def experts_backward(x_bf16, W_gate_up, W_down, shared_gate_up, shared_down, idx, w, d_out, round_act=True):
+    """Backward of experts() for fixed routing, in float64: given d_out [T, H],
+    returns dict(dx [T, H], dW_gate_up [E, 2I, H], dW_down [E, I, H],
+    d_shared_gate_up [2Is, H], d_shared_down [Is, H], dw [T, k]).  The
+    intermediate's bf16 rounding (round_act) passes gradients unchanged."""
+    x = _c(x_bf16, np.uint16)
+    T, H = x.shape
+    Wgu = _c(W_gate_up, np.uint16)
+    Wd = _c(W_down, np.uint16)
+    E, I = Wgu.shape[0], Wd.shape[1]
+    sgu = _c(shared_gate_up, np.uint16)
+    sd = _c(shared_down, np.uint16)
+    Is = 0 if sd is None else sd.shape[0]
+    idx = _c(idx, np.int32)
+    w = _c(w, np.float32)
+    k = idx.shape[1]
+    dout = _c(d_out, np.float64)
+    c = _cfg(T=T, H=H, E=E, k=k, I=I, Is=Is)
+    r = dict(dx=np.empty((T, H)), dW_gate_up=np.empty((E, 2 * I, H)), dW_down=np.empty((E, I, H)),
+             d_shared_gate_up=None if sgu is None else np.empty((2 * Is, H)),
+             d_shared_down=None if sd is None else np.empty((Is, H)), dw=np.empty((T, k)))
+    rc = _load().orc_experts_backward(ctypes.byref(c), _p(x), _p(Wgu), _p(Wd), _p(sgu), _p(sd), _p(idx), _p(w),
+                                      _p(dout), 1 if round_act else 0, _p(r["dx"]), _p(r["dW_gate_up"]),
+                                      _p(r["dW_down"]), _p(r["d_shared_gate_up"]), _p(r["d_shared_down"]),
+                                      _p(r["dw"]))
+    if rc != 0:
+        raise IndexError("expert index out of range")
+    return r
 
 
 def dense_ffn(x_bf16, W_gate_up, W_down, residual=None, tokens=None):

@@ -273,7 +273,7 @@ double orc_counts_aux(int T, int E, int K, const int32_t *idx, const float *scor
  * and y * weight is added to acc.  Wgu is [2I, H] (gate rows, then up rows),
  * Wd is [I, H]; all products and sums in double. */
 static void swiglu_expert_add(int H, int I, const double *x, const uint16_t *Wgu,
-                              const uint16_t *Wd, double weight, double *a, double *acc)
+                              const uint16_t *Wd, double weight, double *a, double *acc, int round_act)
 {
     for (int i = 0; i < I; ++i) {
         const uint16_t *wg = Wgu + (size_t)i * H;
@@ -284,7 +284,7 @@ static void swiglu_expert_add(int H, int I, const double *x, const uint16_t *Wgu
             U += x[h] * orc_bf16_value(wu[h]);
         }
         double act = G / (1.0 + exp(-G)) * U;
-        a[i] = orc_bf16_value(orc_bf16_round((float)act));
+        a[i] = round_act ? orc_bf16_value(orc_bf16_round((float)act)) : act;
     }
     for (int i = 0; i < I; ++i) {
         const uint16_t *wd = Wd + (size_t)i * H;
@@ -301,9 +301,22 @@ static void swiglu_expert_add(int H, int I, const double *x, const uint16_t *Wgu
  * in double.  tokens (nullable) lists which rows of x to compute; out has one
  * row of H per listed token.  Indices outside [0, E) contribute nothing and
  * are reported by returning -1. */
+int orc_experts_opt(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const uint16_t *Wd,
+                    const uint16_t *sgu, const uint16_t *sd, const int32_t *idx, const float *w,
+                    const uint16_t *residual, int n_tok, const int32_t *tokens, double *out, int round_act);
+
 int orc_experts(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const uint16_t *Wd,
                 const uint16_t *sgu, const uint16_t *sd, const int32_t *idx, const float *w,
                 const uint16_t *residual, int n_tok, const int32_t *tokens, double *out)
+{
+    return orc_experts_opt(c, x, Wgu, Wd, sgu, sd, idx, w, residual, n_tok, tokens, out, 1);
+}
+
+/* As orc_experts; round_act = 0 keeps the SwiGLU intermediate unrounded (the
+ * smooth function the backward's finite-difference checks differentiate). */
+int orc_experts_opt(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const uint16_t *Wd,
+                    const uint16_t *sgu, const uint16_t *sd, const int32_t *idx, const float *w,
+                    const uint16_t *residual, int n_tok, const int32_t *tokens, double *out, int round_act)
 {
     const int H = c->H, I = c->I, Is = c->Is, K = c->k, E = c->E;
     int bad = 0;
@@ -327,10 +340,10 @@ int orc_experts(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const 
                     continue;
                 }
                 swiglu_expert_add(H, I, xd, Wgu + (size_t)e * 2 * I * H, Wd + (size_t)e * I * H,
-                                  (double)w[(size_t)t * K + j], a, acc);
+                                  (double)w[(size_t)t * K + j], a, acc, round_act);
             }
             if (sgu && sd)
-                swiglu_expert_add(H, Is, xd, sgu, sd, 1.0, a, acc);
+                swiglu_expert_add(H, Is, xd, sgu, sd, 1.0, a, acc, round_act);
             if (residual)
                 for (int h = 0; h < H; ++h)
                     acc[h] += orc_bf16_value(residual[(size_t)t * H + h]);
@@ -338,6 +351,143 @@ int orc_experts(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const 
         free(xd);
         free(a);
     }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------- backward of the expert stage */
+
+/* Gradients of one SwiGLU expert applied to one row, for an output gradient
+ * dy (the gradient of this expert's output row y = a . Wd):
+ *   G = x . Wg^T, U = x . Wu^T, a = silu(G) * U (bf16-rounded when round_act,
+ *   the rounding passed through as the identity), y = a . Wd;
+ *   dWd += a (x) dy,  da = Wd . dy,
+ *   dG = da * U * s * (1 + G * (1 - s)),  dU = da * G * s   (s = sigmoid(G)),
+ *   dWg += dG (x) x,  dWu += dU (x) x,  dx = dG . Wg + dU . Wu.
+ * Returns <dout_row, y> (scale 1/weight applied by the caller) through *ydot
+ * when dout_row is not NULL.  Everything in double. */
+static void swiglu_expert_backward(int H, int I, const double *x, const uint16_t *Wgu, const uint16_t *Wd,
+                                   const double *dy, int round_act, double *dWgu, double *dWd, double *dx,
+                                   const double *dout_row, double *ydot)
+{
+    double dot = 0.0;
+    for (int h = 0; h < H; ++h)
+        dx[h] = 0.0;
+    for (int i = 0; i < I; ++i) {
+        const uint16_t *wg = Wgu + (size_t)i * H;
+        const uint16_t *wu = Wgu + (size_t)(I + i) * H;
+        const uint16_t *wd = Wd + (size_t)i * H;
+        double G = 0.0, U = 0.0;
+        for (int h = 0; h < H; ++h) {
+            G += x[h] * orc_bf16_value(wg[h]);
+            U += x[h] * orc_bf16_value(wu[h]);
+        }
+        const double sg = 1.0 / (1.0 + exp(-G));
+        const double act = G * sg * U;
+        const double a = round_act ? orc_bf16_value(orc_bf16_round((float)act)) : act;
+        double da = 0.0;
+        for (int h = 0; h < H; ++h) {
+            const double wdh = orc_bf16_value(wd[h]);
+            da += wdh * dy[h];
+            if (dout_row)
+                dot += a * wdh * dout_row[h];
+        }
+        double *gd = dWd + (size_t)i * H;
+        for (int h = 0; h < H; ++h)
+            gd[h] += a * dy[h];
+        const double dG = da * U * sg * (1.0 + G * (1.0 - sg));
+        const double dU = da * G * sg;
+        double *gg = dWgu + (size_t)i * H;
+        double *gu = dWgu + (size_t)(I + i) * H;
+        for (int h = 0; h < H; ++h) {
+            gg[h] += dG * x[h];
+            gu[h] += dU * x[h];
+            dx[h] += dG * orc_bf16_value(wg[h]) + dU * orc_bf16_value(wu[h]);
+        }
+    }
+    if (ydot)
+        *ydot = dot;
+}
+
+/* Backward of orc_experts (routing fixed, residual passed straight through):
+ * given dout [T, H] (double), writes
+ *   dx   [T, H]      = sum_j w[t,j] * d expert_j / dx + d shared / dx,
+ *   dWgu [E, 2I, H], dWd [E, I, H], dsgu [2Is, H], dsd [Is, H]  (sums over tokens),
+ *   dw   [T, k]      = <dout[t], expert_{idx[t,j]}(x[t])>.
+ * Each expert's gradients are summed by one thread over its tokens in token
+ * order; dx[t] adds the pairs j = 0 .. k-1, then the shared expert, in order.
+ * Returns -1 if an expert index is out of range (the pair is skipped). */
+int orc_experts_backward(const orc_cfg *c, const uint16_t *x, const uint16_t *Wgu, const uint16_t *Wd,
+                         const uint16_t *sgu, const uint16_t *sd, const int32_t *idx, const float *w,
+                         const double *dout, int round_act, double *dx, double *dWgu, double *dWd,
+                         double *dsgu, double *dsd, double *dw)
+{
+    const int T = c->T, H = c->H, I = c->I, Is = c->Is, K = c->k, E = c->E;
+    int bad = 0;
+    double *dxp = calloc((size_t)T * (K + 1) * H, sizeof(double));   /* per (token, pair) */
+    memset(dWgu, 0, sizeof(double) * (size_t)E * 2 * I * H);
+    memset(dWd, 0, sizeof(double) * (size_t)E * I * H);
+    if (dsgu)
+        memset(dsgu, 0, sizeof(double) * (size_t)2 * Is * H);
+    if (dsd)
+        memset(dsd, 0, sizeof(double) * (size_t)Is * H);
+    for (size_t i = 0; i < (size_t)T * K; ++i)
+        dw[i] = 0.0;
+#pragma omp parallel
+    {
+        double *xd = malloc(sizeof(double) * H);
+        double *dy = malloc(sizeof(double) * H);
+#pragma omp for schedule(dynamic, 1)
+        for (int e = 0; e <= E; ++e) {             /* e == E: the shared expert */
+            if (e == E && !(sgu && sd))
+                continue;
+            for (int t = 0; t < T; ++t) {
+                for (int j = 0; j <= K; ++j) {
+                    double wt;
+                    if (e < E) {
+                        if (j == K || idx[(size_t)t * K + j] != e)
+                            continue;
+                        wt = (double)w[(size_t)t * K + j];
+                    } else {
+                        if (j != K)
+                            continue;
+                        wt = 1.0;
+                    }
+                    for (int h = 0; h < H; ++h) {
+                        xd[h] = orc_bf16_value(x[(size_t)t * H + h]);
+                        dy[h] = wt * dout[(size_t)t * H + h];
+                    }
+                    double ydot = 0.0;
+                    if (e < E)
+                        swiglu_expert_backward(H, I, xd, Wgu + (size_t)e * 2 * I * H, Wd + (size_t)e * I * H,
+                                               dy, round_act, dWgu + (size_t)e * 2 * I * H,
+                                               dWd + (size_t)e * I * H, dxp + ((size_t)t * (K + 1) + j) * H,
+                                               dout + (size_t)t * H, &ydot);
+                    else
+                        swiglu_expert_backward(H, Is, xd, sgu, sd, dy, round_act, dsgu, dsd,
+                                               dxp + ((size_t)t * (K + 1) + K) * H, NULL, NULL);
+                    if (e < E)
+                        dw[(size_t)t * K + j] = ydot;
+                }
+            }
+        }
+        free(xd);
+        free(dy);
+    }
+    for (int t = 0; t < T; ++t)
+        for (int j = 0; j < K; ++j) {
+            const int e = idx[(size_t)t * K + j];
+            if (e < 0 || e >= E)
+                bad = 1;
+        }
+#pragma omp parallel for schedule(static)
+    for (int t = 0; t < T; ++t)
+        for (int h = 0; h < H; ++h) {
+            double acc = 0.0;
+            for (int j = 0; j <= K; ++j)
+                acc += dxp[((size_t)t * (K + 1) + j) * H + h];
+            dx[(size_t)t * H + h] = acc;
+        }
+    free(dxp);
     return bad ? -1 : 0;
 }
 
