@@ -29,15 +29,16 @@ MOE_STATUS_COUNT_MISMATCH = 8
 
 MOE_WS_ROUTE = 0
 MOE_WS_FORWARD = 1
+MOE_WS_BACKWARD = 2
 
 # every symbol include/moe.h declares
 EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router_logits",
            "moe_route_from_logits", "moe_forward", "moe_get_status", "moe_last_launch_count",
            "moe_profile_enable", "moe_profile_read", "moe_kernel_name", "moe_strerror", "moe_route_static",
            "moe_debug_inject_timeout", "moe_rmsnorm", "moe_expert_feedback", "moe_prepare_router",
-           "moe_route_prepared", "moe_dense_workspace_bytes", "moe_dense_ffn")
+           "moe_route_prepared", "moe_dense_workspace_bytes", "moe_dense_ffn", "moe_backward")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
-MOE_KERNEL_COUNT = 11
+MOE_KERNEL_COUNT = 16
 
 
 class MoeCfg(ctypes.Structure):
@@ -91,6 +92,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.moe_route_prepared.restype = ctypes.c_int
         lib.moe_route_from_logits.argtypes = [C, P, P, P, P, P, P, P, P, S, P]
         lib.moe_forward.argtypes = [C, P, P, P, P, P, P, P, P, P, P, S, P]
+        lib.moe_backward.argtypes = [C] + [P] * 14 + [P, S, P]
+        lib.moe_backward.restype = ctypes.c_int
         lib.moe_get_status.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
         lib.moe_last_launch_count.argtypes = []
         lib.moe_profile_enable.argtypes = [ctypes.c_int]

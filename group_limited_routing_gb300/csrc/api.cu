@@ -27,11 +27,13 @@ thread_local int g_last_launches = 0;
 // ------------------------------------------------------------- profiling
 enum KernelId {
     KID_SPLIT = 0, KID_ROUTER_GEMM, KID_SELECT, KID_FINALIZE, KID_HIST, KID_SCAN, KID_SCATTER,
-    KID_GEMM_GATE_UP, KID_GEMM_DOWN, KID_COMBINE, KID_DENSE_TILES
+    KID_GEMM_GATE_UP, KID_GEMM_DOWN, KID_COMBINE, KID_DENSE_TILES, KID_BWD_RECOMPUTE, KID_BWD_DGRAD,
+    KID_BWD_DX, KID_BWD_WGRAD, KID_BWD_MISC
 };
 const char *const kKernelNames[MOE_KERNEL_COUNT] = {
     "split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist",
-    "bucket_scan", "bucket_scatter", "gemm_gate_up_swiglu", "gemm_down", "combine", "dense_tiles"};
+    "bucket_scan", "bucket_scatter", "gemm_gate_up_swiglu", "gemm_down", "combine", "dense_tiles",
+    "bwd_gate_up_recompute", "bwd_dgrad_down_swiglu", "bwd_dgrad_x", "bwd_weight_grads", "bwd_pad_and_dw"};
 
 struct ProfRecord {
     cudaEvent_t start, stop;
@@ -171,6 +173,64 @@ FwdLayout fwd_layout(const moe_cfg &c)
     off = align_up(off + (K + 1) * T * H * 2, 256);
     L.total = off;
     return L;
+}
+
+struct BwdLayout {
+    size_t hist, sizes, mtiles, slot_of, eoff, xperm, dop, wperm, gu, aw, dgu, dx, dwp, total;
+    int nchunk, max_mtiles, kTp, rows;
+};
+
+// Backward workspace.  Buckets start on BWD_ROW_ALIGN-row boundaries, so the
+// routed rows take at most kTp = k T + E (BWD_ROW_ALIGN - 1); the shared
+// expert's rows follow at kTp whatever the routing, padded to a whole block.
+BwdLayout bwd_layout(const moe_cfg &c)
+{
+    BwdLayout L;
+    const size_t T = c.T, K = c.k, H = c.H, I = c.I;
+    L.nchunk = (c.T + PERM_CHUNK - 1) / PERM_CHUNK;
+    L.max_mtiles = (int)((K * T) / GEMM_BM + c.E + (T + GEMM_BM - 1) / GEMM_BM + 1);
+    L.kTp = (int)(K * T + (size_t)c.E * (BWD_ROW_ALIGN - 1));
+    L.rows = L.kTp + (c.T + BWD_ROW_ALIGN - 1) / BWD_ROW_ALIGN * BWD_ROW_ALIGN;
+    const size_t R = (size_t)L.rows;
+    size_t off = sizeof(WsHeader);
+    L.hist = off;
+    off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
+    L.sizes = off;
+    off = align_up(off + (size_t)c.E * 4, 256);
+    L.mtiles = off;
+    off = align_up(off + (size_t)L.max_mtiles * 16, 256);
+    L.slot_of = off;
+    off = align_up(off + T * K * 4, 256);
+    L.eoff = off;
+    off = align_up(off + (size_t)(c.E + 1) * 8, 256);
+    L.xperm = off;
+    off = align_up(off + (size_t)L.kTp * H * 2, 256);
+    L.dop = off;
+    off = align_up(off + R * H * 2, 256);
+    L.wperm = off;
+    off = align_up(off + R * 4, 256);
+    L.gu = off;
+    off = align_up(off + R * 2 * I * 4, 256);
+    L.aw = off;
+    off = align_up(off + R * I * 2, 256);
+    L.dgu = off;
+    off = align_up(off + R * 2 * I * 2, 256);
+    L.dx = off;
+    off = align_up(off + R * H * 2, 256);
+    L.dwp = off;
+    off = align_up(off + (size_t)L.kTp * (I / 256) * 4, 256);
+    L.total = off;
+    return L;
+}
+
+int check_backward_cfg(const moe_cfg *c)
+{
+    int rc = check_forward_cfg(c);
+    if (rc != MOE_OK)
+        return rc;
+    if (c->I % 256 != 0)
+        return MOE_ERR_UNSUPPORTED_SHAPE;     // the d(intermediate) tiles are 256 columns wide
+    return MOE_OK;
 }
 
 // --------------------------------------------------------------- device
@@ -319,6 +379,8 @@ size_t moe_workspace_bytes(const moe_cfg *cfg, int which)
         return check_route_cfg(cfg) == MOE_OK ? route_layout(*cfg).total : 0;
     if (which == MOE_WS_FORWARD)
         return check_forward_cfg(cfg) == MOE_OK ? fwd_layout(*cfg).total : 0;
+    if (which == MOE_WS_BACKWARD)
+        return check_backward_cfg(cfg) == MOE_OK ? bwd_layout(*cfg).total : 0;
     return 0;
 }
 
@@ -572,6 +634,164 @@ int moe_dense_ffn(int32_t T, int32_t H, int32_t I, const moe_bf16 *hidden, const
                                           s));
     // k = 0 combine: out = bf16(Y (+ residual))
     GLR_LAUNCH(KID_COMBINE, launch_combine(y, nullptr, nullptr, residual, T, H, 0, out, s));
+    g_last_launches = launches;
+    return MOE_OK;
+}
+
+int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
+                 const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const int32_t *topk_idx,
+                 const float *topk_w, const moe_bf16 *d_out, moe_bf16 *d_hidden, float *dW_gate_up, float *dW_down,
+                 float *d_shared_gate_up, float *d_shared_down, float *d_topk_w, void *ws, size_t ws_bytes,
+                 void *stream)
+{
+    int rc = check_backward_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !W_gate_up || !W_down || !shared_gate_up || !shared_down || !topk_idx || !topk_w || !d_out ||
+        !d_hidden || !dW_gate_up || !dW_down || !d_shared_gate_up || !d_shared_down || !d_topk_w)
+        return MOE_ERR_INVALID_ARG;
+    const BwdLayout L = bwd_layout(*cfg);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(shared_gate_up, 16) ||
+        !aligned(shared_down, 16) || !aligned(d_out, 16) || !aligned(d_hidden, 16) || !aligned(dW_gate_up, 16) ||
+        !aligned(dW_down, 16) || !aligned(d_shared_gate_up, 16) || !aligned(d_shared_down, 16) ||
+        !aligned(topk_idx, 4) || !aligned(topk_w, 4) || !aligned(d_topk_w, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const moe_cfg &c = *cfg;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    WsHeader *hdr = header(ws);
+    int32_t *hist = at<int32_t>(ws, L.hist);
+    int32_t *sizes = at<int32_t>(ws, L.sizes);
+    int4 *mtiles = at<int4>(ws, L.mtiles);
+    int32_t *slot_of = at<int32_t>(ws, L.slot_of);
+    int2 *eoff = at<int2>(ws, L.eoff);
+    uint16_t *xperm = at<uint16_t>(ws, L.xperm);
+    uint16_t *dop = at<uint16_t>(ws, L.dop);
+    float *wperm = at<float>(ws, L.wperm);
+    float *gu = at<float>(ws, L.gu);
+    uint16_t *aw = at<uint16_t>(ws, L.aw);
+    uint16_t *dgu = at<uint16_t>(ws, L.dgu);
+    uint16_t *dx = at<uint16_t>(ws, L.dx);
+    float *dwp = at<float>(ws, L.dwp);
+    const uint64_t R = (uint64_t)L.rows;
+
+    // 1. buckets on 64-row boundaries: X rows, dOut rows, weights per bucket row
+    GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
+    GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
+    GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter_bwd(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
+                                                      xperm, mtiles, hdr, d_out, topk_w, dop, wperm, eoff, L.kTp,
+                                                      s));
+    GLR_LAUNCH(KID_BWD_MISC, launch_zero_pad(eoff, sizes, c.T, c.E, c.H, c.I, xperm, dop, aw, dgu, s));
+
+    // 2. the gate/up products again: G, U (fp32) and w * a (bf16)
+    GemmParams p1;
+    memset(&p1, 0, sizeof(p1));
+    if (!make_map_bf16(&p1.tmA0, xperm, (uint64_t)L.kTp, c.H, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p1.tmA1, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p1.tmB0, W_gate_up, 2ull * c.I * c.E, c.H, GEMM_BK, 128) ||
+        !make_map_bf16(&p1.tmB1, shared_gate_up, 2ull * c.I, c.H, GEMM_BK, 128))
+        return MOE_ERR_CUDA;
+    p1.mtiles = mtiles;
+    p1.num_mtiles = &hdr->num_mtiles;
+    p1.n_tiles = c.I / 128;
+    p1.kblocks = c.H / GEMM_BK;
+    p1.T = c.T;
+    p1.E = c.E;
+    p1.I = c.I;
+    p1.H = c.H;
+    p1.kT = L.kTp;
+    p1.status = &hdr->status;
+    p1.w_perm = wperm;
+    p1.gu_out = gu;
+    p1.aw_out = aw;
+    GLR_LAUNCH(KID_BWD_RECOMPUTE, launch_gemm(GK_GATE_UP_BWD, p1, std::min(sms, L.max_mtiles * p1.n_tiles), s));
+
+    // 3. dA' = dOut_perm . W_down^T, then dw partials and the SwiGLU backward
+    GemmParams p2;
+    memset(&p2, 0, sizeof(p2));
+    if (!make_map_bf16(&p2.tmA0, dop, R, c.H, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p2.tmB0, W_down, (uint64_t)c.I * c.E, c.H, GEMM_BK, 128) ||
+        !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, GEMM_BK, 128))
+        return MOE_ERR_CUDA;
+    p2.mtiles = mtiles;
+    p2.num_mtiles = &hdr->num_mtiles;
+    p2.n_tiles = c.I / 256;
+    p2.kblocks = c.H / GEMM_BK;
+    p2.T = c.T;
+    p2.E = c.E;
+    p2.I = c.I;
+    p2.H = c.H;
+    p2.kT = L.kTp;
+    p2.status = &hdr->status;
+    p2.w_perm = wperm;
+    p2.gu_in = gu;
+    p2.dgu_out = dgu;
+    p2.dw_part = dwp;
+    GLR_LAUNCH(KID_BWD_DGRAD, launch_gemm(GK_DGRAD_DOWN, p2, std::min(sms, L.max_mtiles * p2.n_tiles), s));
+
+    // 4. dX_perm = [dG dU] . W_gate_up[e]: the down GEMM with K = 2I
+    GemmParams p3;
+    memset(&p3, 0, sizeof(p3));
+    if (!make_map_bf16(&p3.tmA0, dgu, R, 2ull * c.I, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p3.tmB0, W_gate_up, 2ull * c.I * c.E, c.H, 64, GEMM_BK) ||
+        !make_map_bf16(&p3.tmB1, shared_gate_up, 2ull * c.I, c.H, 64, GEMM_BK) ||
+        !make_map_bf16(&p3.tmOut, dx, R, c.H, 64, 32))
+        return MOE_ERR_CUDA;
+    p3.out = dx;
+    p3.mtiles = mtiles;
+    p3.num_mtiles = &hdr->num_mtiles;
+    p3.n_tiles = c.H / 256;
+    p3.kblocks = 2 * c.I / GEMM_BK;
+    p3.T = c.T;
+    p3.E = c.E;
+    p3.I = 2 * c.I;
+    p3.H = c.H;
+    p3.kT = L.kTp;
+    p3.ld_out = c.H;
+    p3.status = &hdr->status;
+    GLR_LAUNCH(KID_BWD_DX, launch_gemm(GK_DOWN, p3, std::min(sms, L.max_mtiles * p3.n_tiles), s));
+
+    // 5. d_hidden = sum over the token's rows (weights already applied), d topk_w
+    GLR_LAUNCH(KID_COMBINE, launch_combine(dx, slot_of, nullptr, nullptr, c.T, c.H, c.k, d_hidden, s, L.kTp));
+    GLR_LAUNCH(KID_BWD_MISC, launch_dw_reduce(slot_of, dwp, c.T * c.k, c.I / 256, d_topk_w, s));
+
+    // 6. weight gradients per expert, K over its rows: dW_down = (w a)^T dOut,
+    //    dW_gate_up = [dG dU]^T X
+    for (int which = 0; which < 2; ++which) {
+        GemmParams p4;
+        memset(&p4, 0, sizeof(p4));
+        const uint64_t F = which == 0 ? (uint64_t)c.I : 2ull * c.I;
+        bool ok = make_map_bf16(&p4.tmA0, which == 0 ? aw : dgu, R, F, 64, GEMM_BK);
+        if (which == 0) {
+            ok = ok && make_map_bf16(&p4.tmB0, dop, R, c.H, 64, GEMM_BK);
+            p4.tmB1 = p4.tmB0;
+            p4.b_row_shared = -1;
+        } else {
+            ok = ok && make_map_bf16(&p4.tmB0, xperm, (uint64_t)L.kTp, c.H, 64, GEMM_BK) &&
+                 make_map_bf16(&p4.tmB1, hidden, c.T, c.H, 64, GEMM_BK);
+            p4.b_row_shared = 0;
+        }
+        if (!ok)
+            return MOE_ERR_CUDA;
+        p4.out = which == 0 ? (void *)dW_down : (void *)dW_gate_up;
+        p4.out_shared = which == 0 ? (void *)d_shared_down : (void *)d_shared_gate_up;
+        p4.eoff = eoff;
+        p4.wg_fm = (int)(F / 128);
+        p4.wg_fn = c.H / 256;
+        p4.n_tiles = 1;
+        p4.num_tiles_static = (c.E + 1) * p4.wg_fm * p4.wg_fn;
+        p4.T = c.T;
+        p4.E = c.E;
+        p4.I = c.I;
+        p4.H = c.H;
+        p4.status = &hdr->status;
+        GLR_LAUNCH(KID_BWD_WGRAD, launch_gemm(GK_WGRAD, p4, std::min(sms, p4.num_tiles_static), s));
+    }
     g_last_launches = launches;
     return MOE_OK;
 }

@@ -50,7 +50,9 @@ struct GemmCfg;
 // the product a kind computes (the _SMALL kinds differ only in staging)
 __host__ __device__ constexpr int base_kind(int kind)
 {
-    return kind == GK_GATE_UP_SMALL ? GK_GATE_UP : kind == GK_DOWN_SMALL ? GK_DOWN : kind;
+    return (kind == GK_GATE_UP_SMALL || kind == GK_GATE_UP_BWD) ? GK_GATE_UP
+           : kind == GK_DOWN_SMALL                              ? GK_DOWN
+                                                                : kind;
 }
 
 template <>
@@ -112,6 +114,44 @@ struct GemmCfgSmall : GemmCfg<BASE> {
 template <>
 struct GemmCfg<GK_GATE_UP_SMALL> : GemmCfgSmall<GK_GATE_UP> {};
 
+// Backward: the gate/up products again, with an epilogue that keeps G and U.
+template <>
+struct GemmCfg<GK_GATE_UP_BWD> : GemmCfg<GK_GATE_UP> {
+    static constexpr int NBUF = 1;
+};
+
+// Backward: d(intermediate) = dOut_perm [rows, H] . W_down[e]^T, W_down[e]
+// read as [I, H] rows (K-major, 256 of the I columns per tile).
+template <>
+struct GemmCfg<GK_DGRAD_DOWN> {
+    static constexpr int BN = 256;
+    static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
+    static constexpr int B_HALF = 128 * GEMM_BK * 2;
+    static constexpr int B_BYTES = BN * GEMM_BK * 2;
+    static constexpr int STAGES = 4;
+    static constexpr int SLOTS = 2;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
+    static constexpr int A_ROWS = GEMM_BM;
+    static constexpr int NBUF = 1;
+};
+
+// Backward: weight gradient of one expert, [128 features] x [256 hidden]
+// per tile, K = the expert's (64-row padded) bucket rows; A and B MN-major.
+template <>
+struct GemmCfg<GK_WGRAD> {
+    static constexpr int BN = 256;
+    static constexpr int ATOM = 64 * GEMM_BK * 2;      // 64 columns x 64 rows, 8 KB
+    static constexpr int A_BYTES = 2 * ATOM;
+    static constexpr int B_BYTES = 4 * ATOM;
+    static constexpr int STAGES = 4;
+    static constexpr int SLOTS = 2;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, true, true);
+    static constexpr int A_ROWS = GEMM_BM;
+    static constexpr int NBUF = 1;
+};
+
 template <>
 struct GemmCfg<GK_DOWN_SMALL> : GemmCfgSmall<GK_DOWN> {};
 
@@ -136,6 +176,8 @@ struct TileInfo {
     int rows;     // valid rows (<= 128)
     int nt;       // n-tile index
     int shared;
+    int kblocks;  // K blocks of this tile
+    int b_row;    // GK_WGRAD: first B row
 };
 
 template <int KIND>
@@ -143,7 +185,25 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
 {
     TileInfo ti;
     ti.nt = tile % p.n_tiles;
+    ti.kblocks = p.kblocks;
+    ti.b_row = 0;
     constexpr int BASE = base_kind(KIND);
+    if constexpr (KIND == GK_WGRAD) {
+        // tile = (expert, feature block, hidden block); K over the expert's rows
+        const int per_e = p.wg_fm * p.wg_fn;
+        const int e = tile / per_e;
+        const int r = tile % per_e;
+        const int2 eo = p.eoff[e];
+        ti.group = e;
+        ti.shared = (e == p.E);
+        ti.nt = r % p.wg_fn;
+        ti.rows = 128;
+        ti.a_row = eo.x;
+        ti.b_row = (ti.shared && p.b_row_shared >= 0) ? p.b_row_shared : eo.x;
+        ti.kblocks = eo.y / GEMM_BK;
+        ti.out_row = (ti.shared ? 0 : e * p.wg_fm * 128) + (r / p.wg_fn) * 128;   // feature row of the output
+        return ti;
+    }
     if (BASE == GK_ROUTER) {
         ti.a_row = (tile / p.n_tiles) * GEMM_BM;
         ti.out_row = ti.a_row;
@@ -173,7 +233,24 @@ __device__ __forceinline__ void issue_loads(const GemmParams &p, const TileInfo 
     using C = GemmCfg<KIND>;
     constexpr int BASE = base_kind(KIND);
     const int k0 = kb * GEMM_BK;
-    if constexpr (BASE == GK_ROUTER) {
+    if constexpr (KIND == GK_WGRAD) {
+        // A: 128 features x 64 rows (two MN-major boxes), B: 256 hidden x 64 rows (four)
+        const int f0 = (ti.out_row % (p.wg_fm * 128));
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            tma_load_2d(sA + q * C::ATOM, &p.tmA0, bar, f0 + q * 64, ti.a_row + k0);
+        const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            tma_load_2d(sB + q * C::ATOM, mb, bar, ti.nt * C::BN + q * 64, ti.b_row + k0);
+    } else if constexpr (KIND == GK_DGRAD_DOWN) {
+        // A: dOut_perm rows (K = H); B: 256 rows of W_down[e] read as [I, H]
+        const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
+        const int wrow = (ti.shared ? 0 : ti.group * p.I) + ti.nt * C::BN;
+        tma_load_2d(sA, &p.tmA0, bar, k0, ti.a_row);
+        tma_load_2d(sB, mb, bar, k0, wrow);
+        tma_load_2d(sB + C::B_HALF, mb, bar, k0, wrow + 128);
+    } else if constexpr (BASE == GK_ROUTER) {
         tma_load_2d(sA, &p.tmA0, bar, k0, ti.a_row);
 #pragma unroll
         for (int s = 0; s < 3; ++s)
@@ -209,8 +286,12 @@ __device__ __forceinline__ void issue_mmas(uint32_t sA, uint32_t sB, uint32_t d,
             for (int s = 0; s < 3; ++s)
                 umma_bf16(d, ad, sdesc_kmajor_sw128(sB + s * C::B_PART + kk * 32), C::IDESC,
                           (acc_in || kk > 0 || s > 0) ? 1u : 0u);
-        } else if constexpr (BASE == GK_GATE_UP) {
+        } else if constexpr (BASE == GK_GATE_UP || KIND == GK_DGRAD_DOWN) {
             umma_bf16(d, ad, sdesc_kmajor_sw128(sB + kk * 32), C::IDESC, (acc_in || kk > 0) ? 1u : 0u);
+        } else if constexpr (KIND == GK_WGRAD) {
+            // both operands MN-major: 16 K rows = 2048 B into every 64-column atom
+            umma_bf16(d, sdesc_mnmajor_sw128(sA + kk * 2048, C::ATOM), sdesc_mnmajor_sw128(sB + kk * 2048, C::ATOM),
+                      C::IDESC, (acc_in || kk > 0) ? 1u : 0u);
         } else {
             // 16 K rows = two 8-row atoms = 2048 B further into each 64-wide N atom
             umma_bf16(d, ad, sdesc_mnmajor_sw128(sB + kk * 2048, C::B_ATOM), C::IDESC,
@@ -331,6 +412,147 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
     }
 }
 
+// ---------------------------------------------------------------- backward
+// Writes 16 bytes x 4 (64 bytes) of the warp's row `lane` at gdst, when valid.
+__device__ __forceinline__ void store_row64(char *gdst, const uint4 (&v)[4], bool valid)
+{
+    if (valid) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            reinterpret_cast<uint4 *>(gdst)[j] = v[j];
+    }
+}
+
+// GK_GATE_UP_BWD epilogue (one warp, 32 rows): for its 128 gate + 128 up
+// columns, G and U in fp32 into gu_out [rows, 2I] and
+// aw = bf16(w_row * bf16(silu(G) * U)) into aw_out [rows, I].
+__device__ __forceinline__ void epilogue_gu_bwd(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
+                                                int lane, uint8_t *stage)
+{
+    const int r = quad * 32 + lane;
+    const bool valid = r < ti.rows;
+    const int row = ti.out_row + r;
+    const float w = valid ? p.w_perm[row] : 0.0f;
+    const int valid_rows = ti.rows - quad * 32;
+    const size_t ld_gu = (size_t)2 * p.I * 4, ld_aw = (size_t)p.I * 2;
+    char *gu_base = reinterpret_cast<char *>(p.gu_out) + (size_t)(ti.out_row + quad * 32) * ld_gu;
+    char *aw_base = reinterpret_cast<char *>(p.aw_out) + (size_t)(ti.out_row + quad * 32) * ld_aw;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+        uint32_t g[32], u[32];
+        tmem_load32(tacc + c, g);
+        tmem_load32(tacc + 128 + c, u);
+        const int col = ti.nt * 128 + c;                 // intermediate column
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {           // G, then U: 32 fp32 = 128 bytes per row
+            uint4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t *src = half ? u : g;
+                v[q] = make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
+            }
+            warp_store_rows128(stage, v, lane, gu_base + (size_t)(half * p.I + col) * 4, ld_gu, valid_rows);
+        }
+        uint4 a4[4];
+        uint32_t *pk = reinterpret_cast<uint32_t *>(a4);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float a0 = __bfloat162float(__float2bfloat16_rn(
+                silu_times(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]))));
+            const float a1 = __bfloat162float(__float2bfloat16_rn(
+                silu_times(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]))));
+            pk[i] = pack_bf16x2(w * a0, w * a1);
+        }
+        store_row64(aw_base + (size_t)lane * ld_aw + (size_t)col * 2, a4, valid);
+    }
+}
+
+// GK_DGRAD_DOWN epilogue (one warp, 32 rows, 256 intermediate columns): the
+// accumulator is dA' = dOut . W_down^T; with a = bf16(silu(G) U) it adds the
+// row's partial <a, dA'> (d of the routing weight) to dw_part, then with
+// dA = w dA' and s = sigmoid(G):
+//   dG = dA U s (1 + G (1 - s)),  dU = dA G s   -> bf16 into dgu_out [rows, 2I].
+__device__ __forceinline__ void epilogue_dgrad(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
+                                               int lane)
+{
+    const int r = quad * 32 + lane;
+    const bool valid = r < ti.rows;
+    const int row = ti.out_row + r;
+    const float w = valid ? p.w_perm[row] : 0.0f;
+    const size_t I = (size_t)p.I;
+    const float *gu_row = p.gu_in + (size_t)row * 2 * I;
+    char *dgu_row = reinterpret_cast<char *>(p.dgu_out) + (size_t)row * 2 * I * 2;
+    float dwp = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+        uint32_t acc[32];
+        tmem_load32(tacc + c, acc);
+        const int col = ti.nt * 256 + c;
+        float G[32], U[32];
+        if (valid) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 g4 = reinterpret_cast<const float4 *>(gu_row + col)[q];
+                const float4 u4 = reinterpret_cast<const float4 *>(gu_row + I + col)[q];
+                G[4 * q] = g4.x; G[4 * q + 1] = g4.y; G[4 * q + 2] = g4.z; G[4 * q + 3] = g4.w;
+                U[4 * q] = u4.x; U[4 * q + 1] = u4.y; U[4 * q + 2] = u4.z; U[4 * q + 3] = u4.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                G[i] = U[i] = 0.0f;
+        }
+        uint4 dg4[4], du4[4];
+        uint32_t *pg = reinterpret_cast<uint32_t *>(dg4);
+        uint32_t *pu = reinterpret_cast<uint32_t *>(du4);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            float dgv[2], duv[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float g = G[i + h], u = U[i + h], da1 = __uint_as_float(acc[i + h]);
+                const float a = __bfloat162float(__float2bfloat16_rn(silu_times(g, u)));
+                dwp += a * da1;
+                const float s = 1.0f / (1.0f + __expf(-g));
+                const float da = w * da1;
+                dgv[h] = da * u * s * (1.0f + g * (1.0f - s));
+                duv[h] = da * g * s;
+            }
+            pg[i / 2] = pack_bf16x2(dgv[0], dgv[1]);
+            pu[i / 2] = pack_bf16x2(duv[0], duv[1]);
+        }
+        store_row64(dgu_row + (size_t)col * 2, dg4, valid);
+        store_row64(dgu_row + (I + col) * 2, du4, valid);
+    }
+    if (valid && !ti.shared)
+        p.dw_part[(size_t)row * p.n_tiles + ti.nt] = dwp;
+}
+
+// GK_WGRAD epilogue (one warp, 32 feature rows x 256 hidden columns, fp32);
+// an expert with no rows gets zeros.
+__device__ __forceinline__ void epilogue_wgrad(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
+                                               int lane, uint8_t *stage)
+{
+    const size_t ld = (size_t)p.H * 4;
+    char *base = static_cast<char *>(ti.shared ? p.out_shared : p.out) + (size_t)(ti.out_row + quad * 32) * ld +
+                 (size_t)ti.nt * 256 * 4;
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+        uint32_t r[32];
+        if (ti.kblocks > 0)
+            tmem_load32(tacc + c, r);
+        else
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                r[i] = 0u;
+        uint4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            v[q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        warp_store_rows128(stage, v, lane, base + (size_t)c * 4, ld, 32);
+    }
+}
+
 // Router epilogue warp: adds the K-block partial sums of its 32 rows in fp32
 // (K-block order, round-to-nearest), then writes the 128 logits of each row.
 __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem,
@@ -440,7 +662,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     // (the tile list, A rows) are read only after this
     pdl_wait();
 
-    const int num_tiles = ROUTER ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
+    const int num_tiles = (ROUTER || KIND == GK_WGRAD) ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
     const unsigned long long limit = p.wait_limit_ns ? p.wait_limit_ns : WAIT_LIMIT_NS;
 
     if (warp == 0) {
@@ -451,7 +673,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             bool ok = true;
             for (int tile = blockIdx.x; ok && !p.inject_withhold && tile < num_tiles; tile += gridDim.x) {
                 const TileInfo ti = tile_info<KIND>(p, tile);
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                for (int kb = 0; kb < ti.kblocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, limit)) {
                         ok = false;
                         break;
@@ -482,13 +704,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             bool ok = true;
             uint32_t ctr = 0;   // accumulators used so far (tiles, or K blocks for the router)
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int kblocks = (KIND == GK_WGRAD) ? tile_info<KIND>(p, tile).kblocks : p.kblocks;
                 if (!ROUTER) {
                     const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
                     if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit))
                         break;
                     tc_fence_after();
                 }
-                for (int kb = 0; kb < p.kblocks; ++kb) {
+                for (int kb = 0; kb < kblocks; ++kb) {
                     if (ROUTER) {
                         const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
                         if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit)) {
@@ -546,7 +769,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
                 __syncwarp();
                 tc_fence_after();
                 const uint32_t tacc = tmem + ((uint32_t)(quad * 32) << 16) + slot * C::BN;
-                epilogue_tile<KIND>(p, ti, tacc, quad, lane, stage, buf);
+                if constexpr (KIND == GK_GATE_UP_BWD)
+                    epilogue_gu_bwd(p, ti, tacc, quad, lane, stage);
+                else if constexpr (KIND == GK_DGRAD_DOWN)
+                    epilogue_dgrad(p, ti, tacc, quad, lane);
+                else if constexpr (KIND == GK_WGRAD)
+                    epilogue_wgrad(p, ti, tacc, quad, lane, stage);
+                else
+                    epilogue_tile<KIND>(p, ti, tacc, quad, lane, stage, buf);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
@@ -576,6 +806,9 @@ int gemm_smem_bytes(int kind)
     case GK_GATE_UP: return GemmLayout<GK_GATE_UP>::SMEM;
     case GK_GATE_UP_SMALL: return GemmLayout<GK_GATE_UP_SMALL>::SMEM;
     case GK_DOWN_SMALL: return GemmLayout<GK_DOWN_SMALL>::SMEM;
+    case GK_GATE_UP_BWD: return GemmLayout<GK_GATE_UP_BWD>::SMEM;
+    case GK_DGRAD_DOWN: return GemmLayout<GK_DGRAD_DOWN>::SMEM;
+    case GK_WGRAD: return GemmLayout<GK_WGRAD>::SMEM;
     default: return GemmLayout<GK_DOWN>::SMEM;
     }
 }
@@ -616,6 +849,9 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
     case GK_GATE_UP: return launch_kind<GK_GATE_UP>(p, grid, s);
     case GK_GATE_UP_SMALL: return launch_kind<GK_GATE_UP_SMALL>(p, grid, s);
     case GK_DOWN_SMALL: return launch_kind<GK_DOWN_SMALL>(p, grid, s);
+    case GK_GATE_UP_BWD: return launch_kind<GK_GATE_UP_BWD>(p, grid, s);
+    case GK_DGRAD_DOWN: return launch_kind<GK_DGRAD_DOWN>(p, grid, s);
+    case GK_WGRAD: return launch_kind<GK_WGRAD>(p, grid, s);
     default: return launch_kind<GK_DOWN>(p, grid, s);
     }
 }

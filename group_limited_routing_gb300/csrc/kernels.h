@@ -69,8 +69,17 @@ struct WsHeader {
 // The _SMALL kinds are the grouped GEMMs for T <= GEMM_SMALL_T (decode): every
 // bucket then has at most T rows, so only GEMM_SMALL_T A rows are loaded per
 // stage and the smem this frees goes to a deeper weight ring.
-enum GemmKind { GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4 };
+// Backward kinds: GK_GATE_UP_BWD recomputes the gate/up products (storing
+// G, U and the weighted intermediate); GK_DGRAD_DOWN is d(intermediate) =
+// dOut_perm . W_down^T with the SwiGLU backward in its epilogue; GK_WGRAD is
+// a per-expert weight gradient (M = features, N = hidden, K = the expert's
+// bucket rows, both operands MN-major).
+enum GemmKind {
+    GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4,
+    GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7
+};
 constexpr int GEMM_SMALL_T = 16;
+constexpr int BWD_ROW_ALIGN = 64;   // backward buckets start on 64-row boundaries (K blocks of the weight gradients)
 
 // Parameters of the tensor-core GEMM kernels.  Tensor maps live in the
 // kernel's parameter space (__grid_constant__), so TMA reads them in place.
@@ -89,6 +98,17 @@ struct GemmParams {
     int T, E, I, H, kT;
     int ld_out;           // output row stride in elements
     int *status;
+    // backward kinds
+    const float *w_perm;  // routing weight of every bucket row (1 for shared rows)
+    float *gu_out;        // GK_GATE_UP_BWD: G and U, fp32 [rows, 2I]
+    uint16_t *aw_out;     // GK_GATE_UP_BWD: bf16(w * bf16(silu(G) * U)) [rows, I]
+    const float *gu_in;   // GK_DGRAD_DOWN: G and U
+    uint16_t *dgu_out;    // GK_DGRAD_DOWN: dG and dU, bf16 [rows, 2I]
+    float *dw_part;       // GK_DGRAD_DOWN: per (row, n-tile) partial dot products [kT_padded, n_tiles]
+    const int2 *eoff;     // GK_WGRAD: per expert (first bucket row, padded rows); entry E = shared
+    void *out_shared;     // GK_WGRAD: the shared expert's gradient
+    int wg_fm, wg_fn;     // GK_WGRAD: feature blocks (128) and hidden blocks (256) per expert
+    int b_row_shared;     // GK_WGRAD: first B row of the shared expert, or -1 to use its A rows
     // fault injection for tests: when set, the producer issues no loads, so
     // the first wait of the MMA lane runs out after wait_limit_ns
     int inject_withhold;
@@ -137,8 +157,22 @@ cudaError_t launch_bucket_small(const int32_t *idx, const uint16_t *x, int T, in
 // m-tile list of a dense MLP: T tokens in tiles of mt rows, group 0
 cudaError_t launch_dense_tiles(int T, int mt, int4 *mtiles, WsHeader *hdr, cudaStream_t s);
 
+// out[t] = bf16( sum_j w[t,j] Y[slot_of[t,j]] + Y[shared_row0 + t] (+ residual[t]) );
+// w == NULL means every weight is 1; shared_row0 < 0 means k*T.
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
-                           int T, int H, int k, uint16_t *out, cudaStream_t s);
+                           int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0 = -1);
+
+// backward bucketing: as launch_bucket_scatter, buckets on BWD_ROW_ALIGN rows,
+// plus dOut rows and routing weights per bucket row and the bucket table eoff
+cudaError_t launch_bucket_scatter_bwd(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
+                                      const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
+                                      uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, const uint16_t *dout,
+                                      const float *w, uint16_t *do_perm, float *w_perm, int2 *eoff, int shared_base,
+                                      cudaStream_t s);
+cudaError_t launch_zero_pad(const int2 *eoff, const int32_t *sizes, int T, int E, int H, int I, uint16_t *x_perm,
+                            uint16_t *do_perm, uint16_t *aw, uint16_t *dgu, cudaStream_t s);
+cudaError_t launch_dw_reduce(const int32_t *slot_of, const float *dw_part, int n, int ntiles, float *dw,
+                             cudaStream_t s);
 
 cudaError_t launch_expert_feedback(const int32_t *counts, int E, int T, int k, float gamma, float *bias,
                                    long long *totals, cudaStream_t s);

@@ -99,18 +99,29 @@ cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes,
     return cudaPeekAtLastError();
 }
 
-// Bucket offsets (exclusive scan of the E sizes) and first m-tile of every
-// group, by a 256-thread block into shared memory; thread 0 also checks that
-// every pair was bucketed.  With `write_tiles`, the block writes the m-tile
-// list of the grouped GEMMs (the shared expert is group E, all T tokens).
+// Bucket offsets (exclusive scan of the E sizes, each rounded up to `pad`
+// rows: 1 for the forward, BWD_ROW_ALIGN for the backward) and first m-tile of
+// every group, by a 256-thread block into shared memory; thread 0 also checks
+// that every pair was bucketed.  With `write_tiles`, the block writes the
+// m-tile list of the grouped GEMMs (the shared expert is group E, all T
+// tokens) and, when eoff is given, every bucket's (first row, padded rows),
+// the shared expert's rows starting at shared_base.
 __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, int K, int *offset, int *tstart,
                                int *wsum_rows, int *wsum_tiles, bool write_tiles, int4 *__restrict__ mtiles,
-                               WsHeader *__restrict__ hdr)
+                               WsHeader *__restrict__ hdr, int pad = 1, int2 *__restrict__ eoff = nullptr,
+                               int shared_base = 0)
 {
+    __shared__ int true_rows;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int e = threadIdx.x;   // blockDim.x == 256 >= E
-    const int n = (e < E) ? sizes[e] : 0;
-    const int nt = (n + GEMM_BM - 1) / GEMM_BM;
+    const int n0 = (e < E) ? sizes[e] : 0;
+    const int n = (n0 + pad - 1) / pad * pad;    // rows the bucket occupies
+    const int nt = (n0 + GEMM_BM - 1) / GEMM_BM;
+    if (threadIdx.x == 0)
+        true_rows = 0;
+    __syncthreads();
+    if (n0)
+        atomicAdd(&true_rows, n0);               // integer: exact in any order
     int a = n, b = nt;           // inclusive warp scans
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -140,19 +151,23 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
             off += wsum_rows[q];
             tiles += wsum_tiles[q];
         }
-        offset[E] = off;             // == K*T unless indices were out of range
+        offset[E] = off;             // padded rows of all buckets (== K*T for pad 1 and valid indices)
         tstart[E] = tiles;
         if (write_tiles) {
             hdr->num_mtiles = tiles + (T + GEMM_BM - 1) / GEMM_BM;
-            if (off != K * T)
+            if (true_rows != K * T)
                 atomicOr(&hdr->status, ST_COUNT_MISMATCH);
+            if (eoff)
+                eoff[E] = make_int2(shared_base, (T + pad - 1) / pad * pad);
         }
     }
     __syncthreads();
     if (write_tiles) {
+        if (e < E && eoff)
+            eoff[e] = make_int2(offset[e], n);
         if (e < E)
-            for (int i = 0, r = 0; r < n; ++i, r += GEMM_BM)
-                mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n - r), 0);
+            for (int i = 0, r = 0; r < n0; ++i, r += GEMM_BM)
+                mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n0 - r), 0);
         const int ntile_sh = (T + GEMM_BM - 1) / GEMM_BM;
         for (int i = threadIdx.x; i < ntile_sh; i += blockDim.x)
             mtiles[tstart[E] + i] = make_int4(E, i * GEMM_BM, min(GEMM_BM, T - i * GEMM_BM), 0);
@@ -163,13 +178,26 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
 // Stable slots for one chunk, then the row gather.  Warp 0 assigns slots in
 // (token, j) order, 32 pairs at a time: lanes holding the same expert find
 // each other with __match_any_sync and take consecutive slots by lane rank.
+// With `bw` (the backward), buckets start on BWD_ROW_ALIGN-row boundaries,
+// every bucket row also receives the token's output gradient row (unweighted)
+// and its routing weight, and the shared expert's rows (after the padded
+// routed rows) receive every token's gradient row with weight 1.
+struct ScatterBwd {
+    const uint16_t *dout;   // [T, H]
+    const float *w;         // [T, K]
+    uint16_t *do_perm;      // [rows, H]
+    float *w_perm;          // [rows]
+    int2 *eoff;             // [E + 1]
+    int shared_base;        // first shared-expert row (past every routed row for any routing)
+};
+
 __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__restrict__ idx,
                                                              const uint16_t *__restrict__ x,
                                                              const int32_t *__restrict__ chunk_base,
                                                              const int32_t *__restrict__ sizes, int T, int H,
                                                              int E, int K, int32_t *__restrict__ slot_of,
                                                              uint16_t *__restrict__ x_perm, int4 *__restrict__ mtiles,
-                                                             WsHeader *__restrict__ hdr)
+                                                             WsHeader *__restrict__ hdr, ScatterBwd bw)
 {
     pdl_wait();
     __shared__ int offset[258];
@@ -181,7 +209,9 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
     int *slots = sm + E;       // [PERM_CHUNK * K]
     const int t0 = blockIdx.x * PERM_CHUNK;
     const int nt = min(PERM_CHUNK, T - t0);
-    bucket_offsets(sizes, T, E, K, offset, tstart, wsum_rows, wsum_tiles, blockIdx.x == 0, mtiles, hdr);
+    const bool backward = bw.do_perm != nullptr;
+    bucket_offsets(sizes, T, E, K, offset, tstart, wsum_rows, wsum_tiles, blockIdx.x == 0, mtiles, hdr,
+                   backward ? BWD_ROW_ALIGN : 1, bw.eoff, bw.shared_base);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         next[e] = offset[e] + chunk_base[(size_t)e * gridDim.x + blockIdx.x];   // [expert][chunk]
     __syncthreads();
@@ -205,9 +235,14 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
             if (in) {
                 slots[i] = slot;
                 slot_of[(size_t)t0 * K + i] = slot;
+                if (backward && slot >= 0)
+                    bw.w_perm[slot] = bw.w[(size_t)t0 * K + i];
             }
         }
     }
+    if (backward)
+        for (int tt = threadIdx.x; tt < nt; tt += blockDim.x)
+            bw.w_perm[bw.shared_base + t0 + tt] = 1.0f;   // shared-expert rows
     __syncthreads();
     // gather: each token row is read once and written to its K slots
     const int vec_per_row = H / 8;                    // 16-byte vectors
@@ -235,6 +270,21 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
                                 reinterpret_cast<uint4 *>(x_perm + (size_t)slot * H)[vv] = val[u];
                         }
                 }
+                if (backward) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int tt = tl + u * rows_per_pass;
+                        if (tt < nt) {
+                            const uint4 g = reinterpret_cast<const uint4 *>(bw.dout + (size_t)(t0 + tt) * H)[vv];
+                            reinterpret_cast<uint4 *>(bw.do_perm + (size_t)(bw.shared_base + t0 + tt) * H)[vv] = g;
+                            for (int j = 0; j < K; ++j) {
+                                const int slot = slots[tt * K + j];
+                                if (slot >= 0)
+                                    reinterpret_cast<uint4 *>(bw.do_perm + (size_t)slot * H)[vv] = g;
+                            }
+                        }
+                    }
+                }
             }
         }
     }
@@ -246,8 +296,88 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
 {
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
+    const ScatterBwd none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
-                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr);
+                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_bucket_scatter_bwd(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
+                                      const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
+                                      uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, const uint16_t *dout,
+                                      const float *w, uint16_t *do_perm, float *w_perm, int2 *eoff, int shared_base,
+                                      cudaStream_t s)
+{
+    const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
+    const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
+    const ScatterBwd bw = {dout, w, do_perm, w_perm, eoff, shared_base};
+    const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
+                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, bw);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+// Zeroes the padding rows of every backward bucket (the weight-gradient GEMMs
+// run their K loop over whole 64-row blocks): rows [first + n, first + padded)
+// of the routed buckets in x_perm and all three of do_perm, aw, dgu; of the
+// shared rows in do_perm, aw, dgu.  Block b takes bucket b (b == E: shared).
+__global__ void zero_pad_kernel(const int2 *__restrict__ eoff, const int32_t *__restrict__ sizes, int T, int E,
+                                int H, int I, uint16_t *__restrict__ x_perm, uint16_t *__restrict__ do_perm,
+                                uint16_t *__restrict__ aw, uint16_t *__restrict__ dgu)
+{
+    pdl_wait();
+    const int e = blockIdx.x;
+    const int2 eo = eoff[e];
+    const int n = (e < E) ? sizes[e] : T;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    for (int r = eo.x + n; r < eo.x + eo.y; ++r) {
+        for (int v = threadIdx.x; v < H / 8; v += blockDim.x) {
+            if (e < E)
+                reinterpret_cast<uint4 *>(x_perm + (size_t)r * H)[v] = z;
+            reinterpret_cast<uint4 *>(do_perm + (size_t)r * H)[v] = z;
+        }
+        for (int v = threadIdx.x; v < I / 8; v += blockDim.x)
+            reinterpret_cast<uint4 *>(aw + (size_t)r * I)[v] = z;
+        for (int v = threadIdx.x; v < 2 * I / 8; v += blockDim.x)
+            reinterpret_cast<uint4 *>(dgu + (size_t)r * 2 * I)[v] = z;
+    }
+}
+
+cudaError_t launch_zero_pad(const int2 *eoff, const int32_t *sizes, int T, int E, int H, int I, uint16_t *x_perm,
+                            uint16_t *do_perm, uint16_t *aw, uint16_t *dgu, cudaStream_t s)
+{
+    const cudaError_t le = launch_pdl(zero_pad_kernel, dim3(E + 1), dim3(256), 0, s, eoff, sizes, T, E, H, I, x_perm,
+                                      do_perm, aw, dgu);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+// d topk_w[t, j] = sum over the n-tiles of the partial dot products of the
+// pair's bucket row (fixed order); a skipped pair gets 0.
+__global__ void dw_reduce_kernel(const int32_t *__restrict__ slot_of, const float *__restrict__ dw_part, int n,
+                                 int ntiles, float *__restrict__ dw)
+{
+    pdl_wait();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n)
+        return;
+    const int slot = slot_of[i];
+    float v = 0.0f;
+    if (slot >= 0)
+        for (int q = 0; q < ntiles; ++q)
+            v += dw_part[(size_t)slot * ntiles + q];
+    dw[i] = v;
+}
+
+cudaError_t launch_dw_reduce(const int32_t *slot_of, const float *dw_part, int n, int ntiles, float *dw,
+                             cudaStream_t s)
+{
+    const cudaError_t le = launch_pdl(dw_reduce_kernel, dim3((n + 255) / 256), dim3(256), 0, s, slot_of, dw_part, n,
+                                      ntiles, dw);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
@@ -411,7 +541,7 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v, floa
 // One token's 16-byte column vector: the K expert rows (in batches of eight,
 // every load of a batch issued before any use) and the shared row.
 __device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, const int *s_slot, const float *s_w,
-                                            const uint16_t *__restrict__ residual, int T, int H, int K, int t,
+                                            const uint16_t *__restrict__ residual, size_t srow0, int H, int K, int t,
                                             int tl, int vv, uint16_t *__restrict__ out)
 {
     float acc[8], racc[8];
@@ -420,7 +550,7 @@ __device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, cons
         acc[q] = 0.0f;
         racc[q] = 0.0f;
     }
-    const uint4 sv = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + t) * H)[vv];
+    const uint4 sv = reinterpret_cast<const uint4 *>(Y + (srow0 + t) * H)[vv];
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     for (int j0 = 0; j0 < K; j0 += 8) {
         uint4 yv[8];
@@ -455,12 +585,12 @@ __device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, cons
 // Two tokens at once: both tokens' row loads are issued before any is used
 // (same arithmetic, in the same order, as combine_one for each token).
 __device__ __forceinline__ void combine_two(const uint16_t *__restrict__ Y, const int *s_slot, const float *s_w,
-                                            const uint16_t *__restrict__ residual, int T, int H, int K, int ta,
-                                            int tla, int tb, int tlb, int vv, uint16_t *__restrict__ out)
+                                            const uint16_t *__restrict__ residual, size_t srow0, int H, int K,
+                                            int ta, int tla, int tb, int tlb, int vv, uint16_t *__restrict__ out)
 {
     if (K > 8) {
-        combine_one(Y, s_slot, s_w, residual, T, H, K, ta, tla, vv, out);
-        combine_one(Y, s_slot, s_w, residual, T, H, K, tb, tlb, vv, out);
+        combine_one(Y, s_slot, s_w, residual, srow0, H, K, ta, tla, vv, out);
+        combine_one(Y, s_slot, s_w, residual, srow0, H, K, tb, tlb, vv, out);
         return;
     }
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
@@ -475,8 +605,8 @@ __device__ __forceinline__ void combine_two(const uint16_t *__restrict__ Y, cons
         ya[u] = (sa >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)sa * H)[vv] : zero;
         yb[u] = (sb >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)sb * H)[vv] : zero;
     }
-    const uint4 sva = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + ta) * H)[vv];
-    const uint4 svb = reinterpret_cast<const uint4 *>(Y + ((size_t)K * T + tb) * H)[vv];
+    const uint4 sva = reinterpret_cast<const uint4 *>(Y + (srow0 + ta) * H)[vv];
+    const uint4 svb = reinterpret_cast<const uint4 *>(Y + (srow0 + tb) * H)[vv];
     uint4 rva = zero, rvb = zero;
     if (residual) {
         rva = reinterpret_cast<const uint4 *>(residual + (size_t)ta * H)[vv];
@@ -514,7 +644,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                                                       const int32_t *__restrict__ slot_of,
                                                       const float *__restrict__ w,
                                                       const uint16_t *__restrict__ residual, int T, int H, int K,
-                                                      int ctok, uint16_t *__restrict__ out)
+                                                      int ctok, long long shared_row0, uint16_t *__restrict__ out)
 {
     pdl_wait();
     __shared__ int s_slot[COMBINE_TOK * 32];
@@ -529,7 +659,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
         __syncthreads();
         for (int i = threadIdx.x; i < nt * K; i += blockDim.x) {
             s_slot[i] = slot_of[(size_t)t0 * K + i];
-            s_w[i] = w[(size_t)t0 * K + i];
+            s_w[i] = w ? w[(size_t)t0 * K + i] : 1.0f;
         }
         __syncthreads();
         if (sub >= rpp)
@@ -537,17 +667,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
         for (int vv = v; vv < vpr; vv += blockDim.x) {
             for (int tl = sub; tl < nt; tl += 2 * rpp) {
                 if (tl + rpp < nt)
-                    combine_two(Y, s_slot, s_w, residual, T, H, K, t0 + tl, tl, t0 + tl + rpp, tl + rpp, vv, out);
+                    combine_two(Y, s_slot, s_w, residual, (size_t)shared_row0, H, K, t0 + tl, tl, t0 + tl + rpp,
+                                tl + rpp, vv, out);
                 else
-                    combine_one(Y, s_slot, s_w, residual, T, H, K, t0 + tl, tl, vv, out);
+                    combine_one(Y, s_slot, s_w, residual, (size_t)shared_row0, H, K, t0 + tl, tl, vv, out);
             }
         }
     }
 }
 
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
-                           int T, int H, int k, uint16_t *out, cudaStream_t s)
+                           int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0)
 {
+    if (shared_row0 < 0)
+        shared_row0 = (long long)k * T;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -559,7 +692,7 @@ cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const floa
     const int nchunks = (T + ctok - 1) / ctok;
     const int blocks = min(nchunks, sms * 8);
     const cudaError_t le = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, Y, slot_of, w, residual, T, H, k,
-                                      ctok, out);
+                                      ctok, shared_row0, out);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

@@ -206,6 +206,37 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
     return out
 
 
+def backward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, d_out,
+             *, ws: Optional[Workspace] = None):
+    """moe_backward (routing fixed): dict(d_hidden [T,H] bf16, dW_gate_up
+    [E,2I,H] fp32, dW_down [E,I,H] fp32, d_shared_gate_up [2Is,H] fp32,
+    d_shared_down [Is,H] fp32, d_topk_w [T,k] fp32)."""
+    dev = hidden.device
+    bf = torch.bfloat16
+    ph = _need(hidden, "hidden", bf, (cfg.T, cfg.H), dev)
+    pgu = _need(W_gate_up, "W_gate_up", bf, (cfg.E, 2 * cfg.I, cfg.H), dev)
+    pd = _need(W_down, "W_down", bf, (cfg.E, cfg.I, cfg.H), dev)
+    psgu = _need(shared_gate_up, "shared_gate_up", bf, (2 * cfg.Is, cfg.H), dev)
+    psd = _need(shared_down, "shared_down", bf, (cfg.Is, cfg.H), dev)
+    pi = _need(topk_idx, "topk_idx", torch.int32, (cfg.T, cfg.k), dev)
+    pw = _need(topk_w, "topk_w", torch.float32, (cfg.T, cfg.k), dev)
+    pdo = _need(d_out, "d_out", bf, (cfg.T, cfg.H), dev)
+    f32 = torch.float32
+    g = dict(d_hidden=torch.empty(cfg.T, cfg.H, dtype=bf, device=dev),
+             dW_gate_up=torch.empty(cfg.E, 2 * cfg.I, cfg.H, dtype=f32, device=dev),
+             dW_down=torch.empty(cfg.E, cfg.I, cfg.H, dtype=f32, device=dev),
+             d_shared_gate_up=torch.empty(2 * cfg.Is, cfg.H, dtype=f32, device=dev),
+             d_shared_down=torch.empty(cfg.Is, cfg.H, dtype=f32, device=dev),
+             d_topk_w=torch.empty(cfg.T, cfg.k, dtype=f32, device=dev))
+    ws = _ws(ws, cfg, _lib.MOE_WS_BACKWARD, dev)
+    rc = _lib.load().moe_backward(ctypes.byref(cfg.c()), ph, pgu, pd, psgu, psd, pi, pw, pdo,
+                                  g["d_hidden"].data_ptr(), g["dW_gate_up"].data_ptr(), g["dW_down"].data_ptr(),
+                                  g["d_shared_gate_up"].data_ptr(), g["d_shared_down"].data_ptr(),
+                                  g["d_topk_w"].data_ptr(), ws.ptr, ws.nbytes, _stream(dev))
+    _lib.check(rc, "moe_backward")
+    return g
+
+
 class DenseWorkspace:
     """A device workspace for moe_dense_ffn (T tokens, hidden H, inner size I)."""
 

@@ -85,6 +85,7 @@ typedef struct moe_cfg {
 /* workspace kinds */
 #define MOE_WS_ROUTE 0
 #define MOE_WS_FORWARD 1
+#define MOE_WS_BACKWARD 2
 
 /* Bytes of workspace that moe_route (which = MOE_WS_ROUTE) or moe_forward
  * (which = MOE_WS_FORWARD) needs for this configuration; 0 if the
@@ -181,6 +182,25 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
                 const int32_t *topk_idx, const float *topk_w, const moe_bf16 *residual,
                 moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
 
+/* Backward of moe_forward for fixed routing (the training step of the layer;
+ * the routing page trains the layer but prints no backward: these are the
+ * gradients of the forward above, the bf16 rounding of the intermediate
+ * passed through as the identity).  Given d_out [T, H] bf16 = dL/d out:
+ *   d_hidden        [T, H] bf16 out: dL/d hidden through the experts and the
+ *                   shared expert (the residual's own identity path is not
+ *                   added; the router's contribution is not included)
+ *   dW_gate_up      [E, 2I, H] fp32 out, dW_down [E, I, H] fp32 out,
+ *   d_shared_gate_up [2I, H] fp32 out, d_shared_down [I, H] fp32 out: the
+ *                   weight gradients summed over the T tokens (overwritten)
+ *   d_topk_w        [T, k] fp32 out: <d_out[t], expert_{topk_idx[t,j]}(hidden[t])>
+ * Other arguments as moe_forward; I % 256 == 0; workspace of
+ * moe_workspace_bytes(cfg, MOE_WS_BACKWARD) bytes.  Deterministic. */
+int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_gate_up,
+                 const moe_bf16 *W_down, const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down,
+                 const int32_t *topk_idx, const float *topk_w, const moe_bf16 *d_out,
+                 moe_bf16 *d_hidden, float *dW_gate_up, float *dW_down, float *d_shared_gate_up,
+                 float *d_shared_down, float *d_topk_w, void *ws, size_t ws_bytes, void *stream);
+
 /* Dense SwiGLU MLP: the first decoder layer of the model on the routing page
  * ("first_k_dense_replace = 1", section 五: layer 0 is an ordinary MLP, the
  * 19 layers after it are MoE).  The page gives the layer neither a formula
@@ -261,7 +281,7 @@ int moe_last_launch_count(void);
  * the recorded events, folds them into per-kernel totals and returns the
  * total milliseconds and launch count of kernel `kernel_id` (0 <=
  * kernel_id < MOE_KERNEL_COUNT), clearing them when reset != 0. */
-#define MOE_KERNEL_COUNT 11
+#define MOE_KERNEL_COUNT 16
 int moe_profile_enable(int on);
 int moe_profile_read(int kernel_id, double *total_ms, int32_t *launches, int reset);
 const char *moe_kernel_name(int kernel_id);
