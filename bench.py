@@ -167,7 +167,9 @@ def algorithmic_work(T, H, E, I, k):
     }
 
 
-def workload_name(w0, dense=0):
+def workload_name(w0, dense=0, backward=False):
+    if backward:
+        return "backward of: " + workload_name_moe(w0)
     if dense:
         return "dense first-layer SwiGLU MLP, T=%d, H=%d, I=%d (size assumed)" % (w0.T, w0.H, dense)
     return workload_name_moe(w0)
@@ -247,6 +249,49 @@ class CpuSample:
 
 
 # ------------------------------------------------------------------- ours
+class BackwardStep:
+    """The layer's backward as the timed step: routing and d_out fixed (one
+    forward call routes the batch); __call__ runs moe_backward into
+    preallocated gradients."""
+
+    def __init__(self, layer, x, seed=99):
+        self.layer = layer
+        self.cfg = layer.cfg
+        self.device = layer.device
+        layer(x)
+        g = torch.Generator(device=x.device)
+        g.manual_seed(seed)
+        self.d_out = torch.randn(x.shape, generator=g, device=x.device).to(torch.bfloat16)
+        self.grads = layer.backward(self.d_out)
+        self.last_launches = 0
+
+    def __call__(self, x, out=None):
+        from group_limited_routing_gb300 import moe
+        if out is not None:
+            self.grads["d_hidden"] = out
+        L = self.layer
+        moe.backward(L.cfg, x, L.W_gate_up, L.W_down, L.shared_gate_up, L.shared_down, L.routing[0], L.routing[1],
+                     self.d_out, ws=L.ws_bwd, out=self.grads)
+        self.last_launches = moe.last_launch_count()
+        return self.grads["d_hidden"]
+
+    def status(self):
+        return self.layer.status()
+
+
+def backward_work(T, H, E, I, k):
+    """Algorithmic work per launch of the backward's kernels (weight-gradient
+    GEMMs: the mean of its two launches, dW_down and dW_gate_up)."""
+    R = (k + 1) * T
+    return {
+        "bwd_gate_up_recompute": dict(bound="tensor", flops=2.0 * R * H * 2 * I, bytes=R * H * 2 + 3 * E * I * H * 2),
+        "bwd_dgrad_down_swiglu": dict(bound="tensor", flops=2.0 * R * H * I, bytes=R * H * 2 + E * I * H * 2),
+        "bwd_dgrad_x": dict(bound="tensor", flops=2.0 * R * 2 * I * H, bytes=R * 2 * I * 2 + 2 * E * I * H * 2),
+        "bwd_weight_grads": dict(bound="tensor", flops=3.0 * R * I * H, bytes=R * H * 2 + 3 * E * I * H * 2),
+        "combine": dict(bound="hbm", bytes=R * H * 2 + T * H * 2 + T * k * 4),
+    }
+
+
 def build_model(w0, dev, dense_inter=0):
     """The step's model: one MoE layer, the 19-layer stack of workload 5, or
     (dense_inter > 0) the dense first-layer MLP of that intermediate size."""
@@ -282,6 +327,8 @@ def run_ours(args, world, rank, local):
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
     cfg, layer = build_model(w0, dev, args.dense)
     x = wl.hidden(w0, dev, layer=rank)      # each replica its own batch
+    if args.backward:
+        layer = BackwardStep(layer, x)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -365,7 +412,7 @@ def run_ours(args, world, rank, local):
 
     # ---- end to end through the public API: pinned host in, pinned host out
     e2e_ms = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.backward:
         e2e_ms = time_e2e(args, world, layer, x, out, stream, dev)
 
     if rank != 0:
@@ -376,7 +423,8 @@ def run_ours(args, world, rank, local):
         counts = layer.routing[2].double().cpu()
         hot_share = float(counts[hot].sum() / counts.sum())
     return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk,
-                  dict(flush=flush, lead=lead, hot_share=hot_share, graph_ms=graph_ms, dense=args.dense))
+                  dict(flush=flush, lead=lead, hot_share=hot_share, graph_ms=graph_ms, dense=args.dense,
+                       backward=args.backward))
 
 
 def time_e2e(args, world, layer, x, out, stream, dev):
@@ -420,7 +468,12 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
     """nprof = layer-steps profiled (steps x layers): per-stage numbers are per layer."""
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
     pk = peaks()
-    work = dense_work(T, H, extra["dense"]) if extra["dense"] else algorithmic_work(T, H, E, I, k)
+    if extra["backward"]:
+        work = backward_work(T, H, E, I, k)
+    elif extra["dense"]:
+        work = dense_work(T, H, extra["dense"])
+    else:
+        work = algorithmic_work(T, H, E, I, k)
     stages = {}
     for name, (tot, n) in prof.items():
         if n == 0:
@@ -442,15 +495,21 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
                 "bucket_scatter")
     rp_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in rp_names if n in stages)
     rp_bytes = T * H * 2 + E * H * 4 + T * k * 8 + T * k * 4 * 2 + T * H * 2 + k * T * H * 2
+    if extra["backward"]:
+        # the backward's bucketing: x and d_out read, both permuted ((k+1)T rows each) written
+        rp_bytes = 2 * T * H * 2 + T * k * 8 + 2 * (k + 1) * T * H * 2
     if rp_ms > 0:
         stages["router_plus_permute"] = {"ms": round(rp_ms, 4), "bound": "hbm",
                                          "gbs": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
                                          "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / pk["hbm"], 4)}
-    g1 = work["gemm_gate_up_swiglu"]
-    g1_ms = prof["gemm_gate_up_swiglu"][0] / max(1, prof["gemm_gate_up_swiglu"][1])
+    # the roofline kernel: the tensor-core stage with the most time per step
+    tensor_stages = [n for n in work if work[n]["bound"] == "tensor" and prof.get(n, (0, 0))[1] > 0]
+    dom = max(tensor_stages, key=lambda n: prof[n][0])
+    g1 = work[dom]
+    g1_ms = prof[dom][0] / max(1, prof[dom][1])
     g1_tf = g1["flops"] / (g1_ms * 1e-3) / 1e12
-    gemms_ms = g1_ms + stages.get("gemm_down", {"ms": 0})["ms"]
-    gemm_flops = work["gemm_gate_up_swiglu"]["flops"] + work["gemm_down"]["flops"]
+    gemms_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in tensor_stages)
+    gemm_flops = sum(work[n]["flops"] * stages[n]["launches_per_step"] for n in tensor_stages)
     stages["expert_gemms"] = {"ms": round(gemms_ms, 4), "bound": "tensor",
                               "tflops": round(gemm_flops / (gemms_ms * 1e-3) / 1e12, 1),
                               "frac": round(gemm_flops / (gemms_ms * 1e-3) / 1e12 / pk["bf16_sustained"], 4)}
@@ -469,7 +528,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded; shapes and distributions of the workload)",
-        "config": {"workload": workload_name(w0, extra["dense"]),
+        "config": {"workload": workload_name(w0, extra["dense"], extra["backward"]),
                    "T_per_gpu": T, "hidden": H, "experts": E, "groups": w0.n_group, "topk_group": w0.topk_group,
                    "k": k, "inter": I, "shared_inter": w0.Is, "layers": w0.layers,
                    "parallelism": "replicas (dp%d)" % world,
@@ -478,10 +537,11 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
                           "expert weights (%.2f GB per layer) larger than L2, no flush" % (3 * E * I * H * 2 / 1e9)),
                    "untimed_lead_in_steps": extra["lead"],
                    "hot_expert_share": None if extra["hot_share"] is None else round(extra["hot_share"], 4)},
-        "roofline": {"kernel": "gemm_gate_up_swiglu", "bound": "tensor", "achieved": round(g1_tf, 1),
+        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(g1_tf, 1),
                      "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                      "frac": round(g1_tf / pk["bf16_sustained"], 4),
-                     "traffic": gemm_traffic("gemm_gate_up_swiglu") if T == 32768 and not extra["dense"] else None,
+                     "traffic": gemm_traffic(dom) if T == 32768 and not (extra["dense"] or extra["backward"])
+                     else None,
                      "traffic_unit": "bytes per launch (ncu dram read + write, profiles/gemm_dram_traffic_T32768.md)",
                      "peak_kind": "%s bf16 dense, sustained" % pk["source"],
                      "algorithmic_flops_per_launch": g1["flops"]},
@@ -496,7 +556,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         "gpu_launches": launches,
         "clocks": clk.summary(),
     }
-    if world == 1 and not args.no_cpu_baseline and not extra["dense"]:
+    if world == 1 and not args.no_cpu_baseline and not extra["dense"] and not extra["backward"]:
         sample = CpuSample(args.workload)
         tps, thr, secs = sample.run(args.cpu_tokens)
         line["cpu_baseline"] = {"value": round(tps, 2), "unit": "tokens/s", "cores": thr, "kind": "oracle",
@@ -566,6 +626,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the layer's backward (moe_backward, routing fixed) instead of its forward")
     ap.add_argument("--dense", type=int, default=0, metavar="I",
                     help="time the dense first-layer MLP of intermediate size I instead of the MoE layer")
     ap.add_argument("--flush-l2", action="store_true",

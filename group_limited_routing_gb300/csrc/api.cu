@@ -181,15 +181,16 @@ struct BwdLayout {
 };
 
 // Backward workspace.  Buckets start on BWD_ROW_ALIGN-row boundaries, so the
-// routed rows take at most kTp = k T + E (BWD_ROW_ALIGN - 1); the shared
-// expert's rows follow at kTp whatever the routing, padded to a whole block.
+// routed rows take at most k T + E (BWD_ROW_ALIGN - 1), rounded up to kTp;
+// the shared expert's rows follow at kTp whatever the routing, padded to a
+// whole block.  G and U (gu) are kept warp-interleaved (32-row blocks).
 BwdLayout bwd_layout(const moe_cfg &c)
 {
     BwdLayout L;
     const size_t T = c.T, K = c.k, H = c.H, I = c.I;
     L.nchunk = (c.T + PERM_CHUNK - 1) / PERM_CHUNK;
     L.max_mtiles = (int)((K * T) / GEMM_BM + c.E + (T + GEMM_BM - 1) / GEMM_BM + 1);
-    L.kTp = (int)(K * T + (size_t)c.E * (BWD_ROW_ALIGN - 1));
+    L.kTp = (int)align_up(K * T + (size_t)c.E * (BWD_ROW_ALIGN - 1), BWD_ROW_ALIGN);
     L.rows = L.kTp + (c.T + BWD_ROW_ALIGN - 1) / BWD_ROW_ALIGN * BWD_ROW_ALIGN;
     const size_t R = (size_t)L.rows;
     size_t off = sizeof(WsHeader);
@@ -706,6 +707,8 @@ int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_g
     p1.H = c.H;
     p1.kT = L.kTp;
     p1.status = &hdr->status;
+    if (!make_map_bf16(&p1.tmOut, aw, R, c.I, 64, 32))
+        return MOE_ERR_CUDA;
     p1.w_perm = wperm;
     p1.gu_out = gu;
     p1.aw_out = aw;
@@ -716,7 +719,8 @@ int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_g
     memset(&p2, 0, sizeof(p2));
     if (!make_map_bf16(&p2.tmA0, dop, R, c.H, GEMM_BK, GEMM_BM) ||
         !make_map_bf16(&p2.tmB0, W_down, (uint64_t)c.I * c.E, c.H, GEMM_BK, 128) ||
-        !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, GEMM_BK, 128))
+        !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, GEMM_BK, 128) ||
+        !make_map_bf16(&p2.tmOut, dgu, R, 2ull * c.I, 64, 32))
         return MOE_ERR_CUDA;
     p2.mtiles = mtiles;
     p2.num_mtiles = &hdr->num_mtiles;

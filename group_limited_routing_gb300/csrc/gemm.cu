@@ -116,9 +116,7 @@ struct GemmCfg<GK_GATE_UP_SMALL> : GemmCfgSmall<GK_GATE_UP> {};
 
 // Backward: the gate/up products again, with an epilogue that keeps G and U.
 template <>
-struct GemmCfg<GK_GATE_UP_BWD> : GemmCfg<GK_GATE_UP> {
-    static constexpr int NBUF = 1;
-};
+struct GemmCfg<GK_GATE_UP_BWD> : GemmCfg<GK_GATE_UP> {};
 
 // Backward: d(intermediate) = dOut_perm [rows, H] . W_down[e]^T, W_down[e]
 // read as [I, H] rows (K-major, 256 of the I columns per tile).
@@ -133,7 +131,7 @@ struct GemmCfg<GK_DGRAD_DOWN> {
     static constexpr int TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
     static constexpr int A_ROWS = GEMM_BM;
-    static constexpr int NBUF = 1;
+    static constexpr int NBUF = 2;
 };
 
 // Backward: weight gradient of one expert, [128 features] x [256 hidden]
@@ -311,6 +309,19 @@ __device__ __forceinline__ float silu_times(float g, float u)
     return g / (1.0f + __expf(-g)) * u;
 }
 
+// sigmoid(g) for the backward epilogues: one exponential and an approximate
+// (branch-free) reciprocal, so that a lane's 32 columns run side by side.
+// g -> -inf gives 1 / inf = 0, g -> +inf gives 1.
+__device__ __forceinline__ float sigmoid_fast(float g)
+{
+    return __fdividef(1.0f, 1.0f + __expf(-g));
+}
+
+__device__ __forceinline__ float round_bf16(float x)
+{
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 // Writes one 128-byte piece of each of the warp's 32 rows (lane = row, eight
 // 16-byte chunks in v) to global memory.  The pieces go through the warp's
 // 4 KB staging buffer (16-byte chunks XOR-swizzled by row, so both the
@@ -413,57 +424,60 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
 }
 
 // ---------------------------------------------------------------- backward
-// Writes 16 bytes x 4 (64 bytes) of the warp's row `lane` at gdst, when valid.
-__device__ __forceinline__ void store_row64(char *gdst, const uint4 (&v)[4], bool valid)
+// G and U of the backward live in a warp-interleaved layout: for each block of
+// 32 rows b and each group j of 4 columns of [G | U] (2I fp32 per row), the
+// 16-byte pieces of the block's 32 rows lie side by side, at byte
+// ((b * 2I / 4 + j) * 32 + row % 32) * 16.  An epilogue warp holds one row
+// per lane, so each of its loads and stores moves 512 contiguous bytes.
+// Blocks never straddle two buckets: buckets start on 64-row boundaries.
+__device__ __forceinline__ float4 *gu_piece(float *gu, int I, int row, int col)
 {
-    if (valid) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            reinterpret_cast<uint4 *>(gdst)[j] = v[j];
-    }
+    const size_t b = (size_t)(row >> 5), j = (size_t)(col >> 2);
+    return reinterpret_cast<float4 *>(gu) + ((b * (size_t)(I >> 1) + j) << 5) + (row & 31);
 }
 
 // GK_GATE_UP_BWD epilogue (one warp, 32 rows): for its 128 gate + 128 up
-// columns, G and U in fp32 into gu_out [rows, 2I] and
-// aw = bf16(w_row * bf16(silu(G) * U)) into aw_out [rows, I].
+// columns, G and U (fp32, interleaved as above) into gu_out and
+// aw = bf16(w_row * bf16(silu(G) * U)) into aw_out [rows, I] (TMA stores).
 __device__ __forceinline__ void epilogue_gu_bwd(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
-                                                int lane, uint8_t *stage)
+                                                int lane, uint8_t *stage2, int &buf)
 {
     const int r = quad * 32 + lane;
     const bool valid = r < ti.rows;
     const int row = ti.out_row + r;
     const float w = valid ? p.w_perm[row] : 0.0f;
     const int valid_rows = ti.rows - quad * 32;
-    const size_t ld_gu = (size_t)2 * p.I * 4, ld_aw = (size_t)p.I * 2;
-    char *gu_base = reinterpret_cast<char *>(p.gu_out) + (size_t)(ti.out_row + quad * 32) * ld_gu;
-    char *aw_base = reinterpret_cast<char *>(p.aw_out) + (size_t)(ti.out_row + quad * 32) * ld_aw;
+    const int row0 = ti.out_row + quad * 32;
+    const size_t ld_aw = (size_t)p.I * 2;
+    char *aw_base = reinterpret_cast<char *>(p.aw_out) + (size_t)row0 * ld_aw;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
-        uint32_t g[32], u[32];
-        tmem_load32(tacc + c, g);
-        tmem_load32(tacc + 128 + c, u);
+    for (int c = 0; c < 128; c += 64) {
+        uint32_t g[64], u[64];
+        tmem_load64(tacc + c, g);
+        tmem_load64(tacc + 128 + c, u);
         const int col = ti.nt * 128 + c;                 // intermediate column
+        if (valid) {
+            float4 *pg = gu_piece(p.gu_out, p.I, row, col);
+            float4 *pu = gu_piece(p.gu_out, p.I, row, p.I + col);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {           // G, then U: 32 fp32 = 128 bytes per row
-            uint4 v[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t *src = half ? u : g;
-                v[q] = make_uint4(src[4 * q], src[4 * q + 1], src[4 * q + 2], src[4 * q + 3]);
+            for (int q = 0; q < 16; ++q) {
+                pg[32 * q] = make_float4(__uint_as_float(g[4 * q]), __uint_as_float(g[4 * q + 1]),
+                                         __uint_as_float(g[4 * q + 2]), __uint_as_float(g[4 * q + 3]));
+                pu[32 * q] = make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
+                                         __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3]));
             }
-            warp_store_rows128(stage, v, lane, gu_base + (size_t)(half * p.I + col) * 4, ld_gu, valid_rows);
         }
-        uint4 a4[4];
-        uint32_t *pk = reinterpret_cast<uint32_t *>(a4);
+        uint4 v[8];
+        uint32_t *pk = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float a0 = __bfloat162float(__float2bfloat16_rn(
-                silu_times(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i]))));
-            const float a1 = __bfloat162float(__float2bfloat16_rn(
-                silu_times(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1]))));
+        for (int i = 0; i < 32; ++i) {
+            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+            const float a0 = round_bf16(g0 * sigmoid_fast(g0) * __uint_as_float(u[2 * i]));
+            const float a1 = round_bf16(g1 * sigmoid_fast(g1) * __uint_as_float(u[2 * i + 1]));
             pk[i] = pack_bf16x2(w * a0, w * a1);
         }
-        store_row64(aw_base + (size_t)lane * ld_aw + (size_t)col * 2, a4, valid);
+        store_piece<GemmCfg<GK_GATE_UP_BWD>::NBUF>(p, stage2, buf, v, lane, valid_rows, aw_base + (size_t)col * 2,
+                                                   ld_aw, col, row0);
     }
 }
 
@@ -471,58 +485,68 @@ __device__ __forceinline__ void epilogue_gu_bwd(const GemmParams &p, const TileI
 // accumulator is dA' = dOut . W_down^T; with a = bf16(silu(G) U) it adds the
 // row's partial <a, dA'> (d of the routing weight) to dw_part, then with
 // dA = w dA' and s = sigmoid(G):
-//   dG = dA U s (1 + G (1 - s)),  dU = dA G s   -> bf16 into dgu_out [rows, 2I].
+//   dG = dA U s (1 + G (1 - s)),  dU = dA G s   -> bf16 into dgu_out [rows, 2I]
+// (TMA stores, 64 columns of dG and of dU at a time).
 __device__ __forceinline__ void epilogue_dgrad(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
-                                               int lane)
+                                               int lane, uint8_t *stage2, int &buf)
 {
     const int r = quad * 32 + lane;
     const bool valid = r < ti.rows;
     const int row = ti.out_row + r;
     const float w = valid ? p.w_perm[row] : 0.0f;
-    const size_t I = (size_t)p.I;
-    const float *gu_row = p.gu_in + (size_t)row * 2 * I;
-    char *dgu_row = reinterpret_cast<char *>(p.dgu_out) + (size_t)row * 2 * I * 2;
+    const int valid_rows = ti.rows - quad * 32;
+    const int row0 = ti.out_row + quad * 32;
+    const int I = p.I;
+    const size_t ld = (size_t)2 * I * 2;
+    char *dgu_base = reinterpret_cast<char *>(p.dgu_out) + (size_t)row0 * ld;
     float dwp = 0.0f;
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
-        uint32_t acc[32];
-        tmem_load32(tacc + c, acc);
-        const int col = ti.nt * 256 + c;
-        float G[32], U[32];
-        if (valid) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 g4 = reinterpret_cast<const float4 *>(gu_row + col)[q];
-                const float4 u4 = reinterpret_cast<const float4 *>(gu_row + I + col)[q];
-                G[4 * q] = g4.x; G[4 * q + 1] = g4.y; G[4 * q + 2] = g4.z; G[4 * q + 3] = g4.w;
-                U[4 * q] = u4.x; U[4 * q + 1] = u4.y; U[4 * q + 2] = u4.z; U[4 * q + 3] = u4.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                G[i] = U[i] = 0.0f;
-        }
-        uint4 dg4[4], du4[4];
+    for (int c = 0; c < 256; c += 64) {
+        uint4 dg4[8], du4[8];
         uint32_t *pg = reinterpret_cast<uint32_t *>(dg4);
         uint32_t *pu = reinterpret_cast<uint32_t *>(du4);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-            float dgv[2], duv[2];
+        for (int half = 0; half < 2; ++half) {
+            uint32_t acc[32];
+            tmem_load32(tacc + c + half * 32, acc);
+            const int col = ti.nt * 256 + c + half * 32;
+            float G[32], U[32];
+            if (valid) {
+                const float4 *sg = gu_piece(const_cast<float *>(p.gu_in), I, row, col);
+                const float4 *su = gu_piece(const_cast<float *>(p.gu_in), I, row, I + col);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const float g = G[i + h], u = U[i + h], da1 = __uint_as_float(acc[i + h]);
-                const float a = __bfloat162float(__float2bfloat16_rn(silu_times(g, u)));
-                dwp += a * da1;
-                const float s = 1.0f / (1.0f + __expf(-g));
-                const float da = w * da1;
-                dgv[h] = da * u * s * (1.0f + g * (1.0f - s));
-                duv[h] = da * g * s;
+                for (int q = 0; q < 8; ++q) {
+                    const float4 g4 = sg[32 * q], u4 = su[32 * q];
+                    G[4 * q] = g4.x; G[4 * q + 1] = g4.y; G[4 * q + 2] = g4.z; G[4 * q + 3] = g4.w;
+                    U[4 * q] = u4.x; U[4 * q + 1] = u4.y; U[4 * q + 2] = u4.z; U[4 * q + 3] = u4.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    G[i] = U[i] = 0.0f;
             }
-            pg[i / 2] = pack_bf16x2(dgv[0], dgv[1]);
-            pu[i / 2] = pack_bf16x2(duv[0], duv[1]);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float dgv[2], duv[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float g = G[i + h], u = U[i + h], da1 = __uint_as_float(acc[i + h]);
+                    const float s = sigmoid_fast(g);
+                    const float sg = g * s;                     // silu(G)
+                    dwp = fmaf(round_bf16(sg * u), da1, dwp);
+                    const float da = w * da1;
+                    dgv[h] = da * u * s * fmaf(g, 1.0f - s, 1.0f);
+                    duv[h] = da * sg;
+                }
+                pg[half * 16 + i / 2] = pack_bf16x2(dgv[0], dgv[1]);
+                pu[half * 16 + i / 2] = pack_bf16x2(duv[0], duv[1]);
+            }
         }
-        store_row64(dgu_row + (size_t)col * 2, dg4, valid);
-        store_row64(dgu_row + (I + col) * 2, du4, valid);
+        const int col = ti.nt * 256 + c;
+        store_piece<GemmCfg<GK_DGRAD_DOWN>::NBUF>(p, stage2, buf, dg4, lane, valid_rows,
+                                                  dgu_base + (size_t)col * 2, ld, col, row0);
+        store_piece<GemmCfg<GK_DGRAD_DOWN>::NBUF>(p, stage2, buf, du4, lane, valid_rows,
+                                                  dgu_base + (size_t)(I + col) * 2, ld, I + col, row0);
     }
     if (valid && !ti.shared)
         p.dw_part[(size_t)row * p.n_tiles + ti.nt] = dwp;
@@ -770,9 +794,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
                 tc_fence_after();
                 const uint32_t tacc = tmem + ((uint32_t)(quad * 32) << 16) + slot * C::BN;
                 if constexpr (KIND == GK_GATE_UP_BWD)
-                    epilogue_gu_bwd(p, ti, tacc, quad, lane, stage);
+                    epilogue_gu_bwd(p, ti, tacc, quad, lane, stage, buf);
                 else if constexpr (KIND == GK_DGRAD_DOWN)
-                    epilogue_dgrad(p, ti, tacc, quad, lane);
+                    epilogue_dgrad(p, ti, tacc, quad, lane, stage, buf);
                 else if constexpr (KIND == GK_WGRAD)
                     epilogue_wgrad(p, ti, tacc, quad, lane, stage);
                 else

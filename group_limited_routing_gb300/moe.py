@@ -207,10 +207,11 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
 
 
 def backward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, d_out,
-             *, ws: Optional[Workspace] = None):
+             *, ws: Optional[Workspace] = None, out: Optional[dict] = None):
     """moe_backward (routing fixed): dict(d_hidden [T,H] bf16, dW_gate_up
     [E,2I,H] fp32, dW_down [E,I,H] fp32, d_shared_gate_up [2Is,H] fp32,
-    d_shared_down [Is,H] fp32, d_topk_w [T,k] fp32)."""
+    d_shared_down [Is,H] fp32, d_topk_w [T,k] fp32); `out` (a dict like the
+    result) is filled instead of allocating."""
     dev = hidden.device
     bf = torch.bfloat16
     ph = _need(hidden, "hidden", bf, (cfg.T, cfg.H), dev)
@@ -222,12 +223,16 @@ def backward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_d
     pw = _need(topk_w, "topk_w", torch.float32, (cfg.T, cfg.k), dev)
     pdo = _need(d_out, "d_out", bf, (cfg.T, cfg.H), dev)
     f32 = torch.float32
-    g = dict(d_hidden=torch.empty(cfg.T, cfg.H, dtype=bf, device=dev),
-             dW_gate_up=torch.empty(cfg.E, 2 * cfg.I, cfg.H, dtype=f32, device=dev),
-             dW_down=torch.empty(cfg.E, cfg.I, cfg.H, dtype=f32, device=dev),
-             d_shared_gate_up=torch.empty(2 * cfg.Is, cfg.H, dtype=f32, device=dev),
-             d_shared_down=torch.empty(cfg.Is, cfg.H, dtype=f32, device=dev),
-             d_topk_w=torch.empty(cfg.T, cfg.k, dtype=f32, device=dev))
+    shapes = dict(d_hidden=((cfg.T, cfg.H), bf), dW_gate_up=((cfg.E, 2 * cfg.I, cfg.H), f32),
+                  dW_down=((cfg.E, cfg.I, cfg.H), f32), d_shared_gate_up=((2 * cfg.Is, cfg.H), f32),
+                  d_shared_down=((cfg.Is, cfg.H), f32), d_topk_w=((cfg.T, cfg.k), f32))
+    g = {}
+    for name, (shape, dt) in shapes.items():
+        t = out.get(name) if out else None
+        if t is None:
+            t = torch.empty(*shape, dtype=dt, device=dev)
+        _need(t, name, dt, shape, dev)
+        g[name] = t
     ws = _ws(ws, cfg, _lib.MOE_WS_BACKWARD, dev)
     rc = _lib.load().moe_backward(ctypes.byref(cfg.c()), ph, pgu, pd, psgu, psd, pi, pw, pdo,
                                   g["d_hidden"].data_ptr(), g["dW_gate_up"].data_ptr(), g["dW_down"].data_ptr(),
@@ -354,6 +359,7 @@ class MoELayer:
         self.W_split = prepare_router(self.cfg, self.W_router, out=self.W_split)
 
     def __call__(self, hidden, residual=None, out=None):
+        self._hidden = hidden
         self.routing = route(self.cfg, hidden, self.W_router, self.expert_bias, aux=self.aux, ws=self.ws_route,
                              out=self.routing, W_split=self.W_split)
         n = last_launch_count()
@@ -364,7 +370,23 @@ class MoELayer:
         return y
 
     def status(self) -> int:
-        return self.ws_route.status() | self.ws_fwd.status()
+        st = self.ws_route.status() | self.ws_fwd.status()
+        if getattr(self, "ws_bwd", None) is not None:
+            st |= self.ws_bwd.status()
+        return st
+
+    def backward(self, d_out, out: Optional[dict] = None) -> dict:
+        """Gradients of the last call's output w.r.t. its input, the expert
+        weights and the routing weights, for that call's routing (moe_backward;
+        the router's own gradient and the residual path are not included)."""
+        if self.routing is None:
+            raise RuntimeError("backward() needs a forward call first")
+        if getattr(self, "ws_bwd", None) is None:
+            self.ws_bwd = Workspace(self.cfg, _lib.MOE_WS_BACKWARD, self.device)
+        g = backward(self.cfg, self._hidden, self.W_gate_up, self.W_down, self.shared_gate_up, self.shared_down,
+                     self.routing[0], self.routing[1], d_out, ws=self.ws_bwd, out=out)
+        self.last_launches = last_launch_count()
+        return g
 
     def feedback(self, gamma: float, totals=None) -> None:
         """After a call: nudge expert_bias toward balanced load from this

@@ -110,3 +110,32 @@ def test_backward_launch_count():
                  torch.zeros(T, H, device=DEV, dtype=torch.bfloat16))
     # hist, scan, scatter, pad zeroing, recompute, dgrad, dX, combine, dw, 2 weight-gradient GEMMs
     assert moe.last_launch_count() == 11
+
+
+def test_layer_backward_matches_function_and_reuses_outputs():
+    T, H, I = 333, 512, 256
+    w0 = wl.Workload(88, "bwd", T=T, H=H, I=I, Is=I)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T, H=H, I=I, Is=I)
+    layer = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"], d["shared_gate_up"],
+                         d["shared_down"])
+    with pytest.raises(RuntimeError):
+        layer.backward(torch.zeros(T, H, device=DEV, dtype=torch.bfloat16))
+    layer(d["hidden"])
+    dout = torch.randn(T, H, device=DEV).to(torch.bfloat16)
+    g = layer.backward(dout)
+    ref = moe.backward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"],
+                       layer.routing[0], layer.routing[1], dout)
+    for k in ref:
+        assert torch.equal(g[k], ref[k]), k
+    ptrs = {k: v.data_ptr() for k, v in g.items()}
+    for v in g.values():
+        v.fill_(7)
+    g2 = layer.backward(dout, out=g)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    for k in ref:
+        assert g2[k].data_ptr() == ptrs[k], k              # filled in place
+        assert torch.equal(g2[k], ref[k]), k
+    with pytest.raises(ValueError):
+        layer.backward(dout, out={"d_hidden": torch.empty(T, H + 8, device=DEV, dtype=torch.bfloat16)})
