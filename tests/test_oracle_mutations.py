@@ -27,7 +27,8 @@ MUTATIONS = {
     "selection_without_bias": ("b[e] = s[e] + (bias ? bias[e] : 0.0f);", "b[e] = s[e];"),
     "strided_groups": ("float v = b[j * GS + q];", "float v = b[q * G + j];"),
     "gate_up_swapped": ("double act = G / (1.0 + exp(-G)) * U;", "double act = U / (1.0 + exp(-U)) * G;"),
-    "no_bf16_intermediate": ("a[i] = orc_bf16_value(orc_bf16_round((float)act));", "a[i] = act;"),
+    "no_bf16_intermediate": ("a[i] = round_act ? orc_bf16_value(orc_bf16_round((float)act)) : act;",
+                             "a[i] = act;"),
     "no_shared_expert": ("if (sgu && sd)\n", "if (0)\n"),
     "down_transposed": ("acc[h] += ai * orc_bf16_value(wd[h]);",
                         "acc[h] += ai * orc_bf16_value(Wd[(size_t)h * I + i]);"),
