@@ -304,17 +304,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
-__device__ __forceinline__ float silu_times(float g, float u)
-{
-    return g / (1.0f + __expf(-g)) * u;
-}
-
-// sigmoid(g) for the backward epilogues: one exponential and an approximate
-// (branch-free) reciprocal, so that a lane's 32 columns run side by side.
-// g -> -inf gives 1 / inf = 0, g -> +inf gives 1.
+// sigmoid(g) for the epilogues: one exponential and an approximate
+// (branch-free) reciprocal, so that a lane's columns run side by side instead
+// of each waiting on a division's special-case branch.  g -> -inf gives
+// 1 / inf = 0, g -> +inf gives 1.
 __device__ __forceinline__ float sigmoid_fast(float g)
 {
     return __fdividef(1.0f, 1.0f + __expf(-g));
+}
+
+__device__ __forceinline__ float silu_times(float g, float u)
+{
+    return g * sigmoid_fast(g) * u;
 }
 
 __device__ __forceinline__ float round_bf16(float x)
@@ -471,9 +472,9 @@ __device__ __forceinline__ void epilogue_gu_bwd(const GemmParams &p, const TileI
         uint32_t *pk = reinterpret_cast<uint32_t *>(v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-            const float a0 = round_bf16(g0 * sigmoid_fast(g0) * __uint_as_float(u[2 * i]));
-            const float a1 = round_bf16(g1 * sigmoid_fast(g1) * __uint_as_float(u[2 * i + 1]));
+            // the forward's intermediate, bit for bit (same silu_times)
+            const float a0 = round_bf16(silu_times(__uint_as_float(g[2 * i]), __uint_as_float(u[2 * i])));
+            const float a1 = round_bf16(silu_times(__uint_as_float(g[2 * i + 1]), __uint_as_float(u[2 * i + 1])));
             pk[i] = pack_bf16x2(w * a0, w * a1);
         }
         store_piece<GemmCfg<GK_GATE_UP_BWD>::NBUF>(p, stage2, buf, v, lane, valid_rows, aw_base + (size_t)col * 2,
@@ -532,7 +533,7 @@ __device__ __forceinline__ void epilogue_dgrad(const GemmParams &p, const TileIn
                 for (int h = 0; h < 2; ++h) {
                     const float g = G[i + h], u = U[i + h], da1 = __uint_as_float(acc[i + h]);
                     const float s = sigmoid_fast(g);
-                    const float sg = g * s;                     // silu(G)
+                    const float sg = g * s;                     // silu(G); sg * u == silu_times(g, u)
                     dwp = fmaf(round_bf16(sg * u), da1, dwp);
                     const float da = w * da1;
                     dgv[h] = da * u * s * fmaf(g, 1.0f - s, 1.0f);
