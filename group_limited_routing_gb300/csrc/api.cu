@@ -687,7 +687,7 @@ int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_g
     GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter_bwd(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
                                                       xperm, mtiles, hdr, d_out, topk_w, dop, wperm, eoff, L.kTp,
                                                       s));
-    GLR_LAUNCH(KID_BWD_MISC, launch_zero_pad(eoff, sizes, c.T, c.E, c.H, c.I, xperm, dop, aw, dgu, s));
+    GLR_LAUNCH(KID_BWD_MISC, launch_zero_pad(eoff, sizes, c.T, c.E, c.H, c.I, xperm, dop, aw, dgu, hdr->tile_ctr, s));
 
     // 2. the gate/up products again: G, U (fp32) and w * a (bf16)
     GemmParams p1;
@@ -794,6 +794,7 @@ int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_g
         p4.I = c.I;
         p4.H = c.H;
         p4.status = &hdr->status;
+        p4.tile_ctr = &hdr->tile_ctr[which];
         GLR_LAUNCH(KID_BWD_WGRAD, launch_gemm(GK_WGRAD, p4, std::min(sms, p4.num_tiles_static), s));
     }
     g_last_launches = launches;

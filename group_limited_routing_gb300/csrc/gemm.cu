@@ -153,6 +153,13 @@ struct GemmCfg<GK_WGRAD> {
 template <>
 struct GemmCfg<GK_DOWN_SMALL> : GemmCfgSmall<GK_DOWN> {};
 
+// Run-time tile order: the producer lane claims tiles from a global counter
+// and passes each index through a ring of TQ_RING shared-memory entries to the
+// MMA lane and the four epilogue warps (TQ_TAKERS arrivals free an entry);
+// -1 ends every role's loop.
+constexpr int TQ_RING = 8;
+constexpr int TQ_TAKERS = 5;
+
 template <int KIND>
 struct GemmLayout {
     using C = GemmCfg<KIND>;
@@ -160,9 +167,14 @@ struct GemmLayout {
     // per epilogue warp, 32 rows x 128 B: one buffer for the router, two for
     // the grouped GEMMs (a TMA store can drain one while the other is filled)
     static constexpr int STAGING = C::NBUF * 4 * 4096;
-    // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin
-    static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1;
-    static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16;
+    // tiles claimed at run time (weight gradients: a tile's K is its expert's
+    // bucket, from a few rows to the shared expert's T, so a fixed
+    // round-robin leaves some SMs with far more work than others)
+    static constexpr bool DYN = (KIND == GK_WGRAD);
+    static constexpr int TQ = DYN ? TQ_RING : 0;
+    // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin, tq_full[TQ], tq_empty[TQ]
+    static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1 + 2 * TQ;
+    static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16 + TQ * 4;
     static_assert(SMEM <= 232448, "more than 227 KB of shared memory");
     static_assert(C::A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms need 1024-B alignment");
 };
@@ -189,7 +201,8 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
     if constexpr (KIND == GK_WGRAD) {
         // tile = (expert, feature block, hidden block); K over the expert's rows
         const int per_e = p.wg_fm * p.wg_fn;
-        const int e = tile / per_e;
+        const int eidx = tile / per_e;
+        const int e = (eidx == 0) ? p.E : eidx - 1;      // the shared expert's long tiles first
         const int r = tile % per_e;
         const int2 eo = p.eoff[e];
         ti.group = e;
@@ -649,6 +662,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     uint64_t *bars = reinterpret_cast<uint64_t *>(staging + L::STAGING);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + L::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *tq = reinterpret_cast<volatile int *>(tmem_holder + 4);   // L::TQ entries
 
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -656,6 +670,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     const uint32_t tfull0 = bar0 + 8u * (2 * C::STAGES);
     const uint32_t tempty0 = tfull0 + 8u * C::SLOTS;
     const uint32_t fin_bar = tempty0 + 8u * C::SLOTS;
+    const uint32_t tqfull0 = fin_bar + 8u;
+    const uint32_t tqempty0 = tqfull0 + 8u * L::TQ;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -670,6 +686,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             mbar_init(tempty0 + 8u * a, 4);
         }
         mbar_init(fin_bar, 1);
+        for (int i = 0; i < L::TQ; ++i) {
+            mbar_init(tqfull0 + 8u * i, 1);
+            mbar_init(tqempty0 + 8u * i, TQ_TAKERS);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&p.tmA0);
@@ -690,13 +710,49 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
     const int num_tiles = (ROUTER || KIND == GK_WGRAD) ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
     const unsigned long long limit = p.wait_limit_ns ? p.wait_limit_ns : WAIT_LIMIT_NS;
 
+    // The CTA's n-th tile for the MMA lane and the epilogue warps' lane 0:
+    // blockIdx.x + n gridDim.x, or the producer's n-th claim.  -1: no more
+    // tiles; -2: the wait for the claim ran out.
+    auto take_tile = [&](int n) -> int {
+        if constexpr (!L::DYN) {
+            const int t = blockIdx.x + n * gridDim.x;
+            return t < num_tiles ? t : -1;
+        } else {
+            const uint32_t slot = n % TQ_RING, par = (n / TQ_RING) & 1u;
+            if (!mbar_wait(tqfull0 + 8u * slot, par, abort_flag, limit))
+                return -2;
+            const int t = tq[slot];
+            mbar_arrive(tqempty0 + 8u * slot);
+            return t;
+        }
+    };
+
     if (warp == 0) {
         if (lane == 0) {
             // ---------------------------------------------------- TMA producer
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && !p.inject_withhold && tile < num_tiles; tile += gridDim.x) {
+            for (int n = 0; ok && !p.inject_withhold; ++n) {
+                int tile;
+                if constexpr (L::DYN) {
+                    const uint32_t slot = n % TQ_RING, par = (n / TQ_RING) & 1u;
+                    if (!mbar_wait(tqempty0 + 8u * slot, par ^ 1u, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tile = atomicAdd(p.tile_ctr, 1);
+                    if (tile >= num_tiles)
+                        tile = -1;
+                    tq[slot] = tile;
+                    mbar_arrive(tqfull0 + 8u * slot);            // releases the index to the takers
+                } else {
+                    tile = blockIdx.x + n * gridDim.x;
+                    if (tile >= num_tiles)
+                        tile = -1;
+                }
+                if (tile < 0)
+                    break;
                 const TileInfo ti = tile_info<KIND>(p, tile);
                 for (int kb = 0; kb < ti.kblocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, limit)) {
@@ -728,7 +784,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
             uint32_t phase = 0;
             bool ok = true;
             uint32_t ctr = 0;   // accumulators used so far (tiles, or K blocks for the router)
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int n = 0; ok; ++n) {
+                const int tile = take_tile(n);
+                if (tile < 0)
+                    break;
                 const int kblocks = (KIND == GK_WGRAD) ? tile_info<KIND>(p, tile).kblocks : p.kblocks;
                 if (!ROUTER) {
                     const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
@@ -778,7 +837,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
         uint8_t *stage = staging + (warp - 2) * (C::NBUF * 4096);
         int buf = 0;
         uint32_t ctr = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int n = 0;; ++n) {
+            int tile = 0;
+            if (lane == 0)
+                tile = take_tile(n);
+            tile = __shfl_sync(0xffffffffu, tile, 0);
+            if (tile < 0)
+                break;
             const TileInfo ti = tile_info<KIND>(p, tile);
             if constexpr (ROUTER) {
                 if (!router_epilogue_tile(p, ti, tmem, quad, lane, tfull0, tempty0, ctr, abort_flag, stage, limit))

@@ -63,7 +63,8 @@ constexpr int ST_COUNT_MISMATCH = 8;
 struct WsHeader {
     int status;      // OR of ST_* bits
     int num_mtiles;  // m-tiles of the grouped GEMMs (written on the device)
-    int pad[62];
+    int tile_ctr[2]; // claim counters of the two weight-gradient launches (zeroed on the device)
+    int pad[60];
 };
 
 // The _SMALL kinds are the grouped GEMMs for T <= GEMM_SMALL_T (decode): every
@@ -112,6 +113,7 @@ struct GemmParams {
     // fault injection for tests: when set, the producer issues no loads, so
     // the first wait of the MMA lane runs out after wait_limit_ns
     int inject_withhold;
+    int *tile_ctr;        // GK_WGRAD: tiles claimed so far (zero at launch)
     unsigned long long wait_limit_ns;
 };
 
@@ -170,7 +172,7 @@ cudaError_t launch_bucket_scatter_bwd(const int32_t *idx, const uint16_t *x, con
                                       const float *w, uint16_t *do_perm, float *w_perm, int2 *eoff, int shared_base,
                                       cudaStream_t s);
 cudaError_t launch_zero_pad(const int2 *eoff, const int32_t *sizes, int T, int E, int H, int I, uint16_t *x_perm,
-                            uint16_t *do_perm, uint16_t *aw, uint16_t *dgu, cudaStream_t s);
+                            uint16_t *do_perm, uint16_t *aw, uint16_t *dgu, int *tile_ctr, cudaStream_t s);
 cudaError_t launch_dw_reduce(const int32_t *slot_of, const float *dw_part, int n, int ntiles, float *dw,
                              cudaStream_t s);
 

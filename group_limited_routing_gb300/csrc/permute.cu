@@ -326,10 +326,12 @@ cudaError_t launch_bucket_scatter_bwd(const int32_t *idx, const uint16_t *x, con
 // shared rows in do_perm, aw, dgu.  Block b takes bucket b (b == E: shared).
 __global__ void zero_pad_kernel(const int2 *__restrict__ eoff, const int32_t *__restrict__ sizes, int T, int E,
                                 int H, int I, uint16_t *__restrict__ x_perm, uint16_t *__restrict__ do_perm,
-                                uint16_t *__restrict__ aw, uint16_t *__restrict__ dgu)
+                                uint16_t *__restrict__ aw, uint16_t *__restrict__ dgu, int *__restrict__ tile_ctr)
 {
     pdl_wait();
     const int e = blockIdx.x;
+    if (e == 0 && threadIdx.x < 2)
+        tile_ctr[threadIdx.x] = 0;
     const int2 eo = eoff[e];
     const int n = (e < E) ? sizes[e] : T;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -347,10 +349,10 @@ __global__ void zero_pad_kernel(const int2 *__restrict__ eoff, const int32_t *__
 }
 
 cudaError_t launch_zero_pad(const int2 *eoff, const int32_t *sizes, int T, int E, int H, int I, uint16_t *x_perm,
-                            uint16_t *do_perm, uint16_t *aw, uint16_t *dgu, cudaStream_t s)
+                            uint16_t *do_perm, uint16_t *aw, uint16_t *dgu, int *tile_ctr, cudaStream_t s)
 {
     const cudaError_t le = launch_pdl(zero_pad_kernel, dim3(E + 1), dim3(256), 0, s, eoff, sizes, T, E, H, I, x_perm,
-                                      do_perm, aw, dgu);
+                                      do_perm, aw, dgu, tile_ctr);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
