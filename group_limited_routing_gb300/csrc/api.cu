@@ -211,7 +211,7 @@ BwdLayout bwd_layout(const moe_cfg &c)
     L.wperm = off;
     off = align_up(off + R * 4, 256);
     L.gu = off;
-    off = align_up(off + R * 2 * I * 4, 256);
+    off = align_up(off + R * 2 * I * 2, 256);
     L.aw = off;
     off = align_up(off + R * I * 2, 256);
     L.dgu = off;
@@ -674,7 +674,7 @@ int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_g
     uint16_t *xperm = at<uint16_t>(ws, L.xperm);
     uint16_t *dop = at<uint16_t>(ws, L.dop);
     float *wperm = at<float>(ws, L.wperm);
-    float *gu = at<float>(ws, L.gu);
+    uint16_t *gu = at<uint16_t>(ws, L.gu);
     uint16_t *aw = at<uint16_t>(ws, L.aw);
     uint16_t *dgu = at<uint16_t>(ws, L.dgu);
     uint16_t *dx = at<uint16_t>(ws, L.dx);
@@ -689,7 +689,7 @@ int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_g
                                                       s));
     GLR_LAUNCH(KID_BWD_MISC, launch_zero_pad(eoff, sizes, c.T, c.E, c.H, c.I, xperm, dop, aw, dgu, hdr->tile_ctr, s));
 
-    // 2. the gate/up products again: G, U (fp32) and w * a (bf16)
+    // 2. the gate/up products again: G, U (bf16) and w * a (bf16)
     GemmParams p1;
     memset(&p1, 0, sizeof(p1));
     if (!make_map_bf16(&p1.tmA0, xperm, (uint64_t)L.kTp, c.H, GEMM_BK, GEMM_BM) ||

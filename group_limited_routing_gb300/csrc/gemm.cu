@@ -438,20 +438,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
 }
 
 // ---------------------------------------------------------------- backward
-// G and U of the backward live in a warp-interleaved layout: for each block of
-// 32 rows b and each group j of 4 columns of [G | U] (2I fp32 per row), the
-// 16-byte pieces of the block's 32 rows lie side by side, at byte
-// ((b * 2I / 4 + j) * 32 + row % 32) * 16.  An epilogue warp holds one row
+// G and U of the backward are kept in bf16 (the activations a bf16 training
+// step saves for the SwiGLU backward) in a warp-interleaved layout: for each
+// block of 32 rows b and each group j of 8 columns of [G | U] (2I per row),
+// the 16-byte pieces of the block's 32 rows lie side by side, at byte
+// ((b * 2I / 8 + j) * 32 + row % 32) * 16.  An epilogue warp holds one row
 // per lane, so each of its loads and stores moves 512 contiguous bytes.
 // Blocks never straddle two buckets: buckets start on 64-row boundaries.
-__device__ __forceinline__ float4 *gu_piece(float *gu, int I, int row, int col)
+__device__ __forceinline__ uint4 *gu_piece(uint16_t *gu, int I, int row, int col)
 {
-    const size_t b = (size_t)(row >> 5), j = (size_t)(col >> 2);
-    return reinterpret_cast<float4 *>(gu) + ((b * (size_t)(I >> 1) + j) << 5) + (row & 31);
+    const size_t b = (size_t)(row >> 5), j = (size_t)(col >> 3);
+    return reinterpret_cast<uint4 *>(gu) + ((b * (size_t)(I >> 2) + j) << 5) + (row & 31);
 }
 
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
 // GK_GATE_UP_BWD epilogue (one warp, 32 rows): for its 128 gate + 128 up
-// columns, G and U (fp32, interleaved as above) into gu_out and
+// columns, G and U (bf16, interleaved as above) into gu_out and
 // aw = bf16(w_row * bf16(silu(G) * U)) into aw_out [rows, I] (TMA stores).
 __device__ __forceinline__ void epilogue_gu_bwd(const GemmParams &p, const TileInfo &ti, uint32_t tacc, int quad,
                                                 int lane, uint8_t *stage2, int &buf)
@@ -471,14 +475,19 @@ __device__ __forceinline__ void epilogue_gu_bwd(const GemmParams &p, const TileI
         tmem_load64(tacc + 128 + c, u);
         const int col = ti.nt * 128 + c;                 // intermediate column
         if (valid) {
-            float4 *pg = gu_piece(p.gu_out, p.I, row, col);
-            float4 *pu = gu_piece(p.gu_out, p.I, row, p.I + col);
+            uint4 *pg = gu_piece(p.gu_out, p.I, row, col);
+            uint4 *pu = gu_piece(p.gu_out, p.I, row, p.I + col);
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                pg[32 * q] = make_float4(__uint_as_float(g[4 * q]), __uint_as_float(g[4 * q + 1]),
-                                         __uint_as_float(g[4 * q + 2]), __uint_as_float(g[4 * q + 3]));
-                pu[32 * q] = make_float4(__uint_as_float(u[4 * q]), __uint_as_float(u[4 * q + 1]),
-                                         __uint_as_float(u[4 * q + 2]), __uint_as_float(u[4 * q + 3]));
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t *gq = g + 8 * q, *uq = u + 8 * q;
+                pg[32 * q] = make_uint4(pack_bf16x2(__uint_as_float(gq[0]), __uint_as_float(gq[1])),
+                                        pack_bf16x2(__uint_as_float(gq[2]), __uint_as_float(gq[3])),
+                                        pack_bf16x2(__uint_as_float(gq[4]), __uint_as_float(gq[5])),
+                                        pack_bf16x2(__uint_as_float(gq[6]), __uint_as_float(gq[7])));
+                pu[32 * q] = make_uint4(pack_bf16x2(__uint_as_float(uq[0]), __uint_as_float(uq[1])),
+                                        pack_bf16x2(__uint_as_float(uq[2]), __uint_as_float(uq[3])),
+                                        pack_bf16x2(__uint_as_float(uq[4]), __uint_as_float(uq[5])),
+                                        pack_bf16x2(__uint_as_float(uq[6]), __uint_as_float(uq[7])));
             }
         }
         uint4 v[8];
@@ -526,13 +535,19 @@ __device__ __forceinline__ void epilogue_dgrad(const GemmParams &p, const TileIn
             const int col = ti.nt * 256 + c + half * 32;
             float G[32], U[32];
             if (valid) {
-                const float4 *sg = gu_piece(const_cast<float *>(p.gu_in), I, row, col);
-                const float4 *su = gu_piece(const_cast<float *>(p.gu_in), I, row, I + col);
+                const uint4 *sg = gu_piece(const_cast<uint16_t *>(p.gu_in), I, row, col);
+                const uint4 *su = gu_piece(const_cast<uint16_t *>(p.gu_in), I, row, I + col);
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float4 g4 = sg[32 * q], u4 = su[32 * q];
-                    G[4 * q] = g4.x; G[4 * q + 1] = g4.y; G[4 * q + 2] = g4.z; G[4 * q + 3] = g4.w;
-                    U[4 * q] = u4.x; U[4 * q + 1] = u4.y; U[4 * q + 2] = u4.z; U[4 * q + 3] = u4.w;
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 g8 = sg[32 * q], u8 = su[32 * q];
+                    const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w}, uw[4] = {u8.x, u8.y, u8.z, u8.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        G[8 * q + 2 * k] = bf16_lo(gw[k]);
+                        G[8 * q + 2 * k + 1] = bf16_hi(gw[k]);
+                        U[8 * q + 2 * k] = bf16_lo(uw[k]);
+                        U[8 * q + 2 * k + 1] = bf16_hi(uw[k]);
+                    }
                 }
             } else {
 #pragma unroll

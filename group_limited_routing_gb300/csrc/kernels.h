@@ -101,9 +101,9 @@ struct GemmParams {
     int *status;
     // backward kinds
     const float *w_perm;  // routing weight of every bucket row (1 for shared rows)
-    float *gu_out;        // GK_GATE_UP_BWD: G and U, fp32 [rows, 2I]
+    uint16_t *gu_out;     // GK_GATE_UP_BWD: G and U, bf16 [rows, 2I] (32-row interleaved)
     uint16_t *aw_out;     // GK_GATE_UP_BWD: bf16(w * bf16(silu(G) * U)) [rows, I]
-    const float *gu_in;   // GK_DGRAD_DOWN: G and U
+    const uint16_t *gu_in; // GK_DGRAD_DOWN: G and U
     uint16_t *dgu_out;    // GK_DGRAD_DOWN: dG and dU, bf16 [rows, 2I]
     float *dw_part;       // GK_DGRAD_DOWN: per (row, n-tile) partial dot products [kT_padded, n_tiles]
     const int2 *eoff;     // GK_WGRAD: per expert (first bucket row, padded rows); entry E = shared

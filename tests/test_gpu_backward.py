@@ -14,10 +14,12 @@ from parity import bf16_to_f64, output_errors
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-# gradients pass through two more bf16 roundings than the forward (the
-# weighted intermediate and dG/dU are GEMM operands): looser than the forward
-GRAD_MAX_REL = 4e-2
-GRAD_MEAN_REL = 1.5e-2
+# gradients pass through more bf16 roundings than the forward: the saved G
+# and U, the weighted intermediate and dG/dU (GEMM operands), each a relative
+# 2^-9 at most; measured errors stay under 0.5% of the largest value and 0.4%
+# on average, so these bounds keep a margin of about three
+GRAD_MAX_REL = 1.5e-2
+GRAD_MEAN_REL = 1e-2
 
 
 def u16(t):
