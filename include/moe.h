@@ -223,11 +223,13 @@ int moe_dense_ffn(int32_t T, int32_t H, int32_t I, const moe_bf16 *hidden, const
  * outputs and determinism as moe_route, but the scratch that moe_route keeps
  * in its workspace (the split router weight, the logits, the balance-loss
  * partials) lives in one array inside this library, so the caller supplies
- * only inputs and outputs.  It is meant for callers that must not allocate
- * device memory on the call path: code that runs while a CUDA graph is being
- * captured, plug-in hosts whose operator interface hands over tensors but no
- * allocator, and latency-sensitive loops where a cudaMalloc would synchronise
- * the device.  This entry point itself never calls cudaMalloc or cudaFree.
+ * only inputs and outputs.  It is meant for callers that cannot allocate
+ * device memory on the call path: plug-in hosts whose operator interface
+ * hands over input and output tensors but no allocator, runtimes that own
+ * every byte of device memory and give none to their plug-ins, and
+ * latency-sensitive loops where a cudaMalloc would synchronise the device.
+ * This entry point itself never calls cudaMalloc, cudaFree or any allocating
+ * library routine.
  *
  * The array is a static __device__ buffer of MOE_ROUTE_STATIC_SCRATCH_BYTES
  * (40 MiB), held on every GPU that loads the library until the process exits.

@@ -1,9 +1,9 @@
 """moe_route_static: the router entry point that takes no workspace.
 
-Some callers cannot allocate device memory where they call the router: code
-running inside a CUDA graph capture, plug-in hosts that hand an operator its
-tensors but no allocator, or tight loops where a cudaMalloc would stall the
-device.  moe_route_static keeps the router's scratch in an array inside the
+Some callers cannot allocate device memory where they call the router:
+plug-in hosts that hand an operator its tensors but no allocator, runtimes
+that keep all device memory to themselves, or tight loops where a cudaMalloc
+would stall the device.  moe_route_static keeps the router's scratch in an array inside the
 library instead.  These checks call it through the C ABI and compare it with
 moe_route (which uses a caller workspace) on two calls in a row: the same
 kernels run on the same inputs, so indices, counts, weights and the balance
