@@ -345,7 +345,7 @@ def run_ours(args, world, rank, local):
     layer(x, out=out)
     e1.record(stream)
     torch.cuda.synchronize(dev)
-    lead = max(1, min(2000, int(500.0 / max(e0.elapsed_time(e1), 1e-3))))
+    lead = max(1, min(2000, int(args.lead_in_ms / max(e0.elapsed_time(e1), 1e-3))))
     flush = args.flush_l2 or w0.wid == 1
     scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush else None
     launches = 0
@@ -636,6 +636,8 @@ def main():
                     help="oracle sample for the single-thread CPU figure (0 = skip)")
     ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=(1, 2, 3, 4, 5),
                     help="1 tiny, 2 decode T=16, 3 T=4096, 4 T=32768 skewed (the bench line), 5 19-layer stack")
+    ap.add_argument("--lead-in-ms", type=float, default=500.0,
+                    help="untimed loaded steps before the timed region (0: one step; for profiling captures)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step (default: the workload's 32768); smaller sizes for profiling captures")
     args = ap.parse_args()

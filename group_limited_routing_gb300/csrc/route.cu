@@ -315,6 +315,189 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     }
 }
 
+// The same selection for the page's setting (topk_group of n_group groups
+// kept, instantiated for 4 of 8), with far fewer instructions per token:
+//  * after the group stage every lane has exactly TG candidates (its experts
+//    in the kept groups); it sorts them once by (key desc, group asc), so a
+//    top-k round is two warp reductions plus a shift of the winning lane's
+//    list instead of a scan over all its groups;
+//  * the token's keys and unbiased scores go to a per-warp shared-memory row
+//    (index = expert id), from which the kept groups' keys and each round's
+//    winning score are read by index;
+//  * the next token's logits are loaded before the current one is processed.
+// Results are identical to route_select_kernel's: same score formula, same
+// group scores and ranking, same winner per round (max key, then lowest
+// expert id), the same sequential sum for the normaliser.
+template <int G, int TG>
+__global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
+    const float *__restrict__ logits, const float *__restrict__ bias, int T, int chunk, int K, float rsf, float eps,
+    int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
+    float *__restrict__ ppart, int *__restrict__ status)
+{
+    pdl_wait();
+    constexpr int E = 32 * G;
+    constexpr unsigned FULL = 0xffffffffu;
+    __shared__ int sh_hist[E];
+    __shared__ float sh_p[8][E];
+    __shared__ float sh_s[8][E];       // per warp: the current token's unbiased scores, by expert
+    __shared__ uint32_t sh_k[8][E];    // per warp: its biased-score keys, by expert
+    __shared__ float sh_bias[E];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    bool nonfinite = false;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        sh_hist[e] = 0;
+        const float b = bias ? bias[e] : 0.0f;
+        nonfinite |= !isfinite(b);
+        sh_bias[e] = b;
+    }
+    // per-warp sums of the token-normalised scores (balance loss), by expert
+#pragma unroll
+    for (int j = 0; j < G; ++j)
+        sh_p[warp][32 * j + lane] = 0.0f;
+    __syncthreads();
+
+    const int t0 = blockIdx.x * chunk;
+    const int t1 = min(T, t0 + chunk);
+    float Ln[G];
+    if (t0 + warp < t1) {
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            Ln[j] = __ldg(logits + (size_t)(t0 + warp) * E + 32 * j + lane);
+    }
+    for (int t = t0 + warp; t < t1; t += 8) {
+        float L[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            L[j] = Ln[j];
+        if (t + 8 < t1) {
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                Ln[j] = __ldg(logits + (size_t)(t + 8) * E + 32 * j + lane);
+        }
+        float s[G];
+        uint32_t kk[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            nonfinite |= !(fabsf(L[j]) <= 3.402823466e38f);   // NaN or +-inf
+            s[j] = __frcp_rn(1.0f + expf(-L[j]));              // section 二 step 1
+            kk[j] = fkey(s[j] + sh_bias[32 * j + lane]);       // section 三: choose on s + bias
+            sh_s[warp][32 * j + lane] = s[j];
+            sh_k[warp][32 * j + lane] = kk[j];
+        }
+
+        // group score = top-1 + top-2 of the group's biased scores (a tie for
+        // the top counts twice)
+        float g[G];
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+            const uint32_t m1 = __reduce_max_sync(FULL, kk[j]);
+            const uint32_t m2o = __reduce_max_sync(FULL, kk[j] < m1 ? kk[j] : 0u);
+            const uint32_t m2 = (__popc(__ballot_sync(FULL, kk[j] == m1)) > 1) ? m1 : m2o;
+            g[j] = fkey_value(m1) + fkey_value(m2);
+        }
+
+        // keep the TG best groups (ties to the lower group index)
+        float gl = g[0];
+#pragma unroll
+        for (int j = 1; j < G; ++j)
+            if (lane == j)
+                gl = g[j];
+        int rank = 0;
+#pragma unroll
+        for (int i = 0; i < G; ++i)
+            rank += (g[i] > gl || (g[i] == gl && i < lane)) ? 1 : 0;
+        uint32_t keep = __ballot_sync(FULL, lane < G && rank < TG) & ((1u << G) - 1u);
+        __syncwarp();                                   // the warp's row of keys and scores is written
+
+        // this lane's candidates in ascending group order, then sorted by key
+        // (descending) with adjacent exchanges that swap only on a strictly
+        // larger key, so equal keys keep the lower group first
+        uint32_t ck[TG];
+        int cj[TG];
+#pragma unroll
+        for (int i = 0; i < TG; ++i) {
+            const int j = __ffs(keep) - 1;
+            keep &= keep - 1u;
+            cj[i] = j;
+            ck[i] = sh_k[warp][32 * j + lane];
+        }
+#pragma unroll
+        for (int i = 1; i < TG; ++i) {
+#pragma unroll
+            for (int q = i; q > 0; --q) {
+                if (ck[q] > ck[q - 1]) {
+                    const uint32_t tk = ck[q];
+                    ck[q] = ck[q - 1];
+                    ck[q - 1] = tk;
+                    const int tj = cj[q];
+                    cj[q] = cj[q - 1];
+                    cj[q - 1] = tj;
+                }
+            }
+        }
+
+        // top-K: each round takes the largest head key, ties to the lowest expert id
+        float den = 0.0f;
+        int my_e = -1;
+        float my_s = 0.0f;
+        for (int r = 0; r < K; ++r) {
+            const uint32_t wk = __reduce_max_sync(FULL, ck[0]);
+            const uint32_t cand = (ck[0] == wk) ? (uint32_t)(32 * cj[0] + lane) : 0xffffffffu;
+            const uint32_t we = __reduce_min_sync(FULL, cand);
+            if (cand == we) {                              // the winning lane drops its head
+#pragma unroll
+                for (int i = 0; i + 1 < TG; ++i) {
+                    ck[i] = ck[i + 1];
+                    cj[i] = cj[i + 1];
+                }
+                ck[TG - 1] = 0u;
+            }
+            const float sw = sh_s[warp][we];              // the winner's unbiased score
+            den += sw;                                    // sequential, in output order
+            if (lane == r) {
+                my_e = (int)we;
+                my_s = sw;
+            }
+        }
+        den += eps;
+        if (lane < K) {
+            idx_out[(size_t)t * K + lane] = my_e;
+            w_out[(size_t)t * K + lane] = (my_s / den) * rsf;   // section 二 step 3
+            atomicAdd(&sh_hist[my_e], 1);
+        }
+
+        if (ppart) {
+            float tot = 0.0f;
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                tot += s[j];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                tot += __shfl_xor_sync(FULL, tot, off);
+            const float inv = 1.0f / tot;
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                sh_p[warp][32 * j + lane] += s[j] * inv;
+        }
+        __syncwarp();                                   // row reads done before the next token's writes
+    }
+    if (__any_sync(FULL, nonfinite) && lane == 0)
+        atomicOr(status, ST_NONFINITE);
+
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        if (sh_hist[e])
+            atomicAdd(&counts[e], sh_hist[e]);      // integer sums: the result is order-free
+        if (ppart) {
+            float v = 0.0f;
+            for (int q = 0; q < 8; ++q)
+                v += sh_p[q][e];
+            ppart[(size_t)blockIdx.x * E + e] = v;
+        }
+    }
+}
+
 cudaError_t launch_route_select(const float *logits, const float *bias, int T, int E, int n_group, int topk_group,
                                 int k, float rsf, float eps, int32_t *idx, float *w, int32_t *counts, float *ppart,
                                 int *status, cudaStream_t s)
@@ -328,6 +511,13 @@ cudaError_t launch_route_select(const float *logits, const float *bias, int T, i
         if (le != cudaSuccess)                                                                               \
             return le;                                                                                       \
         break;                                                                                               \
+    }
+    if (n_group == 8 && topk_group == 4) {
+        const cudaError_t le = launch_pdl(route_select_sorted_kernel<8, 4>, dim3(blocks), dim3(256), 0, s, logits,
+                                          bias, T, chunk, k, rsf, eps, idx, w, counts, ppart, status);
+        if (le != cudaSuccess)
+            return le;
+        return cudaPeekAtLastError();
     }
     switch (n_group) {
         GLR_ROUTE_CASE(1)
