@@ -150,21 +150,36 @@ def dense_work(T, H, I):
     }
 
 
-def algorithmic_work(T, H, E, I, k):
+def algorithmic_work(T, H, E, I, k, hit=None, Is=None):
     """Per-launch algorithmic bytes / flops of each kernel (the method's own
-    work: bytes every stage must move at least once, flops of the products)."""
+    work: bytes every stage must move at least once, flops of the products).
+    The grouped GEMMs read the weights of the `hit` experts that received at
+    least one token (all E unless given) plus the shared expert's; each GEMM
+    is reported against the roofline that binds it at this size (HBM when its
+    bytes take longer at the measured copy rate than its flops at the
+    measured sustained tensor rate)."""
     kT = k * T
-    return {
-        "router_gemm": dict(bound="tensor", flops=2.0 * T * E * H,
+    hit = E if hit is None else hit
+    Is = I if Is is None else Is
+    work = {
+        # T <= 32: the CUDA-core router, which streams the fp32 weight once (HBM-bound)
+        "router_gemm": dict(bound="hbm" if T <= 32 else "tensor", flops=2.0 * T * E * H,
                             bytes=T * H * 2 + E * H * 4 + T * E * 4),
         "route_select": dict(bound="hbm", bytes=T * E * 4 + T * k * 8),
         "bucket_scatter": dict(bound="hbm", bytes=T * k * 4 * 2 + T * H * 2 + kT * H * 2),
-        "gemm_gate_up_swiglu": dict(bound="tensor", flops=2.0 * (kT + T) * H * 2 * I,
-                                    bytes=(kT + T) * H * 2 + E * 2 * I * H * 2 + (kT + T) * I * 2),
-        "gemm_down": dict(bound="tensor", flops=2.0 * (kT + T) * I * H,
-                          bytes=(kT + T) * I * 2 + E * I * H * 2 + (kT + T) * H * 2),
+        "gemm_gate_up_swiglu": dict(flops=2.0 * kT * H * 2 * I + 2.0 * T * H * 2 * Is,
+                                    bytes=(kT + T) * H * 2 + (hit * I + Is) * 2 * H * 2 + kT * I * 2 + T * Is * 2),
+        "gemm_down": dict(flops=2.0 * kT * I * H + 2.0 * T * Is * H,
+                          bytes=kT * I * 2 + T * Is * 2 + (hit * I + Is) * H * 2 + (kT + T) * H * 2),
         "combine": dict(bound="hbm", bytes=(kT + T) * H * 2 + T * H * 2 + T * k * 8),
     }
+    pk = peaks()
+    for name in ("gemm_gate_up_swiglu", "gemm_down"):
+        wk = work[name]
+        t_hbm = wk["bytes"] / (pk["hbm"] * 1e9)
+        t_tensor = wk["flops"] / (pk["bf16_sustained"] * 1e12)
+        wk["bound"] = "hbm" if t_hbm > t_tensor else "tensor"
+    return work
 
 
 def workload_name(w0, dense=0, backward=False):
@@ -422,9 +437,13 @@ def run_ours(args, world, rank, local):
     if hot.numel() and getattr(layer, "routing", None) is not None:
         counts = layer.routing[2].double().cpu()
         hot_share = float(counts[hot].sum() / counts.sum())
+    # experts that received tokens (their weights are what the GEMMs stream), mean over layers
+    moe_layers = getattr(layer, "layers", None) or [layer]
+    hits = [int((l.routing[2] > 0).sum().item()) for l in moe_layers if getattr(l, "routing", None) is not None]
+    hit = statistics.mean(hits) if hits else None
     return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk,
                   dict(flush=flush, lead=lead, hot_share=hot_share, graph_ms=graph_ms, dense=args.dense,
-                       backward=args.backward))
+                       backward=args.backward, hit=hit))
 
 
 def time_e2e(args, world, layer, x, out, stream, dev):
@@ -473,7 +492,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
     elif extra["dense"]:
         work = dense_work(T, H, extra["dense"])
     else:
-        work = algorithmic_work(T, H, E, I, k)
+        work = algorithmic_work(T, H, E, I, k, hit=extra.get("hit"), Is=w0.Is)
     stages = {}
     for name, (tot, n) in prof.items():
         if n == 0:
@@ -482,13 +501,13 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         st = {"ms": round(avg, 4), "launches_per_step": round(n / nprof, 2)}
         if name in work:
             wk = work[name]
-            if wk["bound"] == "tensor":
+            st["bound"] = wk["bound"]
+            if "flops" in wk:
                 tf = wk["flops"] / (avg * 1e-3) / 1e12
-                st.update(bound="tensor", tflops=round(tf, 1), frac=round(tf / pk["bf16_sustained"], 4),
-                          gbs=round(wk["bytes"] / (avg * 1e-3) / 1e9, 1))
-            else:
-                gb = wk["bytes"] / (avg * 1e-3) / 1e9
-                st.update(bound="hbm", gbs=round(gb, 1), frac=round(gb / pk["hbm"], 4))
+                st["tflops"] = round(tf, 1)
+            gb = wk["bytes"] / (avg * 1e-3) / 1e9
+            st["gbs"] = round(gb, 1)
+            st["frac"] = round(tf / pk["bf16_sustained"], 4) if wk["bound"] == "tensor" else round(gb / pk["hbm"], 4)
         stages[name] = st
     # router + permute as one HBM stage
     rp_names = ("split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist", "bucket_scan",
@@ -502,17 +521,31 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         stages["router_plus_permute"] = {"ms": round(rp_ms, 4), "bound": "hbm",
                                          "gbs": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
                                          "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / pk["hbm"], 4)}
-    # the roofline kernel: the tensor-core stage with the most time per step
-    tensor_stages = [n for n in work if work[n]["bound"] == "tensor" and prof.get(n, (0, 0))[1] > 0]
+    # the roofline kernel: the tensor-core stage with the most time per step,
+    # against the roofline that binds it at this size
+    tensor_stages = [n for n in work if "flops" in work[n] and prof.get(n, (0, 0))[1] > 0]
     dom = max(tensor_stages, key=lambda n: prof[n][0])
     g1 = work[dom]
     g1_ms = prof[dom][0] / max(1, prof[dom][1])
-    g1_tf = g1["flops"] / (g1_ms * 1e-3) / 1e12
-    gemms_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in tensor_stages)
-    gemm_flops = sum(work[n]["flops"] * stages[n]["launches_per_step"] for n in tensor_stages)
-    stages["expert_gemms"] = {"ms": round(gemms_ms, 4), "bound": "tensor",
-                              "tflops": round(gemm_flops / (gemms_ms * 1e-3) / 1e12, 1),
-                              "frac": round(gemm_flops / (gemms_ms * 1e-3) / 1e12 / pk["bf16_sustained"], 4)}
+    if g1["bound"] == "tensor":
+        g1_ach, g1_peak, g1_unit = g1["flops"] / (g1_ms * 1e-3) / 1e12, pk["bf16_sustained"], "TFLOP/s"
+        g1_kind = "%s bf16 dense, sustained" % pk["source"]
+    else:
+        g1_ach, g1_peak, g1_unit = g1["bytes"] / (g1_ms * 1e-3) / 1e9, pk["hbm"], "GB/s"
+        g1_kind = "%s HBM copy bandwidth" % pk["source"]
+    gemm_names = [n for n in tensor_stages if n != "router_gemm"]
+    if not gemm_names:
+        gemm_names = tensor_stages
+    gemms_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in gemm_names)
+    gemm_flops = sum(work[n]["flops"] * stages[n]["launches_per_step"] for n in gemm_names)
+    gemm_bytes = sum(work[n]["bytes"] * stages[n]["launches_per_step"] for n in gemm_names)
+    g_tf = gemm_flops / (gemms_ms * 1e-3) / 1e12
+    g_gb = gemm_bytes / (gemms_ms * 1e-3) / 1e9
+    g_bound = "hbm" if gemm_bytes / pk["hbm"] / 1e9 > gemm_flops / pk["bf16_sustained"] / 1e12 else "tensor"
+    stages["expert_gemms"] = {"ms": round(gemms_ms, 4), "bound": g_bound, "tflops": round(g_tf, 1),
+                              "gbs": round(g_gb, 1),
+                              "frac": round(g_tf / pk["bf16_sustained"] if g_bound == "tensor" else g_gb / pk["hbm"],
+                                            4)}
 
     value = world * T / (ms_max * 1e-3)
     line = {
@@ -537,14 +570,15 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
                           "expert weights (%.2f GB per layer) larger than L2, no flush" % (3 * E * I * H * 2 / 1e9)),
                    "untimed_lead_in_steps": extra["lead"],
                    "hot_expert_share": None if extra["hot_share"] is None else round(extra["hot_share"], 4)},
-        "roofline": {"kernel": dom, "bound": "tensor", "achieved": round(g1_tf, 1),
-                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": round(g1_tf / pk["bf16_sustained"], 4),
+        "roofline": {"kernel": dom, "bound": g1["bound"], "achieved": round(g1_ach, 1),
+                     "peak": g1_peak, "unit": g1_unit,
+                     "frac": round(g1_ach / g1_peak, 4),
                      "traffic": gemm_traffic(dom) if T == 32768 and not (extra["dense"] or extra["backward"])
                      else None,
                      "traffic_unit": "bytes per launch (ncu dram read + write, profiles/gemm_dram_traffic_T32768.md)",
-                     "peak_kind": "%s bf16 dense, sustained" % pk["source"],
-                     "algorithmic_flops_per_launch": g1["flops"]},
+                     "peak_kind": g1_kind,
+                     "algorithmic_flops_per_launch": g1["flops"],
+                     "algorithmic_bytes_per_launch": g1["bytes"]},
         "stages": stages,
         "e2e": None if e2e_ms is None else
         {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": "tokens/s",

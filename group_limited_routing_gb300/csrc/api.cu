@@ -314,8 +314,9 @@ T *at(void *ws, size_t off)
 int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split, float *logits,
                 int32_t *counts, void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches)
 {
-    if (c.T <= ROUTER_SIMT_MAX_T && c.H % 4 == 0) {
+    if (c.T <= ROUTER_SIMT_MAX_T && c.H % 8 == 0 && aligned(W, 16)) {
         // a few token tiles cannot fill the tensor-core kernel: CUDA cores, fp32 W as is
+        // (16-byte loads of W; a W that is only 4-byte aligned takes the tensor-core path)
         GLR_LAUNCH(KID_ROUTER_GEMM, launch_router_simt(hidden, W, c.T, c.E, c.H, logits, counts, s));
         return MOE_OK;
     }

@@ -60,88 +60,88 @@ cudaError_t launch_split_router(const float *W, uint16_t *W3, int E, int H, int3
 }
 
 // ---------------------------------------------------------------------------
-// Router logits for small T on the CUDA cores.  A block covers 8 experts x
-// SIMT_TOK tokens: the block first stages its tokens' hidden rows in shared
-// memory while warp w loads 2048 columns of expert (8 bx + w)'s fp32 weight
-// row into registers (as it is, no split), so both loads are in flight at
-// once; then each lane sums a strided 1/32 of every token's products with
-// fused multiply-adds, and one butterfly reduction per token finishes the dot
-// product.  Faster than the tensor-core path when a handful of token tiles
-// cannot fill the GPU.  Block (0, 0) also clears `counts` for the routing
-// kernel that follows.
-constexpr int SIMT_TOK = 8;
-constexpr int SIMT_MAX_H = 2048;   // hidden rows staged in shared memory (H <= this; else H-chunks)
+// Router logits for small T (decode) on the CUDA cores, fp32 weight as is.
+// One block per expert: thread i takes 8 consecutive hidden columns
+// (i * 8 + 2048 q), loads that piece of the expert's weight row once and of
+// every token's hidden row, and forms each token's partial dot product with
+// fused multiply-adds in column order; the 256 partials of a token are then
+// added by a butterfly inside each warp and the 8 warp sums in warp order.
+// With a block per expert the weight stream (E H fp32, read once) is spread
+// over the whole GPU.  Block 0 also clears `counts` for the routing kernel
+// that follows.
+constexpr int SIMT_THREADS = 256;
 
-__global__ void __launch_bounds__(256) router_simt_kernel(const uint16_t *__restrict__ x,
-                                                          const float *__restrict__ W, int T, int E, int H,
-                                                          float *__restrict__ logits, int32_t *__restrict__ counts)
+__global__ void __launch_bounds__(SIMT_THREADS) router_simt_kernel(const uint16_t *__restrict__ x,
+                                                                   const float *__restrict__ W, int T, int E, int H,
+                                                                   float *__restrict__ logits,
+                                                                   int32_t *__restrict__ counts)
 {
     pdl_wait();
-    __shared__ __align__(16) uint16_t xs[SIMT_TOK * SIMT_MAX_H];
-    if (blockIdx.x == 0 && blockIdx.y == 0 && counts)
-        for (int e = threadIdx.x; e < E; e += blockDim.x)
-            counts[e] = 0;
-    const int lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int t0 = blockIdx.y * SIMT_TOK;
-    const int nt = min(SIMT_TOK, T - t0);
-    float acc[SIMT_TOK];
+    __shared__ float red[SIMT_THREADS / 32][ROUTER_SIMT_MAX_T];
+    const int e = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (e == 0 && counts)
+        for (int i = threadIdx.x; i < E; i += blockDim.x)
+            counts[i] = 0;
+    float acc[ROUTER_SIMT_MAX_T];
 #pragma unroll
-    for (int tt = 0; tt < SIMT_TOK; ++tt)
-        acc[tt] = 0.0f;
-    const float4 *w4 = reinterpret_cast<const float4 *>(W + (size_t)min(e, E - 1) * H);
-    for (int hc = 0; hc < H; hc += SIMT_MAX_H) {              // H-chunks of at most SIMT_MAX_H columns
-        const int hw = min(SIMT_MAX_H, H - hc);
-        __syncthreads();                                     // the previous chunk's readers are done
-        const int vrow = hw / 8;                             // 16-byte vectors per staged row
-        for (int i = threadIdx.x; i < nt * vrow; i += blockDim.x) {
-            const int tt = i / vrow, v = i % vrow;
-            reinterpret_cast<uint4 *>(xs + tt * SIMT_MAX_H)[v] =
-                __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + tt) * H + hc) + v);
-        }
-        float4 wr[16];                                       // this lane's weights of the chunk
+    for (int t = 0; t < ROUTER_SIMT_MAX_T; ++t)
+        acc[t] = 0.0f;
+    const float *wrow = W + (size_t)e * H;
+    for (int c = threadIdx.x * 8; c < H; c += SIMT_THREADS * 8) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(wrow + c));
+        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(wrow + c + 4));
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int v = lane + 32 * i;
-            wr[i] = (v < hw / 4) ? __ldg(w4 + hc / 4 + v) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        __syncthreads();
+        for (int t0 = 0; t0 < ROUTER_SIMT_MAX_T; t0 += 8) {    // 8 tokens' pieces in flight at a time
+            if (t0 < T) {
+                uint4 xv[8];
 #pragma unroll
-        for (int tt = 0; tt < SIMT_TOK; ++tt) {
-            if (tt < nt) {
-                const uint2 *x4 = reinterpret_cast<const uint2 *>(xs + tt * SIMT_MAX_H);
+                for (int u = 0; u < 8; ++u)
+                    if (t0 + u < T)
+                        xv[u] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + u) * H + c));
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int v = lane + 32 * i;
-                    if (v < hw / 4) {
-                        const uint2 xv = x4[v];
-                        acc[tt] = fmaf(__uint_as_float(xv.x << 16), wr[i].x, acc[tt]);
-                        acc[tt] = fmaf(__uint_as_float(xv.x & 0xffff0000u), wr[i].y, acc[tt]);
-                        acc[tt] = fmaf(__uint_as_float(xv.y << 16), wr[i].z, acc[tt]);
-                        acc[tt] = fmaf(__uint_as_float(xv.y & 0xffff0000u), wr[i].w, acc[tt]);
+                for (int u = 0; u < 8; ++u) {
+                    if (t0 + u < T) {
+                        const uint32_t q[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            acc[t0 + u] = fmaf(__uint_as_float(q[h] << 16), wv[2 * h], acc[t0 + u]);
+                            acc[t0 + u] = fmaf(__uint_as_float(q[h] & 0xffff0000u), wv[2 * h + 1], acc[t0 + u]);
+                        }
                     }
                 }
             }
         }
     }
-    if (e >= E)
-        return;
 #pragma unroll
-    for (int tt = 0; tt < SIMT_TOK; ++tt) {
-        float a = acc[tt];
+    for (int t = 0; t < ROUTER_SIMT_MAX_T; ++t) {
+        if (t < T) {
+            float a = acc[t];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            a += __shfl_xor_sync(0xffffffffu, a, off);
-        if (lane == 0 && tt < nt)
-            logits[(size_t)(t0 + tt) * E + e] = a;
+            for (int off = 16; off > 0; off >>= 1)
+                a += __shfl_xor_sync(0xffffffffu, a, off);
+            if (lane == 0)
+                red[warp][t] = a;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < T) {
+        float a = 0.0f;
+#pragma unroll
+        for (int w = 0; w < SIMT_THREADS / 32; ++w)
+            a += red[w][threadIdx.x];
+        logits[(size_t)threadIdx.x * E + e] = a;
     }
 }
 
 cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, int H, float *logits,
                                int32_t *counts, cudaStream_t s)
 {
-    const dim3 grid((E + 7) / 8, (T + SIMT_TOK - 1) / SIMT_TOK);
-    const cudaError_t le = launch_pdl(router_simt_kernel, dim3(grid), dim3(256), 0, s, x, W, T, E, H, logits, counts);
+    if (T > ROUTER_SIMT_MAX_T || H % 8 != 0)
+        return cudaErrorInvalidValue;
+    const cudaError_t le = launch_pdl(router_simt_kernel, dim3(E), dim3(SIMT_THREADS), 0, s, x, W, T, E, H, logits,
+                                      counts);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
