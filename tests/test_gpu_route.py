@@ -169,3 +169,24 @@ def test_prepared_router_matches_route_bit_for_bit(T):
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_decode_router_with_weight_only_4_byte_aligned():
+    """The CUDA-core router for decode sizes reads W_router in 16-byte pieces;
+    a W_router that is only 4-byte aligned goes to the tensor-core router
+    instead, with the same accuracy against the oracle."""
+    T = 16
+    w0 = wl.WORKLOADS[2].with_T(T)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=T)
+    W = d["W_router"]
+    buf = torch.empty(W.numel() + 1, dtype=torch.float32, device=DEV)
+    Wu = buf[1:].view_as(W)
+    Wu.copy_(W)
+    assert Wu.data_ptr() % 16 == 4
+    L = oracle.router_logits(u16(d["hidden"]), W.cpu().numpy())
+    for Wx, kernels in ((W, 1), (Wu, 2)):          # CUDA-core router / split + tensor-core router
+        g = moe.router_logits(cfg, d["hidden"], Wx).cpu().numpy()
+        assert moe.last_launch_count() == kernels
+        err = np.abs(g.astype(np.float64) - L)
+        assert err.max() <= 2e-6 + 2e-6 * np.abs(L).max(), err.max()
