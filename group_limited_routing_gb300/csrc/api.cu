@@ -328,13 +328,18 @@ int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
     } else if (counts && cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s) != cudaSuccess) {
         return MOE_ERR_CUDA;
     }
+    // all experts of a token tile in one N = 256 MMA when E is a multiple of 256
+    // and there are enough token tiles to give every SM one (below that the
+    // 128-expert tiles spread the work over twice as many SMs)
+    const bool wide = c.E % 256 == 0 && (c.T + GEMM_BM - 1) / GEMM_BM >= sms;
+    const int bn = wide ? 256 : 128;
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
-        !make_map_bf16(&p.tmB0, W3, 3ull * c.E, c.H, GEMM_BK, 128))
+        !make_map_bf16(&p.tmB0, W3, 3ull * c.E, c.H, GEMM_BK, bn))
         return MOE_ERR_CUDA;
     p.out = logits;
-    p.n_tiles = c.E / 128;
+    p.n_tiles = c.E / bn;
     p.num_tiles_static = ((c.T + GEMM_BM - 1) / GEMM_BM) * p.n_tiles;
     p.kblocks = c.H / GEMM_BK;
     p.T = c.T;
@@ -342,7 +347,7 @@ int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
     p.H = c.H;
     p.ld_out = c.E;
     p.status = &header(ws)->status;
-    GLR_LAUNCH(KID_ROUTER_GEMM, launch_gemm(GK_ROUTER, p, std::min(sms, p.num_tiles_static), s));
+    GLR_LAUNCH(KID_ROUTER_GEMM, launch_gemm(wide ? GK_ROUTER_WIDE : GK_ROUTER, p, std::min(sms, p.num_tiles_static), s));
     return MOE_OK;
 }
 

@@ -17,16 +17,20 @@
 //               stacked [E, I, H] as on the page (an MN-major B operand).
 //   GK_*_SMALL  the two grouped products for T <= GEMM_SMALL_T (decode): 16 A
 //               rows per stage and a 6-deep ring of weight tiles.
+//   GK_ROUTER_WIDE  the router with all 256 experts of a token tile in one
+//               N = 256 MMA (half the shared-memory operand traffic per flop
+//               of the 128-expert tiles), two TMEM K-block slots and eight
+//               epilogue warps (two per TMEM lane quadrant, 128 columns each).
 // The grouped kinds also serve the dense first-layer MLP (one weight group).
 //
 // Every kernel starts with griddepcontrol.wait (programmatic dependent
 // launch): its prologue (barriers, TMEM, descriptor prefetch) overlaps the
 // previous kernel's teardown, and nothing global is read before the wait.
 //
-// Roles (192 threads, one CTA per SM):
+// Roles (192 threads, 320 for GK_ROUTER_WIDE; one CTA per SM):
 //   warp 0, one lane : TMA producer, fills a STAGES-deep ring of smem stages
 //   warp 1           : allocates TMEM; one lane issues tcgen05.mma and commits
-//   warps 2..5       : epilogue, TMEM -> registers -> global; warp w reads TMEM
+//   warps 2..5 (..9) : epilogue, TMEM -> registers -> global; warp w reads TMEM
 //                      lanes 32*(w%4) .. +31 (the lane quadrant it may access)
 // TMEM holds SLOTS accumulators: two whole-tile accumulators for the grouped
 // GEMMs (the epilogue of one tile overlaps the MMAs of the next), four K-block
@@ -52,8 +56,16 @@ __host__ __device__ constexpr int base_kind(int kind)
 {
     return (kind == GK_GATE_UP_SMALL || kind == GK_GATE_UP_BWD) ? GK_GATE_UP
            : kind == GK_DOWN_SMALL                              ? GK_DOWN
+           : kind == GK_ROUTER_WIDE                             ? GK_ROUTER
                                                                 : kind;
 }
+
+// K blocks of hidden the wide router prefetches into L2 ahead of its loads
+constexpr int ROUTER_PF = 6;
+
+// epilogue warps of a kind (the block is 64 + 32 x this threads)
+__host__ __device__ constexpr int epi_warps(int kind) { return kind == GK_ROUTER_WIDE ? 8 : 4; }
+__host__ __device__ constexpr int kind_threads(int kind) { return 64 + 32 * epi_warps(kind); }
 
 template <>
 struct GemmCfg<GK_ROUTER> {
@@ -67,6 +79,23 @@ struct GemmCfg<GK_ROUTER> {
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
     static constexpr int A_ROWS = GEMM_BM;
     static constexpr int NBUF = 1;
+};
+
+// 128 tokens x all 256 experts per tile: a stage holds 16 KB of hidden and
+// 3 x 32 KB of W parts, so only two fit; no staging buffers (the epilogue
+// writes each thread's 512 contiguous bytes of logits directly).
+template <>
+struct GemmCfg<GK_ROUTER_WIDE> {
+    static constexpr int BN = 256;
+    static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;
+    static constexpr int B_PART = BN * GEMM_BK * 2;    // 32 KB per W part
+    static constexpr int B_BYTES = 3 * B_PART;
+    static constexpr int STAGES = 2;
+    static constexpr int SLOTS = 2;
+    static constexpr int TMEM_COLS = SLOTS * BN;       // 512
+    static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, false);
+    static constexpr int A_ROWS = GEMM_BM;
+    static constexpr int NBUF = 0;
 };
 
 template <>
@@ -607,16 +636,20 @@ __device__ __forceinline__ void epilogue_wgrad(const GemmParams &p, const TileIn
 }
 
 // Router epilogue warp: adds the K-block partial sums of its 32 rows in fp32
-// (K-block order, round-to-nearest), then writes the 128 logits of each row.
+// (K-block order, round-to-nearest), then writes the 128 logits of each row
+// that it owns (columns half * 128 .. of the tile; half = 0 for the 128-expert
+// tiles, 0 or 1 for the wide kind's two warps per lane quadrant).
+template <int KIND>
 __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem,
-                                                     int quad, int lane, uint32_t tfull0, uint32_t tempty0,
-                                                     uint32_t &kctr, volatile int *abort_flag, uint8_t *stage,
-                                                     unsigned long long limit)
+                                                     int quad, int half, int lane, uint32_t tfull0,
+                                                     uint32_t tempty0, uint32_t &kctr, volatile int *abort_flag,
+                                                     uint8_t *stage, unsigned long long limit)
 {
-    using C = GemmCfg<GK_ROUTER>;
-    float acc[C::BN];
+    using C = GemmCfg<KIND>;
+    constexpr int COLS = 128;
+    float acc[COLS];
 #pragma unroll
-    for (int c = 0; c < C::BN; ++c)
+    for (int c = 0; c < COLS; ++c)
         acc[c] = 0.0f;
     for (int kb = 0; kb < p.kblocks; ++kb, ++kctr) {
         const uint32_t slot = kctr % C::SLOTS;
@@ -629,45 +662,63 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
             return false;
         __syncwarp();
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + slot * C::BN;
+        const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + slot * C::BN + half * COLS;
+        // 64-column loads for the 128-expert tiles; 32-column loads for the
+        // wide kind, whose 320-thread block leaves ~200 registers per thread
+        constexpr int LD = (C::NBUF == 0) ? 32 : 64;
 #pragma unroll
-        for (int c = 0; c < C::BN; c += 64) {
-            uint32_t r[64];
-            tmem_load64(taddr + c, r);
-            if (c + 64 == C::BN) {
+        for (int c = 0; c < COLS; c += LD) {
+            uint32_t r[LD];
+            if constexpr (LD == 64)
+                tmem_load64(taddr + c, r);
+            else
+                tmem_load32(taddr + c, r);
+            if (c + LD == COLS) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(tempty0 + 8u * slot);   // slot free again: the values are in registers
             }
 #pragma unroll
-            for (int i = 0; i < 64; ++i)
+            for (int i = 0; i < LD; ++i)
                 acc[c + i] += __uint_as_float(r[i]);
         }
     }
     const int valid_rows = ti.rows - quad * 32;
     if (valid_rows > 0) {
         const size_t ld_bytes = (size_t)p.ld_out * 4;
-        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes + ti.nt * C::BN * 4;
+        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes +
+                      (size_t)(ti.nt * C::BN + half * COLS) * 4;
+        if constexpr (C::NBUF == 0) {
+            // each thread's 512 contiguous bytes, straight from registers
+            if (lane < valid_rows) {
+                uint4 *dst = reinterpret_cast<uint4 *>(gbase + (size_t)lane * ld_bytes);
 #pragma unroll
-        for (int c = 0; c < C::BN; c += 32) {
-            uint4 v[8];
+                for (int q = 0; q < COLS / 4; ++q)
+                    dst[q] = make_uint4(__float_as_uint(acc[4 * q]), __float_as_uint(acc[4 * q + 1]),
+                                        __float_as_uint(acc[4 * q + 2]), __float_as_uint(acc[4 * q + 3]));
+            }
+        } else {
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-                v[q] = make_uint4(__float_as_uint(acc[c + 4 * q]), __float_as_uint(acc[c + 4 * q + 1]),
-                                  __float_as_uint(acc[c + 4 * q + 2]), __float_as_uint(acc[c + 4 * q + 3]));
-            warp_store_rows128(stage, v, lane, gbase + c * 4, ld_bytes, valid_rows);
+            for (int c = 0; c < COLS; c += 32) {
+                uint4 v[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] = make_uint4(__float_as_uint(acc[c + 4 * q]), __float_as_uint(acc[c + 4 * q + 1]),
+                                      __float_as_uint(acc[c + 4 * q + 2]), __float_as_uint(acc[c + 4 * q + 3]));
+                warp_store_rows128(stage, v, lane, gbase + c * 4, ld_bytes, valid_rows);
+            }
         }
     }
     return true;
 }
 
 template <int KIND>
-__global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid_constant__ GemmParams p)
+__global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const __grid_constant__ GemmParams p)
 {
     using C = GemmCfg<KIND>;
     using L = GemmLayout<KIND>;
-    constexpr bool ROUTER = (KIND == GK_ROUTER);
+    constexpr bool ROUTER = (base_kind(KIND) == GK_ROUTER);
     extern __shared__ uint8_t dsmem[];
 
     const uint32_t raw = smem_u32(dsmem);
@@ -698,7 +749,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
         }
         for (int a = 0; a < C::SLOTS; ++a) {
             mbar_init(tfull0 + 8u * a, 1);
-            mbar_init(tempty0 + 8u * a, 4);
+            mbar_init(tempty0 + 8u * a, epi_warps(KIND));
         }
         mbar_init(fin_bar, 1);
         for (int i = 0; i < L::TQ; ++i) {
@@ -777,6 +828,15 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
                     const uint32_t sA = base + stage * L::STAGE_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), L::STAGE_BYTES);
                     issue_loads<KIND>(p, ti, kb, sA, sA + C::A_BYTES, full_bar(stage));
+                    if constexpr (KIND == GK_ROUTER_WIDE) {
+                        // two stages cannot hide a DRAM read of the hidden rows:
+                        // pull the A box ROUTER_PF K blocks ahead (in this CTA's
+                        // tile order) into L2
+                        const int q = n * p.kblocks + kb + ROUTER_PF;
+                        const int pt = blockIdx.x + (q / p.kblocks) * (int)gridDim.x;
+                        if (pt < num_tiles)
+                            tma_prefetch_l2_2d(&p.tmA0, (q % p.kblocks) * GEMM_BK, (pt / p.n_tiles) * GEMM_BM);
+                    }
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -861,7 +921,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) umma_gemm_kernel(const __grid
                 break;
             const TileInfo ti = tile_info<KIND>(p, tile);
             if constexpr (ROUTER) {
-                if (!router_epilogue_tile(p, ti, tmem, quad, lane, tfull0, tempty0, ctr, abort_flag, stage, limit))
+                if (!router_epilogue_tile<KIND>(p, ti, tmem, quad, (warp - 2) >> 2, lane, tfull0, tempty0, ctr,
+                                                abort_flag, stage, limit))
                     break;
             } else {
                 const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
@@ -908,6 +969,7 @@ int gemm_smem_bytes(int kind)
 {
     switch (kind) {
     case GK_ROUTER: return GemmLayout<GK_ROUTER>::SMEM;
+    case GK_ROUTER_WIDE: return GemmLayout<GK_ROUTER_WIDE>::SMEM;
     case GK_GATE_UP: return GemmLayout<GK_GATE_UP>::SMEM;
     case GK_GATE_UP_SMALL: return GemmLayout<GK_GATE_UP_SMALL>::SMEM;
     case GK_DOWN_SMALL: return GemmLayout<GK_DOWN_SMALL>::SMEM;
@@ -922,6 +984,7 @@ int gemm_tmem_cols(int kind)
 {
     switch (kind) {
     case GK_ROUTER: return GemmCfg<GK_ROUTER>::TMEM_COLS;
+    case GK_ROUTER_WIDE: return GemmCfg<GK_ROUTER_WIDE>::TMEM_COLS;
     case GK_GATE_UP: case GK_GATE_UP_SMALL: return GemmCfg<GK_GATE_UP>::TMEM_COLS;
     default: return GemmCfg<GK_DOWN>::TMEM_COLS;
     }
@@ -940,7 +1003,7 @@ static cudaError_t launch_kind(const GemmParams &p, int grid, cudaStream_t s)
             return e;
         configured_device = dev;
     }
-    const cudaError_t le = launch_pdl(umma_gemm_kernel<KIND>, dim3(grid), dim3(GEMM_THREADS),
+    const cudaError_t le = launch_pdl(umma_gemm_kernel<KIND>, dim3(grid), dim3(kind_threads(KIND)),
                                       (size_t)GemmLayout<KIND>::SMEM, s, p);
     if (le != cudaSuccess)
         return le;
@@ -951,6 +1014,7 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
 {
     switch (kind) {
     case GK_ROUTER: return launch_kind<GK_ROUTER>(p, grid, s);
+    case GK_ROUTER_WIDE: return launch_kind<GK_ROUTER_WIDE>(p, grid, s);
     case GK_GATE_UP: return launch_kind<GK_GATE_UP>(p, grid, s);
     case GK_GATE_UP_SMALL: return launch_kind<GK_GATE_UP_SMALL>(p, grid, s);
     case GK_DOWN_SMALL: return launch_kind<GK_DOWN_SMALL>(p, grid, s);

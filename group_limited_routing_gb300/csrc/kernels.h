@@ -77,7 +77,7 @@ struct WsHeader {
 // bucket rows, both operands MN-major).
 enum GemmKind {
     GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4,
-    GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7
+    GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7, GK_ROUTER_WIDE = 8
 };
 constexpr int GEMM_SMALL_T = 16;
 constexpr int BWD_ROW_ALIGN = 64;   // backward buckets start on 64-row boundaries (K blocks of the weight gradients)

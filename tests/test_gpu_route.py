@@ -49,8 +49,9 @@ def test_route_matches_oracle(wid, T):
     assert n_near <= max(2, T // 100)
 
 
-@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (4, 32), (3, 4096), (4, 2048)])
+@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (4, 32), (3, 4096), (4, 2048), (4, 32768)])
 def test_router_logits_accuracy(wid, T):
+    # T=32768 takes the 256-expert router tiles (enough token tiles for every SM)
     w0 = wl.WORKLOADS[wid].with_T(T)
     d = wl.layer_inputs(w0, DEV, with_experts=False)
     cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
@@ -190,3 +191,32 @@ def test_decode_router_with_weight_only_4_byte_aligned():
         assert moe.last_launch_count() == kernels
         err = np.abs(g.astype(np.float64) - L)
         assert err.max() <= 2e-6 + 2e-6 * np.abs(L).max(), err.max()
+
+
+@pytest.mark.parametrize("n_group,topk_group,k", [(8, 4, 8), (8, 2, 8), (4, 2, 6), (8, 4, 32)])
+def test_exact_ties_go_to_the_lower_index(n_group, topk_group, k):
+    """Logits on a coarse grid (13 values 0.25 apart, bias 0) make exact ties
+    at every level: equal experts, equal group scores, equal 4th and 5th
+    groups.  Distinct grid values give distinct scores on both sides, and equal
+    logits give equal scores and equal sums on both sides, so wherever the
+    oracle sees an exact tie the GPU sees the same tie, and the lower index must
+    win on both.  Tokens where some gap is non-zero but below 1e-5 (two
+    different pairs whose sums nearly coincide) are left out."""
+    rng = np.random.default_rng(1000 * n_group + 10 * topk_group + k)
+    T, E = 2048, 32 * n_group
+    L = (0.25 * rng.integers(0, 13, size=(T, E))).astype(np.float32)
+    cfg = moe.MoeConfig(T=T, H=2048, E=E, n_group=n_group, topk_group=topk_group, k=k)
+    gi, gw, gc, _, _ = [a.cpu().numpy() if a is not None else None for a in
+                        moe.route_from_logits(cfg, torch.from_numpy(L).to(DEV), None)]
+    ref = oracle.route(L, n_group=n_group, topk_group=topk_group, k=k)
+    from parity import order_margin
+
+    def clear(m):
+        return (m == 0.0) | (m >= 1e-5)
+    ok = clear(ref["margin_group"]) & clear(ref["margin_expert"]) & clear(order_margin(ref, None))
+    tied = (ref["margin_group"] == 0.0) | (ref["margin_expert"] == 0.0)
+    assert ok.sum() >= T * 0.9 and (tied & ok).sum() >= T // 4, (ok.sum(), (tied & ok).sum())
+    bad = np.nonzero((gi[ok] != ref["idx"][ok]).any(axis=1))[0]
+    assert bad.size == 0, "token %d: gpu %s ref %s" % (np.nonzero(ok)[0][bad[0]], gi[ok][bad[0]], ref["idx"][ok][bad[0]])
+    assert np.abs(gw[ok].astype(np.float64) - ref["w"][ok]).max() <= 1e-6
+    assert np.array_equal(gc, np.bincount(gi.ravel(), minlength=E))
