@@ -47,7 +47,7 @@ constexpr int ROUTE_CHUNK = 32;    // tokens per block of the routing kernel (4 
 constexpr int ROUTE_CHUNK_SMALL = 8;  // ... and for T <= ROUTE_SMALL_T (1 per warp, 4x the blocks)
 constexpr int ROUTE_SMALL_T = 8192;
 inline int route_chunk(int T) { return T <= ROUTE_SMALL_T ? ROUTE_CHUNK_SMALL : ROUTE_CHUNK; }
-constexpr int PERM_CHUNK = 32;     // tokens per block of the bucketing kernels
+constexpr int PERM_CHUNK = 16;     // tokens per block of the bucketing kernels
 constexpr int GEMM_BM = 128;       // tensor-core tile rows (tokens)
 constexpr int GEMM_BK = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16)
 constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue

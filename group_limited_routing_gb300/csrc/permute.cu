@@ -24,76 +24,99 @@
 namespace glr {
 
 // ---------------------------------------------------------------------------
+// Per-chunk expert histograms hist[e][c] (chunks of PERM_CHUNK tokens).  A
+// block counts HIST_CHUNKS consecutive chunks in shared memory and writes each
+// expert's HIST_CHUNKS counts side by side (fewer, fuller stores than one
+// block per chunk).
+constexpr int HIST_CHUNKS = 4;
+
 __global__ void __launch_bounds__(256) bucket_hist_kernel(const int32_t *__restrict__ idx, int T, int E, int K,
-                                                          int32_t *__restrict__ hist, int *__restrict__ status)
+                                                          int nchunk, int32_t *__restrict__ hist,
+                                                          int *__restrict__ status)
 {
     pdl_wait();
-    extern __shared__ int sh[];
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        sh[e] = 0;
+    extern __shared__ int sh[];                     // [HIST_CHUNKS][E]
+    for (int i = threadIdx.x; i < HIST_CHUNKS * E; i += blockDim.x)
+        sh[i] = 0;
     __syncthreads();
-    const long long n0 = (long long)blockIdx.x * PERM_CHUNK * K;
-    const long long n1 = min((long long)T * K, n0 + (long long)PERM_CHUNK * K);
+    const int c0 = blockIdx.x * HIST_CHUNKS;
+    const long long n0 = (long long)c0 * PERM_CHUNK * K;
+    const long long n1 = min((long long)T * K, n0 + (long long)HIST_CHUNKS * PERM_CHUNK * K);
     bool bad = false;
     for (long long i = n0 + threadIdx.x; i < n1; i += blockDim.x) {
         const int e = idx[i];
+        const int q = (int)((i - n0) / (PERM_CHUNK * K));
         if (e >= 0 && e < E)
-            atomicAdd(&sh[e], 1);
+            atomicAdd(&sh[q * E + e], 1);
         else
             bad = true;
     }
     if (__syncthreads_or(bad) && threadIdx.x == 0)
         atomicOr(status, ST_BAD_INDEX);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
-        hist[(size_t)e * gridDim.x + blockIdx.x] = sh[e];   // [expert][chunk]
+#pragma unroll
+        for (int q = 0; q < HIST_CHUNKS; ++q)
+            if (c0 + q < nchunk)
+                hist[(size_t)e * nchunk + c0 + q] = sh[q * E + e];   // [expert][chunk]
 }
 
 cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status, cudaStream_t s)
 {
-    const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
-    const cudaError_t le = launch_pdl(bucket_hist_kernel, dim3(blocks), dim3(256), E * sizeof(int), s, idx, T, E, k,
-                                      hist, status);
+    const int nchunk = (T + PERM_CHUNK - 1) / PERM_CHUNK;
+    const int blocks = (nchunk + HIST_CHUNKS - 1) / HIST_CHUNKS;
+    const cudaError_t le = launch_pdl(bucket_hist_kernel, dim3(blocks), dim3(256), HIST_CHUNKS * E * sizeof(int), s,
+                                      idx, T, E, k, nchunk, hist, status);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
 }
 
 // ---------------------------------------------------------------------------
-// Per-bucket scan: one warp per expert (8 per block).  hist is
-// [expert][chunk]; in place, hist[e][c] becomes the number of bucket-e rows of
-// the chunks before c (contiguous loads, warp prefix sums), and sizes[e] the
-// bucket's size.  The bucket offsets follow in bucket_scatter.
+// Per-bucket scan: one block per expert.  hist is [expert][chunk]; in place,
+// hist[e][c] becomes the number of bucket-e rows of the chunks before c, and
+// sizes[e] the bucket's size.  Thread i takes a run of consecutive chunks:
+// its run's sum, a block-wide exclusive scan of the 256 sums (warp shuffles,
+// then the 8 warp totals in warp order), then the run is rewritten in place.
+// The bucket offsets follow in bucket_scatter.
 __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ hist, int nchunk, int E,
                                                           int32_t *__restrict__ sizes)
 {
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-    if (e >= E)
-        return;
+    __shared__ int wtot[8];
+    const int e = blockIdx.x;
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int32_t *row = hist + (size_t)e * nchunk;
-    int carry = 0;
-    for (int c0 = 0; c0 < nchunk; c0 += 32) {
-        const int c = c0 + lane;
-        const int h = (c < nchunk) ? row[c] : 0;
-        int incl = h;
+    const int per = (nchunk + blockDim.x - 1) / blockDim.x;
+    const int c0 = threadIdx.x * per;
+    const int c1 = min(nchunk, c0 + per);
+    int sum = 0;
+    for (int c = c0; c < c1; ++c)
+        sum += row[c];
+    int incl = sum;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off)
-                incl += y;
-        }
-        if (c < nchunk)
-            row[c] = carry + incl - h;
-        carry += __shfl_sync(0xffffffffu, incl, 31);
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off)
+            incl += y;
     }
-    if (lane == 0)
-        sizes[e] = carry;
+    if (lane == 31)
+        wtot[w] = incl;
+    __syncthreads();
+    int run = incl - sum;                         // exclusive within the warp
+    for (int q = 0; q < w; ++q)
+        run += wtot[q];
+    for (int c = c0; c < c1; ++c) {
+        const int h = row[c];
+        row[c] = run;
+        run += h;
+    }
+    if (threadIdx.x == blockDim.x - 1)
+        sizes[e] = run;                           // the last run ends at the bucket's size
 }
 
 cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s)
 {
-    const cudaError_t le = launch_pdl(bucket_scan_kernel, dim3((E + 7) / 8), dim3(256), 0, s, hist, nchunk, E, sizes);
+    const cudaError_t le = launch_pdl(bucket_scan_kernel, dim3(E), dim3(256), 0, s, hist, nchunk, E, sizes);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
