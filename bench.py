@@ -521,6 +521,15 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         stages["router_plus_permute"] = {"ms": round(rp_ms, 4), "bound": "hbm",
                                          "gbs": round(rp_bytes / (rp_ms * 1e-3) / 1e9, 1),
                                          "frac": round(rp_bytes / (rp_ms * 1e-3) / 1e9 / pk["hbm"], 4)}
+    # the same stage without the router GEMM, which is tensor-bound (fp32-accurate
+    # logits take three bf16 products each): selection + bucketing + row scatter
+    sp_names = ("route_select", "route_finalize", "bucket_hist", "bucket_scan", "bucket_scatter")
+    sp_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in sp_names if n in stages)
+    sp_bytes = T * E * 4 + T * k * 8 + T * k * 4 * 2 + T * H * 2 + k * T * H * 2
+    if sp_ms > 0 and not extra["backward"] and not extra["dense"]:
+        stages["select_plus_permute"] = {"ms": round(sp_ms, 4), "bound": "hbm",
+                                         "gbs": round(sp_bytes / (sp_ms * 1e-3) / 1e9, 1),
+                                         "frac": round(sp_bytes / (sp_ms * 1e-3) / 1e9 / pk["hbm"], 4)}
     # the roofline kernel: the tensor-core stage with the most time per step,
     # against the roofline that binds it at this size
     tensor_stages = [n for n in work if "flops" in work[n] and prof.get(n, (0, 0))[1] > 0]
