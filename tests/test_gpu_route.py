@@ -49,9 +49,10 @@ def test_route_matches_oracle(wid, T):
     assert n_near <= max(2, T // 100)
 
 
-@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (4, 32), (3, 4096), (4, 2048), (4, 32768)])
+@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (4, 32), (3, 4096), (4, 2048), (4, 32768), (4, 19500)])
 def test_router_logits_accuracy(wid, T):
-    # T=32768 takes the 256-expert router tiles (enough token tiles for every SM)
+    # T=32768 and 19500 take the 256-expert router tiles (a token tile for every
+    # SM); 19500 ends in a part-filled tile
     w0 = wl.WORKLOADS[wid].with_T(T)
     d = wl.layer_inputs(w0, DEV, with_experts=False)
     cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
