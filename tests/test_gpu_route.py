@@ -221,3 +221,30 @@ def test_exact_ties_go_to_the_lower_index(n_group, topk_group, k):
     assert bad.size == 0, "token %d: gpu %s ref %s" % (np.nonzero(ok)[0][bad[0]], gi[ok][bad[0]], ref["idx"][ok][bad[0]])
     assert np.abs(gw[ok].astype(np.float64) - ref["w"][ok]).max() <= 1e-6
     assert np.array_equal(gc, np.bincount(gi.ravel(), minlength=E))
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_route_from_logits_random_settings(case):
+    """Seeded random group settings (the supported 4 or 8 groups of 32, any
+    number kept, k up to 32), ragged T, random logit scale and bias: the GPU
+    selection against the oracle under the usual near-tie rules, counts exact,
+    balance-loss terms close."""
+    rng = np.random.default_rng(7000 + case)
+    n_group = int(rng.choice([4, 8]))
+    topk_group = int(rng.integers(1, n_group + 1))
+    k = int(rng.integers(1, min(32, 32 * topk_group) + 1))
+    T = int(rng.integers(1, 3000))
+    E = 32 * n_group
+    L = (rng.standard_normal((T, E)) * rng.uniform(0.2, 4.0)).astype(np.float32)
+    bias = None if case % 3 == 0 else (rng.standard_normal(E) * rng.uniform(0.0, 0.2)).astype(np.float32)
+    cfg = moe.MoeConfig(T=T, H=2048, E=E, n_group=n_group, topk_group=topk_group, k=k)
+    gi, gw, gc, gP, gl = [a.cpu().numpy() if a is not None else None for a in
+                          moe.route_from_logits(cfg, torch.from_numpy(L).to(DEV),
+                                                None if bias is None else torch.from_numpy(bias).to(DEV), aux=True)]
+    ref = oracle.route(L, bias=bias, n_group=n_group, topk_group=topk_group, k=k)
+    n_near, near = compare_routing(gi, gw, ref, E, bias=bias)
+    rc, rP, rl = oracle.counts_aux(ref["idx"], ref["scores"], E=E)
+    compare_counts(gc, gi, rc, ref["idx"], near, E)
+    np.testing.assert_allclose(gP, rP, rtol=1e-4, atol=1e-7)
+    assert abs(gl[0] - rl) <= 1e-4 * abs(rl)
+    assert n_near <= max(2, T // 50), (n_group, topk_group, k, T, n_near)
