@@ -52,7 +52,7 @@ def gemm_traffic(kernel: str):
     import hashlib
     csrc = os.path.join(ROOT, "group_limited_routing_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh", "kernels.h"):
+    for f in ("gemm.cu", "ptx.cuh"):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     try:

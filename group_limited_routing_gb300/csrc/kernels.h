@@ -50,7 +50,6 @@ inline int route_chunk(int T) { return T <= ROUTE_SMALL_T ? ROUTE_CHUNK_SMALL : 
 constexpr int PERM_CHUNK = 16;     // tokens per block of the bucketing kernels
 constexpr int GEMM_BM = 128;       // tensor-core tile rows (tokens)
 constexpr int GEMM_BK = 64;        // K per pipeline stage (one 128-byte swizzle row of bf16)
-constexpr int GEMM_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int MAX_GROUPS = 8;      // routing warp: one expert per lane per group
 
 // status bits (mirror include/moe.h)

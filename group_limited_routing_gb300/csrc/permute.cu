@@ -4,7 +4,7 @@
 // Bias与Fused MoE详解", section 四, the eager inference path) sorts tokens into
 // one bucket per expert, runs each bucket through its expert and sums the
 // weighted results.  Here:
-//   bucket_hist    per 128-token chunk, hits per expert        (reads topk_idx)
+//   bucket_hist    per PERM_CHUNK-token chunk, hits per expert  (reads topk_idx)
 //   bucket_scan    each chunk's start inside every bucket (relative) and the
 //                  bucket sizes
 //   bucket_scatter bucket offsets (exclusive scan of the sizes) and, block 0,
