@@ -411,13 +411,14 @@ cudaError_t launch_dw_reduce(const int32_t *slot_of, const float *dw_part, int n
 // ---------------------------------------------------------------------------
 // Small batches (T <= BUCKET_SMALL_MAX_T): the three bucketing steps in one
 // launch.  Every block recomputes the (tiny) bucketing from topk_idx in shared
-// memory -- thread e counts expert e's pairs, a block scan gives the bucket
-// offsets, then thread e walks the pairs in (token, j) order and hands out its
-// bucket's slots, so slots are stable exactly as in the general path -- and
-// copies its share of the hidden rows into X_perm; block 0 also writes the
-// bucket sizes, slot_of and the m-tile list, in tiles of at most `mt` rows
-// (16 for the small-T GEMM kinds, else 128; a bucket can exceed T rows when a
-// token lists an expert twice), then the shared group (all T tokens).
+// memory -- per-expert counts with shared-memory atomics (exact, order-free),
+// a block scan gives the bucket offsets, then one warp walks the pairs in
+// (token, j) order, 32 at a time, and hands out slots with __match_any_sync,
+// so slots are stable exactly as in the general path -- and copies its share
+// of the hidden rows into X_perm; block 0 also writes the bucket sizes,
+// slot_of and the m-tile list, in tiles of at most `mt` rows (16 for the
+// small-T GEMM kinds, else 128; a bucket can exceed T rows when a token lists
+// an expert twice), then the shared group (all T tokens).
 __global__ void __launch_bounds__(256) bucket_small_kernel(const int32_t *__restrict__ idx,
                                                            const uint16_t *__restrict__ x, int T, int H, int E,
                                                            int K, int mt, int32_t *__restrict__ sizes,
@@ -429,8 +430,12 @@ __global__ void __launch_bounds__(256) bucket_small_kernel(const int32_t *__rest
     __shared__ int s_idx[BUCKET_SMALL_MAX_T * 32];
     __shared__ int s_slot[BUCKET_SMALL_MAX_T * 32];
     __shared__ int s_wsum[8][2];
+    __shared__ int s_cnt[256];
+    __shared__ int s_next[256];
     const int n = T * K;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    s_cnt[tid] = 0;                          // blockDim.x == 256 >= E
+    __syncthreads();
     bool bad = false;
     for (int i = tid; i < n; i += blockDim.x) {
         const int e = idx[i];
@@ -438,13 +443,12 @@ __global__ void __launch_bounds__(256) bucket_small_kernel(const int32_t *__rest
         bad |= !ok;
         s_idx[i] = ok ? e : -1;
         s_slot[i] = -1;
+        if (ok)
+            atomicAdd(&s_cnt[e], 1);
     }
     __syncthreads();
-    const int e = tid;                       // blockDim.x == 256 >= E
-    int cnt = 0;
-    if (e < E)
-        for (int i = 0; i < n; ++i)
-            cnt += (s_idx[i] == e) ? 1 : 0;
+    const int e = tid;
+    const int cnt = (e < E) ? s_cnt[e] : 0;
     const int ntile = (cnt + mt - 1) / mt;   // m-tiles of bucket e
     int a = cnt, b = ntile;                  // inclusive warp scans: rows, m-tiles
 #pragma unroll
@@ -472,10 +476,25 @@ __global__ void __launch_bounds__(256) bucket_small_kernel(const int32_t *__rest
     }
     const int offset = ra + a - cnt;         // first slot of bucket e
     const int tile = rb + b - ntile;         // its first m-tile
-    if (e < E && cnt)
-        for (int i = 0, s = offset; i < n; ++i)
-            if (s_idx[i] == e)
-                s_slot[i] = s++;
+    s_next[e] = offset;
+    __syncthreads();
+    if (w == 0) {
+        // stable slots: pairs in (token, j) order, a bucket's rows in that order
+        for (int base = 0; base < n; base += 32) {
+            const int i = base + lane;
+            const int ei = (i < n) ? s_idx[i] : -1;
+            const unsigned peers = __match_any_sync(0xffffffffu, ei);
+            int slot = -1;
+            if (ei >= 0)
+                slot = s_next[ei] + __popc(peers & ((1u << lane) - 1u));
+            __syncwarp();
+            if (ei >= 0 && (__ffs(peers) - 1) == lane)   // lowest lane of the peer group
+                s_next[ei] += __popc(peers);
+            __syncwarp();
+            if (i < n)
+                s_slot[i] = slot;
+        }
+    }
     __syncthreads();
     if (blockIdx.x == 0) {
         if (e < E) {
