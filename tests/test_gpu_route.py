@@ -49,10 +49,11 @@ def test_route_matches_oracle(wid, T):
     assert n_near <= max(2, T // 100)
 
 
-@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (4, 32), (3, 4096), (4, 2048), (4, 32768), (4, 19500)])
+@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (2, 1), (2, 31), (4, 32), (3, 4096), (4, 2048), (4, 32768),
+                                   (4, 19500)])
 def test_router_logits_accuracy(wid, T):
-    # T=32768 and 19500 take the 256-expert router tiles (a token tile for every
-    # SM); 19500 ends in a part-filled tile
+    # T <= 32: the CUDA-core router; T=32768 and 19500 take the 256-expert
+    # router tiles (a token tile for every SM), 19500 ending in a part-filled tile
     w0 = wl.WORKLOADS[wid].with_T(T)
     d = wl.layer_inputs(w0, DEV, with_experts=False)
     cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
