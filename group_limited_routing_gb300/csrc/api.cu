@@ -125,17 +125,38 @@ int check_forward_cfg(const moe_cfg *c)
 struct RouteLayout {
     size_t w3, logits, ppart, total;
     int nchunk;
+    int ksplit;   // K parts of the router GEMM's logits region
 };
+
+// K parts of the router GEMM: when the 128-expert tiles are few, each tile's
+// K range is split into parts that run on different SMs (partial logits, added
+// in part order by the routing kernel), up to ROUTER_MAX_KSPLIT parts and
+// ~ROUTER_SPLIT_UNITS work units.  The decode-size CUDA-core router and the
+// wide tiles never split.
+constexpr int ROUTER_SPLIT_UNITS = 152;
+
+int router_ksplit(const moe_cfg &c)
+{
+    if (c.T <= ROUTER_SIMT_MAX_T)
+        return 1;
+    const int tiles = ((c.T + GEMM_BM - 1) / GEMM_BM) * (c.E / 128);
+    const int kb = c.H / GEMM_BK;
+    int ks = 1;
+    while (ks < ROUTER_MAX_KSPLIT && tiles * ks * 2 <= ROUTER_SPLIT_UNITS && kb % (ks * 2) == 0)
+        ks *= 2;
+    return ks;
+}
 
 RouteLayout route_layout(const moe_cfg &c)
 {
     RouteLayout L;
     L.nchunk = (c.T + route_chunk(c.T) - 1) / route_chunk(c.T);
+    L.ksplit = router_ksplit(c);
     size_t off = sizeof(WsHeader);
     L.w3 = off;
     off = align_up(off + 3ull * c.E * c.H * 2, 256);
     L.logits = off;
-    off = align_up(off + (size_t)c.T * c.E * 4, 256);
+    off = align_up(off + (size_t)L.ksplit * c.T * c.E * 4, 256);
     L.ppart = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
     L.total = off;
@@ -311,9 +332,13 @@ T *at(void *ws, size_t off)
 // counts (nullable) is cleared by the split kernel, for the routing kernel after it.
 // W_split: the bf16 x 3 split of W made by moe_prepare_router, or NULL to
 // split W into the workspace here (that launch also clears counts).
+// ksplit_max: K parts the logits buffer has room for (L.ksplit, or 1 for a
+// caller's [T, E] buffer); nparts receives the parts actually written.
 int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split, float *logits,
-                int32_t *counts, void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches)
+                int32_t *counts, void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches,
+                int ksplit_max, int &nparts)
 {
+    nparts = 1;
     if (c.T <= ROUTER_SIMT_MAX_T && c.H % 8 == 0 && aligned(W, 16)) {
         // a few token tiles cannot fill the tensor-core kernel: CUDA cores, fp32 W as is
         // (16-byte loads of W; a W that is only 4-byte aligned takes the tensor-core path)
@@ -338,27 +363,33 @@ int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
     if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
         !make_map_bf16(&p.tmB0, W3, 3ull * c.E, c.H, GEMM_BK, bn))
         return MOE_ERR_CUDA;
+    const int ks = wide ? 1 : std::max(1, std::min(ksplit_max, L.ksplit));
     p.out = logits;
     p.n_tiles = c.E / bn;
-    p.num_tiles_static = ((c.T + GEMM_BM - 1) / GEMM_BM) * p.n_tiles;
-    p.kblocks = c.H / GEMM_BK;
+    p.ksplit = ks;
+    p.part_stride = (long long)c.T * c.E;
+    p.num_tiles_static = ((c.T + GEMM_BM - 1) / GEMM_BM) * p.n_tiles * ks;
+    p.kblocks = c.H / GEMM_BK / ks;
     p.T = c.T;
     p.E = c.E;
     p.H = c.H;
     p.ld_out = c.E;
     p.status = &header(ws)->status;
     GLR_LAUNCH(KID_ROUTER_GEMM, launch_gemm(wide ? GK_ROUTER_WIDE : GK_ROUTER, p, std::min(sms, p.num_tiles_static), s));
+    nparts = ks;
     return MOE_OK;
 }
 
 // counts must be zero on the stream when this runs.
-int route_select(const moe_cfg &c, const float *logits, const float *bias, int32_t *idx, float *w,
+// logits: nparts K-part buffers of [T, E] (see router_gemm).
+int route_select(const moe_cfg &c, const float *logits, int nparts, const float *bias, int32_t *idx, float *w,
                  int32_t *counts, float *aux_P, float *aux_loss, void *ws, const RouteLayout &L, cudaStream_t s,
                  int &launches)
 {
     float *ppart = (aux_P || aux_loss) ? at<float>(ws, L.ppart) : nullptr;
-    GLR_LAUNCH(KID_SELECT, launch_route_select(logits, bias, c.T, c.E, c.n_group, c.topk_group, c.k, c.rsf, c.eps, idx,
-                                               w, counts, ppart, &header(ws)->status, s));
+    GLR_LAUNCH(KID_SELECT, launch_route_select(logits, nparts, (long long)c.T * c.E, bias, c.T, c.E, c.n_group,
+                                               c.topk_group, c.k, c.rsf, c.eps, idx, w, counts, ppart,
+                                               &header(ws)->status, s));
     if (ppart)
         GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(counts, ppart, L.nchunk, c.T, c.E, c.k, aux_P, aux_loss, s));
     return MOE_OK;
@@ -418,8 +449,9 @@ int moe_router_logits(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W
     if ((rc = device_check(&sms)) != MOE_OK)
         return rc;
     int launches = 0;
+    int nparts = 1;
     rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, nullptr, ws, L, sms,
-                     static_cast<cudaStream_t>(stream), launches);
+                     static_cast<cudaStream_t>(stream), launches, 1, nparts);
     g_last_launches = launches;
     return rc;
 }
@@ -446,7 +478,7 @@ int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * cfg->E, s) != cudaSuccess)
         return MOE_ERR_CUDA;
-    rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
+    rc = route_select(*cfg, logits, 1, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
                       launches);
     g_last_launches = launches;
     return rc;
@@ -473,10 +505,12 @@ int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     float *logits = at<float>(ws, L.logits);
-    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches);
+    int nparts = 1;
+    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches, L.ksplit,
+                     nparts);
     if (rc == MOE_OK)
-        rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
-                          launches);
+        rc = route_select(*cfg, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
+                          L, s, launches);
     g_last_launches = launches;
     return rc;
 }
@@ -523,10 +557,12 @@ int moe_route_prepared(const moe_cfg *cfg, const moe_bf16 *hidden, const float *
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
     float *logits = at<float>(ws, L.logits);
-    rc = router_gemm(*cfg, hidden, W_router, W_split, logits, expert_counts, ws, L, sms, s, launches);
+    int nparts = 1;
+    rc = router_gemm(*cfg, hidden, W_router, W_split, logits, expert_counts, ws, L, sms, s, launches, L.ksplit,
+                     nparts);
     if (rc == MOE_OK)
-        rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
-                          launches);
+        rc = route_select(*cfg, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
+                          L, s, launches);
     g_last_launches = launches;
     return rc;
 }
@@ -1088,10 +1124,12 @@ int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_
         return MOE_ERR_CUDA;
     int launches = 0;
     float *logits = at<float>(ws, L.logits);
-    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches);
+    int nparts = 1;
+    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches, L.ksplit,
+                     nparts);
     if (rc == MOE_OK)
-        rc = route_select(*cfg, logits, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws, L, s,
-                          launches);
+        rc = route_select(*cfg, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
+                          L, s, launches);
     if (rc == MOE_OK && status_out &&
         cudaMemcpyAsync(status_out, &header(ws)->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
             cudaSuccess)

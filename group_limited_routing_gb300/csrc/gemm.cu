@@ -217,6 +217,7 @@ struct TileInfo {
     int shared;
     int kblocks;  // K blocks of this tile
     int b_row;    // GK_WGRAD: first B row
+    int kp;       // router: K part (its K blocks start at kp * kblocks)
 };
 
 template <int KIND>
@@ -244,8 +245,14 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
         ti.out_row = (ti.shared ? 0 : e * p.wg_fm * 128) + (r / p.wg_fn) * 128;   // feature row of the output
         return ti;
     }
+    ti.kp = 0;
     if (BASE == GK_ROUTER) {
-        ti.a_row = (tile / p.n_tiles) * GEMM_BM;
+        // tile = (token tile * n_tiles + expert tile) * ksplit + K part
+        const int ks = p.ksplit > 1 ? p.ksplit : 1;
+        ti.kp = tile % ks;
+        const int base = tile / ks;
+        ti.nt = base % p.n_tiles;
+        ti.a_row = (base / p.n_tiles) * GEMM_BM;
         ti.out_row = ti.a_row;
         ti.rows = min(GEMM_BM, p.T - ti.a_row);
         ti.group = 0;
@@ -291,10 +298,11 @@ __device__ __forceinline__ void issue_loads(const GemmParams &p, const TileInfo 
         tma_load_2d(sB, mb, bar, k0, wrow);
         tma_load_2d(sB + C::B_HALF, mb, bar, k0, wrow + 128);
     } else if constexpr (BASE == GK_ROUTER) {
-        tma_load_2d(sA, &p.tmA0, bar, k0, ti.a_row);
+        const int kr = k0 + ti.kp * p.kblocks * GEMM_BK;   // this K part's columns
+        tma_load_2d(sA, &p.tmA0, bar, kr, ti.a_row);
 #pragma unroll
         for (int s = 0; s < 3; ++s)
-            tma_load_2d(sB + s * C::B_PART, &p.tmB0, bar, k0, s * p.E + ti.nt * C::BN);
+            tma_load_2d(sB + s * C::B_PART, &p.tmB0, bar, kr, s * p.E + ti.nt * C::BN);
     } else if constexpr (BASE == GK_GATE_UP) {
         const CUtensorMap *ma = ti.shared ? &p.tmA1 : &p.tmA0;
         const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
@@ -687,8 +695,8 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
     const int valid_rows = ti.rows - quad * 32;
     if (valid_rows > 0) {
         const size_t ld_bytes = (size_t)p.ld_out * 4;
-        char *gbase = static_cast<char *>(p.out) + (size_t)(ti.out_row + quad * 32) * ld_bytes +
-                      (size_t)(ti.nt * C::BN + half * COLS) * 4;
+        char *gbase = static_cast<char *>(p.out) + (size_t)ti.kp * (size_t)p.part_stride * 4 +
+                      (size_t)(ti.out_row + quad * 32) * ld_bytes + (size_t)(ti.nt * C::BN + half * COLS) * 4;
         if constexpr (C::NBUF == 0) {
             // each thread's 512 contiguous bytes, straight from registers
             if (lane < valid_rows) {

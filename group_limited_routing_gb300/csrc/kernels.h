@@ -94,7 +94,9 @@ struct GemmParams {
     const int *num_mtiles;
     int num_tiles_static; // router: tiles known on the host
     int n_tiles;          // n-tiles per m-tile
-    int kblocks;          // K / GEMM_BK
+    int kblocks;          // K / GEMM_BK (router: per K part)
+    int ksplit;           // router: K parts per tile (0 or 1: none); part kp writes out + kp * part_stride
+    long long part_stride; // router: floats between the K parts' logits
     int T, E, I, H, kT;
     int ld_out;           // output row stride in elements
     int *status;
@@ -131,9 +133,12 @@ cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, 
                                int32_t *counts, cudaStream_t s);
 
 // counts[E] must be zero (or hold counts to add to) before the launch.
-cudaError_t launch_route_select(const float *logits, const float *bias, int T, int E, int n_group,
-                                int topk_group, int k, float rsf, float eps, int32_t *idx, float *w,
-                                int32_t *counts, float *ppart, int *status, cudaStream_t s);
+// logits: nparts partial-sum buffers of [T, E], part_stride floats apart (the
+// router GEMM's K parts; 1 part: plain logits), nparts <= ROUTER_MAX_KSPLIT
+constexpr int ROUTER_MAX_KSPLIT = 4;
+cudaError_t launch_route_select(const float *logits, int nparts, long long part_stride, const float *bias, int T,
+                                int E, int n_group, int topk_group, int k, float rsf, float eps, int32_t *idx,
+                                float *w, int32_t *counts, float *ppart, int *status, cudaStream_t s);
 
 cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int nchunk, int T, int E, int k,
                                   float *aux_P, float *aux_loss, cudaStream_t s);

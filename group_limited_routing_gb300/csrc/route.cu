@@ -148,6 +148,25 @@ cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, 
 }
 
 // ---------------------------------------------------------------------------
+// Logit (t, e) when the router GEMM wrote it in `nparts` K parts (partial sums
+// over consecutive K ranges, part p at logits + p * part_stride): their sum in
+// part order, so the result does not depend on scheduling.
+__device__ __forceinline__ float load_logit(const float *__restrict__ logits, size_t off, int nparts,
+                                            long long part_stride)
+{
+    float v[ROUTER_MAX_KSPLIT];
+#pragma unroll
+    for (int q = 0; q < ROUTER_MAX_KSPLIT; ++q)          // every part's load in flight at once
+        v[q] = (q < nparts) ? __ldg(logits + (size_t)q * part_stride + off) : 0.0f;
+    float L = v[0];
+#pragma unroll
+    for (int q = 1; q < ROUTER_MAX_KSPLIT; ++q)
+        if (q < nparts)
+            L += v[q];
+    return L;
+}
+
+// ---------------------------------------------------------------------------
 // Order-preserving map of fp32 onto uint32 (for non-NaN values): a > b as
 // floats exactly when key(a) > key(b), so warp-wide float max is one
 // __reduce_max_sync.  +0 and -0 get neighbouring keys; the scores compared
@@ -174,8 +193,8 @@ __device__ __forceinline__ float fkey_value(uint32_t k)
 // scores of its chunk for the balance loss.
 template <int G>
 __global__ void __launch_bounds__(256) route_select_kernel(
-    const float *__restrict__ logits, const float *__restrict__ bias, int T, int chunk, int TG, int K, float rsf,
-    float eps,
+    const float *__restrict__ logits, int nparts, long long part_stride, const float *__restrict__ bias, int T,
+    int chunk, int TG, int K, float rsf, float eps,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     float *__restrict__ ppart, int *__restrict__ status)
 {
@@ -203,11 +222,10 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     const int t0 = blockIdx.x * chunk;
     const int t1 = min(T, t0 + chunk);
     for (int t = t0 + warp; t < t1; t += 8) {
-        const float *row = logits + (size_t)t * E;
         float s[G], b[G];
 #pragma unroll
         for (int j = 0; j < G; ++j) {
-            const float L = __ldg(row + 32 * j + lane);
+            const float L = load_logit(logits, (size_t)t * E + 32 * j + lane, nparts, part_stride);
             nonfinite |= !isfinite(L) || !isfinite(bias_r[j]);
             s[j] = __frcp_rn(1.0f + expf(-L));        // section 二 step 1 (IEEE-rounded 1/x)
             b[j] = s[j] + bias_r[j];                  // section 三: choose on s + bias
@@ -330,7 +348,8 @@ __global__ void __launch_bounds__(256) route_select_kernel(
 // expert id), the same sequential sum for the normaliser.
 template <int G, int TG>
 __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
-    const float *__restrict__ logits, const float *__restrict__ bias, int T, int chunk, int K, float rsf, float eps,
+    const float *__restrict__ logits, int nparts, long long part_stride, const float *__restrict__ bias, int T,
+    int chunk, int K, float rsf, float eps,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
     float *__restrict__ ppart, int *__restrict__ status)
 {
@@ -363,7 +382,7 @@ __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
     if (t0 + warp < t1) {
 #pragma unroll
         for (int j = 0; j < G; ++j)
-            Ln[j] = __ldg(logits + (size_t)(t0 + warp) * E + 32 * j + lane);
+            Ln[j] = load_logit(logits, (size_t)(t0 + warp) * E + 32 * j + lane, nparts, part_stride);
     }
     for (int t = t0 + warp; t < t1; t += 8) {
         float L[G];
@@ -373,7 +392,7 @@ __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
         if (t + 8 < t1) {
 #pragma unroll
             for (int j = 0; j < G; ++j)
-                Ln[j] = __ldg(logits + (size_t)(t + 8) * E + 32 * j + lane);
+                Ln[j] = load_logit(logits, (size_t)(t + 8) * E + 32 * j + lane, nparts, part_stride);
         }
         float s[G];
         uint32_t kk[G];
@@ -498,23 +517,25 @@ __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
     }
 }
 
-cudaError_t launch_route_select(const float *logits, const float *bias, int T, int E, int n_group, int topk_group,
-                                int k, float rsf, float eps, int32_t *idx, float *w, int32_t *counts, float *ppart,
-                                int *status, cudaStream_t s)
+cudaError_t launch_route_select(const float *logits, int nparts, long long part_stride, const float *bias, int T,
+                                int E, int n_group, int topk_group, int k, float rsf, float eps, int32_t *idx,
+                                float *w, int32_t *counts, float *ppart, int *status, cudaStream_t s)
 {
     const int chunk = route_chunk(T);
     const int blocks = (T + chunk - 1) / chunk;
 #define GLR_ROUTE_CASE(GG)                                                                                   \
     case GG: {                                                                                               \
-        const cudaError_t le = launch_pdl(route_select_kernel<GG>, dim3(blocks), dim3(256), 0, s, logits, bias, \
-                                          T, chunk, topk_group, k, rsf, eps, idx, w, counts, ppart, status);   \
+        const cudaError_t le = launch_pdl(route_select_kernel<GG>, dim3(blocks), dim3(256), 0, s, logits,      \
+                                          nparts, part_stride, bias, T, chunk, topk_group, k, rsf, eps, idx, w,  \
+                                          counts, ppart, status);                                                \
         if (le != cudaSuccess)                                                                               \
             return le;                                                                                       \
         break;                                                                                               \
     }
     if (n_group == 8 && topk_group == 4) {
         const cudaError_t le = launch_pdl(route_select_sorted_kernel<8, 4>, dim3(blocks), dim3(256), 0, s, logits,
-                                          bias, T, chunk, k, rsf, eps, idx, w, counts, ppart, status);
+                                          nparts, part_stride, bias, T, chunk, k, rsf, eps, idx, w, counts, ppart,
+                                          status);
         if (le != cudaSuccess)
             return le;
         return cudaPeekAtLastError();
