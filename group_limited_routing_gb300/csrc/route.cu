@@ -154,6 +154,8 @@ cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, 
 __device__ __forceinline__ float load_logit(const float *__restrict__ logits, size_t off, int nparts,
                                             long long part_stride)
 {
+    if (nparts == 1)
+        return __ldg(logits + off);
     float v[ROUTER_MAX_KSPLIT];
 #pragma unroll
     for (int q = 0; q < ROUTER_MAX_KSPLIT; ++q)          // every part's load in flight at once
