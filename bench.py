@@ -194,7 +194,8 @@ def workload_name_moe(w0):
     if w0.wid == 4:
         return "T=%d full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)" % w0.T
     if w0.wid == 5:
-        return "%d-layer stack (x + moe(rmsnorm(x))), T=%d, full size" % (w0.layers, w0.T)
+        return ("%d-layer stack (x + moe(rmsnorm(x))), T=%d, full size, per-layer expert counts and balance loss"
+                % (w0.layers, w0.T))
     return "%s (T=%d)" % (w0.name, w0.T)
 
 
@@ -324,10 +325,13 @@ def build_model(w0, dev, dense_inter=0):
     ws_r = moe.Workspace(cfg, 0, dev)
     ws_f = moe.Workspace(cfg, 1, dev)
     layers = []
+    # the 19-layer stack workload also computes every layer's balance loss
+    # (E * sum_i f_i P_i from the router scores) beside its expert counts
     for layer in range(w0.layers):
         d = wl.layer_inputs(w0, dev, layer=layer)
         layers.append(moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
-                                   d["shared_gate_up"], d["shared_down"], ws_route=ws_r, ws_fwd=ws_f))
+                                   d["shared_gate_up"], d["shared_down"], aux=w0.layers > 1, ws_route=ws_r,
+                                   ws_fwd=ws_f))
     return cfg, (moe.MoEStack(layers) if w0.layers > 1 else layers[0])
 
 

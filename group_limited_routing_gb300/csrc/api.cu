@@ -123,7 +123,7 @@ int check_forward_cfg(const moe_cfg *c)
 
 // ---------------------------------------------------------------- layouts
 struct RouteLayout {
-    size_t w3, logits, ppart, total;
+    size_t w3, logits, ppart, pfin, total;
     int nchunk;
     int ksplit;   // K parts of the router GEMM's logits region
 };
@@ -159,6 +159,8 @@ RouteLayout route_layout(const moe_cfg &c)
     off = align_up(off + (size_t)L.ksplit * c.T * c.E * 4, 256);
     L.ppart = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
+    L.pfin = off;
+    off = align_up(off + (size_t)ROUTE_FIN_BLOCKS * c.E * 4, 256);
     L.total = off;
     return L;
 }
@@ -389,9 +391,10 @@ int route_select(const moe_cfg &c, const float *logits, int nparts, const float 
     float *ppart = (aux_P || aux_loss) ? at<float>(ws, L.ppart) : nullptr;
     GLR_LAUNCH(KID_SELECT, launch_route_select(logits, nparts, (long long)c.T * c.E, bias, c.T, c.E, c.n_group,
                                                c.topk_group, c.k, c.rsf, c.eps, idx, w, counts, ppart,
-                                               &header(ws)->status, s));
+                                               &header(ws)->status, ppart ? &header(ws)->fin_ticket : nullptr, s));
     if (ppart)
-        GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(counts, ppart, L.nchunk, c.T, c.E, c.k, aux_P, aux_loss, s));
+        GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(counts, ppart, L.nchunk, c.T, c.E, c.k, at<float>(ws, L.pfin),
+                                                       &header(ws)->fin_ticket, aux_P, aux_loss, s));
     return MOE_OK;
 }
 

@@ -63,7 +63,8 @@ struct WsHeader {
     int status;      // OR of ST_* bits
     int num_mtiles;  // m-tiles of the grouped GEMMs (written on the device)
     int tile_ctr[2]; // claim counters of the two weight-gradient launches (zeroed on the device)
-    int pad[60];
+    int fin_ticket;  // blocks of the balance-loss reduction done (back to zero at its end)
+    int pad[59];
 };
 
 // The _SMALL kinds are the grouped GEMMs for T <= GEMM_SMALL_T (decode): every
@@ -138,10 +139,14 @@ cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, 
 constexpr int ROUTER_MAX_KSPLIT = 4;
 cudaError_t launch_route_select(const float *logits, int nparts, long long part_stride, const float *bias, int T,
                                 int E, int n_group, int topk_group, int k, float rsf, float eps, int32_t *idx,
-                                float *w, int32_t *counts, float *ppart, int *status, cudaStream_t s);
+                                float *w, int32_t *counts, float *ppart, int *status, int *fin_ticket,
+                                cudaStream_t s);
 
+// part: at least ROUTE_FIN_BLOCKS x E floats of scratch; ticket: an int that is
+// zero when the launch starts (the routing kernel before it clears it)
+constexpr int ROUTE_FIN_BLOCKS = 32;
 cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int nchunk, int T, int E, int k,
-                                  float *aux_P, float *aux_loss, cudaStream_t s);
+                                  float *part, int *ticket, float *aux_P, float *aux_loss, cudaStream_t s);
 
 cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t *hist, int *status,
                                cudaStream_t s);

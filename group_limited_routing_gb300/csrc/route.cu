@@ -198,13 +198,15 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     const float *__restrict__ logits, int nparts, long long part_stride, const float *__restrict__ bias, int T,
     int chunk, int TG, int K, float rsf, float eps,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
-    float *__restrict__ ppart, int *__restrict__ status)
+    float *__restrict__ ppart, int *__restrict__ status, int *__restrict__ fin_ticket)
 {
     pdl_wait();
     constexpr int E = 32 * G;
     constexpr unsigned FULL = 0xffffffffu;
     __shared__ int sh_hist[E];
     __shared__ float sh_p[8][E];
+    if (fin_ticket && blockIdx.x == 0 && threadIdx.x == 0)
+        *fin_ticket = 0;                           // for the balance-loss reduction that follows
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -353,11 +355,13 @@ __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
     const float *__restrict__ logits, int nparts, long long part_stride, const float *__restrict__ bias, int T,
     int chunk, int K, float rsf, float eps,
     int32_t *__restrict__ idx_out, float *__restrict__ w_out, int32_t *__restrict__ counts,
-    float *__restrict__ ppart, int *__restrict__ status)
+    float *__restrict__ ppart, int *__restrict__ status, int *__restrict__ fin_ticket)
 {
     pdl_wait();
     constexpr int E = 32 * G;
     constexpr unsigned FULL = 0xffffffffu;
+    if (fin_ticket && blockIdx.x == 0 && threadIdx.x == 0)
+        *fin_ticket = 0;                           // for the balance-loss reduction that follows
     __shared__ int sh_hist[E];
     __shared__ float sh_p[8][E];
     __shared__ float sh_s[8][E];       // per warp: the current token's unbiased scores, by expert
@@ -521,7 +525,8 @@ __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
 
 cudaError_t launch_route_select(const float *logits, int nparts, long long part_stride, const float *bias, int T,
                                 int E, int n_group, int topk_group, int k, float rsf, float eps, int32_t *idx,
-                                float *w, int32_t *counts, float *ppart, int *status, cudaStream_t s)
+                                float *w, int32_t *counts, float *ppart, int *status, int *fin_ticket,
+                                cudaStream_t s)
 {
     const int chunk = route_chunk(T);
     const int blocks = (T + chunk - 1) / chunk;
@@ -529,7 +534,7 @@ cudaError_t launch_route_select(const float *logits, int nparts, long long part_
     case GG: {                                                                                               \
         const cudaError_t le = launch_pdl(route_select_kernel<GG>, dim3(blocks), dim3(256), 0, s, logits,      \
                                           nparts, part_stride, bias, T, chunk, topk_group, k, rsf, eps, idx, w,  \
-                                          counts, ppart, status);                                                \
+                                          counts, ppart, status, fin_ticket);                                    \
         if (le != cudaSuccess)                                                                               \
             return le;                                                                                       \
         break;                                                                                               \
@@ -537,7 +542,7 @@ cudaError_t launch_route_select(const float *logits, int nparts, long long part_
     if (n_group == 8 && topk_group == 4) {
         const cudaError_t le = launch_pdl(route_select_sorted_kernel<8, 4>, dim3(blocks), dim3(256), 0, s, logits,
                                           nparts, part_stride, bias, T, chunk, k, rsf, eps, idx, w, counts, ppart,
-                                          status);
+                                          status, fin_ticket);
         if (le != cudaSuccess)
             return le;
         return cudaPeekAtLastError();
@@ -560,45 +565,48 @@ cudaError_t launch_route_select(const float *logits, int nparts, long long part_
 
 // ---------------------------------------------------------------------------
 // Balance loss (only when asked for): P[e] = sum over chunks of ppart[c][e] / T
-// and aux = E * sum_e counts[e] / (k T) * P[e].  One block of 512 threads:
-// warp w reads chunk rows w, w + 16, ... (lane l takes experts l, l + 32, ...,
-// so every load is a coalesced 128-byte run); the 16 warp partials are then
-// added in warp order.  Every sum runs in a fixed order, so the result is
-// reproducible bit for bit.
-constexpr int FIN_WARPS = 16;
+// and aux = E * sum_e counts[e] / (k T) * P[e].  Block b adds a fixed run of
+// chunk rows (thread e takes expert e, so every row is one coalesced load) and
+// stores its partial sums; the last block to finish (a ticket in the
+// workspace header, cleared by the routing kernel that runs just before)
+// adds the partials in block order in double and forms P and the loss.  Every sum runs in a fixed order,
+// so the result is reproducible bit for bit; no block ever waits for another.
+constexpr int FIN_BLOCKS = ROUTE_FIN_BLOCKS;
 
-__global__ void __launch_bounds__(FIN_WARPS * 32) route_finalize_kernel(const int32_t *__restrict__ counts,
-                                                                         const float *__restrict__ ppart, int nchunk,
-                                                                         int T, int E, int K, float *__restrict__ aux_P,
-                                                                         float *__restrict__ aux_loss)
+__global__ void __launch_bounds__(256) route_finalize_kernel(const int32_t *__restrict__ counts,
+                                                             const float *__restrict__ ppart, int nchunk,
+                                                             int rows_per_block, int T, int E, int K,
+                                                             float *__restrict__ part, int *__restrict__ ticket,
+                                                             float *__restrict__ aux_P, float *__restrict__ aux_loss)
 {
     pdl_wait();
-    __shared__ float sp[FIN_WARPS][MAX_GROUPS * 32];
-    __shared__ double red[FIN_WARPS];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int G = E / 32;
-    float pv[MAX_GROUPS];
-#pragma unroll
-    for (int j = 0; j < MAX_GROUPS; ++j)
-        pv[j] = 0.0f;
-#pragma unroll 4
-    for (int ch = warp; ch < nchunk; ch += FIN_WARPS) {
-#pragma unroll
-        for (int j = 0; j < MAX_GROUPS; ++j)
-            if (j < G)
-                pv[j] += ppart[(size_t)ch * E + 32 * j + lane];
+    __shared__ int s_last;
+    __shared__ double red[8];
+    const int e = threadIdx.x;                      // blockDim.x == 256 >= E
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int r0 = blockIdx.x * rows_per_block;
+    const int r1 = min(nchunk, r0 + rows_per_block);
+    if (e < E) {
+        float v = 0.0f;
+#pragma unroll 8
+        for (int r = r0; r < r1; ++r)
+            v += ppart[(size_t)r * E + e];
+        part[(size_t)blockIdx.x * E + e] = v;
     }
-#pragma unroll
-    for (int j = 0; j < MAX_GROUPS; ++j)
-        if (j < G)
-            sp[warp][32 * j + lane] = pv[j];
+    __threadfence();                                // partials visible before the ticket
     __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = (atomicAdd(ticket, 1) == (int)gridDim.x - 1) ? 1 : 0;
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
     double contrib = 0.0;
-    const int e = threadIdx.x;
     if (e < E) {
         double psum = 0.0;
-        for (int w = 0; w < FIN_WARPS; ++w)
-            psum += (double)sp[w][e];
+#pragma unroll 8
+        for (int b = 0; b < (int)gridDim.x; ++b)
+            psum += (double)__ldcg(part + (size_t)b * E + e);
         const double P = psum / (double)T;
         if (aux_P)
             aux_P[e] = (float)P;
@@ -610,19 +618,26 @@ __global__ void __launch_bounds__(FIN_WARPS * 32) route_finalize_kernel(const in
     if (lane == 0)
         red[warp] = contrib;
     __syncthreads();
-    if (threadIdx.x == 0 && aux_loss) {
-        double a = 0.0;
-        for (int w = 0; w < FIN_WARPS; ++w)
-            a += red[w];
-        *aux_loss = (float)((double)E * a);
+    if (threadIdx.x == 0) {
+        if (aux_loss) {
+            double a = 0.0;
+            for (int w = 0; w < 8; ++w)
+                a += red[w];
+            *aux_loss = (float)((double)E * a);
+        }
+        *ticket = 0;                                // ready for the next call on this workspace
     }
 }
 
 cudaError_t launch_route_finalize(const int32_t *counts, const float *ppart, int nchunk, int T, int E, int k,
-                                  float *aux_P, float *aux_loss, cudaStream_t s)
+                                  float *part, int *ticket, float *aux_P, float *aux_loss, cudaStream_t s)
 {
-    const cudaError_t le = launch_pdl(route_finalize_kernel, dim3(1), dim3(FIN_WARPS * 32), 0, s, counts, ppart,
-                                      nchunk, T, E, k, aux_P, aux_loss);
+    if (E > 256 || nchunk < 1)
+        return cudaErrorInvalidValue;
+    const int rows = (nchunk + FIN_BLOCKS - 1) / FIN_BLOCKS;
+    const int blocks = (nchunk + rows - 1) / rows;
+    const cudaError_t le = launch_pdl(route_finalize_kernel, dim3(blocks), dim3(256), 0, s, counts, ppart, nchunk,
+                                      rows, T, E, k, part, ticket, aux_P, aux_loss);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
