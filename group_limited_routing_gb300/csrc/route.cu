@@ -11,6 +11,20 @@
 // and the load-balancing loss E * sum_i f_i * P_i of the InternLumina-U2
 // training-pitfalls article (section "MoE 负载均衡 Loss 别忘加").
 //
+// Kernels, in the order a forward runs them:
+//   split_router_kernel        fp32 router weight -> exact bf16 hi/mid/lo parts
+//                              for the tensor-core router GEMM (once per model);
+//   router_simt_kernel         decode-size router logits on the CUDA cores,
+//                              one block per expert, fp32 weight as is;
+//   route_select_kernel<G>     scores, group-limited top-k, weights and hit
+//                              counts, one warp per token, any n_group <= 8;
+//   route_select_sorted_kernel the same selection specialised for 4 of 8 groups;
+//   route_finalize_kernel      balance loss from the per-chunk score sums,
+//                              several blocks, the last one to finish combines;
+//   expert_feedback_kernel     expert-bias update and running hit totals.
+// Router logits may arrive as several K parts (a split-K router GEMM); the
+// selection kernels add the parts in part order before the sigmoid.
+//
 // Ties go to the lower index at both levels; the k experts come out in order of
 // (biased score desc, index asc).  Everything is deterministic: per-block
 // histograms and score sums are reduced in a fixed order, never with float
