@@ -36,9 +36,13 @@ EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router
            "moe_route_from_logits", "moe_forward", "moe_get_status", "moe_last_launch_count",
            "moe_profile_enable", "moe_profile_read", "moe_kernel_name", "moe_strerror", "moe_route_static",
            "moe_debug_inject_timeout", "moe_rmsnorm", "moe_expert_feedback", "moe_prepare_router",
-           "moe_route_prepared", "moe_dense_workspace_bytes", "moe_dense_ffn", "moe_backward")
+           "moe_route_prepared", "moe_dense_workspace_bytes", "moe_dense_ffn", "moe_backward",
+           "moe_layer_workspace_bytes", "moe_layer")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
-MOE_KERNEL_COUNT = 16
+MOE_LAYER_FUSE_ALWAYS = 1
+MOE_LAYER_FUSE_NEVER = 2
+MOE_FUSED_MIN_T = 19456
+MOE_KERNEL_COUNT = 18
 
 
 class MoeCfg(ctypes.Structure):
@@ -93,6 +97,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.moe_route_from_logits.argtypes = [C, P, P, P, P, P, P, P, P, S, P]
         lib.moe_forward.argtypes = [C, P, P, P, P, P, P, P, P, P, P, S, P]
         lib.moe_backward.argtypes = [C] + [P] * 14 + [P, S, P]
+        lib.moe_layer_workspace_bytes.argtypes = [C, ctypes.c_int]
+        lib.moe_layer_workspace_bytes.restype = S
+        lib.moe_layer.argtypes = [C] + [P] * 13 + [ctypes.c_int, P, S, P]
+        lib.moe_layer.restype = ctypes.c_int
         lib.moe_backward.restype = ctypes.c_int
         lib.moe_get_status.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int]
         lib.moe_last_launch_count.argtypes = []

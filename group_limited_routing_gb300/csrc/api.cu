@@ -28,12 +28,13 @@ thread_local int g_last_launches = 0;
 enum KernelId {
     KID_SPLIT = 0, KID_ROUTER_GEMM, KID_SELECT, KID_FINALIZE, KID_HIST, KID_SCAN, KID_SCATTER,
     KID_GEMM_GATE_UP, KID_GEMM_DOWN, KID_COMBINE, KID_DENSE_TILES, KID_BWD_RECOMPUTE, KID_BWD_DGRAD,
-    KID_BWD_DX, KID_BWD_WGRAD, KID_BWD_MISC
+    KID_BWD_DX, KID_BWD_WGRAD, KID_BWD_MISC, KID_ROUTE_FUSED, KID_TILES
 };
 const char *const kKernelNames[MOE_KERNEL_COUNT] = {
     "split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist",
     "bucket_scan", "bucket_scatter", "gemm_gate_up_swiglu", "gemm_down", "combine", "dense_tiles",
-    "bwd_gate_up_recompute", "bwd_dgrad_down_swiglu", "bwd_dgrad_x", "bwd_weight_grads", "bwd_pad_and_dw"};
+    "bwd_gate_up_recompute", "bwd_dgrad_down_swiglu", "bwd_dgrad_x", "bwd_weight_grads", "bwd_pad_and_dw",
+    "router_route_bucket", "bucket_tiles"};
 
 struct ProfRecord {
     cudaEvent_t start, stop;
@@ -170,7 +171,9 @@ struct FwdLayout {
     int nchunk, max_mtiles;
 };
 
-FwdLayout fwd_layout(const moe_cfg &c)
+// xperm_rows: rows of the bucketed activations (0: k T, the compact layout;
+// the fused router's buckets take E T)
+FwdLayout fwd_layout(const moe_cfg &c, size_t xperm_rows = 0)
 {
     FwdLayout L;
     const size_t T = c.T, K = c.k, H = c.H, I = c.I;
@@ -189,7 +192,7 @@ FwdLayout fwd_layout(const moe_cfg &c)
     L.slot_of = off;
     off = align_up(off + T * K * 4, 256);
     L.xperm = off;
-    off = align_up(off + K * T * H * 2, 256);
+    off = align_up(off + (xperm_rows ? xperm_rows : K * T) * H * 2, 256);
     L.aint = off;
     off = align_up(off + (K + 1) * T * I * 2, 256);
     L.y = off;
@@ -408,6 +411,210 @@ int check_ws(void *ws, size_t ws_bytes, size_t need)
         return MOE_ERR_WORKSPACE_TOO_SMALL;
     return MOE_OK;
 }
+
+// ------------------------------------------------------------ moe_layer
+// One workspace for routing and the expert stage: the routing region, then
+// the expert stage's (its X_perm sized for the fused router's buckets when
+// that path is taken), then the fused router's scratch.  One header (status).
+struct LayerLayout {
+    RouteLayout r;
+    FwdLayout f;
+    size_t gscr, lscr, dest, offs, total;
+    bool fused;
+};
+
+// the fused router's shape: 256 experts in 8 groups, at most FUSED_MAX_K per
+// token, every bucket row index e T + slot within int32, a hidden row within
+// one eighth of the ring (less its barriers) of the 256-expert router
+bool fusable(const moe_cfg &c)
+{
+    return c.E == 256 && c.n_group == 8 && c.k <= FUSED_MAX_K && (long long)c.E * c.T < (1ll << 31) &&
+           c.H <= 14336;   // a hidden row fits one copy slot of the router's shared-memory ring
+}
+
+bool layer_fused(const moe_cfg &c, int flags)
+{
+    if (!fusable(c) || (flags & MOE_LAYER_FUSE_NEVER))
+        return false;
+    return (flags & MOE_LAYER_FUSE_ALWAYS) || c.T >= MOE_FUSED_MIN_T;
+}
+
+LayerLayout layer_layout(const moe_cfg &c, int flags)
+{
+    LayerLayout L;
+    L.fused = layer_fused(c, flags);
+    L.r = route_layout(c);
+    L.f = fwd_layout(c, L.fused ? (size_t)c.E * c.T : 0);
+    const size_t b = L.r.total - sizeof(WsHeader);   // the expert stage's region follows the routing region
+    L.f.hist += b;
+    L.f.sizes += b;
+    L.f.mtiles += b;
+    L.f.slot_of += b;
+    L.f.xperm += b;
+    L.f.aint += b;
+    L.f.y += b;
+    L.f.total += b;
+    const size_t tiles = (size_t)(c.T + GEMM_BM - 1) / GEMM_BM;
+    size_t off = L.f.total;
+    L.gscr = off;
+    off = align_up(off + tiles * GEMM_BM * 8 * 4, 256);
+    L.lscr = off;
+    off = align_up(off + tiles * GEMM_BM * 2 * 3 * FUSED_MAX_K * 4, 256);
+    L.dest = off;
+    off = align_up(off + tiles * GEMM_BM * FUSED_MAX_K * 4, 256);
+    L.offs = off;
+    off = align_up(off + (size_t)(c.E + 1) * 4, 256);
+    L.total = off;
+    return L;
+}
+
+// Routing and bucketing in one launch of the fused router, then the m-tile
+// list.  counts is cleared first (the split launch does it when W_split is
+// NULL); the caller checked every argument.
+int fused_route(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split,
+                const float *bias, int32_t *idx, float *w, int32_t *counts, void *ws, const LayerLayout &L, int sms,
+                cudaStream_t s, int &launches)
+{
+    const uint16_t *W3 = reinterpret_cast<const uint16_t *>(W_split);
+    if (!W3) {
+        uint16_t *W3ws = at<uint16_t>(ws, L.r.w3);
+        GLR_LAUNCH(KID_SPLIT, launch_split_router(W, W3ws, c.E, c.H, counts, s));
+        W3 = W3ws;
+    } else if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s) != cudaSuccess) {
+        return MOE_ERR_CUDA;
+    }
+    GemmParams p;
+    memset(&p, 0, sizeof(p));
+    if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
+        !make_map_bf16(&p.tmB0, W3, 3ull * c.E, c.H, GEMM_BK, 256))
+        return MOE_ERR_CUDA;
+    const int tiles = (c.T + GEMM_BM - 1) / GEMM_BM;
+    p.n_tiles = 1;
+    p.ksplit = 1;
+    p.num_tiles_static = tiles;
+    p.kblocks = c.H / GEMM_BK;
+    p.T = c.T;
+    p.E = c.E;
+    p.H = c.H;
+    p.status = &header(ws)->status;
+    p.bias = bias;
+    p.idx_out = idx;
+    p.w_out = w;
+    p.counts = counts;
+    p.slot_local = at<int32_t>(ws, L.f.slot_of);
+    p.dest = at<int32_t>(ws, L.dest);
+    p.gscr = at<float>(ws, L.gscr);
+    p.lscr = at<uint32_t>(ws, L.lscr);
+    p.hidden = hidden;
+    p.xperm = at<uint16_t>(ws, L.f.xperm);
+    p.topk_group = c.topk_group;
+    p.k = c.k;
+    p.rsf = c.rsf;
+    p.eps = c.eps;
+    GLR_LAUNCH(KID_ROUTE_FUSED, launch_gemm(GK_ROUTER_FUSED, p, std::min(sms, tiles), s));
+    WsHeader *hdr = header(ws);
+    GLR_LAUNCH(KID_TILES, launch_bucket_tiles(counts, c.T, c.E, c.k, at<int4>(ws, L.f.mtiles), hdr,
+                                              at<int32_t>(ws, L.offs), s));
+    return MOE_OK;
+}
+
+// The expert stage of the forward: bucketing (unless offs is given: the fused
+// router then bucketed the pairs itself, bucket e at rows e T .. of X_perm,
+// slot_of holding rows inside the buckets and offs the compact offsets), the
+// two grouped GEMMs and the combine.  Arguments are checked by the caller.
+int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
+                 const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const int32_t *topk_idx,
+                 const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *ws, const FwdLayout &L,
+                 const int32_t *offs, int sms, cudaStream_t s, int &launches)
+{
+    WsHeader *hdr = header(ws);
+    int32_t *hist = at<int32_t>(ws, L.hist);
+    int4 *mtiles = at<int4>(ws, L.mtiles);
+    int32_t *slot_of = at<int32_t>(ws, L.slot_of);
+    uint16_t *xperm = at<uint16_t>(ws, L.xperm);
+    uint16_t *aint = at<uint16_t>(ws, L.aint);
+    uint16_t *y = at<uint16_t>(ws, L.y);
+    const uint64_t kT = (uint64_t)c.k * c.T;
+
+    // bucket the (token, expert) pairs by expert (stable), gather rows --
+    // unless the fused router has done it (bucket e at rows e T .., offsets in offs)
+    int32_t *sizes = at<int32_t>(ws, L.sizes);
+    if (!offs && c.T <= BUCKET_SMALL_MAX_T) {
+        // a handful of tokens: the three bucketing steps in one launch
+        const int mt = c.T <= GEMM_SMALL_T ? GEMM_SMALL_T : GEMM_BM;
+        GLR_LAUNCH(KID_SCATTER, launch_bucket_small(topk_idx, hidden, c.T, c.H, c.E, c.k, mt, sizes, slot_of,
+                                                    xperm, mtiles, hdr, s));
+    } else if (!offs) {
+        GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
+        GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
+        GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
+                                                      xperm, mtiles, hdr, s));
+    }
+
+    // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E);
+    // for T <= GEMM_SMALL_T no bucket has more than T rows: the small kinds
+    // load only that many A rows per stage and keep more weights in flight
+    const bool small = c.T <= GEMM_SMALL_T;
+    const int a_rows = small ? GEMM_SMALL_T : GEMM_BM;
+    GemmParams p1;
+    memset(&p1, 0, sizeof(p1));
+    if (!make_map_bf16(&p1.tmA0, xperm, offs ? (uint64_t)c.E * c.T : kT, c.H, GEMM_BK, a_rows) ||
+        !make_map_bf16(&p1.tmA1, hidden, c.T, c.H, GEMM_BK, a_rows) ||
+        !make_map_bf16(&p1.tmB0, W_gate_up, 2ull * c.I * c.E, c.H, GEMM_BK, 128) ||
+        !make_map_bf16(&p1.tmB1, shared_gate_up, 2ull * c.I, c.H, GEMM_BK, 128))
+        return MOE_ERR_CUDA;
+    if (!make_map_bf16(&p1.tmOut, aint, kT + c.T, c.I, 64, 32))
+        return MOE_ERR_CUDA;
+    p1.out = aint;
+    p1.mtiles = mtiles;
+    p1.num_mtiles = &hdr->num_mtiles;
+    p1.n_tiles = c.I / 128;
+    p1.kblocks = c.H / GEMM_BK;
+    p1.T = c.T;
+    p1.E = c.E;
+    p1.I = c.I;
+    p1.H = c.H;
+    p1.kT = (int)kT;
+    p1.ld_out = c.I;
+    p1.status = &hdr->status;
+    p1.cap_rows = offs ? 1 : 0;
+    if (g_inject_timeouts.load() > 0 && g_inject_timeouts.fetch_sub(1) > 0) {
+        p1.inject_withhold = 1;
+        p1.wait_limit_ns = 50000000ull;
+    }
+    GLR_LAUNCH(KID_GEMM_GATE_UP, launch_gemm(small ? GK_GATE_UP_SMALL : GK_GATE_UP, p1,
+                                             std::min(sms, L.max_mtiles * p1.n_tiles), s));
+
+    // grouped down GEMM (W_down stacked [E, I, H]: an MN-major B operand)
+    GemmParams p2;
+    memset(&p2, 0, sizeof(p2));
+    if (!make_map_bf16(&p2.tmA0, aint, kT + c.T, c.I, GEMM_BK, a_rows) ||
+        !make_map_bf16(&p2.tmB0, W_down, (uint64_t)c.I * c.E, c.H, 64, GEMM_BK) ||
+        !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, 64, GEMM_BK))
+        return MOE_ERR_CUDA;
+    if (!make_map_bf16(&p2.tmOut, y, kT + c.T, c.H, 64, 32))
+        return MOE_ERR_CUDA;
+    p2.out = y;
+    p2.mtiles = mtiles;
+    p2.num_mtiles = &hdr->num_mtiles;
+    p2.n_tiles = c.H / 256;
+    p2.kblocks = c.I / GEMM_BK;
+    p2.T = c.T;
+    p2.E = c.E;
+    p2.I = c.I;
+    p2.H = c.H;
+    p2.kT = (int)kT;
+    p2.ld_out = c.H;
+    p2.status = &hdr->status;
+    GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(small ? GK_DOWN_SMALL : GK_DOWN, p2,
+                                          std::min(sms, L.max_mtiles * p2.n_tiles), s));
+
+    // weighted combine + shared expert (+ residual), one rounding to bf16
+    GLR_LAUNCH(KID_COMBINE, launch_combine(y, slot_of, topk_w, residual, c.T, c.H, c.k, out, s, -1, topk_idx, offs,
+                                           c.E));
+    return MOE_OK;
+}
+
 
 }  // namespace
 
@@ -866,93 +1073,70 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
     int sms = 0;
     if ((rc = device_check(&sms)) != MOE_OK)
         return rc;
+    int launches = 0;
+    rc = forward_impl(*cfg, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, residual, out,
+                      ws, L, nullptr, sms, static_cast<cudaStream_t>(stream), launches);
+    g_last_launches = launches;
+    return rc;
+}
+
+size_t moe_layer_workspace_bytes(const moe_cfg *cfg, int flags)
+{
+    if (check_route_cfg(cfg) != MOE_OK || check_forward_cfg(cfg) != MOE_OK)
+        return 0;
+    return layer_layout(*cfg, flags).total;
+}
+
+int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const moe_bf16 *W_split,
+              const float *expert_bias, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
+              const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const moe_bf16 *residual,
+              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, moe_bf16 *out, int flags, void *ws,
+              size_t ws_bytes, void *stream)
+{
+    int rc = check_route_cfg(cfg);
+    if (rc == MOE_OK)
+        rc = check_forward_cfg(cfg);
+    if (rc != MOE_OK)
+        return rc;
+    if (flags & ~(MOE_LAYER_FUSE_ALWAYS | MOE_LAYER_FUSE_NEVER))
+        return MOE_ERR_INVALID_ARG;
+    if (!hidden || !W_router || !W_gate_up || !W_down || !shared_gate_up || !shared_down || !topk_idx || !topk_w ||
+        !expert_counts || !out)
+        return MOE_ERR_INVALID_ARG;
+    const LayerLayout L = layer_layout(*cfg, flags);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(W_router, 4) || !aligned(W_split, 16) || !aligned(expert_bias, 4) ||
+        !aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(shared_gate_up, 16) ||
+        !aligned(shared_down, 16) || !aligned(residual, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) ||
+        !aligned(topk_w, 4) || !aligned(expert_counts, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
     const moe_cfg &c = *cfg;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
-    WsHeader *hdr = header(ws);
-    int32_t *hist = at<int32_t>(ws, L.hist);
-    int4 *mtiles = at<int4>(ws, L.mtiles);
-    int32_t *slot_of = at<int32_t>(ws, L.slot_of);
-    uint16_t *xperm = at<uint16_t>(ws, L.xperm);
-    uint16_t *aint = at<uint16_t>(ws, L.aint);
-    uint16_t *y = at<uint16_t>(ws, L.y);
-    const uint64_t kT = (uint64_t)c.k * c.T;
-
-    // bucket the (token, expert) pairs by expert (stable), gather rows
-    int32_t *sizes = at<int32_t>(ws, L.sizes);
-    if (c.T <= BUCKET_SMALL_MAX_T) {
-        // a handful of tokens: the three bucketing steps in one launch
-        const int mt = c.T <= GEMM_SMALL_T ? GEMM_SMALL_T : GEMM_BM;
-        GLR_LAUNCH(KID_SCATTER, launch_bucket_small(topk_idx, hidden, c.T, c.H, c.E, c.k, mt, sizes, slot_of,
-                                                    xperm, mtiles, hdr, s));
+    if (L.fused) {
+        rc = fused_route(c, hidden, W_router, W_split, expert_bias, topk_idx, topk_w, expert_counts, ws, L, sms, s,
+                         launches);
+        if (rc == MOE_OK)
+            rc = forward_impl(c, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, residual,
+                              out, ws, L.f, at<int32_t>(ws, L.offs), sms, s, launches);
     } else {
-        GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
-        GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
-        GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
-                                                      xperm, mtiles, hdr, s));
+        float *logits = at<float>(ws, L.r.logits);
+        int nparts = 1;
+        rc = router_gemm(c, hidden, W_router, W_split, logits, expert_counts, ws, L.r, sms, s, launches, L.r.ksplit,
+                         nparts);
+        if (rc == MOE_OK)
+            rc = route_select(c, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, nullptr, nullptr, ws,
+                              L.r, s, launches);
+        if (rc == MOE_OK)
+            rc = forward_impl(c, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, residual,
+                              out, ws, L.f, nullptr, sms, s, launches);
     }
-
-    // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E);
-    // for T <= GEMM_SMALL_T no bucket has more than T rows: the small kinds
-    // load only that many A rows per stage and keep more weights in flight
-    const bool small = c.T <= GEMM_SMALL_T;
-    const int a_rows = small ? GEMM_SMALL_T : GEMM_BM;
-    GemmParams p1;
-    memset(&p1, 0, sizeof(p1));
-    if (!make_map_bf16(&p1.tmA0, xperm, kT, c.H, GEMM_BK, a_rows) ||
-        !make_map_bf16(&p1.tmA1, hidden, c.T, c.H, GEMM_BK, a_rows) ||
-        !make_map_bf16(&p1.tmB0, W_gate_up, 2ull * c.I * c.E, c.H, GEMM_BK, 128) ||
-        !make_map_bf16(&p1.tmB1, shared_gate_up, 2ull * c.I, c.H, GEMM_BK, 128))
-        return MOE_ERR_CUDA;
-    if (!make_map_bf16(&p1.tmOut, aint, kT + c.T, c.I, 64, 32))
-        return MOE_ERR_CUDA;
-    p1.out = aint;
-    p1.mtiles = mtiles;
-    p1.num_mtiles = &hdr->num_mtiles;
-    p1.n_tiles = c.I / 128;
-    p1.kblocks = c.H / GEMM_BK;
-    p1.T = c.T;
-    p1.E = c.E;
-    p1.I = c.I;
-    p1.H = c.H;
-    p1.kT = (int)kT;
-    p1.ld_out = c.I;
-    p1.status = &hdr->status;
-    if (g_inject_timeouts.load() > 0 && g_inject_timeouts.fetch_sub(1) > 0) {
-        p1.inject_withhold = 1;
-        p1.wait_limit_ns = 50000000ull;
-    }
-    GLR_LAUNCH(KID_GEMM_GATE_UP, launch_gemm(small ? GK_GATE_UP_SMALL : GK_GATE_UP, p1,
-                                             std::min(sms, L.max_mtiles * p1.n_tiles), s));
-
-    // grouped down GEMM (W_down stacked [E, I, H]: an MN-major B operand)
-    GemmParams p2;
-    memset(&p2, 0, sizeof(p2));
-    if (!make_map_bf16(&p2.tmA0, aint, kT + c.T, c.I, GEMM_BK, a_rows) ||
-        !make_map_bf16(&p2.tmB0, W_down, (uint64_t)c.I * c.E, c.H, 64, GEMM_BK) ||
-        !make_map_bf16(&p2.tmB1, shared_down, (uint64_t)c.I, c.H, 64, GEMM_BK))
-        return MOE_ERR_CUDA;
-    if (!make_map_bf16(&p2.tmOut, y, kT + c.T, c.H, 64, 32))
-        return MOE_ERR_CUDA;
-    p2.out = y;
-    p2.mtiles = mtiles;
-    p2.num_mtiles = &hdr->num_mtiles;
-    p2.n_tiles = c.H / 256;
-    p2.kblocks = c.I / GEMM_BK;
-    p2.T = c.T;
-    p2.E = c.E;
-    p2.I = c.I;
-    p2.H = c.H;
-    p2.kT = (int)kT;
-    p2.ld_out = c.H;
-    p2.status = &hdr->status;
-    GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(small ? GK_DOWN_SMALL : GK_DOWN, p2,
-                                          std::min(sms, L.max_mtiles * p2.n_tiles), s));
-
-    // weighted combine + shared expert (+ residual), one rounding to bf16
-    GLR_LAUNCH(KID_COMBINE, launch_combine(y, slot_of, topk_w, residual, c.T, c.H, c.k, out, s));
     g_last_launches = launches;
-    return MOE_OK;
+    return rc;
 }
 
 int moe_expert_feedback(const moe_cfg *cfg, const int32_t *expert_counts, float gamma, float *expert_bias,

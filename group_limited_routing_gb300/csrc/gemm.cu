@@ -21,13 +21,21 @@
 //               N = 256 MMA (half the shared-memory operand traffic per flop
 //               of the 128-expert tiles), two TMEM K-block slots and eight
 //               epilogue warps (two per TMEM lane quadrant, 128 columns each).
+//   GK_ROUTER_FUSED  GK_ROUTER_WIDE whose epilogue routes and buckets the
+//               tokens itself (section 二 steps 1-3, section 三, section 四's
+//               bucketing): the two threads holding a token's 256 logits pick
+//               its experts, claim the pairs' rows in the experts' buckets
+//               with one integer atomic per expert and tile, and, after the
+//               CTA's last tile, copy the hidden rows into the buckets -- so
+//               the HBM-bound row copies of some CTAs overlap the MMAs of
+//               others instead of following the whole router.
 // The grouped kinds also serve the dense first-layer MLP (one weight group).
 //
 // Every kernel starts with griddepcontrol.wait (programmatic dependent
 // launch): its prologue (barriers, TMEM, descriptor prefetch) overlaps the
 // previous kernel's teardown, and nothing global is read before the wait.
 //
-// Roles (192 threads, 320 for GK_ROUTER_WIDE; one CTA per SM):
+// Roles (192 threads, 320 for the 256-expert routers; one CTA per SM):
 //   warp 0, one lane : TMA producer, fills a STAGES-deep ring of smem stages
 //   warp 1           : allocates TMEM; one lane issues tcgen05.mma and commits
 //   warps 2..5 (..9) : epilogue, TMEM -> registers -> global; warp w reads TMEM
@@ -56,15 +64,17 @@ __host__ __device__ constexpr int base_kind(int kind)
 {
     return (kind == GK_GATE_UP_SMALL || kind == GK_GATE_UP_BWD) ? GK_GATE_UP
            : kind == GK_DOWN_SMALL                              ? GK_DOWN
-           : kind == GK_ROUTER_WIDE                             ? GK_ROUTER
+           : (kind == GK_ROUTER_WIDE || kind == GK_ROUTER_FUSED) ? GK_ROUTER
                                                                 : kind;
 }
+
+__host__ __device__ constexpr bool wide_router(int kind) { return kind == GK_ROUTER_WIDE || kind == GK_ROUTER_FUSED; }
 
 // K blocks of hidden the wide router prefetches into L2 ahead of its loads
 constexpr int ROUTER_PF = 6;
 
 // epilogue warps of a kind (the block is 64 + 32 x this threads)
-__host__ __device__ constexpr int epi_warps(int kind) { return kind == GK_ROUTER_WIDE ? 8 : 4; }
+__host__ __device__ constexpr int epi_warps(int kind) { return wide_router(kind) ? 8 : 4; }
 __host__ __device__ constexpr int kind_threads(int kind) { return 64 + 32 * epi_warps(kind); }
 
 template <>
@@ -97,6 +107,9 @@ struct GemmCfg<GK_ROUTER_WIDE> {
     static constexpr int A_ROWS = GEMM_BM;
     static constexpr int NBUF = 0;
 };
+
+template <>
+struct GemmCfg<GK_ROUTER_FUSED> : GemmCfg<GK_ROUTER_WIDE> {};
 
 template <>
 struct GemmCfg<GK_GATE_UP> {
@@ -201,9 +214,12 @@ struct GemmLayout {
     // round-robin leaves some SMs with far more work than others)
     static constexpr bool DYN = (KIND == GK_WGRAD);
     static constexpr int TQ = DYN ? TQ_RING : 0;
-    // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin, tq_full[TQ], tq_empty[TQ]
-    static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1 + 2 * TQ;
-    static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16 + TQ * 4;
+    // the fused router's epilogue barrier and per-tile bucket histogram
+    static constexpr bool FUSED = (KIND == GK_ROUTER_FUSED);
+    static constexpr int HIST = FUSED ? 256 * 4 : 0;
+    // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin, tq_full[TQ], tq_empty[TQ] (, epi)
+    static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1 + 2 * TQ + (FUSED ? 1 : 0);
+    static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16 + TQ * 4 + HIST;
     static_assert(SMEM <= 232448, "more than 227 KB of shared memory");
     static_assert(C::A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms need 1024-B alignment");
 };
@@ -263,7 +279,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
         ti.shared = (m.x == p.E);
         ti.rows = m.z;
         if (BASE == GK_GATE_UP) {
-            ti.a_row = m.y;                               // X_perm slot, or token for the shared expert
+            ti.a_row = (p.cap_rows && !ti.shared) ? m.w : m.y;   // X_perm row, or token for the shared expert
             ti.out_row = ti.shared ? p.kT + m.y : m.y;
         } else {
             ti.a_row = ti.shared ? p.kT + m.y : m.y;      // intermediate rows
@@ -643,15 +659,321 @@ __device__ __forceinline__ void epilogue_wgrad(const GemmParams &p, const TileIn
     }
 }
 
+// ---------------------------------------------------------------------------
+// GK_ROUTER_FUSED epilogue.  Thread (half, lane) of the warp pair of lane
+// quadrant q holds token row r = 32 q + lane and its logits of experts
+// 128 half .. 128 half + 127, i.e. groups 4 half .. 4 half + 3 (E = 256 in 8
+// groups of 32).  The two threads of a token exchange what the selection needs
+// through per-CTA global scratch (the stages fill shared memory), with an
+// mbarrier over the eight epilogue warps between the steps.  The arithmetic
+// is that of the routing kernels (route.cu): the same score formula, group
+// score, group ranking, winner order (key desc, expert asc) and sequential
+// normaliser, so the results are bit-identical to routing the same logits
+// there.
+struct FusedCtx {
+    uint32_t ebar;    // epilogue barrier: 8 warp arrivals per phase
+    uint32_t phase;   // phases completed so far
+    int *hist;        // smem [256]: the tile's hits per expert, then the bucket bases
+};
+
+// The eight epilogue warps meet; shared-memory writes made before (and,
+// with global_writes, global ones) are visible to every epilogue thread
+// after.  Bounded like every wait of the kernel.
+__device__ __forceinline__ bool epi_sync(FusedCtx &fz, int lane, volatile int *abort_flag, unsigned long long limit,
+                                         bool global_writes = true)
+{
+    if (global_writes)
+        __threadfence();
+    __syncwarp();
+    int ok = 1;
+    if (lane == 0) {
+        mbar_arrive(fz.ebar);
+        ok = mbar_wait(fz.ebar, fz.phase & 1u, abort_flag, limit) ? 1 : 0;
+    }
+    ++fz.phase;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
+__device__ __forceinline__ float bias_of(const float *bias, int e)
+{
+    return bias ? __ldg(bias + e) : 0.0f;
+}
+
+// Routes the tile's tokens (acc: this thread's 128 logits, overwritten with
+// their scores) and claims their bucket rows; `ew` = epilogue thread 0..255.
+__device__ __forceinline__ bool fused_route_tile(const GemmParams &p, const TileInfo &ti, int tile,
+                                                 float (&acc)[128], int quad, int half, int lane, int ew,
+                                                 FusedCtx &fz, volatile int *abort_flag, unsigned long long limit)
+{
+    const int r = quad * 32 + lane;
+    const bool valid = r < ti.rows;
+    const int t = ti.a_row + r;
+    const int e0 = half * 128;
+    const int K = p.k;
+
+    // scores (section 二 step 1), in place; non-finite logits or biases are reported
+    bool bad = false;
+#pragma unroll
+    for (int c = 0; c < 128; ++c) {
+        const float b = bias_of(p.bias, e0 + c);
+        bad |= !isfinite(acc[c]) || !isfinite(b);
+        acc[c] = router_sigmoid(acc[c]);
+    }
+    if (bad && valid)
+        atomicOr(p.status, ST_NONFINITE);
+
+    // this half's four group scores: the two best biased scores (section 三:
+    // the bias takes part in choosing), a repeated best counting twice
+    float gs[4];
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+        uint32_t m1 = 0u, m2 = 0u;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t u = fkey(acc[gi * 32 + i] + bias_of(p.bias, e0 + gi * 32 + i));
+            m2 = max(m2, min(m1, u));
+            m1 = max(m1, u);
+        }
+        gs[gi] = fkey_value(m1) + fkey_value(m2);
+    }
+    float *gsc = p.gscr + ((size_t)blockIdx.x * GEMM_BM + r) * 8;
+    *reinterpret_cast<float4 *>(gsc + half * 4) = make_float4(gs[0], gs[1], gs[2], gs[3]);
+    if (!epi_sync(fz, lane, abort_flag, limit))
+        return false;
+    // the previous tile's bucket bases have all been read: clear the histogram
+    fz.hist[ew] = 0;
+
+    // keep the topk_group best groups (section 二 step 2), ties to the lower group
+    const float4 go = __ldcg(reinterpret_cast<const float4 *>(gsc + (1 - half) * 4));
+    float g[8];
+    g[4 * half + 0] = gs[0];
+    g[4 * half + 1] = gs[1];
+    g[4 * half + 2] = gs[2];
+    g[4 * half + 3] = gs[3];
+    g[4 * (1 - half) + 0] = go.x;
+    g[4 * (1 - half) + 1] = go.y;
+    g[4 * (1 - half) + 2] = go.z;
+    g[4 * (1 - half) + 3] = go.w;
+    uint32_t keep = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        int rank = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            rank += (g[i] > g[j] || (g[i] == g[j] && i < j)) ? 1 : 0;
+        if (rank < p.topk_group)
+            keep |= 1u << j;
+    }
+
+    // this half's best FUSED_MAX_K experts of the kept groups, sorted by
+    // (key desc, expert asc): candidates arrive in expert order, so one with
+    // a key equal to a listed one stays behind it
+    uint32_t lk[FUSED_MAX_K];
+    int le[FUSED_MAX_K];
+    float ls[FUSED_MAX_K];
+#pragma unroll
+    for (int i = 0; i < FUSED_MAX_K; ++i) {
+        lk[i] = 0u;
+        le[i] = e0;
+        ls[i] = 0.0f;
+    }
+#pragma unroll
+    for (int c = 0; c < 128; ++c) {
+        if (!((keep >> (4 * half + c / 32)) & 1u))
+            continue;
+        const uint32_t u = fkey(acc[c] + bias_of(p.bias, e0 + c));
+        if (u <= lk[FUSED_MAX_K - 1])
+            continue;
+#pragma unroll
+        for (int i = FUSED_MAX_K - 1; i > 0; --i) {
+            const bool up = u > lk[i - 1];       // the candidate ranks above entry i-1: it moves down
+            const bool here = u > lk[i];
+            lk[i] = up ? lk[i - 1] : (here ? u : lk[i]);
+            le[i] = up ? le[i - 1] : (here ? e0 + c : le[i]);
+            ls[i] = up ? ls[i - 1] : (here ? acc[c] : ls[i]);
+        }
+        if (u > lk[0]) {
+            lk[0] = u;
+            le[0] = e0 + c;
+            ls[0] = acc[c];
+        }
+    }
+    uint32_t *lsc = p.lscr + (((size_t)blockIdx.x * GEMM_BM + r) * 2 + half) * (3 * FUSED_MAX_K);
+#pragma unroll
+    for (int i = 0; i < FUSED_MAX_K; i += 4) {
+        *reinterpret_cast<uint4 *>(lsc + i) = make_uint4(lk[i], lk[i + 1], lk[i + 2], lk[i + 3]);
+        *reinterpret_cast<uint4 *>(lsc + FUSED_MAX_K + i) =
+            make_uint4((uint32_t)le[i], (uint32_t)le[i + 1], (uint32_t)le[i + 2], (uint32_t)le[i + 3]);
+        *reinterpret_cast<uint4 *>(lsc + 2 * FUSED_MAX_K + i) =
+            make_uint4(__float_as_uint(ls[i]), __float_as_uint(ls[i + 1]), __float_as_uint(ls[i + 2]),
+                       __float_as_uint(ls[i + 3]));
+    }
+    if (!epi_sync(fz, lane, abort_flag, limit))
+        return false;
+
+    // the lower half's thread merges the two lists: the token's k experts in
+    // output order, their weights (section 二 step 3: sequential sum of the
+    // chosen unbiased scores, + eps, times routed_scaling_factor) and each
+    // pair's rank among the tile's hits of its expert
+    int oe[FUSED_MAX_K], orank[FUSED_MAX_K];
+    if (half == 0) {
+        const uint32_t *osc = lsc + 3 * FUSED_MAX_K;   // the upper half's list
+        uint32_t pk[FUSED_MAX_K];
+        int pe[FUSED_MAX_K];
+        float ps[FUSED_MAX_K];
+#pragma unroll
+        for (int i = 0; i < FUSED_MAX_K; i += 4) {
+            const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(osc + i));
+            const uint4 b = __ldcg(reinterpret_cast<const uint4 *>(osc + FUSED_MAX_K + i));
+            const uint4 c = __ldcg(reinterpret_cast<const uint4 *>(osc + 2 * FUSED_MAX_K + i));
+            pk[i] = a.x; pk[i + 1] = a.y; pk[i + 2] = a.z; pk[i + 3] = a.w;
+            pe[i] = (int)b.x; pe[i + 1] = (int)b.y; pe[i + 2] = (int)b.z; pe[i + 3] = (int)b.w;
+            ps[i] = __uint_as_float(c.x); ps[i + 1] = __uint_as_float(c.y);
+            ps[i + 2] = __uint_as_float(c.z); ps[i + 3] = __uint_as_float(c.w);
+        }
+        float os[FUSED_MAX_K];
+        float den = 0.0f;
+#pragma unroll
+        for (int j = 0; j < FUSED_MAX_K; ++j) {
+            const bool a = lk[0] >= pk[0];          // equal keys: the lower half's expert has the lower id
+            oe[j] = a ? le[0] : pe[0];
+            os[j] = a ? ls[0] : ps[0];
+#pragma unroll
+            for (int i = 0; i < FUSED_MAX_K - 1; ++i) {
+                lk[i] = a ? lk[i + 1] : lk[i];
+                le[i] = a ? le[i + 1] : le[i];
+                ls[i] = a ? ls[i + 1] : ls[i];
+                pk[i] = a ? pk[i] : pk[i + 1];
+                pe[i] = a ? pe[i] : pe[i + 1];
+                ps[i] = a ? ps[i] : ps[i + 1];
+            }
+            lk[FUSED_MAX_K - 1] = a ? 0u : lk[FUSED_MAX_K - 1];
+            pk[FUSED_MAX_K - 1] = a ? pk[FUSED_MAX_K - 1] : 0u;
+            if (j < K)
+                den += os[j];                       // in output order
+        }
+        den += p.eps;
+#pragma unroll
+        for (int j = 0; j < FUSED_MAX_K; ++j) {
+            orank[j] = 0;
+            if (j < K && valid) {
+                p.idx_out[(size_t)t * K + j] = oe[j];
+                p.w_out[(size_t)t * K + j] = (os[j] / den) * p.rsf;
+                orank[j] = atomicAdd(&fz.hist[oe[j]], 1);
+            }
+        }
+    }
+    if (!epi_sync(fz, lane, abort_flag, limit, false))
+        return false;
+
+    // one atomic per expert hit in this tile reserves its rows in the bucket;
+    // the counters end as the experts' hit counts (section 六)
+    {
+        const int h = fz.hist[ew];
+        if (h > 0)
+            fz.hist[ew] = atomicAdd(p.counts + ew, h);
+    }
+    if (!epi_sync(fz, lane, abort_flag, limit, false))
+        return false;
+    if (half == 0 && valid) {
+#pragma unroll
+        for (int j = 0; j < FUSED_MAX_K; ++j) {
+            if (j < K) {
+                const int slot = fz.hist[oe[j]] + orank[j];
+                const bool ok = slot < p.T;       // at most T pairs per expert: one per token
+                p.slot_local[(size_t)t * K + j] = ok ? slot : -1;
+                p.dest[((size_t)tile * GEMM_BM + r) * FUSED_MAX_K + j] = ok ? oe[j] * p.T + slot : -1;
+                if (!ok)
+                    atomicOr(p.status, ST_COUNT_MISMATCH);
+            }
+        }
+    }
+    return true;
+}
+
+// After the CTA's last tile (every MMA done, the stage ring idle): copies the
+// hidden row of every routed pair of the CTA's tiles into the pair's bucket
+// rows with bulk copies through the ring's shared memory.  Warp w (0..7)
+// takes rows w, w + 8, ... of each tile; its lane 0 loads up to FUSED_SLOTS
+// rows into its slice of the ring, then stores each to its k bucket rows,
+// and waits until those stores have read the slice before the next batch.
+constexpr int FUSED_SLOTS = 8;
+constexpr int FUSED_RING_BARS = 8 * FUSED_SLOTS * 8;   // barrier bytes at the ring's end
+__device__ __forceinline__ void fused_copy_rows(const GemmParams &p, int num_tiles, int w, int lane, uint32_t ring,
+                                                uint32_t ring_bytes, volatile int *abort_flag,
+                                                unsigned long long limit)
+{
+    if (lane != 0)
+        return;
+    const uint32_t rowbytes = (uint32_t)p.H * 2;
+    const uint32_t slice = (ring_bytes - FUSED_RING_BARS) / 8 / rowbytes * rowbytes;
+    const int ns = min((int)(slice / rowbytes), FUSED_SLOTS);   // >= 1: the host keeps 2 H <= the slice
+    const uint32_t my = ring + (uint32_t)w * slice;
+    const uint32_t bar0 = ring + ring_bytes - FUSED_RING_BARS + (uint32_t)w * FUSED_SLOTS * 8;
+    fence_proxy_async_smem();                 // the ring was last written by TMA loads
+    for (int b = 0; b < ns; ++b)
+        mbar_init(bar0 + 8u * b, 1);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+    uint32_t parity = 0;                      // bit b: parity of slot b's next completion
+    const int K = p.k;
+    int tile = blockIdx.x, r = w;
+    int dest_row[FUSED_SLOTS];
+    bool ok = true;
+    while (ok) {
+        int nb = 0;
+        while (nb < ns && tile < num_tiles) {
+            const int rows = min(GEMM_BM, p.T - tile * GEMM_BM);
+            if (r >= rows) {
+                tile += gridDim.x;
+                r = w;
+                continue;
+            }
+            const int t = tile * GEMM_BM + r;
+            dest_row[nb] = tile * GEMM_BM + r;    // its row of the destination table
+            const uint32_t bar = bar0 + 8u * nb;
+            mbar_arrive_expect_tx(bar, rowbytes);
+            bulk_load_g2s(my + (uint32_t)nb * rowbytes, p.hidden + (size_t)t * p.H, rowbytes, bar);
+            ++nb;
+            r += 8;
+        }
+        if (nb == 0)
+            break;
+        for (int b = 0; b < nb; ++b) {
+            const uint32_t bar = bar0 + 8u * b;
+            if (ok && !mbar_wait(bar, (parity >> b) & 1u, abort_flag, limit))
+                ok = false;
+            if (!ok) {
+                mbar_drain(bar, (parity >> b) & 1u);   // its load may still land: let it, then stop
+                continue;
+            }
+            parity ^= 1u << b;
+            const int *dr = p.dest + (size_t)dest_row[b] * FUSED_MAX_K;
+            for (int j = 0; j < K; ++j) {
+                const int d = __ldcg(dr + j);
+                if (d >= 0)
+                    bulk_store_s2g(p.xperm + (size_t)d * p.H, my + (uint32_t)b * rowbytes, rowbytes);
+            }
+        }
+        bulk_commit_group();
+        bulk_wait_group_read<0>();            // the slice may be refilled
+    }
+    bulk_wait_group_all();
+}
+
 // Router epilogue warp: adds the K-block partial sums of its 32 rows in fp32
 // (K-block order, round-to-nearest), then writes the 128 logits of each row
 // that it owns (columns half * 128 .. of the tile; half = 0 for the 128-expert
 // tiles, 0 or 1 for the wide kind's two warps per lane quadrant).
+// The fused kind hands the sums to fused_route_tile instead of writing them.
 template <int KIND>
 __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem,
                                                      int quad, int half, int lane, uint32_t tfull0,
                                                      uint32_t tempty0, uint32_t &kctr, volatile int *abort_flag,
-                                                     uint8_t *stage, unsigned long long limit)
+                                                     uint8_t *stage, unsigned long long limit, FusedCtx &fz,
+                                                     int tile, int ew)
 {
     using C = GemmCfg<KIND>;
     constexpr int COLS = 128;
@@ -692,6 +1014,8 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
                 acc[c + i] += __uint_as_float(r[i]);
         }
     }
+    if constexpr (KIND == GK_ROUTER_FUSED)
+        return fused_route_tile(p, ti, tile, acc, quad, half, lane, ew, fz, abort_flag, limit);
     const int valid_rows = ti.rows - quad * 32;
     if (valid_rows > 0) {
         const size_t ld_bytes = (size_t)p.ld_out * 4;
@@ -746,6 +1070,10 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
     const uint32_t fin_bar = tempty0 + 8u * C::SLOTS;
     const uint32_t tqfull0 = fin_bar + 8u;
     const uint32_t tqempty0 = tqfull0 + 8u * L::TQ;
+    FusedCtx fz;
+    fz.ebar = tqempty0 + 8u * L::TQ;             // (fused router only)
+    fz.phase = 0;
+    fz.hist = const_cast<int *>(tq + L::TQ);      // (fused router only) L::HIST bytes
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -764,6 +1092,8 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
             mbar_init(tqfull0 + 8u * i, 1);
             mbar_init(tqempty0 + 8u * i, TQ_TAKERS);
         }
+        if constexpr (L::FUSED)
+            mbar_init(fz.ebar, epi_warps(KIND));
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&p.tmA0);
@@ -836,7 +1166,7 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
                     const uint32_t sA = base + stage * L::STAGE_BYTES;
                     mbar_arrive_expect_tx(full_bar(stage), L::STAGE_BYTES);
                     issue_loads<KIND>(p, ti, kb, sA, sA + C::A_BYTES, full_bar(stage));
-                    if constexpr (KIND == GK_ROUTER_WIDE) {
+                    if constexpr (wide_router(KIND)) {
                         // two stages cannot hide a DRAM read of the hidden rows:
                         // pull the A box ROUTER_PF K blocks ahead (in this CTA's
                         // tile order) into L2
@@ -920,6 +1250,9 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
         uint8_t *stage = staging + (warp - 2) * (C::NBUF * 4096);
         int buf = 0;
         uint32_t ctr = 0;
+        bool fused_ok = true;
+        if constexpr (L::FUSED)
+            fz.hist[(warp - 2) * 32 + lane] = 0;
         for (int n = 0;; ++n) {
             int tile = 0;
             if (lane == 0)
@@ -930,8 +1263,10 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
             const TileInfo ti = tile_info<KIND>(p, tile);
             if constexpr (ROUTER) {
                 if (!router_epilogue_tile<KIND>(p, ti, tmem, quad, (warp - 2) >> 2, lane, tfull0, tempty0, ctr,
-                                                abort_flag, stage, limit))
+                                                abort_flag, stage, limit, fz, tile, (warp - 2) * 32 + lane)) {
+                    fused_ok = false;
                     break;
+                }
             } else {
                 const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
                 int ok = 1;
@@ -960,6 +1295,11 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
         }
         if (!ROUTER && lane == 0)
             bulk_wait_group_all();              // this warp's output stores have completed
+        if constexpr (L::FUSED) {
+            // every tile's bucket rows are claimed: copy the hidden rows
+            if (fused_ok && epi_sync(fz, lane, abort_flag, limit))
+                fused_copy_rows(p, num_tiles, warp - 2, lane, base, C::STAGES * L::STAGE_BYTES, abort_flag, limit);
+        }
     }
 
     __syncwarp();
@@ -978,6 +1318,7 @@ int gemm_smem_bytes(int kind)
     switch (kind) {
     case GK_ROUTER: return GemmLayout<GK_ROUTER>::SMEM;
     case GK_ROUTER_WIDE: return GemmLayout<GK_ROUTER_WIDE>::SMEM;
+    case GK_ROUTER_FUSED: return GemmLayout<GK_ROUTER_FUSED>::SMEM;
     case GK_GATE_UP: return GemmLayout<GK_GATE_UP>::SMEM;
     case GK_GATE_UP_SMALL: return GemmLayout<GK_GATE_UP_SMALL>::SMEM;
     case GK_DOWN_SMALL: return GemmLayout<GK_DOWN_SMALL>::SMEM;
@@ -992,7 +1333,7 @@ int gemm_tmem_cols(int kind)
 {
     switch (kind) {
     case GK_ROUTER: return GemmCfg<GK_ROUTER>::TMEM_COLS;
-    case GK_ROUTER_WIDE: return GemmCfg<GK_ROUTER_WIDE>::TMEM_COLS;
+    case GK_ROUTER_WIDE: case GK_ROUTER_FUSED: return GemmCfg<GK_ROUTER_WIDE>::TMEM_COLS;
     case GK_GATE_UP: case GK_GATE_UP_SMALL: return GemmCfg<GK_GATE_UP>::TMEM_COLS;
     default: return GemmCfg<GK_DOWN>::TMEM_COLS;
     }
@@ -1023,6 +1364,7 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
     switch (kind) {
     case GK_ROUTER: return launch_kind<GK_ROUTER>(p, grid, s);
     case GK_ROUTER_WIDE: return launch_kind<GK_ROUTER_WIDE>(p, grid, s);
+    case GK_ROUTER_FUSED: return launch_kind<GK_ROUTER_FUSED>(p, grid, s);
     case GK_GATE_UP: return launch_kind<GK_GATE_UP>(p, grid, s);
     case GK_GATE_UP_SMALL: return launch_kind<GK_GATE_UP_SMALL>(p, grid, s);
     case GK_DOWN_SMALL: return launch_kind<GK_DOWN_SMALL>(p, grid, s);

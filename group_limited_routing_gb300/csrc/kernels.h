@@ -42,6 +42,29 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// ---- routing arithmetic shared by every kernel that selects experts ---------
+// Sigmoid score of a router logit (routing page, section 二 step 1), with an
+// IEEE-rounded reciprocal, so every selecting kernel gets the same bits.
+__device__ __forceinline__ float router_sigmoid(float L)
+{
+    return __frcp_rn(1.0f + expf(-L));
+}
+
+// Order-preserving map of fp32 onto uint32 (for non-NaN values): a > b as
+// floats exactly when key(a) > key(b), so a float maximum is an integer one.
+// +0 and -0 get neighbouring keys; the scores compared (sigmoid + bias, and
+// sums of two of them) are never -0.
+__device__ __forceinline__ uint32_t fkey(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float fkey_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // ---- sizes shared by the host layer and the kernels -------------------------
 constexpr int ROUTE_CHUNK = 32;    // tokens per block of the routing kernel (4 per warp) ...
 constexpr int ROUTE_CHUNK_SMALL = 8;  // ... and for T <= ROUTE_SMALL_T (1 per warp, 4x the blocks)
@@ -75,10 +98,14 @@ struct WsHeader {
 // dOut_perm . W_down^T with the SwiGLU backward in its epilogue; GK_WGRAD is
 // a per-expert weight gradient (M = features, N = hidden, K = the expert's
 // bucket rows, both operands MN-major).
+// GK_ROUTER_FUSED is the 256-expert router whose epilogue also selects the
+// experts, claims every pair's row in its expert's bucket and copies the
+// hidden rows there (routing and bucketing in one launch).
 enum GemmKind {
     GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4,
-    GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7, GK_ROUTER_WIDE = 8
+    GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7, GK_ROUTER_WIDE = 8, GK_ROUTER_FUSED = 9
 };
+constexpr int FUSED_MAX_K = 8;      // experts per token the fused router selects at most
 constexpr int GEMM_SMALL_T = 16;
 constexpr int BWD_ROW_ALIGN = 64;   // backward buckets start on 64-row boundaries (K blocks of the weight gradients)
 
@@ -117,6 +144,22 @@ struct GemmParams {
     int inject_withhold;
     int *tile_ctr;        // GK_WGRAD: tiles claimed so far (zero at launch)
     unsigned long long wait_limit_ns;
+    // GK_ROUTER_FUSED (E = 256 in 8 groups, one token tile per tile, no K split)
+    const float *bias;        // expert_bias [E], or NULL
+    int32_t *idx_out;         // topk_idx [T, k]
+    float *w_out;             // topk_w [T, k]
+    int32_t *counts;          // expert_counts [E], zero at launch; also the buckets' fill levels
+    int32_t *slot_local;      // [T, k] row of each pair inside its expert's bucket
+    int32_t *dest;            // [token tiles, 128, 8] X_perm row of each pair (scratch)
+    float *gscr;              // [grid, 128, 8] group scores of both halves (scratch)
+    uint32_t *lscr;           // [grid, 128, 2, 24] each half's best k (scratch)
+    const uint16_t *hidden;   // [T, H], the rows copied into the buckets
+    uint16_t *xperm;          // [E * T, H]: expert e's bucket starts at row e * T
+    int topk_group, k;
+    float rsf, eps;
+    // grouped gate/up: routed m-tiles read their A rows from the tile list's
+    // fourth field (the bucket layout above) instead of the second
+    int cap_rows;
 };
 
 // Smem bytes a GEMM kind needs (stages + alignment slack + barriers).
@@ -169,9 +212,19 @@ cudaError_t launch_bucket_small(const int32_t *idx, const uint16_t *x, int T, in
 cudaError_t launch_dense_tiles(int T, int mt, int4 *mtiles, WsHeader *hdr, cudaStream_t s);
 
 // out[t] = bf16( sum_j w[t,j] Y[slot_of[t,j]] + Y[shared_row0 + t] (+ residual[t]) );
-// w == NULL means every weight is 1; shared_row0 < 0 means k*T.
+// w == NULL means every weight is 1; shared_row0 < 0 means k*T.  With `offs`,
+// slot_of holds rows inside each expert's bucket and the Y row of pair (t, j)
+// is offs[idx[t,j]] + slot_of[t,j] (a pair whose expert is not in [0, E) is
+// skipped).
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
-                           int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0 = -1);
+                           int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0 = -1,
+                           const int32_t *idx = nullptr, const int32_t *offs = nullptr, int E = 0);
+
+// After the fused router: bucket offsets (exclusive scan of the E bucket
+// sizes) into offs[E + 1] and the m-tile list of the grouped GEMMs, whose
+// routed m-tiles read their A rows at e * T + r (the fused router's buckets).
+cudaError_t launch_bucket_tiles(const int32_t *sizes, int T, int E, int k, int4 *mtiles, WsHeader *hdr,
+                                int32_t *offs, cudaStream_t s);
 
 // backward bucketing: as launch_bucket_scatter, buckets on BWD_ROW_ALIGN rows,
 // plus dOut rows and routing weights per bucket row and the bucket table eoff

@@ -13,6 +13,8 @@
 //                  stable slot of every (token, j) pair -- slots in a bucket in
 //                  ascending (token, j) order -- and the gather of hidden rows
 //                  into the bucketed activation matrix X_perm
+//   bucket_tiles   after the fused router (which bucketed the pairs itself):
+//                  bucket offsets and the m-tile list only
 //   combine        out[t] = bf16( sum_j w[t,j] * Y[slot(t,j)] + Y_shared[t]
 //                  (+ residual[t]) ) in fp32 (section 五: the shared expert is
 //                  added directly)
@@ -128,11 +130,14 @@ cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes,
 // that every pair was bucketed.  With `write_tiles`, the block writes the
 // m-tile list of the grouped GEMMs (the shared expert is group E, all T
 // tokens) and, when eoff is given, every bucket's (first row, padded rows),
-// the shared expert's rows starting at shared_base.
+// the shared expert's rows starting at shared_base.  With cap > 0 the routed
+// rows were bucketed at e * cap + r (the fused router's layout): the fourth
+// field of every m-tile is then its first A row (the token for the shared
+// expert's m-tiles).
 __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, int K, int *offset, int *tstart,
                                int *wsum_rows, int *wsum_tiles, bool write_tiles, int4 *__restrict__ mtiles,
                                WsHeader *__restrict__ hdr, int pad = 1, int2 *__restrict__ eoff = nullptr,
-                               int shared_base = 0)
+                               int shared_base = 0, int cap = 0)
 {
     __shared__ int true_rows;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -190,10 +195,10 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
             eoff[e] = make_int2(offset[e], n);
         if (e < E)
             for (int i = 0, r = 0; r < n0; ++i, r += GEMM_BM)
-                mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n0 - r), 0);
+                mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n0 - r), cap > 0 ? e * cap + r : 0);
         const int ntile_sh = (T + GEMM_BM - 1) / GEMM_BM;
         for (int i = threadIdx.x; i < ntile_sh; i += blockDim.x)
-            mtiles[tstart[E] + i] = make_int4(E, i * GEMM_BM, min(GEMM_BM, T - i * GEMM_BM), 0);
+            mtiles[tstart[E] + i] = make_int4(E, i * GEMM_BM, min(GEMM_BM, T - i * GEMM_BM), cap > 0 ? i * GEMM_BM : 0);
     }
 }
 
@@ -403,6 +408,33 @@ cudaError_t launch_dw_reduce(const int32_t *slot_of, const float *dw_part, int n
 {
     const cudaError_t le = launch_pdl(dw_reduce_kernel, dim3((n + 255) / 256), dim3(256), 0, s, slot_of, dw_part, n,
                                       ntiles, dw);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
+// After the fused router (which bucketed every pair at e * T + its slot and
+// counted the buckets' sizes): the bucket offsets of the compact layout the
+// grouped GEMMs write (offs[e], offs[E] = k T) and the m-tile list, one block.
+__global__ void __launch_bounds__(256) bucket_tiles_kernel(const int32_t *__restrict__ sizes, int T, int E, int K,
+                                                           int4 *__restrict__ mtiles, WsHeader *__restrict__ hdr,
+                                                           int32_t *__restrict__ offs)
+{
+    pdl_wait();
+    __shared__ int offset[257], tstart[257], wr[8], wt[8];
+    bucket_offsets(sizes, T, E, K, offset, tstart, wr, wt, true, mtiles, hdr, 1, nullptr, 0, T);
+    for (int e = threadIdx.x; e <= E; e += blockDim.x)
+        offs[e] = offset[e];
+}
+
+cudaError_t launch_bucket_tiles(const int32_t *sizes, int T, int E, int k, int4 *mtiles, WsHeader *hdr,
+                                int32_t *offs, cudaStream_t s)
+{
+    if (E > 256)
+        return cudaErrorInvalidValue;
+    const cudaError_t le = launch_pdl(bucket_tiles_kernel, dim3(1), dim3(256), 0, s, sizes, T, E, k, mtiles, hdr,
+                                      offs);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
@@ -688,7 +720,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                                                       const int32_t *__restrict__ slot_of,
                                                       const float *__restrict__ w,
                                                       const uint16_t *__restrict__ residual, int T, int H, int K,
-                                                      int ctok, long long shared_row0, uint16_t *__restrict__ out)
+                                                      int ctok, long long shared_row0, uint16_t *__restrict__ out,
+                                                      const int32_t *__restrict__ idx,
+                                                      const int32_t *__restrict__ offs, int E)
 {
     pdl_wait();
     __shared__ int s_slot[COMBINE_TOK * 32];
@@ -702,7 +736,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
         const int nt = min(ctok, T - t0);
         __syncthreads();
         for (int i = threadIdx.x; i < nt * K; i += blockDim.x) {
-            s_slot[i] = slot_of[(size_t)t0 * K + i];
+            int slot = slot_of[(size_t)t0 * K + i];
+            if (offs && slot >= 0) {
+                const int e = idx[(size_t)t0 * K + i];      // bucket row -> row of the compact layout
+                slot = (e >= 0 && e < E) ? slot + offs[e] : -1;
+            }
+            s_slot[i] = slot;
             s_w[i] = w ? w[(size_t)t0 * K + i] : 1.0f;
         }
         __syncthreads();
@@ -721,7 +760,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
 }
 
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
-                           int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0)
+                           int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0,
+                           const int32_t *idx, const int32_t *offs, int E)
 {
     if (shared_row0 < 0)
         shared_row0 = (long long)k * T;
@@ -738,7 +778,7 @@ cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const floa
     const int nchunks = (T + ctok - 1) / ctok;
     const int blocks = min(nchunks, sms * 8);
     const cudaError_t le = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, Y, slot_of, w, residual, T, H, k,
-                                      ctok, shared_row0, out);
+                                      ctok, shared_row0, out, idx, offs, offs ? E : 0);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

@@ -182,22 +182,6 @@ __device__ __forceinline__ float load_logit(const float *__restrict__ logits, si
     return L;
 }
 
-// ---------------------------------------------------------------------------
-// Order-preserving map of fp32 onto uint32 (for non-NaN values): a > b as
-// floats exactly when key(a) > key(b), so warp-wide float max is one
-// __reduce_max_sync.  +0 and -0 get neighbouring keys; the scores compared
-// here (sigmoid + bias, and sums of two of them) are never -0.
-__device__ __forceinline__ uint32_t fkey(float f)
-{
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float fkey_value(uint32_t k)
-{
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // One warp per token.  Lane l holds experts 32*j + l for j < n_group, so each
 // group lives in one register index across the 32 lanes, and every load of a
 // logits row is a run of 128-byte coalesced accesses.  Group maxima and the
@@ -245,7 +229,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(
         for (int j = 0; j < G; ++j) {
             const float L = load_logit(logits, (size_t)t * E + 32 * j + lane, nparts, part_stride);
             nonfinite |= !isfinite(L) || !isfinite(bias_r[j]);
-            s[j] = __frcp_rn(1.0f + expf(-L));        // section 二 step 1 (IEEE-rounded 1/x)
+            s[j] = router_sigmoid(L);                 // section 二 step 1
             b[j] = s[j] + bias_r[j];                  // section 三: choose on s + bias
         }
 
@@ -419,7 +403,7 @@ __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
 #pragma unroll
         for (int j = 0; j < G; ++j) {
             nonfinite |= !(fabsf(L[j]) <= 3.402823466e38f);   // NaN or +-inf
-            s[j] = __frcp_rn(1.0f + expf(-L[j]));              // section 二 step 1
+            s[j] = router_sigmoid(L[j]);                        // section 二 step 1
             kk[j] = fkey(s[j] + sh_bias[32 * j + lane]);       // section 三: choose on s + bias
             sh_s[warp][32 * j + lane] = s[j];
             sh_k[warp][32 * j + lane] = kk[j];

@@ -45,19 +45,28 @@ class MoeConfig:
         return dataclasses.replace(self, T=T)
 
 
-def workspace_bytes(cfg: MoeConfig, which: int) -> int:
-    n = _lib.load().moe_workspace_bytes(ctypes.byref(cfg.c()), which)
+# workspace kind of moe_layer (a tag of this module; its size also depends on flags)
+WS_LAYER = 3
+
+
+def workspace_bytes(cfg: MoeConfig, which: int, flags: int = 0) -> int:
+    if which == WS_LAYER:
+        n = _lib.load().moe_layer_workspace_bytes(ctypes.byref(cfg.c()), flags)
+    else:
+        n = _lib.load().moe_workspace_bytes(ctypes.byref(cfg.c()), which)
     if n == 0:
         raise ValueError("configuration not supported: %r" % (cfg,))
     return int(n)
 
 
 class Workspace:
-    """A device workspace for moe_route (ROUTE) or moe_forward (FORWARD)."""
+    """A device workspace for moe_route (ROUTE), moe_forward (FORWARD),
+    moe_backward (BACKWARD) or moe_layer (WS_LAYER, sized for `flags`)."""
 
-    def __init__(self, cfg: MoeConfig, which: int, device=None):
+    def __init__(self, cfg: MoeConfig, which: int, device=None, flags: int = 0):
         self.which = which
-        self.nbytes = workspace_bytes(cfg, which)
+        self.flags = flags
+        self.nbytes = workspace_bytes(cfg, which, flags)
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
         assert self.buf.data_ptr() % 256 == 0
         _lib.check(_lib.load().moe_workspace_init(self.ptr, self.nbytes, _stream(self.buf.device)),
@@ -67,8 +76,8 @@ class Workspace:
     def ptr(self) -> int:
         return self.buf.data_ptr()
 
-    def fits(self, cfg: MoeConfig) -> bool:
-        return workspace_bytes(cfg, self.which) <= self.nbytes
+    def fits(self, cfg: MoeConfig, flags: Optional[int] = None) -> bool:
+        return workspace_bytes(cfg, self.which, self.flags if flags is None else flags) <= self.nbytes
 
     def status(self, reset: bool = True) -> int:
         v = ctypes.c_int32(0)
@@ -206,6 +215,43 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
     return out
 
 
+def layer(cfg: MoeConfig, hidden, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
+          residual=None, *, W_split=None, flags: int = 0, ws: Optional[Workspace] = None, out=None, routing=None):
+    """moe_layer: routing and the expert stage in one call (the fused router
+    where the shape and T allow, see include/moe.h).  Returns (out, (topk_idx,
+    topk_w, expert_counts)); `routing` (such a triple) is filled instead of
+    allocating."""
+    dev = hidden.device
+    bf = torch.bfloat16
+    ph = _need(hidden, "hidden", bf, (cfg.T, cfg.H), dev)
+    pwr = _need(W_router, "W_router", torch.float32, (cfg.E, cfg.H), dev)
+    psp = _opt(W_split, "W_split", bf, (3, cfg.E, cfg.H), dev)
+    pb = _opt(expert_bias, "expert_bias", torch.float32, (cfg.E,), dev)
+    pgu = _need(W_gate_up, "W_gate_up", bf, (cfg.E, 2 * cfg.I, cfg.H), dev)
+    pd = _need(W_down, "W_down", bf, (cfg.E, cfg.I, cfg.H), dev)
+    psgu = _need(shared_gate_up, "shared_gate_up", bf, (2 * cfg.Is, cfg.H), dev)
+    psd = _need(shared_down, "shared_down", bf, (cfg.Is, cfg.H), dev)
+    pr = _opt(residual, "residual", bf, (cfg.T, cfg.H), dev)
+    if routing is None:
+        routing = (torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev),
+                   torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev),
+                   torch.empty(cfg.E, dtype=torch.int32, device=dev))
+    pi = _need(routing[0], "topk_idx", torch.int32, (cfg.T, cfg.k), dev)
+    pw = _need(routing[1], "topk_w", torch.float32, (cfg.T, cfg.k), dev)
+    pc = _need(routing[2], "expert_counts", torch.int32, (cfg.E,), dev)
+    if out is None:
+        out = torch.empty(cfg.T, cfg.H, dtype=bf, device=dev)
+    po = _need(out, "out", bf, (cfg.T, cfg.H), dev)
+    if ws is None:
+        ws = Workspace(cfg, WS_LAYER, dev, flags)
+    elif ws.which != WS_LAYER or not ws.fits(cfg, flags):
+        raise ValueError("workspace of the wrong kind or too small")
+    rc = _lib.load().moe_layer(ctypes.byref(cfg.c()), ph, pwr, psp, pb, pgu, pd, psgu, psd, pr, pi, pw, pc, po,
+                               flags, ws.ptr, ws.nbytes, _stream(dev))
+    _lib.check(rc, "moe_layer")
+    return out, routing
+
+
 def backward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, d_out,
              *, ws: Optional[Workspace] = None, out: Optional[dict] = None):
     """moe_backward (routing fixed): dict(d_hidden [T,H] bf16, dW_gate_up
@@ -333,22 +379,33 @@ def profile_read(reset: bool = True) -> dict:
 
 
 class MoELayer:
-    """One MoE layer: weights on the device plus its two workspaces.
+    """One MoE layer: weights on the device plus its workspaces.
 
-    __call__(hidden) runs moe_route then moe_forward on the current stream.
-    The router weight is split once at construction (prepare_router); call
-    prepare() again after changing W_router in place."""
+    __call__(hidden) runs moe_route then moe_forward on the current stream,
+    or, with single_call=True (no balance loss), the one moe_layer call with
+    `flags` (the fused router where it applies).  The router weight is split
+    once at construction (prepare_router); call prepare() again after
+    changing W_router in place."""
 
     def __init__(self, cfg: MoeConfig, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
-                 aux: bool = False, ws_route: Optional[Workspace] = None, ws_fwd: Optional[Workspace] = None):
+                 aux: bool = False, ws_route: Optional[Workspace] = None, ws_fwd: Optional[Workspace] = None,
+                 single_call: bool = False, flags: int = 0):
+        if single_call and aux:
+            raise ValueError("moe_layer does not compute the balance loss: use single_call=False with aux")
         self.cfg = cfg
         self.W_router, self.expert_bias = W_router, expert_bias
         self.W_gate_up, self.W_down = W_gate_up, W_down
         self.shared_gate_up, self.shared_down = shared_gate_up, shared_down
         self.aux = aux
+        self.single_call, self.flags = single_call, flags
         self.device = W_router.device
-        self.ws_route = ws_route or Workspace(cfg, _lib.MOE_WS_ROUTE, self.device)
-        self.ws_fwd = ws_fwd or Workspace(cfg, _lib.MOE_WS_FORWARD, self.device)
+        if single_call:
+            self.ws_layer = Workspace(cfg, WS_LAYER, self.device, flags)
+            self.ws_route = self.ws_fwd = None
+        else:
+            self.ws_layer = None
+            self.ws_route = ws_route or Workspace(cfg, _lib.MOE_WS_ROUTE, self.device)
+            self.ws_fwd = ws_fwd or Workspace(cfg, _lib.MOE_WS_FORWARD, self.device)
         self.routing = None
         self.last_launches = 0
         self.W_split = None
@@ -360,6 +417,12 @@ class MoELayer:
 
     def __call__(self, hidden, residual=None, out=None):
         self._hidden = hidden
+        if self.single_call:
+            y, self.routing = layer(self.cfg, hidden, self.W_router, self.expert_bias, self.W_gate_up, self.W_down,
+                                    self.shared_gate_up, self.shared_down, residual, W_split=self.W_split,
+                                    flags=self.flags, ws=self.ws_layer, out=out, routing=self.routing)
+            self.last_launches = last_launch_count()
+            return y
         self.routing = route(self.cfg, hidden, self.W_router, self.expert_bias, aux=self.aux, ws=self.ws_route,
                              out=self.routing, W_split=self.W_split)
         n = last_launch_count()
@@ -370,7 +433,10 @@ class MoELayer:
         return y
 
     def status(self) -> int:
-        st = self.ws_route.status() | self.ws_fwd.status()
+        if self.single_call:
+            st = self.ws_layer.status()
+        else:
+            st = self.ws_route.status() | self.ws_fwd.status()
         if getattr(self, "ws_bwd", None) is not None:
             st |= self.ws_bwd.status()
         return st

@@ -182,6 +182,38 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
                 const int32_t *topk_idx, const float *topk_w, const moe_bf16 *residual,
                 moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
 
+/* The whole layer in one call: moe_route (without the balance loss) followed
+ * by moe_forward, on one workspace of moe_layer_workspace_bytes(cfg, flags)
+ * bytes (moe_workspace_init() once after allocating it).  Arguments as in
+ * those two calls; W_split is moe_prepare_router's output or NULL (then the
+ * router weight is split inside the call); topk_idx, topk_w and
+ * expert_counts are outputs here.
+ *
+ * Fused routing.  For E = 256 experts in n_group = 8 groups with k <= 8 (the
+ * routing page's setting) and T >= MOE_FUSED_MIN_T, the router's tensor-core
+ * kernel also does the rest of routing and the bucketing of section 四: the
+ * two threads that hold a token's 256 logits select its experts (the same
+ * arithmetic and tie rules as moe_route, so the outputs are identical bit for
+ * bit), claim each pair's row in its expert's bucket with one integer atomic
+ * per expert and 128-token tile, and copy the hidden rows into the buckets.
+ * Bucket e then starts at row e T of a larger activation matrix (E T rows of
+ * H bf16 in the workspace: 34 GB at T = 32768, H = 2048), and the order of
+ * rows inside a bucket depends on scheduling; each expert row's result does
+ * not, and the combine adds every token's rows in a fixed order, so out is
+ * deterministic and equal to the unfused path's.  expert_counts are exact.
+ * flags: MOE_LAYER_FUSE_ALWAYS takes the fused path for any T where the
+ * shape allows it, MOE_LAYER_FUSE_NEVER never; 0 decides by T as above.
+ * Returns MOE_ERR_INVALID_ARG for unknown flags. */
+#define MOE_LAYER_FUSE_ALWAYS 1
+#define MOE_LAYER_FUSE_NEVER 2
+#define MOE_FUSED_MIN_T 19456 /* 152 token tiles of 128: one per SM of a GB300 */
+size_t moe_layer_workspace_bytes(const moe_cfg *cfg, int flags);
+int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const moe_bf16 *W_split,
+              const float *expert_bias, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
+              const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const moe_bf16 *residual,
+              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, moe_bf16 *out, int flags, void *ws,
+              size_t ws_bytes, void *stream);
+
 /* Backward of moe_forward for fixed routing (the training step of the layer;
  * the routing page trains the layer but prints no backward: these are the
  * gradients of the forward above, the bf16 rounding of the intermediate
@@ -273,7 +305,7 @@ int moe_rmsnorm(int32_t T, int32_t H, const moe_bf16 *x, moe_bf16 *out, float ep
 int moe_get_status(void *ws, size_t ws_bytes, void *stream, int32_t *status, int reset);
 
 /* Number of kernels the last successful moe_route / moe_route_prepared /
- * moe_prepare_router / moe_forward / moe_route_from_logits /
+ * moe_prepare_router / moe_forward / moe_layer / moe_route_from_logits /
  * moe_router_logits call on this thread enqueued (memsets not counted). */
 int moe_last_launch_count(void);
 
@@ -283,7 +315,7 @@ int moe_last_launch_count(void);
  * the recorded events, folds them into per-kernel totals and returns the
  * total milliseconds and launch count of kernel `kernel_id` (0 <=
  * kernel_id < MOE_KERNEL_COUNT), clearing them when reset != 0. */
-#define MOE_KERNEL_COUNT 16
+#define MOE_KERNEL_COUNT 18
 int moe_profile_enable(int on);
 int moe_profile_read(int kernel_id, double *total_ms, int32_t *launches, int reset);
 const char *moe_kernel_name(int kernel_id);
