@@ -39,9 +39,7 @@ EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router
            "moe_route_prepared", "moe_dense_workspace_bytes", "moe_dense_ffn", "moe_backward",
            "moe_layer_workspace_bytes", "moe_layer")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
-MOE_LAYER_FUSE_ALWAYS = 1
-MOE_LAYER_FUSE_NEVER = 2
-MOE_FUSED_MIN_T = 19456
+MOE_LAYER_FUSED_ROUTER = 1
 MOE_KERNEL_COUNT = 18
 
 

@@ -419,24 +419,22 @@ int check_ws(void *ws, size_t ws_bytes, size_t need)
 struct LayerLayout {
     RouteLayout r;
     FwdLayout f;
-    size_t gscr, lscr, dest, offs, total;
+    size_t sync, offs, total;   // sync: the fused router's tile queue counter, then one ready count per tile
     bool fused;
 };
 
 // the fused router's shape: 256 experts in 8 groups, at most FUSED_MAX_K per
 // token, every bucket row index e T + slot within int32, a hidden row within
-// one eighth of the ring (less its barriers) of the 256-expert router
+// one warp's share (16 KB) of the 256-expert router's ring
 bool fusable(const moe_cfg &c)
 {
     return c.E == 256 && c.n_group == 8 && c.k <= FUSED_MAX_K && (long long)c.E * c.T < (1ll << 31) &&
-           c.H <= 14336;   // a hidden row fits one copy slot of the router's shared-memory ring
+           c.H <= 8192;   // a hidden row fits one copy slot of the router's shared-memory ring
 }
 
 bool layer_fused(const moe_cfg &c, int flags)
 {
-    if (!fusable(c) || (flags & MOE_LAYER_FUSE_NEVER))
-        return false;
-    return (flags & MOE_LAYER_FUSE_ALWAYS) || c.T >= MOE_FUSED_MIN_T;
+    return (flags & MOE_LAYER_FUSED_ROUTER) && fusable(c);
 }
 
 LayerLayout layer_layout(const moe_cfg &c, int flags)
@@ -456,12 +454,8 @@ LayerLayout layer_layout(const moe_cfg &c, int flags)
     L.f.total += b;
     const size_t tiles = (size_t)(c.T + GEMM_BM - 1) / GEMM_BM;
     size_t off = L.f.total;
-    L.gscr = off;
-    off = align_up(off + tiles * GEMM_BM * 8 * 4, 256);
-    L.lscr = off;
-    off = align_up(off + tiles * GEMM_BM * 2 * 3 * FUSED_MAX_K * 4, 256);
-    L.dest = off;
-    off = align_up(off + tiles * GEMM_BM * FUSED_MAX_K * 4, 256);
+    L.sync = off;
+    off = align_up(off + (tiles + 1) * 4, 256);
     L.offs = off;
     off = align_up(off + (size_t)(c.E + 1) * 4, 256);
     L.total = off;
@@ -483,12 +477,15 @@ int fused_route(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
     } else if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s) != cudaSuccess) {
         return MOE_ERR_CUDA;
     }
+    const int tiles = (c.T + GEMM_BM - 1) / GEMM_BM;
+    int *sync = at<int>(ws, L.sync);
+    if (cudaMemsetAsync(sync, 0, sizeof(int) * (tiles + 1), s) != cudaSuccess)
+        return MOE_ERR_CUDA;
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
         !make_map_bf16(&p.tmB0, W3, 3ull * c.E, c.H, GEMM_BK, 256))
         return MOE_ERR_CUDA;
-    const int tiles = (c.T + GEMM_BM - 1) / GEMM_BM;
     p.n_tiles = 1;
     p.ksplit = 1;
     p.num_tiles_static = tiles;
@@ -502,9 +499,10 @@ int fused_route(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
     p.w_out = w;
     p.counts = counts;
     p.slot_local = at<int32_t>(ws, L.f.slot_of);
-    p.dest = at<int32_t>(ws, L.dest);
-    p.gscr = at<float>(ws, L.gscr);
-    p.lscr = at<uint32_t>(ws, L.lscr);
+    p.unit_ctr = sync;
+    p.ready = sync + 1;
+    p.out = at<float>(ws, L.r.logits);
+    p.ld_out = c.E;
     p.hidden = hidden;
     p.xperm = at<uint16_t>(ws, L.f.xperm);
     p.topk_group = c.topk_group;
@@ -1098,7 +1096,7 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
         rc = check_forward_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
-    if (flags & ~(MOE_LAYER_FUSE_ALWAYS | MOE_LAYER_FUSE_NEVER))
+    if (flags & ~MOE_LAYER_FUSED_ROUTER)
         return MOE_ERR_INVALID_ARG;
     if (!hidden || !W_router || !W_gate_up || !W_down || !shared_gate_up || !shared_down || !topk_idx || !topk_w ||
         !expert_counts || !out)

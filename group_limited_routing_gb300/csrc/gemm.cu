@@ -21,14 +21,13 @@
 //               N = 256 MMA (half the shared-memory operand traffic per flop
 //               of the 128-expert tiles), two TMEM K-block slots and eight
 //               epilogue warps (two per TMEM lane quadrant, 128 columns each).
-//   GK_ROUTER_FUSED  GK_ROUTER_WIDE whose epilogue routes and buckets the
-//               tokens itself (section 二 steps 1-3, section 三, section 四's
-//               bucketing): the two threads holding a token's 256 logits pick
-//               its experts, claim the pairs' rows in the experts' buckets
-//               with one integer atomic per expert and tile, and, after the
-//               CTA's last tile, copy the hidden rows into the buckets -- so
-//               the HBM-bound row copies of some CTAs overlap the MMAs of
-//               others instead of following the whole router.
+//   GK_ROUTER_FUSED  GK_ROUTER_WIDE that also routes and buckets the tokens
+//               (section 二 steps 1-3, section 三, section 四's bucketing):
+//               after its own tiles a CTA takes finished tiles from a queue,
+//               selects their tokens' experts, claims the pairs' rows in the
+//               experts' buckets with one integer atomic per expert and tile,
+//               and copies the hidden rows there -- so the HBM-bound copies of
+//               CTAs with fewer tiles overlap the MMAs of the others.
 // The grouped kinds also serve the dense first-layer MLP (one weight group).
 //
 // Every kernel starts with griddepcontrol.wait (programmatic dependent
@@ -53,6 +52,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "route_token.cuh"
 
 namespace glr {
 
@@ -216,7 +216,7 @@ struct GemmLayout {
     static constexpr int TQ = DYN ? TQ_RING : 0;
     // the fused router's epilogue barrier and per-tile bucket histogram
     static constexpr bool FUSED = (KIND == GK_ROUTER_FUSED);
-    static constexpr int HIST = FUSED ? 256 * 4 : 0;
+    static constexpr int HIST = FUSED ? 256 * 4 + 16 : 0;
     // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin, tq_full[TQ], tq_empty[TQ] (, epi)
     static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1 + 2 * TQ + (FUSED ? 1 : 0);
     static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16 + TQ * 4 + HIST;
@@ -660,30 +660,25 @@ __device__ __forceinline__ void epilogue_wgrad(const GemmParams &p, const TileIn
 }
 
 // ---------------------------------------------------------------------------
-// GK_ROUTER_FUSED epilogue.  Thread (half, lane) of the warp pair of lane
-// quadrant q holds token row r = 32 q + lane and its logits of experts
-// 128 half .. 128 half + 127, i.e. groups 4 half .. 4 half + 3 (E = 256 in 8
-// groups of 32).  The two threads of a token exchange what the selection needs
-// through per-CTA global scratch (the stages fill shared memory), with an
-// mbarrier over the eight epilogue warps between the steps.  The arithmetic
-// is that of the routing kernels (route.cu): the same score formula, group
-// score, group ranking, winner order (key desc, expert asc) and sequential
-// normaliser, so the results are bit-identical to routing the same logits
-// there.
+// GK_ROUTER_FUSED.  The epilogue warps store each tile's logits like the
+// 256-expert router (to p.out, in L2) and mark the tile ready; after the CTA's
+// last tile they take tiles from a queue shared by all CTAs (so CTAs that had
+// fewer tiles start on the first tiles while the others still multiply) and,
+// for each: select every token's experts (route_token, the routing kernel's
+// own code: the same bits), count the tile's hits per expert, claim the rows
+// in the experts' buckets with one integer atomic per expert, and copy the
+// tokens' hidden rows there with bulk copies through the idle stage ring.
 struct FusedCtx {
     uint32_t ebar;    // epilogue barrier: 8 warp arrivals per phase
     uint32_t phase;   // phases completed so far
-    int *hist;        // smem [256]: the tile's hits per expert, then the bucket bases
+    int *hist;        // smem [256]: a tile's hits per expert, then the bucket bases
+    int *unit;        // smem: the tile the CTA took from the queue
 };
 
-// The eight epilogue warps meet; shared-memory writes made before (and,
-// with global_writes, global ones) are visible to every epilogue thread
-// after.  Bounded like every wait of the kernel.
-__device__ __forceinline__ bool epi_sync(FusedCtx &fz, int lane, volatile int *abort_flag, unsigned long long limit,
-                                         bool global_writes = true)
+// The eight epilogue warps meet; shared-memory writes made before are visible
+// to every epilogue thread after.  Bounded like every wait of the kernel.
+__device__ __forceinline__ bool epi_sync(FusedCtx &fz, int lane, volatile int *abort_flag, unsigned long long limit)
 {
-    if (global_writes)
-        __threadfence();
     __syncwarp();
     int ok = 1;
     if (lane == 0) {
@@ -696,284 +691,330 @@ __device__ __forceinline__ bool epi_sync(FusedCtx &fz, int lane, volatile int *a
     return ok != 0;
 }
 
-__device__ __forceinline__ float bias_of(const float *bias, int e)
+// Bounded wait (lane 0) until all eight epilogue warps of the tile's CTA have
+// stored its logits.
+__device__ __forceinline__ bool wait_tile_ready(const int *ready, volatile int *abort_flag, unsigned long long limit)
 {
-    return bias ? __ldg(bias + e) : 0.0f;
+    int v = 0;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ready) : "memory");
+    if (v >= 8)
+        return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ready) : "memory");
+        if (v >= 8)
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag)
+                return false;
+            if (globaltimer_ns() - t0 > limit) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
 }
 
-// Routes the tile's tokens (acc: this thread's 128 logits, overwritten with
-// their scores) and claims their bucket rows; `ew` = epilogue thread 0..255.
-__device__ __forceinline__ bool fused_route_tile(const GemmParams &p, const TileInfo &ti, int tile,
-                                                 float (&acc)[128], int quad, int half, int lane, int ew,
-                                                 FusedCtx &fz, volatile int *abort_flag, unsigned long long limit)
+// Post-phase shared memory, carved from the idle stage ring (bytes):
+//   [0, 128 K)        the tile's logits, then their scores, [128][256] fp32;
+//                     afterwards each warp's FUSED_SLOTS hidden-row slots
+//   group scores [128][8] fp32, the halves' lists [128][2][3 FUSED_MAX_K],
+//   the pairs' bucket rows [128][FUSED_MAX_K], the bias [256];
+//   at the ring's end the barriers of the staging load and of the row slots.
+constexpr int FUSED_SLOTS = 4;
+constexpr uint32_t FP_LOGITS = 0;
+constexpr uint32_t FP_GROUPS = GEMM_BM * 256 * 4;
+constexpr uint32_t FP_LISTS = FP_GROUPS + GEMM_BM * 8 * 4;
+constexpr uint32_t FP_DEST = FP_LISTS + GEMM_BM * 2 * 3 * FUSED_MAX_K * 4;
+constexpr uint32_t FP_BIAS = FP_DEST + GEMM_BM * FUSED_MAX_K * 4;
+constexpr uint32_t FP_END = FP_BIAS + 256 * 4;
+constexpr uint32_t FP_BARS = 8 * (1 + 8 * FUSED_SLOTS);   // staging + 8 warps' slot barriers
+
+// The post phase of one CTA.  All 256 epilogue threads (ew = 0..255, warp
+// w = ew / 32) take tiles from the queue; per tile, thread (h = ew / 128,
+// r = ew % 128) holds token r's experts 128 h .. 128 h + 127 (groups
+// 4 h .. 4 h + 3) and reads them from shared memory starting at column
+// r % 32, so the 32 lanes of a warp hit 32 different banks.  The arithmetic
+// is the routing kernels' (route.cu): the same score formula, group score
+// (the two best biased scores, a repeated best counting twice), group ranking,
+// winner order (key desc, expert asc) and sequential normaliser, so the
+// results are bit-identical to routing the same logits there.
+__device__ __forceinline__ void fused_post(const GemmParams &p, int num_tiles, int w, int lane, int ew, FusedCtx &fz,
+                                          uint8_t *ring_ptr, uint32_t ring, uint32_t ring_bytes,
+                                          volatile int *abort_flag, unsigned long long limit)
 {
-    const int r = quad * 32 + lane;
-    const bool valid = r < ti.rows;
-    const int t = ti.a_row + r;
-    const int e0 = half * 128;
     const int K = p.k;
-
-    // scores (section 二 step 1), in place; non-finite logits or biases are reported
-    bool bad = false;
-#pragma unroll
-    for (int c = 0; c < 128; ++c) {
-        const float b = bias_of(p.bias, e0 + c);
-        bad |= !isfinite(acc[c]) || !isfinite(b);
-        acc[c] = router_sigmoid(acc[c]);
-    }
-    if (bad && valid)
-        atomicOr(p.status, ST_NONFINITE);
-
-    // this half's four group scores: the two best biased scores (section 三:
-    // the bias takes part in choosing), a repeated best counting twice
-    float gs[4];
-#pragma unroll
-    for (int gi = 0; gi < 4; ++gi) {
-        uint32_t m1 = 0u, m2 = 0u;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const uint32_t u = fkey(acc[gi * 32 + i] + bias_of(p.bias, e0 + gi * 32 + i));
-            m2 = max(m2, min(m1, u));
-            m1 = max(m1, u);
-        }
-        gs[gi] = fkey_value(m1) + fkey_value(m2);
-    }
-    float *gsc = p.gscr + ((size_t)blockIdx.x * GEMM_BM + r) * 8;
-    *reinterpret_cast<float4 *>(gsc + half * 4) = make_float4(gs[0], gs[1], gs[2], gs[3]);
-    if (!epi_sync(fz, lane, abort_flag, limit))
-        return false;
-    // the previous tile's bucket bases have all been read: clear the histogram
-    fz.hist[ew] = 0;
-
-    // keep the topk_group best groups (section 二 step 2), ties to the lower group
-    const float4 go = __ldcg(reinterpret_cast<const float4 *>(gsc + (1 - half) * 4));
-    float g[8];
-    g[4 * half + 0] = gs[0];
-    g[4 * half + 1] = gs[1];
-    g[4 * half + 2] = gs[2];
-    g[4 * half + 3] = gs[3];
-    g[4 * (1 - half) + 0] = go.x;
-    g[4 * (1 - half) + 1] = go.y;
-    g[4 * (1 - half) + 2] = go.z;
-    g[4 * (1 - half) + 3] = go.w;
-    uint32_t keep = 0u;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        int rank = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            rank += (g[i] > g[j] || (g[i] == g[j] && i < j)) ? 1 : 0;
-        if (rank < p.topk_group)
-            keep |= 1u << j;
-    }
-
-    // this half's best FUSED_MAX_K experts of the kept groups, sorted by
-    // (key desc, expert asc): candidates arrive in expert order, so one with
-    // a key equal to a listed one stays behind it
-    uint32_t lk[FUSED_MAX_K];
-    int le[FUSED_MAX_K];
-    float ls[FUSED_MAX_K];
-#pragma unroll
-    for (int i = 0; i < FUSED_MAX_K; ++i) {
-        lk[i] = 0u;
-        le[i] = e0;
-        ls[i] = 0.0f;
-    }
-#pragma unroll
-    for (int c = 0; c < 128; ++c) {
-        if (!((keep >> (4 * half + c / 32)) & 1u))
-            continue;
-        const uint32_t u = fkey(acc[c] + bias_of(p.bias, e0 + c));
-        if (u <= lk[FUSED_MAX_K - 1])
-            continue;
-#pragma unroll
-        for (int i = FUSED_MAX_K - 1; i > 0; --i) {
-            const bool up = u > lk[i - 1];       // the candidate ranks above entry i-1: it moves down
-            const bool here = u > lk[i];
-            lk[i] = up ? lk[i - 1] : (here ? u : lk[i]);
-            le[i] = up ? le[i - 1] : (here ? e0 + c : le[i]);
-            ls[i] = up ? ls[i - 1] : (here ? acc[c] : ls[i]);
-        }
-        if (u > lk[0]) {
-            lk[0] = u;
-            le[0] = e0 + c;
-            ls[0] = acc[c];
-        }
-    }
-    uint32_t *lsc = p.lscr + (((size_t)blockIdx.x * GEMM_BM + r) * 2 + half) * (3 * FUSED_MAX_K);
-#pragma unroll
-    for (int i = 0; i < FUSED_MAX_K; i += 4) {
-        *reinterpret_cast<uint4 *>(lsc + i) = make_uint4(lk[i], lk[i + 1], lk[i + 2], lk[i + 3]);
-        *reinterpret_cast<uint4 *>(lsc + FUSED_MAX_K + i) =
-            make_uint4((uint32_t)le[i], (uint32_t)le[i + 1], (uint32_t)le[i + 2], (uint32_t)le[i + 3]);
-        *reinterpret_cast<uint4 *>(lsc + 2 * FUSED_MAX_K + i) =
-            make_uint4(__float_as_uint(ls[i]), __float_as_uint(ls[i + 1]), __float_as_uint(ls[i + 2]),
-                       __float_as_uint(ls[i + 3]));
-    }
-    if (!epi_sync(fz, lane, abort_flag, limit))
-        return false;
-
-    // the lower half's thread merges the two lists: the token's k experts in
-    // output order, their weights (section 二 step 3: sequential sum of the
-    // chosen unbiased scores, + eps, times routed_scaling_factor) and each
-    // pair's rank among the tile's hits of its expert
-    int oe[FUSED_MAX_K], orank[FUSED_MAX_K];
-    if (half == 0) {
-        const uint32_t *osc = lsc + 3 * FUSED_MAX_K;   // the upper half's list
-        uint32_t pk[FUSED_MAX_K];
-        int pe[FUSED_MAX_K];
-        float ps[FUSED_MAX_K];
-#pragma unroll
-        for (int i = 0; i < FUSED_MAX_K; i += 4) {
-            const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(osc + i));
-            const uint4 b = __ldcg(reinterpret_cast<const uint4 *>(osc + FUSED_MAX_K + i));
-            const uint4 c = __ldcg(reinterpret_cast<const uint4 *>(osc + 2 * FUSED_MAX_K + i));
-            pk[i] = a.x; pk[i + 1] = a.y; pk[i + 2] = a.z; pk[i + 3] = a.w;
-            pe[i] = (int)b.x; pe[i + 1] = (int)b.y; pe[i + 2] = (int)b.z; pe[i + 3] = (int)b.w;
-            ps[i] = __uint_as_float(c.x); ps[i + 1] = __uint_as_float(c.y);
-            ps[i + 2] = __uint_as_float(c.z); ps[i + 3] = __uint_as_float(c.w);
-        }
-        float os[FUSED_MAX_K];
-        float den = 0.0f;
-#pragma unroll
-        for (int j = 0; j < FUSED_MAX_K; ++j) {
-            const bool a = lk[0] >= pk[0];          // equal keys: the lower half's expert has the lower id
-            oe[j] = a ? le[0] : pe[0];
-            os[j] = a ? ls[0] : ps[0];
-#pragma unroll
-            for (int i = 0; i < FUSED_MAX_K - 1; ++i) {
-                lk[i] = a ? lk[i + 1] : lk[i];
-                le[i] = a ? le[i + 1] : le[i];
-                ls[i] = a ? ls[i + 1] : ls[i];
-                pk[i] = a ? pk[i] : pk[i + 1];
-                pe[i] = a ? pe[i] : pe[i + 1];
-                ps[i] = a ? ps[i] : ps[i + 1];
-            }
-            lk[FUSED_MAX_K - 1] = a ? 0u : lk[FUSED_MAX_K - 1];
-            pk[FUSED_MAX_K - 1] = a ? pk[FUSED_MAX_K - 1] : 0u;
-            if (j < K)
-                den += os[j];                       // in output order
-        }
-        den += p.eps;
-#pragma unroll
-        for (int j = 0; j < FUSED_MAX_K; ++j) {
-            orank[j] = 0;
-            if (j < K && valid) {
-                p.idx_out[(size_t)t * K + j] = oe[j];
-                p.w_out[(size_t)t * K + j] = (os[j] / den) * p.rsf;
-                orank[j] = atomicAdd(&fz.hist[oe[j]], 1);
-            }
-        }
-    }
-    if (!epi_sync(fz, lane, abort_flag, limit, false))
-        return false;
-
-    // one atomic per expert hit in this tile reserves its rows in the bucket;
-    // the counters end as the experts' hit counts (section 六)
-    {
-        const int h = fz.hist[ew];
-        if (h > 0)
-            fz.hist[ew] = atomicAdd(p.counts + ew, h);
-    }
-    if (!epi_sync(fz, lane, abort_flag, limit, false))
-        return false;
-    if (half == 0 && valid) {
-#pragma unroll
-        for (int j = 0; j < FUSED_MAX_K; ++j) {
-            if (j < K) {
-                const int slot = fz.hist[oe[j]] + orank[j];
-                const bool ok = slot < p.T;       // at most T pairs per expert: one per token
-                p.slot_local[(size_t)t * K + j] = ok ? slot : -1;
-                p.dest[((size_t)tile * GEMM_BM + r) * FUSED_MAX_K + j] = ok ? oe[j] * p.T + slot : -1;
-                if (!ok)
-                    atomicOr(p.status, ST_COUNT_MISMATCH);
-            }
-        }
-    }
-    return true;
-}
-
-// After the CTA's last tile (every MMA done, the stage ring idle): copies the
-// hidden row of every routed pair of the CTA's tiles into the pair's bucket
-// rows with bulk copies through the ring's shared memory.  Warp w (0..7)
-// takes rows w, w + 8, ... of each tile; its lane 0 loads up to FUSED_SLOTS
-// rows into its slice of the ring, then stores each to its k bucket rows,
-// and waits until those stores have read the slice before the next batch.
-constexpr int FUSED_SLOTS = 8;
-constexpr int FUSED_RING_BARS = 8 * FUSED_SLOTS * 8;   // barrier bytes at the ring's end
-__device__ __forceinline__ void fused_copy_rows(const GemmParams &p, int num_tiles, int w, int lane, uint32_t ring,
-                                                uint32_t ring_bytes, volatile int *abort_flag,
-                                                unsigned long long limit)
-{
-    if (lane != 0)
-        return;
+    const int h = ew >> 7, r = ew & 127;
+    const int e0 = 128 * h;
+    float *sl = reinterpret_cast<float *>(ring_ptr + FP_LOGITS);
+    float *sg = reinterpret_cast<float *>(ring_ptr + FP_GROUPS);
+    uint32_t *sls = reinterpret_cast<uint32_t *>(ring_ptr + FP_LISTS);
+    int *sdst = reinterpret_cast<int *>(ring_ptr + FP_DEST);
+    float *sbias = reinterpret_cast<float *>(ring_ptr + FP_BIAS);
+    const uint32_t stage_bar = ring + ring_bytes - FP_BARS;
+    const uint32_t bar0 = stage_bar + 8u + (uint32_t)w * FUSED_SLOTS * 8;
     const uint32_t rowbytes = (uint32_t)p.H * 2;
-    const uint32_t slice = (ring_bytes - FUSED_RING_BARS) / 8 / rowbytes * rowbytes;
-    const int ns = min((int)(slice / rowbytes), FUSED_SLOTS);   // >= 1: the host keeps 2 H <= the slice
-    const uint32_t my = ring + (uint32_t)w * slice;
-    const uint32_t bar0 = ring + ring_bytes - FUSED_RING_BARS + (uint32_t)w * FUSED_SLOTS * 8;
-    fence_proxy_async_smem();                 // the ring was last written by TMA loads
-    for (int b = 0; b < ns; ++b)
-        mbar_init(bar0 + 8u * b, 1);
-    fence_mbar_init();
-    fence_proxy_async_smem();
-    uint32_t parity = 0;                      // bit b: parity of slot b's next completion
-    const int K = p.k;
-    int tile = blockIdx.x, r = w;
-    int dest_row[FUSED_SLOTS];
-    bool ok = true;
-    while (ok) {
-        int nb = 0;
-        while (nb < ns && tile < num_tiles) {
-            const int rows = min(GEMM_BM, p.T - tile * GEMM_BM);
-            if (r >= rows) {
-                tile += gridDim.x;
-                r = w;
-                continue;
-            }
-            const int t = tile * GEMM_BM + r;
-            dest_row[nb] = tile * GEMM_BM + r;    // its row of the destination table
-            const uint32_t bar = bar0 + 8u * nb;
-            mbar_arrive_expect_tx(bar, rowbytes);
-            bulk_load_g2s(my + (uint32_t)nb * rowbytes, p.hidden + (size_t)t * p.H, rowbytes, bar);
-            ++nb;
-            r += 8;
-        }
-        if (nb == 0)
-            break;
-        for (int b = 0; b < nb; ++b) {
-            const uint32_t bar = bar0 + 8u * b;
-            if (ok && !mbar_wait(bar, (parity >> b) & 1u, abort_flag, limit))
-                ok = false;
-            if (!ok) {
-                mbar_drain(bar, (parity >> b) & 1u);   // its load may still land: let it, then stop
-                continue;
-            }
-            parity ^= 1u << b;
-            const int *dr = p.dest + (size_t)dest_row[b] * FUSED_MAX_K;
-            for (int j = 0; j < K; ++j) {
-                const int d = __ldcg(dr + j);
-                if (d >= 0)
-                    bulk_store_s2g(p.xperm + (size_t)d * p.H, my + (uint32_t)b * rowbytes, rowbytes);
-            }
-        }
-        bulk_commit_group();
-        bulk_wait_group_read<0>();            // the slice may be refilled
+    const int ns = min((int)(GEMM_BM * 256 * 4 / 8 / rowbytes), FUSED_SLOTS);   // >= 1: the host keeps H <= 8192
+    const uint32_t my = ring + FP_LOGITS + (uint32_t)w * (GEMM_BM * 256 * 4 / 8);
+    if (lane == 0) {
+        fence_proxy_async_smem();             // the ring was last written by TMA loads
+        if (ew == 0)
+            mbar_init(stage_bar, 1);
+        for (int b = 0; b < ns; ++b)
+            mbar_init(bar0 + 8u * b, 1);
+        fence_mbar_init();
     }
-    bulk_wait_group_all();
+    sbias[ew] = p.bias ? __ldg(p.bias + ew) : 0.0f;
+    uint32_t stage_par = 0, parity = 0;      // parity: bit b = slot b's next completion (lane 0)
+    bool nonfinite = false;
+    for (;;) {
+        if (ew == 0)
+            *fz.unit = atomicAdd(p.unit_ctr, 1);
+        if (!epi_sync(fz, lane, abort_flag, limit))
+            break;
+        const int u = *fz.unit;
+        if (u >= num_tiles)
+            break;
+        const int row0 = u * GEMM_BM;
+        const int rows = min(GEMM_BM, p.T - row0);
+        if (ew == 0) {
+            // every slot's stores have read the ring (each warp waited before the
+            // meeting above): stage the tile's logits once its CTA has stored them
+            bool ok = wait_tile_ready(p.ready + u, abort_flag, limit);
+            if (ok) {
+                fence_proxy_async_global();       // the logits were stored by generic writes
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(stage_bar, (uint32_t)rows * 1024u);
+                bulk_load_g2s(ring + FP_LOGITS, static_cast<const float *>(p.out) + (size_t)row0 * 256,
+                              (uint32_t)rows * 1024u, stage_bar);
+            }
+        }
+        if (!mbar_wait(stage_bar, stage_par, abort_flag, limit))
+            break;
+        stage_par ^= 1u;
+        const bool valid = r < rows;
+        float *row = sl + r * 256 + e0;
+
+        // scores (section 二 step 1), in place; this half's four group scores
+        // on the biased scores (section 三)
+        float gs[4];
+#pragma unroll 1
+        for (int gi = 0; gi < 4; ++gi) {
+            uint32_t m1 = 0u, m2 = 0u;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+                const int c = gi * 32 + ((i + r) & 31);
+                const float L = row[c];
+                const float b = sbias[e0 + c];
+                nonfinite |= valid && (!isfinite(L) || !isfinite(b));
+                const float sc = router_sigmoid(L);
+                row[c] = sc;
+                const uint32_t k = fkey(sc + b);
+                m2 = max(m2, min(m1, k));
+                m1 = max(m1, k);
+            }
+            gs[gi] = fkey_value(m1) + fkey_value(m2);
+        }
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi)
+            sg[r * 8 + 4 * h + gi] = gs[gi];
+        if (!epi_sync(fz, lane, abort_flag, limit))
+            break;
+        // keep the topk_group best groups (section 二 step 2), ties to the lower group
+        float g[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            g[j] = sg[r * 8 + j];
+        uint32_t keep = 0u;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            int rank = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                rank += (g[q] > g[j] || (g[q] == g[j] && q < j)) ? 1 : 0;
+            if (rank < p.topk_group)
+                keep |= 1u << j;
+        }
+        // this half's best FUSED_MAX_K of the kept groups, by (key desc, expert asc)
+        uint32_t lk[FUSED_MAX_K];
+        int le[FUSED_MAX_K];
+        float ls[FUSED_MAX_K];
+#pragma unroll
+        for (int q = 0; q < FUSED_MAX_K; ++q) {
+            lk[q] = 0u;
+            le[q] = 0x7fffffff;
+            ls[q] = 0.0f;
+        }
+#pragma unroll 1
+        for (int gi = 0; gi < 4; ++gi) {
+            if (!((keep >> (4 * h + gi)) & 1u))
+                continue;
+#pragma unroll 2
+            for (int i = 0; i < 32; ++i) {
+                const int c = gi * 32 + ((i + r) & 31);
+                const float sc = row[c];
+                const uint32_t k = fkey(sc + sbias[e0 + c]);
+                const int e = e0 + c;
+                if (k < lk[FUSED_MAX_K - 1] || (k == lk[FUSED_MAX_K - 1] && e > le[FUSED_MAX_K - 1]))
+                    continue;
+#pragma unroll
+                for (int q = FUSED_MAX_K - 1; q > 0; --q) {
+                    const bool up = k > lk[q - 1] || (k == lk[q - 1] && e < le[q - 1]);   // ranks above entry q-1
+                    const bool here = k > lk[q] || (k == lk[q] && e < le[q]);
+                    lk[q] = up ? lk[q - 1] : (here ? k : lk[q]);
+                    le[q] = up ? le[q - 1] : (here ? e : le[q]);
+                    ls[q] = up ? ls[q - 1] : (here ? sc : ls[q]);
+                }
+                if (k > lk[0] || (k == lk[0] && e < le[0])) {
+                    lk[0] = k;
+                    le[0] = e;
+                    ls[0] = sc;
+                }
+            }
+        }
+        // the logits area is refilled by bulk copies after the next meeting:
+        // order this thread's accesses to it before them
+        fence_proxy_async_smem();
+        uint32_t *mine = sls + (r * 2 + h) * 3 * FUSED_MAX_K;
+#pragma unroll
+        for (int q = 0; q < FUSED_MAX_K; ++q) {
+            mine[q] = lk[q];
+            mine[FUSED_MAX_K + q] = (uint32_t)le[q];
+            mine[2 * FUSED_MAX_K + q] = __float_as_uint(ls[q]);
+        }
+        if (!epi_sync(fz, lane, abort_flag, limit))
+            break;
+
+        // the lower half's thread merges the two lists: the token's k experts
+        // in output order, their weights (section 二 step 3) and each pair's
+        // rank among the tile's hits of its expert
+        int oe[FUSED_MAX_K], orank[FUSED_MAX_K];
+        if (h == 0) {
+            const uint32_t *other = sls + (r * 2 + 1) * 3 * FUSED_MAX_K;
+            uint32_t pk[FUSED_MAX_K];
+            int pe[FUSED_MAX_K];
+            float ps[FUSED_MAX_K];
+#pragma unroll
+            for (int q = 0; q < FUSED_MAX_K; ++q) {
+                pk[q] = other[q];
+                pe[q] = (int)other[FUSED_MAX_K + q];
+                ps[q] = __uint_as_float(other[2 * FUSED_MAX_K + q]);
+            }
+            float os[FUSED_MAX_K];
+            float den = 0.0f;
+#pragma unroll
+            for (int j = 0; j < FUSED_MAX_K; ++j) {
+                const bool a = lk[0] >= pk[0];      // equal keys: the lower half's expert has the lower id
+                oe[j] = a ? le[0] : pe[0];
+                os[j] = a ? ls[0] : ps[0];
+#pragma unroll
+                for (int q = 0; q < FUSED_MAX_K - 1; ++q) {
+                    lk[q] = a ? lk[q + 1] : lk[q];
+                    le[q] = a ? le[q + 1] : le[q];
+                    ls[q] = a ? ls[q + 1] : ls[q];
+                    pk[q] = a ? pk[q] : pk[q + 1];
+                    pe[q] = a ? pe[q] : pe[q + 1];
+                    ps[q] = a ? ps[q] : ps[q + 1];
+                }
+                lk[FUSED_MAX_K - 1] = a ? 0u : lk[FUSED_MAX_K - 1];
+                pk[FUSED_MAX_K - 1] = a ? pk[FUSED_MAX_K - 1] : 0u;
+                if (j < K)
+                    den += os[j];                   // in output order
+            }
+            den += p.eps;
+#pragma unroll
+            for (int j = 0; j < FUSED_MAX_K; ++j) {
+                orank[j] = 0;
+                if (j < K && valid && oe[j] >= 0 && oe[j] < 256) {
+                    const int t = row0 + r;
+                    p.idx_out[(size_t)t * K + j] = oe[j];
+                    p.w_out[(size_t)t * K + j] = (os[j] / den) * p.rsf;
+                    orank[j] = atomicAdd(&fz.hist[oe[j]], 1);
+                }
+            }
+        }
+        if (!epi_sync(fz, lane, abort_flag, limit))
+            break;
+        // one atomic per expert hit in this tile reserves its rows in the
+        // bucket; the counters end as the experts' hit counts (section 六)
+        {
+            const int n = fz.hist[ew];
+            if (n > 0)
+                fz.hist[ew] = atomicAdd(p.counts + ew, n);
+        }
+        if (!epi_sync(fz, lane, abort_flag, limit))
+            break;
+        if (h == 0) {
+#pragma unroll
+            for (int j = 0; j < FUSED_MAX_K; ++j) {
+                int d = -1;
+                if (j < K && valid && oe[j] >= 0 && oe[j] < 256) {
+                    const int t = row0 + r;
+                    const int slot = fz.hist[oe[j]] + orank[j];
+                    const bool in = slot < p.T;       // at most T pairs per expert: one per token
+                    p.slot_local[(size_t)t * K + j] = in ? slot : -1;
+                    d = in ? oe[j] * p.T + slot : -1;
+                    if (!in)
+                        atomicOr(p.status, ST_COUNT_MISMATCH);
+                }
+                sdst[r * FUSED_MAX_K + j] = d;
+            }
+        }
+        if (!epi_sync(fz, lane, abort_flag, limit))
+            break;
+        fz.hist[ew] = 0;                          // every base is read: clear for the next tile
+
+        // copy the hidden rows of tokens w, w + 8, ...: lane 0 loads up to ns
+        // of them into the warp's slots, then stores each to its bucket rows
+        bool cok = true;
+        if (lane == 0) {
+            const int ntok = (rows - w + 7) / 8;
+            for (int i0 = 0; i0 < ntok && cok; i0 += ns) {
+                const int nb = min(ns, ntok - i0);
+                for (int b = 0; b < nb; ++b) {
+                    const int t = row0 + w + 8 * (i0 + b);
+                    mbar_arrive_expect_tx(bar0 + 8u * b, rowbytes);
+                    bulk_load_g2s(my + (uint32_t)b * rowbytes, p.hidden + (size_t)t * p.H, rowbytes, bar0 + 8u * b);
+                }
+                for (int b = 0; b < nb; ++b) {
+                    const uint32_t bar = bar0 + 8u * b;
+                    if (cok && !mbar_wait(bar, (parity >> b) & 1u, abort_flag, limit))
+                        cok = false;
+                    if (!cok)
+                        mbar_drain(bar, (parity >> b) & 1u);   // let its load land, then stop
+                    parity ^= 1u << b;
+                    if (!cok)
+                        continue;
+                    const int rr = w + 8 * (i0 + b);
+                    for (int j = 0; j < K; ++j) {
+                        const int d = sdst[rr * FUSED_MAX_K + j];
+                        if (d >= 0)
+                            bulk_store_s2g(p.xperm + (size_t)d * p.H, my + (uint32_t)b * rowbytes, rowbytes);
+                    }
+                }
+                bulk_commit_group();
+                bulk_wait_group_read<0>();        // the slots may be refilled
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, cok ? 1 : 0, 0))
+            break;
+    }
+    if (lane == 0)
+        bulk_wait_group_all();
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0)
+        atomicOr(p.status, ST_NONFINITE);
 }
 
 // Router epilogue warp: adds the K-block partial sums of its 32 rows in fp32
 // (K-block order, round-to-nearest), then writes the 128 logits of each row
 // that it owns (columns half * 128 .. of the tile; half = 0 for the 128-expert
 // tiles, 0 or 1 for the wide kind's two warps per lane quadrant).
-// The fused kind hands the sums to fused_route_tile instead of writing them.
+// The fused kind also counts the warp towards the tile's readiness.
 template <int KIND>
 __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem,
                                                      int quad, int half, int lane, uint32_t tfull0,
                                                      uint32_t tempty0, uint32_t &kctr, volatile int *abort_flag,
-                                                     uint8_t *stage, unsigned long long limit, FusedCtx &fz,
-                                                     int tile, int ew)
+                                                     uint8_t *stage, unsigned long long limit, int tile)
 {
     using C = GemmCfg<KIND>;
     constexpr int COLS = 128;
@@ -1014,8 +1055,6 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
                 acc[c + i] += __uint_as_float(r[i]);
         }
     }
-    if constexpr (KIND == GK_ROUTER_FUSED)
-        return fused_route_tile(p, ti, tile, acc, quad, half, lane, ew, fz, abort_flag, limit);
     const int valid_rows = ti.rows - quad * 32;
     if (valid_rows > 0) {
         const size_t ld_bytes = (size_t)p.ld_out * 4;
@@ -1042,8 +1081,19 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
             }
         }
     }
+    if constexpr (KIND == GK_ROUTER_FUSED) {
+        // this warp's rows of the tile are stored: count it towards the tile's readiness
+        __threadfence();
+        __syncwarp();
+        if (lane == 0)
+            atomicAdd(p.ready + tile, 1);
+    }
     return true;
 }
+
+static_assert(FP_END + FP_BARS <= GemmCfg<GK_ROUTER_FUSED>::STAGES *
+                                      (GemmCfg<GK_ROUTER_FUSED>::A_BYTES + GemmCfg<GK_ROUTER_FUSED>::B_BYTES),
+              "the fused router's post phase does not fit its stage ring");
 
 template <int KIND>
 __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const __grid_constant__ GemmParams p)
@@ -1074,6 +1124,7 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
     fz.ebar = tqempty0 + 8u * L::TQ;             // (fused router only)
     fz.phase = 0;
     fz.hist = const_cast<int *>(tq + L::TQ);      // (fused router only) L::HIST bytes
+    fz.unit = fz.hist + 256;                      // (fused router only)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1263,7 +1314,7 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
             const TileInfo ti = tile_info<KIND>(p, tile);
             if constexpr (ROUTER) {
                 if (!router_epilogue_tile<KIND>(p, ti, tmem, quad, (warp - 2) >> 2, lane, tfull0, tempty0, ctr,
-                                                abort_flag, stage, limit, fz, tile, (warp - 2) * 32 + lane)) {
+                                                abort_flag, stage, limit, tile)) {
                     fused_ok = false;
                     break;
                 }
@@ -1296,9 +1347,11 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
         if (!ROUTER && lane == 0)
             bulk_wait_group_all();              // this warp's output stores have completed
         if constexpr (L::FUSED) {
-            // every tile's bucket rows are claimed: copy the hidden rows
+            // the CTA's tiles are multiplied (every MMA done, the ring idle):
+            // route and bucket tiles from the shared queue
             if (fused_ok && epi_sync(fz, lane, abort_flag, limit))
-                fused_copy_rows(p, num_tiles, warp - 2, lane, base, C::STAGES * L::STAGE_BYTES, abort_flag, limit);
+                fused_post(p, num_tiles, warp - 2, lane, (warp - 2) * 32 + lane, fz, base_ptr, base,
+                           C::STAGES * L::STAGE_BYTES, abort_flag, limit);
         }
     }
 

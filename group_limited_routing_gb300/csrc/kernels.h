@@ -144,15 +144,15 @@ struct GemmParams {
     int inject_withhold;
     int *tile_ctr;        // GK_WGRAD: tiles claimed so far (zero at launch)
     unsigned long long wait_limit_ns;
-    // GK_ROUTER_FUSED (E = 256 in 8 groups, one token tile per tile, no K split)
+    // GK_ROUTER_FUSED (E = 256 in 8 groups, one token tile per tile, no K split;
+    // out: the logits [T, 256] fp32, read back by the post phase)
     const float *bias;        // expert_bias [E], or NULL
     int32_t *idx_out;         // topk_idx [T, k]
     float *w_out;             // topk_w [T, k]
     int32_t *counts;          // expert_counts [E], zero at launch; also the buckets' fill levels
     int32_t *slot_local;      // [T, k] row of each pair inside its expert's bucket
-    int32_t *dest;            // [token tiles, 128, 8] X_perm row of each pair (scratch)
-    float *gscr;              // [grid, 128, 8] group scores of both halves (scratch)
-    uint32_t *lscr;           // [grid, 128, 2, 24] each half's best k (scratch)
+    int *ready;               // [token tiles] epilogue warps done storing the tile's logits (zero at launch)
+    int *unit_ctr;            // the post phase's tile queue (zero at launch)
     const uint16_t *hidden;   // [T, H], the rows copied into the buckets
     uint16_t *xperm;          // [E * T, H]: expert e's bucket starts at row e * T
     int topk_group, k;

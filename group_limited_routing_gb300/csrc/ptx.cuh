@@ -154,6 +154,13 @@ __device__ __forceinline__ void fence_proxy_async_smem()
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Orders this thread's generic-proxy global accesses (an acquire load of a
+// flag, say) before its later async-proxy (TMA) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global()
+{
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // L2 prefetch of one box (no shared memory, no completion to wait for).
 // c0 is the innermost coordinate in elements; it must be 16-byte aligned.
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int c0, int c1)

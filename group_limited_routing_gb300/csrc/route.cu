@@ -33,6 +33,7 @@
 #include <math.h>
 
 #include "kernels.h"
+#include "route_token.cuh"
 
 namespace glr {
 
@@ -182,10 +183,9 @@ __device__ __forceinline__ float load_logit(const float *__restrict__ logits, si
     return L;
 }
 
-// One warp per token.  Lane l holds experts 32*j + l for j < n_group, so each
-// group lives in one register index across the 32 lanes, and every load of a
-// logits row is a run of 128-byte coalesced accesses.  Group maxima and the
-// top-k arg-max rounds are warp reductions (redux) on the keys above.
+// One warp per token (route_token): lane l holds experts 32*j + l for
+// j < n_group, so every load of a logits row is a run of 128-byte coalesced
+// accesses.
 //
 // Block: 8 warps, `chunk` tokens (route_chunk(T)).  Hits per expert go to a shared-memory
 // histogram and then to `counts` with integer atomics (exact, order-free).
@@ -224,79 +224,16 @@ __global__ void __launch_bounds__(256) route_select_kernel(
     const int t0 = blockIdx.x * chunk;
     const int t1 = min(T, t0 + chunk);
     for (int t = t0 + warp; t < t1; t += 8) {
-        float s[G], b[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-            const float L = load_logit(logits, (size_t)t * E + 32 * j + lane, nparts, part_stride);
-            nonfinite |= !isfinite(L) || !isfinite(bias_r[j]);
-            s[j] = router_sigmoid(L);                 // section 二 step 1
-            b[j] = s[j] + bias_r[j];                  // section 三: choose on s + bias
-        }
-
-        // group score = top-1 + top-2 of the biased scores of the group
-        float g[G];
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-            const uint32_t u = fkey(b[j]);
-            const uint32_t m1 = __reduce_max_sync(FULL, u);
-            const int first = __ffs(__ballot_sync(FULL, u == m1)) - 1;
-            const uint32_t m2 = __reduce_max_sync(FULL, lane == first ? 0u : u);   // best of the others
-            g[j] = fkey_value(m1) + fkey_value(m2);
-        }
-
-        // keep the TG best groups (ties to the lower group index): lane j < G
-        // ranks group j, one ballot collects the verdicts
-        float gl = g[0];
-#pragma unroll
-        for (int j = 1; j < G; ++j)
-            if (lane == j)
-                gl = g[j];
-        int rank = 0;
-#pragma unroll
-        for (int i = 0; i < G; ++i)
-            rank += (g[i] > gl || (g[i] == gl && i < lane)) ? 1 : 0;
-        const uint32_t keep = __ballot_sync(FULL, lane < G && rank < TG) & ((1u << G) - 1u);
-
-        // top-K of the surviving experts: K rounds of (max key, then lowest index)
-        uint32_t kb_[G];
+        float L[G], s[G];
 #pragma unroll
         for (int j = 0; j < G; ++j)
-            kb_[j] = fkey(b[j]);
-        uint32_t avail = keep;   // this lane's candidates not yet taken, by group
-        float den = 0.0f;
-        int my_e = -1;
-        float my_s = 0.0f;
-        for (int r = 0; r < K; ++r) {
-            uint32_t bk = 0;
-            int bj = -1;
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                if (((avail >> j) & 1u) && (bj < 0 || kb_[j] > bk)) {   // ascending j: ties keep the lower index
-                    bk = kb_[j];
-                    bj = j;
-                }
-            }
-            const uint32_t wk = __reduce_max_sync(FULL, bj >= 0 ? bk : 0u);
-            const uint32_t we = __reduce_min_sync(FULL, (bj >= 0 && bk == wk) ? (uint32_t)(32 * bj + lane) : 0xffffffffu);
-            const int wl = (int)(we & 31u), wj = (int)(we >> 5);
-            float sl = 0.0f;
-#pragma unroll
-            for (int j = 0; j < G; ++j)
-                if (j == bj)
-                    sl = s[j];
-            const float sw = __shfl_sync(FULL, sl, wl);   // the winner's unbiased score
-            if (lane == wl)
-                avail &= ~(1u << wj);
-            den += sw;                                    // sequential, in output order
-            if (lane == r) {
-                my_e = (int)we;
-                my_s = sw;
-            }
-        }
-        den += eps;
+            L[j] = load_logit(logits, (size_t)t * E + 32 * j + lane, nparts, part_stride);
+        int my_e;
+        float my_w;
+        route_token<G>(L, bias_r, lane, TG, K, rsf, eps, s, my_e, my_w, nonfinite);
         if (lane < K) {
             idx_out[(size_t)t * K + lane] = my_e;
-            w_out[(size_t)t * K + lane] = (my_s / den) * rsf;   // section 二 step 3
+            w_out[(size_t)t * K + lane] = my_w;
             atomicAdd(&sh_hist[my_e], 1);
         }
 

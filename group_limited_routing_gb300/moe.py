@@ -217,8 +217,9 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
 
 def layer(cfg: MoeConfig, hidden, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
           residual=None, *, W_split=None, flags: int = 0, ws: Optional[Workspace] = None, out=None, routing=None):
-    """moe_layer: routing and the expert stage in one call (the fused router
-    where the shape and T allow, see include/moe.h).  Returns (out, (topk_idx,
+    """moe_layer: routing and the expert stage in one call (with
+    flags=MOE_LAYER_FUSED_ROUTER, the fused router where the shape allows it;
+    see include/moe.h).  Returns (out, (topk_idx,
     topk_w, expert_counts)); `routing` (such a triple) is filled instead of
     allocating."""
     dev = hidden.device

@@ -187,26 +187,26 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
  * bytes (moe_workspace_init() once after allocating it).  Arguments as in
  * those two calls; W_split is moe_prepare_router's output or NULL (then the
  * router weight is split inside the call); topk_idx, topk_w and
- * expert_counts are outputs here.
+ * expert_counts are outputs here.  flags = 0 runs the same kernels as the two
+ * calls.
  *
- * Fused routing.  For E = 256 experts in n_group = 8 groups with k <= 8 (the
- * routing page's setting) and T >= MOE_FUSED_MIN_T, the router's tensor-core
- * kernel also does the rest of routing and the bucketing of section 四: the
- * two threads that hold a token's 256 logits select its experts (the same
- * arithmetic and tie rules as moe_route, so the outputs are identical bit for
- * bit), claim each pair's row in its expert's bucket with one integer atomic
- * per expert and 128-token tile, and copy the hidden rows into the buckets.
- * Bucket e then starts at row e T of a larger activation matrix (E T rows of
- * H bf16 in the workspace: 34 GB at T = 32768, H = 2048), and the order of
- * rows inside a bucket depends on scheduling; each expert row's result does
- * not, and the combine adds every token's rows in a fixed order, so out is
- * deterministic and equal to the unfused path's.  expert_counts are exact.
- * flags: MOE_LAYER_FUSE_ALWAYS takes the fused path for any T where the
- * shape allows it, MOE_LAYER_FUSE_NEVER never; 0 decides by T as above.
- * Returns MOE_ERR_INVALID_ARG for unknown flags. */
-#define MOE_LAYER_FUSE_ALWAYS 1
-#define MOE_LAYER_FUSE_NEVER 2
-#define MOE_FUSED_MIN_T 19456 /* 152 token tiles of 128: one per SM of a GB300 */
+ * flags = MOE_LAYER_FUSED_ROUTER (for E = 256 experts in n_group = 8 groups
+ * with k <= 8, H <= 8192; other shapes ignore it): the router's tensor-core
+ * kernel also does the rest of routing and the bucketing of section 四.
+ * After its own token tiles, each CTA takes finished tiles from a queue,
+ * selects their tokens' experts (the same arithmetic and tie rules as
+ * moe_route, so the outputs are identical bit for bit), claims each pair's
+ * row in its expert's bucket with one integer atomic per expert and tile, and
+ * bulk-copies the hidden rows there.  Bucket e then starts at row e T of a
+ * larger activation matrix in the workspace (E T rows of H bf16: 34 GB at
+ * T = 32768, H = 2048), and the order of rows inside a bucket depends on
+ * scheduling; no row's result does, and the combine adds every token's rows in
+ * a fixed order, so out is deterministic and equal to the unfused path's.
+ * On a GB300 this path measures slower than the unfused kernels (its
+ * selection runs on 8 warps per SM and its row copies follow the
+ * multiplications), so it is not the default.  Unknown flags return
+ * MOE_ERR_INVALID_ARG. */
+#define MOE_LAYER_FUSED_ROUTER 1
 size_t moe_layer_workspace_bytes(const moe_cfg *cfg, int flags);
 int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const moe_bf16 *W_split,
               const float *expert_bias, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,

@@ -1,13 +1,13 @@
 """moe_layer on the GPU: routing and the expert stage in one call.
 
-For the routing page's setting (256 experts in 8 groups, k <= 8) the fused
-router selects the experts in its epilogue, claims the bucket rows with
-integer atomics and copies the hidden rows itself.  Checks: the fused call
-against the two-call path bit for bit where both compute the same logits (the
-256-expert router tiles, T >= 19456), against the CPU oracle (routing under
-the near-tie rules, counts exact, outputs within the layer tolerance with the
-GPU's routing as the oracle's input) where the fused path is forced at small
-and ragged T, exact ties built into the logits, a missing bias, determinism,
+With MOE_LAYER_FUSED_ROUTER, for the routing page's setting (256 experts in
+8 groups, k <= 8), the router kernel also selects the experts, claims the
+bucket rows with integer atomics and copies the hidden rows itself.  Checks:
+the fused call against the two-call path bit for bit where both compute the
+same logits (the 256-expert router tiles, a token tile for every SM), against
+the CPU oracle (routing under the near-tie rules, counts exact, outputs within
+the layer tolerance with the GPU's routing as the oracle's input) at small and
+ragged T, exact ties built into the logits, a missing bias, determinism,
 launch counts and a CUDA-graph replay."""
 import numpy as np
 import pytest
@@ -19,7 +19,7 @@ from parity import assert_output_close, bf16_to_f64, compare_counts, compare_rou
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-ALWAYS, NEVER = _lib.MOE_LAYER_FUSE_ALWAYS, _lib.MOE_LAYER_FUSE_NEVER
+FUSED, PLAIN = _lib.MOE_LAYER_FUSED_ROUTER, 0
 
 
 def u16(t):
@@ -36,15 +36,15 @@ def run_layer(cfg, d, flags, residual=None, bias="layer"):
 
 @pytest.mark.parametrize("T", [32768, 19500])
 def test_fused_layer_matches_two_call_path_bit_for_bit(T):
-    """Same logits (both paths take the 256-expert router tiles here), so the
-    same experts, weights and counts, and the same output bits although the
-    rows inside each bucket come in a scheduling-dependent order."""
+    """Same logits (both paths take the 256-expert router tiles at these T:
+    a token tile for every SM), so the same experts, weights and counts, and
+    the same output bits although the rows inside each bucket come in a
+    scheduling-dependent order."""
     w0 = wl.WORKLOADS[4].with_T(T)
     d = wl.layer_inputs(w0, DEV)
     cfg = moe.MoeConfig(T=T)
-    assert T >= _lib.MOE_FUSED_MIN_T
-    of, i_f, w_f, c_f = run_layer(cfg, d, 0)
-    ou, i_u, w_u, c_u = run_layer(cfg, d, NEVER)
+    of, i_f, w_f, c_f = run_layer(cfg, d, FUSED)
+    ou, i_u, w_u, c_u = run_layer(cfg, d, PLAIN)
     assert torch.equal(i_f, i_u)
     assert torch.equal(w_f, w_u)
     assert torch.equal(c_f, c_u)
@@ -54,13 +54,13 @@ def test_fused_layer_matches_two_call_path_bit_for_bit(T):
 
 @pytest.mark.parametrize("wid,T,nsample", [(1, 128, None), (2, 16, None), (2, 1, None), (3, 4096, 192),
                                            (4, 2000, 160), (5, 129, None), (3, 300, None)])
-def test_forced_fused_layer_matches_oracle(wid, T, nsample):
+def test_fused_layer_matches_oracle(wid, T, nsample):
     w0 = wl.WORKLOADS[wid].with_T(T)
     d = wl.layer_inputs(w0, DEV)
     cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
-    ws = moe.Workspace(cfg, moe.WS_LAYER, DEV, ALWAYS)
+    ws = moe.Workspace(cfg, moe.WS_LAYER, DEV, FUSED)
     out, (idx, w, counts) = moe.layer(cfg, d["hidden"], d["W_router"], d["expert_bias"], d["W_gate_up"],
-                                      d["W_down"], d["shared_gate_up"], d["shared_down"], flags=ALWAYS, ws=ws)
+                                      d["W_down"], d["shared_gate_up"], d["shared_down"], flags=FUSED, ws=ws)
     torch.cuda.synchronize()
     assert ws.status() == 0
     gi, gw, gc = idx.cpu().numpy(), w.cpu().numpy(), counts.cpu().numpy()
@@ -101,7 +101,7 @@ def test_fused_exact_ties_go_to_the_lower_index(topk_group, k):
     d["hidden"] = x.to(DEV)
     d["W_router"] = torch.from_numpy(W).to(DEV)
     cfg = moe.MoeConfig(T=T, H=H, I=128, Is=128, topk_group=topk_group, k=k)
-    out, gi, gw, gc = run_layer(cfg, d, ALWAYS, bias=None)
+    out, gi, gw, gc = run_layer(cfg, d, FUSED, bias=None)
     gi, gw, gc = gi.cpu().numpy(), gw.cpu().numpy(), gc.cpu().numpy()
     L = W[:, hot].T.copy()
     np.testing.assert_array_equal(oracle.router_logits(u16(d["hidden"]), W), L)
@@ -118,7 +118,7 @@ def test_fused_exact_ties_go_to_the_lower_index(topk_group, k):
     assert np.abs(gw[ok].astype(np.float64) - ref["w"][ok]).max() <= 1e-6
     assert np.array_equal(gc, np.bincount(gi.ravel(), minlength=E))
     # the two-call path resolves the same ties the same way
-    _, ui, uw, uc = run_layer(cfg, d, NEVER, bias=None)
+    _, ui, uw, uc = run_layer(cfg, d, PLAIN, bias=None)
     assert np.array_equal(ui.cpu().numpy(), gi) and np.array_equal(uw.cpu().numpy(), gw)
 
 
@@ -128,7 +128,7 @@ def test_fused_layer_without_bias_and_with_residual():
     d = wl.layer_inputs(w0, DEV)
     cfg = moe.MoeConfig(T=T)
     res = torch.randn(T, cfg.H, device=DEV).to(torch.bfloat16)
-    out, gi, gw, gc = run_layer(cfg, d, ALWAYS, residual=res, bias=None)
+    out, gi, gw, gc = run_layer(cfg, d, FUSED, residual=res, bias=None)
     x = u16(d["hidden"])
     ref = oracle.route(oracle.router_logits(x, d["W_router"].cpu().numpy()))
     n_near, near = compare_routing(gi.cpu().numpy(), gw.cpu().numpy(), ref, cfg.E)
@@ -144,13 +144,13 @@ def test_fused_layer_is_deterministic():
     w0 = wl.WORKLOADS[4].with_T(T)
     d = wl.layer_inputs(w0, DEV)
     cfg = moe.MoeConfig(T=T)
-    a = run_layer(cfg, d, ALWAYS)
-    b = run_layer(cfg, d, ALWAYS)
+    a = run_layer(cfg, d, FUSED)
+    b = run_layer(cfg, d, FUSED)
     for u, v in zip(a, b):
         assert torch.equal(u, v)
 
 
-@pytest.mark.parametrize("flags,kernels", [(ALWAYS, 5), (NEVER, 8)])
+@pytest.mark.parametrize("flags,kernels", [(FUSED, 5), (PLAIN, 8)])
 def test_layer_launch_count(flags, kernels):
     # fused: router (+ routing + bucketing), m-tile list, gate/up, down, combine;
     # two-call path: router, selection, hist, scan, scatter, gate/up, down, combine
@@ -171,7 +171,7 @@ def test_graphed_fused_layer_matches_eager():
     d = wl.layer_inputs(w0, DEV)
     cfg = moe.MoeConfig(T=T)
     layer = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"], d["shared_gate_up"],
-                         d["shared_down"], single_call=True, flags=ALWAYS)
+                         d["shared_down"], single_call=True, flags=FUSED)
     g = moe.GraphedStep(layer, d["hidden"])
     for seed in range(3):
         x = (torch.randn(T, cfg.H, device=DEV, generator=torch.Generator(DEV).manual_seed(seed))).to(torch.bfloat16)
@@ -189,4 +189,4 @@ def test_layer_rejects_unknown_flags():
     cfg = moe.MoeConfig(T=T)
     with pytest.raises(_lib.MoeError):
         moe.layer(cfg, d["hidden"], d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
-                  d["shared_gate_up"], d["shared_down"], flags=4, ws=moe.Workspace(cfg, moe.WS_LAYER, DEV, 0))
+                  d["shared_gate_up"], d["shared_down"], flags=2, ws=moe.Workspace(cfg, moe.WS_LAYER, DEV, 0))
