@@ -77,6 +77,11 @@ constexpr int ROUTER_PF = 6;
 __host__ __device__ constexpr int epi_warps(int kind) { return wide_router(kind) ? 8 : 4; }
 __host__ __device__ constexpr int kind_threads(int kind) { return 64 + 32 * epi_warps(kind); }
 
+// the fused router's extra barriers: the epilogue warps' meeting, the logits'
+// staging load, the two row tables' full and empty, the copy engine's slots
+constexpr int FUSED_ENGINE_SLOTS = 16;                  // rows in flight in the copy engine at most
+constexpr int FUSED_BARS = 1 + 1 + 2 + 2 + FUSED_ENGINE_SLOTS;
+
 template <>
 struct GemmCfg<GK_ROUTER> {
     static constexpr int BN = 128;                     // experts per tile
@@ -216,9 +221,9 @@ struct GemmLayout {
     static constexpr int TQ = DYN ? TQ_RING : 0;
     // the fused router's epilogue barrier and per-tile bucket histogram
     static constexpr bool FUSED = (KIND == GK_ROUTER_FUSED);
-    static constexpr int HIST = FUSED ? 256 * 4 + 16 : 0;
+    static constexpr int HIST = FUSED ? 256 * 4 + 16 + 16 : 0;   // histogram, queue slot, mailbox
     // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin, tq_full[TQ], tq_empty[TQ] (, epi)
-    static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1 + 2 * TQ + (FUSED ? 1 : 0);
+    static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1 + 2 * TQ + (FUSED ? FUSED_BARS : 0);
     static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16 + TQ * 4 + HIST;
     static_assert(SMEM <= 232448, "more than 227 KB of shared memory");
     static_assert(C::A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms need 1024-B alignment");
@@ -673,6 +678,11 @@ struct FusedCtx {
     uint32_t phase;   // phases completed so far
     int *hist;        // smem [256]: a tile's hits per expert, then the bucket bases
     int *unit;        // smem: the tile the CTA took from the queue
+    int2 *mail;       // smem [2]: (first token, rows) of the tile in each row table; first < 0: done
+    uint32_t stage;   // barrier of the logits' staging load
+    uint32_t dfull;   // [2] a row table is filled (epilogue -> copy engine)
+    uint32_t dempty;  // [2] a row table is read (copy engine -> epilogue)
+    uint32_t eslot;   // [FUSED_ENGINE_SLOTS] the copy engine's row loads
 };
 
 // The eight epilogue warps meet; shared-memory writes made before are visible
@@ -716,19 +726,19 @@ __device__ __forceinline__ bool wait_tile_ready(const int *ready, volatile int *
 }
 
 // Post-phase shared memory, carved from the idle stage ring (bytes):
-//   [0, 128 K)        the tile's logits, then their scores, [128][256] fp32;
-//                     afterwards each warp's FUSED_SLOTS hidden-row slots
+//   [0, 128 K)   the tile's logits, then their scores, [128][256] fp32;
 //   group scores [128][8] fp32, the halves' lists [128][2][3 FUSED_MAX_K],
-//   the pairs' bucket rows [128][FUSED_MAX_K], the bias [256];
-//   at the ring's end the barriers of the staging load and of the row slots.
-constexpr int FUSED_SLOTS = 4;
+//   two tables of the pairs' bucket rows [2][128][FUSED_MAX_K] (one being
+//   filled by the epilogue while the copy engine reads the other), the bias
+//   [256]; from FP_SLOTS to the ring's end the copy engine's row slots.
+// Their barriers live with the kernel's others (FusedCtx).
 constexpr uint32_t FP_LOGITS = 0;
 constexpr uint32_t FP_GROUPS = GEMM_BM * 256 * 4;
 constexpr uint32_t FP_LISTS = FP_GROUPS + GEMM_BM * 8 * 4;
 constexpr uint32_t FP_DEST = FP_LISTS + GEMM_BM * 2 * 3 * FUSED_MAX_K * 4;
-constexpr uint32_t FP_BIAS = FP_DEST + GEMM_BM * FUSED_MAX_K * 4;
+constexpr uint32_t FP_BIAS = FP_DEST + 2 * GEMM_BM * FUSED_MAX_K * 4;
 constexpr uint32_t FP_END = FP_BIAS + 256 * 4;
-constexpr uint32_t FP_BARS = 8 * (1 + 8 * FUSED_SLOTS);   // staging + 8 warps' slot barriers
+constexpr uint32_t FP_SLOTS = (FP_END + 1023u) & ~1023u;
 
 // The post phase of one CTA.  All 256 epilogue threads (ew = 0..255, warp
 // w = ew / 32) take tiles from the queue; per tile, thread (h = ew / 128,
@@ -749,32 +759,34 @@ __device__ __forceinline__ void fused_post(const GemmParams &p, int num_tiles, i
     float *sl = reinterpret_cast<float *>(ring_ptr + FP_LOGITS);
     float *sg = reinterpret_cast<float *>(ring_ptr + FP_GROUPS);
     uint32_t *sls = reinterpret_cast<uint32_t *>(ring_ptr + FP_LISTS);
-    int *sdst = reinterpret_cast<int *>(ring_ptr + FP_DEST);
     float *sbias = reinterpret_cast<float *>(ring_ptr + FP_BIAS);
-    const uint32_t stage_bar = ring + ring_bytes - FP_BARS;
-    const uint32_t bar0 = stage_bar + 8u + (uint32_t)w * FUSED_SLOTS * 8;
-    const uint32_t rowbytes = (uint32_t)p.H * 2;
-    const int ns = min((int)(GEMM_BM * 256 * 4 / 8 / rowbytes), FUSED_SLOTS);   // >= 1: the host keeps H <= 8192
-    const uint32_t my = ring + FP_LOGITS + (uint32_t)w * (GEMM_BM * 256 * 4 / 8);
-    if (lane == 0) {
-        fence_proxy_async_smem();             // the ring was last written by TMA loads
-        if (ew == 0)
-            mbar_init(stage_bar, 1);
-        for (int b = 0; b < ns; ++b)
-            mbar_init(bar0 + 8u * b, 1);
-        fence_mbar_init();
-    }
+    const uint32_t stage_bar = fz.stage;
+    (void)ring_bytes;
     sbias[ew] = p.bias ? __ldg(p.bias + ew) : 0.0f;
-    uint32_t stage_par = 0, parity = 0;      // parity: bit b = slot b's next completion (lane 0)
+    uint32_t stage_par = 0;
     bool nonfinite = false;
-    for (;;) {
-        if (ew == 0)
-            *fz.unit = atomicAdd(p.unit_ctr, 1);
+    for (int nunit = 0;; ++nunit) {
+        const int buf = nunit & 1;
+        if (ew == 0) {
+            // the row table this tile will fill must have been read by the copy engine
+            if (nunit >= 2 && !mbar_wait(fz.dempty + 8u * buf, ((nunit >> 1) - 1) & 1u, abort_flag, limit))
+                *fz.unit = -1;
+            else
+                *fz.unit = atomicAdd(p.unit_ctr, 1);
+        }
         if (!epi_sync(fz, lane, abort_flag, limit))
             break;
         const int u = *fz.unit;
-        if (u >= num_tiles)
+        if (u < 0)
             break;
+        if (u >= num_tiles) {
+            if (ew == 0) {
+                fz.mail[buf] = make_int2(-1, 0);   // no more tiles for the copy engine
+                mbar_arrive(fz.dfull + 8u * buf);
+            }
+            break;
+        }
+        int *sdst = reinterpret_cast<int *>(ring_ptr + FP_DEST) + buf * GEMM_BM * FUSED_MAX_K;
         const int row0 = u * GEMM_BM;
         const int rows = min(GEMM_BM, p.T - row0);
         if (ew == 0) {
@@ -964,45 +976,72 @@ __device__ __forceinline__ void fused_post(const GemmParams &p, int num_tiles, i
             break;
         fz.hist[ew] = 0;                          // every base is read: clear for the next tile
 
-        // copy the hidden rows of tokens w, w + 8, ...: lane 0 loads up to ns
-        // of them into the warp's slots, then stores each to its bucket rows
-        bool cok = true;
-        if (lane == 0) {
-            const int ntok = (rows - w + 7) / 8;
-            for (int i0 = 0; i0 < ntok && cok; i0 += ns) {
-                const int nb = min(ns, ntok - i0);
-                for (int b = 0; b < nb; ++b) {
-                    const int t = row0 + w + 8 * (i0 + b);
-                    mbar_arrive_expect_tx(bar0 + 8u * b, rowbytes);
-                    bulk_load_g2s(my + (uint32_t)b * rowbytes, p.hidden + (size_t)t * p.H, rowbytes, bar0 + 8u * b);
-                }
-                for (int b = 0; b < nb; ++b) {
-                    const uint32_t bar = bar0 + 8u * b;
-                    if (cok && !mbar_wait(bar, (parity >> b) & 1u, abort_flag, limit))
-                        cok = false;
-                    if (!cok)
-                        mbar_drain(bar, (parity >> b) & 1u);   // let its load land, then stop
-                    parity ^= 1u << b;
-                    if (!cok)
-                        continue;
-                    const int rr = w + 8 * (i0 + b);
-                    for (int j = 0; j < K; ++j) {
-                        const int d = sdst[rr * FUSED_MAX_K + j];
-                        if (d >= 0)
-                            bulk_store_s2g(p.xperm + (size_t)d * p.H, my + (uint32_t)b * rowbytes, rowbytes);
-                    }
-                }
-                bulk_commit_group();
-                bulk_wait_group_read<0>();        // the slots may be refilled
-            }
+        // hand the row table to the copy engine (the producer warp's lane 0)
+        if (ew == 0) {
+            fz.mail[buf] = make_int2(row0, rows);
+            mbar_arrive(fz.dfull + 8u * buf);
         }
-        if (!__shfl_sync(0xffffffffu, cok ? 1 : 0, 0))
-            break;
     }
-    if (lane == 0)
-        bulk_wait_group_all();
     if (__any_sync(0xffffffffu, nonfinite) && lane == 0)
         atomicOr(p.status, ST_NONFINITE);
+}
+
+// The copy engine: the producer warp's lane 0, once its loads are issued.
+// For every tile the epilogue warps route (in their order), it loads the
+// tokens' hidden rows into its slots at the ring's end and stores each to its
+// pairs' bucket rows, so the copies of one tile overlap the routing of the
+// next.  Bounded waits; on a failed one it lets its loads in flight land and
+// stops.
+__device__ __forceinline__ void fused_copy_engine(const GemmParams &p, uint8_t *ring_ptr, uint32_t ring,
+                                                 uint32_t ring_bytes, const FusedCtx &fz,
+                                                 volatile int *abort_flag, unsigned long long limit)
+{
+    const uint32_t rowbytes = (uint32_t)p.H * 2;
+    const int ns = min((int)((ring_bytes - FP_SLOTS) / rowbytes), FUSED_ENGINE_SLOTS);   // >= 1: H <= 8192
+    const int K = p.k;
+    uint32_t parity = 0;                      // bit b: parity of slot b's next completion
+    for (int n = 0;; ++n) {
+        const int buf = n & 1;
+        if (!mbar_wait(fz.dfull + 8u * buf, (n >> 1) & 1u, abort_flag, limit))
+            break;
+        const int2 m = fz.mail[buf];
+        if (m.x < 0)
+            break;
+        const int *sdst = reinterpret_cast<const int *>(ring_ptr + FP_DEST) + buf * GEMM_BM * FUSED_MAX_K;
+        bool ok = true;
+        for (int i0 = 0; i0 < m.y && ok; i0 += ns) {
+            const int nb = min(ns, m.y - i0);
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t bar = fz.eslot + 8u * b;
+                mbar_arrive_expect_tx(bar, rowbytes);
+                bulk_load_g2s(ring + FP_SLOTS + (uint32_t)b * rowbytes, p.hidden + (size_t)(m.x + i0 + b) * p.H,
+                              rowbytes, bar);
+            }
+            for (int b = 0; b < nb; ++b) {
+                const uint32_t bar = fz.eslot + 8u * b;
+                if (ok && !mbar_wait(bar, (parity >> b) & 1u, abort_flag, limit))
+                    ok = false;
+                if (!ok)
+                    mbar_drain(bar, (parity >> b) & 1u);   // let its load land
+                parity ^= 1u << b;
+                if (!ok)
+                    continue;
+                const int *dr = sdst + (i0 + b) * FUSED_MAX_K;
+                for (int j = 0; j < K; ++j) {
+                    const int d = dr[j];
+                    if (d >= 0)
+                        bulk_store_s2g(p.xperm + (size_t)d * p.H, ring + FP_SLOTS + (uint32_t)b * rowbytes,
+                                       rowbytes);
+                }
+            }
+            bulk_commit_group();
+            bulk_wait_group_read<0>();            // the slots may be refilled
+        }
+        if (!ok)
+            break;
+        mbar_arrive(fz.dempty + 8u * buf);        // this row table is read
+    }
+    bulk_wait_group_all();
 }
 
 // Router epilogue warp: adds the K-block partial sums of its 32 rows in fp32
@@ -1091,7 +1130,7 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
     return true;
 }
 
-static_assert(FP_END + FP_BARS <= GemmCfg<GK_ROUTER_FUSED>::STAGES *
+static_assert(FP_SLOTS + 8192 * 2 <= GemmCfg<GK_ROUTER_FUSED>::STAGES *
                                       (GemmCfg<GK_ROUTER_FUSED>::A_BYTES + GemmCfg<GK_ROUTER_FUSED>::B_BYTES),
               "the fused router's post phase does not fit its stage ring");
 
@@ -1125,6 +1164,11 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
     fz.phase = 0;
     fz.hist = const_cast<int *>(tq + L::TQ);      // (fused router only) L::HIST bytes
     fz.unit = fz.hist + 256;                      // (fused router only)
+    fz.mail = reinterpret_cast<int2 *>(fz.hist + 260);
+    fz.stage = fz.ebar + 8u;
+    fz.dfull = fz.stage + 8u;
+    fz.dempty = fz.dfull + 16u;
+    fz.eslot = fz.dempty + 16u;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1143,8 +1187,16 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
             mbar_init(tqfull0 + 8u * i, 1);
             mbar_init(tqempty0 + 8u * i, TQ_TAKERS);
         }
-        if constexpr (L::FUSED)
+        if constexpr (L::FUSED) {
             mbar_init(fz.ebar, epi_warps(KIND));
+            mbar_init(fz.stage, 1);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(fz.dfull + 8u * b, 1);
+                mbar_init(fz.dempty + 8u * b, 1);
+            }
+            for (int b = 0; b < FUSED_ENGINE_SLOTS; ++b)
+                mbar_init(fz.eslot + 8u * b, 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_map(&p.tmA0);
@@ -1239,6 +1291,12 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
                 for (int s = 0; s < C::STAGES; ++s)
                     if ((issued >> s) & 1u)
                         mbar_drain(full_bar(s), (issued_parity >> s) & 1u);
+            }
+            if constexpr (L::FUSED) {
+                // the fused router's hidden-row copies, tile by tile as the
+                // epilogue warps route them
+                if (ok)
+                    fused_copy_engine(p, base_ptr, base, C::STAGES * L::STAGE_BYTES, fz, abort_flag, limit);
             }
         }
     } else if (warp == 1) {
