@@ -166,6 +166,9 @@ def algorithmic_work(T, H, E, I, k, hit=None, Is=None):
         "router_gemm": dict(bound="hbm" if T <= 32 else "tensor", flops=2.0 * T * E * H,
                             bytes=T * H * 2 + E * H * 4 + T * E * 4),
         "route_select": dict(bound="hbm", bytes=T * E * 4 + T * k * 8),
+        # the fused router: the router's hidden and weight reads, the routing
+        # outputs, the pairs' bucket rows and the copied rows
+        "router_route_bucket": dict(bound="hbm", bytes=T * H * 2 + E * H * 4 + T * k * 8 + T * k * 4 + kT * H * 2),
         "bucket_scatter": dict(bound="hbm", bytes=T * k * 4 * 2 + T * H * 2 + kT * H * 2),
         "gemm_gate_up_swiglu": dict(flops=2.0 * kT * H * 2 * I + 2.0 * T * H * 2 * Is,
                                     bytes=(kT + T) * H * 2 + (hit * I + Is) * 2 * H * 2 + kT * I * 2 + T * Is * 2),
@@ -308,9 +311,11 @@ def backward_work(T, H, E, I, k):
     }
 
 
-def build_model(w0, dev, dense_inter=0):
+def build_model(w0, dev, dense_inter=0, fused_router=False):
     """The step's model: one MoE layer, the 19-layer stack of workload 5, or
-    (dense_inter > 0) the dense first-layer MLP of that intermediate size."""
+    (dense_inter > 0) the dense first-layer MLP of that intermediate size.
+    fused_router: one moe_layer call per step with the fused router (routing
+    and bucketing inside the router kernel) instead of moe_route + moe_forward."""
     from group_limited_routing_gb300 import moe, workloads as wl
 
     if dense_inter:
@@ -322,6 +327,14 @@ def build_model(w0, dev, dense_inter=0):
 
     cfg = moe.MoeConfig(T=w0.T, H=w0.H, E=w0.E, n_group=w0.n_group, topk_group=w0.topk_group, k=w0.k, I=w0.I,
                         Is=w0.Is)
+    if fused_router:
+        if w0.layers > 1:
+            raise SystemExit("--fused-router runs single layers (the stack needs the balance loss)")
+        from group_limited_routing_gb300 import _lib
+        d = wl.layer_inputs(w0, dev)
+        return cfg, moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
+                                 d["shared_gate_up"], d["shared_down"], single_call=True,
+                                 flags=_lib.MOE_LAYER_FUSED_ROUTER)
     ws_r = moe.Workspace(cfg, 0, dev)
     ws_f = moe.Workspace(cfg, 1, dev)
     layers = []
@@ -344,7 +357,7 @@ def run_ours(args, world, rank, local):
     if args.tokens:
         w0 = w0.with_T(args.tokens)
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
-    cfg, layer = build_model(w0, dev, args.dense)
+    cfg, layer = build_model(w0, dev, args.dense, args.fused_router)
     x = wl.hidden(w0, dev, layer=rank)      # each replica its own batch
     if args.backward:
         layer = BackwardStep(layer, x)
@@ -515,7 +528,7 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
         stages[name] = st
     # router + permute as one HBM stage
     rp_names = ("split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist", "bucket_scan",
-                "bucket_scatter")
+                "bucket_scatter", "router_route_bucket", "bucket_tiles")
     rp_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in rp_names if n in stages)
     rp_bytes = T * H * 2 + E * H * 4 + T * k * 8 + T * k * 4 * 2 + T * H * 2 + k * T * H * 2
     if extra["backward"]:
@@ -582,6 +595,8 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
                           if extra["flush"] else
                           "expert weights (%.2f GB per layer) larger than L2, no flush" % (3 * E * I * H * 2 / 1e9)),
                    "untimed_lead_in_steps": extra["lead"],
+                   "path": ("moe_layer with the fused router (routing and bucketing in the router kernel)"
+                            if getattr(args, "fused_router", False) else "moe_route + moe_forward"),
                    "hot_expert_share": None if extra["hot_share"] is None else round(extra["hot_share"], 4)},
         "roofline": {"kernel": dom, "bound": g1["bound"], "achieved": round(g1_ach, 1),
                      "peak": g1_peak, "unit": g1_unit,
@@ -685,6 +700,8 @@ def main():
                     help="1 tiny, 2 decode T=16, 3 T=4096, 4 T=32768 skewed (the bench line), 5 19-layer stack")
     ap.add_argument("--lead-in-ms", type=float, default=500.0,
                     help="untimed loaded steps before the timed region (0: one step; for profiling captures)")
+    ap.add_argument("--fused-router", action="store_true",
+                    help="one moe_layer call per step with routing and bucketing fused into the router kernel")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step (default: the workload's 32768); smaller sizes for profiling captures")
     args = ap.parse_args()
