@@ -740,8 +740,8 @@ constexpr uint32_t FP_BIAS = FP_DEST + 2 * GEMM_BM * FUSED_MAX_K * 4;
 constexpr uint32_t FP_END = FP_BIAS + 256 * 4;
 constexpr uint32_t FP_SLOTS = (FP_END + 1023u) & ~1023u;
 
-// The post phase of one CTA.  All 256 epilogue threads (ew = 0..255, warp
-// w = ew / 32) take tiles from the queue; per tile, thread (h = ew / 128,
+// The post phase of one CTA.  All 256 epilogue threads (ew = 0..255) take
+// tiles from the queue; per tile, thread (h = ew / 128,
 // r = ew % 128) holds token r's experts 128 h .. 128 h + 127 (groups
 // 4 h .. 4 h + 3) and reads them from shared memory starting at column
 // r % 32, so the 32 lanes of a warp hit 32 different banks.  The arithmetic
@@ -749,9 +749,9 @@ constexpr uint32_t FP_SLOTS = (FP_END + 1023u) & ~1023u;
 // (the two best biased scores, a repeated best counting twice), group ranking,
 // winner order (key desc, expert asc) and sequential normaliser, so the
 // results are bit-identical to routing the same logits there.
-__device__ __forceinline__ void fused_post(const GemmParams &p, int num_tiles, int w, int lane, int ew, FusedCtx &fz,
-                                          uint8_t *ring_ptr, uint32_t ring, uint32_t ring_bytes,
-                                          volatile int *abort_flag, unsigned long long limit)
+__device__ __forceinline__ void fused_post(const GemmParams &p, int num_tiles, int lane, int ew, FusedCtx &fz,
+                                          uint8_t *ring_ptr, uint32_t ring, volatile int *abort_flag,
+                                          unsigned long long limit)
 {
     const int K = p.k;
     const int h = ew >> 7, r = ew & 127;
@@ -761,7 +761,6 @@ __device__ __forceinline__ void fused_post(const GemmParams &p, int num_tiles, i
     uint32_t *sls = reinterpret_cast<uint32_t *>(ring_ptr + FP_LISTS);
     float *sbias = reinterpret_cast<float *>(ring_ptr + FP_BIAS);
     const uint32_t stage_bar = fz.stage;
-    (void)ring_bytes;
     sbias[ew] = p.bias ? __ldg(p.bias + ew) : 0.0f;
     uint32_t stage_par = 0;
     bool nonfinite = false;
@@ -790,8 +789,8 @@ __device__ __forceinline__ void fused_post(const GemmParams &p, int num_tiles, i
         const int row0 = u * GEMM_BM;
         const int rows = min(GEMM_BM, p.T - row0);
         if (ew == 0) {
-            // every slot's stores have read the ring (each warp waited before the
-            // meeting above): stage the tile's logits once its CTA has stored them
+            // every thread is done with the previous tile's scores (the meeting
+            // above): stage this tile's logits once its CTA has stored them
             bool ok = wait_tile_ready(p.ready + u, abort_flag, limit);
             if (ok) {
                 fence_proxy_async_global();       // the logits were stored by generic writes
@@ -1408,8 +1407,7 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
             // the CTA's tiles are multiplied (every MMA done, the ring idle):
             // route and bucket tiles from the shared queue
             if (fused_ok && epi_sync(fz, lane, abort_flag, limit))
-                fused_post(p, num_tiles, warp - 2, lane, (warp - 2) * 32 + lane, fz, base_ptr, base,
-                           C::STAGES * L::STAGE_BYTES, abort_flag, limit);
+                fused_post(p, num_tiles, lane, (warp - 2) * 32 + lane, fz, base_ptr, base, abort_flag, limit);
         }
     }
 
