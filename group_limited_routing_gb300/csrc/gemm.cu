@@ -36,9 +36,11 @@
 //
 // Roles (192 threads, 320 for the 256-expert routers; one CTA per SM):
 //   warp 0, one lane : TMA producer, fills a STAGES-deep ring of smem stages
+//                      (the fused router: then the copy engine of the rows)
 //   warp 1           : allocates TMEM; one lane issues tcgen05.mma and commits
 //   warps 2..5 (..9) : epilogue, TMEM -> registers -> global; warp w reads TMEM
 //                      lanes 32*(w%4) .. +31 (the lane quadrant it may access)
+//                      (the fused router: then the routing of queued tiles)
 // TMEM holds SLOTS accumulators: two whole-tile accumulators for the grouped
 // GEMMs (the epilogue of one tile overlaps the MMAs of the next), four K-block
 // slots for the router.  Tiles are 128 rows x BN columns; CTAs walk the tile
