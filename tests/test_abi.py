@@ -153,3 +153,22 @@ def test_dense_workspace_bytes(lib):
     assert lib.moe_dense_workspace_bytes(1000, 2000, 4608) == 0     # H % 256
     assert lib.moe_dense_workspace_bytes(0, 2048, 4608) == 0
     assert lib.moe_dense_workspace_bytes(2000, 2048, 4608) > f
+
+
+def test_layer_workspace_bytes(lib):
+    """moe_layer's workspace holds both calls' regions; the fused router's
+    buckets (E T rows of X_perm instead of k T) only when asked for and where
+    the shape allows it; unknown shapes give 0."""
+    c = cfg(T=1024)
+    r = lib.moe_workspace_bytes(ctypes.byref(c), _lib.MOE_WS_ROUTE)
+    f = lib.moe_workspace_bytes(ctypes.byref(c), _lib.MOE_WS_FORWARD)
+    plain = lib.moe_layer_workspace_bytes(ctypes.byref(c), 0)
+    fused = lib.moe_layer_workspace_bytes(ctypes.byref(c), _lib.MOE_LAYER_FUSED_ROUTER)
+    assert plain >= r + f - 256
+    assert fused - plain >= (256 - 8) * 1024 * 2048 * 2
+    # 4 groups of 32: not the fused router's shape, the flag changes nothing
+    c4 = cfg(T=1024, E=128, n_group=4, topk_group=2)
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(c4), _lib.MOE_LAYER_FUSED_ROUTER) == \
+        lib.moe_layer_workspace_bytes(ctypes.byref(c4), 0) > 0
+    assert lib.moe_layer_workspace_bytes(ctypes.byref(cfg(H=100)), 0) == 0
+    assert lib.moe_layer_workspace_bytes(None, 0) == 0
