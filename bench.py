@@ -267,6 +267,48 @@ class CpuSample:
         return n_tokens / dt / self.layers, o.max_threads(), dt
 
 
+def routing_parity(x, layer, tol=1e-5):
+    """The bench batch's routing against the CPU oracle's, over every token
+    (part of the CPU-oracle leg: the oracle recomputes the fp32 logits and the
+    selection from the GPU run's own inputs).  Tokens whose oracle margin at
+    the group (4th/5th) or expert (8th/9th) boundary is below tol are counted
+    as near ties; tokens whose chosen set is clear but whose order inside it
+    hangs on a gap below tol, as order ties; each class with how many of its
+    tokens the GPU answered differently.  `exact_elsewhere` is whether every
+    other token's indices are bit-identical."""
+    import oracle
+
+    def u16(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    if getattr(layer, "layers", None):
+        layer = layer.layers[0]          # a stack: its first layer sees the bench input itself
+    if getattr(layer, "routing", None) is None:
+        return None
+    t0 = time.perf_counter()
+    bias = None if layer.expert_bias is None else layer.expert_bias.detach().cpu().numpy()
+    L = oracle.router_logits(u16(x), layer.W_router.detach().cpu().numpy())
+    c = layer.cfg
+    ref = oracle.route(L, bias=bias, n_group=c.n_group, topk_group=c.topk_group, k=c.k, rsf=c.rsf, eps=c.eps)
+    gi = layer.routing[0].cpu().numpy()
+    gw = layer.routing[1].cpu().numpy().astype(np.float64)
+    near = (ref["margin_group"] < tol) | (ref["margin_expert"] < tol)
+    b = (ref["scores"] + (np.float32(0) if bias is None else bias.astype(np.float32))).astype(np.float32)
+    bs = np.take_along_axis(b, ref["idx"].astype(np.int64), axis=1).astype(np.float64)
+    order = (~near) & ((bs[:, :-1] - bs[:, 1:]).min(axis=1) < tol) if c.k > 1 else np.zeros_like(near)
+    rest = ~near & ~order
+    differs = (gi != ref["idx"]).any(axis=1)
+    T = gi.shape[0]
+    return {"tokens": int(T), "tol": tol,
+            "near_tie_tokens": int(near.sum()), "near_tie_pct": round(100.0 * near.sum() / T, 4),
+            "near_tie_differ": int((near & differs).sum()),
+            "order_tie_tokens": int(order.sum()), "order_tie_pct": round(100.0 * order.sum() / T, 4),
+            "order_tie_differ": int((order & differs).sum()),
+            "exact_elsewhere": bool(not differs[rest].any()),
+            "max_w_err_elsewhere": float(np.abs(gw[rest] - ref["w"][rest]).max()) if rest.any() else 0.0,
+            "oracle_s": round(time.perf_counter() - t0, 1)}
+
+
 # ------------------------------------------------------------------- ours
 class BackwardStep:
     """The layer's backward as the timed step: routing and d_out fixed (one
@@ -458,9 +500,13 @@ def run_ours(args, world, rank, local):
     moe_layers = getattr(layer, "layers", None) or [layer]
     hits = [int((l.routing[2] > 0).sum().item()) for l in moe_layers if getattr(l, "routing", None) is not None]
     hit = statistics.mean(hits) if hits else None
-    return report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk,
+    line = report(args, world, w0, ms_max, prof, nprof * w0.layers, e2e_ms, launches, clk,
                   dict(flush=flush, lead=lead, hot_share=hot_share, graph_ms=graph_ms, dense=args.dense,
                        backward=args.backward, hit=hit))
+    if world == 1 and not args.no_cpu_baseline and not args.dense and not args.backward:
+        # the CPU-oracle leg also checks the timed batch's routing, token by token
+        line["parity"] = routing_parity(x, layer)
+    return line
 
 
 def time_e2e(args, world, layer, x, out, stream, dev):

@@ -692,6 +692,21 @@ int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *
     return rc;
 }
 
+int moe_router_scores(const float *logits, float *scores, int64_t n, void *stream)
+{
+    if (!logits || !scores || n < 1)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(logits, 4) || !aligned(scores, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0, rc = MOE_OK;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    if (launch_router_scores(logits, scores, (long long)n, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    g_last_launches = 1;
+    return MOE_OK;
+}
+
 int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const float *expert_bias,
               int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss, void *ws,
               size_t ws_bytes, void *stream)
@@ -1258,26 +1273,75 @@ const char *moe_strerror(int code)
 static __device__ __align__(256) unsigned char g_route_static_scratch[MOE_ROUTE_STATIC_SCRATCH_BYTES];
 
 static std::mutex g_static_mu;
-static void *g_static_addr[64];   // device address of the array, per device
 
-// Device address of the array on the current device, looked up once per
-// device with that device current (host code only ever sees a stand-in for
-// the symbol, so it must never hand `g_route_static_scratch` to a kernel).
+// A __device__ array has one address per CUDA context, not per device: a host
+// that makes its own driver context current, or a process that resets the
+// device, sees a new address.  So the looked-up address is cached per context,
+// keyed by the driver's unique context id (never reused within a process).
+struct StaticAddr {
+    unsigned long long ctx_id;
+    void *addr;
+};
+static StaticAddr g_static_addr[64];
+static int g_static_n = 0, g_static_next = 0;
+
+typedef CUresult (*PFN_ctx_get_current)(CUcontext *);
+typedef CUresult (*PFN_ctx_get_id)(CUcontext, unsigned long long *);
+
+// id of the context current on this thread; false when there is none yet
+static bool current_ctx_id(unsigned long long *id)
+{
+    static PFN_ctx_get_current get_cur = nullptr;
+    static PFN_ctx_get_id get_id = nullptr;
+    static bool looked_up = false;
+    if (!looked_up) {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &r1) == cudaSuccess &&
+            r1 == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) == cudaSuccess &&
+            r2 == cudaDriverEntryPointSuccess) {
+            get_cur = reinterpret_cast<PFN_ctx_get_current>(p);
+            get_id = reinterpret_cast<PFN_ctx_get_id>(q);
+        }
+        looked_up = true;
+    }
+    if (!get_cur || !get_id)
+        return false;
+    CUcontext c = nullptr;
+    if (get_cur(&c) != CUDA_SUCCESS || !c)
+        return false;
+    return get_id(c, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current context.  The first call in a
+// context looks it up with cudaGetSymbolAddress (host code only ever sees a
+// stand-in for the symbol, so it must never hand `g_route_static_scratch` to a
+// kernel); later calls in the same context reuse it.
 static int static_scratch(void **addr)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (dev < 0 || dev >= 64)
-        return MOE_ERR_UNSUPPORTED_DEVICE;
     std::lock_guard<std::mutex> g(g_static_mu);
-    if (!g_static_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_route_static_scratch) != cudaSuccess || !p)
-            return MOE_ERR_CUDA;
-        g_static_addr[dev] = p;
+    unsigned long long id = 0;
+    if (current_ctx_id(&id)) {
+        for (int i = 0; i < g_static_n; ++i)
+            if (g_static_addr[i].ctx_id == id) {
+                *addr = g_static_addr[i].addr;
+                return MOE_OK;
+            }
     }
-    *addr = g_static_addr[dev];
+    // set-up in this context (the lookup also makes the runtime's context
+    // current when none was)
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_route_static_scratch) != cudaSuccess || !p)
+        return MOE_ERR_CUDA;
+    if (!current_ctx_id(&id))
+        return MOE_ERR_CUDA;
+    const int slot = g_static_n < 64 ? g_static_n++ : (g_static_next++ & 63);
+    g_static_addr[slot] = StaticAddr{id, p};
+    *addr = p;
     return MOE_OK;
 }
 

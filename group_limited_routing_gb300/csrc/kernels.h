@@ -176,6 +176,9 @@ constexpr int ROUTER_SIMT_MAX_T = 32;   // decode sizes; the tensor-core path wi
 cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, int H, float *logits,
                                int32_t *counts, cudaStream_t s);
 
+// scores[i] = router_sigmoid(logits[i]) (n > 0)
+cudaError_t launch_router_scores(const float *logits, float *scores, long long n, cudaStream_t s);
+
 // counts[E] must be zero (or hold counts to add to) before the launch.
 // logits: nparts partial-sum buffers of [T, E], part_stride floats apart (the
 // router GEMM's K parts; 1 part: plain logits), nparts <= ROUTER_MAX_KSPLIT

@@ -32,6 +32,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 #include "route_token.cuh"
 
@@ -157,6 +159,25 @@ cudaError_t launch_router_simt(const uint16_t *x, const float *W, int T, int E, 
         return cudaErrorInvalidValue;
     const cudaError_t le = launch_pdl(router_simt_kernel, dim3(E), dim3(SIMT_THREADS), 0, s, x, W, T, E, H, logits,
                                       counts);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
+// The routing kernels' sigmoid over a flat array (a diagnostic: the scores
+// the selection ranks, for comparison with an exact sigmoid).
+__global__ void router_scores_kernel(const float *__restrict__ L, float *__restrict__ s, long long n)
+{
+    pdl_wait();
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+        s[i] = router_sigmoid(L[i]);
+}
+
+cudaError_t launch_router_scores(const float *L, float *s, long long n, cudaStream_t st)
+{
+    const long long blocks = std::min<long long>((n + 255) / 256, 152 * 8);
+    const cudaError_t le = launch_pdl(router_scores_kernel, dim3((unsigned)blocks), dim3(256), 0, st, L, s, n);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

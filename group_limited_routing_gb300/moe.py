@@ -172,6 +172,17 @@ def router_logits(cfg: MoeConfig, hidden, W_router, *, ws: Optional[Workspace] =
     return logits
 
 
+def router_scores(logits):
+    """moe_router_scores: the routing kernels' fp32 sigmoid of every logit."""
+    dev = logits.device
+    if logits.dtype != torch.float32 or not logits.is_contiguous() or logits.device.type != "cuda":
+        raise ValueError("logits: contiguous fp32 CUDA tensor expected")
+    out = torch.empty_like(logits)
+    _lib.check(_lib.load().moe_router_scores(logits.data_ptr(), out.data_ptr(), logits.numel(), _stream(dev)),
+               "moe_router_scores")
+    return out
+
+
 def route_from_logits(cfg: MoeConfig, logits, expert_bias=None, *, aux: bool = False,
                       ws: Optional[Workspace] = None):
     """moe_route_from_logits: same outputs as route(), from fp32 logits."""

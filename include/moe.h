@@ -153,6 +153,14 @@ int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *
                           int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
                           float *aux_P, float *aux_loss, void *ws, size_t ws_bytes, void *stream);
 
+/* The sigmoid scores the selecting kernels rank (routing page, section 二
+ * step 1): scores[i] = 1 / (1 + exp(-logits[i])) in fp32, computed with the
+ * very device function those kernels use (an fp32 exponential, then an
+ * IEEE round-to-nearest reciprocal of 1 + exp(-L); not correctly rounded as
+ * a whole).  For measuring that function against an exact sigmoid.
+ * logits, scores: n fp32 values on the device, 4-byte aligned (may alias). */
+int moe_router_scores(const float *logits, float *scores, int64_t n, void *stream);
+
 /* Expert stage of the routing page, sections 四 and 五:
  *   out[t] = bf16( sum_j topk_w[t,j] * FFN_{topk_idx[t,j]}(hidden[t])
  *                  + FFN_shared(hidden[t]) (+ residual[t]) )
@@ -267,13 +275,16 @@ int moe_dense_ffn(int32_t T, int32_t H, int32_t I, const moe_bf16 *hidden, const
  * (40 MiB), held on every GPU that loads the library until the process exits.
  * That covers T up to 32768 tokens at E = 256, H = 2048 (more for smaller E
  * or H); larger configurations are rejected with MOE_ERR_UNSUPPORTED_SHAPE
- * before anything is launched.  The first call on a device looks up the
- * array's device address (with that device current); make that first call
- * before any stream capture.  Every call on a device shares the one array:
- * calls whose work overlaps on the GPU (other streams, other threads) race
- * and must be serialised by the caller.  Each call clears the status word it
- * uses; status_out (a DEVICE pointer, or NULL) receives that call's
- * MOE_STATUS_* bits in stream order. */
+ * before anything is launched.  The array has its own address in every CUDA
+ * context; the first call in a context (per device, and again after a device
+ * reset or in a context the host created itself) looks that address up with
+ * the context current, so make that first call before any stream capture.
+ * Every call on a device shares the one array: calls whose work overlaps on
+ * the GPU (other streams, other threads) race and must be serialised by the
+ * caller.  Each call clears the status word it uses; status_out (a DEVICE
+ * pointer, or NULL) receives that call's MOE_STATUS_* bits in stream order,
+ * and is written only when the call returns MOE_OK (on an error return it
+ * keeps whatever it held). */
 #define MOE_ROUTE_STATIC_SCRATCH_BYTES (40u << 20)
 int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
                      const float *expert_bias, int32_t *topk_idx, float *topk_w,

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from group_limited_routing_gb300 import moe, workloads as wl
-from parity import compare_counts, compare_routing
+from parity import compare_counts, compare_routing, record
 from test_oracle_pins import _parse_logits
 
 pytestmark = pytest.mark.gpu
@@ -46,6 +46,7 @@ def test_route_matches_oracle(wid, T):
     assert abs(gloss - rloss) <= 1e-4 * abs(rloss)
     print("workload %d T=%d near-tie tokens %d (%.3f%%), order-only ties %d, max w err %.2e" % (
         wid, T, n_near, 100.0 * n_near / T, rep["order_tie_tokens"], rep["max_w_err"]))
+    record("moe_route, workload %d, T=%d" % (wid, T), rep)
     assert n_near <= max(2, T // 100)
 
 
@@ -65,6 +66,26 @@ def test_router_logits_accuracy(wid, T):
     print("workload %d: router logits max abs err %.3e (max |logit| %.2f)" % (wid, err.max(), np.abs(L).max()))
 
 
+def test_router_sigmoid_ulp_distance():
+    """The routing kernels' fp32 sigmoid (an fp32 exponential, then a
+    round-to-nearest reciprocal of 1 + exp(-L)) against the oracle's sigmoid
+    (double, rounded once to fp32): how many fp32 steps apart they are."""
+    rng = np.random.default_rng(5)
+    grid = np.linspace(-30.0, 30.0, 1 << 20, dtype=np.float32)
+    L = np.concatenate([grid, rng.standard_normal(1 << 20).astype(np.float32) * 3.0])
+    L = L[: (L.size // 256) * 256]
+    got = moe.router_scores(torch.from_numpy(L).to(DEV)).cpu().numpy()
+    ref = oracle.route(L.reshape(-1, 256))["scores"].ravel()
+    # positive floats: the distance in fp32 steps is the difference of the bit patterns
+    ulps = np.abs(got.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+    hist = {int(u): int(c) for u, c in zip(*np.unique(ulps, return_counts=True))}
+    print("router sigmoid: fp32 steps from the exact sigmoid (count by distance): %s" % hist)
+    record("router sigmoid vs exact (fp32 steps), %d logits in [-30, 30] and N(0, 9)" % L.size,
+           dict(T=int(L.size), ulp_hist=hist, max_ulps=int(ulps.max()),
+                frac_exact=float((ulps == 0).mean())))
+    assert ulps.max() <= 4
+
+
 @pytest.mark.parametrize("T,n_group,topk_group,k,scale", [
     (1, 8, 4, 8, 1.0), (130, 8, 4, 8, 1.0), (1000, 8, 1, 8, 2.0), (777, 8, 8, 8, 1.0),
     (513, 8, 4, 1, 1.0), (300, 8, 4, 32, 1.0), (257, 4, 2, 6, 1.0), (129, 4, 4, 32, 3.0),
@@ -79,7 +100,7 @@ def test_route_from_logits_edge_shapes(T, n_group, topk_group, k, scale):
                           moe.route_from_logits(cfg, torch.from_numpy(L).to(DEV), torch.from_numpy(bias).to(DEV),
                                                 aux=True)]
     ref = oracle.route(L, bias=bias, n_group=n_group, topk_group=topk_group, k=k)
-    n_near, near = compare_routing(gi, gw, ref, E, bias=bias)
+    n_near, near = compare_routing(gi, gw, ref, E, bias=bias, n_group=n_group, topk_group=topk_group)
     rc, rP, rl = oracle.counts_aux(ref["idx"], ref["scores"], E=E)
     compare_counts(gc, gi, rc, ref["idx"], near, E)
     np.testing.assert_allclose(gP, rP, rtol=1e-4, atol=1e-7)
@@ -243,7 +264,7 @@ def test_route_from_logits_random_settings(case):
                           moe.route_from_logits(cfg, torch.from_numpy(L).to(DEV),
                                                 None if bias is None else torch.from_numpy(bias).to(DEV), aux=True)]
     ref = oracle.route(L, bias=bias, n_group=n_group, topk_group=topk_group, k=k)
-    n_near, near = compare_routing(gi, gw, ref, E, bias=bias)
+    n_near, near = compare_routing(gi, gw, ref, E, bias=bias, n_group=n_group, topk_group=topk_group)
     rc, rP, rl = oracle.counts_aux(ref["idx"], ref["scores"], E=E)
     compare_counts(gc, gi, rc, ref["idx"], near, E)
     np.testing.assert_allclose(gP, rP, rtol=1e-4, atol=1e-7)

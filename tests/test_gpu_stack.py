@@ -12,11 +12,11 @@ import torch
 
 import oracle
 from group_limited_routing_gb300 import moe, workloads as wl
-from parity import assert_output_close, bf16_to_f64, compare_counts, compare_routing
+from parity import assert_output_close, bf16_to_f64, compare_counts, compare_routing, record
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-FULL_ROUTE_LAYERS = (0, 9, 18)
+FULL_ROUTE_LAYERS = tuple(range(19))   # every layer's routing on every token
 
 
 def u16(t):
@@ -30,6 +30,7 @@ def test_nineteen_layer_stack_teacher_forced():
     x = wl.hidden(w0, DEV)
     tokens = np.union1d(wl.token_sample(w0.T, 64, seed=5).numpy(), [0, w0.T - 1]).astype(np.int32)
     losses, near_total = [], 0
+    tally = dict(T=0, near_tie_tokens=0, near_tie_differ=0, order_tie_tokens=0, order_tie_differ=0, max_w_err=0.0)
     for layer in range(w0.layers):
         d = wl.layer_inputs(w0, DEV, layer=layer)
         L = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"], d["shared_gate_up"],
@@ -50,8 +51,11 @@ def test_nineteen_layer_stack_teacher_forced():
 
         rows = np.arange(w0.T) if layer in FULL_ROUTE_LAYERS else tokens
         ref = oracle.route(oracle.router_logits(np.ascontiguousarray(xs[rows]), W), bias=bias)
-        n_near, near = compare_routing(idx[rows], w[rows], ref, cfg.E, bias=bias)
+        rep = {}
+        n_near, near = compare_routing(idx[rows], w[rows], ref, cfg.E, rep, bias=bias)
         near_total += n_near
+        for key in tally:
+            tally[key] = max(tally[key], rep[key]) if key == "max_w_err" else tally[key] + rep[key]
         if layer in FULL_ROUTE_LAYERS:
             rc, rP, _ = oracle.counts_aux(ref["idx"], ref["scores"])
             compare_counts(counts, idx, rc, ref["idx"], near, cfg.E)
@@ -68,6 +72,7 @@ def test_nineteen_layer_stack_teacher_forced():
             layer, n_near, e["mean_rel"], losses[-1], float(out.abs().max())))
         x = out
         del L, d
+    record("moe_route in the 19-layer stack, T=8192 per layer (all layers' tokens)", tally)
     assert all(np.isfinite(losses)) and all(0.5 < v < 10.0 for v in losses)
     assert torch.isfinite(x.float()).all()
     assert float(x.float().std()) < 10.0

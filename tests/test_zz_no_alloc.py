@@ -23,21 +23,26 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _static_route(cfg, x, W, bias):
+def _outputs(cfg):
+    return dict(idx=torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=DEV),
+                w=torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=DEV),
+                counts=torch.empty(cfg.E, dtype=torch.int32, device=DEV),
+                P=torch.empty(cfg.E, dtype=torch.float32, device=DEV),
+                loss=torch.empty(1, dtype=torch.float32, device=DEV),
+                status=torch.full((1,), -1, dtype=torch.int32, device=DEV))
+
+
+def _static_route(cfg, x, W, bias, o):
+    """One call into the library on outputs allocated beforehand; returns the
+    device's free bytes and torch's allocated bytes, both read after it."""
     lib = _lib.load()
-    idx = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=DEV)
-    w = torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=DEV)
-    counts = torch.empty(cfg.E, dtype=torch.int32, device=DEV)
-    P = torch.empty(cfg.E, dtype=torch.float32, device=DEV)
-    loss = torch.empty(1, dtype=torch.float32, device=DEV)
-    status = torch.full((1,), -1, dtype=torch.int32, device=DEV)
     stream = torch.cuda.current_stream().cuda_stream
-    rc = lib.moe_route_static(ctypes.byref(cfg.c()), x.data_ptr(), W.data_ptr(), bias.data_ptr(), idx.data_ptr(),
-                              w.data_ptr(), counts.data_ptr(), P.data_ptr(), loss.data_ptr(), status.data_ptr(),
-                              stream)
+    rc = lib.moe_route_static(ctypes.byref(cfg.c()), x.data_ptr(), W.data_ptr(), bias.data_ptr(),
+                              o["idx"].data_ptr(), o["w"].data_ptr(), o["counts"].data_ptr(), o["P"].data_ptr(),
+                              o["loss"].data_ptr(), o["status"].data_ptr(), stream)
     assert rc == _lib.MOE_OK, _lib.strerror(rc)
     torch.cuda.synchronize()
-    return idx, w, counts, P, loss, int(status.item())
+    return torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
 
 
 @pytest.mark.parametrize("wid,T", [(4, 32768), (1, 128)])
@@ -47,14 +52,21 @@ def test_static_route_matches_workspace_route_twice(wid, T):
     cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
     ref = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=True)
     torch.cuda.synchronize()
-    for _ in range(2):
-        idx, w, counts, P, loss, status = _static_route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
-        assert status == 0
-        assert torch.equal(idx, ref[0])
-        assert torch.equal(counts, ref[2])
-        assert torch.equal(w, ref[1])
-        assert torch.equal(P, ref[3])
-        assert torch.equal(loss, ref[4])
+    outs = [_outputs(cfg), _outputs(cfg)]
+    torch.cuda.synchronize()
+    mem = [(torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated())]
+    for o in outs:
+        mem.append(_static_route(cfg, d["hidden"], d["W_router"], d["expert_bias"], o))
+        assert int(o["status"].item()) == 0
+        assert torch.equal(o["idx"], ref[0])
+        assert torch.equal(o["counts"], ref[2])
+        assert torch.equal(o["w"], ref[1])
+        assert torch.equal(o["P"], ref[3])
+        assert torch.equal(o["loss"], ref[4])
+    # nothing is allocated by the call itself: after the first call (which may
+    # load the library's code onto the device), neither the device's free
+    # memory nor torch's allocator moves
+    assert mem[2] == mem[1], mem
 
 
 def test_static_route_rejects_configurations_beyond_its_array():
