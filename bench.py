@@ -1,6 +1,7 @@
 """Benchmark of the GB300 MoE layer forward (route + expert stage).
 
-One step = moe_route + moe_forward over one batch of T tokens of the full-size
+One step = the layer forward (moe_layer: routing and the expert stage in one
+call; --two-call: moe_route + moe_forward) over one batch of T tokens of the full-size
 skewed workload (T=32768, hidden 2048, 256 experts in 8 groups, top-4 groups,
 top-8, SwiGLU experts [256, 512, 2048], one shared expert, 16 hot experts with
 router rows x3 and expert_bias ~ N(0, 0.05)).  Inputs are seeded synthetic
@@ -353,7 +354,7 @@ def backward_work(T, H, E, I, k):
     }
 
 
-def build_model(w0, dev, dense_inter=0, fused_router=False):
+def build_model(w0, dev, dense_inter=0, fused_router=False, two_call=False):
     """The step's model: one MoE layer, the 19-layer stack of workload 5, or
     (dense_inter > 0) the dense first-layer MLP of that intermediate size.
     fused_router: one moe_layer call per step with the fused router (routing
@@ -377,16 +378,17 @@ def build_model(w0, dev, dense_inter=0, fused_router=False):
         return cfg, moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
                                  d["shared_gate_up"], d["shared_down"], single_call=True,
                                  flags=_lib.MOE_LAYER_FUSED_ROUTER)
-    ws_r = moe.Workspace(cfg, 0, dev)
-    ws_f = moe.Workspace(cfg, 1, dev)
+    # one moe_layer call per layer and step (two_call: moe_route + moe_forward)
+    ws = dict(ws_route=moe.Workspace(cfg, 0, dev), ws_fwd=moe.Workspace(cfg, 1, dev)) if two_call else \
+        dict(ws_layer=moe.Workspace(cfg, moe.WS_LAYER, dev))
     layers = []
     # the 19-layer stack workload also computes every layer's balance loss
     # (E * sum_i f_i P_i from the router scores) beside its expert counts
     for layer in range(w0.layers):
         d = wl.layer_inputs(w0, dev, layer=layer)
         layers.append(moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
-                                   d["shared_gate_up"], d["shared_down"], aux=w0.layers > 1, ws_route=ws_r,
-                                   ws_fwd=ws_f))
+                                   d["shared_gate_up"], d["shared_down"], aux=w0.layers > 1,
+                                   single_call=not two_call, **ws))
     return cfg, (moe.MoEStack(layers) if w0.layers > 1 else layers[0])
 
 
@@ -399,7 +401,7 @@ def run_ours(args, world, rank, local):
     if args.tokens:
         w0 = w0.with_T(args.tokens)
     T, H, E, I, k = w0.T, w0.H, w0.E, w0.I, w0.k
-    cfg, layer = build_model(w0, dev, args.dense, args.fused_router)
+    cfg, layer = build_model(w0, dev, args.dense, args.fused_router, args.two_call)
     x = wl.hidden(w0, dev, layer=rank)      # each replica its own batch
     if args.backward:
         layer = BackwardStep(layer, x)
@@ -642,7 +644,9 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
                           "expert weights (%.2f GB per layer) larger than L2, no flush" % (3 * E * I * H * 2 / 1e9)),
                    "untimed_lead_in_steps": extra["lead"],
                    "path": ("moe_layer with the fused router (routing and bucketing in the router kernel)"
-                            if getattr(args, "fused_router", False) else "moe_route + moe_forward"),
+                            if getattr(args, "fused_router", False) else
+                            "moe_route + moe_forward" if getattr(args, "two_call", False) else
+                            "moe_layer (routing and expert stage in one call)"),
                    "hot_expert_share": None if extra["hot_share"] is None else round(extra["hot_share"], 4)},
         "roofline": {"kernel": dom, "bound": g1["bound"], "achieved": round(g1_ach, 1),
                      "peak": g1_peak, "unit": g1_unit,
@@ -748,6 +752,8 @@ def main():
                     help="untimed loaded steps before the timed region (0: one step; for profiling captures)")
     ap.add_argument("--fused-router", action="store_true",
                     help="one moe_layer call per step with routing and bucketing fused into the router kernel")
+    ap.add_argument("--two-call", action="store_true",
+                    help="time the two calls moe_route + moe_forward per step instead of the one moe_layer call")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step (default: the workload's 32768); smaller sizes for profiling captures")
     args = ap.parse_args()

@@ -97,7 +97,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.moe_backward.argtypes = [C] + [P] * 14 + [P, S, P]
         lib.moe_layer_workspace_bytes.argtypes = [C, ctypes.c_int]
         lib.moe_layer_workspace_bytes.restype = S
-        lib.moe_layer.argtypes = [C] + [P] * 13 + [ctypes.c_int, P, S, P]
+        lib.moe_layer.argtypes = [C] + [P] * 15 + [ctypes.c_int, P, S, P]
         lib.moe_layer.restype = ctypes.c_int
         lib.moe_backward.restype = ctypes.c_int
         lib.moe_get_status.argtypes = [P, S, P, ctypes.POINTER(ctypes.c_int32), ctypes.c_int]

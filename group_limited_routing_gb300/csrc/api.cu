@@ -124,7 +124,7 @@ int check_forward_cfg(const moe_cfg *c)
 
 // ---------------------------------------------------------------- layouts
 struct RouteLayout {
-    size_t w3, logits, ppart, pfin, total;
+    size_t w3, logits, gscore, ppart, pfin, total;
     int nchunk;
     int ksplit;   // K parts of the router GEMM's logits region
 };
@@ -158,6 +158,8 @@ RouteLayout route_layout(const moe_cfg &c)
     off = align_up(off + 3ull * c.E * c.H * 2, 256);
     L.logits = off;
     off = align_up(off + (size_t)L.ksplit * c.T * c.E * 4, 256);
+    L.gscore = off;                     // group scores of the scored router output [T, E / 32]
+    off = align_up(off + (size_t)c.T * (c.E / 32) * 4, 256);
     L.ppart = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
     L.pfin = off;
@@ -339,11 +341,18 @@ T *at(void *ws, size_t off)
 // split W into the workspace here (that launch also clears counts).
 // ksplit_max: K parts the logits buffer has room for (L.ksplit, or 1 for a
 // caller's [T, E] buffer); nparts receives the parts actually written.
+// gscore (nullable): ask for the scored output (sigmoid scores in `logits`,
+// group scores in gscore, bias = `bias`); `scored` tells whether it was
+// produced -- only by the tensor-core router without a K split, for the
+// routing page's 256 experts in 8 groups of which 4 are kept.
 int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split, float *logits,
                 int32_t *counts, void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches,
-                int ksplit_max, int &nparts)
+                int ksplit_max, int &nparts, const float *bias = nullptr, float *gscore = nullptr,
+                bool *scored = nullptr)
 {
     nparts = 1;
+    if (scored)
+        *scored = false;
     if (c.T <= ROUTER_SIMT_MAX_T && c.H % 8 == 0 && aligned(W, 16)) {
         // a few token tiles cannot fill the tensor-core kernel: CUDA cores, fp32 W as is
         // (16-byte loads of W; a W that is only 4-byte aligned takes the tensor-core path)
@@ -380,25 +389,64 @@ int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
     p.H = c.H;
     p.ld_out = c.E;
     p.status = &header(ws)->status;
+    const bool sc = gscore && ks == 1 && c.E == 256 && c.n_group == 8 && c.topk_group == 4;
+    if (sc) {
+        p.gscore = gscore;
+        p.bias = bias;
+    }
     GLR_LAUNCH(KID_ROUTER_GEMM, launch_gemm(wide ? GK_ROUTER_WIDE : GK_ROUTER, p, std::min(sms, p.num_tiles_static), s));
     nparts = ks;
+    if (scored)
+        *scored = sc;
     return MOE_OK;
 }
 
 // counts must be zero on the stream when this runs.
 // logits: nparts K-part buffers of [T, E] (see router_gemm).
+// scored: `logits` holds the router's scored output (router_gemm); then
+// chunk_hist (nullable) receives the bucketing histogram [E][ceil(T / 16)]
+// from the same launch.
 int route_select(const moe_cfg &c, const float *logits, int nparts, const float *bias, int32_t *idx, float *w,
                  int32_t *counts, float *aux_P, float *aux_loss, void *ws, const RouteLayout &L, cudaStream_t s,
-                 int &launches)
+                 int &launches, bool scored = false, int32_t *chunk_hist = nullptr)
 {
     float *ppart = (aux_P || aux_loss) ? at<float>(ws, L.ppart) : nullptr;
-    GLR_LAUNCH(KID_SELECT, launch_route_select(logits, nparts, (long long)c.T * c.E, bias, c.T, c.E, c.n_group,
-                                               c.topk_group, c.k, c.rsf, c.eps, idx, w, counts, ppart,
-                                               &header(ws)->status, ppart ? &header(ws)->fin_ticket : nullptr, s));
+    int *ticket = ppart ? &header(ws)->fin_ticket : nullptr;
+    int nchunk = L.nchunk;
+    if (scored) {
+        GLR_LAUNCH(KID_SELECT, launch_route_select_scored(logits, at<float>(ws, L.gscore), bias, c.T, c.E, c.k, c.rsf,
+                                                          c.eps, idx, w, counts, ppart, &header(ws)->status, ticket,
+                                                          chunk_hist, s));
+        nchunk = (c.T + route_chunk_hist(c.T) - 1) / route_chunk_hist(c.T);
+    } else {
+        GLR_LAUNCH(KID_SELECT, launch_route_select(logits, nparts, (long long)c.T * c.E, bias, c.T, c.E, c.n_group,
+                                                   c.topk_group, c.k, c.rsf, c.eps, idx, w, counts, ppart,
+                                                   &header(ws)->status, ticket, s));
+    }
     if (ppart)
-        GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(counts, ppart, L.nchunk, c.T, c.E, c.k, at<float>(ws, L.pfin),
+        GLR_LAUNCH(KID_FINALIZE, launch_route_finalize(counts, ppart, nchunk, c.T, c.E, c.k, at<float>(ws, L.pfin),
                                                        &header(ws)->fin_ticket, aux_P, aux_loss, s));
     return MOE_OK;
+}
+
+// Router GEMM and selection (moe_route's kernels): the scored router output
+// when the shape allows it.  With chunk_hist, hist_done tells whether the
+// selection wrote the bucketing histogram there.
+int route_all(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split, const float *bias,
+              int32_t *idx, float *w, int32_t *counts, float *aux_P, float *aux_loss, void *ws, const RouteLayout &L,
+              int sms, cudaStream_t s, int &launches, int32_t *chunk_hist = nullptr, bool *hist_done = nullptr)
+{
+    float *logits = at<float>(ws, L.logits);
+    int nparts = 1;
+    bool scored = false;
+    int rc = router_gemm(c, hidden, W, W_split, logits, counts, ws, L, sms, s, launches, L.ksplit, nparts, bias,
+                         at<float>(ws, L.gscore), &scored);
+    if (rc == MOE_OK)
+        rc = route_select(c, logits, nparts, bias, idx, w, counts, aux_P, aux_loss, ws, L, s, launches, scored,
+                          scored ? chunk_hist : nullptr);
+    if (hist_done)
+        *hist_done = scored && chunk_hist;
+    return rc;
 }
 
 int check_ws(void *ws, size_t ws_bytes, size_t need)
@@ -523,7 +571,7 @@ int fused_route(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
 int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
                  const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const int32_t *topk_idx,
                  const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *ws, const FwdLayout &L,
-                 const int32_t *offs, int sms, cudaStream_t s, int &launches)
+                 const int32_t *offs, int sms, cudaStream_t s, int &launches, bool hist_ready = false)
 {
     WsHeader *hdr = header(ws);
     int32_t *hist = at<int32_t>(ws, L.hist);
@@ -543,7 +591,9 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
         GLR_LAUNCH(KID_SCATTER, launch_bucket_small(topk_idx, hidden, c.T, c.H, c.E, c.k, mt, sizes, slot_of,
                                                     xperm, mtiles, hdr, s));
     } else if (!offs) {
-        GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
+        // (the routing kernel of moe_layer may have written the histogram already)
+        if (!hist_ready)
+            GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
         GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
         GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
                                                       xperm, mtiles, hdr, s));
@@ -727,13 +777,8 @@ int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
         return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
-    float *logits = at<float>(ws, L.logits);
-    int nparts = 1;
-    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches, L.ksplit,
-                     nparts);
-    if (rc == MOE_OK)
-        rc = route_select(*cfg, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
-                          L, s, launches);
+    rc = route_all(*cfg, hidden, W_router, nullptr, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
+                   L, sms, s, launches);
     g_last_launches = launches;
     return rc;
 }
@@ -779,13 +824,8 @@ int moe_route_prepared(const moe_cfg *cfg, const moe_bf16 *hidden, const float *
         return rc;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     int launches = 0;
-    float *logits = at<float>(ws, L.logits);
-    int nparts = 1;
-    rc = router_gemm(*cfg, hidden, W_router, W_split, logits, expert_counts, ws, L, sms, s, launches, L.ksplit,
-                     nparts);
-    if (rc == MOE_OK)
-        rc = route_select(*cfg, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
-                          L, s, launches);
+    rc = route_all(*cfg, hidden, W_router, W_split, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
+                   L, sms, s, launches);
     g_last_launches = launches;
     return rc;
 }
@@ -1103,8 +1143,8 @@ size_t moe_layer_workspace_bytes(const moe_cfg *cfg, int flags)
 int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const moe_bf16 *W_split,
               const float *expert_bias, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
               const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const moe_bf16 *residual,
-              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, moe_bf16 *out, int flags, void *ws,
-              size_t ws_bytes, void *stream)
+              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss,
+              moe_bf16 *out, int flags, void *ws, size_t ws_bytes, void *stream)
 {
     int rc = check_route_cfg(cfg);
     if (rc == MOE_OK)
@@ -1113,6 +1153,8 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
         return rc;
     if (flags & ~MOE_LAYER_FUSED_ROUTER)
         return MOE_ERR_INVALID_ARG;
+    if ((aux_P || aux_loss) && layer_fused(*cfg, flags))
+        return MOE_ERR_INVALID_ARG;          // the fused router forms no balance-loss sums
     if (!hidden || !W_router || !W_gate_up || !W_down || !shared_gate_up || !shared_down || !topk_idx || !topk_w ||
         !expert_counts || !out)
         return MOE_ERR_INVALID_ARG;
@@ -1122,7 +1164,7 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
     if (!aligned(hidden, 16) || !aligned(W_router, 4) || !aligned(W_split, 16) || !aligned(expert_bias, 4) ||
         !aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(shared_gate_up, 16) ||
         !aligned(shared_down, 16) || !aligned(residual, 16) || !aligned(out, 16) || !aligned(topk_idx, 4) ||
-        !aligned(topk_w, 4) || !aligned(expert_counts, 4))
+        !aligned(topk_w, 4) || !aligned(expert_counts, 4) || !aligned(aux_P, 4) || !aligned(aux_loss, 4))
         return MOE_ERR_MISALIGNED;
     int sms = 0;
     if ((rc = device_check(&sms)) != MOE_OK)
@@ -1137,16 +1179,14 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
             rc = forward_impl(c, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, residual,
                               out, ws, L.f, at<int32_t>(ws, L.offs), sms, s, launches);
     } else {
-        float *logits = at<float>(ws, L.r.logits);
-        int nparts = 1;
-        rc = router_gemm(c, hidden, W_router, W_split, logits, expert_counts, ws, L.r, sms, s, launches, L.r.ksplit,
-                         nparts);
-        if (rc == MOE_OK)
-            rc = route_select(c, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, nullptr, nullptr, ws,
-                              L.r, s, launches);
+        // the routing kernel also writes the bucketing histogram where the
+        // expert stage reads it (when the router's scored output is taken)
+        bool hist_done = false;
+        rc = route_all(c, hidden, W_router, W_split, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
+                       L.r, sms, s, launches, at<int32_t>(ws, L.f.hist), &hist_done);
         if (rc == MOE_OK)
             rc = forward_impl(c, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, residual,
-                              out, ws, L.f, nullptr, sms, s, launches);
+                              out, ws, L.f, nullptr, sms, s, launches, hist_done);
     }
     g_last_launches = launches;
     return rc;
@@ -1372,13 +1412,8 @@ int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_
     if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess)
         return MOE_ERR_CUDA;
     int launches = 0;
-    float *logits = at<float>(ws, L.logits);
-    int nparts = 1;
-    rc = router_gemm(*cfg, hidden, W_router, nullptr, logits, expert_counts, ws, L, sms, s, launches, L.ksplit,
-                     nparts);
-    if (rc == MOE_OK)
-        rc = route_select(*cfg, logits, nparts, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
-                          L, s, launches);
+    rc = route_all(*cfg, hidden, W_router, nullptr, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
+                   L, sms, s, launches);
     if (rc == MOE_OK && status_out &&
         cudaMemcpyAsync(status_out, &header(ws)->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s) !=
             cudaSuccess)

@@ -224,9 +224,12 @@ struct GemmLayout {
     // the fused router's epilogue barrier and per-tile bucket histogram
     static constexpr bool FUSED = (KIND == GK_ROUTER_FUSED);
     static constexpr int HIST = FUSED ? 256 * 4 + 16 + 16 : 0;   // histogram, queue slot, mailbox
+    // the router kinds' copy of expert_bias (256 floats at most) for the scored output
+    static constexpr int BIAS = (base_kind(KIND) == GK_ROUTER && !FUSED) ? 256 * 4 : 0;
     // full[STAGES], empty[STAGES], tfull[SLOTS], tempty[SLOTS], fin, tq_full[TQ], tq_empty[TQ] (, epi)
     static constexpr int NBARS = 2 * C::STAGES + 2 * C::SLOTS + 1 + 2 * TQ + (FUSED ? FUSED_BARS : 0);
-    static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16 + TQ * 4 + HIST;
+    static constexpr int SMEM = C::STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16 + TQ * 4 + HIST +
+                                BIAS;
     static_assert(SMEM <= 232448, "more than 227 KB of shared memory");
     static_assert(C::A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "swizzle atoms need 1024-B alignment");
 };
@@ -1054,7 +1057,8 @@ template <int KIND>
 __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const TileInfo &ti, uint32_t tmem,
                                                      int quad, int half, int lane, uint32_t tfull0,
                                                      uint32_t tempty0, uint32_t &kctr, volatile int *abort_flag,
-                                                     uint8_t *stage, unsigned long long limit, int tile)
+                                                     uint8_t *stage, unsigned long long limit, int tile,
+                                                     const float *sbias)
 {
     using C = GemmCfg<KIND>;
     constexpr int COLS = 128;
@@ -1096,6 +1100,38 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
         }
     }
     const int valid_rows = ti.rows - quad * 32;
+    if (p.gscore != nullptr) {
+        // scored output (routing page, section 二 step 1 and the group score
+        // of step 2, with section 三's bias): the sigmoid of every logit
+        // replaces it, and each of the row's four groups of 32 gets the sum
+        // of its two best biased scores (a tie for the top counts twice)
+        const int e0 = ti.nt * C::BN + half * COLS;
+        bool bad = false;
+        float gq[COLS / 32];
+#pragma unroll
+        for (int q = 0; q < COLS / 32; ++q) {
+            float m1 = -INFINITY, m2 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float L = acc[32 * q + i];
+                bad |= !(fabsf(L) <= 3.402823466e38f);       // NaN or +-inf
+                const float sc = router_sigmoid(L);
+                acc[32 * q + i] = sc;
+                const float b = sc + sbias[e0 + 32 * q + i];   // one address for the warp: a broadcast
+                m2 = fmaxf(m2, fminf(m1, b));
+                m1 = fmaxf(m1, b);
+            }
+            gq[q] = m1 + m2;
+        }
+        if (lane < valid_rows) {
+            float *g = p.gscore + (size_t)(ti.out_row + quad * 32 + lane) * (p.E / 32) + e0 / 32;
+#pragma unroll
+            for (int q = 0; q < COLS / 32; ++q)
+                g[q] = gq[q];
+        }
+        if (__any_sync(0xffffffffu, bad && lane < valid_rows) && lane == 0)
+            atomicOr(p.status, ST_NONFINITE);
+    }
     if (valid_rows > 0) {
         const size_t ld_bytes = (size_t)p.ld_out * 4;
         char *gbase = static_cast<char *>(p.out) + (size_t)ti.kp * (size_t)p.part_stride * 4 +
@@ -1151,6 +1187,7 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + L::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     volatile int *tq = reinterpret_cast<volatile int *>(tmem_holder + 4);   // L::TQ entries
+    float *sbias = reinterpret_cast<float *>(const_cast<int *>(tq + L::TQ) + L::HIST / 4);   // L::BIAS bytes
 
     const uint32_t bar0 = smem_u32(bars);
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -1361,6 +1398,16 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
         int buf = 0;
         uint32_t ctr = 0;
         bool fused_ok = true;
+        if constexpr (L::BIAS > 0) {
+            // the scored router output adds expert_bias: a copy in shared
+            // memory, shared by the epilogue warps (named barrier 1)
+            if (p.gscore) {
+                const int et = threadIdx.x - 64;
+                for (int e = et; e < p.E; e += 32 * epi_warps(KIND))
+                    sbias[e] = p.bias ? p.bias[e] : 0.0f;
+                asm volatile("bar.sync 1, %0;" ::"r"(32 * epi_warps(KIND)) : "memory");
+            }
+        }
         if constexpr (L::FUSED)
             fz.hist[(warp - 2) * 32 + lane] = 0;
         for (int n = 0;; ++n) {
@@ -1373,7 +1420,7 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
             const TileInfo ti = tile_info<KIND>(p, tile);
             if constexpr (ROUTER) {
                 if (!router_epilogue_tile<KIND>(p, ti, tmem, quad, (warp - 2) >> 2, lane, tfull0, tempty0, ctr,
-                                                abort_flag, stage, limit, tile)) {
+                                                abort_flag, stage, limit, tile, sbias)) {
                     fused_ok = false;
                     break;
                 }

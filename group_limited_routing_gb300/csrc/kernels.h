@@ -43,11 +43,45 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // ---- routing arithmetic shared by every kernel that selects experts ---------
-// Sigmoid score of a router logit (routing page, section 二 step 1), with an
-// IEEE-rounded reciprocal, so every selecting kernel gets the same bits.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Sigmoid score of a router logit (routing page, section 二 step 1),
+// s = 1 / (1 + exp(-L)), in a dozen fp32 instructions without branches, and
+// the same bits in every selecting kernel.  exp(-L) = 2^(-L log2 e): the
+// product with log2 e (split into its fp32 value and the remainder) is formed
+// as a rounded part a plus its residual r, the residual found with one FMA
+// (the FMA form of the error-free product, Ogita, Rump and Oishi 2005); the
+// hardware's 2^a is then scaled by 2^r ~ 1 + r ln 2, and 1 / (1 + e) is the
+// hardware reciprocal refined by one Newton-Raphson step.  L is clamped at
+// -87 so that 1 + e stays finite (the clamp moves s by less than 2e-38).  Not
+// correctly rounded: the test suite measures its distance from an exact
+// sigmoid.
 __device__ __forceinline__ float router_sigmoid(float L)
 {
-    return __frcp_rn(1.0f + expf(-L));
+    constexpr float LOG2E_HI = 1.44269502162933349609375f;   // log2(e) rounded to fp32
+    constexpr float LOG2E_LO = 1.925963033500011e-08f;       // log2(e) - LOG2E_HI
+    constexpr float LN2 = 0.693147180559945309f;
+    const float x = fmaxf(L, -87.0f);
+    const float a = -x * LOG2E_HI;
+    float r = fmaf(-x, LOG2E_HI, -a);                         // (-x) LOG2E_HI - a, exactly
+    r = fmaf(-x, LOG2E_LO, r);
+    float e = ex2_approx(a);
+    e = fmaf(e, r * LN2, e);
+    const float d = 1.0f + e;
+    const float y = rcp_approx(d);
+    return fmaf(y, fmaf(-d, y, 1.0f), y);
 }
 
 // Order-preserving map of fp32 onto uint32 (for non-NaN values): a > b as
@@ -160,6 +194,12 @@ struct GemmParams {
     // grouped gate/up: routed m-tiles read their A rows from the tile list's
     // fourth field (the bucket layout above) instead of the second
     int cap_rows;
+    // router kinds, scored output (no K split): when set, `out` receives the
+    // sigmoid scores s = router_sigmoid(logit) instead of the logits, and
+    // gscore [T, E / 32] every group's score (the sum of its two best biased
+    // scores s + bias, bias = `bias` or zero); non-finite logits set
+    // ST_NONFINITE
+    float *gscore;
 };
 
 // Smem bytes a GEMM kind needs (stages + alignment slack + barriers).
@@ -187,6 +227,18 @@ cudaError_t launch_route_select(const float *logits, int nparts, long long part_
                                 int E, int n_group, int topk_group, int k, float rsf, float eps, int32_t *idx,
                                 float *w, int32_t *counts, float *ppart, int *status, int *fin_ticket,
                                 cudaStream_t s);
+
+// The same selection from the router GEMM's scored output (sigmoid scores
+// [T, E] and group scores [T, E / 32]), for 8 groups of 32 with 4 kept; same
+// outputs, bit for bit.  chunk_hist (nullable): per PERM_CHUNK-token chunk
+// hits per expert, [E][ceil(T / PERM_CHUNK)] (the bucketing histogram).
+cudaError_t launch_route_select_scored(const float *scores, const float *gscore, const float *bias, int T, int E,
+                                       int k, float rsf, float eps, int32_t *idx, float *w, int32_t *counts,
+                                       float *ppart, int *status, int *fin_ticket, int32_t *chunk_hist,
+                                       cudaStream_t s);
+// tokens per block of the routing kernels when they also write the bucketing
+// histogram (whole PERM_CHUNK chunks per block)
+inline int route_chunk_hist(int T) { return T <= ROUTE_SMALL_T ? PERM_CHUNK : 2 * PERM_CHUNK; }
 
 // part: at least ROUTE_FIN_BLOCKS x E floats of scratch; ticket: an int that is
 // zero when the launch starts (the routing kernel before it clears it)

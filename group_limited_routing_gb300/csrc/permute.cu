@@ -91,9 +91,39 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ 
     const int per = (nchunk + blockDim.x - 1) / blockDim.x;
     const int c0 = threadIdx.x * per;
     const int c1 = min(nchunk, c0 + per);
+    // runs of up to SCAN_REG chunks stay in registers between the two passes
+    // (16-byte loads and stores when the rows and runs allow it)
+    constexpr int SCAN_REG = 16;
+    int v[SCAN_REG];
+    const bool in_regs = per <= SCAN_REG;
+    const bool vec = in_regs && (per % 4 == 0) && (nchunk % 4 == 0);
     int sum = 0;
-    for (int c = c0; c < c1; ++c)
-        sum += row[c];
+    if (vec) {
+#pragma unroll
+        for (int q = 0; q < SCAN_REG / 4; ++q) {
+            if (4 * q < per && c0 + 4 * q < nchunk) {
+                const int4 x = *reinterpret_cast<const int4 *>(row + c0 + 4 * q);
+                v[4 * q] = x.x;
+                v[4 * q + 1] = x.y;
+                v[4 * q + 2] = x.z;
+                v[4 * q + 3] = x.w;
+            } else {
+                v[4 * q] = v[4 * q + 1] = v[4 * q + 2] = v[4 * q + 3] = 0;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < SCAN_REG; ++i)
+            sum += v[i];
+    } else if (in_regs) {
+#pragma unroll
+        for (int i = 0; i < SCAN_REG; ++i) {
+            v[i] = (i < per && c0 + i < c1) ? row[c0 + i] : 0;
+            sum += v[i];
+        }
+    } else {
+        for (int c = c0; c < c1; ++c)
+            sum += row[c];
+    }
     int incl = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -107,10 +137,34 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ 
     int run = incl - sum;                         // exclusive within the warp
     for (int q = 0; q < w; ++q)
         run += wtot[q];
-    for (int c = c0; c < c1; ++c) {
-        const int h = row[c];
-        row[c] = run;
-        run += h;
+    if (vec) {
+#pragma unroll
+        for (int q = 0; q < SCAN_REG / 4; ++q) {
+            int4 x;
+            x.x = run;
+            run += v[4 * q];
+            x.y = run;
+            run += v[4 * q + 1];
+            x.z = run;
+            run += v[4 * q + 2];
+            x.w = run;
+            run += v[4 * q + 3];
+            if (4 * q < per && c0 + 4 * q < nchunk)
+                *reinterpret_cast<int4 *>(row + c0 + 4 * q) = x;
+        }
+    } else if (in_regs) {
+#pragma unroll
+        for (int i = 0; i < SCAN_REG; ++i) {
+            if (i < per && c0 + i < c1)
+                row[c0 + i] = run;
+            run += v[i];
+        }
+    } else {
+        for (int c = c0; c < c1; ++c) {
+            const int h = row[c];
+            row[c] = run;
+            run += h;
+        }
     }
     if (threadIdx.x == blockDim.x - 1)
         sizes[e] = run;                           // the last run ends at the bucket's size

@@ -479,6 +479,211 @@ __global__ void __launch_bounds__(256, 5) route_select_sorted_kernel(
     }
 }
 
+// The same selection from the router GEMM's scored output: the sigmoid scores
+// s [T, E] and every group's score [T, G] were formed in the GEMM's epilogue
+// (router_epilogue_tile), with the same router_sigmoid and the same fp32
+// additions, so nothing of the selection changes.  Per token (one warp) the
+// kernel reads the 8 group scores, keeps the TG best (ties to the lower
+// group), reads only the kept groups' scores (one coalesced row piece each)
+// and runs the top-K rounds of route_select_sorted_kernel on them; the
+// winner's unbiased score travels with its candidate, so no shared-memory
+// row is needed.  With `ppart` every score of the token is read for the
+// balance-loss sums (same order of additions as the other kernels).  With
+// `chunk_hist` the block (chunk = 16 or 32 tokens) also writes the hits per
+// expert of each PERM_CHUNK-token chunk, [E][nchunk_perm].
+template <int G, int TG>
+__global__ void __launch_bounds__(256) route_select_scored_kernel(
+    const float *__restrict__ scores, const float *__restrict__ gscore, const float *__restrict__ bias, int T,
+    int chunk, int K, float rsf, float eps, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
+    int32_t *__restrict__ counts, float *__restrict__ ppart, int *__restrict__ status, int *__restrict__ fin_ticket,
+    int32_t *__restrict__ chunk_hist, int nchunk_perm)
+{
+    pdl_wait();
+    constexpr int E = 32 * G;
+    constexpr unsigned FULL = 0xffffffffu;
+    constexpr int NQ = 2;                          // PERM_CHUNK chunks per block at most
+    if (fin_ticket && blockIdx.x == 0 && threadIdx.x == 0)
+        *fin_ticket = 0;                           // for the balance-loss reduction that follows
+    __shared__ int sh_hist[NQ][E];
+    __shared__ float sh_p[8][E];
+    __shared__ float sh_bias[E];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    bool nonfinite = false;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const float b = bias ? bias[e] : 0.0f;
+        nonfinite |= !isfinite(b);
+        sh_bias[e] = b;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+            sh_hist[q][e] = 0;
+    }
+    if (ppart) {
+#pragma unroll
+        for (int j = 0; j < G; ++j)
+            sh_p[warp][32 * j + lane] = 0.0f;
+    }
+    __syncthreads();
+
+    const int t0 = blockIdx.x * chunk;
+    const int t1 = min(T, t0 + chunk);
+    static_assert(G % 4 == 0, "group scores are read as float4");
+    // the token's group scores (every lane reads the same row of G floats);
+    // the next token's row is loaded before the current token is processed
+    float4 gn[G / 4];
+    if (t0 + warp < t1) {
+#pragma unroll
+        for (int v = 0; v < G / 4; ++v)
+            gn[v] = __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)(t0 + warp) * G) + v);
+    }
+    for (int t = t0 + warp; t < t1; t += 8) {
+        float g[G];
+#pragma unroll
+        for (int v = 0; v < G / 4; ++v) {
+            g[4 * v] = gn[v].x;
+            g[4 * v + 1] = gn[v].y;
+            g[4 * v + 2] = gn[v].z;
+            g[4 * v + 3] = gn[v].w;
+        }
+        if (t + 8 < t1) {
+#pragma unroll
+            for (int v = 0; v < G / 4; ++v)
+                gn[v] = __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)(t + 8) * G) + v);
+        }
+        float gl = g[0];
+#pragma unroll
+        for (int j = 1; j < G; ++j)
+            if (lane == j)
+                gl = g[j];
+        int rank = 0;
+#pragma unroll
+        for (int i = 0; i < G; ++i)
+            rank += (g[i] > gl || (g[i] == gl && i < lane)) ? 1 : 0;
+        uint32_t keep = __ballot_sync(FULL, lane < G && rank < TG) & ((1u << G) - 1u);
+
+        // this lane's candidates (its expert of each kept group), ascending
+        // group, then sorted by key (descending), equal keys keep the lower
+        // group; the candidates' groups are packed 8 bits each into cjp
+        // (entry i in bits 8i), so dropping the head is one shift
+        uint32_t ck[TG];
+        int cj[TG];
+        const float *srow = scores + (size_t)t * E + lane;
+#pragma unroll
+        for (int i = 0; i < TG; ++i) {
+            const int j = __ffs(keep) - 1;
+            keep &= keep - 1u;
+            cj[i] = j;
+            ck[i] = fkey(__ldg(srow + 32 * j) + sh_bias[32 * j + lane]);   // section 三: choose on s + bias
+        }
+#pragma unroll
+        for (int i = 1; i < TG; ++i) {
+#pragma unroll
+            for (int q = i; q > 0; --q) {
+                if (ck[q] > ck[q - 1]) {
+                    const uint32_t tk = ck[q];
+                    ck[q] = ck[q - 1];
+                    ck[q - 1] = tk;
+                    const int tj = cj[q];
+                    cj[q] = cj[q - 1];
+                    cj[q - 1] = tj;
+                }
+            }
+        }
+        uint32_t cjp = 0;
+#pragma unroll
+        for (int i = 0; i < TG; ++i)
+            cjp |= (uint32_t)cj[i] << (8 * i);
+
+        // top-K: each round takes the largest head key, ties to the lowest expert id
+        int my_e = -1;
+        for (int r = 0; r < K; ++r) {
+            const uint32_t wk = __reduce_max_sync(FULL, ck[0]);
+            const uint32_t cand = (ck[0] == wk) ? (((cjp & 0xffu) << 5) | (uint32_t)lane) : 0xffffffffu;
+            const uint32_t we = __reduce_min_sync(FULL, cand);
+            if (cand == we) {                              // the winning lane drops its head
+#pragma unroll
+                for (int i = 0; i + 1 < TG; ++i)
+                    ck[i] = ck[i + 1];
+                ck[TG - 1] = 0u;
+                cjp >>= 8;
+            }
+            if (lane == r)
+                my_e = (int)we;
+        }
+        // the winners' unbiased scores; the normaliser adds them in output order
+        const float my_s = (lane < K) ? __ldg(scores + (size_t)t * E + my_e) : 0.0f;
+        float den = 0.0f;
+        for (int r = 0; r < K; ++r)
+            den += __shfl_sync(FULL, my_s, r);
+        den += eps;
+        if (lane < K) {
+            idx_out[(size_t)t * K + lane] = my_e;
+            w_out[(size_t)t * K + lane] = (my_s / den) * rsf;   // section 二 step 3
+            atomicAdd(&sh_hist[(t - t0) / PERM_CHUNK][my_e], 1);
+        }
+
+        if (ppart) {
+            float sj[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                sj[j] = __ldg(srow + 32 * j);
+            float tot = 0.0f;
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                tot += sj[j];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                tot += __shfl_xor_sync(FULL, tot, off);
+            const float inv = 1.0f / tot;
+#pragma unroll
+            for (int j = 0; j < G; ++j)
+                sh_p[warp][32 * j + lane] += sj[j] * inv;
+        }
+    }
+    if (__any_sync(FULL, nonfinite) && lane == 0)
+        atomicOr(status, ST_NONFINITE);
+
+    __syncthreads();
+    const int q0 = t0 / PERM_CHUNK;
+    const int nq = (t1 - t0 + PERM_CHUNK - 1) / PERM_CHUNK;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int tot = 0;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+            tot += sh_hist[q][e];
+        if (tot)
+            atomicAdd(&counts[e], tot);              // integer sums: the result is order-free
+        if (chunk_hist) {
+            for (int q = 0; q < nq; ++q)
+                chunk_hist[(size_t)e * nchunk_perm + q0 + q] = sh_hist[q][e];   // [expert][chunk]
+        }
+        if (ppart) {
+            float v = 0.0f;
+            for (int q = 0; q < 8; ++q)
+                v += sh_p[q][e];
+            ppart[(size_t)blockIdx.x * E + e] = v;
+        }
+    }
+}
+
+cudaError_t launch_route_select_scored(const float *scores, const float *gscore, const float *bias, int T, int E,
+                                       int k, float rsf, float eps, int32_t *idx, float *w, int32_t *counts,
+                                       float *ppart, int *status, int *fin_ticket, int32_t *chunk_hist,
+                                       cudaStream_t s)
+{
+    if (E != 256)
+        return cudaErrorInvalidValue;
+    const int chunk = route_chunk_hist(T);          // whole bucketing chunks per block
+    const int blocks = (T + chunk - 1) / chunk;
+    const int nchunk_perm = (T + PERM_CHUNK - 1) / PERM_CHUNK;
+    const cudaError_t le = launch_pdl(route_select_scored_kernel<8, 4>, dim3(blocks), dim3(256), 0, s, scores,
+                                      gscore, bias, T, chunk, k, rsf, eps, idx, w, counts, ppart, status, fin_ticket,
+                                      chunk_hist, nchunk_perm);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
 cudaError_t launch_route_select(const float *logits, int nparts, long long part_stride, const float *bias, int T,
                                 int E, int n_group, int topk_group, int k, float rsf, float eps, int32_t *idx,
                                 float *w, int32_t *counts, float *ppart, int *status, int *fin_ticket,

@@ -227,11 +227,13 @@ def forward(cfg: MoeConfig, hidden, W_gate_up, W_down, shared_gate_up, shared_do
 
 
 def layer(cfg: MoeConfig, hidden, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
-          residual=None, *, W_split=None, flags: int = 0, ws: Optional[Workspace] = None, out=None, routing=None):
+          residual=None, *, W_split=None, flags: int = 0, ws: Optional[Workspace] = None, out=None, routing=None,
+          aux: bool = False):
     """moe_layer: routing and the expert stage in one call (with
     flags=MOE_LAYER_FUSED_ROUTER, the fused router where the shape allows it;
-    see include/moe.h).  Returns (out, (topk_idx,
-    topk_w, expert_counts)); `routing` (such a triple) is filled instead of
+    see include/moe.h).  Returns (out, (topk_idx, topk_w, expert_counts)),
+    or with aux=True (out, (topk_idx, topk_w, expert_counts, aux_P [E],
+    aux_loss [1])); `routing` (such a tuple) is filled instead of
     allocating."""
     dev = hidden.device
     bf = torch.bfloat16
@@ -244,13 +246,18 @@ def layer(cfg: MoeConfig, hidden, W_router, expert_bias, W_gate_up, W_down, shar
     psgu = _need(shared_gate_up, "shared_gate_up", bf, (2 * cfg.Is, cfg.H), dev)
     psd = _need(shared_down, "shared_down", bf, (cfg.Is, cfg.H), dev)
     pr = _opt(residual, "residual", bf, (cfg.T, cfg.H), dev)
-    if routing is None:
+    if routing is None or len(routing) != (5 if aux else 3):
         routing = (torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev),
                    torch.empty(cfg.T, cfg.k, dtype=torch.float32, device=dev),
                    torch.empty(cfg.E, dtype=torch.int32, device=dev))
+        if aux:
+            routing += (torch.empty(cfg.E, dtype=torch.float32, device=dev),
+                        torch.empty(1, dtype=torch.float32, device=dev))
     pi = _need(routing[0], "topk_idx", torch.int32, (cfg.T, cfg.k), dev)
     pw = _need(routing[1], "topk_w", torch.float32, (cfg.T, cfg.k), dev)
     pc = _need(routing[2], "expert_counts", torch.int32, (cfg.E,), dev)
+    pP = _need(routing[3], "aux_P", torch.float32, (cfg.E,), dev) if aux else None
+    pl = _need(routing[4], "aux_loss", torch.float32, (1,), dev) if aux else None
     if out is None:
         out = torch.empty(cfg.T, cfg.H, dtype=bf, device=dev)
     po = _need(out, "out", bf, (cfg.T, cfg.H), dev)
@@ -258,8 +265,8 @@ def layer(cfg: MoeConfig, hidden, W_router, expert_bias, W_gate_up, W_down, shar
         ws = Workspace(cfg, WS_LAYER, dev, flags)
     elif ws.which != WS_LAYER or not ws.fits(cfg, flags):
         raise ValueError("workspace of the wrong kind or too small")
-    rc = _lib.load().moe_layer(ctypes.byref(cfg.c()), ph, pwr, psp, pb, pgu, pd, psgu, psd, pr, pi, pw, pc, po,
-                               flags, ws.ptr, ws.nbytes, _stream(dev))
+    rc = _lib.load().moe_layer(ctypes.byref(cfg.c()), ph, pwr, psp, pb, pgu, pd, psgu, psd, pr, pi, pw, pc, pP, pl,
+                               po, flags, ws.ptr, ws.nbytes, _stream(dev))
     _lib.check(rc, "moe_layer")
     return out, routing
 
@@ -391,19 +398,21 @@ def profile_read(reset: bool = True) -> dict:
 
 
 class MoELayer:
-    """One MoE layer: weights on the device plus its workspaces.
+    """One MoE layer: weights on the device plus its workspace(s).
 
-    __call__(hidden) runs moe_route then moe_forward on the current stream,
-    or, with single_call=True (no balance loss), the one moe_layer call with
-    `flags` (the fused router where it applies).  The router weight is split
-    once at construction (prepare_router); call prepare() again after
-    changing W_router in place."""
+    __call__(hidden) runs the one moe_layer call on the current stream (with
+    `flags`: the fused router where it applies), or, with single_call=False,
+    moe_route then moe_forward (the two calls of the C ABI; same outputs).
+    aux=True also returns the balance loss (not with the fused router).  The
+    router weight is split once at construction (prepare_router); call
+    prepare() again after changing W_router in place.  Layers of a stack may
+    share one workspace (ws_layer, or ws_route / ws_fwd for the two calls)."""
 
     def __init__(self, cfg: MoeConfig, W_router, expert_bias, W_gate_up, W_down, shared_gate_up, shared_down,
                  aux: bool = False, ws_route: Optional[Workspace] = None, ws_fwd: Optional[Workspace] = None,
-                 single_call: bool = False, flags: int = 0):
-        if single_call and aux:
-            raise ValueError("moe_layer does not compute the balance loss: use single_call=False with aux")
+                 single_call: bool = True, flags: int = 0, ws_layer: Optional[Workspace] = None):
+        if single_call and aux and (flags & _lib.MOE_LAYER_FUSED_ROUTER):
+            raise ValueError("the fused router does not compute the balance loss")
         self.cfg = cfg
         self.W_router, self.expert_bias = W_router, expert_bias
         self.W_gate_up, self.W_down = W_gate_up, W_down
@@ -412,7 +421,9 @@ class MoELayer:
         self.single_call, self.flags = single_call, flags
         self.device = W_router.device
         if single_call:
-            self.ws_layer = Workspace(cfg, WS_LAYER, self.device, flags)
+            if ws_layer is not None and (ws_layer.which != WS_LAYER or not ws_layer.fits(cfg, flags)):
+                raise ValueError("workspace of the wrong kind or too small")
+            self.ws_layer = ws_layer or Workspace(cfg, WS_LAYER, self.device, flags)
             self.ws_route = self.ws_fwd = None
         else:
             self.ws_layer = None
@@ -432,7 +443,7 @@ class MoELayer:
         if self.single_call:
             y, self.routing = layer(self.cfg, hidden, self.W_router, self.expert_bias, self.W_gate_up, self.W_down,
                                     self.shared_gate_up, self.shared_down, residual, W_split=self.W_split,
-                                    flags=self.flags, ws=self.ws_layer, out=out, routing=self.routing)
+                                    flags=self.flags, ws=self.ws_layer, out=out, routing=self.routing, aux=self.aux)
             self.last_launches = last_launch_count()
             return y
         self.routing = route(self.cfg, hidden, self.W_router, self.expert_bias, aux=self.aux, ws=self.ws_route,
@@ -527,7 +538,10 @@ class MoEStack:
         return x
 
     def status(self) -> int:
-        return self.layers[0].ws_route.status() | self.layers[0].ws_fwd.status()
+        st = 0
+        for L in self.layers:
+            st |= L.status()
+        return st
 
 
 class GraphedStep:

@@ -190,13 +190,16 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
                 const int32_t *topk_idx, const float *topk_w, const moe_bf16 *residual,
                 moe_bf16 *out, void *ws, size_t ws_bytes, void *stream);
 
-/* The whole layer in one call: moe_route (without the balance loss) followed
- * by moe_forward, on one workspace of moe_layer_workspace_bytes(cfg, flags)
- * bytes (moe_workspace_init() once after allocating it).  Arguments as in
- * those two calls; W_split is moe_prepare_router's output or NULL (then the
- * router weight is split inside the call); topk_idx, topk_w and
- * expert_counts are outputs here.  flags = 0 runs the same kernels as the two
- * calls.
+/* The whole layer in one call: moe_route followed by moe_forward, on one
+ * workspace of moe_layer_workspace_bytes(cfg, flags) bytes
+ * (moe_workspace_init() once after allocating it).  Arguments as in those two
+ * calls; W_split is moe_prepare_router's output or NULL (then the router
+ * weight is split inside the call); topk_idx, topk_w, expert_counts and the
+ * optional aux_P [E] / aux_loss [1] (the balance loss, as in moe_route; NULL
+ * to skip) are outputs here.  flags = 0 gives the same outputs, bit for bit,
+ * as the two calls; because one call owns both halves, its routing kernel
+ * also writes the expert stage's bucketing histogram (per 16-token chunk,
+ * hits per expert), so the expert stage skips that pass.
  *
  * flags = MOE_LAYER_FUSED_ROUTER (for E = 256 experts in n_group = 8 groups
  * with k <= 8, H <= 8192; other shapes ignore it): the router's tensor-core
@@ -212,15 +215,16 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
  * a fixed order, so out is deterministic and equal to the unfused path's.
  * On a GB300 this path measures slower than the unfused kernels (its
  * selection runs on 8 warps per SM and its row copies follow the
- * multiplications), so it is not the default.  Unknown flags return
+ * multiplications), so it is not the default.  It forms no balance loss:
+ * aux_P / aux_loss must be NULL with it.  Unknown flags return
  * MOE_ERR_INVALID_ARG. */
 #define MOE_LAYER_FUSED_ROUTER 1
 size_t moe_layer_workspace_bytes(const moe_cfg *cfg, int flags);
 int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const moe_bf16 *W_split,
               const float *expert_bias, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
               const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const moe_bf16 *residual,
-              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, moe_bf16 *out, int flags, void *ws,
-              size_t ws_bytes, void *stream);
+              int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss,
+              moe_bf16 *out, int flags, void *ws, size_t ws_bytes, void *stream);
 
 /* Backward of moe_forward for fixed routing (the training step of the layer;
  * the routing page trains the layer but prints no backward: these are the

@@ -190,3 +190,23 @@ def test_layer_rejects_unknown_flags():
     with pytest.raises(_lib.MoeError):
         moe.layer(cfg, d["hidden"], d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
                   d["shared_gate_up"], d["shared_down"], flags=2, ws=moe.Workspace(cfg, moe.WS_LAYER, DEV, 0))
+
+
+@pytest.mark.parametrize("T", [33, 600, 4864, 4865, 8192, 19500, 32768])
+def test_layer_matches_the_two_calls_bit_for_bit(T):
+    """moe_layer (flags 0, with the balance loss) against moe_route +
+    moe_forward on the same inputs: the same routing kernels (from T = 4865
+    on, the router's scored output, whose selection kernel also writes the
+    bucketing histogram that moe_layer's expert stage then reads instead of
+    counting again), so every output agrees bit for bit."""
+    w0 = wl.WORKLOADS[4].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T)
+    out, (idx, w, counts, P, loss) = moe.layer(cfg, d["hidden"], d["W_router"], d["expert_bias"], d["W_gate_up"],
+                                               d["W_down"], d["shared_gate_up"], d["shared_down"], aux=True)
+    ri, rw, rc, rP, rl = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=True)
+    ro = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], ri, rw)
+    torch.cuda.synchronize()
+    for a, b in ((idx, ri), (w, rw), (counts, rc), (P, rP), (loss, rl), (out, ro)):
+        assert torch.equal(a, b)
+    assert int(counts.sum()) == T * cfg.k

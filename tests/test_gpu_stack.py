@@ -93,13 +93,12 @@ def test_moe_stack_object_matches_layer_loop():
     HostPipeline over the stack gives the same bytes again."""
     w0 = wl.WORKLOADS[5].with_T(1000)
     cfg = moe.MoeConfig(T=w0.T, H=w0.H, I=w0.I, Is=w0.Is)
-    ws_r = moe.Workspace(cfg, 0, DEV)
-    ws_f = moe.Workspace(cfg, 1, DEV)
+    ws_l = moe.Workspace(cfg, moe.WS_LAYER, DEV)
     layers = []
     for layer in range(3):
         d = wl.layer_inputs(w0, DEV, layer=layer)
         layers.append(moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
-                                   d["shared_gate_up"], d["shared_down"], ws_route=ws_r, ws_fwd=ws_f))
+                                   d["shared_gate_up"], d["shared_down"], ws_layer=ws_l))
     stack = moe.MoEStack(layers)
     x = wl.hidden(w0, DEV)
     y = torch.empty_like(x)
