@@ -370,8 +370,11 @@ int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
     // all experts of a token tile in one N = 256 MMA when E is a multiple of 256
     // and there are enough token tiles to give every SM one (below that the
     // 128-expert tiles spread the work over twice as many SMs)
+    // (on CTA pairs, each CTA loading the weight parts of 128 experts, when E
+    // is exactly 256)
     const bool wide = c.E % 256 == 0 && (c.T + GEMM_BM - 1) / GEMM_BM >= sms;
-    const int bn = wide ? 256 : 128;
+    const bool pair = wide && c.E == 256;
+    const int bn = (wide && !pair) ? 256 : 128;
     GemmParams p;
     memset(&p, 0, sizeof(p));
     if (!make_map_bf16(&p.tmA0, hidden, c.T, c.H, GEMM_BK, GEMM_BM) ||
@@ -394,7 +397,14 @@ int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
         p.gscore = gscore;
         p.bias = bias;
     }
-    GLR_LAUNCH(KID_ROUTER_GEMM, launch_gemm(wide ? GK_ROUTER_WIDE : GK_ROUTER, p, std::min(sms, p.num_tiles_static), s));
+    if (pair) {
+        p.n_tiles = 1;
+        p.num_tiles_static = (c.T + 255) / 256;
+        GLR_LAUNCH(KID_ROUTER_GEMM, launch_gemm(GK_ROUTER_PAIR, p, 2 * std::min(sms / 2, p.num_tiles_static), s));
+    } else {
+        GLR_LAUNCH(KID_ROUTER_GEMM,
+                   launch_gemm(wide ? GK_ROUTER_WIDE : GK_ROUTER, p, std::min(sms, p.num_tiles_static), s));
+    }
     nparts = ks;
     if (scored)
         *scored = sc;

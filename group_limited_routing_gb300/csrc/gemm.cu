@@ -52,6 +52,8 @@
 // status word gets MOE_STATUS_TIMEOUT.  Nothing traps.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "route_token.cuh"
@@ -74,6 +76,12 @@ __host__ __device__ constexpr bool wide_router(int kind) { return kind == GK_ROU
 
 // K blocks of hidden the wide router prefetches into L2 ahead of its loads
 constexpr int ROUTER_PF = 6;
+
+// K blocks (of 64) the router's tensor core sums into one TMEM slot before the
+// epilogue adds the slot to its fp32 running sums (24 MMAs per slot: the
+// tensor core's own accumulation stays short, and the promotion round trip
+// is paid once per 128 K)
+constexpr int ROUTER_KPS = 2;
 
 // epilogue warps of a kind (the block is 64 + 32 x this threads)
 __host__ __device__ constexpr int epi_warps(int kind) { return wide_router(kind) ? 8 : 4; }
@@ -1058,7 +1066,7 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
                                                      int quad, int half, int lane, uint32_t tfull0,
                                                      uint32_t tempty0, uint32_t &kctr, volatile int *abort_flag,
                                                      uint8_t *stage, unsigned long long limit, int tile,
-                                                     const float *sbias)
+                                                     const float *sbias, uint32_t tempty_cluster = 0)
 {
     using C = GemmCfg<KIND>;
     constexpr int COLS = 128;
@@ -1066,7 +1074,8 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
 #pragma unroll
     for (int c = 0; c < COLS; ++c)
         acc[c] = 0.0f;
-    for (int kb = 0; kb < p.kblocks; ++kb, ++kctr) {
+    const int ngroups = (p.kblocks + ROUTER_KPS - 1) / ROUTER_KPS;
+    for (int kg = 0; kg < ngroups; ++kg, ++kctr) {
         const uint32_t slot = kctr % C::SLOTS;
         const uint32_t par = (kctr / C::SLOTS) & 1u;
         int ok = 1;
@@ -1091,8 +1100,14 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
             if (c + LD == COLS) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(tempty0 + 8u * slot);   // slot free again: the values are in registers
+                if (lane == 0) {
+                    // slot free again: the values are in registers (a CTA pair
+                    // counts both CTAs' warps on the leader's barrier)
+                    if (tempty_cluster)
+                        mbar_arrive_cluster(tempty_cluster + 8u * slot);
+                    else
+                        mbar_arrive(tempty0 + 8u * slot);
+                }
             }
 #pragma unroll
             for (int i = 0; i < LD; ++i)
@@ -1356,7 +1371,7 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
                     tc_fence_after();
                 }
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (ROUTER) {
+                    if (ROUTER && kb % ROUTER_KPS == 0) {
                         const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
                         if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit)) {
                             ok = false;
@@ -1371,10 +1386,10 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
                     tc_fence_after();
                     const uint32_t sA = base + stage * L::STAGE_BYTES;
                     const uint32_t d = tmem + (ctr % C::SLOTS) * C::BN;
-                    issue_mmas<KIND>(sA, sA + C::A_BYTES, d, ROUTER ? false : kb > 0);
+                    issue_mmas<KIND>(sA, sA + C::A_BYTES, d, ROUTER ? (kb % ROUTER_KPS != 0) : kb > 0);
                     umma_commit(empty_bar(stage));               // frees the stage once read
-                    if (ROUTER) {
-                        umma_commit(tfull0 + 8u * (ctr % C::SLOTS));  // K-block partial ready
+                    if (ROUTER && (kb % ROUTER_KPS == ROUTER_KPS - 1 || kb == kblocks - 1)) {
+                        umma_commit(tfull0 + 8u * (ctr % C::SLOTS));  // the slot's partial sum is ready
                         ++ctr;
                     }
                     if (++stage == C::STAGES) {
@@ -1471,9 +1486,244 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
         atomicOr(p.status, ST_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// GK_ROUTER_PAIR: the 256-expert router on CTA pairs (tcgen05 cta_group::2).
+// A pair takes 256 tokens x all 256 experts per tile: each CTA loads its own
+// 128 token rows and the hi/mid/lo weight parts of its half of the experts
+// (CTA rank r: experts 128 r .. 128 r + 127), so a stage is 16 KB + 48 KB
+// instead of the single-CTA wide router's 16 KB + 96 KB; the even CTA issues
+// M = 256, N = 256 MMAs that read both CTAs' shared memory and leave each
+// CTA's 128 rows of the K-block partial sums in its own TMEM.  Each CTA's
+// eight epilogue warps then do exactly what the wide router's do (K-block
+// promotion in fp32, scored output), so the logits are bit-identical to it.
+// Barriers: the leader's full[stage] counts both CTAs' TMA bytes (the peer's
+// loads complete on it across the pair); the MMA commits arrive on empty[] and
+// tfull[] of both CTAs; the leader's tempty[] counts both CTAs' epilogue warps.
+struct PairRouterCfg {
+    static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;   // this CTA's 128 token rows
+    static constexpr int B_PART = 128 * GEMM_BK * 2;        // this CTA's 128 experts of one part
+    static constexpr int STAGE_BYTES = A_BYTES + 3 * B_PART; // 64 KB
+    static constexpr int STAGES = 3;
+    static constexpr int SLOTS = 2;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(256, 256, false, false);
+    static constexpr int NBARS = 2 * STAGES + 2 * SLOTS + 1;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + NBARS * 8 + 16 + 256 * 4 /*bias*/;
+    static_assert(SMEM <= 232448, "more than 227 KB of shared memory");
+};
+static_assert(GemmCfg<GK_ROUTER_WIDE>::SLOTS == PairRouterCfg::SLOTS && GemmCfg<GK_ROUTER_WIDE>::BN == 256,
+              "the pair router reuses the wide router's epilogue");
+
+constexpr int PAIR_THREADS = 64 + 32 * 8;
+
+__global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __grid_constant__ GemmParams p)
+{
+    using C = PairRouterCfg;
+    extern __shared__ uint8_t dsmem[];
+    const uint32_t raw = smem_u32(dsmem);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = dsmem + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(base_ptr + C::STAGES * C::STAGE_BYTES);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + C::NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    float *sbias = reinterpret_cast<float *>(tmem_holder + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int st) { return bar0 + 8u * st; };
+    auto empty_bar = [&](int st) { return bar0 + 8u * (C::STAGES + st); };
+    const uint32_t tfull0 = bar0 + 8u * (2 * C::STAGES);
+    const uint32_t tempty0 = tfull0 + 8u * C::SLOTS;
+    const uint32_t fin_bar = tempty0 + 8u * C::SLOTS;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < C::STAGES; ++st) {
+            mbar_init(full_bar(st), 1);
+            mbar_init(empty_bar(st), 1);
+        }
+        for (int a = 0; a < C::SLOTS; ++a) {
+            mbar_init(tfull0 + 8u * a, 1);
+            mbar_init(tempty0 + 8u * a, 2 * 8);      // both CTAs' epilogue warps
+        }
+        mbar_init(fin_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&p.tmA0);
+        tma_prefetch_map(&p.tmB0);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();            // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    pdl_wait();
+
+    const int npairs = (int)gridDim.x / 2;
+    const int pair = (int)blockIdx.x / 2;
+    const int num_tiles = p.num_tiles_static;           // 256-token tiles
+    const unsigned long long limit = p.wait_limit_ns ? p.wait_limit_ns : WAIT_LIMIT_NS;
+    bool aborted_peer_loads = false;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            const uint32_t full_leader0 = mapa_shared(full_bar(0), 0);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_parity = 0;
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int tile = pair + n * npairs;
+                if (tile >= num_tiles)
+                    break;
+                const int a_row = tile * 256 + (int)rank * GEMM_BM;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sA = base + stage * C::STAGE_BYTES;
+                    if (leader)
+                        mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+                    const uint32_t fb = full_leader0 + 8u * stage;
+                    tma_load_2d_pair(sA, &p.tmA0, fb, kb * GEMM_BK, a_row);
+#pragma unroll
+                    for (int part = 0; part < 3; ++part)
+                        tma_load_2d_pair(sA + C::A_BYTES + part * C::B_PART, &p.tmB0, fb, kb * GEMM_BK,
+                                         part * p.E + (int)rank * 128);
+                    // pull this CTA's hidden rows ROUTER_PF K blocks ahead into L2
+                    const int q = n * p.kblocks + kb + ROUTER_PF;
+                    const int pt = pair + (q / p.kblocks) * npairs;
+                    const int prow = pt * 256 + (int)rank * GEMM_BM;
+                    if (pt < num_tiles && prow < p.T)
+                        tma_prefetch_l2_2d(&p.tmA0, (q % p.kblocks) * GEMM_BK, prow);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                if (leader) {
+                    // the leader's full barriers count both CTAs' copies in flight
+                    for (int st = 0; st < C::STAGES; ++st)
+                        if ((issued >> st) & 1u)
+                            mbar_drain(full_bar(st), (issued_parity >> st) & 1u);
+                } else {
+                    aborted_peer_loads = issued != 0;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            uint32_t ctr = 0;   // K-block slots used so far
+            for (int n = 0; ok; ++n) {
+                const int tile = pair + n * npairs;
+                if (tile >= num_tiles)
+                    break;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                    if (kb % ROUTER_KPS == 0) {
+                        if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = base + stage * C::STAGE_BYTES;
+                    const uint32_t d = tmem + slot * 256;
+#pragma unroll
+                    for (int kk = 0; kk < GEMM_BK / 16; ++kk) {
+                        const uint64_t ad = sdesc_kmajor_sw128(sA + kk * 32);
+#pragma unroll
+                        for (int part = 0; part < 3; ++part)
+                            umma_bf16_pair(d, ad, sdesc_kmajor_sw128(sA + C::A_BYTES + part * C::B_PART + kk * 32),
+                                           C::IDESC, (kk > 0 || part > 0 || kb % ROUTER_KPS != 0) ? 1u : 0u);
+                    }
+                    umma_commit_pair(empty_bar(stage), 0x3);          // both CTAs' stage is read
+                    if (kb % ROUTER_KPS == ROUTER_KPS - 1 || kb == p.kblocks - 1) {
+                        umma_commit_pair(tfull0 + 8u * slot, 0x3);    // the slot's partial sum ready in both TMEMs
+                        ++ctr;
+                    }
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // no MMA may still be writing either CTA's TMEM when it is freed
+            umma_commit_pair(fin_bar, 0x1);
+            mbar_drain(fin_bar, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        uint32_t ctr = 0;
+        if (p.gscore) {
+            for (int e = threadIdx.x - 64; e < p.E; e += 32 * 8)
+                sbias[e] = p.bias ? p.bias[e] : 0.0f;
+            asm volatile("bar.sync 1, %0;" ::"r"(32 * 8) : "memory");
+        }
+        const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+        for (int n = 0;; ++n) {
+            const int tile = pair + n * npairs;
+            if (tile >= num_tiles)
+                break;
+            TileInfo ti;
+            ti.group = 0;
+            ti.shared = 0;
+            ti.nt = 0;
+            ti.kp = 0;
+            ti.b_row = 0;
+            ti.kblocks = p.kblocks;
+            ti.a_row = tile * 256 + (int)rank * GEMM_BM;
+            ti.out_row = ti.a_row;
+            ti.rows = min(GEMM_BM, p.T - ti.a_row);     // <= 0: the pair's last tile ends in the other CTA
+            if (!router_epilogue_tile<GK_ROUTER_WIDE>(p, ti, tmem, quad, (warp - 2) >> 2, lane, tfull0, tempty0,
+                                                      ctr, abort_flag, nullptr, limit, tile, sbias, tempty_leader))
+                break;
+        }
+    }
+
+    __syncwarp();
+    if (aborted_peer_loads) {
+        // loads of this CTA complete on the leader's barriers, which this CTA
+        // cannot wait on: give copies in flight time to land before the pair
+        // leaves (only after a wait has run out)
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 100000ull) {
+        }
+    }
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag)
+        atomicOr(p.status, ST_TIMEOUT);
+}
+
 int gemm_smem_bytes(int kind)
 {
     switch (kind) {
+    case GK_ROUTER_PAIR: return PairRouterCfg::SMEM;
     case GK_ROUTER: return GemmLayout<GK_ROUTER>::SMEM;
     case GK_ROUTER_WIDE: return GemmLayout<GK_ROUTER_WIDE>::SMEM;
     case GK_ROUTER_FUSED: return GemmLayout<GK_ROUTER_FUSED>::SMEM;
@@ -1489,6 +1739,8 @@ int gemm_smem_bytes(int kind)
 
 int gemm_tmem_cols(int kind)
 {
+    if (kind == GK_ROUTER_PAIR)
+        return PairRouterCfg::TMEM_COLS;
     switch (kind) {
     case GK_ROUTER: return GemmCfg<GK_ROUTER>::TMEM_COLS;
     case GK_ROUTER_WIDE: case GK_ROUTER_FUSED: return GemmCfg<GK_ROUTER_WIDE>::TMEM_COLS;
@@ -1517,9 +1769,54 @@ static cudaError_t launch_kind(const GemmParams &p, int grid, cudaStream_t s)
     return cudaPeekAtLastError();
 }
 
+// The pair router: grid = 2 x clusters (at most what fits at once), each
+// cluster two CTAs on one TPC, with programmatic stream serialisation.
+static cudaError_t launch_router_pair(const GemmParams &p, int grid, cudaStream_t s)
+{
+    static int configured_device = -1;
+    static int max_clusters = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(PAIR_THREADS);
+    cfg.dynamicSmemBytes = PairRouterCfg::SMEM;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (configured_device != dev) {
+        cudaError_t e = cudaFuncSetAttribute(router_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             PairRouterCfg::SMEM);
+        if (e != cudaSuccess)
+            return e;
+        cfg.gridDim = dim3(2);
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, router_pair_kernel, &cfg);
+        if (e != cudaSuccess)
+            return e;
+        if (n < 1)
+            return cudaErrorInvalidConfiguration;
+        max_clusters = n;
+        configured_device = dev;
+    }
+    const int clusters = std::max(1, std::min(grid / 2, max_clusters));
+    cfg.gridDim = dim3(2 * clusters);
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, router_pair_kernel, p);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
 cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
 {
     switch (kind) {
+    case GK_ROUTER_PAIR: return launch_router_pair(p, grid, s);
     case GK_ROUTER: return launch_kind<GK_ROUTER>(p, grid, s);
     case GK_ROUTER_WIDE: return launch_kind<GK_ROUTER_WIDE>(p, grid, s);
     case GK_ROUTER_FUSED: return launch_kind<GK_ROUTER_FUSED>(p, grid, s);

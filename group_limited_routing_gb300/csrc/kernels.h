@@ -132,12 +132,15 @@ struct WsHeader {
 // dOut_perm . W_down^T with the SwiGLU backward in its epilogue; GK_WGRAD is
 // a per-expert weight gradient (M = features, N = hidden, K = the expert's
 // bucket rows, both operands MN-major).
+// GK_ROUTER_PAIR is the 256-expert router on CTA pairs (tiles of 256 tokens,
+// each CTA loading half of the weight parts; grid = 2 x the pairs).
 // GK_ROUTER_FUSED is the 256-expert router whose epilogue also selects the
 // experts, claims every pair's row in its expert's bucket and copies the
 // hidden rows there (routing and bucketing in one launch).
 enum GemmKind {
     GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4,
-    GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7, GK_ROUTER_WIDE = 8, GK_ROUTER_FUSED = 9
+    GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7, GK_ROUTER_WIDE = 8, GK_ROUTER_FUSED = 9,
+    GK_ROUTER_PAIR = 10
 };
 constexpr int FUSED_MAX_K = 8;      // experts per token the fused router selects at most
 constexpr int GEMM_SMALL_T = 16;

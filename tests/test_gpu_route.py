@@ -64,6 +64,8 @@ def test_router_logits_accuracy(wid, T):
     # bf16 x (hi + mid + lo) products are exact; only fp32 accumulation differs
     assert err.max() <= 2e-6 + 2e-6 * np.abs(L).max(), err.max()
     print("workload %d: router logits max abs err %.3e (max |logit| %.2f)" % (wid, err.max(), np.abs(L).max()))
+    record("router logits vs exact, workload %d, T=%d" % (wid, T),
+           dict(T=int(T), max_abs_err=float(err.max()), max_abs_logit=float(np.abs(L).max())))
 
 
 def test_router_sigmoid_ulp_distance():
