@@ -195,8 +195,8 @@ def workload_name(w0, dense=0, backward=False):
 
 
 def workload_name_moe(w0):
-    if w0.wid == 4:
-        return "T=%d full-size layer, 16 hot experts (router rows x3), expert_bias~N(0,0.05)" % w0.T
+    if w0.wid in (4, 6):
+        return "T=%d full-size layer, 16 hot experts (router rows x%g), expert_bias~N(0,0.05)" % (w0.T, w0.hot_scale)
     if w0.wid == 5:
         return ("%d-layer stack (x + moe(rmsnorm(x))), T=%d, full size, per-layer expert counts and balance loss"
                 % (w0.layers, w0.T))
@@ -746,8 +746,9 @@ def main():
                     help="scrub L2 between timed steps (always on for workload 1, whose weights fit in L2)")
     ap.add_argument("--cpu-tokens-1t", type=int, default=256,
                     help="oracle sample for the single-thread CPU figure (0 = skip)")
-    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=(1, 2, 3, 4, 5),
-                    help="1 tiny, 2 decode T=16, 3 T=4096, 4 T=32768 skewed (the bench line), 5 19-layer stack")
+    ap.add_argument("--workload", type=int, default=WORKLOAD_ID, choices=(1, 2, 3, 4, 5, 6),
+                    help="1 tiny, 2 decode T=16, 3 T=4096, 4 T=32768 skewed (the bench line), 5 19-layer stack, "
+                         "6 T=32768 with ~half of all assignments on 16 hot experts")
     ap.add_argument("--lead-in-ms", type=float, default=500.0,
                     help="untimed loaded steps before the timed region (0: one step; for profiling captures)")
     ap.add_argument("--fused-router", action="store_true",

@@ -136,6 +136,9 @@ struct RouteLayout {
 // wide tiles never split.
 constexpr int ROUTER_SPLIT_UNITS = 152;
 
+// tokens from which the grouped down GEMM runs on CTA pairs
+constexpr int PAIR_DOWN_MIN_T = 16384;
+
 int router_ksplit(const moe_cfg &c)
 {
     if (c.T <= ROUTER_SIMT_MAX_T)
@@ -169,8 +172,8 @@ RouteLayout route_layout(const moe_cfg &c)
 }
 
 struct FwdLayout {
-    size_t hist, sizes, mtiles, slot_of, xperm, aint, y, total;
-    int nchunk, max_mtiles;
+    size_t hist, sizes, mtiles, ptiles, slot_of, xperm, aint, y, total;
+    int nchunk, max_mtiles, max_ptiles;
 };
 
 // xperm_rows: rows of the bucketed activations (0: k T, the compact layout;
@@ -184,6 +187,8 @@ FwdLayout fwd_layout(const moe_cfg &c, size_t xperm_rows = 0)
     // mt = rows per m-tile (GEMM_SMALL_T for the small-T GEMM kinds)
     const size_t mt = (c.T <= GEMM_SMALL_T) ? GEMM_SMALL_T : GEMM_BM;
     L.max_mtiles = (int)((K * T) / mt + c.E + (T + mt - 1) / mt + 1);
+    // 256-row pair tiles of the CTA-pair down GEMM: the same bound for 256 rows
+    L.max_ptiles = (int)((K * T) / (2 * GEMM_BM) + c.E + (T + 2 * GEMM_BM - 1) / (2 * GEMM_BM) + 1);
     size_t off = sizeof(WsHeader);
     L.hist = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
@@ -191,6 +196,8 @@ FwdLayout fwd_layout(const moe_cfg &c, size_t xperm_rows = 0)
     off = align_up(off + (size_t)c.E * 4, 256);
     L.mtiles = off;
     off = align_up(off + (size_t)L.max_mtiles * 16, 256);
+    L.ptiles = off;
+    off = align_up(off + (size_t)L.max_ptiles * 16, 256);
     L.slot_of = off;
     off = align_up(off + T * K * 4, 256);
     L.xperm = off;
@@ -505,6 +512,7 @@ LayerLayout layer_layout(const moe_cfg &c, int flags)
     L.f.hist += b;
     L.f.sizes += b;
     L.f.mtiles += b;
+    L.f.ptiles += b;
     L.f.slot_of += b;
     L.f.xperm += b;
     L.f.aint += b;
@@ -606,8 +614,12 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
             GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
         GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
         GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
-                                                      xperm, mtiles, hdr, s));
+                                                      xperm, mtiles, hdr, s, at<int4>(ws, L.ptiles)));
     }
+    // the down GEMM runs on CTA pairs over 256-row tiles at large T (the
+    // bucketing above writes their list); below that the 128-row tiles waste
+    // fewer rows in buckets' part-filled last tiles, which measured faster
+    const bool pair_down = !offs && c.T >= PAIR_DOWN_MIN_T;
 
     // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E);
     // for T <= GEMM_SMALL_T no bucket has more than T rows: the small kinds
@@ -664,8 +676,14 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
     p2.kT = (int)kT;
     p2.ld_out = c.H;
     p2.status = &hdr->status;
-    GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(small ? GK_DOWN_SMALL : GK_DOWN, p2,
-                                          std::min(sms, L.max_mtiles * p2.n_tiles), s));
+    if (pair_down) {
+        p2.mtiles = at<int4>(ws, L.ptiles);
+        p2.num_mtiles = &hdr->num_ptiles;
+        GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(GK_DOWN_PAIR, p2, 2 * std::min(sms / 2, L.max_ptiles * p2.n_tiles), s));
+    } else {
+        GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(small ? GK_DOWN_SMALL : GK_DOWN, p2,
+                                              std::min(sms, L.max_mtiles * p2.n_tiles), s));
+    }
 
     // weighted combine + shared expert (+ residual), one rounding to bf16
     GLR_LAUNCH(KID_COMBINE, launch_combine(y, slot_of, topk_w, residual, c.T, c.H, c.k, out, s, -1, topk_idx, offs,

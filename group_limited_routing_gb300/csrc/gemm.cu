@@ -1720,10 +1720,252 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
         atomicOr(p.status, ST_TIMEOUT);
 }
 
+// ---------------------------------------------------------------------------
+// GK_DOWN_PAIR: the grouped down GEMM on CTA pairs (tcgen05 cta_group::2).
+// A pair tile is 256 consecutive rows of one bucket (the pair-tile list of
+// bucket_scatter) x 256 hidden columns: each CTA loads its own 128 rows of the
+// intermediate and 128 of the 256 W_down columns (two 64-column MN-major
+// atoms), so a stage is 16 + 16 KB instead of 16 + 32 KB and six stages fit
+// beside the epilogue's staging buffers; the even CTA issues M = 256, N = 256
+// MMAs over both CTAs' shared memory and each CTA's TMEM receives its 128 rows.
+// Rows of a pair tile beyond its bucket (the bucket's last tile) belong to the
+// next bucket or to nothing; their results are never stored.  The epilogue is
+// the single-CTA down GEMM's (bf16 rows, TMA stores), per CTA.
+struct PairDownCfg {
+    static constexpr int A_BYTES = GEMM_BM * GEMM_BK * 2;   // 16 KB
+    static constexpr int B_ATOM = 64 * GEMM_BK * 2;         // 64 columns x 64 K, 8 KB
+    static constexpr int B_BYTES = 2 * B_ATOM;              // this CTA's 128 columns
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = 6;
+    static constexpr int SLOTS = 2;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NBUF = 2;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(256, 256, false, true);
+    static constexpr int STAGING = NBUF * 4 * 4096;
+    static constexpr int NBARS = 2 * STAGES + 2 * SLOTS + 1;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + STAGING + 1024 /*align*/ + NBARS * 8 + 16;
+    static_assert(SMEM <= 232448, "more than 227 KB of shared memory");
+    static_assert(STAGE_BYTES % 1024 == 0, "swizzle atoms need 1024-B alignment");
+};
+static_assert(GemmCfg<GK_DOWN>::NBUF == PairDownCfg::NBUF, "the pair down GEMM reuses the down GEMM's epilogue");
+
+constexpr int PAIR_DOWN_THREADS = 64 + 32 * 4;
+
+__global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const __grid_constant__ GemmParams p)
+{
+    using C = PairDownCfg;
+    extern __shared__ uint8_t dsmem[];
+    const uint32_t raw = smem_u32(dsmem);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *base_ptr = dsmem + (base - raw);
+    uint8_t *staging = base_ptr + C::STAGES * C::STAGE_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(staging + C::STAGING);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + C::NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int st) { return bar0 + 8u * st; };
+    auto empty_bar = [&](int st) { return bar0 + 8u * (C::STAGES + st); };
+    const uint32_t tfull0 = bar0 + 8u * (2 * C::STAGES);
+    const uint32_t tempty0 = tfull0 + 8u * C::SLOTS;
+    const uint32_t fin_bar = tempty0 + 8u * C::SLOTS;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < C::STAGES; ++st) {
+            mbar_init(full_bar(st), 1);
+            mbar_init(empty_bar(st), 1);
+        }
+        for (int a = 0; a < C::SLOTS; ++a) {
+            mbar_init(tfull0 + 8u * a, 1);
+            mbar_init(tempty0 + 8u * a, 2 * 4);      // both CTAs' epilogue warps
+        }
+        mbar_init(fin_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_map(&p.tmA0);
+        tma_prefetch_map(&p.tmB0);
+        tma_prefetch_map(&p.tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();            // both CTAs' barriers initialised and TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    pdl_wait();                // the pair-tile list and the A rows come from earlier kernels
+
+    const int npairs = (int)gridDim.x / 2;
+    const int pair = (int)blockIdx.x / 2;
+    const int num_tiles = (*p.num_mtiles) * p.n_tiles;
+    const unsigned long long limit = p.wait_limit_ns ? p.wait_limit_ns : WAIT_LIMIT_NS;
+    bool aborted_peer_loads = false;
+
+    // this CTA's half of pair tile `tile`
+    auto half_tile = [&](int tile) {
+        const int4 m = p.mtiles[tile / p.n_tiles];
+        TileInfo ti;
+        ti.group = m.x;
+        ti.shared = (m.x == p.E);
+        ti.nt = tile % p.n_tiles;
+        ti.kblocks = p.kblocks;
+        ti.kp = 0;
+        ti.b_row = 0;
+        ti.a_row = (ti.shared ? p.kT + m.y : m.y) + (int)rank * GEMM_BM;   // intermediate rows
+        ti.out_row = ti.a_row;
+        ti.rows = min(GEMM_BM, m.z - (int)rank * GEMM_BM);                 // <= 0: nothing to store
+        return ti;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            const uint32_t full_leader0 = mapa_shared(full_bar(0), 0);
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, issued_parity = 0;
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int tile = pair + n * npairs;
+                if (tile >= num_tiles)
+                    break;
+                const TileInfo ti = half_tile(tile);
+                const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
+                const int col0 = ti.nt * 256 + (int)rank * 128;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sA = base + stage * C::STAGE_BYTES;
+                    if (leader)
+                        mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
+                    const uint32_t fb = full_leader0 + 8u * stage;
+                    const int k0 = kb * GEMM_BK;
+                    const int krow = (ti.shared ? 0 : ti.group * p.I) + k0;
+                    tma_load_2d_pair(sA, &p.tmA0, fb, k0, ti.a_row);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q)
+                        tma_load_2d_pair(sA + C::A_BYTES + q * C::B_ATOM, mb, fb, col0 + q * 64, krow);
+                    issued |= 1u << stage;
+                    issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                if (leader) {
+                    for (int st = 0; st < C::STAGES; ++st)
+                        if ((issued >> st) & 1u)
+                            mbar_drain(full_bar(st), (issued_parity >> st) & 1u);
+                } else {
+                    aborted_peer_loads = issued != 0;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------------ MMA issuer
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            uint32_t ctr = 0;   // tile accumulators used so far
+            for (int n = 0; ok; ++n) {
+                const int tile = pair + n * npairs;
+                if (tile >= num_tiles)
+                    break;
+                const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit))
+                    break;
+                tc_fence_after();
+                const uint32_t d = tmem + slot * 256;
+                for (int kb = 0; kb < p.kblocks; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = base + stage * C::STAGE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < GEMM_BK / 16; ++kk)
+                        // 16 K rows = two 8-row atoms = 2048 B further into each 64-wide N atom
+                        umma_bf16_pair(d, sdesc_kmajor_sw128(sA + kk * 32),
+                                       sdesc_mnmajor_sw128(sA + C::A_BYTES + kk * 2048, C::B_ATOM), C::IDESC,
+                                       (kb > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit_pair(empty_bar(stage), 0x3);          // both CTAs' stage is read
+                    if (++stage == C::STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) {
+                    umma_commit_pair(tfull0 + 8u * slot, 0x3);        // tile accumulator ready in both TMEMs
+                    ++ctr;
+                }
+            }
+            umma_commit_pair(fin_bar, 0x1);
+            mbar_drain(fin_bar, 0);
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;
+        uint8_t *stage = staging + (warp - 2) * (C::NBUF * 4096);
+        int buf = 0;
+        uint32_t ctr = 0;
+        const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+        for (int n = 0;; ++n) {
+            const int tile = pair + n * npairs;
+            if (tile >= num_tiles)
+                break;
+            const TileInfo ti = half_tile(tile);
+            const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+            int ok = 1;
+            if (lane == 0)
+                ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag, limit) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok)
+                break;
+            __syncwarp();
+            tc_fence_after();
+            const uint32_t tacc = tmem + ((uint32_t)(quad * 32) << 16) + slot * 256;
+            epilogue_tile<GK_DOWN>(p, ti, tacc, quad, lane, stage, buf);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive_cluster(tempty_leader + 8u * slot);
+            ++ctr;
+        }
+        if (lane == 0)
+            bulk_wait_group_all();              // this warp's output stores have completed
+    }
+
+    __syncwarp();
+    if (aborted_peer_loads) {
+        const unsigned long long t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 100000ull) {
+        }
+    }
+    tc_fence_before();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, C::TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag)
+        atomicOr(p.status, ST_TIMEOUT);
+}
+
 int gemm_smem_bytes(int kind)
 {
     switch (kind) {
     case GK_ROUTER_PAIR: return PairRouterCfg::SMEM;
+    case GK_DOWN_PAIR: return PairDownCfg::SMEM;
     case GK_ROUTER: return GemmLayout<GK_ROUTER>::SMEM;
     case GK_ROUTER_WIDE: return GemmLayout<GK_ROUTER_WIDE>::SMEM;
     case GK_ROUTER_FUSED: return GemmLayout<GK_ROUTER_FUSED>::SMEM;
@@ -1741,6 +1983,8 @@ int gemm_tmem_cols(int kind)
 {
     if (kind == GK_ROUTER_PAIR)
         return PairRouterCfg::TMEM_COLS;
+    if (kind == GK_DOWN_PAIR)
+        return PairDownCfg::TMEM_COLS;
     switch (kind) {
     case GK_ROUTER: return GemmCfg<GK_ROUTER>::TMEM_COLS;
     case GK_ROUTER_WIDE: case GK_ROUTER_FUSED: return GemmCfg<GK_ROUTER_WIDE>::TMEM_COLS;
@@ -1769,10 +2013,15 @@ static cudaError_t launch_kind(const GemmParams &p, int grid, cudaStream_t s)
     return cudaPeekAtLastError();
 }
 
-// The pair router: grid = 2 x clusters (at most what fits at once), each
+// A CTA-pair kernel: grid = 2 x clusters (at most what fits at once), each
 // cluster two CTAs on one TPC, with programmatic stream serialisation.
-static cudaError_t launch_router_pair(const GemmParams &p, int grid, cudaStream_t s)
+template <int KIND>
+static cudaError_t launch_pair(const GemmParams &p, int grid, cudaStream_t s)
 {
+    constexpr bool ROUTER = (KIND == GK_ROUTER_PAIR);
+    auto kernel = ROUTER ? router_pair_kernel : down_pair_kernel;
+    constexpr int SMEM = ROUTER ? PairRouterCfg::SMEM : PairDownCfg::SMEM;
+    constexpr int THREADS = ROUTER ? PAIR_THREADS : PAIR_DOWN_THREADS;
     static int configured_device = -1;
     static int max_clusters = 0;
     int dev = 0;
@@ -1785,19 +2034,18 @@ static cudaError_t launch_router_pair(const GemmParams &p, int grid, cudaStream_
     attr[1].val.clusterDim.x = 2;
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(PAIR_THREADS);
-    cfg.dynamicSmemBytes = PairRouterCfg::SMEM;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(router_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             PairRouterCfg::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess)
             return e;
         cfg.gridDim = dim3(2);
         int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, router_pair_kernel, &cfg);
+        e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
         if (e != cudaSuccess)
             return e;
         if (n < 1)
@@ -1807,7 +2055,7 @@ static cudaError_t launch_router_pair(const GemmParams &p, int grid, cudaStream_
     }
     const int clusters = std::max(1, std::min(grid / 2, max_clusters));
     cfg.gridDim = dim3(2 * clusters);
-    const cudaError_t le = cudaLaunchKernelEx(&cfg, router_pair_kernel, p);
+    const cudaError_t le = cudaLaunchKernelEx(&cfg, kernel, p);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
@@ -1816,7 +2064,8 @@ static cudaError_t launch_router_pair(const GemmParams &p, int grid, cudaStream_
 cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
 {
     switch (kind) {
-    case GK_ROUTER_PAIR: return launch_router_pair(p, grid, s);
+    case GK_ROUTER_PAIR: return launch_pair<GK_ROUTER_PAIR>(p, grid, s);
+    case GK_DOWN_PAIR: return launch_pair<GK_DOWN_PAIR>(p, grid, s);
     case GK_ROUTER: return launch_kind<GK_ROUTER>(p, grid, s);
     case GK_ROUTER_WIDE: return launch_kind<GK_ROUTER_WIDE>(p, grid, s);
     case GK_ROUTER_FUSED: return launch_kind<GK_ROUTER_FUSED>(p, grid, s);

@@ -121,7 +121,8 @@ struct WsHeader {
     int num_mtiles;  // m-tiles of the grouped GEMMs (written on the device)
     int tile_ctr[2]; // claim counters of the two weight-gradient launches (zeroed on the device)
     int fin_ticket;  // blocks of the balance-loss reduction done (back to zero at its end)
-    int pad[59];
+    int num_ptiles;  // 256-row pair tiles of the CTA-pair grouped GEMM (written on the device)
+    int pad[58];
 };
 
 // The _SMALL kinds are the grouped GEMMs for T <= GEMM_SMALL_T (decode): every
@@ -134,13 +135,15 @@ struct WsHeader {
 // bucket rows, both operands MN-major).
 // GK_ROUTER_PAIR is the 256-expert router on CTA pairs (tiles of 256 tokens,
 // each CTA loading half of the weight parts; grid = 2 x the pairs).
+// GK_DOWN_PAIR is the grouped down GEMM on CTA pairs: 256-row pair tiles of
+// one bucket, each CTA loading its 128 A rows and half of the W_down columns.
 // GK_ROUTER_FUSED is the 256-expert router whose epilogue also selects the
 // experts, claims every pair's row in its expert's bucket and copies the
 // hidden rows there (routing and bucketing in one launch).
 enum GemmKind {
     GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4,
     GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7, GK_ROUTER_WIDE = 8, GK_ROUTER_FUSED = 9,
-    GK_ROUTER_PAIR = 10
+    GK_ROUTER_PAIR = 10, GK_DOWN_PAIR = 11
 };
 constexpr int FUSED_MAX_K = 8;      // experts per token the fused router selects at most
 constexpr int GEMM_SMALL_T = 16;
@@ -155,7 +158,7 @@ struct GemmParams {
     CUtensorMap tmB1;   // gate_up: shared_gate_up [2I, H]; down: shared_down [I, H]
     CUtensorMap tmOut;  // grouped: the output, boxes of 64 columns x 32 rows (TMA stores)
     void *out;          // router: logits fp32 [T, E]; gate_up: intermediate bf16; down: Y bf16
-    const int4 *mtiles; // grouped: {group, first row, rows, 0}
+    const int4 *mtiles; // grouped: {group, first row, rows, 0} (pair kinds: the 256-row pair tiles)
     const int *num_mtiles;
     int num_tiles_static; // router: tiles known on the host
     int n_tiles;          // n-tiles per m-tile
@@ -255,9 +258,11 @@ cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t 
 // hist [E][nchunk] -> per-chunk starts inside each bucket (relative); sizes[E]
 cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s);
 
+// ptiles (nullable): also the 256-row pair-tile list (hdr->num_ptiles)
 cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
                                   const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
-                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s);
+                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s,
+                                  int4 *ptiles = nullptr);
 
 // T <= BUCKET_SMALL_MAX_T: hist, scan and scatter in one launch (same outputs)
 constexpr int BUCKET_SMALL_MAX_T = 32;

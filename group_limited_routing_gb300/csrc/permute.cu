@@ -188,53 +188,70 @@ cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes,
 // rows were bucketed at e * cap + r (the fused router's layout): the fourth
 // field of every m-tile is then its first A row (the token for the shared
 // expert's m-tiles).
+//
+// With ptiles (the forward's CTA-pair GEMMs), the block also writes the list
+// of pair tiles: every bucket (and the shared expert's T rows) cut into
+// 256-row tiles {group, first row, rows <= 256, 0}, their count in
+// hdr->num_ptiles.
 __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, int K, int *offset, int *tstart,
                                int *wsum_rows, int *wsum_tiles, bool write_tiles, int4 *__restrict__ mtiles,
                                WsHeader *__restrict__ hdr, int pad = 1, int2 *__restrict__ eoff = nullptr,
-                               int shared_base = 0, int cap = 0)
+                               int shared_base = 0, int cap = 0, int4 *__restrict__ ptiles = nullptr)
 {
     __shared__ int true_rows;
+    __shared__ int wsum_pt[8];
+    __shared__ int pt_total;
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int e = threadIdx.x;   // blockDim.x == 256 >= E
     const int n0 = (e < E) ? sizes[e] : 0;
     const int n = (n0 + pad - 1) / pad * pad;    // rows the bucket occupies
     const int nt = (n0 + GEMM_BM - 1) / GEMM_BM;
+    const int np = (n0 + 2 * GEMM_BM - 1) / (2 * GEMM_BM);
     if (threadIdx.x == 0)
         true_rows = 0;
     __syncthreads();
     if (n0)
         atomicAdd(&true_rows, n0);               // integer: exact in any order
-    int a = n, b = nt;           // inclusive warp scans
+    int a = n, b = nt, c = np;   // inclusive warp scans
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
         const int ya = __shfl_up_sync(0xffffffffu, a, off);
         const int yb = __shfl_up_sync(0xffffffffu, b, off);
+        const int yc = __shfl_up_sync(0xffffffffu, c, off);
         if (lane >= off) {
             a += ya;
             b += yb;
+            c += yc;
         }
     }
     if (lane == 31) {
         wsum_rows[w] = a;
         wsum_tiles[w] = b;
+        wsum_pt[w] = c;
     }
     __syncthreads();
-    int ra = 0, rb = 0;
+    int ra = 0, rb = 0, rc = 0;
     for (int q = 0; q < w; ++q) {
         ra += wsum_rows[q];
         rb += wsum_tiles[q];
+        rc += wsum_pt[q];
     }
     offset[e] = ra + a - n;
     tstart[e] = rb + b - nt;
+    const int pstart = rc + c - np;
     __syncthreads();
     if (threadIdx.x == 0) {
-        int off = 0, tiles = 0;
+        int off = 0, tiles = 0, pts = 0;
         for (int q = 0; q < 8; ++q) {
             off += wsum_rows[q];
             tiles += wsum_tiles[q];
+            pts += wsum_pt[q];
         }
         offset[E] = off;             // padded rows of all buckets (== K*T for pad 1 and valid indices)
         tstart[E] = tiles;
+        pt_total = pts;
+        if (write_tiles && ptiles)
+            hdr->num_ptiles = pts + (T + 2 * GEMM_BM - 1) / (2 * GEMM_BM);
         if (write_tiles) {
             hdr->num_mtiles = tiles + (T + GEMM_BM - 1) / GEMM_BM;
             if (true_rows != K * T)
@@ -253,6 +270,15 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
         const int ntile_sh = (T + GEMM_BM - 1) / GEMM_BM;
         for (int i = threadIdx.x; i < ntile_sh; i += blockDim.x)
             mtiles[tstart[E] + i] = make_int4(E, i * GEMM_BM, min(GEMM_BM, T - i * GEMM_BM), cap > 0 ? i * GEMM_BM : 0);
+        if (ptiles) {
+            constexpr int PM = 2 * GEMM_BM;
+            if (e < E)
+                for (int i = 0, r = 0; r < n0; ++i, r += PM)
+                    ptiles[pstart + i] = make_int4(e, offset[e] + r, min(PM, n0 - r), 0);
+            const int np_sh = (T + PM - 1) / PM;
+            for (int i = threadIdx.x; i < np_sh; i += blockDim.x)
+                ptiles[pt_total + i] = make_int4(E, i * PM, min(PM, T - i * PM), 0);
+        }
     }
 }
 
@@ -279,7 +305,8 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
                                                              const int32_t *__restrict__ sizes, int T, int H,
                                                              int E, int K, int32_t *__restrict__ slot_of,
                                                              uint16_t *__restrict__ x_perm, int4 *__restrict__ mtiles,
-                                                             WsHeader *__restrict__ hdr, ScatterBwd bw)
+                                                             WsHeader *__restrict__ hdr, ScatterBwd bw,
+                                                             int4 *__restrict__ ptiles)
 {
     pdl_wait();
     __shared__ int offset[258];
@@ -293,7 +320,7 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
     const int nt = min(PERM_CHUNK, T - t0);
     const bool backward = bw.do_perm != nullptr;
     bucket_offsets(sizes, T, E, K, offset, tstart, wsum_rows, wsum_tiles, blockIdx.x == 0, mtiles, hdr,
-                   backward ? BWD_ROW_ALIGN : 1, bw.eoff, bw.shared_base);
+                   backward ? BWD_ROW_ALIGN : 1, bw.eoff, bw.shared_base, 0, ptiles);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         next[e] = offset[e] + chunk_base[(size_t)e * gridDim.x + blockIdx.x];   // [expert][chunk]
     __syncthreads();
@@ -374,13 +401,13 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
 
 cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
                                   const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
-                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s)
+                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s, int4 *ptiles)
 {
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
     const ScatterBwd none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
-                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none);
+                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none, ptiles);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
@@ -396,7 +423,7 @@ cudaError_t launch_bucket_scatter_bwd(const int32_t *idx, const uint16_t *x, con
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
     const ScatterBwd bw = {dout, w, do_perm, w_perm, eoff, shared_base};
     const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
-                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, bw);
+                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, bw, (int4 *)nullptr);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

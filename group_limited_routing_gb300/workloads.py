@@ -57,6 +57,10 @@ WORKLOADS = {
                 T=32768, H=2048, bias="normal0.05", hot_experts_per_group=2, hot_scale=3.0),
     5: Workload(5, "19-layer stack T=8192 full size, residual, per-layer counts and aux loss",
                 T=8192, H=2048, layers=19, residual=True),
+    # workload 4's recipe with the hot rows scaled x5 instead of x3: about half
+    # of all assignments then land on the 16 hot experts (x3 gives ~36%)
+    6: Workload(6, "T=32768 full size, 16 hot experts (router rows x5, ~50% of assignments), bias~N(0,0.05)",
+                T=32768, H=2048, bias="normal0.05", hot_experts_per_group=2, hot_scale=5.0),
 }
 
 

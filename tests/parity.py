@@ -169,6 +169,27 @@ def compare_counts(gpu_counts, gpu_idx, ref_counts, ref_idx, near, E):
     assert np.array_equal(g_excl, r_excl)
 
 
+def covering_tokens(idx, T, E, mt=128):
+    """Tokens that put at least one compared row into every m-tile of the
+    grouped GEMMs, from a routing idx [T, k] (host numpy): the bucket of expert
+    e holds its (token, j) pairs in ascending (token, j) order, cut into
+    mt-row m-tiles; one token per m-tile (its first row), the token of every
+    bucket's last row (its part-filled last tile), and for the shared expert
+    (all T tokens in order) one token per m-tile plus the last."""
+    idx = np.asarray(idx)
+    k = idx.shape[1]
+    flat = idx.ravel().astype(np.int64)
+    order = np.argsort(flat, kind="stable")          # pair ids, by expert then (token, j)
+    experts = flat[order]
+    starts = np.searchsorted(experts, np.arange(E))
+    r = np.arange(flat.size) - starts[experts]
+    first_of_tile = (r % mt) == 0
+    last_of_bucket = np.r_[experts[1:] != experts[:-1], True]
+    tok = order[first_of_tile | last_of_bucket] // k
+    shared = np.r_[np.arange(0, T, mt), T - 1]
+    return np.unique(np.concatenate([tok, shared])).astype(np.int32)
+
+
 def output_errors(out, ref):
     out = np.asarray(out, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)

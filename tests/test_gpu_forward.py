@@ -12,7 +12,7 @@ import torch
 
 import oracle
 from group_limited_routing_gb300 import moe, workloads as wl
-from parity import assert_output_close, bf16_to_f64
+from parity import assert_output_close, bf16_to_f64, covering_tokens
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -57,17 +57,27 @@ def small_layer(T, H=512, I=128, E=256, seed=0):
     return cfg, d
 
 
-@pytest.mark.parametrize("wid,T,nsample", [(1, 128, None), (2, 16, None), (3, 4096, 256), (4, 32768, 256),
-                                           (5, 8192, 192)])
+@pytest.mark.parametrize("wid,T,nsample", [(1, 128, None), (2, 16, None), (3, 4096, 256), (4, 32768, "cover"),
+                                           (5, 8192, 192), (6, 32768, "cover")])
 def test_forward_matches_oracle_on_workloads(wid, T, nsample):
+    """nsample "cover": every m-tile of both grouped GEMMs (each bucket's
+    128-row tiles, its part-filled last tile, the shared expert's tiles) has
+    at least one compared row; workload 6 puts ~half of all rows on 16 hot
+    experts (~8k rows each)."""
     w0 = wl.WORKLOADS[wid].with_T(T)
     d = wl.layer_inputs(w0, DEV)
     cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
-    idx, w, _, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    idx, w, counts, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
     tokens = None
-    if nsample is not None:
+    if nsample == "cover":
+        tokens = covering_tokens(idx.cpu().numpy(), T, cfg.E)
+    elif nsample is not None:
         tokens = np.union1d(wl.token_sample(T, nsample, seed=wid).numpy(), [0, T - 1]).astype(np.int32)
-    check(cfg, d, idx, w, tokens, what="workload %d T=%d" % (wid, T))
+    if w0.hot_experts_per_group:
+        c = counts.cpu().numpy()
+        print("workload %d: hot-expert share %.3f" % (wid, c[wl.hot_experts(w0).numpy()].sum() / c.sum()))
+    check(cfg, d, idx, w, tokens, what="workload %d T=%d (%s tokens)" % (wid, T, "all" if tokens is None
+                                                                           else len(tokens)))
 
 
 @pytest.mark.parametrize("T", [1, 7, 16, 17, 32, 33, 128, 300, 1000])
@@ -268,5 +278,33 @@ def test_large_batch_sampled_parity():
     torch.cuda.synchronize()
     assert int(counts.sum()) == 8 * T
     assert torch.equal(counts.cpu(), torch.bincount(idx.cpu().view(-1).long(), minlength=256).to(torch.int32))
-    tokens = np.union1d(wl.token_sample(T, 96, seed=77).numpy(), [0, T - 1]).astype(np.int32)
-    check(cfg, d, idx, w, tokens, what="T=%d sampled" % T)
+    tokens = covering_tokens(idx.cpu().numpy(), T, cfg.E)
+    check(cfg, d, idx, w, tokens, what="T=%d, a row in every m-tile (%d tokens)" % (T, len(tokens)))
+
+
+@pytest.mark.parametrize("T", [16384, 20000])
+def test_forward_pair_tiles_edge_buckets(T):
+    """The CTA-pair down GEMM (256-row pair tiles, T >= 16384) on bucket
+    sizes that end a pair tile in every way: empty, 1, 127, 128, 129, 255,
+    256, 257 and 383 rows, one bucket of ~half of all rows, the rest spread;
+    every m-tile compared."""
+    k, E = 8, 256
+    cfg, d = small_layer(T, seed=6)
+    rng = np.random.default_rng(T)
+    sizes = {3: 1, 4: 127, 5: 128, 6: 129, 7: 255, 8: 256, 9: 257, 10: 383}
+    pairs = []
+    for e, n in sizes.items():
+        pairs += [e] * n
+    pairs += [40] * (T * k // 2)                   # one hot bucket, half of all rows
+    rest = list(range(50, 250))
+    need = T * k - len(pairs)
+    pairs += (rest * (need // len(rest) + 1))[:need]
+    pairs = np.array(pairs, dtype=np.int32)
+    rng.shuffle(pairs)
+    idx = pairs.reshape(T, k).copy()
+    counts = np.bincount(idx.ravel(), minlength=E)
+    assert [counts[e] for e in sizes] == list(sizes.values()) and counts[0] == 0
+    w = rng.random((T, k)).astype(np.float32)
+    tokens = covering_tokens(idx, T, E)
+    check(cfg, d, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), tokens,
+          what="pair tiles T=%d (%d tokens)" % (T, len(tokens)))

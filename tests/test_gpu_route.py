@@ -29,7 +29,7 @@ def run_route(cfg, x, W, bias, aux=True):
         (P.cpu().numpy() if P is not None else None), (float(loss.item()) if loss is not None else None)
 
 
-@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (3, 4096), (4, 32768), (5, 8192)])
+@pytest.mark.parametrize("wid,T", [(1, 128), (2, 16), (3, 4096), (4, 32768), (5, 8192), (6, 32768)])
 def test_route_matches_oracle(wid, T):
     w0 = wl.WORKLOADS[wid].with_T(T)
     d = wl.layer_inputs(w0, DEV, with_experts=False)

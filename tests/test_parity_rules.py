@@ -100,3 +100,26 @@ def test_exact_group_tie_allows_either_side_only():
     rep = {}
     compare_routing(other[None, :].astype(np.int32), _weights(s, other)[None, :].astype(np.float32), ref, 256, rep)
     assert rep["near_tie_tokens"] == 1 and rep["near_tie_differ"] == 1
+
+
+def test_covering_tokens_reach_every_m_tile():
+    """covering_tokens picks, from a routing, tokens whose rows fall into every
+    128-row m-tile of every bucket (stable (token, j) order inside a bucket),
+    into every bucket's last row, and into every m-tile of the shared expert."""
+    from parity import covering_tokens
+    rng = np.random.default_rng(3)
+    T, k, E = 3000, 8, 256
+    p = np.ones(E)
+    p[:4] = 200.0                                    # a few long buckets
+    p[200:] = 0.0                                    # and empty ones
+    idx = rng.choice(E, size=(T, k), p=p / p.sum()).astype(np.int32)
+    tok = set(covering_tokens(idx, T, E).tolist())
+    for e in range(E):
+        rows = [t for t in range(T) for j in range(k) if idx[t, j] == e]   # bucket order
+        for r0 in range(0, len(rows), 128):
+            assert any(t in tok for t in rows[r0:r0 + 128]), (e, r0)
+        if rows:
+            assert rows[-1] in tok
+    for r0 in range(0, T, 128):
+        assert any(t in tok for t in range(r0, min(T, r0 + 128)))
+    assert T - 1 in tok
