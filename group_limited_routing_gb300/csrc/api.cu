@@ -137,7 +137,7 @@ struct RouteLayout {
 constexpr int ROUTER_SPLIT_UNITS = 152;
 
 // tokens from which the grouped down GEMM runs on CTA pairs
-constexpr int PAIR_DOWN_MIN_T = 16384;
+constexpr int PAIR_DOWN_MIN_T = 24576;
 
 int router_ksplit(const moe_cfg &c)
 {
@@ -618,7 +618,9 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
     }
     // the down GEMM runs on CTA pairs over 256-row tiles at large T (the
     // bucketing above writes their list); below that the 128-row tiles waste
-    // fewer rows in buckets' part-filled last tiles, which measured faster
+    // fewer rows in buckets' part-filled last tiles (measured, workload-4
+    // recipe: T = 4096 / 8192 / 16384 / 32768 took 0.119 / 0.169 / 0.280 /
+    // 0.510 ms on single CTAs and 0.133 / 0.181 / 0.283 / 0.492 ms on pairs)
     const bool pair_down = !offs && c.T >= PAIR_DOWN_MIN_T;
 
     // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E);

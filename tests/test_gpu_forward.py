@@ -282,9 +282,9 @@ def test_large_batch_sampled_parity():
     check(cfg, d, idx, w, tokens, what="T=%d, a row in every m-tile (%d tokens)" % (T, len(tokens)))
 
 
-@pytest.mark.parametrize("T", [16384, 20000])
+@pytest.mark.parametrize("T", [24576, 30000])
 def test_forward_pair_tiles_edge_buckets(T):
-    """The CTA-pair down GEMM (256-row pair tiles, T >= 16384) on bucket
+    """The CTA-pair down GEMM (256-row pair tiles, T >= 24576) on bucket
     sizes that end a pair tile in every way: empty, 1, 127, 128, 129, 255,
     256, 257 and 383 rows, one bucket of ~half of all rows, the rest spread;
     every m-tile compared."""
