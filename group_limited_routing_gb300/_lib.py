@@ -37,7 +37,8 @@ EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router
            "moe_profile_enable", "moe_profile_read", "moe_kernel_name", "moe_strerror", "moe_route_static",
            "moe_debug_inject_timeout", "moe_rmsnorm", "moe_expert_feedback", "moe_prepare_router",
            "moe_route_prepared", "moe_dense_workspace_bytes", "moe_dense_ffn", "moe_backward",
-           "moe_layer_workspace_bytes", "moe_layer", "moe_router_scores")
+           "moe_layer_workspace_bytes", "moe_layer", "moe_router_scores", "moe_ep_dispatch_workspace_bytes",
+           "moe_ep_dispatch", "moe_expert_rows_workspace_bytes", "moe_expert_rows", "moe_combine")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
 MOE_LAYER_FUSED_ROUTER = 1
 MOE_KERNEL_COUNT = 18
@@ -117,6 +118,16 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
         lib.moe_debug_inject_timeout.restype = ctypes.c_int
         lib.moe_route_static.argtypes = [C, P, P, P, P, P, P, P, P, P, P]
         lib.moe_route_static.restype = ctypes.c_int
+        lib.moe_ep_dispatch_workspace_bytes.argtypes = [C, I32]
+        lib.moe_ep_dispatch_workspace_bytes.restype = S
+        lib.moe_ep_dispatch.argtypes = [C, I32, P, P, P, P, P, P, P, S, P]
+        lib.moe_ep_dispatch.restype = ctypes.c_int
+        lib.moe_expert_rows_workspace_bytes.argtypes = [C, I32]
+        lib.moe_expert_rows_workspace_bytes.restype = S
+        lib.moe_expert_rows.argtypes = [C, I32, P, P, P, P, P, P, S, P]
+        lib.moe_expert_rows.restype = ctypes.c_int
+        lib.moe_combine.argtypes = [C, P, ctypes.c_int64, ctypes.c_int64, P, P, P, P, P]
+        lib.moe_combine.restype = ctypes.c_int
         lib.moe_router_scores.argtypes = [P, P, ctypes.c_int64, P]
         lib.moe_router_scores.restype = ctypes.c_int
         lib.moe_strerror.argtypes = [ctypes.c_int]

@@ -589,8 +589,12 @@ int fused_route(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const 
 int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,
                  const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const int32_t *topk_idx,
                  const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *ws, const FwdLayout &L,
-                 const int32_t *offs, int sms, cudaStream_t s, int &launches, bool hist_ready = false)
+                 const int32_t *offs, int sms, cudaStream_t s, int &launches, bool hist_ready = false,
+                 bool with_shared = true)
 {
+    // with_shared = false (moe_expert_rows): no shared-expert group, k = 1, and
+    // out receives every pair's unweighted expert row in pair order instead
+    // of the combine
     WsHeader *hdr = header(ws);
     int32_t *hist = at<int32_t>(ws, L.hist);
     int4 *mtiles = at<int4>(ws, L.mtiles);
@@ -603,7 +607,7 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
     // bucket the (token, expert) pairs by expert (stable), gather rows --
     // unless the fused router has done it (bucket e at rows e T .., offsets in offs)
     int32_t *sizes = at<int32_t>(ws, L.sizes);
-    if (!offs && c.T <= BUCKET_SMALL_MAX_T) {
+    if (!offs && c.T <= BUCKET_SMALL_MAX_T && with_shared) {
         // a handful of tokens: the three bucketing steps in one launch
         const int mt = c.T <= GEMM_SMALL_T ? GEMM_SMALL_T : GEMM_BM;
         GLR_LAUNCH(KID_SCATTER, launch_bucket_small(topk_idx, hidden, c.T, c.H, c.E, c.k, mt, sizes, slot_of,
@@ -614,7 +618,12 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
             GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
         GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
         GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
-                                                      xperm, mtiles, hdr, s, at<int4>(ws, L.ptiles)));
+                                                      xperm, mtiles, hdr, s, at<int4>(ws, L.ptiles), with_shared));
+    }
+    if (!with_shared) {
+        // (placeholders for the shared group's operands, which no tile reads)
+        shared_gate_up = W_gate_up;
+        shared_down = W_down;
     }
     // the down GEMM runs on CTA pairs over 256-row tiles at large T (the
     // bucketing above writes their list); below that the 128-row tiles waste
@@ -626,7 +635,7 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
     // grouped gate/up GEMM with the SwiGLU epilogue (shared expert = group E);
     // for T <= GEMM_SMALL_T no bucket has more than T rows: the small kinds
     // load only that many A rows per stage and keep more weights in flight
-    const bool small = c.T <= GEMM_SMALL_T;
+    const bool small = c.T <= GEMM_SMALL_T && with_shared;
     const int a_rows = small ? GEMM_SMALL_T : GEMM_BM;
     GemmParams p1;
     memset(&p1, 0, sizeof(p1));
@@ -687,9 +696,45 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
                                               std::min(sms, L.max_mtiles * p2.n_tiles), s));
     }
 
+    if (!with_shared) {
+        // every row's expert output, back in the rows' own order
+        GLR_LAUNCH(KID_COMBINE, launch_rows_gather(y, slot_of, c.T, c.H, out, s));
+        return MOE_OK;
+    }
     // weighted combine + shared expert (+ residual), one rounding to bf16
     GLR_LAUNCH(KID_COMBINE, launch_combine(y, slot_of, topk_w, residual, c.T, c.H, c.k, out, s, -1, topk_idx, offs,
                                            c.E));
+    return MOE_OK;
+}
+
+// ------------------------------------------------------ expert parallelism
+struct EpLayout {
+    size_t dest, hist, mtiles, total;
+    int nchunk;
+};
+
+EpLayout ep_layout(const moe_cfg &c, int ranks)
+{
+    EpLayout L;
+    const size_t n = (size_t)c.T * c.k;
+    L.nchunk = (c.T + PERM_CHUNK - 1) / PERM_CHUNK;
+    size_t off = sizeof(WsHeader);
+    L.dest = off;
+    off = align_up(off + n * 4, 256);
+    L.hist = off;
+    off = align_up(off + (size_t)L.nchunk * ranks * 4, 256);
+    L.mtiles = off;
+    off = align_up(off + (n / GEMM_BM + ranks + 2) * 16, 256);
+    L.total = off;
+    return L;
+}
+
+int check_ep(const moe_cfg *c, int ranks)
+{
+    if (!c || ranks < 1 || c->T < 1 || c->k < 1 || c->E < 1 || c->H < 8)
+        return MOE_ERR_INVALID_ARG;
+    if (c->E % ranks != 0 || ranks > 256 || c->k > 32 || c->H % 8 != 0 || c->T > (1 << 24))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
 
@@ -1336,6 +1381,121 @@ const char *moe_strerror(int code)
     case MOE_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300)";
     default: return "unknown error code";
     }
+}
+
+size_t moe_ep_dispatch_workspace_bytes(const moe_cfg *cfg, int32_t ranks)
+{
+    return check_ep(cfg, ranks) == MOE_OK ? ep_layout(*cfg, ranks).total : 0;
+}
+
+int moe_ep_dispatch(const moe_cfg *cfg, int32_t ranks, const moe_bf16 *hidden, const int32_t *topk_idx,
+                    int32_t *send_counts, moe_bf16 *x_send, int32_t *e_send, int32_t *slot_of, void *ws,
+                    size_t ws_bytes, void *stream)
+{
+    int rc = check_ep(cfg, ranks);
+    if (rc != MOE_OK)
+        return rc;
+    if (!hidden || !topk_idx || !send_counts || !x_send || !e_send || !slot_of)
+        return MOE_ERR_INVALID_ARG;
+    const EpLayout L = ep_layout(*cfg, ranks);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(hidden, 16) || !aligned(x_send, 16) || !aligned(topk_idx, 4) || !aligned(send_counts, 4) ||
+        !aligned(e_send, 4) || !aligned(slot_of, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const moe_cfg &c = *cfg;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    WsHeader *hdr = header(ws);
+    int32_t *dest = at<int32_t>(ws, L.dest);
+    int32_t *hist = at<int32_t>(ws, L.hist);
+    const long long n = (long long)c.T * c.k;
+    int launches = 0;
+    // the pairs bucketed by destination rank, stably (rows to one rank in
+    // ascending (token, j) order), with the same kernels that bucket them by
+    // expert; the bucketed copy of the rows is the send buffer
+    GLR_LAUNCH(KID_HIST, launch_ep_dest(topk_idx, n, c.E, c.E / ranks, dest, s));
+    GLR_LAUNCH(KID_HIST, launch_bucket_hist(dest, c.T, ranks, c.k, hist, &hdr->status, s));
+    GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, ranks, send_counts, s));
+    GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(dest, reinterpret_cast<const uint16_t *>(hidden), hist, send_counts,
+                                                  c.T, c.H, ranks, c.k, slot_of, reinterpret_cast<uint16_t *>(x_send),
+                                                  at<int4>(ws, L.mtiles), hdr, s, nullptr, false));
+    GLR_LAUNCH(KID_SCATTER, launch_ep_local_ids(topk_idx, slot_of, n, c.E / ranks, e_send, s));
+    g_last_launches = launches;
+    return MOE_OK;
+}
+
+size_t moe_expert_rows_workspace_bytes(const moe_cfg *cfg, int32_t rows)
+{
+    if (!cfg || rows < 1)
+        return 0;
+    moe_cfg c = *cfg;
+    c.T = rows;
+    c.k = 1;
+    c.Is = c.I;
+    return check_forward_cfg(&c) == MOE_OK ? fwd_layout(c).total : 0;
+}
+
+int moe_expert_rows(const moe_cfg *cfg, int32_t rows, const moe_bf16 *x, const int32_t *expert,
+                    const moe_bf16 *W_gate_up, const moe_bf16 *W_down, moe_bf16 *y, void *ws, size_t ws_bytes,
+                    void *stream)
+{
+    if (!cfg || rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (rows == 0) {
+        g_last_launches = 0;
+        return MOE_OK;                        // nothing received
+    }
+    moe_cfg c = *cfg;
+    c.T = rows;
+    c.k = 1;
+    c.Is = c.I;
+    int rc = check_forward_cfg(&c);
+    if (rc != MOE_OK)
+        return rc;
+    if (!x || !expert || !W_gate_up || !W_down || !y)
+        return MOE_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(c);
+    if ((rc = check_ws(ws, ws_bytes, L.total)) != MOE_OK)
+        return rc;
+    if (!aligned(x, 16) || !aligned(W_gate_up, 16) || !aligned(W_down, 16) || !aligned(y, 16) ||
+        !aligned(expert, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    int launches = 0;
+    rc = forward_impl(c, x, W_gate_up, W_down, nullptr, nullptr, expert, nullptr, nullptr, y, ws, L, nullptr, sms,
+                      static_cast<cudaStream_t>(stream), launches, false, false);
+    g_last_launches = launches;
+    return rc;
+}
+
+int moe_combine(const moe_cfg *cfg, const moe_bf16 *Y, int64_t y_rows, int64_t shared_row0, const int32_t *slot_of,
+                const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *stream)
+{
+    if (!cfg || cfg->T < 1 || cfg->k < 1 || cfg->k > 32 || cfg->H < 8 || !Y || !slot_of || !out)
+        return MOE_ERR_INVALID_ARG;
+    if (cfg->H % 8 != 0)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (shared_row0 < 0 || shared_row0 + cfg->T > y_rows)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(Y, 16) || !aligned(residual, 16) || !aligned(out, 16) || !aligned(slot_of, 4) ||
+        !aligned(topk_w, 4))
+        return MOE_ERR_MISALIGNED;
+    int sms = 0, rc = MOE_OK;
+    if ((rc = device_check(&sms)) != MOE_OK)
+        return rc;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int launches = 0;
+    GLR_LAUNCH(KID_COMBINE, launch_combine(reinterpret_cast<const uint16_t *>(Y), slot_of, topk_w,
+                                           reinterpret_cast<const uint16_t *>(residual), cfg->T, cfg->H, cfg->k,
+                                           reinterpret_cast<uint16_t *>(out), s, shared_row0, nullptr, nullptr, 0,
+                                           y_rows));
+    g_last_launches = launches;
+    return MOE_OK;
 }
 
 // ------------------------------------------------------ moe_route_static

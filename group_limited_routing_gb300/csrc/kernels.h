@@ -258,11 +258,20 @@ cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t 
 // hist [E][nchunk] -> per-chunk starts inside each bucket (relative); sizes[E]
 cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s);
 
-// ptiles (nullable): also the 256-row pair-tile list (hdr->num_ptiles)
+// ptiles (nullable): also the 256-row pair-tile list (hdr->num_ptiles);
+// with_shared = false: no shared-expert group in the tile lists
 cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
                                   const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
                                   uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s,
-                                  int4 *ptiles = nullptr);
+                                  int4 *ptiles = nullptr, bool with_shared = true);
+
+// expert parallelism: the destination rank of every pair, the received
+// rows' local expert ids, and a gather of bf16 rows by slot
+cudaError_t launch_ep_dest(const int32_t *idx, long long n, int E, int per_rank, int32_t *dest, cudaStream_t s);
+cudaError_t launch_ep_local_ids(const int32_t *idx, const int32_t *slot_of, long long n, int per_rank,
+                                int32_t *e_send, cudaStream_t s);
+cudaError_t launch_rows_gather(const uint16_t *rows, const int32_t *slot_of, int n, int H, uint16_t *out,
+                               cudaStream_t s);
 
 // T <= BUCKET_SMALL_MAX_T: hist, scan and scatter in one launch (same outputs)
 constexpr int BUCKET_SMALL_MAX_T = 32;
@@ -279,9 +288,11 @@ cudaError_t launch_dense_tiles(int T, int mt, int4 *mtiles, WsHeader *hdr, cudaS
 // slot_of holds rows inside each expert's bucket and the Y row of pair (t, j)
 // is offs[idx[t,j]] + slot_of[t,j] (a pair whose expert is not in [0, E) is
 // skipped).
+// y_rows >= 0: Y's row count; pair rows at or past it are skipped like -1.
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0 = -1,
-                           const int32_t *idx = nullptr, const int32_t *offs = nullptr, int E = 0);
+                           const int32_t *idx = nullptr, const int32_t *offs = nullptr, int E = 0,
+                           long long y_rows = -1);
 
 // After the fused router: bucket offsets (exclusive scan of the E bucket
 // sizes) into offs[E + 1] and the m-tile list of the grouped GEMMs, whose

@@ -21,6 +21,8 @@
 // Everything is deterministic: no float atomics, fixed summation order.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace glr {
@@ -196,7 +198,8 @@ cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes,
 __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, int K, int *offset, int *tstart,
                                int *wsum_rows, int *wsum_tiles, bool write_tiles, int4 *__restrict__ mtiles,
                                WsHeader *__restrict__ hdr, int pad = 1, int2 *__restrict__ eoff = nullptr,
-                               int shared_base = 0, int cap = 0, int4 *__restrict__ ptiles = nullptr)
+                               int shared_base = 0, int cap = 0, int4 *__restrict__ ptiles = nullptr,
+                               bool with_shared = true)
 {
     __shared__ int true_rows;
     __shared__ int wsum_pt[8];
@@ -251,9 +254,9 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
         tstart[E] = tiles;
         pt_total = pts;
         if (write_tiles && ptiles)
-            hdr->num_ptiles = pts + (T + 2 * GEMM_BM - 1) / (2 * GEMM_BM);
+            hdr->num_ptiles = pts + (with_shared ? (T + 2 * GEMM_BM - 1) / (2 * GEMM_BM) : 0);
         if (write_tiles) {
-            hdr->num_mtiles = tiles + (T + GEMM_BM - 1) / GEMM_BM;
+            hdr->num_mtiles = tiles + (with_shared ? (T + GEMM_BM - 1) / GEMM_BM : 0);
             if (true_rows != K * T)
                 atomicOr(&hdr->status, ST_COUNT_MISMATCH);
             if (eoff)
@@ -267,7 +270,7 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
         if (e < E)
             for (int i = 0, r = 0; r < n0; ++i, r += GEMM_BM)
                 mtiles[tstart[e] + i] = make_int4(e, offset[e] + r, min(GEMM_BM, n0 - r), cap > 0 ? e * cap + r : 0);
-        const int ntile_sh = (T + GEMM_BM - 1) / GEMM_BM;
+        const int ntile_sh = with_shared ? (T + GEMM_BM - 1) / GEMM_BM : 0;
         for (int i = threadIdx.x; i < ntile_sh; i += blockDim.x)
             mtiles[tstart[E] + i] = make_int4(E, i * GEMM_BM, min(GEMM_BM, T - i * GEMM_BM), cap > 0 ? i * GEMM_BM : 0);
         if (ptiles) {
@@ -275,7 +278,7 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
             if (e < E)
                 for (int i = 0, r = 0; r < n0; ++i, r += PM)
                     ptiles[pstart + i] = make_int4(e, offset[e] + r, min(PM, n0 - r), 0);
-            const int np_sh = (T + PM - 1) / PM;
+            const int np_sh = with_shared ? (T + PM - 1) / PM : 0;
             for (int i = threadIdx.x; i < np_sh; i += blockDim.x)
                 ptiles[pt_total + i] = make_int4(E, i * PM, min(PM, T - i * PM), 0);
         }
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
                                                              int E, int K, int32_t *__restrict__ slot_of,
                                                              uint16_t *__restrict__ x_perm, int4 *__restrict__ mtiles,
                                                              WsHeader *__restrict__ hdr, ScatterBwd bw,
-                                                             int4 *__restrict__ ptiles)
+                                                             int4 *__restrict__ ptiles, int with_shared)
 {
     pdl_wait();
     __shared__ int offset[258];
@@ -320,7 +323,7 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
     const int nt = min(PERM_CHUNK, T - t0);
     const bool backward = bw.do_perm != nullptr;
     bucket_offsets(sizes, T, E, K, offset, tstart, wsum_rows, wsum_tiles, blockIdx.x == 0, mtiles, hdr,
-                   backward ? BWD_ROW_ALIGN : 1, bw.eoff, bw.shared_base, 0, ptiles);
+                   backward ? BWD_ROW_ALIGN : 1, bw.eoff, bw.shared_base, 0, ptiles, with_shared != 0);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         next[e] = offset[e] + chunk_base[(size_t)e * gridDim.x + blockIdx.x];   // [expert][chunk]
     __syncthreads();
@@ -401,13 +404,15 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
 
 cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const int32_t *chunk_base,
                                   const int32_t *sizes, int T, int H, int E, int k, int32_t *slot_of,
-                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s, int4 *ptiles)
+                                  uint16_t *x_perm, int4 *mtiles, WsHeader *hdr, cudaStream_t s, int4 *ptiles,
+                                  bool with_shared)
 {
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
     const ScatterBwd none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0};
     const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
-                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none, ptiles);
+                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none, ptiles,
+                                      with_shared ? 1 : 0);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
@@ -423,7 +428,7 @@ cudaError_t launch_bucket_scatter_bwd(const int32_t *idx, const uint16_t *x, con
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
     const ScatterBwd bw = {dout, w, do_perm, w_perm, eoff, shared_base};
     const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
-                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, bw, (int4 *)nullptr);
+                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, bw, (int4 *)nullptr, 1);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
@@ -803,7 +808,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                                                       const uint16_t *__restrict__ residual, int T, int H, int K,
                                                       int ctok, long long shared_row0, uint16_t *__restrict__ out,
                                                       const int32_t *__restrict__ idx,
-                                                      const int32_t *__restrict__ offs, int E)
+                                                      const int32_t *__restrict__ offs, int E, long long y_rows)
 {
     pdl_wait();
     __shared__ int s_slot[COMBINE_TOK * 32];
@@ -822,7 +827,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                 const int e = idx[(size_t)t0 * K + i];      // bucket row -> row of the compact layout
                 slot = (e >= 0 && e < E) ? slot + offs[e] : -1;
             }
-            s_slot[i] = slot;
+            s_slot[i] = (slot < y_rows) ? slot : -1;        // a caller's row index past Y is skipped
             s_w[i] = w ? w[(size_t)t0 * K + i] : 1.0f;
         }
         __syncthreads();
@@ -842,8 +847,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
 
 cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const float *w, const uint16_t *residual,
                            int T, int H, int k, uint16_t *out, cudaStream_t s, long long shared_row0,
-                           const int32_t *idx, const int32_t *offs, int E)
+                           const int32_t *idx, const int32_t *offs, int E, long long y_rows)
 {
+    if (y_rows < 0)
+        y_rows = 1ll << 62;
     if (shared_row0 < 0)
         shared_row0 = (long long)k * T;
     int dev = 0, sms = 148;
@@ -859,7 +866,89 @@ cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const floa
     const int nchunks = (T + ctok - 1) / ctok;
     const int blocks = min(nchunks, sms * 8);
     const cudaError_t le = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, Y, slot_of, w, residual, T, H, k,
-                                      ctok, shared_row0, out, idx, offs, offs ? E : 0);
+                                      ctok, shared_row0, out, idx, offs, offs ? E : 0, y_rows);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Expert parallelism (the training-pitfalls article's section "专家并行（EP）
+// 怎么切": the expert stacks sharded along their first dimension over R
+// ranks, rank r holding experts [r E/R, (r + 1) E/R)).
+
+// dest[i] = idx[i] / per_rank (the rank that holds the pair's expert); an id
+// outside [0, E) gets -1 (skipped by the bucketing, flagged there)
+__global__ void ep_dest_kernel(const int32_t *__restrict__ idx, long long n, int E, int per_rank,
+                               int32_t *__restrict__ dest)
+{
+    pdl_wait();
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int e = idx[i];
+        dest[i] = (e >= 0 && e < E) ? e / per_rank : -1;
+    }
+}
+
+// e_send[slot_of[i]] = idx[i] - dest * per_rank: every sent row's expert, as
+// an id local to the rank that receives it
+__global__ void ep_local_ids_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ slot_of,
+                                    long long n, int per_rank, int32_t *__restrict__ e_send)
+{
+    pdl_wait();
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const int slot = slot_of[i];
+        if (slot >= 0)
+            e_send[slot] = idx[i] % per_rank;
+    }
+}
+
+// out[i] = rows[slot_of[i]] (bf16 rows of H, 16-byte pieces); a row whose
+// slot is -1 gets zeros
+__global__ void rows_gather_kernel(const uint16_t *__restrict__ rows, const int32_t *__restrict__ slot_of, int n,
+                                   int H, uint16_t *__restrict__ out)
+{
+    pdl_wait();
+    const int vpr = H / 8;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < (long long)n * vpr;
+         q += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(q / vpr), v = (int)(q % vpr);
+        const int slot = slot_of[i];
+        reinterpret_cast<uint4 *>(out + (size_t)i * H)[v] =
+            slot >= 0 ? reinterpret_cast<const uint4 *>(rows + (size_t)slot * H)[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+static int grid_for(long long n)
+{
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return (int)std::max<long long>(1, std::min<long long>((n + 255) / 256, (long long)sms * 8));
+}
+
+cudaError_t launch_ep_dest(const int32_t *idx, long long n, int E, int per_rank, int32_t *dest, cudaStream_t s)
+{
+    const cudaError_t le = launch_pdl(ep_dest_kernel, dim3(grid_for(n)), dim3(256), 0, s, idx, n, E, per_rank, dest);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_ep_local_ids(const int32_t *idx, const int32_t *slot_of, long long n, int per_rank,
+                                int32_t *e_send, cudaStream_t s)
+{
+    const cudaError_t le = launch_pdl(ep_local_ids_kernel, dim3(grid_for(n)), dim3(256), 0, s, idx, slot_of, n,
+                                      per_rank, e_send);
+    if (le != cudaSuccess)
+        return le;
+    return cudaPeekAtLastError();
+}
+
+cudaError_t launch_rows_gather(const uint16_t *rows, const int32_t *slot_of, int n, int H, uint16_t *out,
+                               cudaStream_t s)
+{
+    const cudaError_t le = launch_pdl(rows_gather_kernel, dim3(grid_for((long long)n * (H / 8))), dim3(256), 0, s,
+                                      rows, slot_of, n, H, out);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

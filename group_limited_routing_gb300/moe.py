@@ -352,6 +352,91 @@ def dense_ffn(hidden, W_gate_up, W_down, residual=None, *, ws: Optional[DenseWor
     return out
 
 
+class SizedWorkspace:
+    """A device workspace of a given byte size (the expert-parallel calls)."""
+
+    def __init__(self, nbytes: int, what: str, device=None):
+        if nbytes == 0:
+            raise ValueError("unsupported shape for %s" % what)
+        self.nbytes = int(nbytes)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        assert self.buf.data_ptr() % 256 == 0
+        _lib.check(_lib.load().moe_workspace_init(self.ptr, self.nbytes, _stream(self.buf.device)),
+                   "moe_workspace_init")
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def status(self, reset: bool = True) -> int:
+        v = ctypes.c_int32(0)
+        _lib.check(_lib.load().moe_get_status(self.ptr, self.nbytes, _stream(self.buf.device), ctypes.byref(v),
+                                              1 if reset else 0), "moe_get_status")
+        return int(v.value)
+
+
+def ep_dispatch(cfg: MoeConfig, ranks: int, hidden, topk_idx, *, ws: Optional[SizedWorkspace] = None):
+    """moe_ep_dispatch: the pairs grouped by the rank holding their expert.
+    Returns (send_counts [ranks] int32, x_send [kT, H] bf16, e_send [kT] int32
+    local expert ids, slot_of [T, k] int32)."""
+    dev = hidden.device
+    ph = _need(hidden, "hidden", torch.bfloat16, (cfg.T, cfg.H), dev)
+    pi = _need(topk_idx, "topk_idx", torch.int32, (cfg.T, cfg.k), dev)
+    n = cfg.T * cfg.k
+    counts = torch.empty(ranks, dtype=torch.int32, device=dev)
+    x_send = torch.empty(n, cfg.H, dtype=torch.bfloat16, device=dev)
+    e_send = torch.empty(n, dtype=torch.int32, device=dev)
+    slot_of = torch.empty(cfg.T, cfg.k, dtype=torch.int32, device=dev)
+    need = int(_lib.load().moe_ep_dispatch_workspace_bytes(ctypes.byref(cfg.c()), ranks))
+    if need and (ws is None or ws.nbytes < need):
+        ws = SizedWorkspace(need, "moe_ep_dispatch", dev)
+    # (an unsupported shape has no workspace size: the call itself names the error)
+    rc = _lib.load().moe_ep_dispatch(ctypes.byref(cfg.c()), ranks, ph, pi, counts.data_ptr(), x_send.data_ptr(),
+                                     e_send.data_ptr(), slot_of.data_ptr(), ws.ptr if need else None,
+                                     ws.nbytes if need else 0, _stream(dev))
+    _lib.check(rc, "moe_ep_dispatch")
+    return counts, x_send, e_send, slot_of
+
+
+def expert_rows(cfg: MoeConfig, x, expert, W_gate_up, W_down, *, ws: Optional[SizedWorkspace] = None, out=None):
+    """moe_expert_rows: y[i] = expert[i]'s SwiGLU FFN of x[i] (unweighted), with
+    cfg.E local experts' weights W_gate_up [E, 2I, H] / W_down [E, I, H]."""
+    dev = x.device
+    rows = x.shape[0]
+    px = _need(x, "x", torch.bfloat16, (rows, cfg.H), dev)
+    pe = _need(expert, "expert", torch.int32, (rows,), dev)
+    pgu = _need(W_gate_up, "W_gate_up", torch.bfloat16, (cfg.E, 2 * cfg.I, cfg.H), dev)
+    pd = _need(W_down, "W_down", torch.bfloat16, (cfg.E, cfg.I, cfg.H), dev)
+    if out is None:
+        out = torch.empty(rows, cfg.H, dtype=torch.bfloat16, device=dev)
+    po = _need(out, "out", torch.bfloat16, (rows, cfg.H), dev)
+    if rows == 0:
+        return out
+    need = int(_lib.load().moe_expert_rows_workspace_bytes(ctypes.byref(cfg.c()), rows))
+    if need and (ws is None or ws.nbytes < need):
+        ws = SizedWorkspace(need, "moe_expert_rows", dev)
+    rc = _lib.load().moe_expert_rows(ctypes.byref(cfg.c()), rows, px, pe, pgu, pd, po, ws.ptr if need else None,
+                                     ws.nbytes if need else 0, _stream(dev))
+    _lib.check(rc, "moe_expert_rows")
+    return out
+
+
+def combine(cfg: MoeConfig, Y, shared_row0: int, slot_of, topk_w, residual=None, out=None):
+    """moe_combine: out[t] = bf16(sum_j w[t,j] Y[slot_of[t,j]] + Y[shared_row0 + t] (+ residual[t]))."""
+    dev = Y.device
+    rows = Y.shape[0]
+    py = _need(Y, "Y", torch.bfloat16, (rows, cfg.H), dev)
+    ps = _need(slot_of, "slot_of", torch.int32, (cfg.T, cfg.k), dev)
+    pw = _need(topk_w, "topk_w", torch.float32, (cfg.T, cfg.k), dev)
+    pr = _opt(residual, "residual", torch.bfloat16, (cfg.T, cfg.H), dev)
+    if out is None:
+        out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    po = _need(out, "out", torch.bfloat16, (cfg.T, cfg.H), dev)
+    rc = _lib.load().moe_combine(ctypes.byref(cfg.c()), py, rows, shared_row0, ps, pw, pr, po, _stream(dev))
+    _lib.check(rc, "moe_combine")
+    return out
+
+
 def expert_feedback(cfg: MoeConfig, counts, gamma: float, expert_bias=None, totals=None) -> None:
     """moe_expert_feedback: in place, bias += +-gamma toward the balanced load
     (routing article §三) and totals += counts (§六)."""

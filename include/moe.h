@@ -262,6 +262,68 @@ int moe_dense_ffn(int32_t T, int32_t H, int32_t I, const moe_bf16 *hidden, const
                   const moe_bf16 *W_down, const moe_bf16 *residual, moe_bf16 *out, void *ws,
                   size_t ws_bytes, void *stream);
 
+/* ---- Expert parallelism -------------------------------------------------
+ * The InternLumina-U2 training-pitfalls article, section "专家并行（EP）怎么
+ * 切": the stacked expert weights are sharded along their first (expert)
+ * dimension over R ranks, rank r holding experts [r E/R, (r + 1) E/R) of
+ * W_gate_up and W_down; the router, the bias and the shared expert are
+ * replicated.  A rank's forward then runs, with two all-to-all exchanges of
+ * rows between the ranks (done by the caller, e.g. torch.distributed):
+ *   moe_route                      its own tokens' routing;
+ *   moe_ep_dispatch                the rows to send, grouped by destination;
+ *   (all-to-all: counts, rows, expert ids)
+ *   moe_expert_rows                the received rows through the local experts;
+ *   (all-to-all back, into the first k T rows of a [k T + T, H] buffer)
+ *   moe_dense_ffn                  the shared expert into that buffer's last T rows;
+ *   moe_combine                    the weighted sum, as moe_forward's.
+ * Each row's expert output does not depend on where the row is computed and
+ * the combine adds in moe_forward's order, so the result equals moe_forward's
+ * bit for bit. */
+
+/* Groups the (token, j) pairs by the rank that holds their expert
+ * (topk_idx / (E / ranks)), stably (ascending (token, j) within a rank):
+ *   send_counts [ranks]   rows for each destination rank;
+ *   x_send [k T, H] bf16  the hidden row of every pair, in that order (rank
+ *                         0's rows first);
+ *   e_send [k T] int32    the pair's expert as an id local to its rank;
+ *   slot_of [T, k] int32  the row of pair (t, j) in x_send (its results come
+ *                         back to the same row), -1 for an expert id outside
+ *                         [0, E) (flagged in the workspace's status word).
+ * Needs E % ranks == 0, ranks <= 256, H % 8 == 0; the workspace is
+ * moe_ep_dispatch_workspace_bytes(cfg, ranks) bytes (moe_workspace_init()
+ * once).  Device pointers, asynchronous on `stream`. */
+size_t moe_ep_dispatch_workspace_bytes(const moe_cfg *cfg, int32_t ranks);
+int moe_ep_dispatch(const moe_cfg *cfg, int32_t ranks, const moe_bf16 *hidden, const int32_t *topk_idx,
+                    int32_t *send_counts, moe_bf16 *x_send, int32_t *e_send, int32_t *slot_of, void *ws,
+                    size_t ws_bytes, void *stream);
+
+/* The expert stage for a set of rows that each name their expert:
+ *   y[i] = bf16( down_e( silu(gate_e x[i]) * up_e x[i] ) ),  e = expert[i],
+ * unweighted, with the weights of E = cfg->E local experts (W_gate_up
+ * [E, 2I, H], W_down [E, I, H], as moe_forward's; cfg->H and cfg->I as
+ * there; cfg->T, k and the shared expert are not used).  The rows are
+ * bucketed by expert and run through the same grouped tensor-core GEMMs as
+ * moe_forward's, so y[i] equals moe_forward's row for the same pair bit for
+ * bit.  rows may be 0 (nothing launched); an expert id outside [0, E) gives a
+ * zero row and sets the status word.  The workspace is
+ * moe_expert_rows_workspace_bytes(cfg, rows) bytes (moe_workspace_init()
+ * once; a workspace sized for more rows serves fewer). */
+size_t moe_expert_rows_workspace_bytes(const moe_cfg *cfg, int32_t rows);
+int moe_expert_rows(const moe_cfg *cfg, int32_t rows, const moe_bf16 *x, const int32_t *expert,
+                    const moe_bf16 *W_gate_up, const moe_bf16 *W_down, moe_bf16 *y, void *ws, size_t ws_bytes,
+                    void *stream);
+
+/* moe_forward's last step on rows computed elsewhere (routing page, section
+ * 五: the shared expert added directly):
+ *   out[t] = bf16( sum_j topk_w[t,j] Y[slot_of[t,j]] + Y[shared_row0 + t]
+ *                  (+ residual[t]) ),
+ * in fp32, j in order, then the shared row, then the residual.  Y [y_rows, H]
+ * bf16; slot_of [T, k] (-1 or a row at or past y_rows: the pair is skipped);
+ * topk_w [T, k] fp32; residual [T, H] or NULL; out [T, H] (may alias
+ * residual).  Needs shared_row0 + T <= y_rows, H % 8 == 0. */
+int moe_combine(const moe_cfg *cfg, const moe_bf16 *Y, int64_t y_rows, int64_t shared_row0, const int32_t *slot_of,
+                const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *stream);
+
 /* Router without caller-provided scratch (no counterpart on the pages: it is
  * an interface convenience, not part of the method).  Same computation,
  * outputs and determinism as moe_route, but the scratch that moe_route keeps
