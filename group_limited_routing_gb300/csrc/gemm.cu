@@ -1546,7 +1546,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
         }
         for (int a = 0; a < C::SLOTS; ++a) {
             mbar_init(tfull0 + 8u * a, 1);
-            mbar_init(tempty0 + 8u * a, 2 * 8);      // both CTAs' epilogue warps
+            // this CTA's epilogue warps; the leader's also counts the peer's forwarder
+            mbar_init(tempty0 + 8u * a, 8 + (leader ? 1 : 0));
         }
         mbar_init(fin_bar, 1);
         *abort_flag = 0;
@@ -1574,6 +1575,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
         if (lane == 0) {
             // ---------------------------------------------------- TMA producer
             const uint32_t full_leader0 = mapa_shared(full_bar(0), 0);
+            // every hidden row is read by one CTA once: its lines go first
+            // when L2 needs room, so that the scores this kernel writes stay
+            // there for the routing kernel that reads them next
+            const uint64_t once = l2_policy_evict_first();
             int stage = 0;
             uint32_t phase = 0, issued = 0, issued_parity = 0;
             bool ok = true;
@@ -1591,7 +1596,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
                     if (leader)
                         mbar_arrive_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);
                     const uint32_t fb = full_leader0 + 8u * stage;
-                    tma_load_2d_pair(sA, &p.tmA0, fb, kb * GEMM_BK, a_row);
+                    tma_load_2d_pair_hint(sA, &p.tmA0, fb, kb * GEMM_BK, a_row, once);
 #pragma unroll
                     for (int part = 0; part < 3; ++part)
                         tma_load_2d_pair(sA + C::A_BYTES + part * C::B_PART, &p.tmB0, fb, kb * GEMM_BK,
@@ -1601,7 +1606,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
                     const int pt = pair + (q / p.kblocks) * npairs;
                     const int prow = pt * 256 + (int)rank * GEMM_BM;
                     if (pt < num_tiles && prow < p.T)
-                        tma_prefetch_l2_2d(&p.tmA0, (q % p.kblocks) * GEMM_BK, prow);
+                        tma_prefetch_l2_2d_hint(&p.tmA0, (q % p.kblocks) * GEMM_BK, prow, once);
                     issued |= 1u << stage;
                     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                     if (++stage == C::STAGES) {
@@ -1670,6 +1675,28 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
             // no MMA may still be writing either CTA's TMEM when it is freed
             umma_commit_pair(fin_bar, 0x1);
             mbar_drain(fin_bar, 0);
+        } else if (lane == 0) {
+            // ------------------------------------------- the peer's forwarder
+            // hands each TMEM slot back to the leader's MMA issuer once this
+            // CTA's epilogue warps have read it (their local arrivals need no
+            // cluster-scope release)
+            const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+            const int groups = (p.kblocks + ROUTER_KPS - 1) / ROUTER_KPS;
+            uint32_t ctr = 0;
+            bool ok = true;
+            for (int n = 0; ok; ++n) {
+                const int tile = pair + n * npairs;
+                if (tile >= num_tiles)
+                    break;
+                for (int g = 0; g < groups; ++g, ++ctr) {
+                    const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                    if (!mbar_wait(tempty0 + 8u * slot, par, abort_flag, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_cluster(tempty_leader + 8u * slot);
+                }
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -1680,7 +1707,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
                 sbias[e] = p.bias ? p.bias[e] : 0.0f;
             asm volatile("bar.sync 1, %0;" ::"r"(32 * 8) : "memory");
         }
-        const uint32_t tempty_leader = mapa_shared(tempty0, 0);
         for (int n = 0;; ++n) {
             const int tile = pair + n * npairs;
             if (tile >= num_tiles)
@@ -1696,7 +1722,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
             ti.out_row = ti.a_row;
             ti.rows = min(GEMM_BM, p.T - ti.a_row);     // <= 0: the pair's last tile ends in the other CTA
             if (!router_epilogue_tile<GK_ROUTER_WIDE>(p, ti, tmem, quad, (warp - 2) >> 2, lane, tfull0, tempty0,
-                                                      ctr, abort_flag, nullptr, limit, tile, sbias, tempty_leader))
+                                                      ctr, abort_flag, nullptr, limit, tile, sbias))
                 break;
         }
     }
@@ -1781,7 +1807,8 @@ __global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const _
         }
         for (int a = 0; a < C::SLOTS; ++a) {
             mbar_init(tfull0 + 8u * a, 1);
-            mbar_init(tempty0 + 8u * a, 2 * 4);      // both CTAs' epilogue warps
+            // this CTA's epilogue warps; the leader's also counts the peer's forwarder
+            mbar_init(tempty0 + 8u * a, 4 + (leader ? 1 : 0));
         }
         mbar_init(fin_bar, 1);
         *abort_flag = 0;
@@ -1911,6 +1938,19 @@ __global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const _
             }
             umma_commit_pair(fin_bar, 0x1);
             mbar_drain(fin_bar, 0);
+        } else if (lane == 0) {
+            // ------------------------------------------- the peer's forwarder
+            const uint32_t tempty_leader = mapa_shared(tempty0, 0);
+            uint32_t ctr = 0;
+            for (int n = 0;; ++n, ++ctr) {
+                const int tile = pair + n * npairs;
+                if (tile >= num_tiles)
+                    break;
+                const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                if (!mbar_wait(tempty0 + 8u * slot, par, abort_flag, limit))
+                    break;
+                mbar_arrive_cluster(tempty_leader + 8u * slot);
+            }
         }
     } else {
         // ------------------------------------------------------------ epilogue
@@ -1918,7 +1958,6 @@ __global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const _
         uint8_t *stage = staging + (warp - 2) * (C::NBUF * 4096);
         int buf = 0;
         uint32_t ctr = 0;
-        const uint32_t tempty_leader = mapa_shared(tempty0, 0);
         for (int n = 0;; ++n) {
             const int tile = pair + n * npairs;
             if (tile >= num_tiles)
@@ -1938,7 +1977,7 @@ __global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const _
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive_cluster(tempty_leader + 8u * slot);
+                mbar_arrive(tempty0 + 8u * slot);   // (the peer's forwarder passes it on to the leader)
             ++ctr;
         }
         if (lane == 0)

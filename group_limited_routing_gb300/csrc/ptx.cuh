@@ -322,7 +322,11 @@ __device__ __forceinline__ void cluster_sync()
 }
 
 // Arrives once on an mbarrier given by its shared::cluster address (in this
-// CTA or the peer), with release semantics at cluster scope.
+// CTA or the peer), with release semantics at cluster scope (what a thread of
+// one CTA must use to hand the other CTA's MMA issuer a TMEM slot).  The
+// release waits for the thread's earlier memory operations, so the pair
+// kernels let one otherwise idle thread forward their epilogue warps' local
+// arrivals with it.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
@@ -336,6 +340,34 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
         "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(c0), "r"(c1)
         : "memory");
+}
+
+// L2 policy that marks lines to be evicted first (data read once that should
+// not push other data out of L2)
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d_pair with an L2 cache policy for the loaded lines
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const CUtensorMap *map, uint32_t cbar, int c0,
+                                                      int c1, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%3, %4}], [%2], %5;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+// tma_prefetch_l2_2d with an L2 cache policy
+__device__ __forceinline__ void tma_prefetch_l2_2d_hint(const CUtensorMap *map, int c0, int c1, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "l"(policy)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t holder_smem, uint32_t ncols)

@@ -666,6 +666,227 @@ __global__ void __launch_bounds__(256) route_select_scored_kernel(
     }
 }
 
+// The same selection with four threads per token (no balance-loss sums, k <=
+// 8): lanes 4i .. 4i + 3 of a warp take token i, a block of 128 threads 32
+// tokens (two bucketing chunks).
+//  * Each lane ranks two of the token's eight group scores; the quad ORs its
+//    lanes' bits into the kept-group mask (TG best groups, ties to the lower
+//    group).
+//  * Lane q takes the q-th kept group (ascending) and runs its 32 experts in
+//    ascending id order through an 8-entry list kept in descending order of
+//    biased score: an expert moves ahead of an entry only when strictly
+//    larger, so equal scores keep the lower id first.
+//  * Two merge steps (lanes q ^ 1, then q ^ 2) combine the quad's lists: the
+//    better of A[p] and B[7 - p] for every p is the top half of a bitonic
+//    sequence, which three compare-exchange stages sort -- "better" meaning a
+//    larger biased score, or an equal one with a lower expert id.
+// The result is the warp kernels' (biased score desc, id asc) order, and the
+// weights use the same sequential normaliser, so the outputs agree bit for
+// bit.  Every lane holds the merged list; lane q writes entries 2q, 2q + 1.
+__device__ __forceinline__ bool sel_better(float va, int ea, float vb, int eb)
+{
+    return va > vb || (va == vb && (unsigned)ea < (unsigned)eb);
+}
+
+__device__ __forceinline__ void sel_cas(float &va, int &ea, float &vb, int &eb)
+{
+    // after the call (va, ea) is the better of the two
+    const bool sw = sel_better(vb, eb, va, ea);
+    const float tv = va;
+    const int te = ea;
+    va = sw ? vb : va;
+    ea = sw ? eb : ea;
+    vb = sw ? tv : vb;
+    eb = sw ? te : eb;
+}
+
+// merges this lane's sorted list with the one of lane ^ mask (both lanes end
+// with the same sorted top 8)
+__device__ __forceinline__ void sel_merge(float (&v)[8], int (&e)[8], int lane, int mask)
+{
+    float ov[8];
+    int oe[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        ov[p] = __shfl_xor_sync(0xffffffffu, v[p], mask);
+        oe[p] = __shfl_xor_sync(0xffffffffu, e[p], mask);
+    }
+    const bool lower = (lane & mask) == 0;   // the list of the lower lane plays A in both lanes
+    float a[8], b[8];
+    int ae[8], be[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        a[p] = lower ? v[p] : ov[p];
+        ae[p] = lower ? e[p] : oe[p];
+        b[p] = lower ? ov[p] : v[p];
+        be[p] = lower ? oe[p] : e[p];
+    }
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const bool ta = sel_better(a[p], ae[p], b[7 - p], be[7 - p]);
+        v[p] = ta ? a[p] : b[7 - p];
+        e[p] = ta ? ae[p] : be[7 - p];
+    }
+#pragma unroll
+    for (int d = 4; d > 0; d >>= 1)
+#pragma unroll
+        for (int p = 0; p < 8; ++p)
+            if ((p & d) == 0)
+                sel_cas(v[p], e[p], v[p + d], e[p + d]);
+}
+
+template <int G, int TG>
+__global__ void __launch_bounds__(128) route_select_quad_kernel(
+    const float *__restrict__ scores, const float *__restrict__ gscore, const float *__restrict__ bias, int T,
+    int K, float rsf, float eps, int32_t *__restrict__ idx_out, float *__restrict__ w_out,
+    int32_t *__restrict__ counts, int *__restrict__ status, int32_t *__restrict__ chunk_hist, int nchunk_perm)
+{
+    pdl_wait();
+    constexpr int E = 32 * G;
+    constexpr int GP = 33;
+    static_assert(G == 8 && TG == 4, "four kept groups, one per lane of a quad");
+    static_assert(2 * PERM_CHUNK == 32, "a block is two bucketing chunks");
+    __shared__ float sb[G * GP];
+    __shared__ int sh_hist[2][E];
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int q = tid & 3;
+    bool nonfinite = false;
+    for (int e = tid; e < E; e += blockDim.x) {
+        const float b = bias ? bias[e] : 0.0f;
+        nonfinite |= !isfinite(b);
+        sb[(e >> 5) * GP + (e & 31)] = b;
+        sh_hist[0][e] = 0;
+        sh_hist[1][e] = 0;
+    }
+    __syncthreads();
+    const int tl = tid >> 2;                      // the token's place in the block
+    const int t0 = blockIdx.x * 32;
+    const int t = t0 + tl;
+    const bool valid = t < T;
+
+    // kept groups: this lane ranks groups 2q and 2q + 1
+    float g[G];
+#pragma unroll
+    for (int v = 0; v < G / 4; ++v) {
+        const float4 x = valid ? __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)t * G) + v)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        g[4 * v] = x.x;
+        g[4 * v + 1] = x.y;
+        g[4 * v + 2] = x.z;
+        g[4 * v + 3] = x.w;
+    }
+    uint32_t keep = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int j = 2 * q + h;
+        float gj = g[0];
+#pragma unroll
+        for (int i = 1; i < G; ++i)
+            gj = (i == j) ? g[i] : gj;
+        int rank = 0;
+#pragma unroll
+        for (int i = 0; i < G; ++i)
+            rank += (g[i] > gj || (g[i] == gj && i < j)) ? 1 : 0;
+        keep |= (rank < TG) ? (1u << j) : 0u;
+    }
+    keep |= __shfl_xor_sync(0xffffffffu, keep, 1);
+    keep |= __shfl_xor_sync(0xffffffffu, keep, 2);
+
+    // this lane's kept group: the q-th set bit of keep
+    uint32_t kk = keep;
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+        if (i < q)
+            kk &= kk - 1u;
+    const int j = valid ? __ffs(kk) - 1 : 0;
+    const float4 *s4 = reinterpret_cast<const float4 *>(scores + (size_t)(valid ? t : 0) * E + 32 * j);
+    float4 sv[8];
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4)
+        sv[i4] = valid ? __ldg(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    // (empty entries hold the most negative finite float and id -1)
+    float v[8];
+    int ev[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        v[p] = -3.402823466e38f;
+        ev[p] = -1;
+    }
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4) {
+        const float sc[4] = {sv[i4].x, sv[i4].y, sv[i4].z, sv[i4].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float b = sc[u] + sb[j * GP + 4 * i4 + u];   // section 三: choose on s + bias
+            const int id = 32 * j + 4 * i4 + u;
+            // the candidate replaces the last entry when it beats it, then moves
+            // up past every strictly smaller entry
+            const bool in = b > v[7];
+            v[7] = in ? b : v[7];
+            ev[7] = in ? id : ev[7];
+#pragma unroll
+            for (int p = 7; p > 0; --p) {
+                const bool up = v[p] > v[p - 1];
+                const float tv = v[p - 1];
+                const int te = ev[p - 1];
+                v[p - 1] = up ? v[p] : tv;
+                ev[p - 1] = up ? ev[p] : te;
+                v[p] = up ? tv : v[p];
+                ev[p] = up ? te : ev[p];
+            }
+        }
+    }
+    sel_merge(v, ev, lane, 1);
+    sel_merge(v, ev, lane, 2);
+
+    // weights from the unbiased scores, normaliser in output order (section 二 step 3)
+    const float *srow = scores + (size_t)(valid ? t : 0) * E;
+    float sw[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+        sw[p] = (valid && p < K && ev[p] >= 0) ? __ldg(srow + ev[p]) : 0.0f;
+    float den = 0.0f;
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+        if (p < K)
+            den += sw[p];
+    den += eps;
+    if (valid) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = 2 * q + h;
+            float wp = sw[0];
+            int ep = ev[0];
+#pragma unroll
+            for (int i = 1; i < 8; ++i) {
+                wp = (i == p) ? sw[i] : wp;
+                ep = (i == p) ? ev[i] : ep;
+            }
+            if (p < K) {
+                idx_out[(size_t)t * K + p] = ep;
+                w_out[(size_t)t * K + p] = (wp / den) * rsf;
+                if (ep >= 0)
+                    atomicAdd(&sh_hist[tl / PERM_CHUNK][ep], 1);
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, nonfinite) && lane == 0)
+        atomicOr(status, ST_NONFINITE);
+    __syncthreads();
+    const int nq = (min(T, t0 + 32) - t0 + PERM_CHUNK - 1) / PERM_CHUNK;
+    for (int e = tid; e < E; e += blockDim.x) {
+        const int a = sh_hist[0][e], b = sh_hist[1][e];
+        if (a + b)
+            atomicAdd(&counts[e], a + b);            // integer sums: the result is order-free
+        if (chunk_hist) {
+            chunk_hist[(size_t)e * nchunk_perm + 2 * blockIdx.x] = a;
+            if (nq > 1)
+                chunk_hist[(size_t)e * nchunk_perm + 2 * blockIdx.x + 1] = b;
+        }
+    }
+}
+
 cudaError_t launch_route_select_scored(const float *scores, const float *gscore, const float *bias, int T, int E,
                                        int k, float rsf, float eps, int32_t *idx, float *w, int32_t *counts,
                                        float *ppart, int *status, int *fin_ticket, int32_t *chunk_hist,
@@ -673,6 +894,17 @@ cudaError_t launch_route_select_scored(const float *scores, const float *gscore,
 {
     if (E != 256)
         return cudaErrorInvalidValue;
+    if (!ppart && k <= 8) {
+        // four threads per token, 32 tokens (two bucketing chunks) per block
+        const int blocks = (T + 31) / 32;
+        const int nchunk_perm = (T + PERM_CHUNK - 1) / PERM_CHUNK;
+        const cudaError_t le = launch_pdl(route_select_quad_kernel<8, 4>, dim3(blocks), dim3(128), 0, s, scores,
+                                          gscore, bias, T, k, rsf, eps, idx, w, counts, status, chunk_hist,
+                                          nchunk_perm);
+        if (le != cudaSuccess)
+            return le;
+        return cudaPeekAtLastError();
+    }
     const int chunk = route_chunk_hist(T);          // whole bucketing chunks per block
     const int blocks = (T + chunk - 1) / chunk;
     const int nchunk_perm = (T + PERM_CHUNK - 1) / PERM_CHUNK;

@@ -112,6 +112,20 @@ def test_scored_router_output_selects_like_the_logits(wid, T):
     assert abs(float(gl.item()) - float(ll.item())) <= 1e-5 * abs(float(ll.item()))
 
 
+@pytest.mark.parametrize("wid,T", [(4, 4865), (5, 8192), (3, 9001), (6, 19500), (4, 32768), (4, 131072)])
+def test_thread_per_token_selection_equals_the_warp_kernel(wid, T):
+    """Without the balance loss, the scored routing runs one thread per token;
+    with it, one warp per token (the kernel the oracle tests above check).
+    Both must give the same experts, weights and counts bit for bit."""
+    w0 = wl.WORKLOADS[wid].with_T(T)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
+    ti, tw, tc, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=False)
+    gi, gw, gc, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=True)
+    torch.cuda.synchronize()
+    assert torch.equal(ti, gi) and torch.equal(tw, gw) and torch.equal(tc, gc)
+
+
 @pytest.mark.parametrize("T,n_group,topk_group,k,scale", [
     (1, 8, 4, 8, 1.0), (130, 8, 4, 8, 1.0), (1000, 8, 1, 8, 2.0), (777, 8, 8, 8, 1.0),
     (513, 8, 4, 1, 1.0), (300, 8, 4, 32, 1.0), (257, 4, 2, 6, 1.0), (129, 4, 4, 32, 3.0),
