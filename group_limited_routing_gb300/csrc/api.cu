@@ -161,8 +161,8 @@ RouteLayout route_layout(const moe_cfg &c)
     off = align_up(off + 3ull * c.E * c.H * 2, 256);
     L.logits = off;
     off = align_up(off + (size_t)L.ksplit * c.T * c.E * 4, 256);
-    L.gscore = off;                     // group scores of the scored router output [T, E / 32]
-    off = align_up(off + (size_t)c.T * (c.E / 32) * 4, 256);
+    L.gscore = off;                     // each group's two best scores, scored router output [T, E / 32, 2]
+    off = align_up(off + (size_t)c.T * (c.E / 32) * 2 * 4, 256);
     L.ppart = off;
     off = align_up(off + (size_t)L.nchunk * c.E * 4, 256);
     L.pfin = off;

@@ -1118,11 +1118,12 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
     if (p.gscore != nullptr) {
         // scored output (routing page, section 二 step 1 and the group score
         // of step 2, with section 三's bias): the sigmoid of every logit
-        // replaces it, and each of the row's four groups of 32 gets the sum
-        // of its two best biased scores (a tie for the top counts twice)
+        // replaces it, and each of the row's four groups of 32 gets its two
+        // best biased scores (a tie for the top counts twice; the group score
+        // is their sum)
         const int e0 = ti.nt * C::BN + half * COLS;
         bool bad = false;
-        float gq[COLS / 32];
+        float g1[COLS / 32], g2[COLS / 32];
 #pragma unroll
         for (int q = 0; q < COLS / 32; ++q) {
             float m1 = -INFINITY, m2 = -INFINITY;
@@ -1136,13 +1137,16 @@ __device__ __forceinline__ bool router_epilogue_tile(const GemmParams &p, const 
                 m2 = fmaxf(m2, fminf(m1, b));
                 m1 = fmaxf(m1, b);
             }
-            gq[q] = m1 + m2;
+            g1[q] = m1;
+            g2[q] = m2;
         }
         if (lane < valid_rows) {
-            float *g = p.gscore + (size_t)(ti.out_row + quad * 32 + lane) * (p.E / 32) + e0 / 32;
+            float *g = p.gscore + ((size_t)(ti.out_row + quad * 32 + lane) * (p.E / 32) + e0 / 32) * 2;
 #pragma unroll
-            for (int q = 0; q < COLS / 32; ++q)
-                g[q] = gq[q];
+            for (int q = 0; q < COLS / 32; ++q) {
+                g[2 * q] = g1[q];
+                g[2 * q + 1] = g2[q];
+            }
         }
         if (__any_sync(0xffffffffu, bad && lane < valid_rows) && lane == 0)
             atomicOr(p.status, ST_NONFINITE);

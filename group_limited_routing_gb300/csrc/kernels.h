@@ -202,9 +202,9 @@ struct GemmParams {
     int cap_rows;
     // router kinds, scored output (no K split): when set, `out` receives the
     // sigmoid scores s = router_sigmoid(logit) instead of the logits, and
-    // gscore [T, E / 32] every group's score (the sum of its two best biased
-    // scores s + bias, bias = `bias` or zero); non-finite logits set
-    // ST_NONFINITE
+    // gscore [T, E / 32, 2] every group's two best biased scores s + bias
+    // (bias = `bias` or zero; a tie for the top counts twice; the group score
+    // is their fp32 sum); non-finite logits set ST_NONFINITE
     float *gscore;
 };
 
@@ -235,7 +235,8 @@ cudaError_t launch_route_select(const float *logits, int nparts, long long part_
                                 cudaStream_t s);
 
 // The same selection from the router GEMM's scored output (sigmoid scores
-// [T, E] and group scores [T, E / 32]), for 8 groups of 32 with 4 kept; same
+// [T, E] and every group's two best biased scores [T, E / 32, 2]), for 8
+// groups of 32 with 4 kept; same
 // outputs, bit for bit.  chunk_hist (nullable): per PERM_CHUNK-token chunk
 // hits per expert, [E][ceil(T / PERM_CHUNK)] (the bucketing histogram).
 cudaError_t launch_route_select_scored(const float *scores, const float *gscore, const float *bias, int T, int E,

@@ -527,28 +527,27 @@ __global__ void __launch_bounds__(256) route_select_scored_kernel(
 
     const int t0 = blockIdx.x * chunk;
     const int t1 = min(T, t0 + chunk);
-    static_assert(G % 4 == 0, "group scores are read as float4");
-    // the token's group scores (every lane reads the same row of G floats);
-    // the next token's row is loaded before the current token is processed
-    float4 gn[G / 4];
+    static_assert(G % 2 == 0, "group score pairs are read as float4");
+    // the token's groups' two best scores (every lane reads the same row of
+    // 2 G floats); the next token's row is loaded before the current token is
+    // processed; the group score is their sum
+    float4 gn[G / 2];
     if (t0 + warp < t1) {
 #pragma unroll
-        for (int v = 0; v < G / 4; ++v)
-            gn[v] = __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)(t0 + warp) * G) + v);
+        for (int v = 0; v < G / 2; ++v)
+            gn[v] = __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)(t0 + warp) * 2 * G) + v);
     }
     for (int t = t0 + warp; t < t1; t += 8) {
         float g[G];
 #pragma unroll
-        for (int v = 0; v < G / 4; ++v) {
-            g[4 * v] = gn[v].x;
-            g[4 * v + 1] = gn[v].y;
-            g[4 * v + 2] = gn[v].z;
-            g[4 * v + 3] = gn[v].w;
+        for (int v = 0; v < G / 2; ++v) {
+            g[2 * v] = gn[v].x + gn[v].y;
+            g[2 * v + 1] = gn[v].z + gn[v].w;
         }
         if (t + 8 < t1) {
 #pragma unroll
-            for (int v = 0; v < G / 4; ++v)
-                gn[v] = __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)(t + 8) * G) + v);
+            for (int v = 0; v < G / 2; ++v)
+                gn[v] = __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)(t + 8) * 2 * G) + v);
         }
         float gl = g[0];
 #pragma unroll
@@ -748,6 +747,7 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
     static_assert(2 * PERM_CHUNK == 32, "a block is two bucketing chunks");
     __shared__ float sb[G * GP];
     __shared__ int sh_hist[2][E];
+    __shared__ float sbq[128 * 33];              // per lane: its group's 32 biased scores
     const int tid = threadIdx.x, lane = tid & 31;
     const int q = tid & 3;
     bool nonfinite = false;
@@ -764,17 +764,21 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
     const int t = t0 + tl;
     const bool valid = t < T;
 
-    // kept groups: this lane ranks groups 2q and 2q + 1
-    float g[G];
+    // the token's groups' two best biased scores; group score = their sum
+    float m1[G], m2[G], g[G];
 #pragma unroll
-    for (int v = 0; v < G / 4; ++v) {
-        const float4 x = valid ? __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)t * G) + v)
+    for (int v2 = 0; v2 < G / 2; ++v2) {
+        const float4 x = valid ? __ldg(reinterpret_cast<const float4 *>(gscore + (size_t)t * 2 * G) + v2)
                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        g[4 * v] = x.x;
-        g[4 * v + 1] = x.y;
-        g[4 * v + 2] = x.z;
-        g[4 * v + 3] = x.w;
+        m1[2 * v2] = x.x;
+        m2[2 * v2] = x.y;
+        m1[2 * v2 + 1] = x.z;
+        m2[2 * v2 + 1] = x.w;
     }
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+        g[i] = m1[i] + m2[i];
+    // kept groups: this lane ranks groups 2q and 2q + 1
     uint32_t keep = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -791,6 +795,13 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
     }
     keep |= __shfl_xor_sync(0xffffffffu, keep, 1);
     keep |= __shfl_xor_sync(0xffffffffu, keep, 2);
+    // a floor under the token's 8th-best score: the kept groups hold 2 TG >= 8
+    // scores at or above the smallest of their top-2, so nothing below it can
+    // be chosen (TG = 4, k <= 8)
+    float floor8 = 3.402823466e38f;
+#pragma unroll
+    for (int i = 0; i < G; ++i)
+        floor8 = ((keep >> i) & 1u) ? fminf(floor8, m2[i]) : floor8;
 
     // this lane's kept group: the q-th set bit of keep
     uint32_t kk = keep;
@@ -800,12 +811,27 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
             kk &= kk - 1u;
     const int j = valid ? __ffs(kk) - 1 : 0;
     const float4 *s4 = reinterpret_cast<const float4 *>(scores + (size_t)(valid ? t : 0) * E + 32 * j);
-    float4 sv[8];
+    // the group's biased scores into this lane's shared-memory row, and the
+    // bits of those at or above the floor
+    float *brow = sbq + (size_t)tid * 33;
+    uint32_t cand = 0;
 #pragma unroll
-    for (int i4 = 0; i4 < 8; ++i4)
-        sv[i4] = valid ? __ldg(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 sv = valid ? __ldg(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float sc[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float b = sc[u] + sb[j * GP + 4 * i4 + u];   // section 三: choose on s + bias
+            brow[4 * i4 + u] = b;
+            cand |= (valid && b >= floor8) ? (1u << (4 * i4 + u)) : 0u;
+        }
+    }
+    __syncwarp();
 
-    // (empty entries hold the most negative finite float and id -1)
+    // this lane's candidates in ascending id order through an 8-entry list in
+    // descending order of biased score: a candidate enters when it beats the
+    // last entry and moves up past every strictly smaller one, so equal
+    // scores keep the lower id first (empty entries: most negative float, id -1)
     float v[8];
     int ev[8];
 #pragma unroll
@@ -813,28 +839,23 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
         v[p] = -3.402823466e38f;
         ev[p] = -1;
     }
+    while (cand) {
+        const int i = __ffs(cand) - 1;
+        cand &= cand - 1u;
+        const float b = brow[i];
+        const int id = 32 * j + i;
+        const bool in = b > v[7];
+        v[7] = in ? b : v[7];
+        ev[7] = in ? id : ev[7];
 #pragma unroll
-    for (int i4 = 0; i4 < 8; ++i4) {
-        const float sc[4] = {sv[i4].x, sv[i4].y, sv[i4].z, sv[i4].w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const float b = sc[u] + sb[j * GP + 4 * i4 + u];   // section 三: choose on s + bias
-            const int id = 32 * j + 4 * i4 + u;
-            // the candidate replaces the last entry when it beats it, then moves
-            // up past every strictly smaller entry
-            const bool in = b > v[7];
-            v[7] = in ? b : v[7];
-            ev[7] = in ? id : ev[7];
-#pragma unroll
-            for (int p = 7; p > 0; --p) {
-                const bool up = v[p] > v[p - 1];
-                const float tv = v[p - 1];
-                const int te = ev[p - 1];
-                v[p - 1] = up ? v[p] : tv;
-                ev[p - 1] = up ? ev[p] : te;
-                v[p] = up ? tv : v[p];
-                ev[p] = up ? te : ev[p];
-            }
+        for (int p = 7; p > 0; --p) {
+            const bool up = v[p] > v[p - 1];
+            const float tv = v[p - 1];
+            const int te = ev[p - 1];
+            v[p - 1] = up ? v[p] : tv;
+            ev[p - 1] = up ? ev[p] : te;
+            v[p] = up ? tv : v[p];
+            ev[p] = up ? te : ev[p];
         }
     }
     sel_merge(v, ev, lane, 1);
