@@ -348,10 +348,21 @@ T *at(void *ws, size_t off)
 // split W into the workspace here (that launch also clears counts).
 // ksplit_max: K parts the logits buffer has room for (L.ksplit, or 1 for a
 // caller's [T, E] buffer); nparts receives the parts actually written.
+// Whether router_gemm gives the scored output when asked: the tensor-core
+// router without a K split, for the routing page's 256 experts in 8 groups of
+// which 4 are kept.
+bool router_scores(const moe_cfg &c, const RouteLayout &L, const float *W, int sms)
+{
+    if (c.T <= ROUTER_SIMT_MAX_T && c.H % 8 == 0 && aligned(W, 16))
+        return false;                     // the CUDA-core router
+    const bool wide = c.E % 256 == 0 && (c.T + GEMM_BM - 1) / GEMM_BM >= sms;
+    const int ks = wide ? 1 : L.ksplit;
+    return ks == 1 && c.E == 256 && c.n_group == 8 && c.topk_group == 4;
+}
+
 // gscore (nullable): ask for the scored output (sigmoid scores in `logits`,
-// group scores in gscore, bias = `bias`); `scored` tells whether it was
-// produced -- only by the tensor-core router without a K split, for the
-// routing page's 256 experts in 8 groups of which 4 are kept.
+// each group's two best scores in gscore, bias = `bias`); `scored` tells
+// whether it was produced (router_scores).  counts (nullable) is cleared.
 int router_gemm(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split, float *logits,
                 int32_t *counts, void *ws, const RouteLayout &L, int sms, cudaStream_t s, int &launches,
                 int ksplit_max, int &nparts, const float *bias = nullptr, float *gscore = nullptr,
@@ -448,21 +459,31 @@ int route_select(const moe_cfg &c, const float *logits, int nparts, const float 
 
 // Router GEMM and selection (moe_route's kernels): the scored router output
 // when the shape allows it.  With chunk_hist, hist_done tells whether the
-// selection wrote the bucketing histogram there.
+// selection wrote the bucketing histogram there, and counts_left whether it
+// left `counts` to the scan of that histogram (no balance loss asked for:
+// the loss needs the counts before the scan runs).
 int route_all(const moe_cfg &c, const moe_bf16 *hidden, const float *W, const moe_bf16 *W_split, const float *bias,
               int32_t *idx, float *w, int32_t *counts, float *aux_P, float *aux_loss, void *ws, const RouteLayout &L,
-              int sms, cudaStream_t s, int &launches, int32_t *chunk_hist = nullptr, bool *hist_done = nullptr)
+              int sms, cudaStream_t s, int &launches, int32_t *chunk_hist = nullptr, bool *hist_done = nullptr,
+              bool *counts_left = nullptr)
 {
     float *logits = at<float>(ws, L.logits);
     int nparts = 1;
     bool scored = false;
-    int rc = router_gemm(c, hidden, W, W_split, logits, counts, ws, L, sms, s, launches, L.ksplit, nparts, bias,
-                         at<float>(ws, L.gscore), &scored);
+    // with the histogram asked for, the expert stage's scan of it forms the
+    // counts: the routing kernel then leaves them alone (no atomics, no clear)
+    const bool by_scan = chunk_hist && !aux_P && !aux_loss && router_scores(c, L, W, sms);
+    int rc = router_gemm(c, hidden, W, W_split, logits, by_scan ? nullptr : counts, ws, L, sms, s, launches,
+                         L.ksplit, nparts, bias, at<float>(ws, L.gscore), &scored);
+    if (rc == MOE_OK && by_scan && !scored)
+        rc = MOE_ERR_CUDA;               // (router_scores disagrees with the router: never expected)
     if (rc == MOE_OK)
-        rc = route_select(c, logits, nparts, bias, idx, w, counts, aux_P, aux_loss, ws, L, s, launches, scored,
-                          scored ? chunk_hist : nullptr);
+        rc = route_select(c, logits, nparts, bias, idx, w, by_scan ? nullptr : counts, aux_P, aux_loss, ws, L, s,
+                          launches, scored, scored ? chunk_hist : nullptr);
     if (hist_done)
         *hist_done = scored && chunk_hist;
+    if (counts_left)
+        *counts_left = by_scan;
     return rc;
 }
 
@@ -590,7 +611,7 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
                  const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const int32_t *topk_idx,
                  const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *ws, const FwdLayout &L,
                  const int32_t *offs, int sms, cudaStream_t s, int &launches, bool hist_ready = false,
-                 bool with_shared = true)
+                 bool with_shared = true, int32_t *counts_out = nullptr)
 {
     // with_shared = false (moe_expert_rows): no shared-expert group, k = 1, and
     // out receives every pair's unweighted expert row in pair order instead
@@ -616,7 +637,7 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
         // (the routing kernel of moe_layer may have written the histogram already)
         if (!hist_ready)
             GLR_LAUNCH(KID_HIST, launch_bucket_hist(topk_idx, c.T, c.E, c.k, hist, &hdr->status, s));
-        GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s));
+        GLR_LAUNCH(KID_SCAN, launch_bucket_scan(hist, L.nchunk, c.E, sizes, s, counts_out));
         GLR_LAUNCH(KID_SCATTER, launch_bucket_scatter(topk_idx, hidden, hist, sizes, c.T, c.H, c.E, c.k, slot_of,
                                                       xperm, mtiles, hdr, s, at<int4>(ws, L.ptiles), with_shared));
     }
@@ -1256,12 +1277,13 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
     } else {
         // the routing kernel also writes the bucketing histogram where the
         // expert stage reads it (when the router's scored output is taken)
-        bool hist_done = false;
+        bool hist_done = false, counts_left = false;
         rc = route_all(c, hidden, W_router, W_split, expert_bias, topk_idx, topk_w, expert_counts, aux_P, aux_loss, ws,
-                       L.r, sms, s, launches, at<int32_t>(ws, L.f.hist), &hist_done);
+                       L.r, sms, s, launches, at<int32_t>(ws, L.f.hist), &hist_done, &counts_left);
         if (rc == MOE_OK)
             rc = forward_impl(c, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, residual,
-                              out, ws, L.f, nullptr, sms, s, launches, hist_done);
+                              out, ws, L.f, nullptr, sms, s, launches, hist_done, true,
+                              counts_left ? expert_counts : nullptr);
     }
     g_last_launches = launches;
     return rc;

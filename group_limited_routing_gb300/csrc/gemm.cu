@@ -1644,7 +1644,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) router_pair_kernel(const __gr
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
                     if (kb % ROUTER_KPS == 0) {
-                        if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit)) {
+                        // (the peer's forwarder arrives here across the pair)
+                        if (!mbar_wait_cluster(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit)) {
                             ok = false;
                             break;
                         }
@@ -1912,7 +1913,8 @@ __global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const _
                 if (tile >= num_tiles)
                     break;
                 const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
-                if (!mbar_wait(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit))
+                // (the peer's forwarder arrives here across the pair)
+                if (!mbar_wait_cluster(tempty0 + 8u * slot, par ^ 1u, abort_flag, limit))
                     break;
                 tc_fence_after();
                 const uint32_t d = tmem + slot * 256;

@@ -257,7 +257,9 @@ cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t 
                                cudaStream_t s);
 
 // hist [E][nchunk] -> per-chunk starts inside each bucket (relative); sizes[E]
-cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s);
+// (and the same into sizes2[E] when given)
+cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s,
+                               int32_t *sizes2 = nullptr);
 
 // ptiles (nullable): also the 256-row pair-tile list (hdr->num_ptiles);
 // with_shared = false: no shared-expert group in the tile lists

@@ -83,7 +83,7 @@ cudaError_t launch_bucket_hist(const int32_t *idx, int T, int E, int k, int32_t 
 // then the 8 warp totals in warp order), then the run is rewritten in place.
 // The bucket offsets follow in bucket_scatter.
 __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ hist, int nchunk, int E,
-                                                          int32_t *__restrict__ sizes)
+                                                          int32_t *__restrict__ sizes, int32_t *__restrict__ sizes2)
 {
     pdl_wait();
     __shared__ int wtot[8];
@@ -168,13 +168,16 @@ __global__ void __launch_bounds__(256) bucket_scan_kernel(int32_t *__restrict__ 
             run += h;
         }
     }
-    if (threadIdx.x == blockDim.x - 1)
+    if (threadIdx.x == blockDim.x - 1) {
         sizes[e] = run;                           // the last run ends at the bucket's size
+        if (sizes2)
+            sizes2[e] = run;                      // (moe_layer's expert_counts output)
+    }
 }
 
-cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s)
+cudaError_t launch_bucket_scan(int32_t *hist, int nchunk, int E, int32_t *sizes, cudaStream_t s, int32_t *sizes2)
 {
-    const cudaError_t le = launch_pdl(bucket_scan_kernel, dim3(E), dim3(256), 0, s, hist, nchunk, E, sizes);
+    const cudaError_t le = launch_pdl(bucket_scan_kernel, dim3(E), dim3(256), 0, s, hist, nchunk, E, sizes, sizes2);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(256) route_select_scored_kernel(
 #pragma unroll
         for (int q = 0; q < NQ; ++q)
             tot += sh_hist[q][e];
-        if (tot)
+        if (counts && tot)
             atomicAdd(&counts[e], tot);              // integer sums: the result is order-free
         if (chunk_hist) {
             for (int q = 0; q < nq; ++q)
@@ -898,7 +898,7 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
     const int nq = (min(T, t0 + 32) - t0 + PERM_CHUNK - 1) / PERM_CHUNK;
     for (int e = tid; e < E; e += blockDim.x) {
         const int a = sh_hist[0][e], b = sh_hist[1][e];
-        if (a + b)
+        if (counts && a + b)
             atomicAdd(&counts[e], a + b);            // integer sums: the result is order-free
         if (chunk_hist) {
             chunk_hist[(size_t)e * nchunk_perm + 2 * blockIdx.x] = a;
