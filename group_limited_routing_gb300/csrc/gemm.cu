@@ -459,9 +459,13 @@ __device__ __forceinline__ void store_piece(const GemmParams &p, uint8_t *stage2
         }
         buf = (buf + 1) % NBUF;
     } else if (valid_rows > 0) {
+        // this path commits no bulk group, so "all but the newest NBUF - 1
+        // groups have read smem" no longer means "every other buffer is
+        // free": after a masked piece the newest group can be the one that
+        // reads this very buffer.  Wait until every store has left smem.
         uint8_t *stage = stage2 + buf * 4096;
         if (lane == 0)
-            bulk_wait_group_read<NBUF - 1>();
+            bulk_wait_group_read<0>();
         __syncwarp();
         warp_store_rows128(stage, v, lane, gbase, ld_bytes, valid_rows);
         buf = (buf + 1) % NBUF;

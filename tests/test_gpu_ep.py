@@ -34,11 +34,30 @@ def test_ep_local_equals_moe_forward(world, T, wid):
     shards = _shards(cfg, d, world)
     xs = [wl.hidden(w0, DEV, layer=r) for r in range(world)]
     outs = ep.ep_forward_local(shards, xs)
+    snap = [o.clone() for o in outs]
     for r in range(world):
         idx, w, _, _, _ = moe.route(cfg, xs[r], d["W_router"], d["expert_bias"])
         ref = moe.forward(cfg, xs[r], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
         torch.cuda.synchronize()
-        assert torch.equal(outs[r], ref), "rank %d of %d" % (r, world)
+        assert torch.equal(outs[r], ref), "rank %d of %d: %s" % (r, world, _mismatch_report(
+            cfg, d, shards, xs, outs, r, ref, idx, w, snap))
+
+
+def _mismatch_report(cfg, d, shards, xs, outs, r, ref, idx, w, snap):
+    """What differs when a rank's output is not moe_forward's: the tokens,
+    the routing, and whether each side repeats itself."""
+    bad = (outs[r] != ref).any(1).nonzero().flatten()
+    disp = shards[r].dispatch(xs[r])
+    ref2 = moe.forward(cfg, xs[r], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
+    outs2 = ep.ep_forward_local(shards, xs)
+    torch.cuda.synchronize()
+    t0 = int(bad[0])
+    return ("%d tokens differ (first %s, max |diff| %g); EP routing equals moe_route: %s / %s; token %d experts %s; "
+            "moe_forward repeats itself: %s; the EP step repeats itself: %s, and then equals moe_forward: %s; "
+            "the output changed after the EP step: %s" % (
+                bad.numel(), bad[:8].tolist(), (outs[r].float() - ref.float()).abs().max().item(),
+                torch.equal(disp.idx, idx), torch.equal(disp.w, w), t0, idx[t0].tolist(), torch.equal(ref2, ref),
+                torch.equal(outs2[r], outs[r]), torch.equal(outs2[r], ref), not torch.equal(snap[r], outs[r])))
 
 
 def test_ep_rank_that_receives_nothing():
