@@ -305,6 +305,7 @@ struct ScatterBwd {
     int shared_base;        // first shared-expert row (past every routed row for any routing)
 };
 
+template <bool EARLY>
 __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__restrict__ idx,
                                                              const uint16_t *__restrict__ x,
                                                              const int32_t *__restrict__ chunk_base,
@@ -325,6 +326,22 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
     const int t0 = blockIdx.x * PERM_CHUNK;
     const int nt = min(PERM_CHUNK, T - t0);
     const bool backward = bw.do_perm != nullptr;
+    // forward, with a whole number of rows per pass (H / 8 divides the block):
+    // every thread loads its 16-byte column of the chunk's rows now, so that
+    // the loads are in flight while the offsets and slots are worked out
+    const int vec_per_row = H / 8;                    // 16-byte vectors
+    const bool early = EARLY && !backward && vec_per_row <= (int)blockDim.x && blockDim.x % vec_per_row == 0;
+    const int rpp = early ? (int)blockDim.x / vec_per_row : 1;
+    uint4 val_e[EARLY ? PERM_CHUNK : 1];
+    if (early) {
+        const int sub = threadIdx.x / vec_per_row, v = threadIdx.x % vec_per_row;
+#pragma unroll
+        for (int u = 0; u < PERM_CHUNK; ++u) {
+            const int tt = sub + u * rpp;
+            if (u * rpp < PERM_CHUNK && tt < nt)
+                val_e[u] = reinterpret_cast<const uint4 *>(x + (size_t)(t0 + tt) * H)[v];
+        }
+    }
     bucket_offsets(sizes, T, E, K, offset, tstart, wsum_rows, wsum_tiles, blockIdx.x == 0, mtiles, hdr,
                    backward ? BWD_ROW_ALIGN : 1, bw.eoff, bw.shared_base, 0, ptiles, with_shared != 0);
     for (int e = threadIdx.x; e < E; e += blockDim.x)
@@ -359,8 +376,22 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
         for (int tt = threadIdx.x; tt < nt; tt += blockDim.x)
             bw.w_perm[bw.shared_base + t0 + tt] = 1.0f;   // shared-expert rows
     __syncthreads();
+    if (early) {
+        // each token row read once (above) and written to its K slots
+        const int sub = threadIdx.x / vec_per_row, v = threadIdx.x % vec_per_row;
+#pragma unroll
+        for (int u = 0; u < PERM_CHUNK; ++u) {
+            const int tt = sub + u * rpp;
+            if (u * rpp < PERM_CHUNK && tt < nt)
+                for (int j = 0; j < K; ++j) {
+                    const int slot = slots[tt * K + j];
+                    if (slot >= 0)
+                        reinterpret_cast<uint4 *>(x_perm + (size_t)slot * H)[v] = val_e[u];
+                }
+        }
+        return;
+    }
     // gather: each token row is read once and written to its K slots
-    const int vec_per_row = H / 8;                    // 16-byte vectors
     const int rows_per_pass = blockDim.x / vec_per_row > 0 ? blockDim.x / vec_per_row : 1;
     const int sub = threadIdx.x / vec_per_row;
     const int v = threadIdx.x % vec_per_row;
@@ -413,9 +444,16 @@ cudaError_t launch_bucket_scatter(const int32_t *idx, const uint16_t *x, const i
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
     const ScatterBwd none = {nullptr, nullptr, nullptr, nullptr, nullptr, 0};
-    const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
-                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none, ptiles,
-                                      with_shared ? 1 : 0);
+    // (the row loads go out before the slots are known when whole rows fit a
+    // pass of the block: H / 8 divides 256)
+    const int vpr = H / 8;
+    const bool early = vpr <= 256 && 256 % vpr == 0;
+    const cudaError_t le = early ? launch_pdl(bucket_scatter_kernel<true>, dim3(blocks), dim3(256), smem, s, idx, x,
+                                              chunk_base, sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none, ptiles,
+                                              with_shared ? 1 : 0)
+                                 : launch_pdl(bucket_scatter_kernel<false>, dim3(blocks), dim3(256), smem, s, idx, x,
+                                              chunk_base, sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, none, ptiles,
+                                              with_shared ? 1 : 0);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();
@@ -430,8 +468,8 @@ cudaError_t launch_bucket_scatter_bwd(const int32_t *idx, const uint16_t *x, con
     const int blocks = (T + PERM_CHUNK - 1) / PERM_CHUNK;
     const size_t smem = (size_t)(E + PERM_CHUNK * k) * sizeof(int);
     const ScatterBwd bw = {dout, w, do_perm, w_perm, eoff, shared_base};
-    const cudaError_t le = launch_pdl(bucket_scatter_kernel, dim3(blocks), dim3(256), smem, s, idx, x, chunk_base,
-                                      sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, bw, (int4 *)nullptr, 1);
+    const cudaError_t le = launch_pdl(bucket_scatter_kernel<false>, dim3(blocks), dim3(256), smem, s, idx, x,
+                                      chunk_base, sizes, T, H, E, k, slot_of, x_perm, mtiles, hdr, bw, (int4 *)nullptr, 1);
     if (le != cudaSuccess)
         return le;
     return cudaPeekAtLastError();

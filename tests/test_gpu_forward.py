@@ -188,6 +188,37 @@ def test_forward_is_deterministic():
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("wid,T", [(4, 8192), (6, 30000)])
+def test_forward_on_freshly_mapped_memory_repeats_itself(wid, T):
+    """The grouped GEMMs on a workspace and outputs the driver has just
+    mapped (the allocator's cache emptied first: cold address translation,
+    slow TMA stores) must give the warm run's rows bit for bit, through
+    moe_forward and through moe_expert_rows on ~2T rows.  A bucket's
+    part-filled output piece once reused a staging buffer that the previous
+    TMA store of the same warp could still be reading."""
+    w0 = wl.WORKLOADS[wid].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is)
+    idx, w, _, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"])
+    ref = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w)
+    cfg_r = moe.MoeConfig(T=T, H=w0.H, I=w0.I, Is=w0.Is, E=64, n_group=2)
+    n = 2 * T
+    xr = d["hidden"].repeat(2, 1).contiguous()
+    er = (idx.flatten()[:n] % 64).to(torch.int32).contiguous()
+    ref_rows = moe.expert_rows(cfg_r, xr, er, d["W_gate_up"][:64], d["W_down"][:64])
+    torch.cuda.synchronize()
+    for rep in range(3):
+        torch.cuda.empty_cache()
+        out = moe.forward(cfg, d["hidden"], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"],
+                          idx, w)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref), "moe_forward, repetition %d" % rep
+        torch.cuda.empty_cache()
+        rows = moe.expert_rows(cfg_r, xr, er, d["W_gate_up"][:64], d["W_down"][:64])
+        torch.cuda.synchronize()
+        assert torch.equal(rows, ref_rows), "moe_expert_rows, repetition %d" % rep
+
+
 @pytest.mark.parametrize("T,kernels", [(128, 6), (32, 4), (16, 4)])
 def test_forward_launch_count(T, kernels):
     # hist, scan, scatter (one launch for T <= 32), gate/up GEMM, down GEMM, combine
