@@ -578,7 +578,12 @@ def report(args, world, w0, ms_max, prof, nprof, e2e_ms, launches, clk, extra):
     rp_names = ("split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist", "bucket_scan",
                 "bucket_scatter", "router_route_bucket", "bucket_tiles")
     rp_ms = sum(stages[n]["ms"] * stages[n]["launches_per_step"] for n in rp_names if n in stages)
-    rp_bytes = T * H * 2 + E * H * 4 + T * k * 8 + T * k * 4 * 2 + T * H * 2 + k * T * H * 2
+    # the stage's algorithmic bytes per token (x read by the router, idx and w
+    # written, the scores between the two kernels written and read, idx read
+    # again by the bucketing, the two slot maps, x read by the gather and its
+    # k copies written) plus the router weight once
+    rp_bytes = (T * H * 2 + T * k * 8 + 2 * T * E * 4 + T * k * 4 + T * k * 4 * 2 + T * H * 2 + k * T * H * 2
+                + E * H * 4)
     if extra["backward"]:
         # the backward's bucketing: x and d_out read, both permuted ((k+1)T rows each) written
         rp_bytes = 2 * T * H * 2 + T * k * 8 + 2 * (k + 1) * T * H * 2
