@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
     static_assert(2 * PERM_CHUNK == 32, "a block is two bucketing chunks");
     __shared__ float sb[G * GP];
     __shared__ int sh_hist[2][E];
-    __shared__ float sbq[128 * 33];              // per lane: its group's 32 biased scores
+    __shared__ float sbq[128 * 33];              // per lane: its kept group's 32 scores
     const int tid = threadIdx.x, lane = tid & 31;
     const int q = tid & 3;
     bool nonfinite = false;
@@ -811,8 +811,9 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
             kk &= kk - 1u;
     const int j = valid ? __ffs(kk) - 1 : 0;
     const float4 *s4 = reinterpret_cast<const float4 *>(scores + (size_t)(valid ? t : 0) * E + 32 * j);
-    // the group's biased scores into this lane's shared-memory row, and the
-    // bits of those at or above the floor
+    // the group's scores into this lane's shared-memory row (the weights
+    // below read them back from there), and the bits of those whose biased
+    // score is at or above the floor
     float *brow = sbq + (size_t)tid * 33;
     uint32_t cand = 0;
 #pragma unroll
@@ -822,7 +823,7 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const float b = sc[u] + sb[j * GP + 4 * i4 + u];   // section 三: choose on s + bias
-            brow[4 * i4 + u] = b;
+            brow[4 * i4 + u] = sc[u];
             cand |= (valid && b >= floor8) ? (1u << (4 * i4 + u)) : 0u;
         }
     }
@@ -842,7 +843,7 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
     while (cand) {
         const int i = __ffs(cand) - 1;
         cand &= cand - 1u;
-        const float b = brow[i];
+        const float b = brow[i] + sb[j * GP + i];         // the same fp32 sum as above
         const int id = 32 * j + i;
         const bool in = b > v[7];
         v[7] = in ? b : v[7];
@@ -861,12 +862,17 @@ __global__ void __launch_bounds__(128) route_select_quad_kernel(
     sel_merge(v, ev, lane, 1);
     sel_merge(v, ev, lane, 2);
 
-    // weights from the unbiased scores, normaliser in output order (section 二 step 3)
-    const float *srow = scores + (size_t)(valid ? t : 0) * E;
+    // weights from the unbiased scores, normaliser in output order (section 二
+    // step 3); the score of expert e sits in the row of the quad lane that
+    // handled its group (group g is the lane's kept group when g is the
+    // lane's-index-th set bit of keep)
+    const float *qrows = sbq + (size_t)(tid & ~3) * 33;
     float sw[8];
 #pragma unroll
-    for (int p = 0; p < 8; ++p)
-        sw[p] = (valid && p < K && ev[p] >= 0) ? __ldg(srow + ev[p]) : 0.0f;
+    for (int p = 0; p < 8; ++p) {
+        const int e = ev[p];
+        sw[p] = (valid && p < K && e >= 0) ? qrows[__popc(keep & ((1u << (e >> 5)) - 1u)) * 33 + (e & 31)] : 0.0f;
+    }
     float den = 0.0f;
 #pragma unroll
     for (int p = 0; p < 8; ++p)
