@@ -288,6 +288,15 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
     }
 }
 
+// A 16-byte store marked as streaming (evict first): the bucketed copy of the
+// rows is written once and read once by the next kernel, and should not push
+// other lines out of L2 on the way.
+__device__ __forceinline__ void st_global_streaming(uint4 *p, const uint4 v)
+{
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Stable slots for one chunk, then the row gather.  Warp 0 assigns slots in
 // (token, j) order, 32 pairs at a time: lanes holding the same expert find
@@ -386,7 +395,7 @@ __global__ void __launch_bounds__(256) bucket_scatter_kernel(const int32_t *__re
                 for (int j = 0; j < K; ++j) {
                     const int slot = slots[tt * K + j];
                     if (slot >= 0)
-                        reinterpret_cast<uint4 *>(x_perm + (size_t)slot * H)[v] = val_e[u];
+                        st_global_streaming(reinterpret_cast<uint4 *>(x_perm + (size_t)slot * H) + v, val_e[u]);
                 }
         }
         return;
