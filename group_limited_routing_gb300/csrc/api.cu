@@ -28,13 +28,14 @@ thread_local int g_last_launches = 0;
 enum KernelId {
     KID_SPLIT = 0, KID_ROUTER_GEMM, KID_SELECT, KID_FINALIZE, KID_HIST, KID_SCAN, KID_SCATTER,
     KID_GEMM_GATE_UP, KID_GEMM_DOWN, KID_COMBINE, KID_DENSE_TILES, KID_BWD_RECOMPUTE, KID_BWD_DGRAD,
-    KID_BWD_DX, KID_BWD_WGRAD, KID_BWD_MISC, KID_ROUTE_FUSED, KID_TILES
+    KID_BWD_DX, KID_BWD_WGRAD, KID_BWD_MISC, KID_ROUTE_FUSED, KID_TILES,
+    KID_STAGE_ROUTE_PERMUTE   // (per-stage timing) the routing and bucketing kernels as one interval
 };
 const char *const kKernelNames[MOE_KERNEL_COUNT] = {
     "split_router", "router_gemm", "route_select", "route_finalize", "bucket_hist",
     "bucket_scan", "bucket_scatter", "gemm_gate_up_swiglu", "gemm_down", "combine", "dense_tiles",
     "bwd_gate_up_recompute", "bwd_dgrad_down_swiglu", "bwd_dgrad_x", "bwd_weight_grads", "bwd_pad_and_dw",
-    "router_route_bucket", "bucket_tiles"};
+    "router_route_bucket", "bucket_tiles", "router_plus_permute"};
 
 struct ProfRecord {
     cudaEvent_t start, stop;
@@ -61,6 +62,37 @@ cudaEvent_t pool_event()
     return e;
 }
 
+// Per-stage timing (moe_profile_enable(2)): the kernels of the routing and
+// bucketing stage form one interval and every other kernel its own, and
+// events are recorded only where the stage changes, so that the kernels of
+// one stage still overlap each other's launch and tail (programmatic stream
+// serialisation) as they do unprofiled.  The open stage of this thread:
+thread_local int t_stage = -1;
+thread_local cudaEvent_t t_stage_start = nullptr;
+thread_local cudaStream_t t_stage_stream = nullptr;
+
+int prof_stage(int kid)
+{
+    switch (kid) {
+    case KID_SPLIT: case KID_ROUTER_GEMM: case KID_SELECT: case KID_FINALIZE: case KID_HIST: case KID_SCAN:
+    case KID_SCATTER: case KID_ROUTE_FUSED: case KID_TILES:
+        return KID_STAGE_ROUTE_PERMUTE;
+    default:
+        return kid;
+    }
+}
+
+// ends the open stage with an event on its stream (g_prof_mu held)
+void prof_close_stage_locked()
+{
+    if (t_stage < 0)
+        return;
+    cudaEvent_t stop = pool_event();
+    cudaEventRecord(stop, t_stage_stream);
+    g_prof_pending.push_back(ProfRecord{t_stage_start, stop, t_stage});
+    t_stage = -1;
+}
+
 struct ProfScope {
     bool on;
     ProfRecord r;
@@ -70,6 +102,18 @@ struct ProfScope {
         if (!on)
             return;
         std::lock_guard<std::mutex> g(g_prof_mu);
+        if (g_prof_on.load(std::memory_order_relaxed) == 2) {
+            const int stage = prof_stage(kid);
+            if (stage != t_stage || st != t_stage_stream) {
+                prof_close_stage_locked();
+                t_stage = stage;
+                t_stage_stream = st;
+                t_stage_start = pool_event();
+                cudaEventRecord(t_stage_start, st);
+            }
+            on = false;
+            return;
+        }
         r.start = pool_event();
         r.stop = pool_event();
         r.kid = kid;
@@ -83,6 +127,18 @@ struct ProfScope {
         std::lock_guard<std::mutex> g(g_prof_mu);
         g_prof_pending.push_back(r);
         on = false;
+    }
+};
+
+// At the end of every public call that launches kernels: closes the stage
+// left open by its last launch.
+struct ProfCall {
+    ~ProfCall()
+    {
+        if (g_prof_on.load(std::memory_order_relaxed) != 2)
+            return;
+        std::lock_guard<std::mutex> g(g_prof_mu);
+        prof_close_stage_locked();
     }
 };
 
@@ -789,6 +845,7 @@ int moe_workspace_init(void *ws, size_t ws_bytes, void *stream)
 int moe_router_logits(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, float *logits, void *ws,
                       size_t ws_bytes, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_route_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
@@ -814,6 +871,7 @@ int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *
                           float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss, void *ws,
                           size_t ws_bytes, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_route_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
@@ -840,6 +898,7 @@ int moe_route_from_logits(const moe_cfg *cfg, const float *logits, const float *
 
 int moe_router_scores(const float *logits, float *scores, int64_t n, void *stream)
 {
+    ProfCall prof_call_;
     if (!logits || !scores || n < 1)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(logits, 4) || !aligned(scores, 4))
@@ -857,6 +916,7 @@ int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
               int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss, void *ws,
               size_t ws_bytes, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_route_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
@@ -881,6 +941,7 @@ int moe_route(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
 
 int moe_prepare_router(const moe_cfg *cfg, const float *W_router, moe_bf16 *W_split, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_route_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
@@ -903,6 +964,7 @@ int moe_route_prepared(const moe_cfg *cfg, const moe_bf16 *hidden, const float *
                        const float *expert_bias, int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
                        float *aux_P, float *aux_loss, void *ws, size_t ws_bytes, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_route_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
@@ -964,6 +1026,7 @@ int moe_dense_ffn(int32_t T, int32_t H, int32_t I, const moe_bf16 *hidden, const
                   const moe_bf16 *W_down, const moe_bf16 *residual, moe_bf16 *out, void *ws, size_t ws_bytes,
                   void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_dense(T, H, I);
     if (rc != MOE_OK)
         return rc;
@@ -1046,6 +1109,7 @@ int moe_backward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_g
                  float *d_shared_gate_up, float *d_shared_down, float *d_topk_w, void *ws, size_t ws_bytes,
                  void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_backward_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
@@ -1207,6 +1271,7 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
                 const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *ws, size_t ws_bytes,
                 void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_forward_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
@@ -1242,6 +1307,7 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
               int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss,
               moe_bf16 *out, int flags, void *ws, size_t ws_bytes, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_route_cfg(cfg);
     if (rc == MOE_OK)
         rc = check_forward_cfg(cfg);
@@ -1292,6 +1358,7 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
 int moe_expert_feedback(const moe_cfg *cfg, const int32_t *expert_counts, float gamma, float *expert_bias,
                         int64_t *totals, void *stream)
 {
+    ProfCall prof_call_;
     if (!cfg || cfg->E < 1 || cfg->T < 1 || cfg->k < 1 || !expert_counts || !isfinite(gamma))
         return MOE_ERR_INVALID_ARG;
     if (!aligned(expert_counts, 4) || !aligned(expert_bias, 4) || !aligned(totals, 8))
@@ -1309,6 +1376,7 @@ int moe_expert_feedback(const moe_cfg *cfg, const int32_t *expert_counts, float 
 
 int moe_rmsnorm(int32_t T, int32_t H, const moe_bf16 *x, moe_bf16 *out, float eps, void *stream)
 {
+    ProfCall prof_call_;
     if (T < 1 || H < 8 || H % 8 != 0 || !x || !out || !isfinite(eps) || eps < 0.0f)
         return MOE_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(out, 16))
@@ -1353,7 +1421,11 @@ int moe_debug_inject_timeout(int launches)
 
 int moe_profile_enable(int on)
 {
-    g_prof_on.store(on ? 1 : 0);
+    if (on < 0 || on > 2)
+        return MOE_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(g_prof_mu);
+    prof_close_stage_locked();
+    g_prof_on.store(on);
     return MOE_OK;
 }
 
@@ -1414,6 +1486,7 @@ int moe_ep_dispatch(const moe_cfg *cfg, int32_t ranks, const moe_bf16 *hidden, c
                     int32_t *send_counts, moe_bf16 *x_send, int32_t *e_send, int32_t *slot_of, void *ws,
                     size_t ws_bytes, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_ep(cfg, ranks);
     if (rc != MOE_OK)
         return rc;
@@ -1464,6 +1537,7 @@ int moe_expert_rows(const moe_cfg *cfg, int32_t rows, const moe_bf16 *x, const i
                     const moe_bf16 *W_gate_up, const moe_bf16 *W_down, moe_bf16 *y, void *ws, size_t ws_bytes,
                     void *stream)
 {
+    ProfCall prof_call_;
     if (!cfg || rows < 0)
         return MOE_ERR_INVALID_ARG;
     if (rows == 0) {
@@ -1498,6 +1572,7 @@ int moe_expert_rows(const moe_cfg *cfg, int32_t rows, const moe_bf16 *x, const i
 int moe_combine(const moe_cfg *cfg, const moe_bf16 *Y, int64_t y_rows, int64_t shared_row0, const int32_t *slot_of,
                 const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *stream)
 {
+    ProfCall prof_call_;
     if (!cfg || cfg->T < 1 || cfg->k < 1 || cfg->k > 32 || cfg->H < 8 || !Y || !slot_of || !out)
         return MOE_ERR_INVALID_ARG;
     if (cfg->H % 8 != 0)
@@ -1601,6 +1676,7 @@ int moe_route_static(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_
                      int32_t *topk_idx, float *topk_w, int32_t *expert_counts, float *aux_P, float *aux_loss,
                      int32_t *status_out, void *stream)
 {
+    ProfCall prof_call_;
     int rc = check_route_cfg(cfg);
     if (rc != MOE_OK)
         return rc;

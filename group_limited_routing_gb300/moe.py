@@ -464,9 +464,11 @@ def last_launch_count() -> int:
     return int(_lib.load().moe_last_launch_count())
 
 
-def profile_enable(on: bool = True) -> None:
-    """Bracket every kernel the library launches with CUDA events."""
-    _lib.load().moe_profile_enable(1 if on else 0)
+def profile_enable(on: bool = True, stages: bool = False) -> None:
+    """Bracket every kernel the library launches with CUDA events, or with
+    stages=True time the routing and bucketing kernels of a call as one
+    interval ("router_plus_permute") and every other kernel on its own."""
+    _lib.check(_lib.load().moe_profile_enable((2 if stages else 1) if on else 0), "moe_profile_enable")
 
 
 def profile_read(reset: bool = True) -> dict:

@@ -386,13 +386,20 @@ int moe_get_status(void *ws, size_t ws_bytes, void *stream, int32_t *status, int
  * moe_router_logits call on this thread enqueued (memsets not counted). */
 int moe_last_launch_count(void);
 
-/* Per-kernel timing.  While enabled, every kernel the library launches is
- * bracketed by two CUDA events recorded on its stream (a few microseconds of
- * overhead per launch, no synchronisation).  moe_profile_read() waits for
- * the recorded events, folds them into per-kernel totals and returns the
- * total milliseconds and launch count of kernel `kernel_id` (0 <=
- * kernel_id < MOE_KERNEL_COUNT), clearing them when reset != 0. */
-#define MOE_KERNEL_COUNT 18
+/* Kernel timing.  moe_profile_enable(1): every kernel the library launches
+ * is bracketed by two CUDA events recorded on its stream (a few microseconds
+ * of overhead per launch, no synchronisation; the events also keep a kernel
+ * from starting before the previous one has ended).  moe_profile_enable(2):
+ * per stage -- the routing and bucketing kernels of a call (router GEMM,
+ * selection, balance-loss reduction, histogram, scan, scatter) are timed as
+ * one interval, kernel id MOE_KERNEL_STAGE_ROUTE_PERMUTE, and every other
+ * kernel on its own; events are recorded only where the stage changes.
+ * moe_profile_enable(0) stops.  moe_profile_read() waits for the recorded
+ * events, folds them into per-kernel totals and returns the total
+ * milliseconds and interval count of `kernel_id` (0 <= kernel_id <
+ * MOE_KERNEL_COUNT), clearing them when reset != 0. */
+#define MOE_KERNEL_COUNT 19
+#define MOE_KERNEL_STAGE_ROUTE_PERMUTE 18
 int moe_profile_enable(int on);
 int moe_profile_read(int kernel_id, double *total_ms, int32_t *launches, int reset);
 const char *moe_kernel_name(int kernel_id);
