@@ -138,6 +138,20 @@ def test_strerror(lib):
     assert lib.moe_strerror(-99).decode() == "unknown error code"
 
 
+def test_profile_modes(lib):
+    """0 off, 1 per kernel, 2 per stage; anything else is refused.  The names
+    cover every id, the last one being the routing-and-bucketing stage."""
+    assert lib.moe_profile_enable(2) == _lib.MOE_OK
+    assert lib.moe_profile_enable(1) == _lib.MOE_OK
+    assert lib.moe_profile_enable(0) == _lib.MOE_OK
+    assert lib.moe_profile_enable(3) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_profile_enable(-1) == _lib.MOE_ERR_INVALID_ARG
+    names = [lib.moe_kernel_name(k).decode() for k in range(_lib.MOE_KERNEL_COUNT)]
+    assert all(names) and len(set(names)) == len(names)
+    assert names[-1] == "router_plus_permute"
+    assert lib.moe_kernel_name(_lib.MOE_KERNEL_COUNT).decode() == ""
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
     monkeypatch.setattr(_lib, "_handle", None)

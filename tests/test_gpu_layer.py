@@ -165,6 +165,34 @@ def test_layer_launch_count(flags, kernels):
     assert layer.status() == 0
 
 
+def test_stage_profile_times_routing_and_bucketing_as_one_interval():
+    """moe_profile_enable(2): one router_plus_permute interval per moe_layer
+    call, the other kernels one interval each, and no per-kernel records of
+    the routing stage's kernels; outputs as with profiling off."""
+    T, calls = 4096, 3
+    w0 = wl.WORKLOADS[4].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T)
+    layer = moe.MoELayer(cfg, d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"], d["shared_gate_up"],
+                         d["shared_down"], single_call=True)
+    ref = layer(d["hidden"]).clone()
+    moe.profile_read(reset=True)
+    moe.profile_enable(True, stages=True)
+    try:
+        for _ in range(calls):
+            out = layer(d["hidden"])
+        torch.cuda.synchronize()
+    finally:
+        moe.profile_enable(False)
+    prof = moe.profile_read(reset=True)
+    assert torch.equal(out, ref)
+    assert prof["router_plus_permute"][1] == calls and prof["router_plus_permute"][0] > 0
+    for name in ("gemm_gate_up_swiglu", "gemm_down", "combine"):
+        assert prof[name][1] == calls, name
+    for name in ("router_gemm", "route_select", "bucket_scan", "bucket_scatter"):
+        assert prof[name][1] == 0, name
+
+
 def test_graphed_fused_layer_matches_eager():
     T = 1000
     w0 = wl.WORKLOADS[3].with_T(T)
