@@ -91,7 +91,11 @@ class ExpertShard:
         if cfg.E % world != 0:
             raise ValueError("E = %d experts do not split over %d ranks" % (cfg.E, world))
         self.cfg, self.rank, self.world = cfg, rank, world
-        self.cfg_local = dataclasses.replace(cfg, E=cfg.E // world, n_group=max(1, cfg.n_group // world))
+        # the local experts' stage only (no routing happens on the received
+        # rows); the routing fields are kept consistent for the checks
+        n_group = max(1, cfg.n_group // world)
+        self.cfg_local = dataclasses.replace(cfg, E=cfg.E // world, n_group=n_group,
+                                             topk_group=min(cfg.topk_group, n_group))
         self.W_router, self.expert_bias = W_router, expert_bias
         self.W_gate_up_local, self.W_down_local = W_gate_up_local, W_down_local
         self.shared_gate_up, self.shared_down = shared_gate_up, shared_down

@@ -60,6 +60,25 @@ def _mismatch_report(cfg, d, shards, xs, outs, r, ref, idx, w, snap):
                 torch.equal(outs2[r], outs[r]), torch.equal(outs2[r], ref), not torch.equal(snap[r], outs[r])))
 
 
+def test_ep_with_residual_equals_moe_forward():
+    """The residual is added in the combine on each rank as moe_forward adds
+    it: bit for bit."""
+    T, world = 2048, 2
+    w0 = wl.WORKLOADS[4].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T)
+    shards = _shards(cfg, d, world)
+    xs = [wl.hidden(w0, DEV, layer=r) for r in range(world)]
+    res = [wl.hidden(w0, DEV, layer=10 + r) for r in range(world)]
+    outs = ep.ep_forward_local(shards, xs, res)
+    for r in range(world):
+        idx, w, _, _, _ = moe.route(cfg, xs[r], d["W_router"], d["expert_bias"])
+        ref = moe.forward(cfg, xs[r], d["W_gate_up"], d["W_down"], d["shared_gate_up"], d["shared_down"], idx, w,
+                          res[r])
+        torch.cuda.synchronize()
+        assert torch.equal(outs[r], ref), "rank %d" % r
+
+
 def test_ep_rank_that_receives_nothing():
     """A bias that keeps every token off rank 1's experts: rank 1 receives no
     rows (moe_expert_rows with 0 rows), and both outputs still equal
