@@ -750,6 +750,15 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v, floa
     }
 }
 
+// A 16-byte load marked as streaming (evict first): every row of Y is read
+// once, by one token.
+__device__ __forceinline__ uint4 ld_stream(const uint16_t *p)
+{
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
 // One token's 16-byte column vector: the K expert rows (in batches of eight,
 // every load of a batch issued before any use) and the shared row.
 __device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, const int *s_slot, const float *s_w,
@@ -762,7 +771,7 @@ __device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, cons
         acc[q] = 0.0f;
         racc[q] = 0.0f;
     }
-    const uint4 sv = reinterpret_cast<const uint4 *>(Y + (srow0 + t) * H)[vv];
+    const uint4 sv = ld_stream(Y + (srow0 + t) * H + (size_t)vv * 8);
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     for (int j0 = 0; j0 < K; j0 += 8) {
         uint4 yv[8];
@@ -772,7 +781,7 @@ __device__ __forceinline__ void combine_one(const uint16_t *__restrict__ Y, cons
             const int j = j0 + u;
             const int slot = (j < K) ? s_slot[tl * K + j] : -1;
             wv[u] = (slot >= 0) ? s_w[tl * K + j] : 0.0f;
-            yv[u] = (slot >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)slot * H)[vv] : zero;
+            yv[u] = (slot >= 0) ? ld_stream(Y + (size_t)slot * H + (size_t)vv * 8) : zero;
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -814,11 +823,11 @@ __device__ __forceinline__ void combine_two(const uint16_t *__restrict__ Y, cons
         const int sb = (u < K) ? s_slot[tlb * K + u] : -1;
         wa[u] = (sa >= 0) ? s_w[tla * K + u] : 0.0f;
         wb[u] = (sb >= 0) ? s_w[tlb * K + u] : 0.0f;
-        ya[u] = (sa >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)sa * H)[vv] : zero;
-        yb[u] = (sb >= 0) ? reinterpret_cast<const uint4 *>(Y + (size_t)sb * H)[vv] : zero;
+        ya[u] = (sa >= 0) ? ld_stream(Y + (size_t)sa * H + (size_t)vv * 8) : zero;
+        yb[u] = (sb >= 0) ? ld_stream(Y + (size_t)sb * H + (size_t)vv * 8) : zero;
     }
-    const uint4 sva = reinterpret_cast<const uint4 *>(Y + (srow0 + ta) * H)[vv];
-    const uint4 svb = reinterpret_cast<const uint4 *>(Y + (srow0 + tb) * H)[vv];
+    const uint4 sva = ld_stream(Y + (srow0 + ta) * H + (size_t)vv * 8);
+    const uint4 svb = ld_stream(Y + (srow0 + tb) * H + (size_t)vv * 8);
     uint4 rva = zero, rvb = zero;
     if (residual) {
         rva = reinterpret_cast<const uint4 *>(residual + (size_t)ta * H)[vv];
