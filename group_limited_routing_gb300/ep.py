@@ -53,7 +53,8 @@ class Dispatched:
 
 class CudaOps:
     """The five operations of an expert-parallel step in the library's CUDA
-    kernels (one workspace each, reused across steps)."""
+    kernels.  Each keeps its workspace across steps and grows it when a step
+    needs more (the rows a rank receives change from step to step)."""
 
     def __init__(self, cfg: moe.MoeConfig, device):
         self.cfg = cfg
@@ -63,18 +64,30 @@ class CudaOps:
         self.ws_rows = None
         self.ws_dense = None
 
+    def _sized(self, ws, need, what):
+        if need and (ws is None or ws.nbytes < need):
+            ws = moe.SizedWorkspace(need, what, self.device)
+        return ws
+
     def route(self, x, W_router, W_split, expert_bias):
         idx, w, _, _, _ = moe.route(self.cfg, x, W_router, expert_bias, ws=self.ws_route, W_split=W_split)
         return idx, w
 
     def dispatch(self, ranks, x, idx):
-        out = moe.ep_dispatch(self.cfg, ranks, x, idx, ws=self.ws_dispatch)
-        return out
+        self.ws_dispatch = self._sized(self.ws_dispatch, moe.ep_dispatch_workspace_bytes(self.cfg, ranks),
+                                       "moe_ep_dispatch")
+        return moe.ep_dispatch(self.cfg, ranks, x, idx, ws=self.ws_dispatch)
 
     def expert_rows(self, cfg_local, x_recv, e_recv, W_gate_up, W_down):
+        if x_recv.shape[0]:
+            self.ws_rows = self._sized(self.ws_rows, moe.expert_rows_workspace_bytes(cfg_local, x_recv.shape[0]),
+                                       "moe_expert_rows")
         return moe.expert_rows(cfg_local, x_recv, e_recv, W_gate_up, W_down, ws=self.ws_rows)
 
     def shared(self, x, shared_gate_up, shared_down, out):
+        T, H = x.shape
+        if self.ws_dense is None or self.ws_dense.shape != (T, H, shared_down.shape[0]):
+            self.ws_dense = moe.DenseWorkspace(T, H, shared_down.shape[0], self.device)
         return moe.dense_ffn(x, shared_gate_up, shared_down, ws=self.ws_dense, out=out)
 
     def combine(self, Y, shared_row0, slot_of, w, residual):

@@ -375,6 +375,16 @@ class SizedWorkspace:
         return int(v.value)
 
 
+def ep_dispatch_workspace_bytes(cfg: MoeConfig, ranks: int) -> int:
+    """moe_ep_dispatch_workspace_bytes (0: the shape is not supported)."""
+    return int(_lib.load().moe_ep_dispatch_workspace_bytes(ctypes.byref(cfg.c()), ranks))
+
+
+def expert_rows_workspace_bytes(cfg: MoeConfig, rows: int) -> int:
+    """moe_expert_rows_workspace_bytes (0: the shape is not supported)."""
+    return int(_lib.load().moe_expert_rows_workspace_bytes(ctypes.byref(cfg.c()), rows))
+
+
 def ep_dispatch(cfg: MoeConfig, ranks: int, hidden, topk_idx, *, ws: Optional[SizedWorkspace] = None):
     """moe_ep_dispatch: the pairs grouped by the rank holding their expert.
     Returns (send_counts [ranks] int32, x_send [kT, H] bf16, e_send [kT] int32
