@@ -6,6 +6,8 @@ five workloads' shapes (sampled tokens at full size), ragged T, empty and
 overfull buckets (0, 1, 127, 128, 129 rows and one expert holding every
 row), zero weights (shared expert only), the residual, bad indices and
 determinism."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -108,6 +110,21 @@ def test_forward_bucket_sizes_and_empty_experts():
     assert [counts[e] for e in sizes] == list(sizes.values()) and counts[0] == 0
     w = rng.random((T, k)).astype(np.float32)
     check(cfg, d, torch.from_numpy(idx).to(DEV), torch.from_numpy(w).to(DEV), what="bucket sizes")
+
+
+@pytest.mark.parametrize("H,k,T", [(512, 4, 300), (512, 1, 97), (512, 12, 300), (1536, 8, 257), (2048, 5, 130),
+                                   (4096, 8, 40)])
+def test_forward_other_k_and_hidden_sizes(H, k, T):
+    # k < 8 pads the combine's eight-term sum with zero rows, k > 8 takes its
+    # batches of eight; H = 512 puts four tokens in a combine block, H = 4096
+    # gives a thread two column vectors of a row; H = 1536 and 4096 run the
+    # bucketing's row gather without its loads-first path
+    cfg, d = small_layer(T, H=H, seed=k)
+    cfg = dataclasses.replace(cfg, k=k)
+    idx, w = wl.random_routing(T, cfg.E, k, seed=H + k, device=DEV)
+    check(cfg, d, idx, w, what="H=%d k=%d T=%d" % (H, k, T))
+    r = (torch.randn(T, H, device=DEV) * 0.5).to(torch.bfloat16)
+    check(cfg, d, idx, w, residual=r, what="H=%d k=%d T=%d with residual" % (H, k, T))
 
 
 @pytest.mark.parametrize("T", [500, 32, 16, 5])
