@@ -68,6 +68,33 @@ def test_router_logits_accuracy(wid, T):
            dict(T=int(T), max_abs_err=float(err.max()), max_abs_logit=float(np.abs(L).max())))
 
 
+def test_router_logits_are_batch_invariant():
+    """Within the CTA-pair router's range (T >= 19456) a token's logits and
+    routing do not depend on the batch around it: the first 19456 tokens of a
+    32768-token batch (128 tiles on the pairs, some pairs taking two) come out
+    bit for bit as in a 19456-token batch (one tile per pair).  (Below that
+    range the router splits K over SMs for small batches, which changes the
+    summation order.)"""
+    w0 = wl.WORKLOADS[4].with_T(32768)
+    d = wl.layer_inputs(w0, DEV, with_experts=False)
+    cfg = moe.MoeConfig(T=32768, H=w0.H, I=w0.I, Is=w0.Is)
+    n = 19456
+    cfg1 = cfg.with_T(n)
+    x1 = d["hidden"][:n].contiguous()
+    big = moe.router_logits(cfg, d["hidden"], d["W_router"])
+    small = moe.router_logits(cfg1, x1, d["W_router"])
+    torch.cuda.synchronize()
+    assert torch.equal(big[:n], small)
+    bi, bw, bc, _, _ = moe.route(cfg, d["hidden"], d["W_router"], d["expert_bias"], aux=False)
+    si, sw, sc, _, _ = moe.route(cfg1, x1, d["W_router"], d["expert_bias"], aux=False)
+    torch.cuda.synchronize()
+    assert torch.equal(bi[:n], si) and torch.equal(bw[:n], sw)
+    # and the same batch again
+    again = moe.router_logits(cfg, d["hidden"], d["W_router"])
+    torch.cuda.synchronize()
+    assert torch.equal(again, big)
+
+
 def test_router_sigmoid_ulp_distance():
     """The routing kernels' fp32 sigmoid (the hardware 2^x on a compensated
     argument, then the hardware reciprocal of 1 + exp(-L) with one Newton
