@@ -330,12 +330,13 @@ def test_large_batch_sampled_parity():
     check(cfg, d, idx, w, tokens, what="T=%d, a row in every m-tile (%d tokens)" % (T, len(tokens)))
 
 
-@pytest.mark.parametrize("T", [24576, 30000])
+@pytest.mark.parametrize("T", [24576, 24780, 30000])
 def test_forward_pair_tiles_edge_buckets(T):
     """The CTA-pair down GEMM (256-row pair tiles, T >= 24576) on bucket
     sizes that end a pair tile in every way: empty, 1, 127, 128, 129, 255,
     256, 257 and 383 rows, one bucket of ~half of all rows, the rest spread;
-    every m-tile compared."""
+    every m-tile compared.  The shared expert's last pair tile holds 48 rows
+    at T = 30000 and 204 at T = 24780."""
     k, E = 8, 256
     cfg, d = small_layer(T, seed=6)
     rng = np.random.default_rng(T)
