@@ -1873,6 +1873,10 @@ __global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const _
                 const TileInfo ti = half_tile(tile);
                 const CUtensorMap *mb = ti.shared ? &p.tmB1 : &p.tmB0;
                 const int col0 = ti.nt * 256 + (int)rank * 128;
+                // a half with no rows of the bucket (its last pair tile ends in
+                // the even CTA) loads rows past the end of the intermediate:
+                // TMA fills them with zeros without reading memory
+                const int a_row = ti.rows > 0 ? ti.a_row : p.kT + p.T;
                 for (int kb = 0; kb < p.kblocks; ++kb) {
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, limit)) {
                         ok = false;
@@ -1884,7 +1888,7 @@ __global__ void __launch_bounds__(PAIR_DOWN_THREADS, 1) down_pair_kernel(const _
                     const uint32_t fb = full_leader0 + 8u * stage;
                     const int k0 = kb * GEMM_BK;
                     const int krow = (ti.shared ? 0 : ti.group * p.I) + k0;
-                    tma_load_2d_pair(sA, &p.tmA0, fb, k0, ti.a_row);
+                    tma_load_2d_pair(sA, &p.tmA0, fb, k0, a_row);
 #pragma unroll
                     for (int q = 0; q < 2; ++q)
                         tma_load_2d_pair(sA + C::A_BYTES + q * C::B_ATOM, mb, fb, col0 + q * 64, krow);
