@@ -733,10 +733,11 @@ cudaError_t launch_dense_tiles(int T, int mt, int4 *mtiles, WsHeader *hdr, cudaS
 
 // ---------------------------------------------------------------------------
 // out[t] = bf16( Y[K*T + t] + sum_j w[t,j] * Y[slot_of[t,j]] (+ residual[t]) ),
-// fp32 accumulation in j order.  A block takes ctok <= COMBINE_TOK tokens at a time:
-// their slots and weights are loaded once into shared memory, then a thread
-// owns one 16-byte column vector (8 values) of a token and issues all of its
-// row loads before the first use.
+// fp32 accumulation in j order.  A block owns one contiguous slice of the
+// tokens (all slices within a token of the same length) and takes it ctok <=
+// COMBINE_TOK tokens at a time: their slots and weights are loaded once into
+// shared memory, then a thread owns one 16-byte column vector (8 values) of a
+// token and issues all of its row loads before the first use.
 constexpr int COMBINE_TOK = 32;
 
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 &v, float wgt)
@@ -875,10 +876,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
     const int vpr = H / 8;                                   // 16-byte vectors per row
     const int rpp = max(1, (int)blockDim.x / vpr);           // tokens per pass
     const int sub = threadIdx.x / vpr, v = threadIdx.x % vpr;
-    const int nchunks = (T + ctok - 1) / ctok;
-    for (int chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
-        const int t0 = chunk * ctok;
-        const int nt = min(ctok, T - t0);
+    // this block's tokens: one contiguous slice, the same length (to a token)
+    // for every block, so that all blocks end together
+    const int t_begin = (int)((long long)T * blockIdx.x / gridDim.x);
+    const int t_end = (int)((long long)T * (blockIdx.x + 1) / gridDim.x);
+    for (int t0 = t_begin; t0 < t_end; t0 += ctok) {
+        const int nt = min(ctok, t_end - t0);
         __syncthreads();
         for (int i = threadIdx.x; i < nt * K; i += blockDim.x) {
             int slot = slot_of[(size_t)t0 * K + i];
@@ -922,8 +925,10 @@ cudaError_t launch_combine(const uint16_t *Y, const int32_t *slot_of, const floa
     int ctok = COMBINE_TOK;
     while (ctok > 2 && (T + ctok - 1) / ctok < sms)
         ctok >>= 1;
-    const int nchunks = (T + ctok - 1) / ctok;
-    const int blocks = min(nchunks, sms * 8);
+    // one slice of tokens per block, two blocks per SM (the kernel's
+    // registers allow two): every block streams its slice to the end instead
+    // of a last partial round of 32-token blocks
+    const int blocks = (int)std::min<long long>(((long long)T + ctok - 1) / ctok, 2ll * sms);
     const cudaError_t le = launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, s, Y, slot_of, w, residual, T, H, k,
                                       ctok, shared_row0, out, idx, offs, offs ? E : 0, y_rows);
     if (le != cudaSuccess)
