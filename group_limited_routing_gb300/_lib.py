@@ -41,6 +41,7 @@ EXPORTS = ("moe_workspace_bytes", "moe_workspace_init", "moe_route", "moe_router
            "moe_ep_dispatch", "moe_expert_rows_workspace_bytes", "moe_expert_rows", "moe_combine")
 MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
 MOE_LAYER_FUSED_ROUTER = 1
+MOE_LAYER_FUSED_COMBINE = 2
 MOE_KERNEL_COUNT = 19
 
 

@@ -667,7 +667,7 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
                  const moe_bf16 *shared_gate_up, const moe_bf16 *shared_down, const int32_t *topk_idx,
                  const float *topk_w, const moe_bf16 *residual, moe_bf16 *out, void *ws, const FwdLayout &L,
                  const int32_t *offs, int sms, cudaStream_t s, int &launches, bool hist_ready = false,
-                 bool with_shared = true, int32_t *counts_out = nullptr)
+                 bool with_shared = true, int32_t *counts_out = nullptr, bool fused_combine = false)
 {
     // with_shared = false (moe_expert_rows): no shared-expert group, k = 1, and
     // out receives every pair's unweighted expert row in pair order instead
@@ -764,10 +764,31 @@ int forward_impl(const moe_cfg &c, const moe_bf16 *hidden, const moe_bf16 *W_gat
     p2.kT = (int)kT;
     p2.ld_out = c.H;
     p2.status = &hdr->status;
+    // with fused_combine (moe_layer's MOE_LAYER_FUSED_COMBINE): the shared
+    // expert's down GEMM with the combine in its epilogue, after the routed
+    // pair tiles, whose rows it reads; no shared rows in Y and no separate
+    // combine launch.  Bit-identical to the default, and slower on a GB300
+    // (its eight epilogue warps keep fewer row loads in flight than the
+    // combine kernel), so not the default.
+    const bool down_combine = fused_combine && pair_down && with_shared && c.k <= 8;
     if (pair_down) {
         p2.mtiles = at<int4>(ws, L.ptiles);
-        p2.num_mtiles = &hdr->num_ptiles;
+        p2.num_mtiles = down_combine ? &hdr->num_ptiles_routed : &hdr->num_ptiles;
         GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(GK_DOWN_PAIR, p2, 2 * std::min(sms / 2, L.max_ptiles * p2.n_tiles), s));
+        if (down_combine) {
+            GemmParams p3 = p2;
+            p3.mtiles = nullptr;
+            p3.num_mtiles = nullptr;
+            p3.num_tiles_static = ((c.T + GEMM_BM - 1) / GEMM_BM) * p3.n_tiles;
+            p3.out = out;
+            p3.cmb_y = y;
+            p3.cmb_slot = slot_of;
+            p3.cmb_w = topk_w;
+            p3.cmb_res = residual;
+            p3.cmb_k = c.k;
+            GLR_LAUNCH(KID_COMBINE, launch_gemm(GK_DOWN_COMBINE, p3, std::min(sms, p3.num_tiles_static), s));
+            return MOE_OK;
+        }
     } else {
         GLR_LAUNCH(KID_GEMM_DOWN, launch_gemm(small ? GK_DOWN_SMALL : GK_DOWN, p2,
                                               std::min(sms, L.max_mtiles * p2.n_tiles), s));
@@ -1313,7 +1334,7 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
         rc = check_forward_cfg(cfg);
     if (rc != MOE_OK)
         return rc;
-    if (flags & ~MOE_LAYER_FUSED_ROUTER)
+    if (flags & ~(MOE_LAYER_FUSED_ROUTER | MOE_LAYER_FUSED_COMBINE))
         return MOE_ERR_INVALID_ARG;
     if ((aux_P || aux_loss) && layer_fused(*cfg, flags))
         return MOE_ERR_INVALID_ARG;          // the fused router forms no balance-loss sums
@@ -1349,7 +1370,7 @@ int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router,
         if (rc == MOE_OK)
             rc = forward_impl(c, hidden, W_gate_up, W_down, shared_gate_up, shared_down, topk_idx, topk_w, residual,
                               out, ws, L.f, nullptr, sms, s, launches, hist_done, true,
-                              counts_left ? expert_counts : nullptr);
+                              counts_left ? expert_counts : nullptr, (flags & MOE_LAYER_FUSED_COMBINE) != 0);
     }
     g_last_launches = launches;
     return rc;

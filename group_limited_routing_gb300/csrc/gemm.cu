@@ -67,7 +67,7 @@ struct GemmCfg;
 __host__ __device__ constexpr int base_kind(int kind)
 {
     return (kind == GK_GATE_UP_SMALL || kind == GK_GATE_UP_BWD) ? GK_GATE_UP
-           : kind == GK_DOWN_SMALL                              ? GK_DOWN
+           : (kind == GK_DOWN_SMALL || kind == GK_DOWN_COMBINE)  ? GK_DOWN
            : (kind == GK_ROUTER_WIDE || kind == GK_ROUTER_FUSED) ? GK_ROUTER
                                                                 : kind;
 }
@@ -85,7 +85,10 @@ constexpr int ROUTER_PF = 6;
 constexpr int ROUTER_KPS = 4;
 
 // epilogue warps of a kind (the block is 64 + 32 x this threads)
-__host__ __device__ constexpr int epi_warps(int kind) { return wide_router(kind) ? 8 : 4; }
+__host__ __device__ constexpr int epi_warps(int kind)
+{
+    return (wide_router(kind) || kind == GK_DOWN_COMBINE) ? 8 : 4;
+}
 __host__ __device__ constexpr int kind_threads(int kind) { return 64 + 32 * epi_warps(kind); }
 
 // the fused router's extra barriers: the epilogue warps' meeting, the logits'
@@ -153,6 +156,15 @@ struct GemmCfg<GK_DOWN> {
     static constexpr uint32_t IDESC = idesc_bf16_f32(GEMM_BM, BN, false, true);
     static constexpr int A_ROWS = GEMM_BM;
     static constexpr int NBUF = 2;
+};
+
+// The shared expert's down GEMM with the combine in its epilogue: the down
+// GEMM's operands, three stages, and 64 KB of staging for the tile's output
+// rows in token-major order (128 rows x 512 B).
+template <>
+struct GemmCfg<GK_DOWN_COMBINE> : GemmCfg<GK_DOWN> {
+    static constexpr int STAGES = 3;
+    static constexpr int NBUF = 4;
 };
 
 // Small-T kinds: only GEMM_SMALL_T A rows per stage (2 KB); the MMA still
@@ -281,6 +293,16 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile)
         return ti;
     }
     ti.kp = 0;
+    if constexpr (KIND == GK_DOWN_COMBINE) {
+        // the shared expert's 128-token tiles, n-tiles of one tile adjacent
+        const int m = tile / p.n_tiles;
+        ti.group = p.E;
+        ti.shared = 1;
+        ti.rows = min(GEMM_BM, p.T - m * GEMM_BM);
+        ti.a_row = p.kT + m * GEMM_BM;                  // the shared rows of the intermediate
+        ti.out_row = m * GEMM_BM;                       // the tile's first token
+        return ti;
+    }
     if (BASE == GK_ROUTER) {
         // tile = (token tile * n_tiles + expert tile) * ksplit + K part
         const int ks = p.ksplit > 1 ? p.ksplit : 1;
@@ -509,6 +531,137 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
             for (int i = 0; i < 32; ++i)
                 pk[i] = pack_bf16x2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
             store_piece<GemmCfg<KIND>::NBUF>(p, stage2, buf, v, lane, valid_rows, gbase + c * 2, ld_bytes, ti.nt * 256 + c, row0);
+        }
+    }
+}
+
+// Named barrier 1 over the eight epilogue warps of GK_DOWN_COMBINE, with the
+// AND of `ok` over them (so that all of them leave their tile loop together).
+__device__ __forceinline__ bool epi_barrier_and(int ok)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(ok)
+        : "memory");
+    return r != 0;
+}
+
+// A 16-byte load of a routed row, streaming (evict first): each is read once.
+__device__ __forceinline__ uint4 ld_row_stream(const uint16_t *ptr)
+{
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+    return v;
+}
+
+// acc += wgt * (8 bf16 values), in fp32
+__device__ __forceinline__ void cmb_add8(float (&acc)[8], const uint4 &v, float wgt)
+{
+    const __nv_bfloat162 *p2 = reinterpret_cast<const __nv_bfloat162 *>(&v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(p2[q]);
+        acc[2 * q] += wgt * f.x;
+        acc[2 * q + 1] += wgt * f.y;
+    }
+}
+
+// GK_DOWN_COMBINE, one of the eight epilogue warps (two per TMEM lane
+// quadrant, each with 128 of the tile's 256 columns).  First the shared
+// expert's output rows of the tile, rounded to bf16 as the down GEMM stores
+// them, into a token-major tile in shared memory (rows of 512 B; 16-byte
+// chunk c of row r at chunk c ^ (r & 31), so that the row-per-lane writes
+// and the chunk-per-lane reads below each touch every bank once); the
+// accumulator slot then goes back to the MMA.  Then each warp takes 16 of
+// the tile's tokens, four at a time, a 16-byte column vector per lane, and
+// forms the combine's sum in its order: the eight weighted routed rows (a
+// skipped pair, or j >= k, adds weight 0 times a zero row), then the shared
+// row, then the residual; one rounding to bf16 into the layer output.
+__device__ __forceinline__ void epilogue_down_combine(const GemmParams &p, const TileInfo &ti, uint32_t tslot,
+                                                      int warp, int lane, uint8_t *tile_s, uint32_t tempty)
+{
+    const int ew = warp - 2;
+    const int quad = warp & 3, half = ew >> 2;
+    {
+        const int r = quad * 32 + lane;
+        uint8_t *row = tile_s + r * 512;
+        const uint32_t tacc = tslot + ((uint32_t)(quad * 32) << 16) + half * 128;
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 64) {
+            uint32_t v[64];
+            tmem_load64(tacc + c, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int chunk = (half * 128 + c) / 8 + q;
+                const uint4 w4 = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]), __uint_as_float(v[8 * q + 1])),
+                                            pack_bf16x2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3])),
+                                            pack_bf16x2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5])),
+                                            pack_bf16x2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7])));
+                *reinterpret_cast<uint4 *>(row + ((chunk ^ (r & 31)) << 4)) = w4;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0)
+        mbar_arrive(tempty);                                    // the slot is in shared memory now
+    asm volatile("bar.sync 1, 256;" ::: "memory");              // every row of the tile is
+    const size_t H = (size_t)p.H;
+    const int K = p.cmb_k;
+    const int col = ti.nt * 256 + lane * 8;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+    for (int tb = ew * 16; tb < ew * 16 + 16 && tb < ti.rows; tb += 4) {
+        // slots and weights of tokens tb .. tb + 3: lane l holds pair (tb + l / 8, l % 8)
+        const int tl = tb + (lane >> 3), j = lane & 7;
+        int sl = -1;
+        float wl = 0.0f;
+        if (tl < ti.rows && j < K) {
+            const size_t pi = (size_t)(ti.out_row + tl) * K + j;
+            sl = p.cmb_slot[pi];
+            wl = p.cmb_w ? p.cmb_w[pi] : 1.0f;
+        }
+        uint4 yv[4][8];
+        float wv[4][8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int sj = __shfl_sync(0xffffffffu, sl, u * 8 + jj);
+                const float wj = __shfl_sync(0xffffffffu, wl, u * 8 + jj);
+                wv[u][jj] = sj >= 0 ? wj : 0.0f;
+                yv[u][jj] = sj >= 0 ? ld_row_stream(p.cmb_y + (size_t)sj * H + col) : zero;
+            }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int t = tb + u;
+            if (t < ti.rows) {
+                float acc[8], racc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    acc[q] = 0.0f;
+                    racc[q] = 0.0f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj)
+                    cmb_add8(racc, yv[u][jj], wv[u][jj]);
+                const uint4 sv = *reinterpret_cast<const uint4 *>(tile_s + t * 512 + ((lane ^ (t & 31)) << 4));
+                cmb_add8(acc, sv, 1.0f);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    acc[q] += racc[q];
+                const size_t o = (size_t)(ti.out_row + t) * H + col;
+                if (p.cmb_res)
+                    cmb_add8(acc, *reinterpret_cast<const uint4 *>(p.cmb_res + o), 1.0f);
+                const uint4 ov = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                            pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+                *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + o) = ov;
+            }
         }
     }
 }
@@ -1276,7 +1429,8 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
     // (the tile list, A rows) are read only after this
     pdl_wait();
 
-    const int num_tiles = (ROUTER || KIND == GK_WGRAD) ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
+    const int num_tiles =
+        (ROUTER || KIND == GK_WGRAD || KIND == GK_DOWN_COMBINE) ? p.num_tiles_static : (*p.num_mtiles) * p.n_tiles;
     const unsigned long long limit = p.wait_limit_ns ? p.wait_limit_ns : WAIT_LIMIT_NS;
 
     // The CTA's n-th tile for the MMA lane and the epilogue warps' lane 0:
@@ -1448,6 +1602,19 @@ __global__ void __launch_bounds__(kind_threads(KIND), 1) umma_gemm_kernel(const 
                     fused_ok = false;
                     break;
                 }
+            } else if constexpr (KIND == GK_DOWN_COMBINE) {
+                const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
+                int ok = 1;
+                if (lane == 0)
+                    ok = mbar_wait(tfull0 + 8u * slot, par, abort_flag, limit) ? 1 : 0;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                // every epilogue warp is past its reads of the previous tile's
+                // rows in shared memory, and all of them agree to go on
+                if (!epi_barrier_and(ok))
+                    break;
+                tc_fence_after();
+                epilogue_down_combine(p, ti, tmem + slot * C::BN, warp, lane, staging, tempty0 + 8u * slot);
+                ++ctr;
             } else {
                 const uint32_t slot = ctr % C::SLOTS, par = (ctr / C::SLOTS) & 1u;
                 int ok = 1;
@@ -2026,6 +2193,7 @@ int gemm_smem_bytes(int kind)
     case GK_GATE_UP: return GemmLayout<GK_GATE_UP>::SMEM;
     case GK_GATE_UP_SMALL: return GemmLayout<GK_GATE_UP_SMALL>::SMEM;
     case GK_DOWN_SMALL: return GemmLayout<GK_DOWN_SMALL>::SMEM;
+    case GK_DOWN_COMBINE: return GemmLayout<GK_DOWN_COMBINE>::SMEM;
     case GK_GATE_UP_BWD: return GemmLayout<GK_GATE_UP_BWD>::SMEM;
     case GK_DGRAD_DOWN: return GemmLayout<GK_DGRAD_DOWN>::SMEM;
     case GK_WGRAD: return GemmLayout<GK_WGRAD>::SMEM;
@@ -2126,6 +2294,7 @@ cudaError_t launch_gemm(int kind, const GemmParams &p, int grid, cudaStream_t s)
     case GK_GATE_UP: return launch_kind<GK_GATE_UP>(p, grid, s);
     case GK_GATE_UP_SMALL: return launch_kind<GK_GATE_UP_SMALL>(p, grid, s);
     case GK_DOWN_SMALL: return launch_kind<GK_DOWN_SMALL>(p, grid, s);
+    case GK_DOWN_COMBINE: return launch_kind<GK_DOWN_COMBINE>(p, grid, s);
     case GK_GATE_UP_BWD: return launch_kind<GK_GATE_UP_BWD>(p, grid, s);
     case GK_DGRAD_DOWN: return launch_kind<GK_DGRAD_DOWN>(p, grid, s);
     case GK_WGRAD: return launch_kind<GK_WGRAD>(p, grid, s);

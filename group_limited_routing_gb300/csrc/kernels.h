@@ -122,7 +122,8 @@ struct WsHeader {
     int tile_ctr[2]; // claim counters of the two weight-gradient launches (zeroed on the device)
     int fin_ticket;  // blocks of the balance-loss reduction done (back to zero at its end)
     int num_ptiles;  // 256-row pair tiles of the CTA-pair grouped GEMM (written on the device)
-    int pad[58];
+    int num_ptiles_routed;  // the routed buckets' pair tiles among them (they come first)
+    int pad[57];
 };
 
 // The _SMALL kinds are the grouped GEMMs for T <= GEMM_SMALL_T (decode): every
@@ -137,13 +138,17 @@ struct WsHeader {
 // each CTA loading half of the weight parts; grid = 2 x the pairs).
 // GK_DOWN_PAIR is the grouped down GEMM on CTA pairs: 256-row pair tiles of
 // one bucket, each CTA loading its 128 A rows and half of the W_down columns.
+// GK_DOWN_COMBINE is the shared expert's down GEMM with the combine in its
+// epilogue: per 128-token tile and 256 hidden columns, the shared rows'
+// output plus the weighted sum of each token's routed rows, written to the
+// layer output.
 // GK_ROUTER_FUSED is the 256-expert router whose epilogue also selects the
 // experts, claims every pair's row in its expert's bucket and copies the
 // hidden rows there (routing and bucketing in one launch).
 enum GemmKind {
     GK_ROUTER = 0, GK_GATE_UP = 1, GK_DOWN = 2, GK_GATE_UP_SMALL = 3, GK_DOWN_SMALL = 4,
     GK_GATE_UP_BWD = 5, GK_DGRAD_DOWN = 6, GK_WGRAD = 7, GK_ROUTER_WIDE = 8, GK_ROUTER_FUSED = 9,
-    GK_ROUTER_PAIR = 10, GK_DOWN_PAIR = 11
+    GK_ROUTER_PAIR = 10, GK_DOWN_PAIR = 11, GK_DOWN_COMBINE = 12
 };
 constexpr int FUSED_MAX_K = 8;      // experts per token the fused router selects at most
 constexpr int GEMM_SMALL_T = 16;
@@ -200,6 +205,13 @@ struct GemmParams {
     // grouped gate/up: routed m-tiles read their A rows from the tile list's
     // fourth field (the bucket layout above) instead of the second
     int cap_rows;
+    // GK_DOWN_COMBINE: out[t] = bf16(Y_shared[t] + sum_j w[t,j] Y[slot_of[t,j]]
+    // (+ residual[t])) for the tile's tokens; out is `out`, ld_out = H
+    const uint16_t *cmb_y;      // the routed rows [kT, H]
+    const int32_t *cmb_slot;    // slot_of [T, k]
+    const float *cmb_w;         // topk_w [T, k]
+    const uint16_t *cmb_res;    // residual [T, H] or NULL
+    int cmb_k;
     // router kinds, scored output (no K split): when set, `out` receives the
     // sigmoid scores s = router_sigmoid(logit) instead of the logits, and
     // gscore [T, E / 32, 2] every group's two best biased scores s + bias

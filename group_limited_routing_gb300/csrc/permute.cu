@@ -256,8 +256,10 @@ __device__ void bucket_offsets(const int32_t *__restrict__ sizes, int T, int E, 
         offset[E] = off;             // padded rows of all buckets (== K*T for pad 1 and valid indices)
         tstart[E] = tiles;
         pt_total = pts;
-        if (write_tiles && ptiles)
+        if (write_tiles && ptiles) {
             hdr->num_ptiles = pts + (with_shared ? (T + 2 * GEMM_BM - 1) / (2 * GEMM_BM) : 0);
+            hdr->num_ptiles_routed = pts;
+        }
         if (write_tiles) {
             hdr->num_mtiles = tiles + (with_shared ? (T + GEMM_BM - 1) / GEMM_BM : 0);
             if (true_rows != K * T)

@@ -231,7 +231,8 @@ def layer(cfg: MoeConfig, hidden, W_router, expert_bias, W_gate_up, W_down, shar
           aux: bool = False):
     """moe_layer: routing and the expert stage in one call (with
     flags=MOE_LAYER_FUSED_ROUTER, the fused router where the shape allows it;
-    see include/moe.h).  Returns (out, (topk_idx, topk_w, expert_counts)),
+    with MOE_LAYER_FUSED_COMBINE, the combine in the shared expert's down
+    GEMM; see include/moe.h).  Returns (out, (topk_idx, topk_w, expert_counts)),
     or with aux=True (out, (topk_idx, topk_w, expert_counts, aux_P [E],
     aux_loss [1])); `routing` (such a tuple) is filled instead of
     allocating."""

@@ -216,9 +216,20 @@ int moe_forward(const moe_cfg *cfg, const moe_bf16 *hidden, const moe_bf16 *W_ga
  * On a GB300 this path measures slower than the unfused kernels (its
  * selection runs on 8 warps per SM and its row copies follow the
  * multiplications), so it is not the default.  It forms no balance loss:
- * aux_P / aux_loss must be NULL with it.  Unknown flags return
+ * aux_P / aux_loss must be NULL with it.
+ *
+ * flags = MOE_LAYER_FUSED_COMBINE (where the down GEMM runs on CTA pairs:
+ * T >= 24576, k <= 8, without MOE_LAYER_FUSED_ROUTER; ignored otherwise):
+ * the shared expert's down projection runs after the routed experts' and
+ * forms the combine of section 五 in its epilogue (the routing page, section
+ * 四's "fused" MoE), so the shared rows never go through memory and the
+ * combine is not a launch of its own.  The sum is the combine's, term for
+ * term, so out is identical bit for bit to flags = 0.  On a GB300 it measures
+ * slower (the GEMM's epilogue warps keep fewer row loads in flight than the
+ * combine kernel), so it is not the default.  Unknown flags return
  * MOE_ERR_INVALID_ARG. */
 #define MOE_LAYER_FUSED_ROUTER 1
+#define MOE_LAYER_FUSED_COMBINE 2
 size_t moe_layer_workspace_bytes(const moe_cfg *cfg, int flags);
 int moe_layer(const moe_cfg *cfg, const moe_bf16 *hidden, const float *W_router, const moe_bf16 *W_split,
               const float *expert_bias, const moe_bf16 *W_gate_up, const moe_bf16 *W_down,

@@ -52,6 +52,22 @@ def test_fused_layer_matches_two_call_path_bit_for_bit(T):
     assert int(c_f.sum()) == T * cfg.k
 
 
+@pytest.mark.parametrize("T,with_residual", [(32768, False), (24780, True), (4096, False)])
+def test_fused_combine_matches_the_default_bit_for_bit(T, with_residual):
+    """MOE_LAYER_FUSED_COMBINE: the shared expert's down GEMM forms the
+    combine in its epilogue (from T = 24576 on, where the down GEMM runs on
+    CTA pairs; T = 24780 ends in a 76-token shared tile; at T = 4096 the flag
+    changes nothing).  Same routing, same output bits as the default."""
+    w0 = wl.WORKLOADS[4].with_T(T)
+    d = wl.layer_inputs(w0, DEV)
+    cfg = moe.MoeConfig(T=T)
+    res = (torch.randn(T, cfg.H, device=DEV) * 0.5).to(torch.bfloat16) if with_residual else None
+    od, i_d, w_d, c_d = run_layer(cfg, d, PLAIN, residual=res)
+    of, i_f, w_f, c_f = run_layer(cfg, d, _lib.MOE_LAYER_FUSED_COMBINE, residual=res)
+    assert torch.equal(i_f, i_d) and torch.equal(w_f, w_d) and torch.equal(c_f, c_d)
+    assert torch.equal(of, od)
+
+
 @pytest.mark.parametrize("wid,T,nsample", [(1, 128, None), (2, 16, None), (2, 1, None), (3, 4096, 192),
                                            (4, 2000, 160), (5, 129, None), (3, 300, None)])
 def test_fused_layer_matches_oracle(wid, T, nsample):
@@ -217,7 +233,7 @@ def test_layer_rejects_unknown_flags():
     cfg = moe.MoeConfig(T=T)
     with pytest.raises(_lib.MoeError):
         moe.layer(cfg, d["hidden"], d["W_router"], d["expert_bias"], d["W_gate_up"], d["W_down"],
-                  d["shared_gate_up"], d["shared_down"], flags=2, ws=moe.Workspace(cfg, moe.WS_LAYER, DEV, 0))
+                  d["shared_gate_up"], d["shared_down"], flags=4, ws=moe.Workspace(cfg, moe.WS_LAYER, DEV, 0))
 
 
 @pytest.mark.parametrize("T", [33, 600, 4864, 4865, 8192, 19500, 32768])
