@@ -43,6 +43,7 @@ MOE_ROUTE_STATIC_SCRATCH_BYTES = 40 << 20
 MOE_LAYER_FUSED_ROUTER = 1
 MOE_LAYER_FUSED_COMBINE = 2
 MOE_KERNEL_COUNT = 19
+MOE_KERNEL_STAGE_ROUTE_PERMUTE = 18   # moe_profile_read id of the routing + bucketing stage (mode 2)
 
 
 class MoeCfg(ctypes.Structure):

@@ -30,6 +30,18 @@ def test_header_declares_the_binding_exports():
     assert header_functions() == sorted(_lib.EXPORTS)
 
 
+def test_header_constants_match_the_binding():
+    # every #define MOE_* with an integer value in the header has the same
+    # value under the same name in the binding
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    defs = dict(re.findall(r"^#define\s+(MOE_\w+)\s+\(?(-?\d+)\)?\s*(?:/\*.*\*/)?\s*$", src, flags=re.M))
+    assert {"MOE_LAYER_FUSED_COMBINE", "MOE_KERNEL_COUNT", "MOE_STATUS_TIMEOUT", "MOE_ERR_TIMEOUT"} <= set(defs)
+    missing = [n for n in defs if not hasattr(_lib, n)]
+    assert not missing, missing
+    for name, value in defs.items():
+        assert getattr(_lib, name) == int(value), name
+
+
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT\s+(moe_\w+)", out))
