@@ -48,3 +48,16 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2
+
+
+def test_gemm_traffic_summary_matches_the_gemm_sources():
+    """The bench line's roofline `traffic` comes from the committed ncu
+    summary only while the GEMM sources hash to the value recorded there;
+    the committed summary is the one taken from the committed sources."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    for kernel in ("gemm_gate_up_swiglu", "gemm_down", "router_gemm"):
+        v = bench.gemm_traffic(kernel)
+        assert v is not None and v > 0, kernel
