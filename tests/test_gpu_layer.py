@@ -52,15 +52,17 @@ def test_fused_layer_matches_two_call_path_bit_for_bit(T):
     assert int(c_f.sum()) == T * cfg.k
 
 
-@pytest.mark.parametrize("T,with_residual", [(32768, False), (24780, True), (4096, False)])
-def test_fused_combine_matches_the_default_bit_for_bit(T, with_residual):
+@pytest.mark.parametrize("T,with_residual,k", [(32768, False, 8), (24780, True, 8), (24576, False, 6),
+                                               (4096, False, 8)])
+def test_fused_combine_matches_the_default_bit_for_bit(T, with_residual, k):
     """MOE_LAYER_FUSED_COMBINE: the shared expert's down GEMM forms the
     combine in its epilogue (from T = 24576 on, where the down GEMM runs on
-    CTA pairs; T = 24780 ends in a 76-token shared tile; at T = 4096 the flag
-    changes nothing).  Same routing, same output bits as the default."""
+    CTA pairs; T = 24780 ends in a 76-token shared tile; k = 6 pads the
+    eight-term sum with zero rows; at T = 4096 the flag changes nothing).
+    Same routing, same output bits as the default."""
     w0 = wl.WORKLOADS[4].with_T(T)
     d = wl.layer_inputs(w0, DEV)
-    cfg = moe.MoeConfig(T=T)
+    cfg = moe.MoeConfig(T=T, k=k)
     res = (torch.randn(T, cfg.H, device=DEV) * 0.5).to(torch.bfloat16) if with_residual else None
     od, i_d, w_d, c_d = run_layer(cfg, d, PLAIN, residual=res)
     of, i_f, w_f, c_f = run_layer(cfg, d, _lib.MOE_LAYER_FUSED_COMBINE, residual=res)
